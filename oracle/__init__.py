@@ -1,0 +1,258 @@
+"""CPU oracle for SageAttention3's microscaled FP4 attention forward.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  The product
+library (``bit_attention_gb300``) never imports, links or calls it, and the two
+share no code: this wrapper marshals numpy arrays into the plain C oracle in
+``sage_oracle.c`` and nothing else.
+
+The method follows the senqingzn.com article on SageAttention3 (sections
+"Solving two obstacles and one difficulty" and "FP4 attention inference
+acceleration and hardware implementation/optimisation") and the abstract of
+"SageAttention3: Microscaling FP4 Attention for Inference and An Exploration
+of 8-Bit Training".  See ``sage_oracle.c`` for the step-by-step definition.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_SRC = os.path.join(_HERE, "sage_oracle.c")
+_lock = threading.Lock()
+_lib = None
+
+PMODE = {"tile": 0, "running": 1}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FP contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load(path: str):
+    L = ctypes.CDLL(path)
+    _declare(L)
+    return L
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _load(_LIB_PATH)
+    return _lib
+
+
+class swapped:
+    """Context manager: route this module's calls through another build of the
+    oracle (used by the tests that plant mistakes in a copy of the source)."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        lib()
+        self.saved = _lib
+        _lib = _load(self.path)
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
+
+
+def _declare(L):
+    u8p = ctypes.POINTER(ctypes.c_uint8)
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f32p = ctypes.POINTER(ctypes.c_float)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    L.sor_e2m1_value.restype = ctypes.c_double
+    L.sor_e2m1_value.argtypes = [ctypes.c_int]
+    L.sor_e2m1_encode.restype = ctypes.c_int
+    L.sor_e2m1_encode.argtypes = [ctypes.c_float]
+    L.sor_e4m3_value.restype = ctypes.c_double
+    L.sor_e4m3_value.argtypes = [ctypes.c_int]
+    L.sor_e4m3_encode.restype = ctypes.c_int
+    L.sor_e4m3_encode.argtypes = [ctypes.c_float]
+    L.sor_encode_range.restype = None
+    L.sor_encode_range.argtypes = [ctypes.c_uint32, ctypes.c_uint32, u8p, u8p]
+    L.sor_quant_group16.restype = None
+    L.sor_quant_group16.argtypes = [f32p, u8p, u8p]
+    L.sor_quantize_rows.restype = None
+    L.sor_quantize_rows.argtypes = [u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p, u8p]
+    L.sor_quantize_v.restype = None
+    L.sor_quantize_v.argtypes = [u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p, u8p]
+    L.sor_attention.restype = ctypes.c_int
+    L.sor_attention.argtypes = [u8p, u8p, u8p, u8p, u8p, u8p, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                i64p, ctypes.c_int64, f64p, f64p, f64p]
+    L.sor_attention_exact.restype = ctypes.c_int
+    L.sor_attention_exact.argtypes = [u16p, u16p, u16p, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int64,
+                                      f64p]
+    L.sor_num_threads.restype = ctypes.c_int
+
+
+def _p(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _u16(x) -> np.ndarray:
+    """bf16 data as its raw 16-bit patterns (accepts torch bf16 tensors or uint16 arrays)."""
+    if isinstance(x, np.ndarray):
+        assert x.dtype == np.uint16
+        return np.ascontiguousarray(x)
+    import torch
+    assert x.dtype == torch.bfloat16
+    return np.ascontiguousarray(x.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def round_up(x: int, m: int) -> int:
+    return (x + m - 1) // m * m
+
+
+# ---------------------------------------------------------------- codecs
+def e2m1_value(code: int) -> float:
+    return lib().sor_e2m1_value(int(code))
+
+
+def e2m1_encode(x: float) -> int:
+    return lib().sor_e2m1_encode(float(x))
+
+
+def e4m3_value(bits: int) -> float:
+    return lib().sor_e4m3_value(int(bits))
+
+
+def e4m3_encode(x: float) -> int:
+    return lib().sor_e4m3_encode(float(x))
+
+
+def encode_range(first: int, count: int):
+    e2 = np.empty(count, np.uint8)
+    e4 = np.empty(count, np.uint8)
+    lib().sor_encode_range(first, count, _p(e2, ctypes.c_uint8), _p(e4, ctypes.c_uint8))
+    return e2, e4
+
+
+def quant_group16(x):
+    x = np.ascontiguousarray(np.asarray(x, np.float32))
+    assert x.shape == (16,)
+    codes = np.empty(16, np.uint8)
+    sc = np.zeros(1, np.uint8)
+    lib().sor_quant_group16(_p(x, ctypes.c_float), _p(codes, ctypes.c_uint8), _p(sc, ctypes.c_uint8))
+    return codes, int(sc[0])
+
+
+# ------------------------------------------------------------ quantizers
+def quantize_rows(x, BH: int, N: int, D: int):
+    """Q/K: bf16 [BH,N,D] -> codes [BH,N_pad,D/2], scales [BH,N_pad,D/16] (plain layout)."""
+    x = _u16(x).reshape(-1)
+    assert x.size == BH * N * D
+    Np = round_up(N, 128)
+    codes = np.empty((BH, Np, D // 2), np.uint8)
+    scales = np.empty((BH, Np, D // 16), np.uint8)
+    lib().sor_quantize_rows(_p(x, ctypes.c_uint16), BH, N, D, _p(codes, ctypes.c_uint8),
+                            _p(scales, ctypes.c_uint8))
+    return codes, scales
+
+
+def quantize_v(v, BH: int, N: int, D: int):
+    """V: bf16 [BH,N,D] -> V^T codes [BH,D,N_pad/2], scales [BH,D,N_pad/16] (plain layout)."""
+    v = _u16(v).reshape(-1)
+    assert v.size == BH * N * D
+    Np = round_up(N, 128)
+    codes = np.empty((BH, D, Np // 2), np.uint8)
+    scales = np.empty((BH, D, Np // 16), np.uint8)
+    lib().sor_quantize_v(_p(v, ctypes.c_uint16), BH, N, D, _p(codes, ctypes.c_uint8),
+                         _p(scales, ctypes.c_uint8))
+    return codes, scales
+
+
+class Quantized:
+    """The oracle's quantized Q, K, V^T for one problem."""
+
+    def __init__(self, q, k, v, BH: int, N: int, D: int):
+        self.BH, self.N, self.D = BH, N, D
+        self.qc, self.qs = quantize_rows(q, BH, N, D)
+        self.kc, self.ks = quantize_rows(k, BH, N, D)
+        self.vc, self.vs = quantize_v(v, BH, N, D)
+
+
+# ------------------------------------------------------------- attention
+def attention(qz: Quantized, causal: bool, pmode: str = "tile", rows=None, kv_tile: int = 128):
+    """Tiled FP4 attention. Returns (O [nrows,D] float64, l [nrows], m [nrows])."""
+    BH, N, D = qz.BH, qz.N, qz.D
+    if rows is None:
+        rows_a = None
+        nrows = BH * N
+    else:
+        rows_a = np.ascontiguousarray(np.asarray(rows, np.int64))
+        nrows = rows_a.size
+    out = np.empty((nrows, D), np.float64)
+    ol = np.empty(nrows, np.float64)
+    om = np.empty(nrows, np.float64)
+    rc = lib().sor_attention(
+        _p(qz.qc, ctypes.c_uint8), _p(qz.qs, ctypes.c_uint8), _p(qz.kc, ctypes.c_uint8),
+        _p(qz.ks, ctypes.c_uint8), _p(qz.vc, ctypes.c_uint8), _p(qz.vs, ctypes.c_uint8),
+        BH, N, D, int(bool(causal)), PMODE[pmode], kv_tile,
+        _p(rows_a, ctypes.c_int64) if rows_a is not None else None, nrows,
+        _p(out, ctypes.c_double), _p(ol, ctypes.c_double), _p(om, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle attention rejected its arguments")
+    return out, ol, om
+
+
+def attention_exact(q, k, v, BH: int, N: int, D: int, causal: bool, rows=None):
+    """Unquantized softmax(QK^T/sqrt(D))V in float64 from the bf16 inputs."""
+    q, k, v = _u16(q).reshape(-1), _u16(k).reshape(-1), _u16(v).reshape(-1)
+    if rows is None:
+        rows_a, nrows = None, BH * N
+    else:
+        rows_a = np.ascontiguousarray(np.asarray(rows, np.int64))
+        nrows = rows_a.size
+    out = np.empty((nrows, D), np.float64)
+    rc = lib().sor_attention_exact(
+        _p(q, ctypes.c_uint16), _p(k, ctypes.c_uint16), _p(v, ctypes.c_uint16), BH, N, D,
+        int(bool(causal)), _p(rows_a, ctypes.c_int64) if rows_a is not None else None, nrows,
+        _p(out, ctypes.c_double))
+    if rc != 0:
+        raise ValueError("oracle exact attention rejected its arguments")
+    return out
+
+
+def num_threads() -> int:
+    return lib().sor_num_threads()
+
+
+# -------------------------------------------------- decoding helpers
+def decode_rows(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Decode [.., R, C/2] codes and [.., R, C/16] scales (plain layout) to float64 [.., R, C]."""
+    e2 = np.array([e2m1_value(i) for i in range(16)])
+    e4 = np.array([e4m3_value(i) for i in range(256)])
+    lo = codes & 0x0F
+    hi = codes >> 4
+    el = np.stack([lo, hi], axis=-1).reshape(*codes.shape[:-1], codes.shape[-1] * 2)
+    vals = e2[el]
+    sc = np.repeat(e4[scales], 16, axis=-1)
+    return vals * sc
