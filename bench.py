@@ -1,0 +1,328 @@
+"""Benchmark: SageAttention3 NVFP4 attention forward on GB300.
+
+One step = the whole hot path over one batch: quantize Q, K, V (bf16 -> NVFP4)
+and the fused FP4 attention forward.  Metric: TOPS = 4*B*H*N^2*D / t (causal
+counted at half).  Inputs are synthetic and seeded (bit_attention_gb300.synth);
+the default workload is B4 H32 N4096 D128 (LLM-prefill shape with K outlier
+channels), whose bf16 inputs (384 MiB) exceed L2, so no flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle timed on the host cores
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch of
+the same workload (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 attention fwd TOPS (4*B*H*N^2*D/t) on 1 GB300; % of dense FP4 peak"
+FP4_OVER_BF16 = 6.0  # nominal dense FP4 / BF16 tensor rate (13.5 / 2.25 PFLOP/s)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": p["bf16_tflops"], "hbm_gbs": p["hbm_gbs"], "src": "measured"}
+    return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "src": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"]}
+        loaded = [x for x in sm if mx and x > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_oracle_sample(w, target_s: float, seed: int = 0):
+    """Time the oracle's attention on a bounded row sample of workload w.
+    Returns (TOPS, seconds, rows, threads)."""
+    import numpy as np
+    import oracle
+    from bit_attention_gb300.synth import make_qkv
+    # a reduced batch with the same per-row work (full N, same D and pattern)
+    q, k, v = make_qkv(1, 1, w.N, w.D, w.pattern, seed=seed)
+    qz = oracle.Quantized(q, k, v, 1, w.N, w.D)
+    rng = np.random.default_rng(seed)
+    rows_done, secs, ops = 0, 0.0, 0.0
+    batch = max(oracle.num_threads(), 1)
+    while secs < target_s and rows_done < w.N:
+        rows = rng.integers(0, w.N, size=batch)
+        t0 = time.perf_counter()
+        oracle.attention(qz, w.causal, rows=rows)
+        secs += time.perf_counter() - t0
+        keys = (rows + 1) if w.causal else np.full(batch, w.N)
+        ops += float((4.0 * keys * w.D).sum())
+        rows_done += batch
+        batch = min(batch * 2, 1024)
+    return ops / secs / 1e12, secs, rows_done, oracle.num_threads()
+
+
+def run_reference(args, w, world, rank):
+    """--impl reference: the CPU oracle, timed on the host cores."""
+    if rank != 0:
+        return
+    tops = []
+    rows_total, threads = 0, 1
+    for i in range(args.warmup + args.steps):
+        v, secs, rows, threads = cpu_oracle_sample(w, args.ref_seconds, seed=i)
+        if i >= args.warmup:
+            tops.append(v)
+            rows_total += rows
+    value = statistics.mean(tops)
+    sample = (f"oracle attention (FP64 C, OpenMP) on ~{rows_total // max(args.steps, 1)} random "
+              f"query rows per step of one (b,h) of the workload, full N={w.N}; "
+              f"quantization excluded")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+           "ms_per_step": None, "dtype": "f64", "data": "synthetic",
+           "config": w.describe(),
+           "cpu_baseline": {"value": value, "unit": "TOPS", "cores": threads, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llm")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--causal", type=int, default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=6.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+
+    from bit_attention_gb300.synth import WORKLOADS, Workload
+    w = WORKLOADS[args.workload]
+    if args.causal is not None:
+        w = Workload(w.name, w.B, w.H, w.N, w.D, bool(args.causal), w.pattern)
+
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+        return
+
+    import torch
+    from bit_attention_gb300 import sage_fp4 as S
+    from bit_attention_gb300.synth import make_workload
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q, k, v = make_workload(w, seed=rank)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    z = S.QuantizedQKV(w.B, w.H, w.N, w.D, device=dev)
+    o = torch.empty_like(qd)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        S.quantize_qkv(qd, kd, vd, out=z)
+        S.attn_fwd(z, w.causal, out=o)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if z.get_status() != 0:
+        raise RuntimeError("kernel status nonzero after warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            S.quantize_qkv(qd, kd, vd, out=z)
+            e1.record(stream)
+            S.attn_fwd(z, w.causal, out=o)
+            e2.record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    total_ms = max_over_ranks(total_ms, world)
+    ms_step = total_ms / args.steps
+    q_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev)
+    a_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev)
+    status = z.get_status()
+    if status != 0:
+        raise RuntimeError(f"kernel status {S.strerror(status)}")
+
+    ops = w.ops
+    value = ops * world / (ms_step * 1e-3) / 1e12
+    pk = peaks()
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    attn_tops = ops / (a_ms * 1e-3) / 1e12
+    elems = w.B * w.H * w.N * w.D
+    quant_bytes = 3 * elems * 2 + 3 * (elems // 2 + elems // 16)
+    quant_gbs = quant_bytes / (q_ms * 1e-3) / 1e9
+
+    # end to end through the public API: pinned host inputs -> device, quantize,
+    # attention, O back to pinned host memory, every step
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+
+        def e2e_step():
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            S.quantize_qkv(qd, kd, vd, out=z)
+            S.attn_fwd(z, w.causal, out=o)
+            ho.copy_(o, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(s0.elapsed_time(s1), world) / args.steps
+        e2e = {"value": ops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": 3 * elems * 2,
+               "d2h_bytes_per_step": elems * 2}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v_cpu, secs, rows, threads = cpu_oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": v_cpu, "unit": "TOPS", "cores": threads, "kind": "oracle",
+               "sample": f"oracle attention on {rows} random query rows of one (b,h), full N={w.N}, "
+                         f"{secs:.1f} s; quantization excluded"}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "nvfp4 (e2m1 codes, e4m3 scales) / fp32 accumulate",
+            "data": "synthetic (seeded, bit_attention_gb300.synth)",
+            "config": dict(w.describe(), l2="bf16 inputs 3x larger than L2; no flush",
+                           parallelism=f"weak, {world} independent batch(es)"),
+            "attn_kernel": {"ms": a_ms, "tops": attn_tops, "frac_of_fp4_peak": attn_tops / fp4_peak},
+            "quant_kernels": {"ms": q_ms, "gbs": quant_bytes / (q_ms * 1e-3) / 1e9,
+                              "frac_of_hbm": quant_gbs / pk["hbm_gbs"]},
+            "roofline": {"bound": "tensor", "achieved": attn_tops, "peak": fp4_peak,
+                         "unit": "TFLOP/s", "frac": attn_tops / fp4_peak, "traffic": None,
+                         "peak_src": f"{pk['src']} bf16 x {FP4_OVER_BF16:g} (nominal FP4/BF16)"},
+            "e2e": e2e, "cpu_baseline": cpu, "clocks": clk.summary(),
+            "gpu_launches": 3 * args.steps,
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,251 @@
+// api.cu -- the C ABI declared in include/sage_fp4.h: argument checks (before
+// anything touches the device), tensor-map encoding, launches, status words.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <limits.h>
+#include <math.h>
+#include <string.h>
+
+#include "../../include/sage_fp4.h"
+#include "kernels.h"
+#include "layout.cuh"
+
+using namespace sagefp4;
+
+namespace {
+
+bool dims_ok(int B, int H, int N, int D) {
+  if (B < 0 || H < 0 || N < 0) return false;
+  if (D != 64 && D != 128) return false;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long Np = (static_cast<long long>(N) + 127) / 128 * 128;
+  if (Np > (1LL << 30)) return false;
+  if (BH * Np > INT_MAX) return false;            // code rows are indexed with 32-bit ints
+  if (BH * Np / 128 > static_cast<long long>(UINT_MAX)) return false;
+  return true;
+}
+
+bool is_empty(int B, int H, int N) { return static_cast<long long>(B) * H * N == 0; }
+
+bool aligned(const void* p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct WsLayout {
+  size_t qc, qs, kc, ks, vc, vs, st, total;
+};
+
+WsLayout ws_layout(int B, int H, int N, int D) {
+  const size_t BH = static_cast<size_t>(B) * H;
+  const OperandSizes os = operand_sizes(N, D);
+  WsLayout w;
+  size_t off = 0;
+  w.qc = off;
+  off += align256(BH * os.q_codes);
+  w.qs = off;
+  off += align256(BH * os.q_scales);
+  w.kc = off;
+  off += align256(BH * os.q_codes);
+  w.ks = off;
+  off += align256(BH * os.q_scales);
+  w.vc = off;
+  off += align256(BH * os.vt_codes);
+  w.vs = off;
+  off += align256(BH * os.vt_scales);
+  w.st = off;
+  off += 256;
+  w.total = off;
+  return w;
+}
+
+bool tensor_ok(const sage_fp4_tensor& t) { return aligned(t.codes, 16) && aligned(t.scales, 16); }
+
+bool qkv_ok(const sage_fp4_qkv* x) {
+  return x && tensor_ok(x->q) && tensor_ok(x->k) && tensor_ok(x->vt) && aligned(x->status, 4);
+}
+
+// The kernels are compiled for sm_103a only.
+int check_device() {
+  static int cache[64];  // 0 unknown, 1 supported, 2 not
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SAGE_FP4_ECUDA;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev] == 1 ? SAGE_FP4_OK : SAGE_FP4_EUNSUPPORTED;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return SAGE_FP4_ECUDA;
+  const bool ok = (major == 10 && minor == 3);
+  if (dev >= 0 && dev < 64) cache[dev] = ok ? 1 : 2;
+  return ok ? SAGE_FP4_OK : SAGE_FP4_EUNSUPPORTED;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D byte tensor [rows][inner] (row pitch = inner), box [box_rows][box_inner].
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+              uint32_t box_rows, CUtensorMapSwizzle swz) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+CUtensorMapSwizzle swizzle_for_row(int row_bytes) {
+  return row_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                         : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? SAGE_FP4_OK : SAGE_FP4_ECUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t sage_fp4_workspace_bytes(int B, int H, int N, int D) {
+  if (!dims_ok(B, H, N, D)) return 0;
+  return ws_layout(B, H, N, D).total;
+}
+
+int sage_fp4_qkv_from_workspace(void* workspace, size_t workspace_bytes, int B, int H, int N, int D,
+                                sage_fp4_qkv* out) {
+  if (!out || !dims_ok(B, H, N, D) || !aligned(workspace, 256)) return SAGE_FP4_EINVAL;
+  const WsLayout w = ws_layout(B, H, N, D);
+  if (workspace_bytes < w.total) return SAGE_FP4_EINVAL;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  out->q.codes = base + w.qc;
+  out->q.scales = base + w.qs;
+  out->k.codes = base + w.kc;
+  out->k.scales = base + w.ks;
+  out->vt.codes = base + w.vc;
+  out->vt.scales = base + w.vs;
+  out->status = reinterpret_cast<int32_t*>(base + w.st);
+  return SAGE_FP4_OK;
+}
+
+int sage_fp4_quantize_qkv(const void* q, const void* k, const void* v, const sage_fp4_qkv* out,
+                          int B, int H, int N, int D, void* stream) {
+  if (!dims_ok(B, H, N, D) || !out) return SAGE_FP4_EINVAL;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return SAGE_FP4_EINVAL;
+  if (!tensor_ok(out->q) || !tensor_ok(out->k) || !tensor_ok(out->vt)) return SAGE_FP4_EINVAL;
+  if (is_empty(B, H, N)) return SAGE_FP4_OK;
+  int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  cudaError_t e = launch_quant_rows(q, k, out->q.codes, out->q.scales, out->k.codes, out->k.scales,
+                                    BH, N, D, st);
+  if (e != cudaSuccess) return SAGE_FP4_ECUDA;
+  return from_cuda(launch_quant_v(v, out->vt.codes, out->vt.scales, BH, N, D, st));
+}
+
+int sage_fp4_attn_fwd(const sage_fp4_qkv* qkv, void* o, int B, int H, int N, int D, int causal,
+                      void* stream) {
+  if (!dims_ok(B, H, N, D) || !qkv_ok(qkv) || !aligned(o, 16)) return SAGE_FP4_EINVAL;
+  if (causal != 0 && causal != 1) return SAGE_FP4_EINVAL;
+  if (is_empty(B, H, N)) return SAGE_FP4_OK;
+  int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  const int BH = B * H;
+  const int Np = round_up_int(N, 128);
+  CUtensorMap tq, tk, tv;
+  const CUtensorMapSwizzle qk_swz = swizzle_for_row(D / 2);
+  if (!make_map(&tq, qkv->q.codes, D / 2, static_cast<uint64_t>(BH) * Np, D / 2, 128, qk_swz) ||
+      !make_map(&tk, qkv->k.codes, D / 2, static_cast<uint64_t>(BH) * Np, D / 2, 128, qk_swz) ||
+      !make_map(&tv, qkv->vt.codes, Np / 2, static_cast<uint64_t>(BH) * D, 64, D,
+                CU_TENSOR_MAP_SWIZZLE_64B))
+    return SAGE_FP4_ECUDA;
+  AttnParams p;
+  p.sfq = qkv->q.scales;
+  p.sfk = qkv->k.scales;
+  p.sfv = qkv->vt.scales;
+  p.o = o;
+  p.status = qkv->status;
+  p.BH = BH;
+  p.N = N;
+  p.Np = Np;
+  p.causal = causal;
+  p.n_qt = Np / 128;
+  p.a = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
+  p.flags = 0;
+  return from_cuda(launch_attn(tq, tk, tv, p, D, static_cast<cudaStream_t>(stream)));
+}
+
+int sage_fp4_get_status(const sage_fp4_qkv* qkv, void* stream) {
+  if (!qkv || !aligned(qkv->status, 4)) return SAGE_FP4_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SAGE_FP4_ECUDA;
+  int32_t h = 0;
+  if (cudaMemcpy(&h, qkv->status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SAGE_FP4_ECUDA;
+  if (h != 0 && cudaMemset(qkv->status, 0, sizeof(h)) != cudaSuccess) return SAGE_FP4_ECUDA;
+  return h;
+}
+
+const char* sage_fp4_strerror(int status) {
+  switch (status) {
+    case SAGE_FP4_OK:
+      return "ok";
+    case SAGE_FP4_EINVAL:
+      return "invalid argument (null or misaligned pointer, bad size, or D not 64/128)";
+    case SAGE_FP4_ECUDA:
+      return "CUDA runtime or driver error";
+    case SAGE_FP4_ETIMEOUT:
+      return "a kernel's bounded wait gave up; the output is not valid";
+    case SAGE_FP4_EUNSUPPORTED:
+      return "device is not sm_103 (kernels are built for sm_103a)";
+    default:
+      return "unknown status";
+  }
+}
+
+int sage_fp4_cvt_probe(uint32_t first, uint32_t count, uint8_t* e2m1, uint8_t* e4m3,
+                       void* stream) {
+  if (!e2m1 && !e4m3) return SAGE_FP4_EINVAL;
+  if (count == 0) return SAGE_FP4_OK;
+  int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  return from_cuda(launch_cvt_probe(first, count, e2m1, e4m3, static_cast<cudaStream_t>(stream)));
+}
+
+int sage_fp4_mma_probe(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* b_codes,
+                       const uint8_t* b_scales, int n, int K, int a_by_threads, float* d,
+                       int32_t* status, void* stream) {
+  if (n != 64 && n != 128) return SAGE_FP4_EINVAL;
+  if (K != 64 && K != 128 && K != 256) return SAGE_FP4_EINVAL;
+  if (!aligned(a_codes, 16) || !aligned(a_scales, 16) || !aligned(b_codes, 16) ||
+      !aligned(b_scales, 16) || !aligned(d, 4) || !aligned(status, 4))
+    return SAGE_FP4_EINVAL;
+  int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  CUtensorMap ta, tb;
+  const CUtensorMapSwizzle swz = swizzle_for_row(K / 2);
+  if (!make_map(&ta, a_codes, K / 2, 128, K / 2, 128, swz) ||
+      !make_map(&tb, b_codes, K / 2, n, K / 2, n, swz))
+    return SAGE_FP4_ECUDA;
+  MmaProbeParams p;
+  p.a_codes = a_codes;
+  p.a_scales = a_scales;
+  p.b_scales = b_scales;
+  p.d = d;
+  p.status = status;
+  p.n = n;
+  p.K = K;
+  p.a_by_threads = a_by_threads ? 1 : 0;
+  return from_cuda(launch_mma_probe(ta, tb, p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

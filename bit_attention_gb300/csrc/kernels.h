@@ -1,0 +1,44 @@
+// kernels.h -- launchers shared between the kernel translation units and the
+// C ABI (api.cu).  Internal to the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sagefp4 {
+
+cudaError_t launch_quant_rows(const void* q, const void* k, uint8_t* qc, uint8_t* qs, uint8_t* kc,
+                              uint8_t* ks, int BH, int N, int D, cudaStream_t st);
+cudaError_t launch_quant_v(const void* v, uint8_t* vc, uint8_t* vs, int BH, int N, int D,
+                           cudaStream_t st);
+
+struct AttnParams {
+  const uint8_t* sfq;  // Q scales (block layout), per (b,h) N_pad*D/16 bytes
+  const uint8_t* sfk;  // K scales
+  const uint8_t* sfv;  // V^T scales, per (b,h) 8*N_pad bytes
+  void* o;             // bf16 [BH][N][D]
+  int32_t* status;
+  int BH, N, Np, causal, n_qt;
+  float a;  // log2(e) / sqrt(D): softmax scale folded into exp2
+  int flags;
+};
+
+cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const AttnParams& p, int D, cudaStream_t st);
+
+cudaError_t launch_cvt_probe(uint32_t first, uint32_t count, uint8_t* e2m1, uint8_t* e4m3,
+                             cudaStream_t st);
+
+struct MmaProbeParams {
+  const uint8_t* a_codes;
+  const uint8_t* a_scales;
+  const uint8_t* b_scales;
+  float* d;
+  int32_t* status;
+  int n, K, a_by_threads;
+};
+cudaError_t launch_mma_probe(const CUtensorMap& ta, const CUtensorMap& tb, const MmaProbeParams& p,
+                             cudaStream_t st);
+
+}  // namespace sagefp4

@@ -1,0 +1,168 @@
+// probe.cu -- diagnostic kernels that expose the device primitives the
+// attention path is built from, so that tests can pin them one at a time:
+//   * the FP32 -> E2M1 / E4M3 conversions, over any range of bit patterns;
+//   * one block-scaled FP4 tensor-core product of a 128-row tile, with its
+//     operands staged exactly as the attention kernel stages Q/K/V (TMA with
+//     hardware swizzle) or P (thread stores into the swizzled layout).
+#include <cuda_fp16.h>
+
+#include "../../include/sage_fp4.h"
+#include "kernels.h"
+#include "layout.cuh"
+#include "ptx.cuh"
+
+namespace sagefp4 {
+
+namespace {
+
+__global__ void cvt_probe_kernel(uint32_t first, uint32_t count, uint8_t* e2m1, uint8_t* e4m3) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
+       i += stride) {
+    const float x = __uint_as_float(first + static_cast<uint32_t>(i));
+    if (e2m1) e2m1[i] = static_cast<uint8_t>(cvt_e2m1x2(x, 0.0f));
+    if (e4m3) e4m3[i] = static_cast<uint8_t>(cvt_e4m3(x));
+  }
+}
+
+constexpr uint64_t kProbeWaitNs = 1000ull * 1000ull * 1000ull;
+
+__device__ __forceinline__ bool probe_wait(uint32_t bar, uint32_t parity, int32_t* err) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kProbeWaitNs) {
+      atomicCAS(err, 0, SAGE_FP4_ETIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Physical 16-byte chunk of logical chunk c in row r of a K-major tile with
+// rows of RB bytes under the matching swizzle (32/64/128-byte).
+template <int RB>
+__device__ __forceinline__ int swz_chunk(int r, int c) {
+  if (RB == 32) return c ^ ((r >> 2) & 1);
+  if (RB == 64) return c ^ ((r >> 1) & 3);
+  return c ^ (r & 7);
+}
+
+template <int K>
+__global__ void __launch_bounds__(128, 1)
+    mma_probe_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+                     const MmaProbeParams p, int32_t* err) {
+  constexpr int RB = K / 2;          // bytes per operand row
+  constexpr int KB = K / 64;         // MMAs (K = 64 each)
+  constexpr uint32_t swz = (RB == 32) ? kSwizzle32B : (RB == 64) ? kSwizzle64B : kSwizzle128B;
+  constexpr uint32_t sbo = 8 * RB;
+  constexpr int oA = 0, oB = 128 * RB, oSFA = 2 * 128 * RB, oSFB = oSFA + KB * 512,
+                oBar = oSFB + KB * 512, oSlot = oBar + 16;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_addr(sm);
+  const int warp = threadIdx.x >> 5;
+  const uint32_t bar_load = sb + oBar, bar_mma = sb + oBar + 8;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + oSlot);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_load, 1);
+    mbar_init(bar_mma, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_addr(slot), 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+
+  if (threadIdx.x == 0) {
+    const uint32_t bytes = (p.a_by_threads ? 0 : 128 * RB) + p.n * RB + 2 * KB * 512;
+    mbar_arrive_expect_tx(bar_load, bytes);
+    if (!p.a_by_threads) tma_load_2d(sb + oA, &ta, 0, 0, bar_load);
+    tma_load_2d(sb + oB, &tb, 0, 0, bar_load);
+    bulk_load(sb + oSFA, p.a_scales, KB * 512, bar_load);
+    bulk_load(sb + oSFB, p.b_scales, KB * 512, bar_load);
+  }
+  if (p.a_by_threads) {
+    for (int i = threadIdx.x; i < 128 * (RB / 16); i += blockDim.x) {
+      const int r = i / (RB / 16), c = i % (RB / 16);
+      const uint4 v = reinterpret_cast<const uint4*>(p.a_codes + r * RB)[c];
+      *reinterpret_cast<uint4*>(sm + oA + r * RB + swz_chunk<RB>(r, c) * 16) = v;
+    }
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    ok = probe_wait(bar_load, 0, err);
+    if (ok) {
+      tc_fence_after();
+      for (int kb = 0; kb < KB; ++kb) {
+        tc_cp_32x128b_warpx4(tmem + 128 + 4 * kb, smem_desc(sb + oSFA + 512 * kb, 0, 128, kSwizzleNone));
+        tc_cp_32x128b_warpx4(tmem + 160 + 4 * kb, smem_desc(sb + oSFB + 512 * kb, 0, 128, kSwizzleNone));
+      }
+      const uint32_t idesc = idesc_nvfp4(128, static_cast<uint32_t>(p.n));
+      for (int kb = 0; kb < KB; ++kb) {
+        const uint64_t ad = smem_desc(sb + oA + 32 * kb, 16, sbo, swz);
+        const uint64_t bd = smem_desc(sb + oB + 32 * kb, 16, sbo, swz);
+        mma_nvfp4(tmem, ad, bd, idesc, tmem + 128 + 4 * kb, tmem + 160 + 4 * kb, kb > 0);
+      }
+      tc_commit(bar_mma);
+    }
+  }
+  __syncthreads();
+  ok = (*reinterpret_cast<volatile int32_t*>(err) == 0);
+  if (ok && probe_wait(bar_mma, 0, err)) {
+    tc_fence_after();
+    const int r = threadIdx.x;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    for (int c = 0; c < p.n / 16; ++c) {
+      uint32_t v[16];
+      tmem_ld16(tmem + c * 16 + lane_base, v);
+      tmem_wait_ld();
+      for (int i = 0; i < 16; ++i) p.d[r * p.n + c * 16 + i] = __uint_as_float(v[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+template <int K>
+cudaError_t launch_mma_probe_k(const CUtensorMap& ta, const CUtensorMap& tb,
+                               const MmaProbeParams& p, cudaStream_t st) {
+  const int smem = 2 * 128 * (K / 2) + 2 * (K / 64) * 512 + 64 + 1024;
+  cudaError_t e =
+      cudaFuncSetAttribute(mma_probe_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  mma_probe_kernel<K><<<1, 128, smem, st>>>(ta, tb, p, p.status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_cvt_probe(uint32_t first, uint32_t count, uint8_t* e2m1, uint8_t* e4m3,
+                             cudaStream_t st) {
+  unsigned blocks = (count + 255) / 256;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  if (blocks == 0) blocks = 1;
+  cvt_probe_kernel<<<blocks, 256, 0, st>>>(first, count, e2m1, e4m3);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mma_probe(const CUtensorMap& ta, const CUtensorMap& tb, const MmaProbeParams& p,
+                             cudaStream_t st) {
+  if (p.K == 64) return launch_mma_probe_k<64>(ta, tb, p, st);
+  if (p.K == 128) return launch_mma_probe_k<128>(ta, tb, p, st);
+  return launch_mma_probe_k<256>(ta, tb, p, st);
+}
+
+}  // namespace sagefp4

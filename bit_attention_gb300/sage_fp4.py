@@ -1,0 +1,232 @@
+"""Thin Python binding of the C ABI in ``include/sage_fp4.h``.
+
+Argument marshalling only: every step of the attention path runs in the CUDA
+kernels of ``_build/libsagefp4.so``.  PyTorch provides device memory and
+streams.  There is no fallback: if the library cannot be built or loaded, or a
+call fails, an exception is raised.
+
+Functions named ``sage_fp4_*`` mirror the C entry points one to one and take
+raw device pointers; ``quantize_qkv`` and ``attn_fwd`` are the torch-tensor
+conveniences built on them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+from . import build as _build
+
+OK, EINVAL, ECUDA, ETIMEOUT, EUNSUPPORTED = 0, -1, -2, -3, -4
+
+_HEADER = os.path.join(_build.ROOT, "include", "sage_fp4.h")
+_lock = threading.Lock()
+_lib = None
+
+
+class SageFp4Error(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {strerror(code)} (status {code})")
+        self.code = code
+
+
+class sage_fp4_tensor(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+
+
+class sage_fp4_qkv(ctypes.Structure):
+    _fields_ = [("q", sage_fp4_tensor), ("k", sage_fp4_tensor), ("vt", sage_fp4_tensor),
+                ("status", ctypes.c_void_p)]
+
+
+def header_functions() -> list:
+    """Names of the functions declared in include/sage_fp4.h."""
+    text = open(_HEADER).read()
+    return sorted(set(re.findall(r"^[a-z_ 0-9\*]+?\b(sage_fp4_[a-z_0-9]+)\s*\(", text, re.M)))
+
+
+def load(build: bool = True) -> ctypes.CDLL:
+    """Load the library, building it first when it is missing or stale."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build else _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"CUDA library not built: {path}")
+            L = ctypes.CDLL(path)
+            vp, i, sz, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint32
+            qp = ctypes.POINTER(sage_fp4_qkv)
+            sig = {
+                "sage_fp4_workspace_bytes": (sz, [i, i, i, i]),
+                "sage_fp4_qkv_from_workspace": (i, [vp, sz, i, i, i, i, qp]),
+                "sage_fp4_quantize_qkv": (i, [vp, vp, vp, qp, i, i, i, i, vp]),
+                "sage_fp4_attn_fwd": (i, [qp, vp, i, i, i, i, i, vp]),
+                "sage_fp4_get_status": (i, [qp, vp]),
+                "sage_fp4_strerror": (ctypes.c_char_p, [i]),
+                "sage_fp4_cvt_probe": (i, [u32, u32, vp, vp, vp]),
+                "sage_fp4_mma_probe": (i, [vp, vp, vp, vp, i, i, i, vp, vp, vp]),
+            }
+            for name, (res, args) in sig.items():
+                fn = getattr(L, name)
+                fn.restype, fn.argtypes = res, args
+            _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return load().sage_fp4_strerror(int(code)).decode()
+    except Exception:  # the library itself failed to load
+        return f"status {code}"
+
+
+def _check(code: int, what: str) -> int:
+    if code != OK:
+        raise SageFp4Error(code, what)
+    return code
+
+
+# ------------------------------------------------------------- raw entry points
+def sage_fp4_workspace_bytes(B: int, H: int, N: int, D: int) -> int:
+    return load().sage_fp4_workspace_bytes(B, H, N, D)
+
+
+def sage_fp4_qkv_from_workspace(ws_ptr: int, ws_bytes: int, B: int, H: int, N: int, D: int):
+    out = sage_fp4_qkv()
+    rc = load().sage_fp4_qkv_from_workspace(ws_ptr, ws_bytes, B, H, N, D, ctypes.byref(out))
+    return rc, out
+
+
+def sage_fp4_quantize_qkv(q_ptr, k_ptr, v_ptr, qkv: sage_fp4_qkv, B, H, N, D, stream) -> int:
+    return load().sage_fp4_quantize_qkv(q_ptr, k_ptr, v_ptr, ctypes.byref(qkv), B, H, N, D, stream)
+
+
+def sage_fp4_attn_fwd(qkv: sage_fp4_qkv, o_ptr, B, H, N, D, causal, stream) -> int:
+    return load().sage_fp4_attn_fwd(ctypes.byref(qkv), o_ptr, B, H, N, D, int(causal), stream)
+
+
+def sage_fp4_get_status(qkv: sage_fp4_qkv, stream) -> int:
+    return load().sage_fp4_get_status(ctypes.byref(qkv), stream)
+
+
+def sage_fp4_strerror(code: int) -> str:
+    return strerror(code)
+
+
+def sage_fp4_cvt_probe(first: int, count: int, e2m1_ptr, e4m3_ptr, stream) -> int:
+    return load().sage_fp4_cvt_probe(first, count, e2m1_ptr, e4m3_ptr, stream)
+
+
+def sage_fp4_mma_probe(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threads, d, status,
+                       stream) -> int:
+    return load().sage_fp4_mma_probe(a_codes, a_scales, b_codes, b_scales, n, K,
+                                     int(a_by_threads), d, status, stream)
+
+
+# ------------------------------------------------------------- torch conveniences
+def _stream(stream=None) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _round_up(x: int, m: int) -> int:
+    return (x + m - 1) // m * m
+
+
+class QuantizedQKV:
+    """NVFP4 Q, K, V^T in one workspace tensor, with torch views of each part."""
+
+    def __init__(self, B: int, H: int, N: int, D: int, device=None):
+        import torch
+        self.B, self.H, self.N, self.D = B, H, N, D
+        self.Np = _round_up(N, 128)
+        nbytes = sage_fp4_workspace_bytes(B, H, N, D)
+        if nbytes == 0:
+            raise SageFp4Error(EINVAL, f"workspace for B={B} H={H} N={N} D={D}")
+        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+        rc, self.struct = sage_fp4_qkv_from_workspace(self.workspace.data_ptr(), nbytes, B, H, N, D)
+        _check(rc, "sage_fp4_qkv_from_workspace")
+
+    def _view(self, ptr: int, shape):
+        off = ptr - self.workspace.data_ptr()
+        n = 1
+        for s in shape:
+            n *= s
+        return self.workspace[off:off + n].view(*shape)
+
+    @property
+    def q_codes(self):
+        return self._view(self.struct.q.codes, (self.B * self.H, self.Np, self.D // 2))
+
+    @property
+    def q_scales(self):
+        return self._view(self.struct.q.scales, (self.B * self.H, self.Np * self.D // 16))
+
+    @property
+    def k_codes(self):
+        return self._view(self.struct.k.codes, (self.B * self.H, self.Np, self.D // 2))
+
+    @property
+    def k_scales(self):
+        return self._view(self.struct.k.scales, (self.B * self.H, self.Np * self.D // 16))
+
+    @property
+    def vt_codes(self):
+        return self._view(self.struct.vt.codes, (self.B * self.H, self.D, self.Np // 2))
+
+    @property
+    def vt_scales(self):
+        return self._view(self.struct.vt.scales, (self.B * self.H, 8 * self.Np))
+
+    @property
+    def status(self):
+        return self._view(self.struct.status, (4,)).view(torch_int32())
+
+    def get_status(self, stream=None) -> int:
+        return sage_fp4_get_status(self.struct, _stream(stream))
+
+
+def torch_int32():
+    import torch
+    return torch.int32
+
+
+def _check_input(x, B, H, N, D, name):
+    import torch
+    if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+        raise SageFp4Error(EINVAL, f"{name} must be a contiguous bf16 CUDA tensor")
+    if tuple(x.shape) != (B, H, N, D):
+        raise SageFp4Error(EINVAL, f"{name} has shape {tuple(x.shape)}, expected {(B, H, N, D)}")
+
+
+def quantize_qkv(q, k, v, out: QuantizedQKV | None = None, stream=None) -> QuantizedQKV:
+    """bf16 [B,H,N,D] Q, K, V on the GPU -> NVFP4 operands (one call, two kernels)."""
+    B, H, N, D = q.shape
+    for x, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _check_input(x, B, H, N, D, nm)
+    if out is None:
+        out = QuantizedQKV(B, H, N, D, device=q.device)
+    rc = sage_fp4_quantize_qkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.struct, B, H, N, D,
+                               _stream(stream))
+    _check(rc, "sage_fp4_quantize_qkv")
+    return out
+
+
+def attn_fwd(qkv: QuantizedQKV, causal: bool = False, out=None, stream=None):
+    """SageAttention3 FP4 attention forward over quantized operands -> bf16 [B,H,N,D]."""
+    import torch
+    B, H, N, D = qkv.B, qkv.H, qkv.N, qkv.D
+    if out is None:
+        out = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=qkv.workspace.device)
+    else:
+        _check_input(out, B, H, N, D, "out")
+    rc = sage_fp4_attn_fwd(qkv.struct, out.data_ptr(), B, H, N, D, causal, _stream(stream))
+    _check(rc, "sage_fp4_attn_fwd")
+    return out
+
+
+def attention(q, k, v, causal: bool = False, stream=None):
+    """Quantize and attend: bf16 Q, K, V [B,H,N,D] -> bf16 O."""
+    return attn_fwd(quantize_qkv(q, k, v, stream=stream), causal, stream=stream)

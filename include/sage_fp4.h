@@ -1,0 +1,152 @@
+/*
+ * sage_fp4.h -- C ABI of the GB300 (sm_103a) NVFP4 attention forward library.
+ *
+ * The method is SageAttention3's microscaled FP4 attention for inference:
+ *   - Q, K and V are quantized to NVFP4: E2M1 4-bit codes with one E4M3 scale
+ *     per 1x16 group (senqingzn.com article on SageAttention3, section
+ *     "Solving two obstacles and one difficulty", solution 1; section "FP4
+ *     attention inference acceleration and hardware implementation/
+ *     optimisation", NVFP4 paragraph);
+ *   - S = Q K^T and O = P V run on FP4 tensor cores with FP32 accumulation
+ *     (same section, accumulator paragraph; abstract of "SageAttention3:
+ *     Microscaling FP4 Attention for Inference and An Exploration of 8-Bit
+ *     Training");
+ *   - the online softmax is fused with a two-level quantization of P: each
+ *     token's row segment is first rescaled into [0, 448*6], then quantized
+ *     to NVFP4 in 1x16 groups (section "Solving two obstacles and one
+ *     difficulty", solution 2; the 16-element row maximum is fused with the
+ *     online softmax, hardware section).
+ *
+ * Conventions for every call:
+ *   - B, H, N, D: batch, heads, sequence length, head dimension.  D is 64 or
+ *     128.  Q, K, V and O are bf16, contiguous [B, H, N, D].
+ *   - N_pad = N rounded up to a multiple of 128.
+ *   - The softmax scale is 1/sqrt(D).  Causal: key j is visible to query i
+ *     iff j <= i (queries and keys share one sequence).
+ *   - Every pointer passed to a computing call is DEVICE memory owned by the
+ *     caller; the library allocates nothing, frees nothing and keeps no global
+ *     state besides per-device caches of kernel attributes.  All computing
+ *     calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).
+ *   - Inputs must be finite; NaN or Inf inputs give unspecified results.
+ *   - Return value: SAGE_FP4_OK or a negative status.  Argument errors are
+ *     detected on the host before anything is launched.  Errors found while a
+ *     kernel runs (a bounded wait that gave up) are written to the status word
+ *     and returned by sage_fp4_get_status().
+ *
+ * NVFP4 tensor layout (one quantized operand):
+ *   codes   packed E2M1, two per byte, the element with the even index in the
+ *           LOW nibble.  E2M1: bit 3 sign, bits 2-1 exponent (bias 1), bit 0
+ *           mantissa; values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives.
+ *   scales  E4M3 (bias 7, largest 448, sign bit 0), one per 16 elements along
+ *           the operand's contraction axis, stored in the 128x4 block layout
+ *           that block-scaled tensor-core MMAs read: for an operand of R rows
+ *           (R padded to a multiple of 128) and C contraction elements (C a
+ *           multiple of 64), the scale of row r and group g (g = element/16)
+ *           is at byte
+ *             ((r/128) * (C/64) + g/4) * 512 + (r%32) * 16 + ((r%128)/32) * 4 + g%4.
+ *   q, k    rows are tokens: codes [B*H][N_pad][D/2], scales with R = N_pad,
+ *           C = D, per (b,h) N_pad*D/16 bytes.  Groups run along D.
+ *   vt      V transposed, rows are channels: codes [B*H][D][N_pad/2], scales
+ *           with R = 128 (D padded to 128), C = N_pad, per (b,h) 8*N_pad bytes.
+ *           Groups run along tokens, the contraction axis of P V.
+ *   Rows/tokens in [N, N_pad) and padding channel rows hold code 0, scale 0.
+ *
+ * Quantization rule for one group x[0..15] (the pages fix the format, not the
+ * rounding; this is the reading, identical in the CPU oracle):
+ *   s = E4M3_rn(amax/6), with amax/6 a round-to-nearest float division;
+ *   if s == 0 every code is 0; else r = 1/s (round-to-nearest float) and
+ *   code_i = E2M1_rn(x_i * r) with the product rounded to float once;
+ *   both conversions round to nearest, ties to even, and saturate (E2M1 at
+ *   +-6, E4M3 at 448); a negative value that rounds to zero is -0 (code 0x8).
+ */
+#ifndef SAGE_FP4_H
+#define SAGE_FP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SAGE_FP4_OK 0
+#define SAGE_FP4_EINVAL (-1)      /* bad argument: null or misaligned pointer, bad size or D */
+#define SAGE_FP4_ECUDA (-2)       /* CUDA runtime/driver error at launch or copy */
+#define SAGE_FP4_ETIMEOUT (-3)    /* a kernel's bounded wait gave up (see sage_fp4_get_status) */
+#define SAGE_FP4_EUNSUPPORTED (-4) /* device is not sm_103 (the kernels are built for sm_103a) */
+
+typedef struct sage_fp4_tensor {
+  uint8_t *codes;  /* packed E2M1, 16-byte aligned */
+  uint8_t *scales; /* E4M3 in the 128x4 block layout, 16-byte aligned */
+} sage_fp4_tensor;
+
+typedef struct sage_fp4_qkv {
+  sage_fp4_tensor q;  /* quantized Q, rows = tokens */
+  sage_fp4_tensor k;  /* quantized K, rows = tokens */
+  sage_fp4_tensor vt; /* quantized V^T, rows = channels */
+  int32_t *status;    /* one int32 in device memory, zero-initialised by the caller */
+} sage_fp4_qkv;
+
+/* Bytes of one device buffer that holds all quantized operands plus the status
+ * word, each sub-buffer 256-byte aligned.  0 if the sizes are invalid. */
+size_t sage_fp4_workspace_bytes(int B, int H, int N, int D);
+
+/* Carve `workspace` (device memory of at least sage_fp4_workspace_bytes bytes,
+ * 256-byte aligned) into the operand pointers of *out.  Pointer arithmetic
+ * only: nothing is launched, nothing is written to the device.  The status
+ * word must still be zeroed by the caller (e.g. by zeroing the workspace). */
+int sage_fp4_qkv_from_workspace(void *workspace, size_t workspace_bytes, int B, int H, int N,
+                                int D, sage_fp4_qkv *out);
+
+/* Quantize bf16 Q, K, V ([B,H,N,D], contiguous, 16-byte aligned device memory)
+ * into the NVFP4 operands of *out (layouts above): Q and K along D, V along
+ * tokens into V^T.  Codes and scales are bit-exact with the rule above.
+ * Two kernel launches on `stream`.  Does not touch out->status. */
+int sage_fp4_quantize_qkv(const void *q, const void *k, const void *v, const sage_fp4_qkv *out,
+                          int B, int H, int N, int D, void *stream);
+
+/* Attention forward over quantized operands: O = softmax(Q K^T / sqrt(D)) V
+ * computed by the SageAttention3 FP4 method (block-scaled FP4 MMAs with FP32
+ * accumulation; online softmax over KV tiles of 128 keys fused with two-level
+ * P quantization, level 1 normalising each KV tile's row segment so that its
+ * maximum becomes 448*6).  o: bf16 [B,H,N,D] device memory, written in full.
+ * One kernel launch on `stream`.  Kernel-time failures set *qkv->status. */
+int sage_fp4_attn_fwd(const sage_fp4_qkv *qkv, void *o, int B, int H, int N, int D, int causal,
+                      void *stream);
+
+/* Synchronise `stream`, read the status word of `qkv`, reset it to 0 and
+ * return it (SAGE_FP4_OK, SAGE_FP4_ETIMEOUT) or SAGE_FP4_ECUDA if the copy
+ * itself failed. */
+int sage_fp4_get_status(const sage_fp4_qkv *qkv, void *stream);
+
+/* Static description of a status code. */
+const char *sage_fp4_strerror(int status);
+
+/* ---- diagnostics (tests use these to pin the device primitives) ---------- */
+
+/* Convert the floats whose bit patterns are first .. first+count-1 with the
+ * device's round-to-nearest saturating conversions used by the kernels:
+ * e2m1[i] = E2M1 code (low nibble), e4m3[i] = E4M3 byte.  Either output may
+ * be NULL.  Device memory. */
+int sage_fp4_cvt_probe(uint32_t first, uint32_t count, uint8_t *e2m1, uint8_t *e4m3,
+                       void *stream);
+
+/* One block-scaled FP4 tensor-core product D = A B^T for a 128-row tile, the
+ * building block of S = Q K^T and O = P V.  a: codes [128][K/2] and scales
+ * (block layout, R = 128, C = K); b: codes [n][K/2] and scales (R = 128 with
+ * rows >= n zero, C = K); d: float [128][n] row-major.  K in {64, 128, 256},
+ * n in {64, 128}.  a_by_threads = 1 stages A through ordinary shared-memory
+ * stores in the kernel's swizzled layout (the path P takes); 0 loads it with
+ * the tensor-memory-access engine (the path Q, K, V take).  status: one
+ * zero-initialised int32 that a timed-out wait sets to SAGE_FP4_ETIMEOUT.
+ * Device memory; codes and scales 16-byte aligned.  One launch on `stream`. */
+int sage_fp4_mma_probe(const uint8_t *a_codes, const uint8_t *a_scales, const uint8_t *b_codes,
+                       const uint8_t *b_scales, int n, int K, int a_by_threads, float *d,
+                       int32_t *status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAGE_FP4_H */

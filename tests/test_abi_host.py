@@ -1,0 +1,96 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every function include/sage_fp4.h declares, sizes its workspace, and rejects
+bad arguments before touching the device."""
+import ctypes
+
+import pytest
+
+from bit_attention_gb300 import sage_fp4 as S
+
+
+def test_library_exports_every_header_function():
+    lib = S.load()
+    names = S.header_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_workspace_bytes():
+    # per (b,h): Q,K codes N_pad*D/2 and scales N_pad*D/16; V^T codes D*N_pad/2,
+    # scales 128*N_pad/16; each part 256-aligned, plus 256 bytes of status
+    B, H, N, D = 4, 32, 4096, 128
+    BH, Np = B * H, 4096
+    parts = [BH * Np * D // 2, BH * Np * D // 16] * 2 + [BH * D * Np // 2, BH * 128 * Np // 16]
+    assert S.sage_fp4_workspace_bytes(B, H, N, D) == sum((p + 255) // 256 * 256 for p in parts) + 256
+    assert S.sage_fp4_workspace_bytes(1, 1, 17, 64) > 0
+    assert S.sage_fp4_workspace_bytes(1, 1, 17, 96) == 0
+    assert S.sage_fp4_workspace_bytes(-1, 1, 17, 64) == 0
+
+
+def test_workspace_carving_is_pointer_arithmetic():
+    base = 0x7000_0000
+    nbytes = S.sage_fp4_workspace_bytes(2, 3, 300, 64)
+    rc, q = S.sage_fp4_qkv_from_workspace(base, nbytes, 2, 3, 300, 64)
+    assert rc == 0
+    ptrs = [q.q.codes, q.q.scales, q.k.codes, q.k.scales, q.vt.codes, q.vt.scales, q.status]
+    assert ptrs == sorted(ptrs) and ptrs[0] == base
+    assert all(p % 256 == 0 for p in ptrs)
+    assert q.status + 4 <= base + nbytes
+    assert S.sage_fp4_qkv_from_workspace(base, nbytes - 1, 2, 3, 300, 64)[0] == S.EINVAL
+    assert S.sage_fp4_qkv_from_workspace(base + 16, nbytes, 2, 3, 300, 64)[0] == S.EINVAL
+
+
+def _qkv():
+    rc, q = S.sage_fp4_qkv_from_workspace(0x7000_0000, 1 << 30, 1, 2, 512, 128)
+    assert rc == 0
+    return q
+
+
+@pytest.mark.parametrize("args", [
+    dict(D=96), dict(N=-1), dict(B=-2), dict(o=0), dict(o=0x1008), dict(causal=2),
+])
+def test_attn_rejects_bad_arguments(args):
+    a = dict(B=1, H=2, N=512, D=128, o=0x1000, causal=0)
+    a.update(args)
+    rc = S.sage_fp4_attn_fwd(_qkv(), a["o"], a["B"], a["H"], a["N"], a["D"], a["causal"], None)
+    assert rc == S.EINVAL
+
+
+def test_attn_rejects_bad_operands():
+    q = _qkv()
+    q.k.codes = 0
+    assert S.sage_fp4_attn_fwd(q, 0x1000, 1, 2, 512, 128, 0, None) == S.EINVAL
+    q = _qkv()
+    q.vt.scales += 8
+    assert S.sage_fp4_attn_fwd(q, 0x1000, 1, 2, 512, 128, 0, None) == S.EINVAL
+    q = _qkv()
+    q.status = 0
+    assert S.sage_fp4_attn_fwd(q, 0x1000, 1, 2, 512, 128, 0, None) == S.EINVAL
+
+
+def test_quantize_rejects_bad_arguments():
+    q = _qkv()
+    assert S.sage_fp4_quantize_qkv(0, 0x2000, 0x3000, q, 1, 2, 512, 128, None) == S.EINVAL
+    assert S.sage_fp4_quantize_qkv(0x1004, 0x2000, 0x3000, q, 1, 2, 512, 128, None) == S.EINVAL
+    assert S.sage_fp4_quantize_qkv(0x1000, 0x2000, 0x3000, q, 1, 2, 512, 80, None) == S.EINVAL
+
+
+def test_empty_problems_are_no_ops():
+    # nothing to compute: OK without touching the device
+    q = _qkv()
+    assert S.sage_fp4_attn_fwd(q, 0x1000, 0, 2, 512, 128, 0, None) == S.OK
+    assert S.sage_fp4_attn_fwd(q, 0x1000, 1, 2, 0, 128, 1, None) == S.OK
+    assert S.sage_fp4_quantize_qkv(0x1000, 0x2000, 0x3000, q, 1, 0, 512, 64, None) == S.OK
+
+
+def test_probe_argument_checks():
+    assert S.sage_fp4_mma_probe(0x1000, 0x2000, 0x3000, 0x4000, 96, 64, 0, 0x5000, 0x6000, None) == S.EINVAL
+    assert S.sage_fp4_mma_probe(0x1000, 0x2000, 0x3000, 0x4000, 64, 32, 0, 0x5000, 0x6000, None) == S.EINVAL
+    assert S.sage_fp4_cvt_probe(0, 16, None, None, None) == S.EINVAL
+
+
+def test_strerror():
+    for code in (S.OK, S.EINVAL, S.ECUDA, S.ETIMEOUT, S.EUNSUPPORTED):
+        assert S.strerror(code) and S.strerror(code) != "unknown status"
+    assert S.strerror(12345) == "unknown status"

@@ -1,0 +1,89 @@
+"""Attention kernel parity against the oracle.
+
+Tolerance (the target's): relative L1 <= 5e-3 and cosine >= 0.999 between the
+kernel's bf16 O and the oracle's float64 O.  The two cannot agree bit for bit:
+the kernel takes exp2 in FP32 hardware approximation and accumulates in FP32,
+so a P code at a rounding boundary can land on the neighbouring E2M1 value,
+and O is rounded to bf16 (about 1e-3 of the budget).
+
+Small shapes are compared on every row; the full-size workloads, in the
+launch configuration the benchmark times, on a deterministic row sample that
+covers every (batch, head), first/last rows and tile edges.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_attention_gb300 import sage_fp4 as S
+from bit_attention_gb300.synth import WORKLOADS, make_qkv
+from helpers import cosine, rel_l1, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+REL_L1_MAX = 5e-3
+COS_MIN = 0.999
+
+
+def run_gpu(q, k, v, causal):
+    z = S.quantize_qkv(q.cuda(), k.cuda(), v.cuda())
+    o = S.attn_fwd(z, causal)
+    torch.cuda.synchronize()
+    assert z.get_status() == 0
+    return o
+
+
+def compare(q, k, v, causal, rows=None, label=""):
+    B, H, N, D = q.shape
+    o = run_gpu(q, k, v, causal).float().cpu().numpy().reshape(B * H * N, D)
+    qz = oracle.Quantized(q, k, v, B * H, N, D)
+    ref, _, _ = oracle.attention(qz, causal, "tile", rows=rows)
+    got = o if rows is None else o[rows]
+    assert np.isfinite(got).all()
+    e, c = rel_l1(got, ref), cosine(got, ref)
+    exact = oracle.attention_exact(q, k, v, B * H, N, D, causal, rows=rows)
+    print(f"{label} vs oracle rel-L1 {e:.2e} cos {c:.6f}; vs exact fp64 rel-L1 "
+          f"{rel_l1(got, exact):.3e} cos {cosine(got, exact):.5f}")
+    assert e <= REL_L1_MAX and c >= COS_MIN, (e, c)
+    return got, ref
+
+
+@pytest.mark.parametrize("B,H,N,D,causal,pattern", [
+    (1, 2, 512, 128, False, "iid"),
+    (1, 2, 512, 128, True, "iid"),
+    (2, 2, 300, 64, False, "iid"),
+    (2, 2, 300, 64, True, "k_head_mean"),
+    (1, 1, 17, 128, False, "iid"),
+    (1, 1, 17, 64, True, "iid"),
+    (1, 1, 128, 64, False, "iid"),
+    (1, 2, 1000, 128, True, "k_channel_outliers"),
+    (1, 2, 1100, 128, False, "k_channel_outliers"),
+    (1, 3, 777, 128, False, "sparse_outliers"),
+    (3, 1, 257, 64, True, "sparse_outliers"),
+])
+def test_attention_matches_oracle(B, H, N, D, causal, pattern):
+    q, k, v = make_qkv(B, H, N, D, pattern, seed=B * 1000 + N)
+    compare(q, k, v, causal, label=f"B{B} H{H} N{N} D{D} causal={causal} {pattern}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_all_keys_equal_gives_mean_of_v(causal):
+    # every score of a row is equal, so P quantizes exactly and O is the mean of
+    # the decoded V rows (causal: of rows 0..i) -- a closed form the oracle is
+    # pinned to
+    q, k, v = make_qkv(1, 2, 640, 128, "equal_k", seed=5)
+    got, ref = compare(q, k, v, causal, label=f"equal K causal={causal}")
+    assert np.abs(got - ref).max() <= 2 ** -8 * np.abs(ref).max() + 1e-6
+
+
+def test_zero_q():
+    q, k, v = make_qkv(1, 1, 384, 64, "zeros_q", seed=6)
+    compare(q, k, v, False, label="zero Q")
+
+
+@pytest.mark.parametrize("name", ["small", "llm", "llm_causal", "dit", "dit_long"])
+def test_full_workloads_sampled(name):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.pattern, seed=0)
+    rows = None if name == "small" else sample_rows(w.B * w.H, w.N, per_head=6, seed=1)
+    compare(q, k, v, w.causal, rows=rows, label=w.name)

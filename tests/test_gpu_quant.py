@@ -1,0 +1,74 @@
+"""Quantize kernel parity: codes and scales bit-exact with the oracle.
+
+Shapes span several 128-row tiles and ragged tails (N not a multiple of 16 or
+128), both head dims, the workloads' value patterns, and the full LLM-prefill
+workload (B4 H32 N4096 D128) compared in full.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_attention_gb300 import sage_fp4 as S
+from bit_attention_gb300.synth import WORKLOADS, make_qkv
+from helpers import block_to_plain
+
+pytestmark = pytest.mark.gpu
+
+
+def check_quant(q, k, v):
+    B, H, N, D = q.shape
+    BH = B * H
+    z = S.quantize_qkv(q.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    Np = z.Np
+    for name, x, codes, scales in (("q", q, z.q_codes, z.q_scales), ("k", k, z.k_codes, z.k_scales)):
+        rc, rs = oracle.quantize_rows(x, BH, N, D)
+        gc = codes.cpu().numpy()
+        gs = block_to_plain(scales.cpu().numpy(), Np, D // 16)
+        assert np.array_equal(gc, rc), f"{name} codes differ at {np.argwhere(gc != rc)[:5]}"
+        assert np.array_equal(gs, rs), f"{name} scales differ at {np.argwhere(gs != rs)[:5]}"
+    rc, rs = oracle.quantize_v(v, BH, N, D)
+    gc = z.vt_codes.cpu().numpy()
+    gs = block_to_plain(z.vt_scales.cpu().numpy(), 128, Np // 16)
+    assert np.array_equal(gc, rc), f"vt codes differ at {np.argwhere(gc != rc)[:5]}"
+    assert np.array_equal(gs[:, :D], rs), f"vt scales differ at {np.argwhere(gs[:, :D] != rs)[:5]}"
+    assert not gs[:, D:].any()
+    return z
+
+
+@pytest.mark.parametrize("B,H,N,D,pattern", [
+    (1, 2, 512, 128, "iid"),
+    (2, 3, 200, 64, "iid"),
+    (1, 1, 17, 128, "iid"),
+    (1, 2, 1000, 128, "k_channel_outliers"),
+    (2, 2, 130, 64, "k_head_mean"),
+    (1, 3, 777, 128, "sparse_outliers"),
+    (1, 1, 1, 64, "iid"),
+])
+def test_quantize_bit_exact(B, H, N, D, pattern):
+    q, k, v = make_qkv(B, H, N, D, pattern, seed=N)
+    check_quant(q, k, v)
+
+
+def test_quantize_special_values():
+    # zeros, tiny values whose scale rounds to zero, negative values that round
+    # to zero (-0 code), exact maxima, large values up to the E4M3 saturation
+    B, H, N, D = 1, 1, 256, 128
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((B, H, N, D)).astype(np.float32)
+    x[0, 0, 0] = 0.0
+    x[0, 0, 1] = 1e-5 * rng.standard_normal(D)
+    x[0, 0, 2, :16] = -1e-3
+    x[0, 0, 2, 0] = 6.0
+    x[0, 0, 3] = 3000.0 * rng.standard_normal(D)
+    x[0, 0, 4] = np.tile(np.array([6.0, 4.0, 3.0, 2.0, 1.5, 1.0, 0.5, 0.25] * 2, np.float32), D // 16)
+    x[0, 0, 5] = -x[0, 0, 4] * 0.75
+    t = torch.from_numpy(x).to(torch.bfloat16)
+    check_quant(t, t.clone(), t.clone())
+
+
+def test_quantize_full_llm_workload():
+    w = WORKLOADS["llm"]
+    q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.pattern, seed=0)
+    check_quant(q, k, v)
