@@ -113,13 +113,20 @@ def dist_init():
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time: the job finishes when every rank has."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(ops_per_rank: float, world: int, ms_per_step_max: float) -> float:
+    """Whole-job TOPS: every rank processes its own batch (weak scaling)."""
+    return ops_per_rank * world / (ms_per_step_max * 1e-3) / 1e12
 
 
 def barrier(world: int):
@@ -140,7 +147,7 @@ def cpu_oracle_sample(w, target_s: float, seed: int = 0):
     rng = np.random.default_rng(seed)
     rows_done, secs, ops = 0, 0.0, 0.0
     batch = max(oracle.num_threads(), 1)
-    while secs < target_s and rows_done < w.N:
+    while secs < target_s:
         rows = rng.integers(0, w.N, size=batch)
         t0 = time.perf_counter()
         oracle.attention(qz, w.causal, rows=rows)
@@ -186,6 +193,7 @@ def main():
     ap.add_argument("--workload", default="llm")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--causal", type=int, default=None)
+    ap.add_argument("--shape", default=None, help="B,H,N,D override (profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=6.0)
@@ -198,6 +206,9 @@ def main():
     w = WORKLOADS[args.workload]
     if args.causal is not None:
         w = Workload(w.name, w.B, w.H, w.N, w.D, bool(args.causal), w.pattern)
+    if args.shape:
+        B, H, N, D = (int(x) for x in args.shape.split(","))
+        w = Workload(f"attn_fwd B{B} H{H} N{N} D{D} {w.pattern}", B, H, N, D, w.causal, w.pattern)
 
     world, rank, local = dist_init()
     if args.impl == "reference":
@@ -253,7 +264,7 @@ def main():
         raise RuntimeError(f"kernel status {S.strerror(status)}")
 
     ops = w.ops
-    value = ops * world / (ms_step * 1e-3) / 1e12
+    value = job_throughput(ops, world, ms_step)
     pk = peaks()
     fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
     attn_tops = ops / (a_ms * 1e-3) / 1e12
