@@ -207,6 +207,8 @@ const char* sage_fp4_strerror(int status) {
       return "a kernel's bounded wait gave up; the output is not valid";
     case SAGE_FP4_EUNSUPPORTED:
       return "device is not sm_103 (kernels are built for sm_103a)";
+    case SAGE_FP4_ETOOLARGE:
+      return "problem needs more than the no-allocation entry's fixed 64 MiB scratch";
     default:
       return "unknown status";
   }

@@ -18,7 +18,7 @@ import threading
 
 from . import build as _build
 
-OK, EINVAL, ECUDA, ETIMEOUT, EUNSUPPORTED = 0, -1, -2, -3, -4
+OK, EINVAL, ECUDA, ETIMEOUT, EUNSUPPORTED, ETOOLARGE = 0, -1, -2, -3, -4, -5
 
 _HEADER = os.path.join(_build.ROOT, "include", "sage_fp4.h")
 _lock = threading.Lock()
@@ -66,6 +66,7 @@ def load(build: bool = True) -> ctypes.CDLL:
                 "sage_fp4_strerror": (ctypes.c_char_p, [i]),
                 "sage_fp4_cvt_probe": (i, [u32, u32, vp, vp, vp]),
                 "sage_fp4_mma_probe": (i, [vp, vp, vp, vp, i, i, i, vp, vp, vp]),
+                "sage_fp4_attention_noalloc": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -122,6 +123,13 @@ def sage_fp4_mma_probe(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threads,
                        stream) -> int:
     return load().sage_fp4_mma_probe(a_codes, a_scales, b_codes, b_scales, n, K,
                                      int(a_by_threads), d, status, stream)
+
+
+def sage_fp4_attention_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, status_ptr, B, H, N, D, causal,
+                               stream) -> int:
+    """One-call quantize + attention that allocates nothing (fixed device scratch)."""
+    return load().sage_fp4_attention_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, status_ptr, B, H, N, D,
+                                             int(causal), stream)
 
 
 # ------------------------------------------------------------- torch conveniences

@@ -75,6 +75,7 @@ extern "C" {
 #define SAGE_FP4_ECUDA (-2)       /* CUDA runtime/driver error at launch or copy */
 #define SAGE_FP4_ETIMEOUT (-3)    /* a kernel's bounded wait gave up (see sage_fp4_get_status) */
 #define SAGE_FP4_EUNSUPPORTED (-4) /* device is not sm_103 (the kernels are built for sm_103a) */
+#define SAGE_FP4_ETOOLARGE (-5)   /* problem needs more than the no-allocation entry's fixed scratch */
 
 typedef struct sage_fp4_tensor {
   uint8_t *codes;  /* packed E2M1, 16-byte aligned */
@@ -122,6 +123,41 @@ int sage_fp4_get_status(const sage_fp4_qkv *qkv, void *stream);
 
 /* Static description of a status code. */
 const char *sage_fp4_strerror(int status);
+
+/* ---- one-call attention for callers that cannot allocate ------------------ */
+
+/* Size of the fixed device scratch array behind sage_fp4_attention_noalloc. */
+#define SAGE_FP4_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* No counterpart in the pages: a convenience of this library.  Quantize bf16
+ * q, k, v ([B,H,N,D], contiguous, 16-byte aligned) and run the attention
+ * forward into bf16 o, in one call that allocates nothing.  It is meant for
+ * callers that cannot call cudaMalloc: code running inside another
+ * framework's operator without access to its allocator, plugins whose host
+ * owns every device allocation, code that must not allocate after start-up.
+ *
+ * The quantized operands live in one file-scope device array of
+ * SAGE_FP4_NOALLOC_SCRATCH_BYTES (64 MiB) instead of a caller workspace.
+ * Every GPU that loads the library's module holds that array until the
+ * process exits.  Problems whose operands need more (sage_fp4_workspace_bytes
+ * minus 256) are rejected with SAGE_FP4_ETOOLARGE before anything runs; the
+ * LLM prefill shape B1 H32 N8192 D128 (~54 MiB) fits, B4 H32 N4096 D128 does
+ * not.
+ *
+ * status: one int32 of device memory, zero-initialised by the caller, set to
+ * SAGE_FP4_ETIMEOUT if a bounded device wait gives up (as in
+ * sage_fp4_attn_fwd; launches skip their work while it is nonzero).
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture.  All calls share the array and it keeps the last call's contents;
+ * each call rewrites every byte it reads, so nothing has to be cleared
+ * between calls.  Calls whose work overlaps on the GPU (unordered streams or
+ * host threads) race on the array: order them.  Asynchronous on `stream`;
+ * three kernel launches. */
+int sage_fp4_attention_noalloc(const void *q, const void *k, const void *v, void *o,
+                               int32_t *status, int B, int H, int N, int D, int causal,
+                               void *stream);
 
 /* ---- diagnostics (tests use these to pin the device primitives) ---------- */
 
