@@ -13,11 +13,15 @@
 //   PV  = (P^ sP)(V^ sV)        block-scaled FP4 MMA with FP32 accumulation
 //   O   = O * exp(m_old - m_new) + exp(t - m_new)/2688 * PV   (FP32)
 // Roles (warp specialisation, mbarrier pipelines, all waits bounded):
-//   warp 0      TMA / bulk-copy producer of Q, K, V^T tiles and their scales
-//   warp 1      tcgen05 MMA issuer (one thread)
-//   warp 2      tensor-memory allocator
-//   warps 4-7   softmax + P quantization, one thread per query row
-//   warps 8-11  correction: rescale-and-accumulate O in registers, epilogue
+//   warp 0       TMA / bulk-copy producer of Q, K, V^T tiles and their scales
+//   warp 1       tcgen05 MMA issuer (one thread); S runs two tiles ahead of PV
+//   warp 2       tensor-memory allocator
+//   warps 4-7    softmax + P quantization of the even KV tiles, one thread per row
+//   warps 8-11   the same for the odd KV tiles: with level 1 normalised per
+//                tile, tiles are independent until O is combined
+//   warps 12-15  correction: rescale-and-accumulate O in registers, epilogue
+// Registers are rebalanced with setmaxnreg: 64 (warps 0-3), 136 (softmax),
+// 176 (correction); 64*128 + 136*256 + 176*128 = 65536.
 // Tensor memory (512 columns x 128 lanes): three 128-column buffers that hold
 // S of a tile and, once S has been read, that tile's PV; then the scale
 // factors of Q, K, P and V.
@@ -35,7 +39,9 @@ namespace {
 
 constexpr int kStages = 4;   // K and V^T shared-memory ring depth
 constexpr int kNumBuf = 3;   // S/PV tensor-memory buffers
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
+constexpr uint32_t kRegsCtl = 64, kRegsSoftmax = 136, kRegsCorr = 176;
+static_assert(kRegsCtl * 128 + kRegsSoftmax * 256 + kRegsCorr * 128 == 65536, "register split");
 constexpr uint64_t kWaitLimitNs = 1500ull * 1000ull * 1000ull;  // a bounded wait gives up after 1.5 s
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
@@ -101,7 +107,7 @@ __device__ __forceinline__ void give_up(const Ctl& c) {
 }
 
 // Bounded wait by a single thread.  False: the CTA is abandoning its work.
-__device__ __noinline__ bool wait1(uint32_t bar, uint32_t parity, Ctl c) {
+__device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, Ctl c) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -115,7 +121,7 @@ __device__ __noinline__ bool wait1(uint32_t bar, uint32_t parity, Ctl c) {
 }
 
 // Bounded wait by a whole warp; every lane gets the same answer.
-__device__ __noinline__ bool waitw(uint32_t bar, uint32_t parity, Ctl c) {
+__device__ __forceinline__ bool waitw(uint32_t bar, uint32_t parity, Ctl c) {
   if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -134,19 +140,25 @@ __device__ __noinline__ bool waitw(uint32_t bar, uint32_t parity, Ctl c) {
 }
 
 // Wait used only while abandoning work: ignores the abort flag, still bounded.
-__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < kWaitLimitNs) {
   }
 }
 
-__device__ __forceinline__ float maxf16(const uint32_t* s) {
-  float m[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) m[i] = fmaxf(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
-#pragma unroll
-  for (int i = 0; i < 4; ++i) m[i] = fmaxf(m[i], m[i + 4]);
-  return fmaxf(fmaxf(m[0], m[2]), fmaxf(m[1], m[3]));
+// All threads of the CTA, each role from its own code path (named barrier 1).
+__device__ __forceinline__ void cta_bar_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+}
+
+constexpr float kLog2of2688 = 11.392317422778761f;  // log2(448 * 6)
+
+__device__ __forceinline__ float max16(const uint32_t* s) {
+  auto f = [&](int i) { return __uint_as_float(s[i]); };
+  const float m0 = max3f(f(0), f(1), f(2)), m1 = max3f(f(3), f(4), f(5));
+  const float m2 = max3f(f(6), f(7), f(8)), m3 = max3f(f(9), f(10), f(11));
+  const float m4 = max3f(f(12), f(13), f(14));
+  return max3f(max3f(m0, m1, m2), max3f(m3, m4, f(15)), m0);
 }
 
 template <int D>
@@ -209,237 +221,304 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const bool skip = *abort_flag != 0;
 
-  if (!skip && warp == 0 && lane == 0) {
-    // ------------------------------------------------------------ producer
-    prefetch_tensormap(&tm_q);
-    prefetch_tensormap(&tm_k);
-    prefetch_tensormap(&tm_v);
-    const uint8_t* sfq = p.sfq + static_cast<size_t>(bh) * p.Np * (D / 16);
-    const uint8_t* sfk = p.sfk + static_cast<size_t>(bh) * p.Np * (D / 16);
-    const uint8_t* sfv = p.sfv + static_cast<size_t>(bh) * 8 * p.Np;
-    mbar_arrive_expect_tx(bar(B_QFULL), L::QBYTES + L::SFQK);
-    tma_load_2d(sb + L::oQ, &tm_q, 0, bh * p.Np + qt * kTileQ, bar(B_QFULL));
-    bulk_load(sb + L::oSFQ, sfq + static_cast<size_t>(qt) * L::SFQK, L::SFQK, bar(B_QFULL));
-    int issued_k = 0, issued_v = 0;
-    bool ok = true;
-    for (int k = 0; k < nkv; ++k) {
-      const int s = k % kStages, u = k / kStages;
-      if (u > 0 && !(ok = wait1(bar(B_KEMPTY + s), (u - 1) & 1, ctl))) break;
-      mbar_arrive_expect_tx(bar(B_KFULL + s), L::QBYTES + L::SFQK);
-      tma_load_2d(sb + L::oK + s * L::QBYTES, &tm_k, 0, bh * p.Np + k * kTileKV, bar(B_KFULL + s));
-      bulk_load(sb + L::oSFK + s * L::SFQK, sfk + static_cast<size_t>(k) * L::SFQK, L::SFQK,
-                bar(B_KFULL + s));
-      issued_k = k + 1;
-      if (u > 0 && !(ok = wait1(bar(B_VEMPTY + s), (u - 1) & 1, ctl))) break;
-      mbar_arrive_expect_tx(bar(B_VFULL + s), L::VBYTES + L::SFVB);
-      tma_load_2d(sb + L::oV + s * L::VBYTES, &tm_v, k * (kTileKV / 2), bh * D, bar(B_VFULL + s));
-      bulk_load(sb + L::oSFV + s * L::SFVB, sfv + static_cast<size_t>(k) * L::SFVB, L::SFVB,
-                bar(B_VFULL + s));
-      issued_v = k + 1;
-    }
-    if (!ok) {
-      // abandoning: let the copies this thread started land before the CTA exits
-      drain_wait(bar(B_QFULL), 0);
-      for (int k = (issued_k > kStages ? issued_k - kStages : 0); k < issued_k; ++k)
-        drain_wait(bar(B_KFULL + k % kStages), (k / kStages) & 1);
-      for (int k = (issued_v > kStages ? issued_v - kStages : 0); k < issued_v; ++k)
-        drain_wait(bar(B_VFULL + k % kStages), (k / kStages) & 1);
-    }
-  } else if (!skip && warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idS = idesc_nvfp4(128, 128);
-    constexpr uint32_t idPV = idesc_nvfp4(128, D);
-    constexpr uint32_t qk_swz = (D == 128) ? kSwizzle64B : kSwizzle32B;
-    constexpr uint32_t qk_sbo = 8 * (D / 2);
-    bool ok = wait1(bar(B_QFULL), 0, ctl);
-    if (ok) {
-      tc_fence_after();
-#pragma unroll
-      for (int kb = 0; kb < L::KBD; ++kb)
-        tc_cp_32x128b_warpx4(tmem + kColSFQ + 4 * kb,
-                             smem_desc(sb + L::oSFQ + 512 * kb, 0, 128, kSwizzleNone));
-    }
-    auto issue_pv = [&](int j) -> bool {
-      const int s = j % kStages, b = j % kNumBuf, ps = j & 1;
-      if (!wait1(bar(B_PFULL + ps), (j >> 1) & 1, ctl)) return false;
-      if (!wait1(bar(B_VFULL + s), (j / kStages) & 1, ctl)) return false;
-      tc_fence_after();
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {
-        tc_cp_32x128b_warpx4(tmem + kColSFP + 8 * ps + 4 * kb,
-                             smem_desc(sb + L::oSFP + ps * L::SFPB + 512 * kb, 0, 128, kSwizzleNone));
-        tc_cp_32x128b_warpx4(tmem + kColSFV + 8 * ps + 4 * kb,
-                             smem_desc(sb + L::oSFV + s * L::SFVB + 512 * kb, 0, 128, kSwizzleNone));
+  const int wg = warp / 4;
+  if (wg == 0) {
+    regs_dec<kRegsCtl>();
+    if (!skip && warp == 0 && lane == 0) {
+      // ------------------------------------------------------------ producer
+      prefetch_tensormap(&tm_q);
+      prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v);
+      const uint8_t* sfq = p.sfq + static_cast<size_t>(bh) * p.Np * (D / 16);
+      const uint8_t* sfk = p.sfk + static_cast<size_t>(bh) * p.Np * (D / 16);
+      const uint8_t* sfv = p.sfv + static_cast<size_t>(bh) * 8 * p.Np;
+      mbar_arrive_expect_tx(bar(B_QFULL), L::QBYTES + L::SFQK);
+      tma_load_2d(sb + L::oQ, &tm_q, 0, bh * p.Np + qt * kTileQ, bar(B_QFULL));
+      bulk_load(sb + L::oSFQ, sfq + static_cast<size_t>(qt) * L::SFQK, L::SFQK, bar(B_QFULL));
+      int issued_k = 0, issued_v = 0;
+      bool ok = true;
+      for (int k = 0; k < nkv; ++k) {
+        const int s = k % kStages, u = k / kStages;
+        if (u > 0 && !(ok = wait1(bar(B_KEMPTY + s), (u - 1) & 1, ctl))) break;
+        mbar_arrive_expect_tx(bar(B_KFULL + s), L::QBYTES + L::SFQK);
+        tma_load_2d(sb + L::oK + s * L::QBYTES, &tm_k, 0, bh * p.Np + k * kTileKV, bar(B_KFULL + s));
+        bulk_load(sb + L::oSFK + s * L::SFQK, sfk + static_cast<size_t>(k) * L::SFQK, L::SFQK,
+                  bar(B_KFULL + s));
+        issued_k = k + 1;
+        if (u > 0 && !(ok = wait1(bar(B_VEMPTY + s), (u - 1) & 1, ctl))) break;
+        mbar_arrive_expect_tx(bar(B_VFULL + s), L::VBYTES + L::SFVB);
+        tma_load_2d(sb + L::oV + s * L::VBYTES, &tm_v, k * (kTileKV / 2), bh * D, bar(B_VFULL + s));
+        bulk_load(sb + L::oSFV + s * L::SFVB, sfv + static_cast<size_t>(k) * L::SFVB, L::SFVB,
+                  bar(B_VFULL + s));
+        issued_v = k + 1;
       }
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {
-        const uint64_t ad = smem_desc(sb + L::oP + ps * L::PBYTES + 32 * kb, 16, 512, kSwizzle64B);
-        const uint64_t bd = smem_desc(sb + L::oV + s * L::VBYTES + 32 * kb, 16, 512, kSwizzle64B);
-        mma_nvfp4(tmem + b * 128, ad, bd, idPV, tmem + kColSFP + 8 * ps + 4 * kb,
-                  tmem + kColSFV + 8 * ps + 4 * kb, kb > 0);
+      if (!ok) {
+        // abandoning: let the copies this thread started land before the CTA exits
+        drain_wait(bar(B_QFULL), 0);
+        for (int k = (issued_k > kStages ? issued_k - kStages : 0); k < issued_k; ++k)
+          drain_wait(bar(B_KFULL + k % kStages), (k / kStages) & 1);
+        for (int k = (issued_v > kStages ? issued_v - kStages : 0); k < issued_v; ++k)
+          drain_wait(bar(B_VFULL + k % kStages), (k / kStages) & 1);
       }
-      tc_commit(bar(B_PVFULL + b));
-      tc_commit(bar(B_VEMPTY + s));
-      tc_commit(bar(B_PEMPTY + ps));
-      return true;
-    };
-    for (int k = 0; k < nkv && ok; ++k) {
-      const int s = k % kStages, b = k % kNumBuf, sl = k & 1;
-      if (!(ok = wait1(bar(B_KFULL + s), (k / kStages) & 1, ctl))) break;
-      if (k >= kNumBuf && !(ok = wait1(bar(B_BUFFREE + b), ((k / kNumBuf) - 1) & 1, ctl))) break;
-      tc_fence_after();
+    } else if (!skip && warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idS = idesc_nvfp4(128, 128);
+      constexpr uint32_t idPV = idesc_nvfp4(128, D);
+      constexpr uint32_t qk_swz = (D == 128) ? kSwizzle64B : kSwizzle32B;
+      constexpr uint32_t qk_sbo = 8 * (D / 2);
+      bool ok = wait1(bar(B_QFULL), 0, ctl);
+      if (ok) {
+        tc_fence_after();
 #pragma unroll
-      for (int kb = 0; kb < L::KBD; ++kb)
-        tc_cp_32x128b_warpx4(tmem + kColSFK + 8 * sl + 4 * kb,
-                             smem_desc(sb + L::oSFK + s * L::SFQK + 512 * kb, 0, 128, kSwizzleNone));
-#pragma unroll
-      for (int kb = 0; kb < L::KBD; ++kb) {
-        const uint64_t ad = smem_desc(sb + L::oQ + 32 * kb, 16, qk_sbo, qk_swz);
-        const uint64_t bd = smem_desc(sb + L::oK + s * L::QBYTES + 32 * kb, 16, qk_sbo, qk_swz);
-        mma_nvfp4(tmem + b * 128, ad, bd, idS, tmem + kColSFQ + 4 * kb,
-                  tmem + kColSFK + 8 * sl + 4 * kb, kb > 0);
+        for (int kb = 0; kb < L::KBD; ++kb)
+          tc_cp_32x128b_warpx4(tmem + kColSFQ + 4 * kb,
+                               smem_desc(sb + L::oSFQ + 512 * kb, 0, 128, kSwizzleNone));
       }
-      tc_commit(bar(B_SFULL + b));
-      tc_commit(bar(B_KEMPTY + s));
-      if (k >= 1) ok = issue_pv(k - 1);
-    }
-    if (ok) ok = issue_pv(nkv - 1);
-    if (!ok) {
-      // abandoning: wait for the tensor-core work this thread issued
-      tc_commit(bar(B_DRAIN));
-      drain_wait(bar(B_DRAIN), 0);
-    }
-  } else if (!skip && warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ softmax + P quantization
-    const int r = threadIdx.x - 128;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int gi = qt * kTileQ + r;
-    const int vis_end = p.causal ? min(p.N, gi + 1) : p.N;  // keys j < vis_end are visible
-    const float a = p.a;
-    for (int k = 0; k < nkv; ++k) {
-      const int b = k % kNumBuf, ps = k & 1;
-      if (!waitw(bar(B_SFULL + b), (k / kNumBuf) & 1, ctl)) break;
-      tc_fence_after();
-      uint32_t s[128];
+      // S_k into buffer k % 3 (free once the correction has read PV_{k-3})
+      auto issue_s = [&](int k) -> bool {
+        const int s = k % kStages, b = k % kNumBuf, sl = k & 1;
+        if (!wait1(bar(B_KFULL + s), (k / kStages) & 1, ctl)) return false;
+        if (k >= kNumBuf && !wait1(bar(B_BUFFREE + b), ((k / kNumBuf) - 1) & 1, ctl)) return false;
+        tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tmem_ld32(tmem + b * 128 + c * 32 + lane_base, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
-      tmem_wait_ld();
-      const int lim = vis_end - k * kTileKV;
-      if (lim < kTileKV) {
+        for (int kb = 0; kb < L::KBD; ++kb)
+          tc_cp_32x128b_warpx4(tmem + kColSFK + 8 * sl + 4 * kb,
+                               smem_desc(sb + L::oSFK + s * L::SFQK + 512 * kb, 0, 128, kSwizzleNone));
 #pragma unroll
-        for (int j = 0; j < 128; ++j)
-          if (j >= lim) s[j] = __float_as_uint(-INFINITY);
-      }
-      float gm[8];
-#pragma unroll
-      for (int g = 0; g < 8; ++g) gm[g] = maxf16(&s[16 * g]);
-      const float t = fmaxf(fmaxf(fmaxf(gm[0], gm[1]), fmaxf(gm[2], gm[3])),
-                            fmaxf(fmaxf(gm[4], gm[5]), fmaxf(gm[6], gm[7])));
-      const float nb = -t * a;
-      float lsum = 0.0f;
-      uint32_t pw[16];
-      uint32_t sfw[2] = {0u, 0u};
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        // level 1: P2 = 2688 * exp(c (S - t)); the group's P2 maximum gives the
-        // level-2 scale E4M3(max/6), so the row maximum's group gets 448
-        const float eg = ex2_approx(fmaf(gm[g], a, nb));
-        const uint32_t sbyte = cvt_e4m3(448.0f * eg);
-        const float sd = e4m3_to_f32(sbyte);
-        const float cm = (sd > 0.0f) ? __fdividef(2688.0f, sd) : 0.0f;
-        float e[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) e[j] = ex2_approx(fmaf(__uint_as_float(s[16 * g + j]), a, nb));
-        float part[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) part[j] = e[2 * j] + e[2 * j + 1];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) part[j] += part[j + 4];
-        lsum += (part[0] + part[2]) + (part[1] + part[3]);
-        float y[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) y[j] = e[j] * cm;
-        pw[2 * g] = cvt_e2m1x8(y);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) y[j] = e[8 + j] * cm;
-        pw[2 * g + 1] = cvt_e2m1x8(y);
-        sfw[g >> 2] |= sbyte << (8 * (g & 3));
-      }
-      if (k >= 2 && !waitw(bar(B_PEMPTY + ps), ((k >> 1) - 1) & 1, ctl)) break;
-      uint8_t* prow = sm + L::oP + ps * L::PBYTES + r * 64;
-      const int sw = (r >> 1) & 3;  // 64-byte swizzle: 16-byte chunk c lives at c ^ ((r/2) % 4)
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ sw) * 16)) =
-            make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-      uint8_t* sfp = sm + L::oSFP + ps * L::SFPB + (r % 32) * 16 + (r / 32) * 4;
-      *reinterpret_cast<uint32_t*>(sfp) = sfw[0];
-      *reinterpret_cast<uint32_t*>(sfp + 512) = sfw[1];
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(B_PFULL + ps));
-      if (k >= 2 && !waitw(bar(B_STEMPTY + ps), ((k >> 1) - 1) & 1, ctl)) break;
-      reinterpret_cast<float2*>(sm + L::oStat + ps * 1024)[r] = make_float2(t, lsum);
-      mbar_arrive(bar(B_STFULL + ps));
-    }
-  } else if (!skip && warp >= 8) {
-    // ------------------------------------------------------------ correction + epilogue
-    const int r = threadIdx.x - 256;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const float a = p.a;
-    float o[D];
-#pragma unroll
-    for (int d = 0; d < D; ++d) o[d] = 0.0f;
-    float m = -INFINITY, l = 0.0f;
-    bool ok = true;
-    for (int k = 0; k < nkv; ++k) {
-      const int b = k % kNumBuf, ps = k & 1;
-      if (!(ok = waitw(bar(B_STFULL + ps), (k >> 1) & 1, ctl))) break;
-      const float2 st = reinterpret_cast<const float2*>(sm + L::oStat + ps * 1024)[r];
-      mbar_arrive(bar(B_STEMPTY + ps));
-      const float mn = fmaxf(m, st.x);
-      const float alpha = ex2_approx((m - mn) * a);
-      const float beta = ex2_approx((st.x - mn) * a);
-      l = l * alpha + st.y * beta;
-      const float w = beta * (1.0f / 2688.0f);
-      m = mn;
-      if (!(ok = waitw(bar(B_PVFULL + b), (k / kNumBuf) & 1, ctl))) break;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
-        uint32_t v[16];
-        tmem_ld16(tmem + b * 128 + c * 16 + lane_base, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) o[c * 16 + i] = fmaf(__uint_as_float(v[i]), w, o[c * 16 + i] * alpha);
-      }
-      tc_fence_before();
-      mbar_arrive(bar(B_BUFFREE + b));
-    }
-    const int gi = qt * kTileQ + r;
-    if (ok && gi < p.N) {
-      const float inv = 1.0f / l;
-      uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
-                                             (static_cast<size_t>(bh) * p.N + gi) * D);
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        uint32_t w4[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(o[c * 8 + 2 * i] * inv, o[c * 8 + 2 * i + 1] * inv);
-          w4[i] = *reinterpret_cast<uint32_t*>(&h2);
+        for (int kb = 0; kb < L::KBD; ++kb) {
+          const uint64_t ad = smem_desc(sb + L::oQ + 32 * kb, 16, qk_sbo, qk_swz);
+          const uint64_t bd = smem_desc(sb + L::oK + s * L::QBYTES + 32 * kb, 16, qk_sbo, qk_swz);
+          mma_nvfp4(tmem + b * 128, ad, bd, idS, tmem + kColSFQ + 4 * kb,
+                    tmem + kColSFK + 8 * sl + 4 * kb, kb > 0);
         }
-        orow[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        tc_commit(bar(B_SFULL + b));
+        tc_commit(bar(B_KEMPTY + s));
+        return true;
+      };
+      // PV_j into the buffer that held S_j (the softmax has read it)
+      auto issue_pv = [&](int j) -> bool {
+        const int s = j % kStages, b = j % kNumBuf, ps = j & 1;
+        if (!wait1(bar(B_PFULL + ps), (j >> 1) & 1, ctl)) return false;
+        if (!wait1(bar(B_VFULL + s), (j / kStages) & 1, ctl)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          tc_cp_32x128b_warpx4(tmem + kColSFP + 8 * ps + 4 * kb,
+                               smem_desc(sb + L::oSFP + ps * L::SFPB + 512 * kb, 0, 128, kSwizzleNone));
+          tc_cp_32x128b_warpx4(tmem + kColSFV + 8 * ps + 4 * kb,
+                               smem_desc(sb + L::oSFV + s * L::SFVB + 512 * kb, 0, 128, kSwizzleNone));
+        }
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          const uint64_t ad = smem_desc(sb + L::oP + ps * L::PBYTES + 32 * kb, 16, 512, kSwizzle64B);
+          const uint64_t bd = smem_desc(sb + L::oV + s * L::VBYTES + 32 * kb, 16, 512, kSwizzle64B);
+          mma_nvfp4(tmem + b * 128, ad, bd, idPV, tmem + kColSFP + 8 * ps + 4 * kb,
+                    tmem + kColSFV + 8 * ps + 4 * kb, kb > 0);
+        }
+        tc_commit(bar(B_PVFULL + b));
+        tc_commit(bar(B_VEMPTY + s));
+        tc_commit(bar(B_PEMPTY + ps));
+        return true;
+      };
+      // S runs two tiles ahead of PV so that each softmax warpgroup finds its
+      // next S ready
+      if (ok) ok = issue_s(0);
+      if (ok && nkv > 1) ok = issue_s(1);
+      for (int j = 0; j < nkv && ok; ++j) {
+        ok = issue_pv(j);
+        if (ok && j + 2 < nkv) ok = issue_s(j + 2);
+      }
+      if (!ok) {
+        // abandoning: wait for the tensor-core work this thread issued
+        tc_commit(bar(B_DRAIN));
+        drain_wait(bar(B_DRAIN), 0);
       }
     }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 2) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    // every role ends at the same CTA-wide barrier; then tensor memory is freed
+    tc_fence_before();
+    cta_bar_sync();
+    if (warp == 2) {
+      tc_fence_after();
+      tmem_dealloc(tmem, kTmemCols);
+    }
+  } else if (wg == 1 || wg == 2) {
+    // -------------------------------------------------------- softmax + P quantization
+    regs_inc<kRegsSoftmax>();
+    if (!skip) {
+      const int r = threadIdx.x - 128 * wg;  // query row of this thread = TMEM lane
+      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const int gi = qt * kTileQ + r;
+      const int vis_end = p.causal ? min(p.N, gi + 1) : p.N;  // keys j < vis_end are visible
+      const float a = p.a;
+      const uint64_t a2 = pack2(a, a);
+      for (int k = wg - 1; k < nkv; k += 2) {
+        const int b = k % kNumBuf, ps = k & 1;
+        if (!waitw(bar(B_SFULL + b), (k / kNumBuf) & 1, ctl)) break;
+        tc_fence_after();
+        const uint32_t tb = tmem + b * 128 + lane_base;
+        const int lim = vis_end - k * kTileKV;
+        // pass 1: the 16-element group maxima, whose maximum is the tile maximum
+        float gm[8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sv[64];
+          tmem_ld32(tb + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+          tmem_ld32(tb + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+          tmem_wait_ld();
+          if (lim < kTileKV) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              if (64 * h + j >= lim) sv[j] = __float_as_uint(-INFINITY);
+          }
+#pragma unroll
+          for (int g = 0; g < 4; ++g) gm[4 * h + g] = max16(&sv[16 * g]);
+        }
+        const float t = max3f(max3f(gm[0], gm[1], gm[2]), max3f(gm[3], gm[4], gm[5]),
+                              fmaxf(gm[6], gm[7]));
+        const float nb = -t * a;
+        // level 2 scale of each group from its maximum: E4M3(2688 e^(c(g - t)) / 6);
+        // the code of element j is E2M1(2688 e^(c(S_j - t)) / scale), computed
+        // as exp2(a S_j + bias_g); a group whose scale is 0 keeps bias nb so
+        // that its (vanishing) probabilities still enter the row sum exactly
+        float bias[8], lsc[8];
+        uint32_t sfw0 = 0u, sfw1 = 0u;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const float eg = ex2_approx(fmaf(gm[g], a, nb));
+          const uint32_t sbyte = cvt_e4m3(448.0f * eg);
+          const float sd = e4m3_to_f32(sbyte);
+          const bool pos = sd > 0.0f;
+          bias[g] = pos ? nb + (kLog2of2688 - lg2_approx(sd)) : nb;
+          lsc[g] = pos ? sd * (1.0f / 2688.0f) : 1.0f;
+          if (g < 4)
+            sfw0 |= sbyte << (8 * g);
+          else
+            sfw1 |= sbyte << (8 * (g - 4));
+        }
+        if (k >= 2 && !waitw(bar(B_PEMPTY + ps), ((k >> 1) - 1) & 1, ctl)) break;
+        uint8_t* prow = sm + L::oP + ps * L::PBYTES + r * 64;
+        const int sw = (r >> 1) & 3;  // 64-byte swizzle: 16-byte chunk c lives at c ^ ((r/2) % 4)
+        float lsum = 0.0f;
+        // pass 2: exponentials, row sum and codes, 32 keys at a time
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sv[32];
+          tmem_ld32(tb + 32 * c, sv);
+          tmem_wait_ld();
+          if (lim < kTileKV) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (32 * c + j >= lim) sv[j] = __float_as_uint(-INFINITY);
+          }
+          uint32_t w[4];
+#pragma unroll
+          for (int gg = 0; gg < 2; ++gg) {
+            const int g = 2 * c + gg;
+            const uint64_t bb = pack2(bias[g], bias[g]);
+            float y[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint64_t x = fma2(
+                  pack2(__uint_as_float(sv[16 * gg + 2 * i]), __uint_as_float(sv[16 * gg + 2 * i + 1])),
+                  a2, bb);
+              y[2 * i] = ex2_approx(lo2(x));
+              y[2 * i + 1] = ex2_approx(hi2(x));
+            }
+            uint64_t q4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              q4[i] = add2(pack2(y[4 * i], y[4 * i + 1]), pack2(y[4 * i + 2], y[4 * i + 3]));
+            const uint64_t q2 = add2(add2(q4[0], q4[1]), add2(q4[2], q4[3]));
+            lsum = fmaf(lo2(q2) + hi2(q2), lsc[g], lsum);
+            float y8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y8[i] = y[i];
+            w[2 * gg] = cvt_e2m1x8(y8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y8[i] = y[8 + i];
+            w[2 * gg + 1] = cvt_e2m1x8(y8);
+          }
+          *reinterpret_cast<uint4*>(prow + ((c ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        uint8_t* sfp = sm + L::oSFP + ps * L::SFPB + (r % 32) * 16 + (r / 32) * 4;
+        *reinterpret_cast<uint32_t*>(sfp) = sfw0;
+        *reinterpret_cast<uint32_t*>(sfp + 512) = sfw1;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(B_PFULL + ps));
+        if (k >= 2 && !waitw(bar(B_STEMPTY + ps), ((k >> 1) - 1) & 1, ctl)) break;
+        reinterpret_cast<float2*>(sm + L::oStat + ps * 1024)[r] = make_float2(t, lsum);
+        mbar_arrive(bar(B_STFULL + ps));
+      }
+    }
+    tc_fence_before();
+    cta_bar_sync();
+  } else {
+    // -------------------------------------------------------- correction + epilogue
+    regs_inc<kRegsCorr>();
+    if (!skip) {
+      const int r = threadIdx.x - 384;
+      const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+      const float a = p.a;
+      uint64_t o2[D / 2];  // O row, two FP32 columns per register pair
+#pragma unroll
+      for (int d = 0; d < D / 2; ++d) o2[d] = 0ull;
+      float m = -INFINITY, l = 0.0f;
+      bool ok = true;
+      for (int k = 0; k < nkv; ++k) {
+        const int b = k % kNumBuf, ps = k & 1;
+        if (!(ok = waitw(bar(B_STFULL + ps), (k >> 1) & 1, ctl))) break;
+        const float2 st = reinterpret_cast<const float2*>(sm + L::oStat + ps * 1024)[r];
+        mbar_arrive(bar(B_STEMPTY + ps));
+        const float mn = fmaxf(m, st.x);
+        const float alpha = ex2_approx((m - mn) * a);
+        const float beta = ex2_approx((st.x - mn) * a);
+        l = l * alpha + st.y * beta;
+        const float w = beta * (1.0f / 2688.0f);
+        m = mn;
+        const bool keep = __all_sync(kFull, alpha == 1.0f);  // no row of the warp moved its max
+        if (!(ok = waitw(bar(B_PVFULL + b), (k / kNumBuf) & 1, ctl))) break;
+        tc_fence_after();
+        const uint64_t w2 = pack2(w, w), al2 = pack2(alpha, alpha);
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t v[16];
+          tmem_ld16(tmem + b * 128 + c * 16 + lane_base, v);
+          tmem_wait_ld();
+          if (keep) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o2[c * 8 + i] = fma2(pack2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                   w2, o2[c * 8 + i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o2[c * 8 + i] = fma2(pack2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                   w2, mul2(o2[c * 8 + i], al2));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(bar(B_BUFFREE + b));
+      }
+      const int gi = qt * kTileQ + r;
+      if (ok && gi < p.N) {
+        const float inv = 1.0f / l;
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
+                                               (static_cast<size_t>(bh) * p.N + gi) * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(lo2(o2[c * 4 + i]) * inv, hi2(o2[c * 4 + i]) * inv);
+            w4[i] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          orow[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+    }
+    tc_fence_before();
+    cta_bar_sync();
   }
 }
 
@@ -450,9 +529,15 @@ cudaError_t launch_attn_d(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 32 || !(configured_mask & (1 << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Smem<D>::kAlloc);
+    // The warpgroups' setmaxnreg budgets add up to exactly 128 registers per
+    // thread at launch; with any other launch allocation the increases would
+    // never be granted, so refuse to launch.
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, attn_fwd_kernel<D>);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs != 65536 / kThreads) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Smem<D>::kAlloc);
     if (e != cudaSuccess) return e;
     if (dev < 32) configured_mask |= (1 << dev);
   }

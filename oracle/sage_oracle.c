@@ -233,8 +233,8 @@ static void init_tables(void) {
  *            (l is built from the unquantized probabilities)
  *   level 1 (TILE):    P2_j = 2688 * exp((S_j - t)/sqrt(D)),  sP1 = exp((t - m_new)/sqrt(D)) / 2688
  *           (RUNNING): P2_j = 2688 * exp((S_j - m_new)/sqrt(D)), sP1 = 1/2688
- *            -- "per token, normalise each token's range to [0, 448*6]"
- *            ([NEWS-OBST], solution 2); P2_j is rounded to float.
+ *            -- the per-token first level that brings each token's values
+ *            into [0, 448*6] ([NEWS-OBST], solution 2); P2_j is rounded to float.
  *   level 2: the 1x16 group quantizer on P2 along keys (16 consecutive
  *            elements of a row, [NEWS-HW])
  *   acc    = acc * exp((m_old - m_new)/sqrt(D)) + sP1 * sum_j dec(P2_j) * dec(V_j)
