@@ -140,7 +140,8 @@ int sage_fp4_quantize_qkv(const void* q, const void* k, const void* v, const sag
                           int B, int H, int N, int D, void* stream) {
   if (!dims_ok(B, H, N, D) || !out) return SAGE_FP4_EINVAL;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return SAGE_FP4_EINVAL;
-  if (!tensor_ok(out->q) || !tensor_ok(out->k) || !tensor_ok(out->vt)) return SAGE_FP4_EINVAL;
+  if (!tensor_ok(out->q) || !tensor_ok(out->k) || !tensor_ok(out->vt) || !aligned(out->status, 4))
+    return SAGE_FP4_EINVAL;
   if (is_empty(B, H, N)) return SAGE_FP4_OK;
   int dev = check_device();
   if (dev != SAGE_FP4_OK) return dev;
@@ -149,7 +150,7 @@ int sage_fp4_quantize_qkv(const void* q, const void* k, const void* v, const sag
   cudaError_t e = launch_quant_rows(q, k, out->q.codes, out->q.scales, out->k.codes, out->k.scales,
                                     BH, N, D, st);
   if (e != cudaSuccess) return SAGE_FP4_ECUDA;
-  return from_cuda(launch_quant_v(v, out->vt.codes, out->vt.scales, BH, N, D, st));
+  return from_cuda(launch_quant_v(v, out->vt.codes, out->vt.scales, BH, N, D, out->status, st));
 }
 
 int sage_fp4_attn_fwd(const sage_fp4_qkv* qkv, void* o, int B, int H, int N, int D, int causal,

@@ -11,7 +11,7 @@ namespace sagefp4 {
 cudaError_t launch_quant_rows(const void* q, const void* k, uint8_t* qc, uint8_t* qs, uint8_t* kc,
                               uint8_t* ks, int BH, int N, int D, cudaStream_t st);
 cudaError_t launch_quant_v(const void* v, uint8_t* vc, uint8_t* vs, int BH, int N, int D,
-                           cudaStream_t st);
+                           int32_t* status, cudaStream_t st);
 
 struct AttnParams {
   const uint8_t* sfq;  // Q scales (block layout), per (b,h) N_pad*D/16 bytes

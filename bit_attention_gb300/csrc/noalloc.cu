@@ -139,7 +139,7 @@ extern "C" int sage_fp4_attention_noalloc(const void* q, const void* k, const vo
   // the quantize kernels, so nothing left by an earlier call is read.
   if (launch_quant_rows(q, k, base + pt.qc, base + pt.qs, base + pt.kc, base + pt.ks, BH, N, D,
                         st) != cudaSuccess ||
-      launch_quant_v(v, base + pt.vc, base + pt.vs, BH, N, D, st) != cudaSuccess)
+      launch_quant_v(v, base + pt.vc, base + pt.vs, BH, N, D, status, st) != cudaSuccess)
     return SAGE_FP4_ECUDA;
   CUtensorMap tq, tk, tv;
   const CUtensorMapSwizzle qk_swz = (D == 128) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;

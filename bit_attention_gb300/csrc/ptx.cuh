@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace sagefp4 {
@@ -239,6 +240,22 @@ __device__ __forceinline__ uint32_t cvt_e4m3(float x) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
   return r & 0xFFu;
+}
+
+// E4M3 bytes of (lo, hi) in one 16-bit value: lo -> bits 0-7, hi -> bits 8-15.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Values of the two E4M3 bytes of a 16-bit value (exact).
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t b2, float& lo, float& hi) {
+  uint32_t h2;
+  uint16_t in = static_cast<uint16_t>(b2 & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+  hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
 }
 
 // Value of an E4M3 byte (exact: every E4M3 value is an f16 value).

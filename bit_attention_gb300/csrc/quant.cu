@@ -7,7 +7,10 @@
 // inference acceleration and hardware implementation/optimisation").
 //
 // Both kernels are HBM-bound streams: 2 bytes read and 0.5625 bytes written
-// per element.
+// per element.  The per-group arithmetic is kept short: amax/6 is one
+// multiply with an FMA residual correction (equal to the correctly rounded
+// quotient for every bf16 amax), and 1/scale comes from a 256-entry table of
+// correctly rounded reciprocals of the E4M3 values.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -30,27 +33,53 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& w, float (&v)[8]) {
   }
 }
 
-// The rule of sage_fp4.h for one group, given its amax: returns the E4M3 byte
-// and the reciprocal of the decoded scale (0 when the scale is 0).
-__device__ __forceinline__ uint32_t group_scale(float amax, float& r) {
-  const float q = __fdiv_rn(amax, 6.0f);
-  const uint32_t sb = cvt_e4m3(q);
-  const float s = e4m3_to_f32(sb);
-  r = (s != 0.0f) ? __frcp_rn(s) : 0.0f;
-  return sb;
+// Round-to-nearest amax / 6 for amax a bf16 magnitude: q0 = amax * RN(1/6),
+// then one FMA-computed residual step.  Checked against correctly rounded
+// division for all 32640 non-negative finite bf16 values.
+__device__ __forceinline__ float div6(float amax) {
+  const float y = 0.16666667163372040f;  // RN(1/6)
+  const float q0 = __fmul_rn(amax, y);
+  const float r = __fmaf_rn(-6.0f, q0, amax);
+  return __fmaf_rn(r, y, q0);
+}
+
+// rtab[b] = RN(1 / value(E4M3 byte b)) for positive finite b, 0 otherwise.
+__device__ __forceinline__ void fill_rtab(float* rtab) {
+  for (int b = threadIdx.x; b < 256; b += blockDim.x) {
+    const float s = e4m3_to_f32(static_cast<uint32_t>(b));
+    rtab[b] = (b > 0 && b < 0x7F) ? __frcp_rn(s) : 0.0f;
+  }
 }
 
 __device__ __forceinline__ uint32_t encode8(const float (&v)[8], float r) {
-  if (r == 0.0f) return 0u;
   float y[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(v[i], r);
   return cvt_e2m1x8(y);
 }
 
+// Lane-wise max(|a|, |b|) of two packed bf16 pairs; the sign bit of each
+// result is the XOR of the operands' signs and is discarded by the caller.
+// Exact for finite inputs.
+__device__ __forceinline__ uint32_t maxabs_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Bytes b0..b3 (each in bits 0-7 of its argument) packed into one word.
+__device__ __forceinline__ uint32_t pack4_bytes(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+}
+
 // Q and K.  A row of D bf16 is D/8 lanes x 16 bytes; the two lanes holding one
-// 16-element group combine their absmax with one shuffle.  Each warp keeps U
-// row-steps of loads in flight.  blockIdx.y selects Q (0) or K (1).
+// 16-element group combine their absmax with one shuffle.  A warp handles a
+// chunk of 8 row-steps (16 rows for D = 128, 32 for D = 64) of one (b,h);
+// chunks never straddle two heads because N_pad is a multiple of 128, and lie
+// inside one 32-row slice of the scale block layout, so a lane's scale address
+// moves by a constant from one row-step to the next.  The warp keeps all its
+// row-steps' loads in flight before it computes.  blockIdx.y selects Q (0) or
+// K (1).
 template <int D>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ x0,
                                                          const uint4* __restrict__ x1,
@@ -59,134 +88,202 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
                                                          uint8_t* __restrict__ c1,
                                                          uint8_t* __restrict__ s1, int BH, int N,
                                                          int Np) {
-  constexpr int LPR = D / 8;     // lanes per row
-  constexpr int RPW = 32 / LPR;  // rows per warp step
-  constexpr int U = 4;
+  constexpr int LPR = D / 8;      // lanes per row
+  constexpr int RPW = 32 / LPR;   // rows per warp step
+  constexpr int U = 8;            // row-steps per chunk
+  constexpr int CHUNK = U * RPW;  // rows per warp chunk
+  static_assert(32 % CHUNK == 0, "a chunk must sit inside one 32-row slice");
+  __shared__ float rtab[256];
+  fill_rtab(rtab);
+  __syncthreads();
   const uint4* __restrict__ x = blockIdx.y ? x1 : x0;
   uint8_t* __restrict__ codes = blockIdx.y ? c1 : c0;
   uint8_t* __restrict__ scales = blockIdx.y ? s1 : s0;
   const int lane = threadIdx.x & 31;
   const int sub = lane % LPR;
   const int rsub = lane / LPR;
-  const long long total = static_cast<long long>(BH) * Np / RPW;
-  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
-  const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-
-  for (long long step0 = w0 * U; step0 < total; step0 += nwarps * U) {
+  const int chunks_per_head = Np / CHUNK;
+  const int total = BH * chunks_per_head;  // BH * Np <= INT_MAX is checked on the host
+  const int nwarps = static_cast<int>((gridDim.x * blockDim.x) >> 5);
+  for (int chunk = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5); chunk < total;
+       chunk += nwarps) {
+    const int bh = chunk / chunks_per_head;
+    const int r0 = (chunk - bh * chunks_per_head) * CHUNK;
+    const int n0 = r0 + rsub;
+    const uint4* __restrict__ src = x + (static_cast<size_t>(bh) * N + n0) * (D / 8) + sub;
     uint4 raw[U];
+    if (r0 + CHUNK <= N) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const long long row = (step0 + u) * RPW + rsub;
-      const int bh = static_cast<int>(row / Np), n = static_cast<int>(row % Np);
-      raw[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (step0 + u < total && n < N)
-        raw[u] = __ldcs(x + (static_cast<size_t>(bh) * N + n) * (D / 8) + sub);
+      for (int u = 0; u < U; ++u) raw[u] = __ldcs(src + u * RPW * (D / 8));
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        raw[u] = (n0 + u * RPW < N) ? __ldcs(src + u * RPW * (D / 8)) : make_uint4(0u, 0u, 0u, 0u);
     }
+    uint8_t* __restrict__ cdst = codes + (static_cast<size_t>(bh) * Np + n0) * (D / 2) + sub * 4;
+    uint8_t* __restrict__ sdst =
+        scales + static_cast<size_t>(bh) * Np * (D / 16) + sf_offset(n0, sub / 2, D / 16);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      if (step0 + u >= total) break;  // uniform across the warp
-      const long long row = (step0 + u) * RPW + rsub;
-      const int bh = static_cast<int>(row / Np), n = static_cast<int>(row % Np);
+      const uint4 w = raw[u];
+      uint32_t m = maxabs_bf16x2(maxabs_bf16x2(w.x, w.y), maxabs_bf16x2(w.z, w.w));
+      m = maxabs_bf16x2(m, __shfl_xor_sync(kFull, m, 1));
+      const float amax = fmaxf(fabsf(__uint_as_float(m << 16)), fabsf(__uint_as_float(m & 0xFFFF0000u)));
+      const uint32_t sb = cvt_e4m3(div6(amax));
+      const float r = rtab[sb];
       float v[8];
-      bf16x8_to_f32(raw[u], v);
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-      float r;
-      const uint32_t sb = group_scale(amax, r);
-      const uint32_t word = encode8(v, r);
-      *reinterpret_cast<uint32_t*>(codes + (static_cast<size_t>(bh) * Np + n) * (D / 2) +
-                                   sub * 4) = word;
+      bf16x8_to_f32(w, v);
+      const uint32_t word = (r != 0.0f) ? encode8(v, r) : 0u;
+      *reinterpret_cast<uint32_t*>(cdst + u * RPW * (D / 2)) = word;
       // four consecutive groups' scales form one 32-bit word of the block layout
-      const uint32_t w = sb | (__shfl_down_sync(kFull, sb, 2) << 8) |
-                         (__shfl_down_sync(kFull, sb, 4) << 16) |
-                         (__shfl_down_sync(kFull, sb, 6) << 24);
-      if ((sub & 7) == 0) {
-        const int g = sub / 2;
-        *reinterpret_cast<uint32_t*>(scales + static_cast<size_t>(bh) * Np * (D / 16) +
-                                     sf_offset(n, g, D / 16)) = w;
-      }
+      const uint32_t sw = pack4_bytes(sb, __shfl_down_sync(kFull, sb, 2), __shfl_down_sync(kFull, sb, 4),
+                                      __shfl_down_sync(kFull, sb, 6));
+      if ((sub & 7) == 0) *reinterpret_cast<uint32_t*>(sdst + u * RPW * 16) = sw;
     }
   }
 }
 
-// V.  One block stages 128 tokens x D channels in shared memory, then each
-// thread quantizes a channel pair over 64 tokens (4 groups along tokens) and
-// writes 32 contiguous code bytes per channel row of V^T plus one scale word.
-template <int D>
-__global__ void __launch_bounds__(128) quant_v_kernel(const uint4* __restrict__ v,
+// V.  Each block walks TT-token tiles of V (tile i of this block = blockIdx.x
+// + i * gridDim.x over (b,h) x tiles).  A tile is brought into shared memory
+// with one 1-D bulk copy into an NS-deep ring, so that the next NS-1 tiles
+// load while this one is quantized.  A work item is one channel pair over 32
+// tokens (two groups along tokens): it writes 16 code bytes to each of two
+// V^T rows and one 16-bit half of a scale word per row.
+template <int D, int TT, int NS>
+__global__ void __launch_bounds__(128) quant_v_kernel(const uint8_t* __restrict__ v,
                                                       uint8_t* __restrict__ vc,
-                                                      uint8_t* __restrict__ vs, int N, int Np) {
-  __shared__ __align__(16) uint32_t tile[128 * (D / 2)];  // [token][channel pair] bf16x2
-  const int ntiles = Np / 128;
-  const int tb = static_cast<int>(blockIdx.x % ntiles);
-  const int bh = static_cast<int>(blockIdx.x / ntiles);
-  const int tid = threadIdx.x;
-  constexpr int CH = D / 8;  // 16-byte chunks per token row
-  for (int i = tid; i < 128 * CH; i += 128) {
-    const int t = i / CH, c = i % CH;
-    const int n = tb * 128 + t;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (n < N) val = __ldcs(v + (static_cast<size_t>(bh) * N + n) * CH + c);
-    *reinterpret_cast<uint4*>(&tile[t * (D / 2) + c * 4]) = val;
+                                                      uint8_t* __restrict__ vs, int BH, int N,
+                                                      int Np, int32_t* status) {
+  static_assert(TT == 64 || TT == 128, "tile of 64 or 128 tokens");
+  constexpr int TILE_BYTES = TT * D * 2;
+  constexpr int ITEMS = (D / 2) * (TT / 32);
+  extern __shared__ __align__(128) uint8_t qv_smem[];
+  uint32_t* tiles = reinterpret_cast<uint32_t*>(qv_smem);  // NS x [TT tokens][D/2 pairs]
+  __shared__ float rtab[256];
+  __shared__ __align__(8) uint64_t bars[NS];
+  fill_rtab(rtab);
+  const int ntiles = Np / TT;
+  const long long work = static_cast<long long>(BH) * ntiles;
+  const uint32_t bar0 = smem_addr(&bars[0]);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(bar0 + 8 * i, 1);
+    mbar_fence_init();
   }
   __syncthreads();
 
-  const size_t vt_row = static_cast<size_t>(Np) / 2;
-  uint8_t* __restrict__ vs_bh = vs + static_cast<size_t>(bh) * 8 * Np;
-  for (int it = tid; it < D; it += 128) {
-    const int pch = it % (D / 2);  // channel pair
-    const int h = it / (D / 2);    // 64-token half of the tile
-    uint32_t clo[8], chi[8];
-    uint32_t slo = 0, shi = 0;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      float lo[16], hi[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint32_t w = tile[(h * 64 + g * 16 + j) * (D / 2) + pch];
-        lo[j] = __uint_as_float(w << 16);
-        hi[j] = __uint_as_float(w & 0xFFFF0000u);
-      }
-      float alo = 0.0f, ahi = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        alo = fmaxf(alo, fabsf(lo[j]));
-        ahi = fmaxf(ahi, fabsf(hi[j]));
-      }
-      float rlo, rhi;
-      slo |= group_scale(alo, rlo) << (8 * g);
-      shi |= group_scale(ahi, rhi) << (8 * g);
-      float t8[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) t8[j] = lo[j];
-      clo[2 * g] = encode8(t8, rlo);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) t8[j] = lo[8 + j];
-      clo[2 * g + 1] = encode8(t8, rlo);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) t8[j] = hi[j];
-      chi[2 * g] = encode8(t8, rhi);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) t8[j] = hi[8 + j];
-      chi[2 * g + 1] = encode8(t8, rhi);
+  // Token rows of tile w that hold data (those past N are not read; they are
+  // zeroed).  With TT = 64 a tile can lie wholly in the padding.
+  auto tile_rows = [&](long long w) -> int {
+    const int tb = static_cast<int>(w % ntiles);
+    return max(0, min(TT, N - tb * TT));
+  };
+  auto issue = [&](long long w, int buf) {
+    const int bh = static_cast<int>(w / ntiles), tb = static_cast<int>(w % ntiles);
+    const uint32_t bytes = static_cast<uint32_t>(tile_rows(w)) * D * 2;
+    mbar_arrive_expect_tx(bar0 + 8 * buf, bytes);
+    if (bytes)
+      bulk_load(smem_addr(qv_smem + buf * TILE_BYTES),
+                v + (static_cast<size_t>(bh) * N + static_cast<size_t>(tb) * TT) * D * 2, bytes,
+                bar0 + 8 * buf);
+  };
+  if (threadIdx.x == 0)
+    for (int s = 0; s < NS - 1; ++s) {
+      const long long ws = blockIdx.x + static_cast<long long>(s) * gridDim.x;
+      if (ws < work) issue(ws, s);
     }
-    const int d0 = 2 * pch, d1 = 2 * pch + 1;
-    uint8_t* row0 = vc + (static_cast<size_t>(bh) * D + d0) * vt_row + tb * 64 + h * 32;
-    uint8_t* row1 = vc + (static_cast<size_t>(bh) * D + d1) * vt_row + tb * 64 + h * 32;
-    reinterpret_cast<uint4*>(row0)[0] = make_uint4(clo[0], clo[1], clo[2], clo[3]);
-    reinterpret_cast<uint4*>(row0)[1] = make_uint4(clo[4], clo[5], clo[6], clo[7]);
-    reinterpret_cast<uint4*>(row1)[0] = make_uint4(chi[0], chi[1], chi[2], chi[3]);
-    reinterpret_cast<uint4*>(row1)[1] = make_uint4(chi[4], chi[5], chi[6], chi[7]);
-    const int g0 = tb * 8 + h * 4;
-    *reinterpret_cast<uint32_t*>(vs_bh + sf_offset(d0, g0, Np / 16)) = slo;
-    *reinterpret_cast<uint32_t*>(vs_bh + sf_offset(d1, g0, Np / 16)) = shi;
-  }
-  // scale rows of the padding channels D..127 of the 128-row block are zero
-  for (int it = tid; it < (128 - D) * 2; it += 128) {
-    const int d = D + it / 2, h = it % 2;
-    *reinterpret_cast<uint32_t*>(vs_bh + sf_offset(d, tb * 8 + h * 4, Np / 16)) = 0u;
+  const size_t vt_row = static_cast<size_t>(Np) / 2;
+  long long w = blockIdx.x;
+  for (int it = 0; w < work; ++it, w += gridDim.x) {
+    const int buf = it % NS;
+    // refill the slot that the last iteration released at its closing barrier
+    const long long wn = w + static_cast<long long>(NS - 1) * gridDim.x;
+    if (threadIdx.x == 0 && wn < work) issue(wn, (it + NS - 1) % NS);
+    // wait for this tile (bounded: a copy that never lands sets the status)
+    {
+      const uint64_t t0 = globaltimer_ns();
+      bool ok = true;
+      while (!mbar_try_wait(bar0 + 8 * buf, (it / NS) & 1)) {
+        if (globaltimer_ns() - t0 > 1500000000ull) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) {
+        if (threadIdx.x == 0) {
+          atomicCAS(status, 0, -3);  // SAGE_FP4_ETIMEOUT
+          // let the copies already issued into the other slots land before exiting
+          const uint64_t t1 = globaltimer_ns();
+          for (int s = 1; s < NS; ++s) {
+            const long long ws = w + static_cast<long long>(s) * gridDim.x;
+            if (ws >= work) break;
+            const int j = it + s;
+            while (!mbar_try_wait(bar0 + 8 * (j % NS), (j / NS) & 1) &&
+                   globaltimer_ns() - t1 < 1500000000ull) {
+            }
+          }
+        }
+        return;
+      }
+    }
+    const int bh = static_cast<int>(w / ntiles), tb = static_cast<int>(w % ntiles);
+    uint32_t* tile = tiles + buf * (TILE_BYTES / 4);
+    const int rows = tile_rows(w);
+    for (int i = rows * (D / 2) + threadIdx.x; i < TT * (D / 2); i += 128) tile[i] = 0u;
+    __syncthreads();
+
+    uint8_t* __restrict__ vs_bh = vs + static_cast<size_t>(bh) * 8 * Np;
+    for (int item = threadIdx.x; item < ITEMS; item += 128) {
+      const int pch = item % (D / 2);  // channel pair
+      const int seg = item / (D / 2);  // 32-token segment of the tile
+      uint32_t clo[4], chi[4];
+      uint32_t sbl[2], sbh[2];
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        float lo[16], hi[16];
+        uint32_t m = 0u;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t wv = tile[(seg * 32 + g * 16 + j) * (D / 2) + pch];
+          m = maxabs_bf16x2(m, wv);  // both channels' running absmax at once
+          lo[j] = __uint_as_float(wv << 16);
+          hi[j] = __uint_as_float(wv & 0xFFFF0000u);
+        }
+        const float alo = fabsf(__uint_as_float(m << 16));
+        const float ahi = fabsf(__uint_as_float(m & 0xFFFF0000u));
+        sbl[g] = cvt_e4m3(div6(alo));
+        sbh[g] = cvt_e4m3(div6(ahi));
+        const float rlo = rtab[sbl[g]], rhi = rtab[sbh[g]];
+        float t8[8];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) t8[j] = lo[8 * q + j];
+          clo[2 * g + q] = (rlo != 0.0f) ? encode8(t8, rlo) : 0u;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) t8[j] = hi[8 * q + j];
+          chi[2 * g + q] = (rhi != 0.0f) ? encode8(t8, rhi) : 0u;
+        }
+      }
+      const int d0 = 2 * pch, d1 = 2 * pch + 1;
+      const size_t col = static_cast<size_t>(tb) * (TT / 2) + seg * 16;
+      *reinterpret_cast<uint4*>(vc + (static_cast<size_t>(bh) * D + d0) * vt_row + col) =
+          make_uint4(clo[0], clo[1], clo[2], clo[3]);
+      *reinterpret_cast<uint4*>(vc + (static_cast<size_t>(bh) * D + d1) * vt_row + col) =
+          make_uint4(chi[0], chi[1], chi[2], chi[3]);
+      const int g0 = tb * (TT / 16) + seg * 2;  // even: the two groups share a 16-bit half
+      *reinterpret_cast<uint16_t*>(vs_bh + sf_offset(d0, g0, Np / 16)) =
+          static_cast<uint16_t>(sbl[0] | (sbl[1] << 8));
+      *reinterpret_cast<uint16_t*>(vs_bh + sf_offset(d1, g0, Np / 16)) =
+          static_cast<uint16_t>(sbh[0] | (sbh[1] << 8));
+    }
+    // scale rows of the padding channels D..127 of the 128-row block are zero
+    for (int i = threadIdx.x; i < (128 - D) * (TT / 64); i += 128) {
+      const int d = D + i / (TT / 64), h = i % (TT / 64);
+      *reinterpret_cast<uint32_t*>(vs_bh + sf_offset(d, tb * (TT / 16) + h * 4, Np / 16)) = 0u;
+    }
+    // this slot is refilled by a bulk copy (async proxy) after the barrier
+    fence_proxy_async_smem();
+    __syncthreads();
   }
 }
 
@@ -202,9 +299,8 @@ int num_sms() {
 cudaError_t launch_quant_rows(const void* q, const void* k, uint8_t* qc, uint8_t* qs, uint8_t* kc,
                               uint8_t* ks, int BH, int N, int D, cudaStream_t st) {
   const int Np = round_up_int(N, 128);
-  const long long rows = static_cast<long long>(BH) * Np;
-  const long long warps_needed = (rows * D / 256 + 3) / 4;  // a warp covers 256 elements per step, 4 steps
-  long long blocks = (warps_needed + 7) / 8;
+  const long long chunks = static_cast<long long>(BH) * Np / (D == 128 ? 16 : 32);  // one warp each
+  long long blocks = (chunks + 7) / 8;
   const long long cap = static_cast<long long>(num_sms()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
@@ -220,16 +316,32 @@ cudaError_t launch_quant_rows(const void* q, const void* k, uint8_t* qc, uint8_t
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_v(const void* v, uint8_t* vc, uint8_t* vs, int BH, int N, int D,
-                           cudaStream_t st) {
-  const int Np = round_up_int(N, 128);
-  const long long blocks = static_cast<long long>(Np / 128) * BH;
-  const unsigned grid = static_cast<unsigned>(blocks);
-  if (D == 128)
-    quant_v_kernel<128><<<grid, 128, 0, st>>>(static_cast<const uint4*>(v), vc, vs, N, Np);
-  else
-    quant_v_kernel<64><<<grid, 128, 0, st>>>(static_cast<const uint4*>(v), vc, vs, N, Np);
+template <int D, int TT, int NS>
+cudaError_t launch_quant_v_cfg(const void* v, uint8_t* vc, uint8_t* vs, int BH, int Np, int N,
+                               int32_t* status, int blocks_per_sm, cudaStream_t st) {
+  const long long work = static_cast<long long>(Np / TT) * BH;
+  const int smem = NS * TT * D * 2;
+  long long blocks = static_cast<long long>(num_sms()) * blocks_per_sm;
+  if (blocks > work) blocks = work;
+  if (blocks < 1) blocks = 1;
+  const cudaError_t e =
+      cudaFuncSetAttribute(quant_v_kernel<D, TT, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  quant_v_kernel<D, TT, NS><<<static_cast<unsigned>(blocks), 128, smem, st>>>(
+      static_cast<const uint8_t*>(v), vc, vs, BH, N, Np, status);
   return cudaGetLastError();
+}
+
+cudaError_t launch_quant_v(const void* v, uint8_t* vc, uint8_t* vs, int BH, int N, int D,
+                           int32_t* status, cudaStream_t st) {
+  const int Np = round_up_int(N, 128);
+  // 64-token tiles, double-buffered: 32 KB (D = 128) or 16 KB (D = 64) of
+  // shared memory per block.  The per-tile arithmetic, not the copy latency,
+  // sets the pace, so more resident blocks beat deeper rings (measured on
+  // GB300: 5.3-5.8 TB/s at D = 128 with six blocks per SM, against 4.0-4.9 TB/s
+  // with four-deep rings and two or three blocks).
+  if (D == 128) return launch_quant_v_cfg<128, 64, 2>(v, vc, vs, BH, Np, N, status, 6, st);
+  return launch_quant_v_cfg<64, 64, 2>(v, vc, vs, BH, Np, N, status, 8, st);
 }
 
 }  // namespace sagefp4
