@@ -1,7 +1,10 @@
 // attn.cu -- fused NVFP4 attention forward for sm_103a (SageAttention3 method).
 //
-// One CTA owns one tile of 128 query rows of one (batch, head) and streams the
-// KV tiles of 128 keys.  Per KV tile:
+// A persistent CTA walks a fixed list of work items; an item is one tile of
+// 128 query rows of one (batch, head), and it streams the item's KV tiles of
+// 128 keys.  The KV tiles of all the CTA's items form one stream g = 0, 1, ...
+// that every role walks in the same order, so the next item's first tiles
+// overlap the current item's last ones.  Per KV tile:
 //   S   = (Q^ sQ)(K^ sK)^T     block-scaled FP4 tensor-core MMA into tensor memory
 //   online softmax over S fused with two-level P quantization: level 1 maps
 //       the tile's row segment onto [0, 448*6] (its maximum becomes 2688),
@@ -13,18 +16,22 @@
 //   PV  = (P^ sP)(V^ sV)        block-scaled FP4 MMA with FP32 accumulation
 //   O   = O * exp(m_old - m_new) + exp(t - m_new)/2688 * PV   (FP32)
 // Roles (warp specialisation, mbarrier pipelines, all waits bounded):
-//   warp 0       TMA / bulk-copy producer of Q, K, V^T tiles and their scales
-//   warp 1       tcgen05 MMA issuer (one thread); S runs two tiles ahead of PV
-//   warp 2       tensor-memory allocator
-//   warps 4-7    softmax + P quantization of the even KV tiles, one thread per row
-//   warps 8-11   the same for the odd KV tiles: with level 1 normalised per
+//   warp 0       bulk-copy producer of Q and K tiles and their scales
+//   warp 1       tcgen05 issuer of S = QK^T (one thread)
+//   warp 2       tensor-memory allocator, then producer of V^T tiles
+//   warp 3       tcgen05 issuer of PV (one thread)
+//   warps 4-7    softmax + P quantization of the even tiles g, one thread per row
+//   warps 8-11   the same for the odd tiles: with level 1 normalised per
 //                tile, tiles are independent until O is combined
 //   warps 12-15  correction: rescale-and-accumulate O in registers, epilogue
-// Registers are rebalanced with setmaxnreg: 64 (warps 0-3), 136 (softmax),
-// 176 (correction); 64*128 + 136*256 + 176*128 = 65536.
-// Tensor memory (512 columns x 128 lanes): three 128-column buffers that hold
-// S of a tile and, once S has been read, that tile's PV; then the scale
-// factors of Q, K, P and V.
+// Every MMA group ends in exactly one tcgen05.commit (each costs ~40 cycles
+// of issue and ~250 cycles until the barrier is seen on GB300); S and PV come
+// from two threads so that neither waits behind the other.
+// Registers are rebalanced with setmaxnreg: 48 (warps 0-3), 144 (softmax),
+// 176 (correction); 48*128 + 144*256 + 176*128 = 65536.
+// Tensor memory (512 columns x 128 lanes): three 128-column buffers; tile g
+// uses buffer g % 3 for S_g and, once the softmax has read S_g, for PV_g.
+// Then double-buffered scale factors of Q, K, V and P.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -37,37 +44,34 @@ namespace sagefp4 {
 
 namespace {
 
-constexpr int kStages = 4;   // K and V^T shared-memory ring depth
-constexpr int kNumBuf = 3;   // S/PV tensor-memory buffers
+constexpr int kStages = 6;   // K and V^T shared-memory ring depth
+constexpr int kNumBuf = 3;   // S/PV tensor-memory buffers, P and row-stat slots
 constexpr int kThreads = 512;
-constexpr uint32_t kRegsCtl = 64, kRegsSoftmax = 136, kRegsCorr = 176;
+constexpr uint32_t kRegsCtl = 48, kRegsSoftmax = 144, kRegsCorr = 176;
 static_assert(kRegsCtl * 128 + kRegsSoftmax * 256 + kRegsCorr * 128 == 65536, "register split");
 constexpr uint64_t kWaitLimitNs = 1500ull * 1000ull * 1000ull;  // a bounded wait gives up after 1.5 s
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // tensor-memory columns
-constexpr uint32_t kColSFQ = 384;  // 2 K-blocks x 4 columns
-constexpr uint32_t kColSFK = 392;  // 2 slots x 8
-constexpr uint32_t kColSFV = 408;  // 2 slots x 8
-constexpr uint32_t kColSFP = 424;  // 2 slots x 8
+constexpr uint32_t kColSFQ = 384;  // 2 item slots x 8
+constexpr uint32_t kColSFK = 400;  // 2 slots x 8
+constexpr uint32_t kColSFV = 416;  // 2 slots x 8
+constexpr uint32_t kColSFP = 432;  // 2 slots x 8
 constexpr uint32_t kTmemCols = 512;
 
-// barrier indices
+// barrier indices.  A barrier of a ring of R serves events n = i, i+R, ...;
+// the waiter for event n waits for completion number n / R (parity (n/R)&1).
 enum {
-  B_QFULL = 0,
-  B_KFULL = 1,
-  B_KEMPTY = B_KFULL + kStages,
-  B_VFULL = B_KEMPTY + kStages,
-  B_VEMPTY = B_VFULL + kStages,
-  B_SFULL = B_VEMPTY + kStages,
-  B_PVFULL = B_SFULL + kNumBuf,
-  B_BUFFREE = B_PVFULL + kNumBuf,
-  B_PFULL = B_BUFFREE + kNumBuf,
-  B_PEMPTY = B_PFULL + 2,
-  B_STFULL = B_PEMPTY + 2,
-  B_STEMPTY = B_STFULL + 2,
-  B_DRAIN = B_STEMPTY + 2,
-  kNumBars = B_DRAIN + 1
+  B_QFULL = 0,                     // Q tile of local item i landed          [2]
+  B_QEMPTY = B_QFULL + 2,          // every S of local item i completed      [2]
+  B_KFULL = B_QEMPTY + 2,          // K_g landed                             [kStages]
+  B_VFULL = B_KFULL + kStages,     // V_g landed                             [kStages]
+  B_SDONE = B_VFULL + kStages,     // S_g in tensor memory, K slot free      [kStages]
+  B_PVDONE = B_SDONE + kStages,    // PV_g in tensor memory, V and P free    [kStages]
+  B_PFULL = B_PVDONE + kStages,    // P_g, its scales and row stats written  [3]
+  B_BUFFREE = B_PFULL + kNumBuf,   // buffer g%3 read by the correction      [3]
+  B_DRAIN = B_BUFFREE + kNumBuf,   // abandoning work: MMAs of one issuer   [2]
+  kNumBars = B_DRAIN + 2
 };
 
 template <int D>
@@ -79,21 +83,24 @@ struct Smem {
   static constexpr int SFVB = 1024;            // V^T scales of one tile (2 K-blocks)
   static constexpr int PBYTES = 128 * 64;      // P code tile: 128 rows x 128 keys
   static constexpr int SFPB = 1024;
+  // swizzled tiles first (every one a multiple of 1 KB from a 1 KB-aligned base)
   static constexpr int oQ = 0;
-  static constexpr int oK = oQ + QBYTES;
+  static constexpr int oK = oQ + 2 * QBYTES;
   static constexpr int oV = oK + kStages * QBYTES;
   static constexpr int oP = oV + kStages * VBYTES;
-  static constexpr int oSFQ = oP + 2 * PBYTES;
-  static constexpr int oSFK = oSFQ + SFQK;
+  static constexpr int oSFQ = oP + kNumBuf * PBYTES;
+  static constexpr int oSFK = oSFQ + 2 * SFQK;
   static constexpr int oSFV = oSFK + kStages * SFQK;
   static constexpr int oSFP = oSFV + kStages * SFVB;
-  static constexpr int oStat = oSFP + 2 * SFPB;
-  static constexpr int oBar = oStat + 2 * 128 * 8;
+  static constexpr int oStat = oSFP + kNumBuf * SFPB;
+  static constexpr int oLut = oStat + kNumBuf * 128 * 8;  // float2 per E4M3 byte
+  static constexpr int oBar = oLut + 256 * 8;
   static constexpr int oMisc = oBar + kNumBars * 8;
   static constexpr int kBytes = oMisc + 16;
   // 1 KB slack to align the base; at least 120 KB so that one CTA owns an SM
   // (the CTA allocates all 512 tensor-memory columns)
   static constexpr int kAlloc = (kBytes + 1024 > 120 * 1024) ? kBytes + 1024 : 120 * 1024;
+  static_assert(kAlloc <= 227 * 1024, "shared memory");
 };
 
 struct Ctl {
@@ -161,6 +168,27 @@ __device__ __forceinline__ float max16(const uint32_t* s) {
   return max3f(max3f(m0, m1, m2), max3f(m3, m4, f(15)), m0);
 }
 
+// A work item: 128 query rows (tile qt) of head bh and its nkv KV tiles.
+// Causal lists start with the longest rows so that the static round-robin
+// over CTAs stays balanced.
+struct Item {
+  int bh, qt, nkv;
+};
+
+__device__ __forceinline__ Item item_at(const AttnParams& p, int it) {
+  Item r;
+  if (p.causal) {
+    r.qt = p.n_qt - 1 - it / p.BH;
+    r.bh = it % p.BH;
+    r.nkv = r.qt + 1;
+  } else {
+    r.bh = it / p.n_qt;
+    r.qt = it % p.n_qt;
+    r.nkv = p.Np / kTileKV;
+  }
+  return r;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -175,41 +203,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::oMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::oMisc + 4);
   const Ctl ctl{abort_flag, p.status};
-
-  // work unit: causal grids start with the longest rows (largest q-tile first)
-  int bh, qt;
-  if (p.causal) {
-    qt = p.n_qt - 1 - static_cast<int>(blockIdx.x / p.BH);
-    bh = static_cast<int>(blockIdx.x % p.BH);
-  } else {
-    bh = static_cast<int>(blockIdx.x / p.n_qt);
-    qt = static_cast<int>(blockIdx.x % p.n_qt);
-  }
-  const int nkv = p.causal ? qt + 1 : p.Np / kTileKV;
+  const int n_items = p.BH * p.n_qt;
+  const int item0 = static_cast<int>(blockIdx.x), istep = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(B_QFULL), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(B_QFULL + s), 1);
+      mbar_init(bar(B_QEMPTY + s), 1);
+      mbar_init(bar(B_DRAIN + s), 1);
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
-      mbar_init(bar(B_KEMPTY + s), 1);
       mbar_init(bar(B_VFULL + s), 1);
-      mbar_init(bar(B_VEMPTY + s), 1);
+      mbar_init(bar(B_SDONE + s), 1);
+      mbar_init(bar(B_PVDONE + s), 1);
     }
     for (int b = 0; b < kNumBuf; ++b) {
-      mbar_init(bar(B_SFULL + b), 1);
-      mbar_init(bar(B_PVFULL + b), 1);
+      mbar_init(bar(B_PFULL + b), 128);
       mbar_init(bar(B_BUFFREE + b), 128);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_PFULL + s), 128);
-      mbar_init(bar(B_PEMPTY + s), 1);
-      mbar_init(bar(B_STFULL + s), 128);
-      mbar_init(bar(B_STEMPTY + s), 128);
-    }
-    mbar_init(bar(B_DRAIN), 1);
     // a launch sharing this status word already gave up: do no work
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(p.status) != 0) ? 1 : 0;
     mbar_fence_init();
+  }
+  // Per E4M3 scale byte b of a P group: (log2(2688) - log2(value(b)), value(b) / 2688),
+  // and (0, 1) for b = 0, whose group keeps the row's own bias.
+  for (int b = threadIdx.x; b < 256; b += kThreads) {
+    float x = 0.0f, y = 1.0f;
+    if (b > 0 && b < 0x7F) {
+      const float v = e4m3_to_f32(static_cast<uint32_t>(b));
+      x = kLog2of2688 - log2f(v);
+      y = v * (1.0f / 2688.0f);
+    }
+    reinterpret_cast<float2*>(sm + L::oLut)[b] = make_float2(x, y);
   }
   if (warp == 2) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -225,113 +251,149 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (wg == 0) {
     regs_dec<kRegsCtl>();
     if (!skip && warp == 0 && lane == 0) {
-      // ------------------------------------------------------------ producer
+      // ---------------------------------------------------- Q and K producer
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
-      prefetch_tensormap(&tm_v);
-      const uint8_t* sfq = p.sfq + static_cast<size_t>(bh) * p.Np * (D / 16);
-      const uint8_t* sfk = p.sfk + static_cast<size_t>(bh) * p.Np * (D / 16);
-      const uint8_t* sfv = p.sfv + static_cast<size_t>(bh) * 8 * p.Np;
-      mbar_arrive_expect_tx(bar(B_QFULL), L::QBYTES + L::SFQK);
-      tma_load_2d(sb + L::oQ, &tm_q, 0, bh * p.Np + qt * kTileQ, bar(B_QFULL));
-      bulk_load(sb + L::oSFQ, sfq + static_cast<size_t>(qt) * L::SFQK, L::SFQK, bar(B_QFULL));
-      int issued_k = 0, issued_v = 0;
+      int nq = 0, nk = 0;  // copies issued
       bool ok = true;
-      for (int k = 0; k < nkv; ++k) {
-        const int s = k % kStages, u = k / kStages;
-        if (u > 0 && !(ok = wait1(bar(B_KEMPTY + s), (u - 1) & 1, ctl))) break;
-        mbar_arrive_expect_tx(bar(B_KFULL + s), L::QBYTES + L::SFQK);
-        tma_load_2d(sb + L::oK + s * L::QBYTES, &tm_k, 0, bh * p.Np + k * kTileKV, bar(B_KFULL + s));
-        bulk_load(sb + L::oSFK + s * L::SFQK, sfk + static_cast<size_t>(k) * L::SFQK, L::SFQK,
-                  bar(B_KFULL + s));
-        issued_k = k + 1;
-        if (u > 0 && !(ok = wait1(bar(B_VEMPTY + s), (u - 1) & 1, ctl))) break;
-        mbar_arrive_expect_tx(bar(B_VFULL + s), L::VBYTES + L::SFVB);
-        tma_load_2d(sb + L::oV + s * L::VBYTES, &tm_v, k * (kTileKV / 2), bh * D, bar(B_VFULL + s));
-        bulk_load(sb + L::oSFV + s * L::SFVB, sfv + static_cast<size_t>(k) * L::SFVB, L::SFVB,
-                  bar(B_VFULL + s));
-        issued_v = k + 1;
+      auto load_q = [&](int i, const Item& it) -> bool {
+        const int s = i & 1;
+        if (i >= 2 && !wait1(bar(B_QEMPTY + s), ((i >> 1) - 1) & 1, ctl)) return false;
+        mbar_arrive_expect_tx(bar(B_QFULL + s), L::QBYTES + L::SFQK);
+        tma_load_2d(sb + L::oQ + s * L::QBYTES, &tm_q, 0, it.bh * p.Np + it.qt * kTileQ, bar(B_QFULL + s));
+        bulk_load(sb + L::oSFQ + s * L::SFQK,
+                  p.sfq + static_cast<size_t>(it.bh) * p.Np * (D / 16) + static_cast<size_t>(it.qt) * L::SFQK,
+                  L::SFQK, bar(B_QFULL + s));
+        nq = i + 1;
+        return true;
+      };
+      int g = 0, i = 0;
+      if (item0 < n_items) ok = load_q(0, item_at(p, item0));
+      for (int it = item0; ok && it < n_items; it += istep, ++i) {
+        const Item I = item_at(p, it);
+        const uint8_t* sfk = p.sfk + static_cast<size_t>(I.bh) * p.Np * (D / 16);
+        for (int k = 0; k < I.nkv; ++k, ++g) {
+          const int s = g % kStages;
+          if (g >= kStages && !(ok = wait1(bar(B_SDONE + s), ((g / kStages) - 1) & 1, ctl))) break;
+          mbar_arrive_expect_tx(bar(B_KFULL + s), L::QBYTES + L::SFQK);
+          tma_load_2d(sb + L::oK + s * L::QBYTES, &tm_k, 0, I.bh * p.Np + k * kTileKV, bar(B_KFULL + s));
+          bulk_load(sb + L::oSFK + s * L::SFQK, sfk + static_cast<size_t>(k) * L::SFQK, L::SFQK,
+                    bar(B_KFULL + s));
+          nk = g + 1;
+          // the next item's Q goes out once a few of this item's tiles are
+          // queued (by then the item before this one has finished its S)
+          if (k == min(kStages - 2, I.nkv - 1) && it + istep < n_items &&
+              !(ok = load_q(i + 1, item_at(p, it + istep))))
+            break;
+        }
       }
       if (!ok) {
         // abandoning: let the copies this thread started land before the CTA exits
-        drain_wait(bar(B_QFULL), 0);
-        for (int k = (issued_k > kStages ? issued_k - kStages : 0); k < issued_k; ++k)
-          drain_wait(bar(B_KFULL + k % kStages), (k / kStages) & 1);
-        for (int k = (issued_v > kStages ? issued_v - kStages : 0); k < issued_v; ++k)
-          drain_wait(bar(B_VFULL + k % kStages), (k / kStages) & 1);
+        for (int j = (nq > 2 ? nq - 2 : 0); j < nq; ++j) drain_wait(bar(B_QFULL + (j & 1)), (j >> 1) & 1);
+        for (int j = (nk > kStages ? nk - kStages : 0); j < nk; ++j)
+          drain_wait(bar(B_KFULL + j % kStages), (j / kStages) & 1);
       }
+    } else if (!skip && warp == 2 && lane == 0) {
+      // -------------------------------------------------------- V producer
+      prefetch_tensormap(&tm_v);
+      int nv = 0;
+      bool ok = true;
+      int g = 0;
+      for (int it = item0; ok && it < n_items; it += istep) {
+        const Item I = item_at(p, it);
+        const uint8_t* sfv = p.sfv + static_cast<size_t>(I.bh) * 8 * p.Np;
+        for (int k = 0; k < I.nkv; ++k, ++g) {
+          const int s = g % kStages;
+          if (g >= kStages && !(ok = wait1(bar(B_PVDONE + s), ((g / kStages) - 1) & 1, ctl))) break;
+          mbar_arrive_expect_tx(bar(B_VFULL + s), L::VBYTES + L::SFVB);
+          tma_load_2d(sb + L::oV + s * L::VBYTES, &tm_v, k * (kTileKV / 2), I.bh * D, bar(B_VFULL + s));
+          bulk_load(sb + L::oSFV + s * L::SFVB, sfv + static_cast<size_t>(k) * L::SFVB, L::SFVB,
+                    bar(B_VFULL + s));
+          nv = g + 1;
+        }
+      }
+      if (!ok)
+        for (int j = (nv > kStages ? nv - kStages : 0); j < nv; ++j)
+          drain_wait(bar(B_VFULL + j % kStages), (j / kStages) & 1);
     } else if (!skip && warp == 1 && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
+      // ------------------------------------------------------- S issuer
       constexpr uint32_t idS = idesc_nvfp4(128, 128);
-      constexpr uint32_t idPV = idesc_nvfp4(128, D);
       constexpr uint32_t qk_swz = (D == 128) ? kSwizzle64B : kSwizzle32B;
       constexpr uint32_t qk_sbo = 8 * (D / 2);
-      bool ok = wait1(bar(B_QFULL), 0, ctl);
-      if (ok) {
-        tc_fence_after();
+      bool ok = true;
+      int g = 0, i = 0;
+      for (int it = item0; ok && it < n_items; it += istep, ++i) {
+        const Item I = item_at(p, it);
+        const int qs = i & 1;
+        if (!(ok = wait1(bar(B_QFULL + qs), (i >> 1) & 1, ctl))) break;
+        bool first = true;
+        for (int k = 0; k < I.nkv; ++k, ++g) {
+          const int s = g % kStages, b = g % kNumBuf, sl = g & 1;
+          if (!(ok = wait1(bar(B_KFULL + s), (g / kStages) & 1, ctl))) break;
+          // buffer b is free once the correction has read PV_{g-3}
+          if (g >= kNumBuf && !(ok = wait1(bar(B_BUFFREE + b), ((g / kNumBuf) - 1) & 1, ctl))) break;
+          tc_fence_after();
+          if (first) {
 #pragma unroll
-        for (int kb = 0; kb < L::KBD; ++kb)
-          tc_cp_32x128b_warpx4(tmem + kColSFQ + 4 * kb,
-                               smem_desc(sb + L::oSFQ + 512 * kb, 0, 128, kSwizzleNone));
+            for (int kb = 0; kb < L::KBD; ++kb)
+              tc_cp_32x128b_warpx4(tmem + kColSFQ + 8 * qs + 4 * kb,
+                                   smem_desc(sb + L::oSFQ + qs * L::SFQK + 512 * kb, 0, 128, kSwizzleNone));
+            first = false;
+          }
+#pragma unroll
+          for (int kb = 0; kb < L::KBD; ++kb)
+            tc_cp_32x128b_warpx4(tmem + kColSFK + 8 * sl + 4 * kb,
+                                 smem_desc(sb + L::oSFK + s * L::SFQK + 512 * kb, 0, 128, kSwizzleNone));
+#pragma unroll
+          for (int kb = 0; kb < L::KBD; ++kb) {
+            const uint64_t ad = smem_desc(sb + L::oQ + qs * L::QBYTES + 32 * kb, 16, qk_sbo, qk_swz);
+            const uint64_t bd = smem_desc(sb + L::oK + s * L::QBYTES + 32 * kb, 16, qk_sbo, qk_swz);
+            mma_nvfp4(tmem + b * 128, ad, bd, idS, tmem + kColSFQ + 8 * qs + 4 * kb,
+                      tmem + kColSFK + 8 * sl + 4 * kb, kb > 0);
+          }
+          tc_commit(bar(B_SDONE + s));
+        }
+        if (ok) tc_commit(bar(B_QEMPTY + qs));
       }
-      // S_k into buffer k % 3 (free once the correction has read PV_{k-3})
-      auto issue_s = [&](int k) -> bool {
-        const int s = k % kStages, b = k % kNumBuf, sl = k & 1;
-        if (!wait1(bar(B_KFULL + s), (k / kStages) & 1, ctl)) return false;
-        if (k >= kNumBuf && !wait1(bar(B_BUFFREE + b), ((k / kNumBuf) - 1) & 1, ctl)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kb = 0; kb < L::KBD; ++kb)
-          tc_cp_32x128b_warpx4(tmem + kColSFK + 8 * sl + 4 * kb,
-                               smem_desc(sb + L::oSFK + s * L::SFQK + 512 * kb, 0, 128, kSwizzleNone));
-#pragma unroll
-        for (int kb = 0; kb < L::KBD; ++kb) {
-          const uint64_t ad = smem_desc(sb + L::oQ + 32 * kb, 16, qk_sbo, qk_swz);
-          const uint64_t bd = smem_desc(sb + L::oK + s * L::QBYTES + 32 * kb, 16, qk_sbo, qk_swz);
-          mma_nvfp4(tmem + b * 128, ad, bd, idS, tmem + kColSFQ + 4 * kb,
-                    tmem + kColSFK + 8 * sl + 4 * kb, kb > 0);
-        }
-        tc_commit(bar(B_SFULL + b));
-        tc_commit(bar(B_KEMPTY + s));
-        return true;
-      };
-      // PV_j into the buffer that held S_j (the softmax has read it)
-      auto issue_pv = [&](int j) -> bool {
-        const int s = j % kStages, b = j % kNumBuf, ps = j & 1;
-        if (!wait1(bar(B_PFULL + ps), (j >> 1) & 1, ctl)) return false;
-        if (!wait1(bar(B_VFULL + s), (j / kStages) & 1, ctl)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-          tc_cp_32x128b_warpx4(tmem + kColSFP + 8 * ps + 4 * kb,
-                               smem_desc(sb + L::oSFP + ps * L::SFPB + 512 * kb, 0, 128, kSwizzleNone));
-          tc_cp_32x128b_warpx4(tmem + kColSFV + 8 * ps + 4 * kb,
-                               smem_desc(sb + L::oSFV + s * L::SFVB + 512 * kb, 0, 128, kSwizzleNone));
-        }
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-          const uint64_t ad = smem_desc(sb + L::oP + ps * L::PBYTES + 32 * kb, 16, 512, kSwizzle64B);
-          const uint64_t bd = smem_desc(sb + L::oV + s * L::VBYTES + 32 * kb, 16, 512, kSwizzle64B);
-          mma_nvfp4(tmem + b * 128, ad, bd, idPV, tmem + kColSFP + 8 * ps + 4 * kb,
-                    tmem + kColSFV + 8 * ps + 4 * kb, kb > 0);
-        }
-        tc_commit(bar(B_PVFULL + b));
-        tc_commit(bar(B_VEMPTY + s));
-        tc_commit(bar(B_PEMPTY + ps));
-        return true;
-      };
-      // S runs two tiles ahead of PV so that each softmax warpgroup finds its
-      // next S ready
-      if (ok) ok = issue_s(0);
-      if (ok && nkv > 1) ok = issue_s(1);
-      for (int j = 0; j < nkv && ok; ++j) {
-        ok = issue_pv(j);
-        if (ok && j + 2 < nkv) ok = issue_s(j + 2);
-      }
+      // the last item's release must land before the CTA can exit
+      if (ok && i > 0) ok = wait1(bar(B_QEMPTY + ((i - 1) & 1)), ((i - 1) >> 1) & 1, ctl);
       if (!ok) {
         // abandoning: wait for the tensor-core work this thread issued
         tc_commit(bar(B_DRAIN));
         drain_wait(bar(B_DRAIN), 0);
+      }
+    } else if (!skip && warp == 3 && lane == 0) {
+      // ------------------------------------------------------ PV issuer
+      constexpr uint32_t idPV = idesc_nvfp4(128, D);
+      bool ok = true;
+      int g = 0;
+      for (int it = item0; ok && it < n_items; it += istep) {
+        const int nkv = item_at(p, it).nkv;
+        for (int k = 0; k < nkv; ++k, ++g) {
+          const int s = g % kStages, b = g % kNumBuf, sl = g & 1;
+          if (!(ok = wait1(bar(B_PFULL + b), (g / kNumBuf) & 1, ctl))) break;
+          if (!(ok = wait1(bar(B_VFULL + s), (g / kStages) & 1, ctl))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb) {
+            tc_cp_32x128b_warpx4(tmem + kColSFP + 8 * sl + 4 * kb,
+                                 smem_desc(sb + L::oSFP + b * L::SFPB + 512 * kb, 0, 128, kSwizzleNone));
+            tc_cp_32x128b_warpx4(tmem + kColSFV + 8 * sl + 4 * kb,
+                                 smem_desc(sb + L::oSFV + s * L::SFVB + 512 * kb, 0, 128, kSwizzleNone));
+          }
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb) {
+            const uint64_t ad = smem_desc(sb + L::oP + b * L::PBYTES + 32 * kb, 16, 512, kSwizzle64B);
+            const uint64_t bd = smem_desc(sb + L::oV + s * L::VBYTES + 32 * kb, 16, 512, kSwizzle64B);
+            mma_nvfp4(tmem + b * 128, ad, bd, idPV, tmem + kColSFP + 8 * sl + 4 * kb,
+                      tmem + kColSFV + 8 * sl + 4 * kb, kb > 0);
+          }
+          tc_commit(bar(B_PVDONE + s));
+        }
+      }
+      if (!ok) {
+        tc_commit(bar(B_DRAIN + 1));
+        drain_wait(bar(B_DRAIN + 1), 0);
       }
     }
     // every role ends at the same CTA-wide barrier; then tensor memory is freed
@@ -345,110 +407,114 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- softmax + P quantization
     regs_inc<kRegsSoftmax>();
     if (!skip) {
+      const int par = wg - 1;                // this warpgroup takes the tiles g with g % 2 == par
       const int r = threadIdx.x - 128 * wg;  // query row of this thread = TMEM lane
       const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-      const int gi = qt * kTileQ + r;
-      const int vis_end = p.causal ? min(p.N, gi + 1) : p.N;  // keys j < vis_end are visible
       const float a = p.a;
       const uint64_t a2 = pack2(a, a);
-      for (int k = wg - 1; k < nkv; k += 2) {
-        const int b = k % kNumBuf, ps = k & 1;
-        if (!waitw(bar(B_SFULL + b), (k / kNumBuf) & 1, ctl)) break;
-        tc_fence_after();
-        const uint32_t tb = tmem + b * 128 + lane_base;
-        const int lim = vis_end - k * kTileKV;
-        // pass 1: the 16-element group maxima, whose maximum is the tile maximum
-        float gm[8];
+      const int sw = (r >> 1) & 3;  // 64-byte swizzle: 16-byte chunk c lives at c ^ ((r/2) % 4)
+      const float2* lut = reinterpret_cast<const float2*>(sm + L::oLut);
+      bool ok = true;
+      int g0 = 0;  // stream index of the current item's first tile
+      for (int it = item0; ok && it < n_items; it += istep) {
+        const Item I = item_at(p, it);
+        const int gi = I.qt * kTileQ + r;
+        const int vis_end = p.causal ? min(p.N, gi + 1) : p.N;  // keys j < vis_end are visible
+        for (int k = (par - g0) & 1; k < I.nkv; k += 2) {
+          const int g = g0 + k;
+          const int b = g % kNumBuf;
+          if (!(ok = waitw(bar(B_SDONE + g % kStages), (g / kStages) & 1, ctl))) break;
+          tc_fence_after();
+          const uint32_t tb = tmem + b * 128 + lane_base;
+          const int lim = vis_end - k * kTileKV;
+          // pass 1: the 16-element group maxima, whose maximum is the tile maximum
+          float gm[8];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t sv[64];
-          tmem_ld32(tb + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-          tmem_ld32(tb + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-          tmem_wait_ld();
-          if (lim < kTileKV) {
+          for (int h = 0; h < 2; ++h) {
+            uint32_t sv[64];
+            tmem_ld32(tb + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+            tmem_ld32(tb + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+            tmem_wait_ld();
+            if (lim < kTileKV) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
-              if (64 * h + j >= lim) sv[j] = __float_as_uint(-INFINITY);
-          }
-#pragma unroll
-          for (int g = 0; g < 4; ++g) gm[4 * h + g] = max16(&sv[16 * g]);
-        }
-        const float t = max3f(max3f(gm[0], gm[1], gm[2]), max3f(gm[3], gm[4], gm[5]),
-                              fmaxf(gm[6], gm[7]));
-        const float nb = -t * a;
-        // level 2 scale of each group from its maximum: E4M3(2688 e^(c(g - t)) / 6);
-        // the code of element j is E2M1(2688 e^(c(S_j - t)) / scale), computed
-        // as exp2(a S_j + bias_g); a group whose scale is 0 keeps bias nb so
-        // that its (vanishing) probabilities still enter the row sum exactly
-        float bias[8], lsc[8];
-        uint32_t sfw0 = 0u, sfw1 = 0u;
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const float eg = ex2_approx(fmaf(gm[g], a, nb));
-          const uint32_t sbyte = cvt_e4m3(448.0f * eg);
-          const float sd = e4m3_to_f32(sbyte);
-          const bool pos = sd > 0.0f;
-          bias[g] = pos ? nb + (kLog2of2688 - lg2_approx(sd)) : nb;
-          lsc[g] = pos ? sd * (1.0f / 2688.0f) : 1.0f;
-          if (g < 4)
-            sfw0 |= sbyte << (8 * g);
-          else
-            sfw1 |= sbyte << (8 * (g - 4));
-        }
-        if (k >= 2 && !waitw(bar(B_PEMPTY + ps), ((k >> 1) - 1) & 1, ctl)) break;
-        uint8_t* prow = sm + L::oP + ps * L::PBYTES + r * 64;
-        const int sw = (r >> 1) & 3;  // 64-byte swizzle: 16-byte chunk c lives at c ^ ((r/2) % 4)
-        float lsum = 0.0f;
-        // pass 2: exponentials, row sum and codes, 32 keys at a time
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sv[32];
-          tmem_ld32(tb + 32 * c, sv);
-          tmem_wait_ld();
-          if (lim < kTileKV) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (32 * c + j >= lim) sv[j] = __float_as_uint(-INFINITY);
-          }
-          uint32_t w[4];
-#pragma unroll
-          for (int gg = 0; gg < 2; ++gg) {
-            const int g = 2 * c + gg;
-            const uint64_t bb = pack2(bias[g], bias[g]);
-            float y[16];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint64_t x = fma2(
-                  pack2(__uint_as_float(sv[16 * gg + 2 * i]), __uint_as_float(sv[16 * gg + 2 * i + 1])),
-                  a2, bb);
-              y[2 * i] = ex2_approx(lo2(x));
-              y[2 * i + 1] = ex2_approx(hi2(x));
+              for (int j = 0; j < 64; ++j)
+                if (64 * h + j >= lim) sv[j] = __float_as_uint(-INFINITY);
             }
-            uint64_t q4[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              q4[i] = add2(pack2(y[4 * i], y[4 * i + 1]), pack2(y[4 * i + 2], y[4 * i + 3]));
-            const uint64_t q2 = add2(add2(q4[0], q4[1]), add2(q4[2], q4[3]));
-            lsum = fmaf(lo2(q2) + hi2(q2), lsc[g], lsum);
-            float y8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) y8[i] = y[i];
-            w[2 * gg] = cvt_e2m1x8(y8);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) y8[i] = y[8 + i];
-            w[2 * gg + 1] = cvt_e2m1x8(y8);
+            for (int q = 0; q < 4; ++q) gm[4 * h + q] = max16(&sv[16 * q]);
           }
-          *reinterpret_cast<uint4*>(prow + ((c ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+          const float t = max3f(max3f(gm[0], gm[1], gm[2]), max3f(gm[3], gm[4], gm[5]),
+                                fmaxf(gm[6], gm[7]));
+          const float nb = -t * a;
+          // level 2 scale of each group from its maximum: E4M3(2688 e^(c(g - t)) / 6);
+          // the code of element j is E2M1(2688 e^(c(S_j - t)) / scale), computed
+          // as exp2(a S_j + bias_g); a group whose scale is 0 keeps bias nb so
+          // that its (vanishing) probabilities still enter the row sum exactly
+          float bias[8], lsc[8];
+          uint32_t s2[4];  // E4M3 scale bytes of groups (2i, 2i+1)
+#pragma unroll
+          for (int q = 0; q < 8; q += 2) {
+            const float e0 = ex2_approx(fmaf(gm[q], a, nb));
+            const float e1 = ex2_approx(fmaf(gm[q + 1], a, nb));
+            s2[q / 2] = cvt_e4m3x2(448.0f * e0, 448.0f * e1);
+            const float2 t0 = lut[s2[q / 2] & 0xFFu], t1 = lut[s2[q / 2] >> 8];
+            bias[q] = nb + t0.x;
+            lsc[q] = t0.y;
+            bias[q + 1] = nb + t1.x;
+            lsc[q + 1] = t1.y;
+          }
+          // P slot b is free once PV_{g-3} has completed
+          if (g >= kNumBuf &&
+              !(ok = waitw(bar(B_PVDONE + (g - kNumBuf) % kStages), ((g - kNumBuf) / kStages) & 1, ctl)))
+            break;
+          uint8_t* prow = sm + L::oP + b * L::PBYTES + r * 64;
+          uint64_t acc[2] = {0ull, 0ull};  // row sum, two FP32x2 chains
+          // pass 2: exponentials, row sum and codes, 32 keys at a time
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t sv[32];
+            tmem_ld32(tb + 32 * c, sv);
+            tmem_wait_ld();
+            if (lim < kTileKV) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (32 * c + j >= lim) sv[j] = __float_as_uint(-INFINITY);
+            }
+            uint32_t w[4];
+#pragma unroll
+            for (int gg = 0; gg < 2; ++gg) {
+              const int q = 2 * c + gg;
+              const uint64_t bb = pack2(bias[q], bias[q]), l2 = pack2(lsc[q], lsc[q]);
+              float y[16];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const uint64_t x = fma2(
+                    pack2(__uint_as_float(sv[16 * gg + 2 * e]), __uint_as_float(sv[16 * gg + 2 * e + 1])),
+                    a2, bb);
+                y[2 * e] = ex2_approx(lo2(x));
+                y[2 * e + 1] = ex2_approx(hi2(x));
+                acc[e & 1] = fma2(pack2(y[2 * e], y[2 * e + 1]), l2, acc[e & 1]);
+              }
+              float y8[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) y8[e] = y[e];
+              w[2 * gg] = cvt_e2m1x8(y8);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) y8[e] = y[8 + e];
+              w[2 * gg + 1] = cvt_e2m1x8(y8);
+            }
+            *reinterpret_cast<uint4*>(prow + ((c ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          uint8_t* sfp = sm + L::oSFP + b * L::SFPB + (r % 32) * 16 + (r / 32) * 4;
+          *reinterpret_cast<uint32_t*>(sfp) = __byte_perm(s2[0], s2[1], 0x5410);
+          *reinterpret_cast<uint32_t*>(sfp + 512) = __byte_perm(s2[2], s2[3], 0x5410);
+          const uint64_t acc2 = add2(acc[0], acc[1]);
+          reinterpret_cast<float2*>(sm + L::oStat + b * 1024)[r] = make_float2(t, lo2(acc2) + hi2(acc2));
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(bar(B_PFULL + b));
         }
-        uint8_t* sfp = sm + L::oSFP + ps * L::SFPB + (r % 32) * 16 + (r / 32) * 4;
-        *reinterpret_cast<uint32_t*>(sfp) = sfw0;
-        *reinterpret_cast<uint32_t*>(sfp + 512) = sfw1;
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(bar(B_PFULL + ps));
-        if (k >= 2 && !waitw(bar(B_STEMPTY + ps), ((k >> 1) - 1) & 1, ctl)) break;
-        reinterpret_cast<float2*>(sm + L::oStat + ps * 1024)[r] = make_float2(t, lsum);
-        mbar_arrive(bar(B_STFULL + ps));
+        g0 += I.nkv;
       }
     }
     tc_fence_before();
@@ -460,66 +526,83 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = threadIdx.x - 384;
       const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
       const float a = p.a;
-      uint64_t o2[D / 2];  // O row, two FP32 columns per register pair
-#pragma unroll
-      for (int d = 0; d < D / 2; ++d) o2[d] = 0ull;
-      float m = -INFINITY, l = 0.0f;
       bool ok = true;
-      for (int k = 0; k < nkv; ++k) {
-        const int b = k % kNumBuf, ps = k & 1;
-        if (!(ok = waitw(bar(B_STFULL + ps), (k >> 1) & 1, ctl))) break;
-        const float2 st = reinterpret_cast<const float2*>(sm + L::oStat + ps * 1024)[r];
-        mbar_arrive(bar(B_STEMPTY + ps));
-        const float mn = fmaxf(m, st.x);
-        const float alpha = ex2_approx((m - mn) * a);
-        const float beta = ex2_approx((st.x - mn) * a);
-        l = l * alpha + st.y * beta;
-        const float w = beta * (1.0f / 2688.0f);
-        m = mn;
-        const bool keep = __all_sync(kFull, alpha == 1.0f);  // no row of the warp moved its max
-        if (!(ok = waitw(bar(B_PVFULL + b), (k / kNumBuf) & 1, ctl))) break;
-        tc_fence_after();
-        const uint64_t w2 = pack2(w, w), al2 = pack2(alpha, alpha);
+      int g = 0;
+      for (int it = item0; ok && it < n_items; it += istep) {
+        const Item I = item_at(p, it);
+        uint64_t o2[D / 2];  // O row, two FP32 columns per register pair
 #pragma unroll
-        for (int c = 0; c < D / 16; ++c) {
-          uint32_t v[16];
-          tmem_ld16(tmem + b * 128 + c * 16 + lane_base, v);
-          tmem_wait_ld();
-          if (keep) {
+        for (int d = 0; d < D / 2; ++d) o2[d] = 0ull;
+        // m is the row's reference maximum: O and l are kept relative to it.
+        // It moves only when a tile's maximum exceeds it by more than 8 / a
+        // (a factor 2^8 on O), so most tiles skip the rescale of O; the result
+        // is the same up to rounding, since O / l does not depend on m.
+        float m = -INFINITY, l = 0.0f;
+        for (int k = 0; k < I.nkv; ++k, ++g) {
+          const int b = g % kNumBuf;
+          // the row stats of tile g are written before P_g is announced
+          if (!(ok = waitw(bar(B_PFULL + b), (g / kNumBuf) & 1, ctl))) break;
+          const float2 st = reinterpret_cast<const float2*>(sm + L::oStat + b * 1024)[r];
+          const bool up = (st.x - m) * a > 8.0f;
+          const float mn = up ? st.x : m;
+          const float alpha = up ? ex2_approx((m - mn) * a) : 1.0f;
+          const float beta = ex2_approx((st.x - mn) * a);
+          l = l * alpha + st.y * beta;
+          const float w = beta * (1.0f / 2688.0f);
+          m = mn;
+          const bool keep = !__any_sync(kFull, up);  // no row of the warp moved its reference
+          if (!(ok = waitw(bar(B_PVDONE + g % kStages), (g / kStages) & 1, ctl))) break;
+          tc_fence_after();
+          const uint64_t w2 = pack2(w, w), al2 = pack2(alpha, alpha);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o2[c * 8 + i] = fma2(pack2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
-                                   w2, o2[c * 8 + i]);
-          } else {
+          for (int h = 0; h < D / 32; ++h) {
+            uint32_t v[32];
+            tmem_ld32(tmem + b * 128 + 32 * h + lane_base, v);
+            tmem_wait_ld();
+            if (keep) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o2[c * 8 + i] = fma2(pack2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
-                                   w2, mul2(o2[c * 8 + i], al2));
+              for (int e = 0; e < 16; ++e)
+                o2[16 * h + e] =
+                    fma2(pack2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), w2, o2[16 * h + e]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                o2[16 * h + e] = fma2(pack2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), w2,
+                                      mul2(o2[16 * h + e], al2));
+            }
           }
+          tc_fence_before();
+          mbar_arrive(bar(B_BUFFREE + b));
         }
-        tc_fence_before();
-        mbar_arrive(bar(B_BUFFREE + b));
-      }
-      const int gi = qt * kTileQ + r;
-      if (ok && gi < p.N) {
-        const float inv = 1.0f / l;
-        uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
-                                               (static_cast<size_t>(bh) * p.N + gi) * D);
+        const int gi = I.qt * kTileQ + r;
+        if (ok && gi < p.N) {
+          const float inv = 1.0f / l;
+          uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
+                                                 (static_cast<size_t>(I.bh) * p.N + gi) * D);
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-          uint32_t w4[4];
+          for (int c = 0; c < D / 8; ++c) {
+            uint32_t w4[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(lo2(o2[c * 4 + i]) * inv, hi2(o2[c * 4 + i]) * inv);
-            w4[i] = *reinterpret_cast<uint32_t*>(&h2);
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 h2 =
+                  __floats2bfloat162_rn(lo2(o2[c * 4 + e]) * inv, hi2(o2[c * 4 + e]) * inv);
+              w4[e] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            orow[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
-          orow[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       }
     }
     tc_fence_before();
     cta_bar_sync();
   }
+}
+
+int num_sms_attn() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms > 0 ? sms : 1;
 }
 
 template <int D>
@@ -541,7 +624,11 @@ cudaError_t launch_attn_d(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     if (e != cudaSuccess) return e;
     if (dev < 32) configured_mask |= (1 << dev);
   }
-  const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.n_qt);
+  // persistent: one CTA per SM (it owns all of the SM's tensor memory), each
+  // taking items blockIdx.x, blockIdx.x + gridDim.x, ...
+  const long long items = static_cast<long long>(p.BH) * p.n_qt;
+  const long long sms = num_sms_attn();
+  const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
   attn_fwd_kernel<D><<<grid, kThreads, Smem<D>::kAlloc, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
