@@ -30,6 +30,15 @@ METRIC = "NVFP4 attention fwd TOPS (4*B*H*N^2*D/t) on 1 GB300; % of dense FP4 pe
 FP4_OVER_BF16 = 6.0  # nominal dense FP4 / BF16 tensor rate (13.5 / 2.25 PFLOP/s)
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum of one attn_fwd_kernel launch,
+# captured with ncu on this build of the kernel (reads 113.36 MB = the
+# compulsory Q, K, V codes and scales; writes 78.93 MB of the 134.2 MB O, the
+# rest leaves L2 after the launch).  Workloads without a capture report null.
+ATTN_TRAFFIC = {
+    "attn_fwd B4 H32 N4096 D128 k-channel-outliers": 113.36e6 + 78.93e6,
+}
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -324,7 +333,9 @@ def main():
             "quant_kernels": {"ms": q_ms, "gbs": quant_bytes / (q_ms * 1e-3) / 1e9,
                               "frac_of_hbm": quant_gbs / pk["hbm_gbs"]},
             "roofline": {"bound": "tensor", "achieved": attn_tops, "peak": fp4_peak,
-                         "unit": "TFLOP/s", "frac": attn_tops / fp4_peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": attn_tops / fp4_peak,
+                         "traffic": ATTN_TRAFFIC.get(w.name),
+                         "traffic_unit": "DRAM bytes (read + write) per attention launch, from ncu",
                          "peak_src": f"{pk['src']} bf16 x {FP4_OVER_BF16:g} (nominal FP4/BF16)"},
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk.summary(),
             "gpu_launches": 3 * args.steps,

@@ -153,8 +153,10 @@ int sage_fp4_quantize_qkv(const void* q, const void* k, const void* v, const sag
   return from_cuda(launch_quant_v(v, out->vt.codes, out->vt.scales, BH, N, D, out->status, st));
 }
 
-int sage_fp4_attn_fwd(const sage_fp4_qkv* qkv, void* o, int B, int H, int N, int D, int causal,
-                      void* stream) {
+namespace {
+
+int attn_fwd_impl(const sage_fp4_qkv* qkv, void* o, int B, int H, int N, int D, int causal, int flags,
+                  uint64_t wait_ns, void* stream) {
   if (!dims_ok(B, H, N, D) || !qkv_ok(qkv) || !aligned(o, 16)) return SAGE_FP4_EINVAL;
   if (causal != 0 && causal != 1) return SAGE_FP4_EINVAL;
   if (is_empty(B, H, N)) return SAGE_FP4_OK;
@@ -181,8 +183,22 @@ int sage_fp4_attn_fwd(const sage_fp4_qkv* qkv, void* o, int B, int H, int N, int
   p.causal = causal;
   p.n_qt = Np / 128;
   p.a = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
-  p.flags = 0;
+  p.flags = flags;
+  p.wait_ns = wait_ns;
   return from_cuda(launch_attn(tq, tk, tv, p, D, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+int sage_fp4_attn_fwd(const sage_fp4_qkv* qkv, void* o, int B, int H, int N, int D, int causal,
+                      void* stream) {
+  return attn_fwd_impl(qkv, o, B, H, N, D, causal, 0, kAttnWaitNs, stream);
+}
+
+int sage_fp4_attn_fwd_stall_test(const sage_fp4_qkv* qkv, void* o, int B, int H, int N, int D,
+                                 int causal, uint64_t wait_limit_ns, void* stream) {
+  if (wait_limit_ns < 1000000ull || wait_limit_ns > kAttnWaitNs) return SAGE_FP4_EINVAL;
+  return attn_fwd_impl(qkv, o, B, H, N, D, causal, kAttnWithholdK, wait_limit_ns, stream);
 }
 
 int sage_fp4_get_status(const sage_fp4_qkv* qkv, void* stream) {

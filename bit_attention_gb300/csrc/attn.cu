@@ -49,7 +49,6 @@ constexpr int kNumBuf = 3;   // S/PV tensor-memory buffers, P and row-stat slots
 constexpr int kThreads = 512;
 constexpr uint32_t kRegsCtl = 48, kRegsSoftmax = 144, kRegsCorr = 176;
 static_assert(kRegsCtl * 128 + kRegsSoftmax * 256 + kRegsCorr * 128 == 65536, "register split");
-constexpr uint64_t kWaitLimitNs = 1500ull * 1000ull * 1000ull;  // a bounded wait gives up after 1.5 s
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // tensor-memory columns
@@ -106,6 +105,7 @@ struct Smem {
 struct Ctl {
   volatile int* abort;
   int32_t* status;
+  uint64_t limit;  // ns after which a bounded wait gives up
 };
 
 __device__ __forceinline__ void give_up(const Ctl& c) {
@@ -120,7 +120,7 @@ __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, Ctl c) {
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*c.abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > c.limit) {
       give_up(c);
       return false;
     }
@@ -137,7 +137,7 @@ __device__ __forceinline__ bool waitw(uint32_t bar, uint32_t parity, Ctl c) {
     if ((threadIdx.x & 31) == 0) {
       if (*c.abort) {
         stop = 1;
-      } else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      } else if (globaltimer_ns() - t0 > c.limit) {
         give_up(c);
         stop = 1;
       }
@@ -147,9 +147,9 @@ __device__ __forceinline__ bool waitw(uint32_t bar, uint32_t parity, Ctl c) {
 }
 
 // Wait used only while abandoning work: ignores the abort flag, still bounded.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const Ctl& c) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < kWaitLimitNs) {
+  while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < c.limit) {
   }
 }
 
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sb + L::oBar + 8 * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::oMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::oMisc + 4);
-  const Ctl ctl{abort_flag, p.status};
+  const Ctl ctl{abort_flag, p.status, p.wait_ns};
   const int n_items = p.BH * p.n_qt;
   const int item0 = static_cast<int>(blockIdx.x), istep = static_cast<int>(gridDim.x);
 
@@ -274,6 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* sfk = p.sfk + static_cast<size_t>(I.bh) * p.Np * (D / 16);
         for (int k = 0; k < I.nkv; ++k, ++g) {
           const int s = g % kStages;
+          if ((p.flags & kAttnWithholdK) && g >= 1) {
+            ok = false;  // failure-detection test: the next K tile never comes
+            break;
+          }
           if (g >= kStages && !(ok = wait1(bar(B_SDONE + s), ((g / kStages) - 1) & 1, ctl))) break;
           mbar_arrive_expect_tx(bar(B_KFULL + s), L::QBYTES + L::SFQK);
           tma_load_2d(sb + L::oK + s * L::QBYTES, &tm_k, 0, I.bh * p.Np + k * kTileKV, bar(B_KFULL + s));
@@ -287,12 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
         }
       }
-      if (!ok) {
-        // abandoning: let the copies this thread started land before the CTA exits
-        for (int j = (nq > 2 ? nq - 2 : 0); j < nq; ++j) drain_wait(bar(B_QFULL + (j & 1)), (j >> 1) & 1);
-        for (int j = (nk > kStages ? nk - kStages : 0); j < nk; ++j)
-          drain_wait(bar(B_KFULL + j % kStages), (j / kStages) & 1);
-      }
+      // every copy this thread started has landed before the CTA exits (at
+      // once after a normal run; after a role gave up, possibly not yet)
+      (void)ok;
+      for (int j = (nq > 2 ? nq - 2 : 0); j < nq; ++j) drain_wait(bar(B_QFULL + (j & 1)), (j >> 1) & 1, ctl);
+      for (int j = (nk > kStages ? nk - kStages : 0); j < nk; ++j)
+        drain_wait(bar(B_KFULL + j % kStages), (j / kStages) & 1, ctl);
     } else if (!skip && warp == 2 && lane == 0) {
       // -------------------------------------------------------- V producer
       prefetch_tensormap(&tm_v);
@@ -312,9 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           nv = g + 1;
         }
       }
-      if (!ok)
-        for (int j = (nv > kStages ? nv - kStages : 0); j < nv; ++j)
-          drain_wait(bar(B_VFULL + j % kStages), (j / kStages) & 1);
+      (void)ok;
+      for (int j = (nv > kStages ? nv - kStages : 0); j < nv; ++j)
+        drain_wait(bar(B_VFULL + j % kStages), (j / kStages) & 1, ctl);
     } else if (!skip && warp == 1 && lane == 0) {
       // ------------------------------------------------------- S issuer
       constexpr uint32_t idS = idesc_nvfp4(128, 128);
@@ -357,11 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // the last item's release must land before the CTA can exit
       if (ok && i > 0) ok = wait1(bar(B_QEMPTY + ((i - 1) & 1)), ((i - 1) >> 1) & 1, ctl);
-      if (!ok) {
-        // abandoning: wait for the tensor-core work this thread issued
-        tc_commit(bar(B_DRAIN));
-        drain_wait(bar(B_DRAIN), 0);
-      }
+      // the tensor-core work this thread issued has completed before tensor
+      // memory is freed (at once after a normal run)
+      tc_commit(bar(B_DRAIN));
+      drain_wait(bar(B_DRAIN), 0, ctl);
     } else if (!skip && warp == 3 && lane == 0) {
       // ------------------------------------------------------ PV issuer
       constexpr uint32_t idPV = idesc_nvfp4(128, D);
@@ -391,10 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_commit(bar(B_PVDONE + s));
         }
       }
-      if (!ok) {
-        tc_commit(bar(B_DRAIN + 1));
-        drain_wait(bar(B_DRAIN + 1), 0);
-      }
+      tc_commit(bar(B_DRAIN + 1));
+      drain_wait(bar(B_DRAIN + 1), 0, ctl);
     }
     // every role ends at the same CTA-wide barrier; then tensor memory is freed
     tc_fence_before();

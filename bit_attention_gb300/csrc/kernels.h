@@ -21,8 +21,16 @@ struct AttnParams {
   int32_t* status;
   int BH, N, Np, causal, n_qt;
   float a;  // log2(e) / sqrt(D): softmax scale folded into exp2
-  int flags;
+  int flags;           // kAttnWithholdK: failure-detection test (see below)
+  uint64_t wait_ns;    // limit of every bounded wait in the kernel
 };
+
+// Failure-detection test: the K producer issues the first KV tile of its
+// stream and then stops, so the S issuer's bounded wait for the next tile
+// gives up, sets the status word to SAGE_FP4_ETIMEOUT, and every role
+// abandons its work through the normal drain path.
+constexpr int kAttnWithholdK = 1;
+constexpr uint64_t kAttnWaitNs = 1500ull * 1000ull * 1000ull;  // 1.5 s
 
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const AttnParams& p, int D, cudaStream_t st);

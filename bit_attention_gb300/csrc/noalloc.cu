@@ -161,5 +161,6 @@ extern "C" int sage_fp4_attention_noalloc(const void* q, const void* k, const vo
   p.n_qt = Np / 128;
   p.a = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
   p.flags = 0;
+  p.wait_ns = kAttnWaitNs;
   return launch_attn(tq, tk, tv, p, D, st) == cudaSuccess ? SAGE_FP4_OK : SAGE_FP4_ECUDA;
 }

@@ -117,6 +117,18 @@ int sage_fp4_quantize_qkv(const void *q, const void *k, const void *v, const sag
 int sage_fp4_attn_fwd(const sage_fp4_qkv *qkv, void *o, int B, int H, int N, int D, int causal,
                       void *stream);
 
+/* No counterpart in the pages: the failure-detection test of the attention
+ * kernel's bounded waits.  The same launch as sage_fp4_attn_fwd, except that
+ * the kernel's K-tile producer stops after the first KV tile of each CTA's
+ * stream and every bounded wait gives up after wait_limit_ns (1 ms to 1.5 s;
+ * sage_fp4_attn_fwd uses 1.5 s).  The waiting roles then abandon their work:
+ * copies and tensor-core operations in flight are waited for, tensor memory is
+ * freed, nothing faults, and *qkv->status becomes SAGE_FP4_ETIMEOUT.  O is left
+ * partly written.  Returns SAGE_FP4_EINVAL for a limit out of range, else as
+ * sage_fp4_attn_fwd; read the outcome with sage_fp4_get_status. */
+int sage_fp4_attn_fwd_stall_test(const sage_fp4_qkv *qkv, void *o, int B, int H, int N, int D,
+                                 int causal, uint64_t wait_limit_ns, void *stream);
+
 /* Synchronise `stream`, read the status word of `qkv`, reset it to 0 and
  * return it (SAGE_FP4_OK, SAGE_FP4_ETIMEOUT) or SAGE_FP4_ECUDA if the copy
  * itself failed. */
