@@ -24,14 +24,17 @@
 //   warps 8-11   the same for the odd tiles: with level 1 normalised per
 //                tile, tiles are independent until O is combined
 //   warps 12-15  correction: rescale-and-accumulate O in registers, epilogue
-// Every MMA group ends in exactly one tcgen05.commit (each costs ~40 cycles
-// of issue and ~250 cycles until the barrier is seen on GB300); S and PV come
-// from two threads so that neither waits behind the other.
+// Tensor memory (512 columns x 128 lanes): each softmax warpgroup owns one
+// 128-column S buffer, which it hands back to the S issuer as soon as it has
+// loaded its rows, so the next S of that warpgroup overlaps the rest of its
+// softmax.  PV goes through separate buffers that the correction empties (one
+// of 128 columns at D = 128, three of 64 at D = 64), so the correction is off
+// the S buffers' loop.  The last 64 columns hold double-buffered scale
+// factors of Q, K, V and P.  Every MMA group ends in exactly one
+// tcgen05.commit (each costs ~40 cycles of issue and ~250 cycles until the
+// barrier is seen on GB300).
 // Registers are rebalanced with setmaxnreg: 48 (warps 0-3), 144 (softmax),
 // 176 (correction); 48*128 + 144*256 + 176*128 = 65536.
-// Tensor memory (512 columns x 128 lanes): three 128-column buffers; tile g
-// uses buffer g % 3 for S_g and, once the softmax has read S_g, for PV_g.
-// Then double-buffered scale factors of Q, K, V and P.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -45,31 +48,38 @@ namespace sagefp4 {
 namespace {
 
 constexpr int kStages = 6;   // K and V^T shared-memory ring depth
-constexpr int kNumBuf = 3;   // S/PV tensor-memory buffers, P and row-stat slots
+constexpr int kPSlots = 3;   // P tiles (and their scales) in shared memory
+constexpr int kEvRing = 6;   // P and row-stat events: slot g % 6
+constexpr int kPvBufsMax = 3;  // PV buffers (D = 64: three of 64 columns; D = 128: one of 128)
+constexpr int kPvRing = 12;  // PV completion events
 constexpr int kThreads = 512;
 constexpr uint32_t kRegsCtl = 48, kRegsSoftmax = 144, kRegsCorr = 176;
 static_assert(kRegsCtl * 128 + kRegsSoftmax * 256 + kRegsCorr * 128 == 65536, "register split");
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // tensor-memory columns
-constexpr uint32_t kColSFQ = 384;  // 2 item slots x 8
-constexpr uint32_t kColSFK = 400;  // 2 slots x 8
-constexpr uint32_t kColSFV = 416;  // 2 slots x 8
-constexpr uint32_t kColSFP = 432;  // 2 slots x 8
+constexpr uint32_t kColS = 0;      // 2 S buffers x 128 (buffer = softmax warpgroup)
+constexpr uint32_t kColPV = 256;   // PV buffers: 1 x 128 (D = 128) or 3 x 64 (D = 64)
+constexpr uint32_t kColSFQ = 448;  // 2 item slots x 8
+constexpr uint32_t kColSFK = 464;  // 2 slots x 8
+constexpr uint32_t kColSFV = 480;  // 2 slots x 8
+constexpr uint32_t kColSFP = 496;  // 2 slots x 8
 constexpr uint32_t kTmemCols = 512;
 
 // barrier indices.  A barrier of a ring of R serves events n = i, i+R, ...;
 // the waiter for event n waits for completion number n / R (parity (n/R)&1).
+// PV is event e = g (one MMA group per tile).
 enum {
   B_QFULL = 0,                     // Q tile of local item i landed          [2]
   B_QEMPTY = B_QFULL + 2,          // every S of local item i completed      [2]
   B_KFULL = B_QEMPTY + 2,          // K_g landed                             [kStages]
   B_VFULL = B_KFULL + kStages,     // V_g landed                             [kStages]
   B_SDONE = B_VFULL + kStages,     // S_g in tensor memory, K slot free      [kStages]
-  B_PVDONE = B_SDONE + kStages,    // PV_g in tensor memory, V and P free    [kStages]
-  B_PFULL = B_PVDONE + kStages,    // P_g, its scales and row stats written  [3]
-  B_BUFFREE = B_PFULL + kNumBuf,   // buffer g%3 read by the correction      [3]
-  B_DRAIN = B_BUFFREE + kNumBuf,   // abandoning work: MMAs of one issuer   [2]
+  B_SFREE = B_SDONE + kStages,     // S buffer w read by its softmax         [2]
+  B_PFULL = B_SFREE + 2,           // P_g, its scales and row stats written  [kEvRing]
+  B_PVDONE = B_PFULL + kEvRing,    // PV_e in tensor memory                  [kPvRing]
+  B_PVFREE = B_PVDONE + kPvRing,   // PV buffer read by the correction       [kPvBufsMax]
+  B_DRAIN = B_PVFREE + kPvBufsMax,    // abandoning work: MMAs of one issuer   [2]
   kNumBars = B_DRAIN + 2
 };
 
@@ -87,12 +97,12 @@ struct Smem {
   static constexpr int oK = oQ + 2 * QBYTES;
   static constexpr int oV = oK + kStages * QBYTES;
   static constexpr int oP = oV + kStages * VBYTES;
-  static constexpr int oSFQ = oP + kNumBuf * PBYTES;
+  static constexpr int oSFQ = oP + kPSlots * PBYTES;
   static constexpr int oSFK = oSFQ + 2 * SFQK;
   static constexpr int oSFV = oSFK + kStages * SFQK;
   static constexpr int oSFP = oSFV + kStages * SFVB;
-  static constexpr int oStat = oSFP + kNumBuf * SFPB;
-  static constexpr int oLut = oStat + kNumBuf * 128 * 8;  // float2 per E4M3 byte
+  static constexpr int oStat = oSFP + kPSlots * SFPB;
+  static constexpr int oLut = oStat + kEvRing * 128 * 8;  // float2 per E4M3 byte
   static constexpr int oBar = oLut + 256 * 8;
   static constexpr int oMisc = oBar + kNumBars * 8;
   static constexpr int kBytes = oMisc + 16;
@@ -194,6 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
   using L = Smem<D>;
+  constexpr int NH = 1;                    // PV groups per tile
+  constexpr int kPvBufs = (D == 128) ? 1 : 3;  // PV buffers of D columns
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -216,12 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_KFULL + s), 1);
       mbar_init(bar(B_VFULL + s), 1);
       mbar_init(bar(B_SDONE + s), 1);
-      mbar_init(bar(B_PVDONE + s), 1);
     }
-    for (int b = 0; b < kNumBuf; ++b) {
-      mbar_init(bar(B_PFULL + b), 128);
-      mbar_init(bar(B_BUFFREE + b), 128);
-    }
+    for (int s = 0; s < 2; ++s) mbar_init(bar(B_SFREE + s), 128);
+    for (int s = 0; s < kEvRing; ++s) mbar_init(bar(B_PFULL + s), 128);
+    for (int s = 0; s < kPvRing; ++s) mbar_init(bar(B_PVDONE + s), 1);
+    for (int s = 0; s < kPvBufsMax; ++s) mbar_init(bar(B_PVFREE + s), 128);
     // a launch sharing this status word already gave up: do no work
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(p.status) != 0) ? 1 : 0;
     mbar_fence_init();
@@ -308,7 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* sfv = p.sfv + static_cast<size_t>(I.bh) * 8 * p.Np;
         for (int k = 0; k < I.nkv; ++k, ++g) {
           const int s = g % kStages;
-          if (g >= kStages && !(ok = wait1(bar(B_PVDONE + s), ((g / kStages) - 1) & 1, ctl))) break;
+          if (g >= kStages) {
+            const int e = (g - kStages) * NH + NH - 1;  // PV of tile g-6
+            if (!(ok = wait1(bar(B_PVDONE + e % kPvRing), (e / kPvRing) & 1, ctl))) break;
+          }
           mbar_arrive_expect_tx(bar(B_VFULL + s), L::VBYTES + L::SFVB);
           tma_load_2d(sb + L::oV + s * L::VBYTES, &tm_v, k * (kTileKV / 2), I.bh * D, bar(B_VFULL + s));
           bulk_load(sb + L::oSFV + s * L::SFVB, sfv + static_cast<size_t>(k) * L::SFVB, L::SFVB,
@@ -332,10 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait1(bar(B_QFULL + qs), (i >> 1) & 1, ctl))) break;
         bool first = true;
         for (int k = 0; k < I.nkv; ++k, ++g) {
-          const int s = g % kStages, b = g % kNumBuf, sl = g & 1;
+          const int s = g % kStages, w = g & 1, sl = g & 1;
           if (!(ok = wait1(bar(B_KFULL + s), (g / kStages) & 1, ctl))) break;
-          // buffer b is free once the correction has read PV_{g-3}
-          if (g >= kNumBuf && !(ok = wait1(bar(B_BUFFREE + b), ((g / kNumBuf) - 1) & 1, ctl))) break;
+          // S buffer w is free once its softmax warpgroup has loaded S_{g-2}
+          if (g >= 2 && !(ok = wait1(bar(B_SFREE + w), ((g >> 1) - 1) & 1, ctl))) break;
           tc_fence_after();
           if (first) {
 #pragma unroll
@@ -352,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kb = 0; kb < L::KBD; ++kb) {
             const uint64_t ad = smem_desc(sb + L::oQ + qs * L::QBYTES + 32 * kb, 16, qk_sbo, qk_swz);
             const uint64_t bd = smem_desc(sb + L::oK + s * L::QBYTES + 32 * kb, 16, qk_sbo, qk_swz);
-            mma_nvfp4(tmem + b * 128, ad, bd, idS, tmem + kColSFQ + 8 * qs + 4 * kb,
+            mma_nvfp4(tmem + kColS + w * 128, ad, bd, idS, tmem + kColSFQ + 8 * qs + 4 * kb,
                       tmem + kColSFK + 8 * sl + 4 * kb, kb > 0);
           }
           tc_commit(bar(B_SDONE + s));
@@ -367,31 +381,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(bar(B_DRAIN), 0, ctl);
     } else if (!skip && warp == 3 && lane == 0) {
       // ------------------------------------------------------ PV issuer
+      // PV_g (N = D) into the next PV buffer.  The loop over h is written for
+      // groups of 64 output columns (V^T rows 64h.., whose scale factors sit
+      // 2h columns further along: each column holds 32 rows); one group of
+      // N = D is used, measured faster than two of 64 at D = 128.
       constexpr uint32_t idPV = idesc_nvfp4(128, D);
       bool ok = true;
       int g = 0;
       for (int it = item0; ok && it < n_items; it += istep) {
         const int nkv = item_at(p, it).nkv;
         for (int k = 0; k < nkv; ++k, ++g) {
-          const int s = g % kStages, b = g % kNumBuf, sl = g & 1;
-          if (!(ok = wait1(bar(B_PFULL + b), (g / kNumBuf) & 1, ctl))) break;
+          const int s = g % kStages, ps = g % kPSlots, sl = g & 1;
+          if (!(ok = wait1(bar(B_PFULL + g % kEvRing), (g / kEvRing) & 1, ctl))) break;
           if (!(ok = wait1(bar(B_VFULL + s), (g / kStages) & 1, ctl))) break;
-          tc_fence_after();
 #pragma unroll
-          for (int kb = 0; kb < 2; ++kb) {
-            tc_cp_32x128b_warpx4(tmem + kColSFP + 8 * sl + 4 * kb,
-                                 smem_desc(sb + L::oSFP + b * L::SFPB + 512 * kb, 0, 128, kSwizzleNone));
-            tc_cp_32x128b_warpx4(tmem + kColSFV + 8 * sl + 4 * kb,
-                                 smem_desc(sb + L::oSFV + s * L::SFVB + 512 * kb, 0, 128, kSwizzleNone));
-          }
+          for (int h = 0; h < NH; ++h) {
+            const int e = g * NH + h, pb = e % kPvBufs;
+            if (e >= kPvBufs && !(ok = wait1(bar(B_PVFREE + pb), ((e / kPvBufs) - 1) & 1, ctl))) break;
+            tc_fence_after();
+            if (h == 0) {
 #pragma unroll
-          for (int kb = 0; kb < 2; ++kb) {
-            const uint64_t ad = smem_desc(sb + L::oP + b * L::PBYTES + 32 * kb, 16, 512, kSwizzle64B);
-            const uint64_t bd = smem_desc(sb + L::oV + s * L::VBYTES + 32 * kb, 16, 512, kSwizzle64B);
-            mma_nvfp4(tmem + b * 128, ad, bd, idPV, tmem + kColSFP + 8 * sl + 4 * kb,
-                      tmem + kColSFV + 8 * sl + 4 * kb, kb > 0);
+              for (int kb = 0; kb < 2; ++kb) {
+                tc_cp_32x128b_warpx4(tmem + kColSFP + 8 * sl + 4 * kb,
+                                     smem_desc(sb + L::oSFP + ps * L::SFPB + 512 * kb, 0, 128, kSwizzleNone));
+                tc_cp_32x128b_warpx4(tmem + kColSFV + 8 * sl + 4 * kb,
+                                     smem_desc(sb + L::oSFV + s * L::SFVB + 512 * kb, 0, 128, kSwizzleNone));
+              }
+            }
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+              const uint64_t ad = smem_desc(sb + L::oP + ps * L::PBYTES + 32 * kb, 16, 512, kSwizzle64B);
+              const uint64_t bd =
+                  smem_desc(sb + L::oV + s * L::VBYTES + h * 64 * 64 + 32 * kb, 16, 512, kSwizzle64B);
+              mma_nvfp4(tmem + kColPV + pb * D, ad, bd, idPV, tmem + kColSFP + 8 * sl + 4 * kb,
+                        tmem + kColSFV + 8 * sl + 4 * kb + 2 * h, kb > 0);
+            }
+            tc_commit(bar(B_PVDONE + e % kPvRing));
           }
-          tc_commit(bar(B_PVDONE + s));
+          if (!ok) break;
         }
       }
       tc_commit(bar(B_DRAIN + 1));
@@ -423,10 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int vis_end = p.causal ? min(p.N, gi + 1) : p.N;  // keys j < vis_end are visible
         for (int k = (par - g0) & 1; k < I.nkv; k += 2) {
           const int g = g0 + k;
-          const int b = g % kNumBuf;
+          const int ps = g % kPSlots;
           if (!(ok = waitw(bar(B_SDONE + g % kStages), (g / kStages) & 1, ctl))) break;
           tc_fence_after();
-          const uint32_t tb = tmem + b * 128 + lane_base;
+          const uint32_t tb = tmem + kColS + par * 128 + lane_base;
           const int lim = vis_end - k * kTileKV;
           // pass 1: the 16-element group maxima, whose maximum is the tile maximum
           float gm[8];
@@ -464,11 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             bias[q + 1] = nb + t1.x;
             lsc[q + 1] = t1.y;
           }
-          // P slot b is free once PV_{g-3} has completed
-          if (g >= kNumBuf &&
-              !(ok = waitw(bar(B_PVDONE + (g - kNumBuf) % kStages), ((g - kNumBuf) / kStages) & 1, ctl)))
-            break;
-          uint8_t* prow = sm + L::oP + b * L::PBYTES + r * 64;
+          // P slot ps is free once PV_{g-3} has completed
+          if (g >= kPSlots) {
+            const int e = (g - kPSlots) * NH + NH - 1;
+            if (!(ok = waitw(bar(B_PVDONE + e % kPvRing), (e / kPvRing) & 1, ctl))) break;
+          }
+          uint8_t* prow = sm + L::oP + ps * L::PBYTES + r * 64;
           uint64_t acc[2] = {0ull, 0ull};  // row sum, two FP32x2 chains
           // pass 2: exponentials, row sum and codes, 32 keys at a time
 #pragma unroll
@@ -476,6 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t sv[32];
             tmem_ld32(tb + 32 * c, sv);
             tmem_wait_ld();
+            if (c == 3) {
+              // the last of S_g is in registers: the buffer can take S_{g+2}
+              tc_fence_before();
+              mbar_arrive(bar(B_SFREE + par));
+            }
             if (lim < kTileKV) {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
@@ -506,14 +539,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             *reinterpret_cast<uint4*>(prow + ((c ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          uint8_t* sfp = sm + L::oSFP + b * L::SFPB + (r % 32) * 16 + (r / 32) * 4;
+          uint8_t* sfp = sm + L::oSFP + ps * L::SFPB + (r % 32) * 16 + (r / 32) * 4;
           *reinterpret_cast<uint32_t*>(sfp) = __byte_perm(s2[0], s2[1], 0x5410);
           *reinterpret_cast<uint32_t*>(sfp + 512) = __byte_perm(s2[2], s2[3], 0x5410);
           const uint64_t acc2 = add2(acc[0], acc[1]);
-          reinterpret_cast<float2*>(sm + L::oStat + b * 1024)[r] = make_float2(t, lo2(acc2) + hi2(acc2));
+          reinterpret_cast<float2*>(sm + L::oStat + (g % kEvRing) * 1024)[r] =
+              make_float2(t, lo2(acc2) + hi2(acc2));
           fence_proxy_async_smem();
           tc_fence_before();
-          mbar_arrive(bar(B_PFULL + b));
+          mbar_arrive(bar(B_PFULL + g % kEvRing));
         }
         g0 += I.nkv;
       }
@@ -540,10 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // is the same up to rounding, since O / l does not depend on m.
         float m = -INFINITY, l = 0.0f;
         for (int k = 0; k < I.nkv; ++k, ++g) {
-          const int b = g % kNumBuf;
           // the row stats of tile g are written before P_g is announced
-          if (!(ok = waitw(bar(B_PFULL + b), (g / kNumBuf) & 1, ctl))) break;
-          const float2 st = reinterpret_cast<const float2*>(sm + L::oStat + b * 1024)[r];
+          if (!(ok = waitw(bar(B_PFULL + g % kEvRing), (g / kEvRing) & 1, ctl))) break;
+          const float2 st = reinterpret_cast<const float2*>(sm + L::oStat + (g % kEvRing) * 1024)[r];
           const bool up = (st.x - m) * a > 8.0f;
           const float mn = up ? st.x : m;
           const float alpha = up ? ex2_approx((m - mn) * a) : 1.0f;
@@ -552,28 +585,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float w = beta * (1.0f / 2688.0f);
           m = mn;
           const bool keep = !__any_sync(kFull, up);  // no row of the warp moved its reference
-          if (!(ok = waitw(bar(B_PVDONE + g % kStages), (g / kStages) & 1, ctl))) break;
-          tc_fence_after();
           const uint64_t w2 = pack2(w, w), al2 = pack2(alpha, alpha);
 #pragma unroll
-          for (int h = 0; h < D / 32; ++h) {
-            uint32_t v[32];
-            tmem_ld32(tmem + b * 128 + 32 * h + lane_base, v);
-            tmem_wait_ld();
-            if (keep) {
+          for (int h = 0; h < NH; ++h) {
+            const int e = g * NH + h, pb = e % kPvBufs;
+            if (!(ok = waitw(bar(B_PVDONE + e % kPvRing), (e / kPvRing) & 1, ctl))) break;
+            tc_fence_after();
 #pragma unroll
-              for (int e = 0; e < 16; ++e)
-                o2[16 * h + e] =
-                    fma2(pack2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), w2, o2[16 * h + e]);
-            } else {
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t v[32];
+              tmem_ld32(tmem + kColPV + pb * D + 32 * c + lane_base, v);
+              tmem_wait_ld();
+              if (c == D / 32 - 1) {
+                // all of this PV half is in registers: its buffer is free
+                tc_fence_before();
+                mbar_arrive(bar(B_PVFREE + pb));
+              }
+              uint64_t* oc = &o2[32 * h + 16 * c];
+              if (keep) {
 #pragma unroll
-              for (int e = 0; e < 16; ++e)
-                o2[16 * h + e] = fma2(pack2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), w2,
-                                      mul2(o2[16 * h + e], al2));
+                for (int j = 0; j < 16; ++j)
+                  oc[j] = fma2(pack2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), w2, oc[j]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  oc[j] = fma2(pack2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), w2,
+                               mul2(oc[j], al2));
+              }
             }
           }
-          tc_fence_before();
-          mbar_arrive(bar(B_BUFFREE + b));
+          if (!ok) break;
         }
         const int gi = I.qt * kTileQ + r;
         if (ok && gi < p.N) {
