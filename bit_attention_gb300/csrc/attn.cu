@@ -33,8 +33,7 @@
 // factors of Q, K, V and P.  Every MMA group ends in exactly one
 // tcgen05.commit (each costs ~40 cycles of issue and ~250 cycles until the
 // barrier is seen on GB300).
-// Registers are rebalanced with setmaxnreg: 48 (warps 0-3), 144 (softmax),
-// 176 (correction); 48*128 + 144*256 + 176*128 = 65536.
+// Registers are rebalanced with setmaxnreg (budgets per head dimension below).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -53,8 +52,22 @@ constexpr int kEvRing = 6;   // P and row-stat events: slot g % 6
 constexpr int kPvBufsMax = 3;  // PV buffers (D = 64: three of 64 columns; D = 128: one of 128)
 constexpr int kPvRing = 12;  // PV completion events
 constexpr int kThreads = 512;
-constexpr uint32_t kRegsCtl = 48, kRegsSoftmax = 144, kRegsCorr = 176;
-static_assert(kRegsCtl * 128 + kRegsSoftmax * 256 + kRegsCorr * 128 == 65536, "register split");
+// Register budgets (setmaxnreg) of the control warps, each softmax thread and
+// each correction thread.  The correction holds its O row (D registers) plus
+// 64 columns of PV, so that it waits once per 64 columns of a PV buffer; at
+// D = 128 that costs the softmax 16 registers (measured net gain 4-6%).
+template <int D>
+struct Regs;
+template <>
+struct Regs<128> {
+  static constexpr uint32_t kCtl = 48, kSoftmax = 128, kCorr = 208;
+};
+template <>
+struct Regs<64> {
+  static constexpr uint32_t kCtl = 48, kSoftmax = 144, kCorr = 176;
+};
+static_assert(Regs<128>::kCtl * 128 + Regs<128>::kSoftmax * 256 + Regs<128>::kCorr * 128 == 65536, "split");
+static_assert(Regs<64>::kCtl * 128 + Regs<64>::kSoftmax * 256 + Regs<64>::kCorr * 128 == 65536, "split");
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // tensor-memory columns
@@ -260,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int wg = warp / 4;
   if (wg == 0) {
-    regs_dec<kRegsCtl>();
+    regs_dec<Regs<D>::kCtl>();
     if (!skip && warp == 0 && lane == 0) {
       // ---------------------------------------------------- Q and K producer
       prefetch_tensormap(&tm_q);
@@ -433,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (wg == 1 || wg == 2) {
     // -------------------------------------------------------- softmax + P quantization
-    regs_inc<kRegsSoftmax>();
+    regs_inc<Regs<D>::kSoftmax>();
     if (!skip) {
       const int par = wg - 1;                // this warpgroup takes the tiles g with g % 2 == par
       const int r = threadIdx.x - 128 * wg;  // query row of this thread = TMEM lane
@@ -556,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cta_bar_sync();
   } else {
     // -------------------------------------------------------- correction + epilogue
-    regs_inc<kRegsCorr>();
+    regs_inc<Regs<D>::kCorr>();
     if (!skip) {
       const int r = threadIdx.x - 384;
       const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -591,24 +604,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int e = g * NH + h, pb = e % kPvBufs;
             if (!(ok = waitw(bar(B_PVDONE + e % kPvRing), (e / kPvRing) & 1, ctl))) break;
             tc_fence_after();
+            // CW columns per wait (64 at D = 128, 32 at D = 64: measured)
+            constexpr int CW = (D == 128) ? 64 : 32;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t v[32];
-              tmem_ld32(tmem + kColPV + pb * D + 32 * c + lane_base, v);
+            for (int c = 0; c < D / CW; ++c) {
+              uint32_t v[CW];
+#pragma unroll
+              for (int x = 0; x < CW / 32; ++x)
+                tmem_ld32(tmem + kColPV + pb * D + CW * c + 32 * x + lane_base,
+                          *reinterpret_cast<uint32_t(*)[32]>(&v[32 * x]));
               tmem_wait_ld();
-              if (c == D / 32 - 1) {
-                // all of this PV half is in registers: its buffer is free
+              if (c == D / CW - 1) {
+                // all of PV_e is in registers: its buffer is free
                 tc_fence_before();
                 mbar_arrive(bar(B_PVFREE + pb));
               }
-              uint64_t* oc = &o2[32 * h + 16 * c];
+              uint64_t* oc = &o2[(CW / 2) * c];
               if (keep) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
+                for (int j = 0; j < CW / 2; ++j)
                   oc[j] = fma2(pack2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), w2, oc[j]);
               } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
+                for (int j = 0; j < CW / 2; ++j)
                   oc[j] = fma2(pack2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), w2,
                                mul2(oc[j], al2));
               }
