@@ -468,21 +468,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t tb = tmem + kColS + par * 128 + lane_base;
           const int lim = vis_end - k * kTileKV;
-          // pass 1: the 16-element group maxima, whose maximum is the tile maximum
+          // pass 1: the 16-element group maxima, whose maximum is the tile
+          // maximum; the second 64 keys stay in registers for pass 2
           float gm[8];
+          uint32_t s64[64];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            uint32_t sv[64];
-            tmem_ld32(tb + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-            tmem_ld32(tb + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+            tmem_ld32(tb + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&s64[0]));
+            tmem_ld32(tb + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&s64[32]));
             tmem_wait_ld();
             if (lim < kTileKV) {
 #pragma unroll
               for (int j = 0; j < 64; ++j)
-                if (64 * h + j >= lim) sv[j] = __float_as_uint(-INFINITY);
+                if (64 * h + j >= lim) s64[j] = __float_as_uint(-INFINITY);
             }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) gm[4 * h + q] = max16(&sv[16 * q]);
+            for (int q = 0; q < 4; ++q) gm[4 * h + q] = max16(&s64[16 * q]);
           }
           const float t = max3f(max3f(gm[0], gm[1], gm[2]), max3f(gm[3], gm[4], gm[5]),
                                 fmaxf(gm[6], gm[7]));
@@ -511,46 +512,58 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* prow = sm + L::oP + ps * L::PBYTES + r * 64;
           uint64_t acc[2] = {0ull, 0ull};  // row sum, two FP32x2 chains
-          // pass 2: exponentials, row sum and codes, 32 keys at a time
+          // pass 2: exponentials, row sum and codes, 64 keys per tensor-memory
+          // wait.  Where registers allow (D = 64), keys 64-127 are still in
+          // registers from pass 1 and go first; otherwise both halves are read
+          // again in order.
+          constexpr bool kKeep = (D == 64);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t sv[32];
-            tmem_ld32(tb + 32 * c, sv);
-            tmem_wait_ld();
-            if (c == 3) {
-              // the last of S_g is in registers: the buffer can take S_{g+2}
-              tc_fence_before();
-              mbar_arrive(bar(B_SFREE + par));
-            }
-            if (lim < kTileKV) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (32 * c + j >= lim) sv[j] = __float_as_uint(-INFINITY);
-            }
-            uint32_t w[4];
-#pragma unroll
-            for (int gg = 0; gg < 2; ++gg) {
-              const int q = 2 * c + gg;
-              const uint64_t bb = pack2(bias[q], bias[q]), l2 = pack2(lsc[q], lsc[q]);
-              float y[16];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const uint64_t x = fma2(
-                    pack2(__uint_as_float(sv[16 * gg + 2 * e]), __uint_as_float(sv[16 * gg + 2 * e + 1])),
-                    a2, bb);
-                y[2 * e] = ex2_approx(lo2(x));
-                y[2 * e + 1] = ex2_approx(hi2(x));
-                acc[e & 1] = fma2(pack2(y[2 * e], y[2 * e + 1]), l2, acc[e & 1]);
+          for (int i2 = 0; i2 < 2; ++i2) {
+            const int c2 = kKeep ? 1 - i2 : i2;
+            if (!kKeep || c2 == 0) {
+              tmem_ld32(tb + 64 * c2, *reinterpret_cast<uint32_t(*)[32]>(&s64[0]));
+              tmem_ld32(tb + 64 * c2 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s64[32]));
+              tmem_wait_ld();
+              if (i2 == 1) {
+                // the last of S_g is in registers: the buffer can take S_{g+2}
+                tc_fence_before();
+                mbar_arrive(bar(B_SFREE + par));
               }
-              float y8[8];
+              if (lim < 64 * (c2 + 1)) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) y8[e] = y[e];
-              w[2 * gg] = cvt_e2m1x8(y8);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) y8[e] = y[8 + e];
-              w[2 * gg + 1] = cvt_e2m1x8(y8);
+                for (int j = 0; j < 64; ++j)
+                  if (64 * c2 + j >= lim) s64[j] = __float_as_uint(-INFINITY);
+              }
             }
-            *reinterpret_cast<uint4*>(prow + ((c ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              const int c = 2 * c2 + cc;
+              const uint32_t* sv = &s64[32 * cc];
+              uint32_t w[4];
+#pragma unroll
+              for (int gg = 0; gg < 2; ++gg) {
+                const int q = 2 * c + gg;
+                const uint64_t bb = pack2(bias[q], bias[q]), l2 = pack2(lsc[q], lsc[q]);
+                float y[16];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const uint64_t x = fma2(
+                      pack2(__uint_as_float(sv[16 * gg + 2 * e]), __uint_as_float(sv[16 * gg + 2 * e + 1])),
+                      a2, bb);
+                  y[2 * e] = ex2_approx(lo2(x));
+                  y[2 * e + 1] = ex2_approx(hi2(x));
+                  acc[e & 1] = fma2(pack2(y[2 * e], y[2 * e + 1]), l2, acc[e & 1]);
+                }
+                float y8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y8[e] = y[e];
+                w[2 * gg] = cvt_e2m1x8(y8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y8[e] = y[8 + e];
+                w[2 * gg + 1] = cvt_e2m1x8(y8);
+              }
+              *reinterpret_cast<uint4*>(prow + ((c ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
           }
           uint8_t* sfp = sm + L::oSFP + ps * L::SFPB + (r % 32) * 16 + (r / 32) * 4;
           *reinterpret_cast<uint32_t*>(sfp) = __byte_perm(s2[0], s2[1], 0x5410);
