@@ -205,6 +205,7 @@ def main():
     ap.add_argument("--shape", default=None, help="B,H,N,D override (profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-sdpa", action="store_true", help="skip the bf16 SDPA context timing")
     ap.add_argument("--ref-seconds", type=float, default=6.0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
@@ -267,7 +268,8 @@ def main():
     total_ms = max_over_ranks(total_ms, world)
     ms_step = total_ms / args.steps
     q_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev)
-    a_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev)
+    a_all = [b.elapsed_time(c) for _, b, c in ev]
+    a_ms = statistics.mean(a_all)
     status = z.get_status()
     if status != 0:
         raise RuntimeError(f"kernel status {S.strerror(status)}")
@@ -313,6 +315,30 @@ def main():
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": 3 * elems * 2,
                "d2h_bytes_per_step": elems * 2}
 
+    # context only (not a target): PyTorch's bf16 scaled_dot_product_attention
+    # on the same inputs and GPU, outside the timed region
+    context = None
+    if not args.no_sdpa:
+        try:
+            import torch.nn.functional as F
+            qs, ks, vs = qd, kd, vd
+            for _ in range(2):
+                F.scaled_dot_product_attention(qs, ks, vs, is_causal=w.causal)
+            torch.cuda.synchronize()
+            times = []
+            for _ in range(5):
+                s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s0.record(stream)
+                F.scaled_dot_product_attention(qs, ks, vs, is_causal=w.causal)
+                s1.record(stream)
+                torch.cuda.synchronize()
+                times.append(s0.elapsed_time(s1))
+            sdpa_ms = statistics.median(times)
+            context = {"sdpa_bf16_ms": sdpa_ms, "sdpa_bf16_tops": ops / (sdpa_ms * 1e-3) / 1e12,
+                       "attn_kernel_speedup_vs_sdpa_bf16": sdpa_ms / a_ms}
+        except Exception as exc:  # context only
+            context = {"sdpa_bf16": f"unavailable: {type(exc).__name__}"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         v_cpu, secs, rows, threads = cpu_oracle_sample(w, args.cpu_seconds)
@@ -329,7 +355,10 @@ def main():
             "data": "synthetic (seeded, bit_attention_gb300.synth)",
             "config": dict(w.describe(), l2="bf16 inputs 3x larger than L2; no flush",
                            parallelism=f"weak, {world} independent batch(es)"),
-            "attn_kernel": {"ms": a_ms, "tops": attn_tops, "frac_of_fp4_peak": attn_tops / fp4_peak},
+            "attn_kernel": {"ms": a_ms, "tops": attn_tops, "frac_of_fp4_peak": attn_tops / fp4_peak,
+                            "ms_median": statistics.median(a_all), "ms_min": min(a_all),
+                            "ms_max": max(a_all)},
+            "context": context,
             "quant_kernels": {"ms": q_ms, "gbs": quant_bytes / (q_ms * 1e-3) / 1e9,
                               "frac_of_hbm": quant_gbs / pk["hbm_gbs"]},
             "roofline": {"bound": "tensor", "achieved": attn_tops, "peak": fp4_peak,
