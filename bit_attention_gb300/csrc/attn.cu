@@ -409,20 +409,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = g % kStages, ps = g % kPSlots, sl = g & 1;
           if (!(ok = wait1(bar(B_PFULL + g % kEvRing), (g / kEvRing) & 1, ctl))) break;
           if (!(ok = wait1(bar(B_VFULL + s), (g / kStages) & 1, ctl))) break;
+          // the scale factors go in while the correction still reads the PV buffer
+          tc_fence_after();
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb) {
+            tc_cp_32x128b_warpx4(tmem + kColSFP + 8 * sl + 4 * kb,
+                                 smem_desc(sb + L::oSFP + ps * L::SFPB + 512 * kb, 0, 128, kSwizzleNone));
+            tc_cp_32x128b_warpx4(tmem + kColSFV + 8 * sl + 4 * kb,
+                                 smem_desc(sb + L::oSFV + s * L::SFVB + 512 * kb, 0, 128, kSwizzleNone));
+          }
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
             const int e = g * NH + h, pb = e % kPvBufs;
             if (e >= kPvBufs && !(ok = wait1(bar(B_PVFREE + pb), ((e / kPvBufs) - 1) & 1, ctl))) break;
             tc_fence_after();
-            if (h == 0) {
-#pragma unroll
-              for (int kb = 0; kb < 2; ++kb) {
-                tc_cp_32x128b_warpx4(tmem + kColSFP + 8 * sl + 4 * kb,
-                                     smem_desc(sb + L::oSFP + ps * L::SFPB + 512 * kb, 0, 128, kSwizzleNone));
-                tc_cp_32x128b_warpx4(tmem + kColSFV + 8 * sl + 4 * kb,
-                                     smem_desc(sb + L::oSFV + s * L::SFVB + 512 * kb, 0, 128, kSwizzleNone));
-              }
-            }
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
               const uint64_t ad = smem_desc(sb + L::oP + ps * L::PBYTES + 32 * kb, 16, 512, kSwizzle64B);
