@@ -363,8 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < I.nkv; ++k, ++g) {
           const int s = g % kStages, w = g & 1, sl = g & 1;
           if (!(ok = wait1(bar(B_KFULL + s), (g / kStages) & 1, ctl))) break;
-          // S buffer w is free once its softmax warpgroup has loaded S_{g-2}
-          if (g >= 2 && !(ok = wait1(bar(B_SFREE + w), ((g >> 1) - 1) & 1, ctl))) break;
+          // the scale factors go in while the softmax still reads the S buffer
           tc_fence_after();
           if (first) {
 #pragma unroll
@@ -377,6 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kb = 0; kb < L::KBD; ++kb)
             tc_cp_32x128b_warpx4(tmem + kColSFK + 8 * sl + 4 * kb,
                                  smem_desc(sb + L::oSFK + s * L::SFQK + 512 * kb, 0, 128, kSwizzleNone));
+          // S buffer w is free once its softmax warpgroup has loaded S_{g-2}
+          if (g >= 2 && !(ok = wait1(bar(B_SFREE + w), ((g >> 1) - 1) & 1, ctl))) break;
+          tc_fence_after();
 #pragma unroll
           for (int kb = 0; kb < L::KBD; ++kb) {
             const uint64_t ad = smem_desc(sb + L::oQ + qs * L::QBYTES + 32 * kb, 16, qk_sbo, qk_swz);
