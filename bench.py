@@ -283,20 +283,18 @@ def main():
     quant_bytes = 3 * elems * 2 + 3 * (elems // 2 + elems // 16)
     quant_gbs = quant_bytes / (q_ms * 1e-3) / 1e9
 
-    # end to end through the public API: pinned host inputs -> device, quantize,
-    # attention, O back to pinned host memory, every step
+    # end to end through the public API: one C-ABI call with pinned host
+    # buffers per step (sage_fp4_attention_host: host -> device copies,
+    # quantize, attention and the copy of O back to host memory, pipelined
+    # over chunks of heads inside the library)
     e2e = None
     if not args.no_e2e:
         hq, hk, hv = (t.pin_memory() for t in (q, k, v))
         ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hws = S.HostWorkspace(w.B, w.H, w.N, w.D)
 
         def e2e_step():
-            qd.copy_(hq, non_blocking=True)
-            kd.copy_(hk, non_blocking=True)
-            vd.copy_(hv, non_blocking=True)
-            S.quantize_qkv(qd, kd, vd, out=z)
-            S.attn_fwd(z, w.causal, out=o)
-            ho.copy_(o, non_blocking=True)
+            S.attention_host(hq, hk, hv, w.causal, out=ho, workspace=hws, stream=stream)
 
         for _ in range(args.warmup):
             e2e_step()
@@ -313,7 +311,8 @@ def main():
         e2e_ms = max_over_ranks(s0.elapsed_time(s1), world) / args.steps
         e2e = {"value": ops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": 3 * elems * 2,
-               "d2h_bytes_per_step": elems * 2}
+               "d2h_bytes_per_step": elems * 2, "call": "sage_fp4_attention_host",
+               "head_chunks": -(-(w.B * w.H) // -(-(w.B * w.H) // 8))}
 
     # context only (not a target): PyTorch's bf16 scaled_dot_product_attention
     # on the same inputs and GPU, outside the timed region

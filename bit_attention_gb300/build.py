@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libsagefp4.so")
-SOURCES = ["quant.cu", "attn.cu", "probe.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["quant.cu", "attn.cu", "probe.cu", "api.cu", "noalloc.cu", "host_pipe.cu"]
 HEADERS = ["ptx.cuh", "layout.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

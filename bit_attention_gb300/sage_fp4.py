@@ -68,6 +68,8 @@ def load(build: bool = True) -> ctypes.CDLL:
                 "sage_fp4_cvt_probe": (i, [u32, u32, vp, vp, vp]),
                 "sage_fp4_mma_probe": (i, [vp, vp, vp, vp, i, i, i, vp, vp, vp]),
                 "sage_fp4_attention_noalloc": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, vp]),
+                "sage_fp4_host_workspace_bytes": (sz, [i, i, i, i]),
+                "sage_fp4_attention_host": (i, [vp, vp, vp, vp, i, i, i, i, i, vp, sz, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -137,6 +139,16 @@ def sage_fp4_attention_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, status_ptr, B, H, N, 
     """One-call quantize + attention that allocates nothing (fixed device scratch)."""
     return load().sage_fp4_attention_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, status_ptr, B, H, N, D,
                                              int(causal), stream)
+
+
+def sage_fp4_host_workspace_bytes(B: int, H: int, N: int, D: int) -> int:
+    return load().sage_fp4_host_workspace_bytes(B, H, N, D)
+
+
+def sage_fp4_attention_host(q_ptr, k_ptr, v_ptr, o_ptr, B, H, N, D, causal, ws_ptr, ws_bytes,
+                            status_ptr, stream) -> int:
+    return load().sage_fp4_attention_host(q_ptr, k_ptr, v_ptr, o_ptr, B, H, N, D, int(causal),
+                                          ws_ptr, ws_bytes, status_ptr, stream)
 
 
 # ------------------------------------------------------------- torch conveniences
@@ -245,3 +257,57 @@ def attn_fwd(qkv: QuantizedQKV, causal: bool = False, out=None, stream=None):
 def attention(q, k, v, causal: bool = False, stream=None):
     """Quantize and attend: bf16 Q, K, V [B,H,N,D] -> bf16 O."""
     return attn_fwd(quantize_qkv(q, k, v, stream=stream), causal, stream=stream)
+
+
+class HostWorkspace:
+    """Device workspace and status word of ``attention_host`` for one problem size."""
+
+    def __init__(self, B: int, H: int, N: int, D: int, device=None):
+        import torch
+        self.B, self.H, self.N, self.D = B, H, N, D
+        self.nbytes = sage_fp4_host_workspace_bytes(B, H, N, D)
+        if self.nbytes == 0:
+            raise SageFp4Error(EINVAL, f"host workspace for B={B} H={H} N={N} D={D}")
+        dev = device or "cuda"
+        self.workspace = torch.empty(self.nbytes, dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(4, dtype=torch.int32, device=dev)
+
+    def get_status(self, stream=None) -> int:
+        """Synchronise, return the status word and reset it to 0."""
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream()
+        s.synchronize()
+        v = int(self.status[0].item())
+        self.status.zero_()
+        return v
+
+
+def _check_host(x, B, H, N, D, name):
+    import torch
+    if x.dtype != torch.bfloat16 or x.is_cuda or not x.is_contiguous():
+        raise SageFp4Error(EINVAL, f"{name} must be a contiguous bf16 CPU tensor")
+    if tuple(x.shape) != (B, H, N, D):
+        raise SageFp4Error(EINVAL, f"{name} has shape {tuple(x.shape)}, expected {(B, H, N, D)}")
+
+
+def attention_host(q, k, v, causal: bool = False, out=None, workspace: HostWorkspace | None = None,
+                   stream=None):
+    """Quantize and attend with Q, K, V and O in host memory (pin them for overlap).
+
+    Asynchronous on ``stream`` like the device calls: synchronise it before
+    reading ``out``."""
+    import torch
+    B, H, N, D = q.shape
+    for x, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _check_host(x, B, H, N, D, nm)
+    if out is None:
+        out = torch.empty((B, H, N, D), dtype=torch.bfloat16, pin_memory=True)
+    else:
+        _check_host(out, B, H, N, D, "out")
+    if workspace is None:
+        workspace = HostWorkspace(B, H, N, D)
+    rc = sage_fp4_attention_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, N,
+                                 D, causal, workspace.workspace.data_ptr(), workspace.nbytes,
+                                 workspace.status.data_ptr(), _stream(stream))
+    _check(rc, "sage_fp4_attention_host")
+    return out

@@ -24,10 +24,12 @@
  *   - The softmax scale is 1/sqrt(D).  Causal: key j is visible to query i
  *     iff j <= i (queries and keys share one sequence).
  *   - Every pointer passed to a computing call is DEVICE memory owned by the
- *     caller; the library allocates nothing, frees nothing and keeps no global
- *     state besides per-device caches of kernel attributes.  All computing
- *     calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
- *     default stream).
+ *     caller, except the q, k, v, o of sage_fp4_attention_host (host memory).
+ *     The library allocates no memory, frees nothing and keeps no global state
+ *     besides per-device caches of kernel attributes and, once
+ *     sage_fp4_attention_host has run on a device, that call's three streams
+ *     and ten events.  All computing calls are asynchronous on `stream` (a
+ *     cudaStream_t; NULL = legacy default stream).
  *   - Inputs must be finite; NaN or Inf inputs give unspecified results.
  *   - Return value: SAGE_FP4_OK or a negative status.  Argument errors are
  *     detected on the host before anything is launched.  Errors found while a
@@ -171,6 +173,43 @@ const char *sage_fp4_strerror(int status);
 int sage_fp4_attention_noalloc(const void *q, const void *k, const void *v, void *o,
                                int32_t *status, int B, int H, int N, int D, int causal,
                                void *stream);
+
+/* ---- the whole path from host memory -------------------------------------- */
+
+/* Bytes of device workspace sage_fp4_attention_host needs for this problem
+ * (0 if the sizes are invalid).  About 3 * (4 * c * N * D * 2) bytes plus
+ * three sets of quantized operands, c = ceil(B*H / 8) heads per chunk. */
+size_t sage_fp4_host_workspace_bytes(int B, int H, int N, int D);
+
+/* No counterpart in the pages: a convenience of this library for callers
+ * whose tensors live in host memory.  The same result as
+ * sage_fp4_quantize_qkv followed by sage_fp4_attn_fwd (bit-identical O), with
+ * q, k, v (bf16 [B,H,N,D], contiguous) read from host memory and o written to
+ * host memory.  Page-locked (pinned) host memory lets the copies overlap the
+ * kernels; pageable memory works, but its copies do not overlap.
+ *
+ * The B*H heads are cut into chunks of ceil(B*H / 8) heads and pipelined
+ * through three staging slots of `workspace` on three streams of the
+ * library's own (copy in / quantize + attention / copy out), so that while
+ * chunk i computes, chunk i+1 is copied in and chunk i-1 copied out.  The
+ * call forks from `stream` (the pipeline starts after the work queued on
+ * `stream` before it) and joins back into it (work queued on `stream` after
+ * it starts once o is complete in host memory); it is therefore asynchronous
+ * like every other call, and usable under stream capture.  Calls on one
+ * device are serialised on the host while they enqueue.
+ *
+ * workspace: device memory of at least sage_fp4_host_workspace_bytes bytes,
+ *   256-byte aligned; its contents need no initialisation.  Calls sharing a
+ *   workspace must be ordered (one stream, or events).
+ * status: one int32 of device memory, zero-initialised by the caller, set to
+ *   SAGE_FP4_ETIMEOUT if a kernel's bounded wait gives up (later chunks then
+ *   skip their work).
+ * Returns SAGE_FP4_EINVAL for bad arguments (checked before anything is
+ * queued), SAGE_FP4_ECUDA if queuing a copy, event or kernel failed (work
+ * already queued then still runs; synchronise before reusing the buffers). */
+int sage_fp4_attention_host(const void *q, const void *k, const void *v, void *o, int B, int H,
+                            int N, int D, int causal, void *workspace, size_t workspace_bytes,
+                            int32_t *status, void *stream);
 
 /* ---- diagnostics (tests use these to pin the device primitives) ---------- */
 

@@ -94,3 +94,39 @@ def test_strerror():
     for code in (S.OK, S.EINVAL, S.ECUDA, S.ETIMEOUT, S.EUNSUPPORTED):
         assert S.strerror(code) and S.strerror(code) != "unknown status"
     assert S.strerror(12345) == "unknown status"
+
+
+def test_host_workspace_bytes():
+    # three slots, each: staged q, k, v, o of c = ceil(B*H/8) heads (256-aligned)
+    # plus the quantized operands of c heads
+    B, H, N, D = 4, 32, 4096, 128
+    c = -(-B * H // 8)
+    stage = (c * N * D * 2 + 255) // 256 * 256
+    qws = (S.sage_fp4_workspace_bytes(1, c, N, D) + 255) // 256 * 256
+    assert S.sage_fp4_host_workspace_bytes(B, H, N, D) == 3 * (4 * stage + qws)
+    # fewer heads than chunks: one head per chunk
+    c1 = (300 * 64 * 2 + 255) // 256 * 256
+    assert S.sage_fp4_host_workspace_bytes(1, 3, 300, 64) == 3 * (4 * c1 + S.sage_fp4_workspace_bytes(1, 1, 300, 64))
+    assert S.sage_fp4_host_workspace_bytes(1, 1, 17, 96) == 0
+    assert S.sage_fp4_host_workspace_bytes(-1, 1, 17, 64) == 0
+    assert S.sage_fp4_host_workspace_bytes(0, 4, 17, 64) == 256
+
+
+def test_host_pipeline_rejects_bad_arguments():
+    B, H, N, D = 1, 2, 512, 128
+    ws = S.sage_fp4_host_workspace_bytes(B, H, N, D)
+    good = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, B=B, H=H, N=N, D=D, causal=0,
+                ws=0x7000_0000, nbytes=ws, status=0x5000)
+
+    def call(**kw):
+        a = dict(good)
+        a.update(kw)
+        return S.sage_fp4_attention_host(a["q"], a["k"], a["v"], a["o"], a["B"], a["H"], a["N"],
+                                         a["D"], a["causal"], a["ws"], a["nbytes"], a["status"], None)
+
+    for bad in (dict(q=0), dict(o=0), dict(status=0), dict(status=0x5002), dict(ws=0),
+                dict(ws=0x7000_0010), dict(nbytes=ws - 1), dict(causal=2), dict(D=96), dict(N=-1)):
+        assert call(**bad) == S.EINVAL, bad
+    # nothing to compute: OK without touching the device
+    assert call(B=0) == S.OK
+    assert call(N=0, nbytes=256) == S.OK
