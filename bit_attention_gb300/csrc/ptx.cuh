@@ -50,21 +50,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// As mbar_try_wait, with a bound on how long the thread may stay suspended
-// waiting for the phase (nanoseconds); it resumes as soon as the phase
-// completes.
-__device__ __forceinline__ bool mbar_try_wait_ns(uint32_t bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
-
 // Non-blocking probe: has the phase with this parity completed?
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -141,18 +126,6 @@ __device__ __forceinline__ void mma_nvfp4(uint32_t d_tmem, uint64_t a_desc, uint
       " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
       : "memory");
-}
-
-// True in exactly one active lane of the warp (the lowest); every lane of
-// the warp must execute it.
-__device__ __forceinline__ bool elect_one() {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "elect.sync _|p, 0xffffffff;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r));
-  return r != 0;
 }
 
 // Arrive on an mbarrier once every tcgen05 operation this thread issued so far
