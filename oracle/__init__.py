@@ -15,6 +15,7 @@ of 8-Bit Training".  See ``sage_oracle.c`` for the step-by-step definition.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 import threading
@@ -104,12 +105,12 @@ def _declare(L):
     L.sor_quantize_v.argtypes = [u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p, u8p]
     L.sor_attention.restype = ctypes.c_int
     L.sor_attention.argtypes = [u8p, u8p, u8p, u8p, u8p, u8p, ctypes.c_int, ctypes.c_int,
-                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                i64p, ctypes.c_int64, f64p, f64p, f64p]
+                                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                                ctypes.c_int, i64p, ctypes.c_int64, f64p, f64p, f64p]
     L.sor_attention_exact.restype = ctypes.c_int
     L.sor_attention_exact.argtypes = [u16p, u16p, u16p, ctypes.c_int, ctypes.c_int,
-                                      ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int64,
-                                      f64p]
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_double, i64p,
+                                      ctypes.c_int64, f64p]
     L.sor_num_threads.restype = ctypes.c_int
 
 
@@ -200,9 +201,16 @@ class Quantized:
 
 
 # ------------------------------------------------------------- attention
-def attention(qz: Quantized, causal: bool, pmode: str = "tile", rows=None, kv_tile: int = 128):
+def default_scale(D: int) -> float:
+    """Softmax scale when none is given: 1/sqrt(D) (the pages name none)."""
+    return 1.0 / math.sqrt(D)
+
+
+def attention(qz: Quantized, causal: bool, pmode: str = "tile", rows=None, kv_tile: int = 128,
+              scale: float | None = None):
     """Tiled FP4 attention. Returns (O [nrows,D] float64, l [nrows], m [nrows])."""
     BH, N, D = qz.BH, qz.N, qz.D
+    scale = default_scale(D) if scale is None else float(scale)
     if rows is None:
         rows_a = None
         nrows = BH * N
@@ -215,7 +223,7 @@ def attention(qz: Quantized, causal: bool, pmode: str = "tile", rows=None, kv_ti
     rc = lib().sor_attention(
         _p(qz.qc, ctypes.c_uint8), _p(qz.qs, ctypes.c_uint8), _p(qz.kc, ctypes.c_uint8),
         _p(qz.ks, ctypes.c_uint8), _p(qz.vc, ctypes.c_uint8), _p(qz.vs, ctypes.c_uint8),
-        BH, N, D, int(bool(causal)), PMODE[pmode], kv_tile,
+        BH, N, D, int(bool(causal)), scale, PMODE[pmode], kv_tile,
         _p(rows_a, ctypes.c_int64) if rows_a is not None else None, nrows,
         _p(out, ctypes.c_double), _p(ol, ctypes.c_double), _p(om, ctypes.c_double))
     if rc != 0:
@@ -223,8 +231,10 @@ def attention(qz: Quantized, causal: bool, pmode: str = "tile", rows=None, kv_ti
     return out, ol, om
 
 
-def attention_exact(q, k, v, BH: int, N: int, D: int, causal: bool, rows=None):
-    """Unquantized softmax(QK^T/sqrt(D))V in float64 from the bf16 inputs."""
+def attention_exact(q, k, v, BH: int, N: int, D: int, causal: bool, rows=None,
+                    scale: float | None = None):
+    """Unquantized softmax(scale QK^T)V in float64 from the bf16 inputs (scale 1/sqrt(D))."""
+    scale = default_scale(D) if scale is None else float(scale)
     q, k, v = _u16(q).reshape(-1), _u16(k).reshape(-1), _u16(v).reshape(-1)
     if rows is None:
         rows_a, nrows = None, BH * N
@@ -234,7 +244,7 @@ def attention_exact(q, k, v, BH: int, N: int, D: int, causal: bool, rows=None):
     out = np.empty((nrows, D), np.float64)
     rc = lib().sor_attention_exact(
         _p(q, ctypes.c_uint16), _p(k, ctypes.c_uint16), _p(v, ctypes.c_uint16), BH, N, D,
-        int(bool(causal)), _p(rows_a, ctypes.c_int64) if rows_a is not None else None, nrows,
+        int(bool(causal)), scale, _p(rows_a, ctypes.c_int64) if rows_a is not None else None, nrows,
         _p(out, ctypes.c_double))
     if rc != 0:
         raise ValueError("oracle exact attention rejected its arguments")

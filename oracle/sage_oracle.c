@@ -224,8 +224,9 @@ static void init_tables(void) {
 #define SOR_MAX_D 256
 #define SOR_MAX_TILE 512
 
-/* One query row.  Softmax scale 1/sqrt(D) (the pages give no scale; this is
- * the standard one).  Per KV tile, in ascending order:
+/* One query row.  Softmax scale `scale` (the pages give none; callers pass
+ * 1/sqrt(D), the standard one, unless they ask for another); below,
+ * "/sqrt(D)" stands for "* scale".  Per KV tile, in ascending order:
  *   S_j    = sum_g sQ_g * sK_jg * sum_{k in g} q_k * k_jk   (decoded, exact)
  *   masked keys (j >= N, or j > i when causal) get S = -inf
  *   t      = max_j S_j over the tile, m_new = max(m_old, t)
@@ -241,8 +242,9 @@ static void init_tables(void) {
  * and finally O = acc / l. */
 static void attend_row(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const uint8_t *ks,
                        const uint8_t *vc, const uint8_t *vs, int N, int N_pad, int D, int causal,
-                       int pmode, int kv_tile, int i, double *out, double *out_l, double *out_m) {
-  const double isd = 1.0 / sqrt((double)D);
+                       double scale, int pmode, int kv_tile, int i, double *out, double *out_l,
+                       double *out_m) {
+  const double isd = scale;
   const int G = D / 16;
   double qv[SOR_MAX_D];
   double acc[SOR_MAX_D];
@@ -314,9 +316,10 @@ static void attend_row(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, 
 
 int sor_attention(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const uint8_t *ks,
                   const uint8_t *vc, const uint8_t *vs, int BH, int N, int D, int causal,
-                  int pmode, int kv_tile, const int64_t *rows, int64_t nrows, double *out,
-                  double *out_l, double *out_m) {
-  if (D % 16 || D > SOR_MAX_D || kv_tile % 16 || kv_tile > SOR_MAX_TILE || kv_tile <= 0 || N < 1)
+                  double scale, int pmode, int kv_tile, const int64_t *rows, int64_t nrows,
+                  double *out, double *out_l, double *out_m) {
+  if (D % 16 || D > SOR_MAX_D || kv_tile % 16 || kv_tile > SOR_MAX_TILE || kv_tile <= 0 || N < 1 ||
+      !(scale > 0.0) || isinf(scale))
     return -1;
   init_tables();
   int N_pad = round_up(N, 128);
@@ -329,17 +332,18 @@ int sor_attention(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const
     attend_row(qc + (size_t)bh * N_pad * (D / 2), qs + (size_t)bh * N_pad * (D / 16),
                kc + (size_t)bh * N_pad * (D / 2), ks + (size_t)bh * N_pad * (D / 16),
                vc + (size_t)bh * D * (N_pad / 2), vs + (size_t)bh * D * (N_pad / 16), N, N_pad, D,
-               causal, pmode, kv_tile, i, out + (size_t)r * D, out_l ? out_l + r : 0,
+               causal, scale, pmode, kv_tile, i, out + (size_t)r * D, out_l ? out_l + r : 0,
                out_m ? out_m + r : 0);
   }
   return 0;
 }
 
-/* Exact softmax(Q K^T / sqrt(D)) V in double, from the bf16 inputs. */
+/* Exact softmax(scale * Q K^T) V in double, from the bf16 inputs. */
 int sor_attention_exact(const uint16_t *q, const uint16_t *k, const uint16_t *v, int BH, int N,
-                        int D, int causal, const int64_t *rows, int64_t nrows, double *out) {
-  if (N < 1 || D < 1) return -1;
-  const double isd = 1.0 / sqrt((double)D);
+                        int D, int causal, double scale, const int64_t *rows, int64_t nrows,
+                        double *out) {
+  if (N < 1 || D < 1 || !(scale > 0.0) || isinf(scale)) return -1;
+  const double isd = scale;
   int64_t total = rows ? nrows : (int64_t)BH * N;
 #pragma omp parallel
   {

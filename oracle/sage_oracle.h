@@ -52,18 +52,21 @@ void sor_quantize_rows(const uint16_t *x, int BH, int N, int D, uint8_t *codes, 
 /* V: bf16 bits [BH][N][D] -> V^T codes/scales, groups along tokens */
 void sor_quantize_v(const uint16_t *v, int BH, int N, int D, uint8_t *codes, uint8_t *scales);
 
-/* Tiled FP4 attention over the quantized tensors.
+/* Tiled FP4 attention over the quantized tensors, softmax scale `scale`
+ * (> 0; 1/sqrt(D) is the standard one).
  * pmode 0 = TILE (level 1 normalises each KV tile's row segment so that its
  * max is 448*6), pmode 1 = RUNNING (normalised against the running row max).
  * rows: flat row ids bh*N + i (NULL = all BH*N rows).  out: [nrows][D]. */
 int sor_attention(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const uint8_t *ks,
                   const uint8_t *vc, const uint8_t *vs, int BH, int N, int D, int causal,
-                  int pmode, int kv_tile, const int64_t *rows, int64_t nrows, double *out,
-                  double *out_l, double *out_m);
+                  double scale, int pmode, int kv_tile, const int64_t *rows, int64_t nrows,
+                  double *out, double *out_l, double *out_m);
 
-/* Exact attention, unquantized, from the bf16 inputs, in double. */
+/* Exact attention softmax(scale * Q K^T) V, unquantized, from the bf16
+ * inputs, in double. */
 int sor_attention_exact(const uint16_t *q, const uint16_t *k, const uint16_t *v, int BH, int N,
-                        int D, int causal, const int64_t *rows, int64_t nrows, double *out);
+                        int D, int causal, double scale, const int64_t *rows, int64_t nrows,
+                        double *out);
 
 int sor_num_threads(void);
 

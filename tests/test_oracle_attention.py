@@ -10,6 +10,10 @@ The pages print no worked example, so the oracle is pinned by mathematics:
 * the online-softmax identity l = sum_j exp((S_j - m)/sqrt(D)) with S from a
   numpy matmul of the decoded operands;
 * TILE and RUNNING level-1 modes coincide when there is one KV tile;
+* the softmax scale enters only as a factor on S: attending to 2Q (whose
+  quantization is Q's with every scale doubled, exactly) at scale c gives the
+  same bits as attending to Q at scale 2c, and the exact path matches numpy
+  softmax at any scale;
 * the measured error against unquantized float64 attention on tiny shapes;
 * mutation checks: plausible mistakes planted in a copy of the oracle source
   each make at least one of these pins fail.
@@ -30,10 +34,10 @@ def bf16(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
 
 
-def softmax_attention(q, k, v, causal):
-    """float64 reference: softmax(q k^T / sqrt(D)) v for [BH,N,D] arrays."""
+def softmax_attention(q, k, v, causal, scale=None):
+    """float64 reference: softmax(scale q k^T) v for [BH,N,D] arrays (scale 1/sqrt(D))."""
     BH, N, D = q.shape
-    s = np.einsum("bid,bjd->bij", q, k) / np.sqrt(D)
+    s = np.einsum("bid,bjd->bij", q, k) * (1.0 / np.sqrt(D) if scale is None else scale)
     if causal:
         s = np.where(np.tril(np.ones((N, N), bool))[None], s, -np.inf)
     s = s - s.max(-1, keepdims=True)
@@ -200,6 +204,40 @@ def test_against_unquantized_attention(case):
         assert cos >= cos_min and rel_l1 <= rel_max, (pmode, cos, rel_l1)
 
 
+@pytest.mark.parametrize("D,causal", [(64, False), (128, True)])
+def test_scale_is_a_factor_on_scores(D, causal):
+    """Q -> 2Q doubles every E4M3 scale of Q exactly and keeps its codes, so S
+    doubles exactly; attention at scale c on 2Q must equal attention at scale
+    2c on Q bit for bit, in the tiled and in the exact oracle."""
+    from bit_attention_gb300.synth import make_qkv
+    BH, N = 2, 300
+    q, k, v = make_qkv(1, BH, N, D, "iid", seed=5)
+    q2 = (q.float() * 2).to(torch.bfloat16)
+    qz, qz2 = oracle.Quantized(q, k, v, BH, N, D), oracle.Quantized(q2, k, v, BH, N, D)
+    assert np.array_equal(qz.qc, qz2.qc)
+    e4 = np.array([oracle.e4m3_value(b) for b in range(256)])
+    assert np.array_equal(e4[qz2.qs], 2 * e4[qz.qs])
+    c = 1.0 / np.sqrt(D)
+    o_twice_q = oracle.attention(qz2, causal, scale=c)[0]
+    o_twice_scale = oracle.attention(qz, causal, scale=2 * c)[0]
+    assert np.array_equal(o_twice_q, o_twice_scale)
+    assert not np.array_equal(o_twice_scale, oracle.attention(qz, causal)[0])
+    e_twice_q = oracle.attention_exact(q2, k, v, BH, N, D, causal, scale=c)
+    e_twice_scale = oracle.attention_exact(q, k, v, BH, N, D, causal, scale=2 * c)
+    assert np.array_equal(e_twice_q, e_twice_scale)
+
+
+@pytest.mark.parametrize("scale", [0.03, 0.5])
+def test_exact_attention_matches_numpy_at_any_scale(scale):
+    from bit_attention_gb300.synth import make_qkv
+    BH, N, D = 2, 200, 64
+    q, k, v = make_qkv(1, BH, N, D, "iid", seed=9)
+    got = oracle.attention_exact(q, k, v, BH, N, D, True, scale=scale)
+    want = softmax_attention(*(t.float().numpy().reshape(BH, N, D).astype(np.float64) for t in (q, k, v)),
+                             True, scale=scale)
+    assert np.abs(got - want.reshape(-1, D)).max() < 1e-10
+
+
 # ---------------------------------------------------------------- mutations
 MUTATIONS = {
     "drop_alpha": ("acc[d] = acc[d] * alpha + sP1 * pv;", "acc[d] = acc[d] + sP1 * pv;"),
@@ -214,6 +252,8 @@ MUTATIONS = {
                         "pv += 448.0 * g_e4m3[vsrow[jg]] * part;"),
     "scale_amax_over_4": ("float q = amax / 6.0f;", "float q = amax / 4.0f;"),
     "e2m1_ties_up": ("(d == bestd && (i & 1) == 0)", "(d == bestd)"),
+    "scale_ignored": ("double *out_m) {\n  const double isd = scale;",
+                      "double *out_m) {\n  const double isd = 1.0 / sqrt((double)D);"),
 }
 
 
@@ -229,6 +269,7 @@ def all_pins():
         ("codec_ties", lambda: __import__("test_oracle_codecs").test_e2m1_ties_and_negative_zero()),
         ("group", lambda: __import__("test_oracle_codecs").test_group_quantizer_bruteforce_and_invariants()),
         ("unquantized", lambda: test_against_unquantized_attention("iid")),
+        ("scale", lambda: test_scale_is_a_factor_on_scores(64, False)),
     ]
     for name, fn in checks:
         try:
