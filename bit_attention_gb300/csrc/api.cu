@@ -111,6 +111,32 @@ CUtensorMapSwizzle swizzle_for_row(int row_bytes) {
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? SAGE_FP4_OK : SAGE_FP4_ECUDA; }
 
+// Strides of one tensor: NULL means the contiguous [B,H,N,D] layout.  Each
+// stride is >= 0 and a multiple of 8 elements (16-byte rows for the vector
+// loads, bulk copies and stores), and the largest element offset fits in 62
+// bits.
+bool strides_of(const sage_fp4_strides* in, int B, int H, int N, int D, Strides* out) {
+  if (!in) {
+    *out = contiguous_bhnd(H, N, D);
+    return true;
+  }
+  const int64_t st[3] = {in->b, in->h, in->n};
+  const int64_t dims[3] = {B, H, N};
+  int64_t last = D;
+  for (int i = 0; i < 3; ++i) {
+    if (st[i] < 0 || st[i] % 8 != 0) return false;
+    int64_t span = 0;
+    if (dims[i] > 0 && (__builtin_mul_overflow(st[i], dims[i] - 1, &span) ||
+                        __builtin_add_overflow(last, span, &last)))
+      return false;
+  }
+  if (last > (int64_t(1) << 62)) return false;
+  *out = Strides{st[0], st[1], st[2]};
+  return true;
+}
+
+bool scale_ok(float s) { return s > 0.0f && s <= 1.0e30f; }
+
 }  // namespace
 
 extern "C" {
@@ -136,29 +162,42 @@ int sage_fp4_qkv_from_workspace(void* workspace, size_t workspace_bytes, int B, 
   return SAGE_FP4_OK;
 }
 
-int sage_fp4_quantize_qkv(const void* q, const void* k, const void* v, const sage_fp4_qkv* out,
-                          int B, int H, int N, int D, void* stream) {
+int sage_fp4_quantize_qkv_strided(const void* q, const sage_fp4_strides* q_strides, const void* k,
+                                  const sage_fp4_strides* k_strides, const void* v,
+                                  const sage_fp4_strides* v_strides, const sage_fp4_qkv* out, int B,
+                                  int H, int N, int D, void* stream) {
   if (!dims_ok(B, H, N, D) || !out) return SAGE_FP4_EINVAL;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return SAGE_FP4_EINVAL;
   if (!tensor_ok(out->q) || !tensor_ok(out->k) || !tensor_ok(out->vt) || !aligned(out->status, 4))
+    return SAGE_FP4_EINVAL;
+  Strides sq, sk, sv;
+  if (!strides_of(q_strides, B, H, N, D, &sq) || !strides_of(k_strides, B, H, N, D, &sk) ||
+      !strides_of(v_strides, B, H, N, D, &sv))
     return SAGE_FP4_EINVAL;
   if (is_empty(B, H, N)) return SAGE_FP4_OK;
   int dev = check_device();
   if (dev != SAGE_FP4_OK) return dev;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int BH = B * H;
-  cudaError_t e = launch_quant_rows(q, k, out->q.codes, out->q.scales, out->k.codes, out->k.scales,
-                                    BH, N, D, st);
+  cudaError_t e = launch_quant_rows(q, k, sq, sk, out->q.codes, out->q.scales, out->k.codes,
+                                    out->k.scales, H, BH, N, D, st);
   if (e != cudaSuccess) return SAGE_FP4_ECUDA;
-  return from_cuda(launch_quant_v(v, out->vt.codes, out->vt.scales, BH, N, D, out->status, st));
+  return from_cuda(launch_quant_v(v, sv, out->vt.codes, out->vt.scales, H, BH, N, D, out->status, st));
+}
+
+int sage_fp4_quantize_qkv(const void* q, const void* k, const void* v, const sage_fp4_qkv* out,
+                          int B, int H, int N, int D, void* stream) {
+  return sage_fp4_quantize_qkv_strided(q, nullptr, k, nullptr, v, nullptr, out, B, H, N, D, stream);
 }
 
 namespace {
 
-int attn_fwd_impl(const sage_fp4_qkv* qkv, void* o, int B, int H, int N, int D, int causal, int flags,
-                  uint64_t wait_ns, void* stream) {
+int attn_fwd_impl(const sage_fp4_qkv* qkv, void* o, const sage_fp4_strides* o_strides, int B, int H,
+                  int N, int D, int causal, float scale, int flags, uint64_t wait_ns, void* stream) {
   if (!dims_ok(B, H, N, D) || !qkv_ok(qkv) || !aligned(o, 16)) return SAGE_FP4_EINVAL;
   if (causal != 0 && causal != 1) return SAGE_FP4_EINVAL;
+  Strides so;
+  if (!strides_of(o_strides, B, H, N, D, &so) || !scale_ok(scale)) return SAGE_FP4_EINVAL;
   if (is_empty(B, H, N)) return SAGE_FP4_OK;
   int dev = check_device();
   if (dev != SAGE_FP4_OK) return dev;
@@ -176,29 +215,40 @@ int attn_fwd_impl(const sage_fp4_qkv* qkv, void* o, int B, int H, int N, int D, 
   p.sfk = qkv->k.scales;
   p.sfv = qkv->vt.scales;
   p.o = o;
+  p.os = so;
   p.status = qkv->status;
+  p.H = H;
   p.BH = BH;
   p.N = N;
   p.Np = Np;
   p.causal = causal;
   p.n_qt = Np / 128;
-  p.a = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
+  p.a = static_cast<float>(1.4426950408889634 * static_cast<double>(scale));
   p.flags = flags;
   p.wait_ns = wait_ns;
   return from_cuda(launch_attn(tq, tk, tv, p, D, static_cast<cudaStream_t>(stream)));
 }
 
+// The softmax scale when the caller gives none: 1/sqrt(D).
+float default_scale(int D) { return static_cast<float>(1.0 / sqrt(static_cast<double>(D > 0 ? D : 1))); }
+
 }  // namespace
+
+int sage_fp4_attn_fwd_ex(const sage_fp4_qkv* qkv, void* o, const sage_fp4_strides* o_strides, int B,
+                         int H, int N, int D, int causal, float softmax_scale, void* stream) {
+  return attn_fwd_impl(qkv, o, o_strides, B, H, N, D, causal, softmax_scale, 0, kAttnWaitNs, stream);
+}
 
 int sage_fp4_attn_fwd(const sage_fp4_qkv* qkv, void* o, int B, int H, int N, int D, int causal,
                       void* stream) {
-  return attn_fwd_impl(qkv, o, B, H, N, D, causal, 0, kAttnWaitNs, stream);
+  return attn_fwd_impl(qkv, o, nullptr, B, H, N, D, causal, default_scale(D), 0, kAttnWaitNs, stream);
 }
 
 int sage_fp4_attn_fwd_stall_test(const sage_fp4_qkv* qkv, void* o, int B, int H, int N, int D,
                                  int causal, uint64_t wait_limit_ns, void* stream) {
   if (wait_limit_ns < 1000000ull || wait_limit_ns > kAttnWaitNs) return SAGE_FP4_EINVAL;
-  return attn_fwd_impl(qkv, o, B, H, N, D, causal, kAttnWithholdK, wait_limit_ns, stream);
+  return attn_fwd_impl(qkv, o, nullptr, B, H, N, D, causal, default_scale(D), kAttnWithholdK,
+                       wait_limit_ns, stream);
 }
 
 int sage_fp4_get_status(const sage_fp4_qkv* qkv, void* stream) {

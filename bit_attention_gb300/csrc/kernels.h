@@ -8,19 +8,32 @@
 
 namespace sagefp4 {
 
-cudaError_t launch_quant_rows(const void* q, const void* k, uint8_t* qc, uint8_t* qs, uint8_t* kc,
-                              uint8_t* ks, int BH, int N, int D, cudaStream_t st);
-cudaError_t launch_quant_v(const void* v, uint8_t* vc, uint8_t* vs, int BH, int N, int D,
-                           int32_t* status, cudaStream_t st);
+// Element strides of a bf16 [B,H,N,D] tensor between batches, heads and
+// tokens; D is contiguous.  All three are multiples of 8 (16 bytes).
+struct Strides {
+  long long b, h, n;
+};
+
+// Strides of the contiguous [B,H,N,D] layout.
+inline Strides contiguous_bhnd(int H, int N, int D) {
+  return Strides{static_cast<long long>(H) * N * D, static_cast<long long>(N) * D, D};
+}
+
+cudaError_t launch_quant_rows(const void* q, const void* k, Strides sq, Strides sk, uint8_t* qc,
+                              uint8_t* qs, uint8_t* kc, uint8_t* ks, int H, int BH, int N, int D,
+                              cudaStream_t st);
+cudaError_t launch_quant_v(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, int H, int BH, int N,
+                           int D, int32_t* status, cudaStream_t st);
 
 struct AttnParams {
   const uint8_t* sfq;  // Q scales (block layout), per (b,h) N_pad*D/16 bytes
   const uint8_t* sfk;  // K scales
   const uint8_t* sfv;  // V^T scales, per (b,h) 8*N_pad bytes
-  void* o;             // bf16 [BH][N][D]
+  void* o;             // bf16 O, row (b, h, n) at element b*os.b + h*os.h + n*os.n
+  Strides os;
   int32_t* status;
-  int BH, N, Np, causal, n_qt;
-  float a;  // log2(e) / sqrt(D): softmax scale folded into exp2
+  int H, BH, N, Np, causal, n_qt;
+  float a;  // log2(e) * softmax scale: the scale folded into exp2
   int flags;           // kAttnWithholdK: failure-detection test (see below)
   uint64_t wait_ns;    // limit of every bounded wait in the kernel
 };

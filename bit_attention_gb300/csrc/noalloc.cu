@@ -137,9 +137,10 @@ extern "C" int sage_fp4_attention_noalloc(const void* q, const void* k, const vo
   const int Np = round_up_int(N, 128);
   // Every byte of the quantized operands, padding included, is rewritten by
   // the quantize kernels, so nothing left by an earlier call is read.
-  if (launch_quant_rows(q, k, base + pt.qc, base + pt.qs, base + pt.kc, base + pt.ks, BH, N, D,
-                        st) != cudaSuccess ||
-      launch_quant_v(v, base + pt.vc, base + pt.vs, BH, N, D, status, st) != cudaSuccess)
+  const Strides dense = contiguous_bhnd(H, N, D);
+  if (launch_quant_rows(q, k, dense, dense, base + pt.qc, base + pt.qs, base + pt.kc, base + pt.ks, H,
+                        BH, N, D, st) != cudaSuccess ||
+      launch_quant_v(v, dense, base + pt.vc, base + pt.vs, H, BH, N, D, status, st) != cudaSuccess)
     return SAGE_FP4_ECUDA;
   CUtensorMap tq, tk, tv;
   const CUtensorMapSwizzle qk_swz = (D == 128) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
@@ -153,7 +154,9 @@ extern "C" int sage_fp4_attention_noalloc(const void* q, const void* k, const vo
   p.sfk = base + pt.ks;
   p.sfv = base + pt.vs;
   p.o = o;
+  p.os = dense;
   p.status = status;
+  p.H = H;
   p.BH = BH;
   p.N = N;
   p.Np = Np;

@@ -79,15 +79,16 @@ __device__ __forceinline__ uint32_t pack4_bytes(uint32_t b0, uint32_t b1, uint32
 // inside one 32-row slice of the scale block layout, so a lane's scale address
 // moves by a constant from one row-step to the next.  The warp keeps all its
 // row-steps' loads in flight before it computes.  blockIdx.y selects Q (0) or
-// K (1).
+// K (1); each input has its own strides (elements, multiples of 8).
 template <int D>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ x0,
                                                          const uint4* __restrict__ x1,
+                                                         Strides t0, Strides t1,
                                                          uint8_t* __restrict__ c0,
                                                          uint8_t* __restrict__ s0,
                                                          uint8_t* __restrict__ c1,
-                                                         uint8_t* __restrict__ s1, int BH, int N,
-                                                         int Np) {
+                                                         uint8_t* __restrict__ s1, int H, int BH,
+                                                         int N, int Np) {
   constexpr int LPR = D / 8;      // lanes per row
   constexpr int RPW = 32 / LPR;   // rows per warp step
   constexpr int U = 8;            // row-steps per chunk
@@ -97,6 +98,8 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
   fill_rtab(rtab);
   __syncthreads();
   const uint4* __restrict__ x = blockIdx.y ? x1 : x0;
+  const Strides t = blockIdx.y ? t1 : t0;
+  const size_t step = static_cast<size_t>(RPW) * static_cast<size_t>(t.n / 8);  // one row-step, in uint4
   uint8_t* __restrict__ codes = blockIdx.y ? c1 : c0;
   uint8_t* __restrict__ scales = blockIdx.y ? s1 : s0;
   const int lane = threadIdx.x & 31;
@@ -110,15 +113,17 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
     const int bh = chunk / chunks_per_head;
     const int r0 = (chunk - bh * chunks_per_head) * CHUNK;
     const int n0 = r0 + rsub;
-    const uint4* __restrict__ src = x + (static_cast<size_t>(bh) * N + n0) * (D / 8) + sub;
+    const int b = bh / H, h = bh - b * H;
+    const uint4* __restrict__ src =
+        x + static_cast<size_t>((b * t.b + h * t.h + static_cast<long long>(n0) * t.n) / 8) + sub;
     uint4 raw[U];
     if (r0 + CHUNK <= N) {
 #pragma unroll
-      for (int u = 0; u < U; ++u) raw[u] = __ldcs(src + u * RPW * (D / 8));
+      for (int u = 0; u < U; ++u) raw[u] = __ldcs(src + u * step);
     } else {
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        raw[u] = (n0 + u * RPW < N) ? __ldcs(src + u * RPW * (D / 8)) : make_uint4(0u, 0u, 0u, 0u);
+        raw[u] = (n0 + u * RPW < N) ? __ldcs(src + u * step) : make_uint4(0u, 0u, 0u, 0u);
     }
     uint8_t* __restrict__ cdst = codes + (static_cast<size_t>(bh) * Np + n0) * (D / 2) + sub * 4;
     uint8_t* __restrict__ sdst =
@@ -145,15 +150,17 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
 
 // V.  Each block walks TT-token tiles of V (tile i of this block = blockIdx.x
 // + i * gridDim.x over (b,h) x tiles).  A tile is brought into shared memory
-// with one 1-D bulk copy into an NS-deep ring, so that the next NS-1 tiles
-// load while this one is quantized.  A work item is one channel pair over 32
-// tokens (two groups along tokens): it writes 16 code bytes to each of two
-// V^T rows and one 16-bit half of a scale word per row.
+// as [TT tokens][D channels] by bulk copies into an NS-deep ring, so that the
+// next NS-1 tiles load while this one is quantized: one copy of the whole
+// tile when a head's tokens are contiguous (token stride D), else one copy
+// per token row, spread over the lanes of warp 0.  A work item is one channel
+// pair over 32 tokens (two groups along tokens): it writes 16 code bytes to
+// each of two V^T rows and one 16-bit half of a scale word per row.
 template <int D, int TT, int NS>
-__global__ void __launch_bounds__(128) quant_v_kernel(const uint8_t* __restrict__ v,
+__global__ void __launch_bounds__(128) quant_v_kernel(const uint8_t* __restrict__ v, Strides sv,
                                                       uint8_t* __restrict__ vc,
-                                                      uint8_t* __restrict__ vs, int BH, int N,
-                                                      int Np, int32_t* status) {
+                                                      uint8_t* __restrict__ vs, int H, int BH,
+                                                      int N, int Np, int32_t* status) {
   static_assert(TT == 64 || TT == 128, "tile of 64 or 128 tokens");
   constexpr int TILE_BYTES = TT * D * 2;
   constexpr int ITEMS = (D / 2) * (TT / 32);
@@ -177,16 +184,26 @@ __global__ void __launch_bounds__(128) quant_v_kernel(const uint8_t* __restrict_
     const int tb = static_cast<int>(w % ntiles);
     return max(0, min(TT, N - tb * TT));
   };
+  // Called by all of warp 0.  Lane 0 announces the bytes before any copy is
+  // issued, so the phase cannot complete before every copy has landed.
+  const int lane = threadIdx.x & 31;
   auto issue = [&](long long w, int buf) {
     const int bh = static_cast<int>(w / ntiles), tb = static_cast<int>(w % ntiles);
-    const uint32_t bytes = static_cast<uint32_t>(tile_rows(w)) * D * 2;
-    mbar_arrive_expect_tx(bar0 + 8 * buf, bytes);
-    if (bytes)
-      bulk_load(smem_addr(qv_smem + buf * TILE_BYTES),
-                v + (static_cast<size_t>(bh) * N + static_cast<size_t>(tb) * TT) * D * 2, bytes,
-                bar0 + 8 * buf);
+    const int b = bh / H, h = bh - b * H;
+    const int rows = tile_rows(w);
+    const uint8_t* src =
+        v + (b * sv.b + h * sv.h + static_cast<long long>(tb) * TT * sv.n) * 2;
+    const uint32_t dst = smem_addr(qv_smem + buf * TILE_BYTES);
+    if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * buf, static_cast<uint32_t>(rows) * D * 2);
+    __syncwarp();
+    if (sv.n == D) {
+      if (lane == 0 && rows > 0) bulk_load(dst, src, static_cast<uint32_t>(rows) * D * 2, bar0 + 8 * buf);
+    } else {
+      for (int r = lane; r < rows; r += 32)
+        bulk_load(dst + r * D * 2, src + static_cast<long long>(r) * sv.n * 2, D * 2, bar0 + 8 * buf);
+    }
   };
-  if (threadIdx.x == 0)
+  if (threadIdx.x < 32)
     for (int s = 0; s < NS - 1; ++s) {
       const long long ws = blockIdx.x + static_cast<long long>(s) * gridDim.x;
       if (ws < work) issue(ws, s);
@@ -197,7 +214,7 @@ __global__ void __launch_bounds__(128) quant_v_kernel(const uint8_t* __restrict_
     const int buf = it % NS;
     // refill the slot that the last iteration released at its closing barrier
     const long long wn = w + static_cast<long long>(NS - 1) * gridDim.x;
-    if (threadIdx.x == 0 && wn < work) issue(wn, (it + NS - 1) % NS);
+    if (threadIdx.x < 32 && wn < work) issue(wn, (it + NS - 1) % NS);
     // wait for this tile (bounded: a copy that never lands sets the status)
     {
       const uint64_t t0 = globaltimer_ns();
@@ -296,8 +313,9 @@ int num_sms() {
 
 }  // namespace
 
-cudaError_t launch_quant_rows(const void* q, const void* k, uint8_t* qc, uint8_t* qs, uint8_t* kc,
-                              uint8_t* ks, int BH, int N, int D, cudaStream_t st) {
+cudaError_t launch_quant_rows(const void* q, const void* k, Strides sq, Strides sk, uint8_t* qc,
+                              uint8_t* qs, uint8_t* kc, uint8_t* ks, int H, int BH, int N, int D,
+                              cudaStream_t st) {
   const int Np = round_up_int(N, 128);
   const long long chunks = static_cast<long long>(BH) * Np / (D == 128 ? 16 : 32);  // one warp each
   long long blocks = (chunks + 7) / 8;
@@ -307,18 +325,18 @@ cudaError_t launch_quant_rows(const void* q, const void* k, uint8_t* qc, uint8_t
   dim3 grid(static_cast<unsigned>(blocks), 2);
   if (D == 128)
     quant_rows_kernel<128><<<grid, 256, 0, st>>>(static_cast<const uint4*>(q),
-                                                 static_cast<const uint4*>(k), qc, qs, kc, ks, BH,
-                                                 N, Np);
+                                                 static_cast<const uint4*>(k), sq, sk, qc, qs, kc,
+                                                 ks, H, BH, N, Np);
   else
     quant_rows_kernel<64><<<grid, 256, 0, st>>>(static_cast<const uint4*>(q),
-                                                static_cast<const uint4*>(k), qc, qs, kc, ks, BH,
-                                                N, Np);
+                                                static_cast<const uint4*>(k), sq, sk, qc, qs, kc,
+                                                ks, H, BH, N, Np);
   return cudaGetLastError();
 }
 
 template <int D, int TT, int NS>
-cudaError_t launch_quant_v_cfg(const void* v, uint8_t* vc, uint8_t* vs, int BH, int Np, int N,
-                               int32_t* status, int blocks_per_sm, cudaStream_t st) {
+cudaError_t launch_quant_v_cfg(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, int H, int BH,
+                               int Np, int N, int32_t* status, int blocks_per_sm, cudaStream_t st) {
   const long long work = static_cast<long long>(Np / TT) * BH;
   const int smem = NS * TT * D * 2;
   long long blocks = static_cast<long long>(num_sms()) * blocks_per_sm;
@@ -328,20 +346,20 @@ cudaError_t launch_quant_v_cfg(const void* v, uint8_t* vc, uint8_t* vs, int BH, 
       cudaFuncSetAttribute(quant_v_kernel<D, TT, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   quant_v_kernel<D, TT, NS><<<static_cast<unsigned>(blocks), 128, smem, st>>>(
-      static_cast<const uint8_t*>(v), vc, vs, BH, N, Np, status);
+      static_cast<const uint8_t*>(v), sv, vc, vs, H, BH, N, Np, status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_v(const void* v, uint8_t* vc, uint8_t* vs, int BH, int N, int D,
-                           int32_t* status, cudaStream_t st) {
+cudaError_t launch_quant_v(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, int H, int BH, int N,
+                           int D, int32_t* status, cudaStream_t st) {
   const int Np = round_up_int(N, 128);
   // 64-token tiles, double-buffered: 32 KB (D = 128) or 16 KB (D = 64) of
   // shared memory per block.  The per-tile arithmetic, not the copy latency,
   // sets the pace, so more resident blocks beat deeper rings (measured on
   // GB300: 5.3-5.8 TB/s at D = 128 with six blocks per SM, against 4.0-4.9 TB/s
   // with four-deep rings and two or three blocks).
-  if (D == 128) return launch_quant_v_cfg<128, 64, 2>(v, vc, vs, BH, Np, N, status, 6, st);
-  return launch_quant_v_cfg<64, 64, 2>(v, vc, vs, BH, Np, N, status, 8, st);
+  if (D == 128) return launch_quant_v_cfg<128, 64, 2>(v, sv, vc, vs, H, BH, Np, N, status, 6, st);
+  return launch_quant_v_cfg<64, 64, 2>(v, sv, vc, vs, H, BH, Np, N, status, 8, st);
 }
 
 }  // namespace sagefp4

@@ -35,6 +35,10 @@ class sage_fp4_tensor(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
 
 
+class sage_fp4_strides(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int64), ("h", ctypes.c_int64), ("n", ctypes.c_int64)]
+
+
 class sage_fp4_qkv(ctypes.Structure):
     _fields_ = [("q", sage_fp4_tensor), ("k", sage_fp4_tensor), ("vt", sage_fp4_tensor),
                 ("status", ctypes.c_void_p)]
@@ -57,11 +61,14 @@ def load(build: bool = True) -> ctypes.CDLL:
             L = ctypes.CDLL(path)
             vp, i, sz, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint32
             qp = ctypes.POINTER(sage_fp4_qkv)
+            sp = ctypes.POINTER(sage_fp4_strides)
             sig = {
                 "sage_fp4_workspace_bytes": (sz, [i, i, i, i]),
                 "sage_fp4_qkv_from_workspace": (i, [vp, sz, i, i, i, i, qp]),
                 "sage_fp4_quantize_qkv": (i, [vp, vp, vp, qp, i, i, i, i, vp]),
                 "sage_fp4_attn_fwd": (i, [qp, vp, i, i, i, i, i, vp]),
+                "sage_fp4_quantize_qkv_strided": (i, [vp, sp, vp, sp, vp, sp, qp, i, i, i, i, vp]),
+                "sage_fp4_attn_fwd_ex": (i, [qp, vp, sp, i, i, i, i, i, ctypes.c_float, vp]),
                 "sage_fp4_attn_fwd_stall_test": (i, [qp, vp, i, i, i, i, i, ctypes.c_uint64, vp]),
                 "sage_fp4_get_status": (i, [qp, vp]),
                 "sage_fp4_strerror": (ctypes.c_char_p, [i]),
@@ -110,6 +117,23 @@ def sage_fp4_attn_fwd(qkv: sage_fp4_qkv, o_ptr, B, H, N, D, causal, stream) -> i
     return load().sage_fp4_attn_fwd(ctypes.byref(qkv), o_ptr, B, H, N, D, int(causal), stream)
 
 
+def sage_fp4_quantize_qkv_strided(q_ptr, q_strides, k_ptr, k_strides, v_ptr, v_strides,
+                                  qkv: sage_fp4_qkv, B, H, N, D, stream) -> int:
+    """Strides: sage_fp4_strides or None (contiguous [B,H,N,D])."""
+    r = ctypes.byref
+    return load().sage_fp4_quantize_qkv_strided(
+        q_ptr, r(q_strides) if q_strides is not None else None, k_ptr,
+        r(k_strides) if k_strides is not None else None, v_ptr,
+        r(v_strides) if v_strides is not None else None, ctypes.byref(qkv), B, H, N, D, stream)
+
+
+def sage_fp4_attn_fwd_ex(qkv: sage_fp4_qkv, o_ptr, o_strides, B, H, N, D, causal, softmax_scale,
+                         stream) -> int:
+    return load().sage_fp4_attn_fwd_ex(ctypes.byref(qkv), o_ptr,
+                                       ctypes.byref(o_strides) if o_strides is not None else None,
+                                       B, H, N, D, int(causal), float(softmax_scale), stream)
+
+
 def sage_fp4_attn_fwd_stall_test(qkv: sage_fp4_qkv, o_ptr, B, H, N, D, causal, wait_limit_ns,
                                  stream) -> int:
     return load().sage_fp4_attn_fwd_stall_test(ctypes.byref(qkv), o_ptr, B, H, N, D, int(causal),
@@ -156,6 +180,18 @@ def _stream(stream=None) -> int:
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
+
+
+def _order_after_current(stream, *tensors):
+    """Work queued on `stream` follows the current stream's (where the tensors
+    were allocated and zeroed), and the allocator keeps the tensors' memory
+    until `stream` is done with it."""
+    import torch
+    if stream is None or stream == torch.cuda.current_stream():
+        return
+    stream.wait_stream(torch.cuda.current_stream())
+    for t in tensors:
+        t.record_stream(stream)
 
 
 def _round_up(x: int, m: int) -> int:
@@ -235,28 +271,80 @@ def quantize_qkv(q, k, v, out: QuantizedQKV | None = None, stream=None) -> Quant
         _check_input(x, B, H, N, D, nm)
     if out is None:
         out = QuantizedQKV(B, H, N, D, device=q.device)
+        _order_after_current(stream, out.workspace)
     rc = sage_fp4_quantize_qkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.struct, B, H, N, D,
                                _stream(stream))
     _check(rc, "sage_fp4_quantize_qkv")
     return out
 
 
-def attn_fwd(qkv: QuantizedQKV, causal: bool = False, out=None, stream=None):
-    """SageAttention3 FP4 attention forward over quantized operands -> bf16 [B,H,N,D]."""
+def attn_fwd(qkv: QuantizedQKV, causal: bool = False, out=None, stream=None, scale=None):
+    """SageAttention3 FP4 attention forward over quantized operands -> bf16 [B,H,N,D].
+
+    scale: softmax scale (default 1/sqrt(D))."""
     import torch
     B, H, N, D = qkv.B, qkv.H, qkv.N, qkv.D
     if out is None:
         out = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=qkv.workspace.device)
     else:
         _check_input(out, B, H, N, D, "out")
-    rc = sage_fp4_attn_fwd(qkv.struct, out.data_ptr(), B, H, N, D, causal, _stream(stream))
+    if scale is None:
+        rc = sage_fp4_attn_fwd(qkv.struct, out.data_ptr(), B, H, N, D, causal, _stream(stream))
+    else:
+        rc = sage_fp4_attn_fwd_ex(qkv.struct, out.data_ptr(), None, B, H, N, D, causal, scale,
+                                  _stream(stream))
     _check(rc, "sage_fp4_attn_fwd")
     return out
 
 
-def attention(q, k, v, causal: bool = False, stream=None):
-    """Quantize and attend: bf16 Q, K, V [B,H,N,D] -> bf16 O."""
-    return attn_fwd(quantize_qkv(q, k, v, stream=stream), causal, stream=stream)
+LAYOUTS = ("HND", "NHD")
+
+
+def _bhnd(x, layout: str, name: str):
+    """(B, H, N, D) and the element strides of a bf16 CUDA tensor in `layout`
+    (HND = [B,H,N,D], NHD = [B,N,H,D]); any strides with a contiguous D axis."""
+    import torch
+    if layout not in LAYOUTS:
+        raise SageFp4Error(EINVAL, f"layout must be one of {LAYOUTS}, not {layout!r}")
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 4 or x.stride(3) != 1:
+        raise SageFp4Error(EINVAL, f"{name} must be a 4-D bf16 CUDA tensor with a contiguous last axis")
+    if layout == "HND":
+        (B, H, N, D), (sb, sh, sn) = x.shape, x.stride()[:3]
+    else:
+        (B, N, H, D), (sb, sn, sh) = x.shape, x.stride()[:3]
+    return (B, H, N, D), sage_fp4_strides(sb, sh, sn)
+
+
+def attention(q, k, v, causal: bool = False, scale=None, layout: str = "HND", out=None,
+              stream=None):
+    """Plug-and-play SageAttention3 FP4 attention: bf16 Q, K, V -> bf16 O.
+
+    layout: "HND" ([B,H,N,D]) or "NHD" ([B,N,H,D]); the tensors may be any
+    views whose last axis is contiguous (e.g. slices of a packed QKV tensor),
+    with 16-byte aligned rows.  scale: softmax scale (default 1/sqrt(D)).
+    O is a new contiguous tensor in `layout` unless `out` is given.
+    Quantization runs in a temporary workspace; three kernel launches."""
+    import torch
+    shape, sq = _bhnd(q, layout, "q")
+    B, H, N, D = shape
+    for x, nm in ((k, "k"), (v, "v")):
+        if _bhnd(x, layout, nm)[0] != shape:
+            raise SageFp4Error(EINVAL, f"{nm} has shape {tuple(x.shape)}, q has {tuple(q.shape)}")
+    sk, sv = _bhnd(k, layout, "k")[1], _bhnd(v, layout, "v")[1]
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    elif _bhnd(out, layout, "out")[0] != shape:
+        raise SageFp4Error(EINVAL, f"out has shape {tuple(out.shape)}, q has {tuple(q.shape)}")
+    so = _bhnd(out, layout, "out")[1]
+    z = QuantizedQKV(B, H, N, D, device=q.device)
+    _order_after_current(stream, z.workspace, out)
+    st = _stream(stream)
+    _check(sage_fp4_quantize_qkv_strided(q.data_ptr(), sq, k.data_ptr(), sk, v.data_ptr(), sv, z.struct,
+                                         B, H, N, D, st), "sage_fp4_quantize_qkv_strided")
+    sc = 1.0 / (D ** 0.5) if scale is None else float(scale)
+    _check(sage_fp4_attn_fwd_ex(z.struct, out.data_ptr(), so, B, H, N, D, causal, sc, st),
+           "sage_fp4_attn_fwd_ex")
+    return out
 
 
 class HostWorkspace:

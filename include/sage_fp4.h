@@ -91,6 +91,15 @@ typedef struct sage_fp4_qkv {
   int32_t *status;    /* one int32 in device memory, zero-initialised by the caller */
 } sage_fp4_qkv;
 
+/* Element strides of a bf16 [B,H,N,D] tensor whose D axis is contiguous:
+ * element (b, h, n, d) is at b*b_stride + h*h_stride + n*n_stride + d.  Each
+ * stride is >= 0 and a multiple of 8 (16 bytes).  Calls that take a pointer
+ * to strides read NULL as the contiguous [B,H,N,D] layout; [B,N,H,D] (NHD) is
+ * {N*H*D, D, H*D}; Q of a packed [B,N,3,H,D] QKV tensor is {3*N*H*D, D, 3*H*D}. */
+typedef struct sage_fp4_strides {
+  int64_t b, h, n;
+} sage_fp4_strides;
+
 /* Bytes of one device buffer that holds all quantized operands plus the status
  * word, each sub-buffer 256-byte aligned.  0 if the sizes are invalid. */
 size_t sage_fp4_workspace_bytes(int B, int H, int N, int D);
@@ -110,6 +119,18 @@ int sage_fp4_qkv_from_workspace(void *workspace, size_t workspace_bytes, int B, 
 int sage_fp4_quantize_qkv(const void *q, const void *k, const void *v, const sage_fp4_qkv *out,
                           int B, int H, int N, int D, void *stream);
 
+/* sage_fp4_quantize_qkv for inputs in any layout with a contiguous D axis:
+ * q, k and v each with its own strides (NULL = contiguous [B,H,N,D]); 16-byte
+ * aligned device memory.  The quantized operands are the same as for the
+ * contiguous copies of the inputs, bit for bit.  SAGE_FP4_EINVAL for a
+ * negative or unaligned stride or offsets beyond 2^62 elements.  No
+ * counterpart in the pages, which describe no API (the plug-and-play use of
+ * the abstract). */
+int sage_fp4_quantize_qkv_strided(const void *q, const sage_fp4_strides *q_strides, const void *k,
+                                  const sage_fp4_strides *k_strides, const void *v,
+                                  const sage_fp4_strides *v_strides, const sage_fp4_qkv *out,
+                                  int B, int H, int N, int D, void *stream);
+
 /* Attention forward over quantized operands: O = softmax(Q K^T / sqrt(D)) V
  * computed by the SageAttention3 FP4 method (block-scaled FP4 MMAs with FP32
  * accumulation; online softmax over KV tiles of 128 keys fused with two-level
@@ -118,6 +139,16 @@ int sage_fp4_quantize_qkv(const void *q, const void *k, const void *v, const sag
  * One kernel launch on `stream`.  Kernel-time failures set *qkv->status. */
 int sage_fp4_attn_fwd(const sage_fp4_qkv *qkv, void *o, int B, int H, int N, int D, int causal,
                       void *stream);
+
+/* sage_fp4_attn_fwd with an explicit softmax scale, O = softmax(softmax_scale
+ * * Q K^T) V, and O written through o_strides (NULL = contiguous [B,H,N,D];
+ * the rows of O must not overlap).  softmax_scale must be > 0 and at most
+ * 1e30 (sage_fp4_attn_fwd uses 1/sqrt(D)); anything else is SAGE_FP4_EINVAL.
+ * The scale multiplies S before the exponentials of the online softmax and of
+ * the first P-quantization level (the pages give the method no scale; this is
+ * the one a drop-in attention takes). */
+int sage_fp4_attn_fwd_ex(const sage_fp4_qkv *qkv, void *o, const sage_fp4_strides *o_strides, int B,
+                         int H, int N, int D, int causal, float softmax_scale, void *stream);
 
 /* No counterpart in the pages: the failure-detection test of the attention
  * kernel's bounded waits.  The same launch as sage_fp4_attn_fwd, except that

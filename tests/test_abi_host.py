@@ -130,3 +130,37 @@ def test_host_pipeline_rejects_bad_arguments():
     # nothing to compute: OK without touching the device
     assert call(B=0) == S.OK
     assert call(N=0, nbytes=256) == S.OK
+
+
+def test_strided_quantize_and_scaled_attention_reject_bad_arguments():
+    q = _qkv()
+    B, H, N, D = 1, 2, 512, 128
+
+    def quant(sq=None, sk=None, sv=None):
+        return S.sage_fp4_quantize_qkv_strided(0x1000, sq, 0x2000, sk, 0x3000, sv, q, B, H, N, D, None)
+
+    nhd = S.sage_fp4_strides(N * H * D, D, H * D)
+    for bad in (S.sage_fp4_strides(N * H * D, D, H * D + 4),   # 8-byte rows
+                S.sage_fp4_strides(-8, D, H * D),               # negative
+                S.sage_fp4_strides(N * H * D, 1 << 62, H * D)):  # offsets past 2^62
+        assert quant(sq=bad) == S.EINVAL
+        assert quant(sv=bad) == S.EINVAL
+    assert S.sage_fp4_quantize_qkv_strided(0x1000, nhd, 0x2000, nhd, 0x3000, nhd, q, 0, H, N, D, None) == S.OK
+
+    def attn(scale, so=None, causal=0):
+        return S.sage_fp4_attn_fwd_ex(q, 0x4000, so, B, H, N, D, causal, scale, None)
+
+    for bad in (0.0, -0.1, float("inf"), float("nan"), 1e31):
+        assert attn(bad) == S.EINVAL, bad
+    assert attn(0.1, so=S.sage_fp4_strides(N * H * D, D, 12)) == S.EINVAL
+    assert S.sage_fp4_attn_fwd_ex(q, 0x4000, nhd, 0, H, N, D, 0, 0.1, None) == S.OK
+
+
+def test_torch_op_is_registered_with_a_fake():
+    import torch
+    from torch._subclasses.fake_tensor import FakeTensorMode
+    import bit_attention_gb300.torch_op  # noqa: F401  (registers the op)
+    with FakeTensorMode():
+        x = torch.empty(2, 300, 3, 64, dtype=torch.bfloat16)
+        o = torch.ops.sage_fp4.attention(x, x, x, True, 0.2, "NHD")
+        assert o.shape == x.shape and o.dtype == torch.bfloat16 and o.is_contiguous()
