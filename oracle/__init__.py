@@ -103,10 +103,17 @@ def _declare(L):
     L.sor_quantize_rows.argtypes = [u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p, u8p]
     L.sor_quantize_v.restype = None
     L.sor_quantize_v.argtypes = [u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p, u8p]
+    L.sor_e8m0_value.restype = ctypes.c_double
+    L.sor_e8m0_value.argtypes = [ctypes.c_int]
+    L.sor_quant_group32_mx.restype = None
+    L.sor_quant_group32_mx.argtypes = [f32p, u8p, u8p]
+    for fn in (L.sor_quantize_rows_fmt, L.sor_quantize_v_fmt):
+        fn.restype = None
+        fn.argtypes = [u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p, u8p]
     L.sor_attention.restype = ctypes.c_int
     L.sor_attention.argtypes = [u8p, u8p, u8p, u8p, u8p, u8p, ctypes.c_int, ctypes.c_int,
-                                ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
-                                ctypes.c_int, i64p, ctypes.c_int64, f64p, f64p, f64p]
+                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int64, f64p, f64p, f64p]
     L.sor_attention_exact.restype = ctypes.c_int
     L.sor_attention_exact.argtypes = [u16p, u16p, u16p, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_double, i64p,
@@ -156,6 +163,20 @@ def encode_range(first: int, count: int):
     return e2, e4
 
 
+def e8m0_value(bits: int) -> float:
+    return lib().sor_e8m0_value(int(bits))
+
+
+def quant_group32_mx(x):
+    """MXFP4 group: 32 floats -> (32 E2M1 codes, E8M0 scale byte)."""
+    x = np.ascontiguousarray(np.asarray(x, np.float32))
+    assert x.shape == (32,)
+    codes = np.empty(32, np.uint8)
+    sc = np.zeros(1, np.uint8)
+    lib().sor_quant_group32_mx(_p(x, ctypes.c_float), _p(codes, ctypes.c_uint8), _p(sc, ctypes.c_uint8))
+    return codes, int(sc[0])
+
+
 def quant_group16(x):
     x = np.ascontiguousarray(np.asarray(x, np.float32))
     assert x.shape == (16,)
@@ -166,38 +187,42 @@ def quant_group16(x):
 
 
 # ------------------------------------------------------------ quantizers
-def quantize_rows(x, BH: int, N: int, D: int):
-    """Q/K: bf16 [BH,N,D] -> codes [BH,N_pad,D/2], scales [BH,N_pad,D/16] (plain layout)."""
+FORMATS = {"nvfp4": 0, "mxfp4": 1}   # microscaling format -> oracle code
+GROUP = {"nvfp4": 16, "mxfp4": 32}   # elements per scale
+
+
+def quantize_rows(x, BH: int, N: int, D: int, fmt: str = "nvfp4"):
+    """Q/K: bf16 [BH,N,D] -> codes [BH,N_pad,D/2], scales [BH,N_pad,D/G] (plain layout)."""
     x = _u16(x).reshape(-1)
     assert x.size == BH * N * D
     Np = round_up(N, 128)
     codes = np.empty((BH, Np, D // 2), np.uint8)
-    scales = np.empty((BH, Np, D // 16), np.uint8)
-    lib().sor_quantize_rows(_p(x, ctypes.c_uint16), BH, N, D, _p(codes, ctypes.c_uint8),
-                            _p(scales, ctypes.c_uint8))
+    scales = np.empty((BH, Np, D // GROUP[fmt]), np.uint8)
+    lib().sor_quantize_rows_fmt(_p(x, ctypes.c_uint16), BH, N, D, FORMATS[fmt],
+                                _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_uint8))
     return codes, scales
 
 
-def quantize_v(v, BH: int, N: int, D: int):
-    """V: bf16 [BH,N,D] -> V^T codes [BH,D,N_pad/2], scales [BH,D,N_pad/16] (plain layout)."""
+def quantize_v(v, BH: int, N: int, D: int, fmt: str = "nvfp4"):
+    """V: bf16 [BH,N,D] -> V^T codes [BH,D,N_pad/2], scales [BH,D,N_pad/G] (plain layout)."""
     v = _u16(v).reshape(-1)
     assert v.size == BH * N * D
     Np = round_up(N, 128)
     codes = np.empty((BH, D, Np // 2), np.uint8)
-    scales = np.empty((BH, D, Np // 16), np.uint8)
-    lib().sor_quantize_v(_p(v, ctypes.c_uint16), BH, N, D, _p(codes, ctypes.c_uint8),
-                         _p(scales, ctypes.c_uint8))
+    scales = np.empty((BH, D, Np // GROUP[fmt]), np.uint8)
+    lib().sor_quantize_v_fmt(_p(v, ctypes.c_uint16), BH, N, D, FORMATS[fmt],
+                             _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_uint8))
     return codes, scales
 
 
 class Quantized:
-    """The oracle's quantized Q, K, V^T for one problem."""
+    """The oracle's quantized Q, K, V^T for one problem, in one microscaling format."""
 
-    def __init__(self, q, k, v, BH: int, N: int, D: int):
-        self.BH, self.N, self.D = BH, N, D
-        self.qc, self.qs = quantize_rows(q, BH, N, D)
-        self.kc, self.ks = quantize_rows(k, BH, N, D)
-        self.vc, self.vs = quantize_v(v, BH, N, D)
+    def __init__(self, q, k, v, BH: int, N: int, D: int, fmt: str = "nvfp4"):
+        self.BH, self.N, self.D, self.fmt = BH, N, D, fmt
+        self.qc, self.qs = quantize_rows(q, BH, N, D, fmt)
+        self.kc, self.ks = quantize_rows(k, BH, N, D, fmt)
+        self.vc, self.vs = quantize_v(v, BH, N, D, fmt)
 
 
 # ------------------------------------------------------------- attention
@@ -223,7 +248,7 @@ def attention(qz: Quantized, causal: bool, pmode: str = "tile", rows=None, kv_ti
     rc = lib().sor_attention(
         _p(qz.qc, ctypes.c_uint8), _p(qz.qs, ctypes.c_uint8), _p(qz.kc, ctypes.c_uint8),
         _p(qz.ks, ctypes.c_uint8), _p(qz.vc, ctypes.c_uint8), _p(qz.vs, ctypes.c_uint8),
-        BH, N, D, int(bool(causal)), scale, PMODE[pmode], kv_tile,
+        BH, N, D, int(bool(causal)), FORMATS[qz.fmt], scale, PMODE[pmode], kv_tile,
         _p(rows_a, ctypes.c_int64) if rows_a is not None else None, nrows,
         _p(out, ctypes.c_double), _p(ol, ctypes.c_double), _p(om, ctypes.c_double))
     if rc != 0:
@@ -256,13 +281,14 @@ def num_threads() -> int:
 
 
 # -------------------------------------------------- decoding helpers
-def decode_rows(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
-    """Decode [.., R, C/2] codes and [.., R, C/16] scales (plain layout) to float64 [.., R, C]."""
+def decode_rows(codes: np.ndarray, scales: np.ndarray, fmt: str = "nvfp4") -> np.ndarray:
+    """Decode [.., R, C/2] codes and [.., R, C/G] scales (plain layout) to float64 [.., R, C]."""
     e2 = np.array([e2m1_value(i) for i in range(16)])
-    e4 = np.array([e4m3_value(i) for i in range(256)])
+    dec = e4m3_value if fmt == "nvfp4" else e8m0_value
+    sv = np.array([dec(i) for i in range(256)])
     lo = codes & 0x0F
     hi = codes >> 4
     el = np.stack([lo, hi], axis=-1).reshape(*codes.shape[:-1], codes.shape[-1] * 2)
     vals = e2[el]
-    sc = np.repeat(e4[scales], 16, axis=-1)
+    sc = np.repeat(sv[scales], GROUP[fmt], axis=-1)
     return vals * sc

@@ -134,6 +134,57 @@ void sor_quant_group16(const float *x, uint8_t *codes16, uint8_t *scale) {
 
 static float bf16_to_f32(uint16_t b) { return f32_from_bits((uint32_t)b << 16); }
 
+/* ------------------------------------------------------------------------ */
+/* 1x32 MXFP4 group quantizer: the alternative the pages weighed and set     */
+/* aside ([NEWS-HW]: E2M1 codes, 1x32 blocks, E8M0 scales).                  */
+/* ------------------------------------------------------------------------ */
+
+/* E8M0: an unsigned power-of-two exponent with bias 127; 0xFF is NaN. */
+double sor_e8m0_value(int b) {
+  if ((b & 0xFF) == 0xFF) return NAN;
+  return ldexp(1.0, (b & 0xFF) - 127);
+}
+
+/* The pages give the format, not the rule.  The rule read here is the one the
+ * OCP Microscaling (MX) v1.0 specification defines for MX conversion: the
+ * shared exponent is floor(log2(amax)) minus the element format's largest
+ * exponent (2 for E2M1), clamped to E8M0's range, and each element is
+ * x / 2^shared rounded to nearest E2M1 (ties to even, saturating at 6).  The
+ * division by a power of two is exact (ldexpf).  An all-zero group takes the
+ * smallest scale byte and all-zero codes. */
+void sor_quant_group32_mx(const float *x, uint8_t *codes32, uint8_t *scale) {
+  float amax = 0.0f;
+  for (int i = 0; i < 32; i++) {
+    float a = fabsf(x[i]);
+    if (a > amax) amax = a;
+  }
+  if (amax == 0.0f) {
+    *scale = 0;
+    for (int i = 0; i < 32; i++) codes32[i] = (uint8_t)sor_e2m1_encode(x[i]);
+    return;
+  }
+  int E;
+  frexpf(amax, &E); /* amax = f * 2^E, f in [0.5, 1): floor(log2(amax)) = E - 1 */
+  int shared = (E - 1) - 2;
+  if (shared < -127) shared = -127;
+  if (shared > 127) shared = 127;
+  *scale = (uint8_t)(shared + 127);
+  for (int i = 0; i < 32; i++) codes32[i] = (uint8_t)sor_e2m1_encode(ldexpf(x[i], -shared));
+}
+
+/* One group of either format: NVFP4 (16 elements, E4M3 scale) or MXFP4 (32
+ * elements, E8M0 scale). */
+static void quant_group(int fmt, const float *x, uint8_t *codes, uint8_t *scale) {
+  if (fmt == SOR_FMT_MXFP4)
+    sor_quant_group32_mx(x, codes, scale);
+  else
+    sor_quant_group16(x, codes, scale);
+}
+
+static int group_size(int fmt) { return fmt == SOR_FMT_MXFP4 ? 32 : 16; }
+
+
+
 static int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 static void put_nibble(uint8_t *row, int idx, int code) {
@@ -147,12 +198,14 @@ static int get_nibble(const uint8_t *row, int idx) {
   return (idx & 1) ? (row[idx >> 1] >> 4) : (row[idx >> 1] & 0x0F);
 }
 
-/* Q and K: groups of 16 consecutive elements along D, the contraction axis of
- * QK^T ([NEWS-OBST], solution 1).  No smoothing (mean subtraction) of K: the
- * pages do not describe one. */
-void sor_quantize_rows(const uint16_t *x, int BH, int N, int D, uint8_t *codes, uint8_t *scales) {
+/* Q and K: groups of consecutive elements along D, the contraction axis of
+ * QK^T ([NEWS-OBST], solution 1): 16 for NVFP4, 32 for MXFP4.  No smoothing
+ * (mean subtraction) of K: the pages do not describe one. */
+void sor_quantize_rows_fmt(const uint16_t *x, int BH, int N, int D, int fmt, uint8_t *codes,
+                           uint8_t *scales) {
+  const int G = group_size(fmt);
   int N_pad = round_up(N, 128);
-  size_t crow = (size_t)D / 2, srow = (size_t)D / 16;
+  size_t crow = (size_t)D / 2, srow = (size_t)D / G;
   memset(codes, 0, (size_t)BH * N_pad * crow);
   memset(scales, 0, (size_t)BH * N_pad * srow);
 #pragma omp parallel for schedule(static)
@@ -161,23 +214,30 @@ void sor_quantize_rows(const uint16_t *x, int BH, int N, int D, uint8_t *codes, 
     const uint16_t *src = x + (size_t)r * D;
     uint8_t *cdst = codes + ((size_t)bh * N_pad + n) * crow;
     uint8_t *sdst = scales + ((size_t)bh * N_pad + n) * srow;
-    for (int g = 0; g < D / 16; g++) {
-      float buf[16];
-      uint8_t c[16];
-      for (int i = 0; i < 16; i++) buf[i] = bf16_to_f32(src[g * 16 + i]);
-      sor_quant_group16(buf, c, &sdst[g]);
-      for (int i = 0; i < 16; i++) put_nibble(cdst, g * 16 + i, c[i]);
+    for (int g = 0; g < D / G; g++) {
+      float buf[32];
+      uint8_t c[32];
+      for (int i = 0; i < G; i++) buf[i] = bf16_to_f32(src[g * G + i]);
+      quant_group(fmt, buf, c, &sdst[g]);
+      for (int i = 0; i < G; i++) put_nibble(cdst, g * G + i, c[i]);
     }
   }
 }
 
-/* V: the contraction axis of PV is the token axis, so the 16-element groups
- * run along tokens for each channel (block scales of a block-scaled product
- * always run along the contraction axis).  Output is V^T.  Tokens past N are
- * zero, which makes an all-padding group's scale and codes zero. */
-void sor_quantize_v(const uint16_t *v, int BH, int N, int D, uint8_t *codes, uint8_t *scales) {
+void sor_quantize_rows(const uint16_t *x, int BH, int N, int D, uint8_t *codes, uint8_t *scales) {
+  sor_quantize_rows_fmt(x, BH, N, D, SOR_FMT_NVFP4, codes, scales);
+}
+
+/* V: the contraction axis of PV is the token axis, so the groups run along
+ * tokens for each channel (block scales of a block-scaled product always run
+ * along the contraction axis).  Output is V^T.  Tokens past N are zero, which
+ * makes an all-padding NVFP4 group's scale and codes zero (an all-padding
+ * MXFP4 group gets the smallest scale byte and zero codes). */
+void sor_quantize_v_fmt(const uint16_t *v, int BH, int N, int D, int fmt, uint8_t *codes,
+                        uint8_t *scales) {
+  const int G = group_size(fmt);
   int N_pad = round_up(N, 128);
-  size_t crow = (size_t)N_pad / 2, srow = (size_t)N_pad / 16;
+  size_t crow = (size_t)N_pad / 2, srow = (size_t)N_pad / G;
   memset(codes, 0, (size_t)BH * D * crow);
   memset(scales, 0, (size_t)BH * D * srow);
 #pragma omp parallel for collapse(2) schedule(static)
@@ -185,18 +245,22 @@ void sor_quantize_v(const uint16_t *v, int BH, int N, int D, uint8_t *codes, uin
     for (int d = 0; d < D; d++) {
       uint8_t *cdst = codes + ((size_t)bh * D + d) * crow;
       uint8_t *sdst = scales + ((size_t)bh * D + d) * srow;
-      for (int g = 0; g < N_pad / 16; g++) {
-        float buf[16];
-        uint8_t c[16];
-        for (int i = 0; i < 16; i++) {
-          int n = g * 16 + i;
+      for (int g = 0; g < N_pad / G; g++) {
+        float buf[32];
+        uint8_t c[32];
+        for (int i = 0; i < G; i++) {
+          int n = g * G + i;
           buf[i] = (n < N) ? bf16_to_f32(v[((size_t)bh * N + n) * D + d]) : 0.0f;
         }
-        sor_quant_group16(buf, c, &sdst[g]);
-        for (int i = 0; i < 16; i++) put_nibble(cdst, g * 16 + i, c[i]);
+        quant_group(fmt, buf, c, &sdst[g]);
+        for (int i = 0; i < G; i++) put_nibble(cdst, g * G + i, c[i]);
       }
     }
   }
+}
+
+void sor_quantize_v(const uint16_t *v, int BH, int N, int D, uint8_t *codes, uint8_t *scales) {
+  sor_quantize_v_fmt(v, BH, N, D, SOR_FMT_NVFP4, codes, scales);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -207,6 +271,7 @@ void sor_quantize_v(const uint16_t *v, int BH, int N, int D, uint8_t *codes, uin
  * codec definitions above. */
 static double g_e2m1[16];
 static double g_e4m3[256];
+static double g_e8m0[256];
 static int g_tables_ready = 0;
 
 static void init_tables(void) {
@@ -216,6 +281,7 @@ static void init_tables(void) {
     if (!g_tables_ready) {
       for (int i = 0; i < 16; i++) g_e2m1[i] = sor_e2m1_value(i);
       for (int i = 0; i < 256; i++) g_e4m3[i] = sor_e4m3_value(i);
+      for (int i = 0; i < 256; i++) g_e8m0[i] = sor_e8m0_value(i);
       g_tables_ready = 1;
     }
   }
@@ -236,16 +302,24 @@ static void init_tables(void) {
  *           (RUNNING): P2_j = 2688 * exp((S_j - m_new)/sqrt(D)), sP1 = 1/2688
  *            -- the per-token first level that brings each token's values
  *            into [0, 448*6] ([NEWS-OBST], solution 2); P2_j is rounded to float.
- *   level 2: the 1x16 group quantizer on P2 along keys (16 consecutive
- *            elements of a row, [NEWS-HW])
+ *   level 2: the group quantizer on P2 along keys (16 consecutive elements
+ *            of a row, [NEWS-HW]; 32 for MXFP4)
+ * For MXFP4 (fmt 1) every group is 32 elements with an E8M0 scale, and the
+ * level-1 target 2688 = 448*6 (largest E4M3 scale times largest E2M1 value,
+ * the range level 1 exists to fill) becomes 6: an E8M0 scale needs no help
+ * with its range, and 6 keeps each row's tile maximum exactly representable
+ * (scale 2^0, code 6), as 2688 does for NVFP4 (scale 448, code 6).
  *   acc    = acc * exp((m_old - m_new)/sqrt(D)) + sP1 * sum_j dec(P2_j) * dec(V_j)
  * and finally O = acc / l. */
 static void attend_row(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const uint8_t *ks,
                        const uint8_t *vc, const uint8_t *vs, int N, int N_pad, int D, int causal,
-                       double scale, int pmode, int kv_tile, int i, double *out, double *out_l,
-                       double *out_m) {
+                       int fmt, double scale, int pmode, int kv_tile, int i, double *out,
+                       double *out_l, double *out_m) {
   const double isd = scale;
-  const int G = D / 16;
+  const int GS = group_size(fmt);                            /* elements per scale */
+  const int G = D / GS;                                      /* Q/K groups per row */
+  const double *sc = (fmt == SOR_FMT_MXFP4) ? g_e8m0 : g_e4m3; /* scale values */
+  const double R = (fmt == SOR_FMT_MXFP4) ? 6.0 : 2688.0;     /* level-1 target */
   double qv[SOR_MAX_D];
   double acc[SOR_MAX_D];
   double S[SOR_MAX_TILE];
@@ -273,8 +347,8 @@ static void attend_row(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, 
       double s = 0.0;
       for (int g = 0; g < G; g++) {
         double part = 0.0;
-        for (int k = 16 * g; k < 16 * g + 16; k++) part += qv[k] * g_e2m1[get_nibble(krow, k)];
-        s += g_e4m3[qs[(size_t)i * G + g]] * g_e4m3[ks[(size_t)j * G + g]] * part;
+        for (int k = GS * g; k < GS * g + GS; k++) part += qv[k] * g_e2m1[get_nibble(krow, k)];
+        s += sc[qs[(size_t)i * G + g]] * sc[ks[(size_t)j * G + g]] * part;
       }
       S[jj] = s;
       if (s > t) t = s;
@@ -287,23 +361,23 @@ static void attend_row(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, 
 
     /* level 1 */
     double ref = (pmode == 0) ? t : m_new;
-    double sP1 = (pmode == 0) ? exp((t - m_new) * isd) / 2688.0 : 1.0 / 2688.0;
-    for (int jj = 0; jj < T; jj++) P2[jj] = (float)(2688.0 * exp((S[jj] - ref) * isd));
+    double sP1 = (pmode == 0) ? exp((t - m_new) * isd) / R : 1.0 / R;
+    for (int jj = 0; jj < T; jj++) P2[jj] = (float)(R * exp((S[jj] - ref) * isd));
     /* level 2 */
-    for (int g = 0; g < T / 16; g++) sor_quant_group16(&P2[16 * g], &pc[16 * g], &ps[g]);
+    for (int g = 0; g < T / GS; g++) quant_group(fmt, &P2[GS * g], &pc[GS * g], &ps[g]);
 
     /* O update */
     for (int d = 0; d < D; d++) {
       const uint8_t *vrow = vc + (size_t)d * (N_pad / 2);
-      const uint8_t *vsrow = vs + (size_t)d * (N_pad / 16);
+      const uint8_t *vsrow = vs + (size_t)d * (N_pad / GS);
       double pv = 0.0;
-      for (int g = 0; g < T / 16; g++) {
-        int jg = (j0 / 16) + g; /* token group index */
-        if (16 * jg >= N_pad) break;
+      for (int g = 0; g < T / GS; g++) {
+        int jg = (j0 / GS) + g; /* token group index */
+        if (GS * jg >= N_pad) break;
         double part = 0.0;
-        for (int k = 0; k < 16; k++)
-          part += g_e2m1[pc[16 * g + k]] * g_e2m1[get_nibble(vrow, 16 * jg + k)];
-        pv += g_e4m3[ps[g]] * g_e4m3[vsrow[jg]] * part;
+        for (int k = 0; k < GS; k++)
+          part += g_e2m1[pc[GS * g + k]] * g_e2m1[get_nibble(vrow, GS * jg + k)];
+        pv += sc[ps[g]] * sc[vsrow[jg]] * part;
       }
       acc[d] = acc[d] * alpha + sP1 * pv;
     }
@@ -316,9 +390,11 @@ static void attend_row(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, 
 
 int sor_attention(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const uint8_t *ks,
                   const uint8_t *vc, const uint8_t *vs, int BH, int N, int D, int causal,
-                  double scale, int pmode, int kv_tile, const int64_t *rows, int64_t nrows,
-                  double *out, double *out_l, double *out_m) {
-  if (D % 16 || D > SOR_MAX_D || kv_tile % 16 || kv_tile > SOR_MAX_TILE || kv_tile <= 0 || N < 1 ||
+                  int fmt, double scale, int pmode, int kv_tile, const int64_t *rows,
+                  int64_t nrows, double *out, double *out_l, double *out_m) {
+  if (fmt != SOR_FMT_NVFP4 && fmt != SOR_FMT_MXFP4) return -1;
+  const int GS = group_size(fmt);
+  if (D % GS || D > SOR_MAX_D || kv_tile % GS || kv_tile > SOR_MAX_TILE || kv_tile <= 0 || N < 1 ||
       !(scale > 0.0) || isinf(scale))
     return -1;
   init_tables();
@@ -329,10 +405,10 @@ int sor_attention(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const
     int64_t id = rows ? rows[r] : r;
     int64_t bh = id / N;
     int i = (int)(id % N);
-    attend_row(qc + (size_t)bh * N_pad * (D / 2), qs + (size_t)bh * N_pad * (D / 16),
-               kc + (size_t)bh * N_pad * (D / 2), ks + (size_t)bh * N_pad * (D / 16),
-               vc + (size_t)bh * D * (N_pad / 2), vs + (size_t)bh * D * (N_pad / 16), N, N_pad, D,
-               causal, scale, pmode, kv_tile, i, out + (size_t)r * D, out_l ? out_l + r : 0,
+    attend_row(qc + (size_t)bh * N_pad * (D / 2), qs + (size_t)bh * N_pad * (D / GS),
+               kc + (size_t)bh * N_pad * (D / 2), ks + (size_t)bh * N_pad * (D / GS),
+               vc + (size_t)bh * D * (N_pad / 2), vs + (size_t)bh * D * (N_pad / GS), N, N_pad, D,
+               causal, fmt, scale, pmode, kv_tile, i, out + (size_t)r * D, out_l ? out_l + r : 0,
                out_m ? out_m + r : 0);
   }
   return 0;

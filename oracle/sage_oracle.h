@@ -47,6 +47,22 @@ void sor_encode_range(uint32_t first, uint32_t count, uint8_t *e2m1, uint8_t *e4
 /* one 16-element group: scale = E4M3(amax/6), codes = E2M1(x * (1/scale)) */
 void sor_quant_group16(const float *x, uint8_t *codes16, uint8_t *scale);
 
+/* Microscaling formats: NVFP4 (1x16, E4M3 scales; the method's) and MXFP4
+ * (1x32, E8M0 scales; the alternative the pages weighed, [NEWS-HW]). */
+#define SOR_FMT_NVFP4 0
+#define SOR_FMT_MXFP4 1
+
+/* E8M0 byte -> 2^(b-127); 0xFF is NaN */
+double sor_e8m0_value(int b);
+/* 32 floats -> 32 E2M1 codes + one E8M0 scale byte (OCP MX rule, see .c) */
+void sor_quant_group32_mx(const float *x, uint8_t *codes32, uint8_t *scale);
+/* Q/K rows and V in either format (plain layouts as below, with D/32 or
+ * N_pad/32 scales per row for MXFP4) */
+void sor_quantize_rows_fmt(const uint16_t *x, int BH, int N, int D, int fmt, uint8_t *codes,
+                           uint8_t *scales);
+void sor_quantize_v_fmt(const uint16_t *v, int BH, int N, int D, int fmt, uint8_t *codes,
+                        uint8_t *scales);
+
 /* Q/K rows: bf16 bits [BH][N][D] -> codes/scales as above */
 void sor_quantize_rows(const uint16_t *x, int BH, int N, int D, uint8_t *codes, uint8_t *scales);
 /* V: bf16 bits [BH][N][D] -> V^T codes/scales, groups along tokens */
@@ -54,13 +70,14 @@ void sor_quantize_v(const uint16_t *v, int BH, int N, int D, uint8_t *codes, uin
 
 /* Tiled FP4 attention over the quantized tensors, softmax scale `scale`
  * (> 0; 1/sqrt(D) is the standard one).
+ * fmt: SOR_FMT_NVFP4 or SOR_FMT_MXFP4 (operands quantized in that format).
  * pmode 0 = TILE (level 1 normalises each KV tile's row segment so that its
- * max is 448*6), pmode 1 = RUNNING (normalised against the running row max).
+ * max is 448*6, or 6 for MXFP4), pmode 1 = RUNNING (normalised against the running row max).
  * rows: flat row ids bh*N + i (NULL = all BH*N rows).  out: [nrows][D]. */
 int sor_attention(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const uint8_t *ks,
                   const uint8_t *vc, const uint8_t *vs, int BH, int N, int D, int causal,
-                  double scale, int pmode, int kv_tile, const int64_t *rows, int64_t nrows,
-                  double *out, double *out_l, double *out_m);
+                  int fmt, double scale, int pmode, int kv_tile, const int64_t *rows,
+                  int64_t nrows, double *out, double *out_l, double *out_m);
 
 /* Exact attention softmax(scale * Q K^T) V, unquantized, from the bf16
  * inputs, in double. */

@@ -243,13 +243,13 @@ MUTATIONS = {
     "drop_alpha": ("acc[d] = acc[d] * alpha + sP1 * pv;", "acc[d] = acc[d] + sP1 * pv;"),
     "drop_sP1": ("acc[d] = acc[d] * alpha + sP1 * pv;", "acc[d] = acc[d] * alpha + pv / 2688.0;"),
     "l_not_rescaled": ("l = l * alpha + lt;", "l = l + lt;"),
-    "exp_sign": ("P2[jj] = (float)(2688.0 * exp((S[jj] - ref) * isd));",
-                 "P2[jj] = (float)(2688.0 * exp((ref - S[jj]) * isd));"),
-    "k_scale_index": ("g_e4m3[ks[(size_t)j * G + g]]", "g_e4m3[ks[(size_t)i * G + g]]"),
-    "v_group_index": ("g_e4m3[vsrow[jg]]", "g_e4m3[vsrow[g]]"),
+    "exp_sign": ("P2[jj] = (float)(R * exp((S[jj] - ref) * isd));",
+                 "P2[jj] = (float)(R * exp((ref - S[jj]) * isd));"),
+    "k_scale_index": ("sc[ks[(size_t)j * G + g]]", "sc[ks[(size_t)i * G + g]]"),
+    "v_group_index": ("sc[vsrow[jg]]", "sc[vsrow[g]]"),
     "causal_off_by_one": ("int kend = causal ? (i + 1) : N;", "int kend = causal ? i : N;"),
-    "no_level2_scale": ("pv += g_e4m3[ps[g]] * g_e4m3[vsrow[jg]] * part;",
-                        "pv += 448.0 * g_e4m3[vsrow[jg]] * part;"),
+    "no_level2_scale": ("pv += sc[ps[g]] * sc[vsrow[jg]] * part;",
+                        "pv += 448.0 * sc[vsrow[jg]] * part;"),
     "scale_amax_over_4": ("float q = amax / 6.0f;", "float q = amax / 4.0f;"),
     "e2m1_ties_up": ("(d == bestd && (i & 1) == 0)", "(d == bestd)"),
     "scale_ignored": ("double *out_m) {\n  const double isd = scale;",
