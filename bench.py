@@ -144,7 +144,7 @@ def barrier(world: int):
         dist.barrier()
 
 
-def cpu_oracle_sample(w, target_s: float, seed: int = 0):
+def cpu_oracle_sample(w, target_s: float, seed: int = 0, fmt: str = "nvfp4"):
     """Time the oracle's attention on a bounded row sample of workload w.
     Returns (TOPS, seconds, rows, threads)."""
     import numpy as np
@@ -152,7 +152,7 @@ def cpu_oracle_sample(w, target_s: float, seed: int = 0):
     from bit_attention_gb300.synth import make_qkv
     # a reduced batch with the same per-row work (full N, same D and pattern)
     q, k, v = make_qkv(1, 1, w.N, w.D, w.pattern, seed=seed)
-    qz = oracle.Quantized(q, k, v, 1, w.N, w.D)
+    qz = oracle.Quantized(q, k, v, 1, w.N, w.D, fmt=fmt)
     rng = np.random.default_rng(seed)
     rows_done, secs, ops = 0, 0.0, 0.0
     batch = max(oracle.num_threads(), 1)
@@ -175,7 +175,7 @@ def run_reference(args, w, world, rank):
     tops = []
     rows_total, threads = 0, 1
     for i in range(args.warmup + args.steps):
-        v, secs, rows, threads = cpu_oracle_sample(w, args.ref_seconds, seed=i)
+        v, secs, rows, threads = cpu_oracle_sample(w, args.ref_seconds, seed=i, fmt=args.fmt)
         if i >= args.warmup:
             tops.append(v)
             rows_total += rows
@@ -186,7 +186,7 @@ def run_reference(args, w, world, rank):
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
            "ms_per_step": None, "dtype": "f64", "data": "synthetic",
-           "config": w.describe(),
+           "config": dict(w.describe(), format=args.fmt),
            "cpu_baseline": {"value": value, "unit": "TOPS", "cores": threads, "kind": "oracle",
                             "sample": sample},
            "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0,
@@ -203,6 +203,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--causal", type=int, default=None)
     ap.add_argument("--shape", default=None, help="B,H,N,D override (profiling cases)")
+    ap.add_argument("--fmt", default="nvfp4", choices=["nvfp4", "mxfp4"],
+                    help="microscaling format (mxfp4: the variant the pages set aside)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-sdpa", action="store_true", help="skip the bf16 SDPA context timing")
@@ -237,7 +239,7 @@ def main():
     stream = torch.cuda.current_stream()
 
     def step():
-        S.quantize_qkv(qd, kd, vd, out=z)
+        S.quantize_qkv(qd, kd, vd, out=z, fmt=args.fmt)
         S.attn_fwd(z, w.causal, out=o)
 
     for _ in range(args.warmup):
@@ -257,7 +259,7 @@ def main():
         for i in range(args.steps):
             e0, e1, e2 = ev[i]
             e0.record(stream)
-            S.quantize_qkv(qd, kd, vd, out=z)
+            S.quantize_qkv(qd, kd, vd, out=z, fmt=args.fmt)
             e1.record(stream)
             S.attn_fwd(z, w.causal, out=o)
             e2.record(stream)
@@ -288,7 +290,7 @@ def main():
     # quantize, attention and the copy of O back to host memory, pipelined
     # over chunks of heads inside the library)
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.fmt == "nvfp4":
         hq, hk, hv = (t.pin_memory() for t in (q, k, v))
         ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         hws = S.HostWorkspace(w.B, w.H, w.N, w.D)
@@ -340,7 +342,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        v_cpu, secs, rows, threads = cpu_oracle_sample(w, args.cpu_seconds)
+        v_cpu, secs, rows, threads = cpu_oracle_sample(w, args.cpu_seconds, fmt=args.fmt)
         cpu = {"value": v_cpu, "unit": "TOPS", "cores": threads, "kind": "oracle",
                "sample": f"oracle attention on {rows} random query rows of one (b,h), full N={w.N}, "
                          f"{secs:.1f} s; quantization excluded"}
@@ -350,9 +352,10 @@ def main():
             "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "nvfp4 (e2m1 codes, e4m3 scales) / fp32 accumulate",
+            "dtype": ("nvfp4 (e2m1 codes, e4m3 scales)" if args.fmt == "nvfp4"
+                      else "mxfp4 (e2m1 codes, e8m0 scales)") + " / fp32 accumulate",
             "data": "synthetic (seeded, bit_attention_gb300.synth)",
-            "config": dict(w.describe(), l2="bf16 inputs 3x larger than L2; no flush",
+            "config": dict(w.describe(), format=args.fmt, l2="bf16 inputs 3x larger than L2; no flush",
                            parallelism=f"weak, {world} independent batch(es)"),
             "attn_kernel": {"ms": a_ms, "tops": attn_tops, "frac_of_fp4_peak": attn_tops / fp4_peak,
                             "ms_median": statistics.median(a_all), "ms_min": min(a_all),
@@ -362,7 +365,7 @@ def main():
                               "frac_of_hbm": quant_gbs / pk["hbm_gbs"]},
             "roofline": {"bound": "tensor", "achieved": attn_tops, "peak": fp4_peak,
                          "unit": "TFLOP/s", "frac": attn_tops / fp4_peak,
-                         "traffic": ATTN_TRAFFIC.get(w.name),
+                         "traffic": ATTN_TRAFFIC.get(w.name) if args.fmt == "nvfp4" else None,
                          "traffic_unit": "DRAM bytes (read + write) per attention launch, from ncu",
                          "peak_src": f"{pk['src']} bf16 x {FP4_OVER_BF16:g} (nominal FP4/BF16)"},
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk.summary(),

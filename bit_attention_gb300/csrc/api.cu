@@ -137,6 +137,8 @@ bool strides_of(const sage_fp4_strides* in, int B, int H, int N, int D, Strides*
 
 bool scale_ok(float s) { return s > 0.0f && s <= 1.0e30f; }
 
+bool format_ok(int f) { return f == SAGE_FP4_FORMAT_NVFP4 || f == SAGE_FP4_FORMAT_MXFP4; }
+
 }  // namespace
 
 extern "C" {
@@ -165,8 +167,8 @@ int sage_fp4_qkv_from_workspace(void* workspace, size_t workspace_bytes, int B, 
 int sage_fp4_quantize_qkv_strided(const void* q, const sage_fp4_strides* q_strides, const void* k,
                                   const sage_fp4_strides* k_strides, const void* v,
                                   const sage_fp4_strides* v_strides, const sage_fp4_qkv* out, int B,
-                                  int H, int N, int D, void* stream) {
-  if (!dims_ok(B, H, N, D) || !out) return SAGE_FP4_EINVAL;
+                                  int H, int N, int D, int format, void* stream) {
+  if (!dims_ok(B, H, N, D) || !out || !format_ok(format)) return SAGE_FP4_EINVAL;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return SAGE_FP4_EINVAL;
   if (!tensor_ok(out->q) || !tensor_ok(out->k) || !tensor_ok(out->vt) || !aligned(out->status, 4))
     return SAGE_FP4_EINVAL;
@@ -179,22 +181,25 @@ int sage_fp4_quantize_qkv_strided(const void* q, const sage_fp4_strides* q_strid
   if (dev != SAGE_FP4_OK) return dev;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int BH = B * H;
+  const bool mx = format == SAGE_FP4_FORMAT_MXFP4;
   cudaError_t e = launch_quant_rows(q, k, sq, sk, out->q.codes, out->q.scales, out->k.codes,
-                                    out->k.scales, H, BH, N, D, st);
+                                    out->k.scales, H, BH, N, D, mx, st);
   if (e != cudaSuccess) return SAGE_FP4_ECUDA;
-  return from_cuda(launch_quant_v(v, sv, out->vt.codes, out->vt.scales, H, BH, N, D, out->status, st));
+  return from_cuda(launch_quant_v(v, sv, out->vt.codes, out->vt.scales, H, BH, N, D, mx, out->status, st));
 }
 
 int sage_fp4_quantize_qkv(const void* q, const void* k, const void* v, const sage_fp4_qkv* out,
                           int B, int H, int N, int D, void* stream) {
-  return sage_fp4_quantize_qkv_strided(q, nullptr, k, nullptr, v, nullptr, out, B, H, N, D, stream);
+  return sage_fp4_quantize_qkv_strided(q, nullptr, k, nullptr, v, nullptr, out, B, H, N, D,
+                                       SAGE_FP4_FORMAT_NVFP4, stream);
 }
 
 namespace {
 
 int attn_fwd_impl(const sage_fp4_qkv* qkv, void* o, const sage_fp4_strides* o_strides, int B, int H,
-                  int N, int D, int causal, float scale, int flags, uint64_t wait_ns, void* stream) {
-  if (!dims_ok(B, H, N, D) || !qkv_ok(qkv) || !aligned(o, 16)) return SAGE_FP4_EINVAL;
+                  int N, int D, int causal, float scale, int format, int flags, uint64_t wait_ns,
+                  void* stream) {
+  if (!dims_ok(B, H, N, D) || !qkv_ok(qkv) || !aligned(o, 16) || !format_ok(format)) return SAGE_FP4_EINVAL;
   if (causal != 0 && causal != 1) return SAGE_FP4_EINVAL;
   Strides so;
   if (!strides_of(o_strides, B, H, N, D, &so) || !scale_ok(scale)) return SAGE_FP4_EINVAL;
@@ -224,6 +229,7 @@ int attn_fwd_impl(const sage_fp4_qkv* qkv, void* o, const sage_fp4_strides* o_st
   p.causal = causal;
   p.n_qt = Np / 128;
   p.a = static_cast<float>(1.4426950408889634 * static_cast<double>(scale));
+  p.mx = format == SAGE_FP4_FORMAT_MXFP4 ? 1 : 0;
   p.flags = flags;
   p.wait_ns = wait_ns;
   return from_cuda(launch_attn(tq, tk, tv, p, D, static_cast<cudaStream_t>(stream)));
@@ -235,20 +241,23 @@ float default_scale(int D) { return static_cast<float>(1.0 / sqrt(static_cast<do
 }  // namespace
 
 int sage_fp4_attn_fwd_ex(const sage_fp4_qkv* qkv, void* o, const sage_fp4_strides* o_strides, int B,
-                         int H, int N, int D, int causal, float softmax_scale, void* stream) {
-  return attn_fwd_impl(qkv, o, o_strides, B, H, N, D, causal, softmax_scale, 0, kAttnWaitNs, stream);
+                         int H, int N, int D, int causal, float softmax_scale, int format,
+                         void* stream) {
+  return attn_fwd_impl(qkv, o, o_strides, B, H, N, D, causal, softmax_scale, format, 0, kAttnWaitNs,
+                       stream);
 }
 
 int sage_fp4_attn_fwd(const sage_fp4_qkv* qkv, void* o, int B, int H, int N, int D, int causal,
                       void* stream) {
-  return attn_fwd_impl(qkv, o, nullptr, B, H, N, D, causal, default_scale(D), 0, kAttnWaitNs, stream);
+  return attn_fwd_impl(qkv, o, nullptr, B, H, N, D, causal, default_scale(D), SAGE_FP4_FORMAT_NVFP4, 0,
+                       kAttnWaitNs, stream);
 }
 
 int sage_fp4_attn_fwd_stall_test(const sage_fp4_qkv* qkv, void* o, int B, int H, int N, int D,
                                  int causal, uint64_t wait_limit_ns, void* stream) {
   if (wait_limit_ns < 1000000ull || wait_limit_ns > kAttnWaitNs) return SAGE_FP4_EINVAL;
-  return attn_fwd_impl(qkv, o, nullptr, B, H, N, D, causal, default_scale(D), kAttnWithholdK,
-                       wait_limit_ns, stream);
+  return attn_fwd_impl(qkv, o, nullptr, B, H, N, D, causal, default_scale(D), SAGE_FP4_FORMAT_NVFP4,
+                       kAttnWithholdK, wait_limit_ns, stream);
 }
 
 int sage_fp4_get_status(const sage_fp4_qkv* qkv, void* stream) {
@@ -290,9 +299,11 @@ int sage_fp4_cvt_probe(uint32_t first, uint32_t count, uint8_t* e2m1, uint8_t* e
   return from_cuda(launch_cvt_probe(first, count, e2m1, e4m3, static_cast<cudaStream_t>(stream)));
 }
 
-int sage_fp4_mma_probe(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* b_codes,
-                       const uint8_t* b_scales, int n, int K, int a_by_threads, float* d,
-                       int32_t* status, void* stream) {
+namespace {
+
+int mma_probe_impl(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* b_codes,
+                   const uint8_t* b_scales, int n, int K, int a_by_threads, int mx, float* d,
+                   int32_t* status, void* stream) {
   if (n != 64 && n != 128) return SAGE_FP4_EINVAL;
   if (K != 64 && K != 128 && K != 256) return SAGE_FP4_EINVAL;
   if (!aligned(a_codes, 16) || !aligned(a_scales, 16) || !aligned(b_codes, 16) ||
@@ -314,7 +325,22 @@ int sage_fp4_mma_probe(const uint8_t* a_codes, const uint8_t* a_scales, const ui
   p.n = n;
   p.K = K;
   p.a_by_threads = a_by_threads ? 1 : 0;
+  p.mx = mx;
   return from_cuda(launch_mma_probe(ta, tb, p, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+int sage_fp4_mma_probe(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* b_codes,
+                       const uint8_t* b_scales, int n, int K, int a_by_threads, float* d,
+                       int32_t* status, void* stream) {
+  return mma_probe_impl(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threads, 0, d, status, stream);
+}
+
+int sage_fp4_mma_probe_mx(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* b_codes,
+                          const uint8_t* b_scales, int n, int K, int a_by_threads, float* d,
+                          int32_t* status, void* stream) {
+  return mma_probe_impl(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threads, 1, d, status, stream);
 }
 
 }  // extern "C"

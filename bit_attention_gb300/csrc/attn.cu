@@ -184,6 +184,7 @@ __device__ __forceinline__ void cta_bar_sync() {
 }
 
 constexpr float kLog2of2688 = 11.392317422778761f;  // log2(448 * 6)
+constexpr float kLog2of6 = 2.5849625007211563f;     // log2(6): the MXFP4 level-1 target
 
 __device__ __forceinline__ float max16(const uint32_t* s) {
   auto f = [&](int i) { return __uint_as_float(s[i]); };
@@ -214,7 +215,8 @@ __device__ __forceinline__ Item item_at(const AttnParams& p, int it) {
   return r;
 }
 
-template <int D, bool kDenseO>
+// kMx: operands and P in MXFP4 (groups of 32, E8M0 scales) instead of NVFP4.
+template <int D, bool kDenseO, bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -350,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_wait(bar(B_VFULL + j % kStages), (j / kStages) & 1, ctl);
     } else if (!skip && warp == 1 && lane == 0) {
       // ------------------------------------------------------- S issuer
-      constexpr uint32_t idS = idesc_nvfp4(128, 128);
+      constexpr uint32_t idS = kMx ? idesc_mxf4(128, 128) : idesc_nvfp4(128, 128);
       constexpr uint32_t qk_swz = (D == 128) ? kSwizzle64B : kSwizzle32B;
       constexpr uint32_t qk_sbo = 8 * (D / 2);
       bool ok = true;
@@ -383,8 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kb = 0; kb < L::KBD; ++kb) {
             const uint64_t ad = smem_desc(sb + L::oQ + qs * L::QBYTES + 32 * kb, 16, qk_sbo, qk_swz);
             const uint64_t bd = smem_desc(sb + L::oK + s * L::QBYTES + 32 * kb, 16, qk_sbo, qk_swz);
-            mma_nvfp4(tmem + kColS + w * 128, ad, bd, idS, tmem + kColSFQ + 8 * qs + 4 * kb,
-                      tmem + kColSFK + 8 * sl + 4 * kb, kb > 0);
+            if constexpr (kMx)
+              mma_mxf4(tmem + kColS + w * 128, ad, bd, idS, tmem + kColSFQ + 8 * qs + 4 * kb,
+                       tmem + kColSFK + 8 * sl + 4 * kb, kb > 0);
+            else
+              mma_nvfp4(tmem + kColS + w * 128, ad, bd, idS, tmem + kColSFQ + 8 * qs + 4 * kb,
+                        tmem + kColSFK + 8 * sl + 4 * kb, kb > 0);
           }
           tc_commit(bar(B_SDONE + s));
         }
@@ -402,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // groups of 64 output columns (V^T rows 64h.., whose scale factors sit
       // 2h columns further along: each column holds 32 rows); one group of
       // N = D is used, measured faster than two of 64 at D = 128.
-      constexpr uint32_t idPV = idesc_nvfp4(128, D);
+      constexpr uint32_t idPV = kMx ? idesc_mxf4(128, D) : idesc_nvfp4(128, D);
       bool ok = true;
       int g = 0;
       for (int it = item0; ok && it < n_items; it += istep) {
@@ -430,8 +436,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t ad = smem_desc(sb + L::oP + ps * L::PBYTES + 32 * kb, 16, 512, kSwizzle64B);
               const uint64_t bd =
                   smem_desc(sb + L::oV + s * L::VBYTES + h * 64 * 64 + 32 * kb, 16, 512, kSwizzle64B);
-              mma_nvfp4(tmem + kColPV + pb * D, ad, bd, idPV, tmem + kColSFP + 8 * sl + 4 * kb,
-                        tmem + kColSFV + 8 * sl + 4 * kb + 2 * h, kb > 0);
+              if constexpr (kMx)
+                mma_mxf4(tmem + kColPV + pb * D, ad, bd, idPV, tmem + kColSFP + 8 * sl + 4 * kb,
+                         tmem + kColSFV + 8 * sl + 4 * kb + 2 * h, kb > 0);
+              else
+                mma_nvfp4(tmem + kColPV + pb * D, ad, bd, idPV, tmem + kColSFP + 8 * sl + 4 * kb,
+                          tmem + kColSFV + 8 * sl + 4 * kb + 2 * h, kb > 0);
             }
             tc_commit(bar(B_PVDONE + e % kPvRing));
           }
@@ -502,17 +512,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             // as exp2(a S_j + bias_g); a group whose scale is 0 keeps bias nb so
             // that its (vanishing) probabilities still enter the row sum exactly
             float bias[8], lsc[8];
-            uint32_t s2[4];  // E4M3 scale bytes of groups (2i, 2i+1)
+            uint32_t s2[4];  // scale bytes of 16-key groups (2i, 2i+1), two per 16 bits
+            if constexpr (kMx) {
+              // MXFP4: level 1 maps the row maximum to 6; each 32-key group's
+              // E8M0 scale comes from its largest P2 = 6 exp2(a (S - t)), and
+              // both 16-key halves take its bias (scale words: [e(2k), e(2k+1), 0, 0])
+              uint32_t e8[4];
 #pragma unroll
-            for (int q = 0; q < 8; q += 2) {
-              const float e0 = ex2_approx(fmaf(gm[q], a, nb));
-              const float e1 = ex2_approx(fmaf(gm[q + 1], a, nb));
-              s2[q / 2] = cvt_e4m3x2(448.0f * e0, 448.0f * e1);
-              const float2 t0 = lut[s2[q / 2] & 0xFFu], t1 = lut[s2[q / 2] >> 8];
-              bias[q] = nb + t0.x;
-              lsc[q] = t0.y;
-              bias[q + 1] = nb + t1.x;
-              lsc[q + 1] = t1.y;
+              for (int j = 0; j < 4; ++j) {
+                const float p2 = 6.0f * ex2_approx(fmaf(fmaxf(gm[2 * j], gm[2 * j + 1]), a, nb));
+                e8[j] = e8m0_of(p2);
+                const float sh = static_cast<float>(static_cast<int>(e8[j]) - 127);
+                bias[2 * j] = bias[2 * j + 1] = nb + (kLog2of6 - sh);
+                lsc[2 * j] = lsc[2 * j + 1] = __uint_as_float(e8[j] << 23) * (1.0f / 6.0f);
+              }
+              s2[0] = e8[0] | (e8[1] << 8);
+              s2[1] = 0u;
+              s2[2] = e8[2] | (e8[3] << 8);
+              s2[3] = 0u;
+            } else {
+#pragma unroll
+              for (int q = 0; q < 8; q += 2) {
+                const float e0 = ex2_approx(fmaf(gm[q], a, nb));
+                const float e1 = ex2_approx(fmaf(gm[q + 1], a, nb));
+                s2[q / 2] = cvt_e4m3x2(448.0f * e0, 448.0f * e1);
+                const float2 t0 = lut[s2[q / 2] & 0xFFu], t1 = lut[s2[q / 2] >> 8];
+                bias[q] = nb + t0.x;
+                lsc[q] = t0.y;
+                bias[q + 1] = nb + t1.x;
+                lsc[q + 1] = t1.y;
+              }
             }
             // P slot ps is free once PV_{g-3} has completed
             if (g >= kPSlots) {
@@ -623,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float alpha = up ? ex2_approx((m - mn) * a) : 1.0f;
           const float beta = ex2_approx((st.x - mn) * a);
           l = l * alpha + st.y * beta;
-          const float w = beta * (1.0f / 2688.0f);
+          const float w = beta * (kMx ? 1.0f / 6.0f : 1.0f / 2688.0f);
           m = mn;
           const bool keep = !__any_sync(kFull, up);  // no row of the warp moved its reference
           const uint64_t w2 = pack2(w, w), al2 = pack2(alpha, alpha);
@@ -706,7 +735,7 @@ int num_sms_attn() {
   return sms > 0 ? sms : 1;
 }
 
-template <int D, bool kDenseO>
+template <int D, bool kDenseO, bool kMx>
 cudaError_t launch_attn_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const AttnParams& p, cudaStream_t st) {
   static int configured_mask = 0;  // one bit per device ordinal (< 32)
@@ -717,10 +746,10 @@ cudaError_t launch_attn_d(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     // thread at launch; with any other launch allocation the increases would
     // never be granted, so refuse to launch.
     cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, attn_fwd_kernel<D, kDenseO>);
+    cudaError_t e = cudaFuncGetAttributes(&attr, attn_fwd_kernel<D, kDenseO, kMx>);
     if (e != cudaSuccess) return e;
     if (attr.numRegs != 65536 / kThreads) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D, kDenseO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, kDenseO, kMx>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem<D>::kAlloc);
     if (e != cudaSuccess) return e;
     if (dev < 32) configured_mask |= (1 << dev);
@@ -730,7 +759,7 @@ cudaError_t launch_attn_d(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   const long long items = static_cast<long long>(p.BH) * p.n_qt;
   const long long sms = num_sms_attn();
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
-  attn_fwd_kernel<D, kDenseO><<<grid, kThreads, Smem<D>::kAlloc, st>>>(tq, tk, tv, p);
+  attn_fwd_kernel<D, kDenseO, kMx><<<grid, kThreads, Smem<D>::kAlloc, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -740,9 +769,18 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
                         const AttnParams& p, int D, cudaStream_t st) {
   const Strides dense = contiguous_bhnd(p.H, p.N, D);
   const bool dense_o = p.os.b == dense.b && p.os.h == dense.h && p.os.n == dense.n;
+  if (p.mx) {
+    if (D == 128)
+      return dense_o ? launch_attn_d<128, true, true>(tq, tk, tv, p, st)
+                     : launch_attn_d<128, false, true>(tq, tk, tv, p, st);
+    return dense_o ? launch_attn_d<64, true, true>(tq, tk, tv, p, st)
+                   : launch_attn_d<64, false, true>(tq, tk, tv, p, st);
+  }
   if (D == 128)
-    return dense_o ? launch_attn_d<128, true>(tq, tk, tv, p, st) : launch_attn_d<128, false>(tq, tk, tv, p, st);
-  return dense_o ? launch_attn_d<64, true>(tq, tk, tv, p, st) : launch_attn_d<64, false>(tq, tk, tv, p, st);
+    return dense_o ? launch_attn_d<128, true, false>(tq, tk, tv, p, st)
+                   : launch_attn_d<128, false, false>(tq, tk, tv, p, st);
+  return dense_o ? launch_attn_d<64, true, false>(tq, tk, tv, p, st)
+                 : launch_attn_d<64, false, false>(tq, tk, tv, p, st);
 }
 
 }  // namespace sagefp4

@@ -19,11 +19,12 @@ inline Strides contiguous_bhnd(int H, int N, int D) {
   return Strides{static_cast<long long>(H) * N * D, static_cast<long long>(N) * D, D};
 }
 
+// mx: MXFP4 (groups of 32, E8M0 scales) instead of NVFP4.
 cudaError_t launch_quant_rows(const void* q, const void* k, Strides sq, Strides sk, uint8_t* qc,
                               uint8_t* qs, uint8_t* kc, uint8_t* ks, int H, int BH, int N, int D,
-                              cudaStream_t st);
+                              bool mx, cudaStream_t st);
 cudaError_t launch_quant_v(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, int H, int BH, int N,
-                           int D, int32_t* status, cudaStream_t st);
+                           int D, bool mx, int32_t* status, cudaStream_t st);
 
 struct AttnParams {
   const uint8_t* sfq;  // Q scales (block layout), per (b,h) N_pad*D/16 bytes
@@ -34,6 +35,7 @@ struct AttnParams {
   int32_t* status;
   int H, BH, N, Np, causal, n_qt;
   float a;  // log2(e) * softmax scale: the scale folded into exp2
+  int mx;   // 1: operands are MXFP4 (groups of 32, E8M0 scales), P quantized the same way
   int flags;           // kAttnWithholdK: failure-detection test (see below)
   uint64_t wait_ns;    // limit of every bounded wait in the kernel
 };
@@ -58,6 +60,7 @@ struct MmaProbeParams {
   float* d;
   int32_t* status;
   int n, K, a_by_threads;
+  int mx;  // 1: MXFP4 product (kind::mxf4, UE8M0 scales, two per row per K = 64)
 };
 cudaError_t launch_mma_probe(const CUtensorMap& ta, const CUtensorMap& tb, const MmaProbeParams& p,
                              cudaStream_t st);

@@ -139,8 +139,8 @@ extern "C" int sage_fp4_attention_noalloc(const void* q, const void* k, const vo
   // the quantize kernels, so nothing left by an earlier call is read.
   const Strides dense = contiguous_bhnd(H, N, D);
   if (launch_quant_rows(q, k, dense, dense, base + pt.qc, base + pt.qs, base + pt.kc, base + pt.ks, H,
-                        BH, N, D, st) != cudaSuccess ||
-      launch_quant_v(v, dense, base + pt.vc, base + pt.vs, H, BH, N, D, status, st) != cudaSuccess)
+                        BH, N, D, false, st) != cudaSuccess ||
+      launch_quant_v(v, dense, base + pt.vc, base + pt.vs, H, BH, N, D, false, status, st) != cudaSuccess)
     return SAGE_FP4_ECUDA;
   CUtensorMap tq, tk, tv;
   const CUtensorMapSwizzle qk_swz = (D == 128) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
@@ -163,6 +163,7 @@ extern "C" int sage_fp4_attention_noalloc(const void* q, const void* k, const vo
   p.causal = causal;
   p.n_qt = Np / 128;
   p.a = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
+  p.mx = 0;
   p.flags = 0;
   p.wait_ns = kAttnWaitNs;
   return launch_attn(tq, tk, tv, p, D, st) == cudaSuccess ? SAGE_FP4_OK : SAGE_FP4_ECUDA;

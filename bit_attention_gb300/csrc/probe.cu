@@ -106,11 +106,14 @@ __global__ void __launch_bounds__(128, 1)
         tc_cp_32x128b_warpx4(tmem + 128 + 4 * kb, smem_desc(sb + oSFA + 512 * kb, 0, 128, kSwizzleNone));
         tc_cp_32x128b_warpx4(tmem + 160 + 4 * kb, smem_desc(sb + oSFB + 512 * kb, 0, 128, kSwizzleNone));
       }
-      const uint32_t idesc = idesc_nvfp4(128, static_cast<uint32_t>(p.n));
+      const uint32_t n = static_cast<uint32_t>(p.n);
       for (int kb = 0; kb < KB; ++kb) {
         const uint64_t ad = smem_desc(sb + oA + 32 * kb, 16, sbo, swz);
         const uint64_t bd = smem_desc(sb + oB + 32 * kb, 16, sbo, swz);
-        mma_nvfp4(tmem, ad, bd, idesc, tmem + 128 + 4 * kb, tmem + 160 + 4 * kb, kb > 0);
+        if (p.mx)
+          mma_mxf4(tmem, ad, bd, idesc_mxf4(128, n), tmem + 128 + 4 * kb, tmem + 160 + 4 * kb, kb > 0);
+        else
+          mma_nvfp4(tmem, ad, bd, idesc_nvfp4(128, n), tmem + 128 + 4 * kb, tmem + 160 + 4 * kb, kb > 0);
       }
       tc_commit(bar_mma);
     }

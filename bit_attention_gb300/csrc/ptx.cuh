@@ -128,6 +128,20 @@ __device__ __forceinline__ void mma_nvfp4(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// The same product for MXFP4 operands: E2M1 codes with one UE8M0 scale per 32
+// elements, two scales per row for each K = 64 step.
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X"
+      " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
 // Arrive on an mbarrier once every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -205,12 +219,26 @@ __host__ __device__ constexpr uint32_t idesc_nvfp4(uint32_t M, uint32_t N) {
   return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// The same for kind::mxf4: scales UE8M0 (bit 23 = 1).
+__host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N) {
+  return idesc_nvfp4(M, N) | (1u << 23);
+}
+
 // ------------------------------------------------------------------ arithmetic
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
 }
+
+// MXFP4 scale of a group (OCP MX rule): the E8M0 byte is the exponent field of
+// amax minus 2 (the largest E2M1 exponent), not below 0; elements are
+// multiplied by the exact power of two 2^(127 - byte) before rounding to E2M1.
+__device__ __forceinline__ uint32_t e8m0_of(float amax) {
+  const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);
+  return static_cast<uint32_t>(e > 2 ? e - 2 : 0);
+}
+__device__ __forceinline__ float e8m0_mult(uint32_t b) { return __uint_as_float((254u - b) << 23); }
 
 // Two FP32 lanes in one 64-bit register: element 0 in the low half.
 __device__ __forceinline__ uint64_t pack2(float lo, float hi) {

@@ -1,5 +1,6 @@
 // quant.cu -- NVFP4 quantization of Q, K (groups of 16 along D) and V (groups
-// of 16 along tokens, written as V^T), bit-exact with the rule in sage_fp4.h.
+// of 16 along tokens, written as V^T), bit-exact with the rule in sage_fp4.h;
+// and the MXFP4 variant (groups of 32, E8M0 scales, same layouts).
 //
 // Method: 1x16 microscaling of both products (senqingzn.com article on
 // SageAttention3, "Solving two obstacles and one difficulty", solution 1);
@@ -79,8 +80,10 @@ __device__ __forceinline__ uint32_t pack4_bytes(uint32_t b0, uint32_t b1, uint32
 // inside one 32-row slice of the scale block layout, so a lane's scale address
 // moves by a constant from one row-step to the next.  The warp keeps all its
 // row-steps' loads in flight before it computes.  blockIdx.y selects Q (0) or
-// K (1); each input has its own strides (elements, multiples of 8).
-template <int D>
+// K (1); each input has its own strides (elements, multiples of 8).  MX: a
+// group of 32 spans four lanes, and each K = 64 step's scale word holds the
+// two E8M0 bytes in its low half.
+template <int D, bool MX>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict__ x0,
                                                          const uint4* __restrict__ x1,
                                                          Strides t0, Strides t1,
@@ -133,16 +136,24 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
       const uint4 w = raw[u];
       uint32_t m = maxabs_bf16x2(maxabs_bf16x2(w.x, w.y), maxabs_bf16x2(w.z, w.w));
       m = maxabs_bf16x2(m, __shfl_xor_sync(kFull, m, 1));
+      if constexpr (MX) m = maxabs_bf16x2(m, __shfl_xor_sync(kFull, m, 2));
       const float amax = fmaxf(fabsf(__uint_as_float(m << 16)), fabsf(__uint_as_float(m & 0xFFFF0000u)));
-      const uint32_t sb = cvt_e4m3(div6(amax));
-      const float r = rtab[sb];
       float v[8];
       bf16x8_to_f32(w, v);
-      const uint32_t word = (r != 0.0f) ? encode8(v, r) : 0u;
+      uint32_t word, sw;
+      if constexpr (MX) {
+        const uint32_t e8 = e8m0_of(amax);
+        word = encode8(v, e8m0_mult(e8));
+        sw = pack4_bytes(e8, __shfl_down_sync(kFull, e8, 4), 0u, 0u);
+      } else {
+        const uint32_t sb = cvt_e4m3(div6(amax));
+        const float r = rtab[sb];
+        word = (r != 0.0f) ? encode8(v, r) : 0u;
+        // four consecutive groups' scales form one 32-bit word of the block layout
+        sw = pack4_bytes(sb, __shfl_down_sync(kFull, sb, 2), __shfl_down_sync(kFull, sb, 4),
+                         __shfl_down_sync(kFull, sb, 6));
+      }
       *reinterpret_cast<uint32_t*>(cdst + u * RPW * (D / 2)) = word;
-      // four consecutive groups' scales form one 32-bit word of the block layout
-      const uint32_t sw = pack4_bytes(sb, __shfl_down_sync(kFull, sb, 2), __shfl_down_sync(kFull, sb, 4),
-                                      __shfl_down_sync(kFull, sb, 6));
       if ((sub & 7) == 0) *reinterpret_cast<uint32_t*>(sdst + u * RPW * 16) = sw;
     }
   }
@@ -155,13 +166,17 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
 // tile when a head's tokens are contiguous (token stride D), else one copy
 // per token row, spread over the lanes of warp 0.  A work item is one channel
 // pair over 32 tokens (two groups along tokens): it writes 16 code bytes to
-// each of two V^T rows and one 16-bit half of a scale word per row.
-template <int D, int TT, int NS>
+// each of two V^T rows and one 16-bit half of a scale word per row.  MX: the
+// 32 tokens are one group; its E8M0 byte goes to byte `seg` of the tile's
+// scale word (a 64-token tile is one K = 64 step), and seg 0 zeroes the
+// word's upper half.
+template <int D, int TT, int NS, bool MX>
 __global__ void __launch_bounds__(128) quant_v_kernel(const uint8_t* __restrict__ v, Strides sv,
                                                       uint8_t* __restrict__ vc,
                                                       uint8_t* __restrict__ vs, int H, int BH,
                                                       int N, int Np, int32_t* status) {
   static_assert(TT == 64 || TT == 128, "tile of 64 or 128 tokens");
+  static_assert(!MX || TT == 64, "MX scale words follow 64-token tiles");
   constexpr int TILE_BYTES = TT * D * 2;
   constexpr int ITEMS = (D / 2) * (TT / 32);
   extern __shared__ __align__(128) uint8_t qv_smem[];
@@ -252,6 +267,40 @@ __global__ void __launch_bounds__(128) quant_v_kernel(const uint8_t* __restrict_
     for (int item = threadIdx.x; item < ITEMS; item += 128) {
       const int pch = item % (D / 2);  // channel pair
       const int seg = item / (D / 2);  // 32-token segment of the tile
+      if constexpr (MX) {
+        uint32_t m = 0u;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) m = maxabs_bf16x2(m, tile[(seg * 32 + j) * (D / 2) + pch]);
+        const uint32_t elo = e8m0_of(fabsf(__uint_as_float(m << 16)));
+        const uint32_t ehi = e8m0_of(fabsf(__uint_as_float(m & 0xFFFF0000u)));
+        const float rlo = e8m0_mult(elo), rhi = e8m0_mult(ehi);
+        uint32_t clo[4], chi[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float lo[8], hi[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t wv = tile[(seg * 32 + q * 8 + j) * (D / 2) + pch];
+            lo[j] = __uint_as_float(wv << 16);
+            hi[j] = __uint_as_float(wv & 0xFFFF0000u);
+          }
+          clo[q] = encode8(lo, rlo);
+          chi[q] = encode8(hi, rhi);
+        }
+        const int d0 = 2 * pch, d1 = 2 * pch + 1;
+        const size_t col = static_cast<size_t>(tb) * (TT / 2) + seg * 16;
+        *reinterpret_cast<uint4*>(vc + (static_cast<size_t>(bh) * D + d0) * vt_row + col) =
+            make_uint4(clo[0], clo[1], clo[2], clo[3]);
+        *reinterpret_cast<uint4*>(vc + (static_cast<size_t>(bh) * D + d1) * vt_row + col) =
+            make_uint4(chi[0], chi[1], chi[2], chi[3]);
+        vs_bh[sf_offset(d0, tb * 4 + seg, Np / 16)] = static_cast<uint8_t>(elo);
+        vs_bh[sf_offset(d1, tb * 4 + seg, Np / 16)] = static_cast<uint8_t>(ehi);
+        if (seg == 0) {
+          *reinterpret_cast<uint16_t*>(vs_bh + sf_offset(d0, tb * 4 + 2, Np / 16)) = 0;
+          *reinterpret_cast<uint16_t*>(vs_bh + sf_offset(d1, tb * 4 + 2, Np / 16)) = 0;
+        }
+        continue;
+      }
       uint32_t clo[4], chi[4];
       uint32_t sbl[2], sbh[2];
 #pragma unroll
@@ -315,7 +364,7 @@ int num_sms() {
 
 cudaError_t launch_quant_rows(const void* q, const void* k, Strides sq, Strides sk, uint8_t* qc,
                               uint8_t* qs, uint8_t* kc, uint8_t* ks, int H, int BH, int N, int D,
-                              cudaStream_t st) {
+                              bool mx, cudaStream_t st) {
   const int Np = round_up_int(N, 128);
   const long long chunks = static_cast<long long>(BH) * Np / (D == 128 ? 16 : 32);  // one warp each
   long long blocks = (chunks + 7) / 8;
@@ -323,18 +372,23 @@ cudaError_t launch_quant_rows(const void* q, const void* k, Strides sq, Strides 
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   dim3 grid(static_cast<unsigned>(blocks), 2);
-  if (D == 128)
-    quant_rows_kernel<128><<<grid, 256, 0, st>>>(static_cast<const uint4*>(q),
-                                                 static_cast<const uint4*>(k), sq, sk, qc, qs, kc,
-                                                 ks, H, BH, N, Np);
-  else
-    quant_rows_kernel<64><<<grid, 256, 0, st>>>(static_cast<const uint4*>(q),
-                                                static_cast<const uint4*>(k), sq, sk, qc, qs, kc,
-                                                ks, H, BH, N, Np);
+  const uint4* x0 = static_cast<const uint4*>(q);
+  const uint4* x1 = static_cast<const uint4*>(k);
+  if (D == 128) {
+    if (mx)
+      quant_rows_kernel<128, true><<<grid, 256, 0, st>>>(x0, x1, sq, sk, qc, qs, kc, ks, H, BH, N, Np);
+    else
+      quant_rows_kernel<128, false><<<grid, 256, 0, st>>>(x0, x1, sq, sk, qc, qs, kc, ks, H, BH, N, Np);
+  } else {
+    if (mx)
+      quant_rows_kernel<64, true><<<grid, 256, 0, st>>>(x0, x1, sq, sk, qc, qs, kc, ks, H, BH, N, Np);
+    else
+      quant_rows_kernel<64, false><<<grid, 256, 0, st>>>(x0, x1, sq, sk, qc, qs, kc, ks, H, BH, N, Np);
+  }
   return cudaGetLastError();
 }
 
-template <int D, int TT, int NS>
+template <int D, int TT, int NS, bool MX>
 cudaError_t launch_quant_v_cfg(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, int H, int BH,
                                int Np, int N, int32_t* status, int blocks_per_sm, cudaStream_t st) {
   const long long work = static_cast<long long>(Np / TT) * BH;
@@ -342,24 +396,27 @@ cudaError_t launch_quant_v_cfg(const void* v, Strides sv, uint8_t* vc, uint8_t* 
   long long blocks = static_cast<long long>(num_sms()) * blocks_per_sm;
   if (blocks > work) blocks = work;
   if (blocks < 1) blocks = 1;
-  const cudaError_t e =
-      cudaFuncSetAttribute(quant_v_kernel<D, TT, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const cudaError_t e = cudaFuncSetAttribute(quant_v_kernel<D, TT, NS, MX>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  quant_v_kernel<D, TT, NS><<<static_cast<unsigned>(blocks), 128, smem, st>>>(
+  quant_v_kernel<D, TT, NS, MX><<<static_cast<unsigned>(blocks), 128, smem, st>>>(
       static_cast<const uint8_t*>(v), sv, vc, vs, H, BH, N, Np, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_v(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, int H, int BH, int N,
-                           int D, int32_t* status, cudaStream_t st) {
+                           int D, bool mx, int32_t* status, cudaStream_t st) {
   const int Np = round_up_int(N, 128);
   // 64-token tiles, double-buffered: 32 KB (D = 128) or 16 KB (D = 64) of
   // shared memory per block.  The per-tile arithmetic, not the copy latency,
   // sets the pace, so more resident blocks beat deeper rings (measured on
   // GB300: 5.3-5.8 TB/s at D = 128 with six blocks per SM, against 4.0-4.9 TB/s
   // with four-deep rings and two or three blocks).
-  if (D == 128) return launch_quant_v_cfg<128, 64, 2>(v, sv, vc, vs, H, BH, Np, N, status, 6, st);
-  return launch_quant_v_cfg<64, 64, 2>(v, sv, vc, vs, H, BH, Np, N, status, 8, st);
+  if (D == 128)
+    return mx ? launch_quant_v_cfg<128, 64, 2, true>(v, sv, vc, vs, H, BH, Np, N, status, 6, st)
+              : launch_quant_v_cfg<128, 64, 2, false>(v, sv, vc, vs, H, BH, Np, N, status, 6, st);
+  return mx ? launch_quant_v_cfg<64, 64, 2, true>(v, sv, vc, vs, H, BH, Np, N, status, 8, st)
+            : launch_quant_v_cfg<64, 64, 2, false>(v, sv, vc, vs, H, BH, Np, N, status, 8, st);
 }
 
 }  // namespace sagefp4

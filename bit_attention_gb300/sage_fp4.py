@@ -19,6 +19,7 @@ import threading
 from . import build as _build
 
 OK, EINVAL, ECUDA, ETIMEOUT, EUNSUPPORTED, ETOOLARGE = 0, -1, -2, -3, -4, -5
+FORMATS = {"nvfp4": 0, "mxfp4": 1}  # SAGE_FP4_FORMAT_*
 
 _HEADER = os.path.join(_build.ROOT, "include", "sage_fp4.h")
 _lock = threading.Lock()
@@ -67,13 +68,14 @@ def load(build: bool = True) -> ctypes.CDLL:
                 "sage_fp4_qkv_from_workspace": (i, [vp, sz, i, i, i, i, qp]),
                 "sage_fp4_quantize_qkv": (i, [vp, vp, vp, qp, i, i, i, i, vp]),
                 "sage_fp4_attn_fwd": (i, [qp, vp, i, i, i, i, i, vp]),
-                "sage_fp4_quantize_qkv_strided": (i, [vp, sp, vp, sp, vp, sp, qp, i, i, i, i, vp]),
-                "sage_fp4_attn_fwd_ex": (i, [qp, vp, sp, i, i, i, i, i, ctypes.c_float, vp]),
+                "sage_fp4_quantize_qkv_strided": (i, [vp, sp, vp, sp, vp, sp, qp, i, i, i, i, i, vp]),
+                "sage_fp4_attn_fwd_ex": (i, [qp, vp, sp, i, i, i, i, i, ctypes.c_float, i, vp]),
                 "sage_fp4_attn_fwd_stall_test": (i, [qp, vp, i, i, i, i, i, ctypes.c_uint64, vp]),
                 "sage_fp4_get_status": (i, [qp, vp]),
                 "sage_fp4_strerror": (ctypes.c_char_p, [i]),
                 "sage_fp4_cvt_probe": (i, [u32, u32, vp, vp, vp]),
                 "sage_fp4_mma_probe": (i, [vp, vp, vp, vp, i, i, i, vp, vp, vp]),
+                "sage_fp4_mma_probe_mx": (i, [vp, vp, vp, vp, i, i, i, vp, vp, vp]),
                 "sage_fp4_attention_noalloc": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, vp]),
                 "sage_fp4_host_workspace_bytes": (sz, [i, i, i, i]),
                 "sage_fp4_attention_host": (i, [vp, vp, vp, vp, i, i, i, i, i, vp, sz, vp, vp]),
@@ -118,20 +120,21 @@ def sage_fp4_attn_fwd(qkv: sage_fp4_qkv, o_ptr, B, H, N, D, causal, stream) -> i
 
 
 def sage_fp4_quantize_qkv_strided(q_ptr, q_strides, k_ptr, k_strides, v_ptr, v_strides,
-                                  qkv: sage_fp4_qkv, B, H, N, D, stream) -> int:
-    """Strides: sage_fp4_strides or None (contiguous [B,H,N,D])."""
+                                  qkv: sage_fp4_qkv, B, H, N, D, stream, fmt: int = 0) -> int:
+    """Strides: sage_fp4_strides or None (contiguous [B,H,N,D]); fmt: SAGE_FP4_FORMAT_*."""
     r = ctypes.byref
     return load().sage_fp4_quantize_qkv_strided(
         q_ptr, r(q_strides) if q_strides is not None else None, k_ptr,
         r(k_strides) if k_strides is not None else None, v_ptr,
-        r(v_strides) if v_strides is not None else None, ctypes.byref(qkv), B, H, N, D, stream)
+        r(v_strides) if v_strides is not None else None, ctypes.byref(qkv), B, H, N, D, int(fmt),
+        stream)
 
 
 def sage_fp4_attn_fwd_ex(qkv: sage_fp4_qkv, o_ptr, o_strides, B, H, N, D, causal, softmax_scale,
-                         stream) -> int:
+                         stream, fmt: int = 0) -> int:
     return load().sage_fp4_attn_fwd_ex(ctypes.byref(qkv), o_ptr,
                                        ctypes.byref(o_strides) if o_strides is not None else None,
-                                       B, H, N, D, int(causal), float(softmax_scale), stream)
+                                       B, H, N, D, int(causal), float(softmax_scale), int(fmt), stream)
 
 
 def sage_fp4_attn_fwd_stall_test(qkv: sage_fp4_qkv, o_ptr, B, H, N, D, causal, wait_limit_ns,
@@ -156,6 +159,12 @@ def sage_fp4_mma_probe(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threads,
                        stream) -> int:
     return load().sage_fp4_mma_probe(a_codes, a_scales, b_codes, b_scales, n, K,
                                      int(a_by_threads), d, status, stream)
+
+
+def sage_fp4_mma_probe_mx(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threads, d, status,
+                          stream) -> int:
+    return load().sage_fp4_mma_probe_mx(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threads, d,
+                                        status, stream)
 
 
 def sage_fp4_attention_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, status_ptr, B, H, N, D, causal,
@@ -264,18 +273,30 @@ def _check_input(x, B, H, N, D, name):
         raise SageFp4Error(EINVAL, f"{name} has shape {tuple(x.shape)}, expected {(B, H, N, D)}")
 
 
-def quantize_qkv(q, k, v, out: QuantizedQKV | None = None, stream=None) -> QuantizedQKV:
-    """bf16 [B,H,N,D] Q, K, V on the GPU -> NVFP4 operands (one call, two kernels)."""
+def quantize_qkv(q, k, v, out: QuantizedQKV | None = None, stream=None,
+                 fmt: str = "nvfp4") -> QuantizedQKV:
+    """bf16 [B,H,N,D] Q, K, V on the GPU -> NVFP4 (or MXFP4) operands (one call, two kernels)."""
     B, H, N, D = q.shape
     for x, nm in ((q, "q"), (k, "k"), (v, "v")):
         _check_input(x, B, H, N, D, nm)
     if out is None:
         out = QuantizedQKV(B, H, N, D, device=q.device)
         _order_after_current(stream, out.workspace)
-    rc = sage_fp4_quantize_qkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.struct, B, H, N, D,
-                               _stream(stream))
+    if fmt == "nvfp4":
+        rc = sage_fp4_quantize_qkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.struct, B, H, N, D,
+                                   _stream(stream))
+    else:
+        rc = sage_fp4_quantize_qkv_strided(q.data_ptr(), None, k.data_ptr(), None, v.data_ptr(), None,
+                                           out.struct, B, H, N, D, _stream(stream), _fmt(fmt))
     _check(rc, "sage_fp4_quantize_qkv")
+    out.fmt = fmt
     return out
+
+
+def _fmt(fmt: str) -> int:
+    if fmt not in FORMATS:
+        raise SageFp4Error(EINVAL, f"format must be one of {tuple(FORMATS)}, not {fmt!r}")
+    return FORMATS[fmt]
 
 
 def attn_fwd(qkv: QuantizedQKV, causal: bool = False, out=None, stream=None, scale=None):
@@ -288,11 +309,13 @@ def attn_fwd(qkv: QuantizedQKV, causal: bool = False, out=None, stream=None, sca
         out = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=qkv.workspace.device)
     else:
         _check_input(out, B, H, N, D, "out")
-    if scale is None:
+    fmt = getattr(qkv, "fmt", "nvfp4")
+    if scale is None and fmt == "nvfp4":
         rc = sage_fp4_attn_fwd(qkv.struct, out.data_ptr(), B, H, N, D, causal, _stream(stream))
     else:
-        rc = sage_fp4_attn_fwd_ex(qkv.struct, out.data_ptr(), None, B, H, N, D, causal, scale,
-                                  _stream(stream))
+        sc = 1.0 / (D ** 0.5) if scale is None else float(scale)
+        rc = sage_fp4_attn_fwd_ex(qkv.struct, out.data_ptr(), None, B, H, N, D, causal, sc,
+                                  _stream(stream), _fmt(fmt))
     _check(rc, "sage_fp4_attn_fwd")
     return out
 
@@ -316,12 +339,13 @@ def _bhnd(x, layout: str, name: str):
 
 
 def attention(q, k, v, causal: bool = False, scale=None, layout: str = "HND", out=None,
-              stream=None):
+              stream=None, fmt: str = "nvfp4"):
     """Plug-and-play SageAttention3 FP4 attention: bf16 Q, K, V -> bf16 O.
 
     layout: "HND" ([B,H,N,D]) or "NHD" ([B,N,H,D]); the tensors may be any
     views whose last axis is contiguous (e.g. slices of a packed QKV tensor),
     with 16-byte aligned rows.  scale: softmax scale (default 1/sqrt(D)).
+    fmt: "nvfp4" (the method's) or "mxfp4" (the alternative the pages weighed).
     O is a new contiguous tensor in `layout` unless `out` is given.
     Quantization runs in a temporary workspace; three kernel launches."""
     import torch
@@ -339,10 +363,11 @@ def attention(q, k, v, causal: bool = False, scale=None, layout: str = "HND", ou
     z = QuantizedQKV(B, H, N, D, device=q.device)
     _order_after_current(stream, z.workspace, out)
     st = _stream(stream)
+    f = _fmt(fmt)
     _check(sage_fp4_quantize_qkv_strided(q.data_ptr(), sq, k.data_ptr(), sk, v.data_ptr(), sv, z.struct,
-                                         B, H, N, D, st), "sage_fp4_quantize_qkv_strided")
+                                         B, H, N, D, st, f), "sage_fp4_quantize_qkv_strided")
     sc = 1.0 / (D ** 0.5) if scale is None else float(scale)
-    _check(sage_fp4_attn_fwd_ex(z.struct, out.data_ptr(), so, B, H, N, D, causal, sc, st),
+    _check(sage_fp4_attn_fwd_ex(z.struct, out.data_ptr(), so, B, H, N, D, causal, sc, st, f),
            "sage_fp4_attn_fwd_ex")
     return out
 

@@ -14,14 +14,15 @@ from . import sage_fp4 as _S
 
 @torch.library.custom_op("sage_fp4::attention", mutates_args=())
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
-              scale: Optional[float] = None, layout: str = "HND") -> torch.Tensor:
+              scale: Optional[float] = None, layout: str = "HND", fmt: str = "nvfp4") -> torch.Tensor:
     """SageAttention3 FP4 attention of bf16 Q, K, V in layout "HND" ([B,H,N,D])
-    or "NHD" ([B,N,H,D]) -> new contiguous bf16 O in the same layout."""
-    return _S.attention(q, k, v, causal=causal, scale=scale, layout=layout)
+    or "NHD" ([B,N,H,D]) -> new contiguous bf16 O in the same layout; fmt
+    "nvfp4" (the method's) or "mxfp4"."""
+    return _S.attention(q, k, v, causal=causal, scale=scale, layout=layout, fmt=fmt)
 
 
 @attention.register_fake
-def _attention_fake(q, k, v, causal=False, scale=None, layout="HND"):
-    if layout not in _S.LAYOUTS:
-        raise ValueError(f"layout must be one of {_S.LAYOUTS}")
+def _attention_fake(q, k, v, causal=False, scale=None, layout="HND", fmt="nvfp4"):
+    if layout not in _S.LAYOUTS or fmt not in _S.FORMATS:
+        raise ValueError(f"layout must be one of {_S.LAYOUTS}, fmt one of {tuple(_S.FORMATS)}")
     return torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)

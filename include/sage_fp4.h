@@ -79,6 +79,22 @@ extern "C" {
 #define SAGE_FP4_EUNSUPPORTED (-4) /* device is not sm_103 (the kernels are built for sm_103a) */
 #define SAGE_FP4_ETOOLARGE (-5)   /* problem needs more than the no-allocation entry's fixed scratch */
 
+/* Microscaling formats of the quantized operands.  NVFP4 is the method's:
+ * E2M1 codes with one E4M3 scale per 16 elements.  MXFP4 is the alternative
+ * the pages weighed and set aside for accuracy ([NEWS-HW] data-type
+ * paragraph): E2M1 codes with one E8M0 scale (a power of two, 2^(b-127)) per
+ * 32 elements.  Scale rule for an MXFP4 group (the OCP MX v1.0 conversion;
+ * the pages fix only the format): b = max(exponent field of amax - 2, 0),
+ * code_i = E2M1_rn(x_i * 2^(127-b)), saturating.  MXFP4 operands use the
+ * same layouts and sizes as NVFP4: in each 32-bit scale word of the block
+ * layout (one per row and K = 64 step) bytes 0 and 1 hold the step's two E8M0
+ * scales and bytes 2 and 3 are zero.  In attention, P is quantized in the
+ * same format; its first level then normalises each row segment's maximum
+ * to 6 instead of 448*6 (E8M0 needs no range help, and 6 keeps the maximum
+ * exact). */
+#define SAGE_FP4_FORMAT_NVFP4 0
+#define SAGE_FP4_FORMAT_MXFP4 1
+
 typedef struct sage_fp4_tensor {
   uint8_t *codes;  /* packed E2M1, 16-byte aligned */
   uint8_t *scales; /* E4M3 in the 128x4 block layout, 16-byte aligned */
@@ -122,14 +138,16 @@ int sage_fp4_quantize_qkv(const void *q, const void *k, const void *v, const sag
 /* sage_fp4_quantize_qkv for inputs in any layout with a contiguous D axis:
  * q, k and v each with its own strides (NULL = contiguous [B,H,N,D]); 16-byte
  * aligned device memory.  The quantized operands are the same as for the
- * contiguous copies of the inputs, bit for bit.  SAGE_FP4_EINVAL for a
- * negative or unaligned stride or offsets beyond 2^62 elements.  No
+ * contiguous copies of the inputs, bit for bit.  format: SAGE_FP4_FORMAT_NVFP4
+ * (as sage_fp4_quantize_qkv) or SAGE_FP4_FORMAT_MXFP4.  SAGE_FP4_EINVAL for
+ * another format, a negative or unaligned stride, or offsets beyond 2^62
+ * elements.  No
  * counterpart in the pages, which describe no API (the plug-and-play use of
  * the abstract). */
 int sage_fp4_quantize_qkv_strided(const void *q, const sage_fp4_strides *q_strides, const void *k,
                                   const sage_fp4_strides *k_strides, const void *v,
                                   const sage_fp4_strides *v_strides, const sage_fp4_qkv *out,
-                                  int B, int H, int N, int D, void *stream);
+                                  int B, int H, int N, int D, int format, void *stream);
 
 /* Attention forward over quantized operands: O = softmax(Q K^T / sqrt(D)) V
  * computed by the SageAttention3 FP4 method (block-scaled FP4 MMAs with FP32
@@ -146,9 +164,12 @@ int sage_fp4_attn_fwd(const sage_fp4_qkv *qkv, void *o, int B, int H, int N, int
  * 1e30 (sage_fp4_attn_fwd uses 1/sqrt(D)); anything else is SAGE_FP4_EINVAL.
  * The scale multiplies S before the exponentials of the online softmax and of
  * the first P-quantization level (the pages give the method no scale; this is
- * the one a drop-in attention takes). */
+ * the one a drop-in attention takes).  format: the format the operands were
+ * quantized in (SAGE_FP4_FORMAT_NVFP4 or SAGE_FP4_FORMAT_MXFP4); P is
+ * quantized in the same one. */
 int sage_fp4_attn_fwd_ex(const sage_fp4_qkv *qkv, void *o, const sage_fp4_strides *o_strides, int B,
-                         int H, int N, int D, int causal, float softmax_scale, void *stream);
+                         int H, int N, int D, int causal, float softmax_scale, int format,
+                         void *stream);
 
 /* No counterpart in the pages: the failure-detection test of the attention
  * kernel's bounded waits.  The same launch as sage_fp4_attn_fwd, except that
@@ -263,6 +284,15 @@ int sage_fp4_cvt_probe(uint32_t first, uint32_t count, uint8_t *e2m1, uint8_t *e
 int sage_fp4_mma_probe(const uint8_t *a_codes, const uint8_t *a_scales, const uint8_t *b_codes,
                        const uint8_t *b_scales, int n, int K, int a_by_threads, float *d,
                        int32_t *status, void *stream);
+
+/* The same product for MXFP4 operands (kind::mxf4: E2M1 codes, one E8M0
+ * scale per 32 elements, [NEWS-HW]'s alternative format).  Scales are given as
+ * for sage_fp4_mma_probe, 512 bytes per K = 64 step in the block layout's
+ * positions: the word of row r holds that row's two E8M0 scales of the step
+ * in bytes 0 and 1; bytes 2 and 3 are not read. */
+int sage_fp4_mma_probe_mx(const uint8_t *a_codes, const uint8_t *a_scales, const uint8_t *b_codes,
+                          const uint8_t *b_scales, int n, int K, int a_by_threads, float *d,
+                          int32_t *status, void *stream);
 
 #ifdef __cplusplus
 }

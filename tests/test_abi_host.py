@@ -136,8 +136,8 @@ def test_strided_quantize_and_scaled_attention_reject_bad_arguments():
     q = _qkv()
     B, H, N, D = 1, 2, 512, 128
 
-    def quant(sq=None, sk=None, sv=None):
-        return S.sage_fp4_quantize_qkv_strided(0x1000, sq, 0x2000, sk, 0x3000, sv, q, B, H, N, D, None)
+    def quant(sq=None, sk=None, sv=None, fmt=0):
+        return S.sage_fp4_quantize_qkv_strided(0x1000, sq, 0x2000, sk, 0x3000, sv, q, B, H, N, D, None, fmt)
 
     nhd = S.sage_fp4_strides(N * H * D, D, H * D)
     for bad in (S.sage_fp4_strides(N * H * D, D, H * D + 4),   # 8-byte rows
@@ -145,14 +145,16 @@ def test_strided_quantize_and_scaled_attention_reject_bad_arguments():
                 S.sage_fp4_strides(N * H * D, 1 << 62, H * D)):  # offsets past 2^62
         assert quant(sq=bad) == S.EINVAL
         assert quant(sv=bad) == S.EINVAL
+    assert quant(fmt=2) == S.EINVAL and quant(fmt=-1) == S.EINVAL
     assert S.sage_fp4_quantize_qkv_strided(0x1000, nhd, 0x2000, nhd, 0x3000, nhd, q, 0, H, N, D, None) == S.OK
 
-    def attn(scale, so=None, causal=0):
-        return S.sage_fp4_attn_fwd_ex(q, 0x4000, so, B, H, N, D, causal, scale, None)
+    def attn(scale, so=None, causal=0, fmt=0):
+        return S.sage_fp4_attn_fwd_ex(q, 0x4000, so, B, H, N, D, causal, scale, None, fmt)
 
     for bad in (0.0, -0.1, float("inf"), float("nan"), 1e31):
         assert attn(bad) == S.EINVAL, bad
     assert attn(0.1, so=S.sage_fp4_strides(N * H * D, D, 12)) == S.EINVAL
+    assert attn(0.1, fmt=7) == S.EINVAL
     assert S.sage_fp4_attn_fwd_ex(q, 0x4000, nhd, 0, H, N, D, 0, 0.1, None) == S.OK
 
 
