@@ -55,6 +55,9 @@ def compare(q, k, v, causal, rows=None, label=""):
     (2, 2, 300, 64, True, "k_head_mean"),
     (1, 1, 17, 128, False, "iid"),
     (1, 1, 17, 64, True, "iid"),
+    (1, 1, 1, 128, False, "iid"),      # a single token
+    (2, 1, 1, 64, True, "iid"),
+    (1, 2, 129, 128, True, "iid"),     # one key past a tile
     (1, 1, 128, 64, False, "iid"),
     (1, 2, 1000, 128, True, "k_channel_outliers"),
     (1, 2, 1100, 128, False, "k_channel_outliers"),
@@ -87,3 +90,19 @@ def test_full_workloads_sampled(name):
     q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.pattern, seed=0)
     rows = None if name == "small" else sample_rows(w.B * w.H, w.N, per_head=6, seed=1)
     compare(q, k, v, w.causal, rows=rows, label=w.name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_long_sequence_sampled(causal):
+    # 128K tokens in one head: 1024 query tiles, up to 1024 KV tiles per row
+    B, H, N, D = 1, 1, 131072, 128
+    q, k, v = make_qkv(B, H, N, D, "k_channel_outliers", seed=12)
+    compare(q, k, v, causal, rows=sample_rows(B * H, N, per_head=24, seed=2),
+            label=f"N={N} causal={causal}")
+
+
+def test_many_heads_sampled():
+    # 1024 (batch, head) pairs of one tile each: many short items per CTA
+    B, H, N, D = 8, 128, 100, 64
+    q, k, v = make_qkv(B, H, N, D, "k_head_mean", seed=13)
+    compare(q, k, v, True, rows=sample_rows(B * H, N, per_head=2, seed=3), label="B8 H128 N100")
