@@ -340,6 +340,11 @@ def main():
         except Exception as exc:  # context only
             context = {"sdpa_bf16": f"unavailable: {type(exc).__name__}"}
 
+    # context: the rate the tensor cores sustain on the attention kernel's own
+    # MMA instruction (back-to-back, operands in shared memory), after the
+    # timed region
+    fp4_mma = S.mma_peak_tflops(n=256)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         v_cpu, secs, rows, threads = cpu_oracle_sample(w, args.cpu_seconds, fmt=args.fmt)
@@ -367,7 +372,9 @@ def main():
                          "unit": "TFLOP/s", "frac": attn_tops / fp4_peak,
                          "traffic": ATTN_TRAFFIC.get(w.name) if args.fmt == "nvfp4" else None,
                          "traffic_unit": "DRAM bytes (read + write) per attention launch, from ncu",
-                         "peak_src": f"{pk['src']} bf16 x {FP4_OVER_BF16:g} (nominal FP4/BF16)"},
+                         "peak_src": f"{pk['src']} bf16 x {FP4_OVER_BF16:g} (nominal FP4/BF16)",
+                         "fp4_mma_measured_tflops": fp4_mma,
+                         "frac_of_fp4_mma_measured": attn_tops / fp4_mma},
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk.summary(),
             "gpu_launches": 3 * args.steps,
         }

@@ -337,6 +337,13 @@ int sage_fp4_mma_probe(const uint8_t* a_codes, const uint8_t* a_scales, const ui
   return mma_probe_impl(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threads, 0, d, status, stream);
 }
 
+int sage_fp4_mma_peak(int iters, int n, int32_t* status, void* stream) {
+  if (iters < 1 || iters > 1000000 || (n != 128 && n != 256) || !aligned(status, 4)) return SAGE_FP4_EINVAL;
+  int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  return from_cuda(launch_mma_peak(iters, n, status, static_cast<cudaStream_t>(stream)));
+}
+
 int sage_fp4_mma_probe_mx(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* b_codes,
                           const uint8_t* b_scales, int n, int K, int a_by_threads, float* d,
                           int32_t* status, void* stream) {

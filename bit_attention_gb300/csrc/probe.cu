@@ -150,6 +150,56 @@ cudaError_t launch_mma_probe_k(const CUtensorMap& ta, const CUtensorMap& tb,
   return cudaGetLastError();
 }
 
+// Tensor-core rate of the attention kernel's MMA instruction: one CTA per
+// SM, one thread issuing `iters` back-to-back block-scaled FP4 MMAs (D += A
+// B^T, M = 128, N = n, K = 64) on operands held in shared memory (bytes of
+// a fixed pseudo-random pattern), then one commit.  The caller times the
+// launch; FLOPs = 2 * 128 * n * 64 * iters per CTA.
+__global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int n, int32_t* err) {
+  constexpr int oA = 0, oB = 4096, oSF = oB + 256 * 32, oBar = oSF + 3 * 512;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_addr(sm);
+  const int warp = threadIdx.x >> 5;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + oBar + 8);
+  // operand bytes: a fixed pattern; scale bytes: E4M3 values 0.5 .. 2
+  for (int i = threadIdx.x; i < oSF / 4; i += blockDim.x)
+    reinterpret_cast<uint32_t*>(sm)[i] = (static_cast<uint32_t>(i) * 2654435761u) ^ 0x5A5A5A5Au;
+  for (int i = threadIdx.x; i < 3 * 512; i += blockDim.x) sm[oSF + i] = static_cast<uint8_t>(0x30 + (i * 7) % 16);
+  fence_proxy_async_smem();
+  if (threadIdx.x == 0) {
+    mbar_init(sb + oBar, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_addr(slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+  if (threadIdx.x == 0) {
+    // scale factors: A in columns 256..259, B in 264..271 (two 128-row blocks)
+    tc_cp_32x128b_warpx4(tmem + 256, smem_desc(sb + oSF, 0, 128, kSwizzleNone));
+    tc_cp_32x128b_warpx4(tmem + 264, smem_desc(sb + oSF + 512, 0, 128, kSwizzleNone));
+    tc_cp_32x128b_warpx4(tmem + 268, smem_desc(sb + oSF + 1024, 0, 128, kSwizzleNone));
+    const uint64_t ad = smem_desc(sb + oA, 16, 8 * 32, kSwizzle32B);
+    const uint64_t bd = smem_desc(sb + oB, 16, 8 * 32, kSwizzle32B);
+    const uint32_t idesc = idesc_nvfp4(128, static_cast<uint32_t>(n));
+    for (int i = 0; i < iters; ++i) mma_nvfp4(tmem, ad, bd, idesc, tmem + 256, tmem + 264, i > 0);
+    tc_commit(sb + oBar);
+    probe_wait(sb + oBar, 0, err);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_cvt_probe(uint32_t first, uint32_t count, uint8_t* e2m1, uint8_t* e4m3,
@@ -158,6 +208,17 @@ cudaError_t launch_cvt_probe(uint32_t first, uint32_t count, uint8_t* e2m1, uint
   if (blocks > 152 * 32) blocks = 152 * 32;
   if (blocks == 0) blocks = 1;
   cvt_probe_kernel<<<blocks, 256, 0, st>>>(first, count, e2m1, e4m3);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mma_peak(int iters, int n, int32_t* status, cudaStream_t st) {
+  const int smem = 4096 + 256 * 32 + 3 * 512 + 64 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(mma_peak_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  mma_peak_kernel<<<sms > 0 ? sms : 1, 128, smem, st>>>(iters, n, status);
   return cudaGetLastError();
 }
 

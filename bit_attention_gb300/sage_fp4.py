@@ -76,6 +76,7 @@ def load(build: bool = True) -> ctypes.CDLL:
                 "sage_fp4_cvt_probe": (i, [u32, u32, vp, vp, vp]),
                 "sage_fp4_mma_probe": (i, [vp, vp, vp, vp, i, i, i, vp, vp, vp]),
                 "sage_fp4_mma_probe_mx": (i, [vp, vp, vp, vp, i, i, i, vp, vp, vp]),
+                "sage_fp4_mma_peak": (i, [i, i, vp, vp]),
                 "sage_fp4_attention_noalloc": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, vp]),
                 "sage_fp4_host_workspace_bytes": (sz, [i, i, i, i]),
                 "sage_fp4_attention_host": (i, [vp, vp, vp, vp, i, i, i, i, i, vp, sz, vp, vp]),
@@ -165,6 +166,30 @@ def sage_fp4_mma_probe_mx(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threa
                           stream) -> int:
     return load().sage_fp4_mma_probe_mx(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threads, d,
                                         status, stream)
+
+
+def sage_fp4_mma_peak(iters, n, status_ptr, stream) -> int:
+    return load().sage_fp4_mma_peak(iters, n, status_ptr, stream)
+
+
+def mma_peak_tflops(n: int = 256, iters: int = 20000, repeats: int = 3) -> float:
+    """Best of `repeats` timed launches of sage_fp4_mma_peak, in TFLOP/s."""
+    import torch
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream()
+    _check(sage_fp4_mma_peak(iters, n, status.data_ptr(), st.cuda_stream), "sage_fp4_mma_peak")
+    best = float("inf")
+    for _ in range(repeats):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        _check(sage_fp4_mma_peak(iters, n, status.data_ptr(), st.cuda_stream), "sage_fp4_mma_peak")
+        e1.record(st)
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    if int(status.item()) != 0:
+        raise SageFp4Error(int(status.item()), "sage_fp4_mma_peak")
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return 2.0 * 128 * n * 64 * iters * sms / (best * 1e-3) / 1e12
 
 
 def sage_fp4_attention_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, status_ptr, B, H, N, D, causal,

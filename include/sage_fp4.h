@@ -294,6 +294,16 @@ int sage_fp4_mma_probe_mx(const uint8_t *a_codes, const uint8_t *a_scales, const
                           const uint8_t *b_scales, int n, int K, int a_by_threads, float *d,
                           int32_t *status, void *stream);
 
+/* The tensor-core rate of the attention kernel's MMA instruction, for the
+ * roofline: one block per SM, each with one thread issuing iters
+ * back-to-back block-scaled FP4 MMAs (M = 128, N = n, K = 64, E4M3 scales,
+ * kind::mxf4nvf4) on operands in shared memory, then one commit and a bounded
+ * wait.  The caller times the launch: FLOPs = 2 * 128 * n * 64 * iters * (number
+ * of SMs).  iters 1 .. 10^6, n 128 or 256.  status: one zero-initialised
+ * int32, set to SAGE_FP4_ETIMEOUT if the wait gives up.  No counterpart in the
+ * pages. */
+int sage_fp4_mma_peak(int iters, int n, int32_t *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

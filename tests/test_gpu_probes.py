@@ -81,3 +81,12 @@ def test_mma_probe_exact_product(K, n, a_by_threads):
     err = np.abs(got - ref) / np.maximum(scale, 1e-30)
     assert np.isfinite(got).all()
     assert err.max() < 1e-5, (err.max(), np.unravel_index(err.argmax(), err.shape))
+
+
+@pytest.mark.parametrize("n", [128, 256])
+def test_mma_peak_rate(n):
+    # back-to-back FP4 MMAs on every SM: a plausible dense FP4 rate for one
+    # GB300 (the nominal dense NVFP4 figure is 13.5-15 PFLOP/s at full clock)
+    tflops = S.mma_peak_tflops(n=n, iters=4000)
+    print(f"FP4 MMA rate, N={n}: {tflops:.0f} TFLOP/s")
+    assert 3000 < tflops < 20000, tflops
