@@ -34,6 +34,9 @@
 // tcgen05.commit (each costs ~40 cycles of issue and ~250 cycles until the
 // barrier is seen on GB300).
 // Registers are rebalanced with setmaxnreg (budgets per head dimension below).
+// Instantiations: D (64, 128) x O layout (dense [B,H,N,D], or through
+// strides) x format (NVFP4, the method's; MXFP4, 1x32 groups with E8M0
+// scales, the alternative the pages set aside -- its level 1 targets 6).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 

@@ -166,3 +166,14 @@ def test_torch_op_is_registered_with_a_fake():
         x = torch.empty(2, 300, 3, 64, dtype=torch.bfloat16)
         o = torch.ops.sage_fp4.attention(x, x, x, True, 0.2, "NHD")
         assert o.shape == x.shape and o.dtype == torch.bfloat16 and o.is_contiguous()
+
+
+def test_binding_argument_counts_match_the_header():
+    import re
+    text = open(S._HEADER).read()
+    decls = dict(re.findall(r"^(?:int|size_t|const char \*)\s*(sage_fp4_\w+)\(([^;]*)\);", text, re.M))
+    lib = S.load()
+    assert set(decls) == set(S.header_functions())
+    for name, args in decls.items():
+        n = len([a for a in args.replace("\n", " ").split(",") if a.strip() and a.strip() != "void"])
+        assert len(getattr(lib, name).argtypes) == n, name
