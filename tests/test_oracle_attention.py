@@ -252,6 +252,11 @@ MUTATIONS = {
                         "pv += 448.0 * sc[vsrow[jg]] * part;"),
     "scale_amax_over_4": ("float q = amax / 6.0f;", "float q = amax / 4.0f;"),
     "e2m1_ties_up": ("(d == bestd && (i & 1) == 0)", "(d == bestd)"),
+    "l_against_tile_max": ("lt += exp((S[jj] - m_new) * isd);", "lt += exp((S[jj] - t) * isd);"),
+    "nibble_order": ("  if (idx & 1)\n    row[idx >> 1] = (uint8_t)((row[idx >> 1] & 0x0F) | (code << 4));",
+                     "  if (!(idx & 1))\n    row[idx >> 1] = (uint8_t)((row[idx >> 1] & 0x0F) | (code << 4));"),
+    "dot_drops_element": ("for (int k = GS * g; k < GS * g + GS; k++)", "for (int k = GS * g + 1; k < GS * g + GS; k++)"),
+    "e4m3_subnormal_step": ("return sign | (int)rint(a * 512.0);", "return sign | (int)rint(a * 256.0);"),
     "scale_ignored": ("double *out_m) {\n  const double isd = scale;",
                       "double *out_m) {\n  const double isd = 1.0 / sqrt((double)D);"),
 }
