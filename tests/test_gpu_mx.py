@@ -166,3 +166,16 @@ def test_nvfp4_beats_mxfp4_at_full_size(name):
         res[fmt] = (cosine(got, exact), rel_l1(got, exact))
     print(name, {f: tuple(round(x, 4) for x in r) for f, r in res.items()})
     assert res["nvfp4"][0] > res["mxfp4"][0] and res["nvfp4"][1] < res["mxfp4"][1], res
+
+
+@pytest.mark.parametrize("D,causal", [(128, False), (64, True)])
+def test_mx_strided_layout_matches_contiguous(D, causal):
+    # the MXFP4 instantiation that writes O through strides (NHD), against the
+    # dense one: the same bits
+    B, H, N = 2, 3, 333
+    q, k, v = (t.cuda() for t in make_qkv(B, H, N, D, "k_channel_outliers", seed=D + 7))
+    want = S.attention(q, k, v, causal, fmt="mxfp4")
+    qn, kn, vn = (x.transpose(1, 2).contiguous() for x in (q, k, v))
+    got = S.attention(qn, kn, vn, causal, layout="NHD", fmt="mxfp4")
+    torch.cuda.synchronize()
+    assert torch.equal(got.transpose(1, 2), want)
