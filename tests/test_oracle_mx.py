@@ -175,3 +175,14 @@ def test_planted_mx_mistake_is_caught(name, tmp_path):
 
 def test_unmutated_oracle_passes_mx_pins():
     assert mx_pins() == []
+
+
+def test_mx_format_matches_the_page():
+    import json
+    facts = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_facts.json")))
+    mx = facts["mxfp4_group"]
+    assert oracle.GROUP["mxfp4"] == mx["size"] == 32 and mx["scale_format"] == "E8M0"
+    # an E8M0 scale is a pure power of two: 2^-127 .. 2^127, no mantissa
+    vals = [oracle.e8m0_value(b) for b in range(255)]
+    assert all(np.frexp(v)[0] == 0.5 for v in vals)
+    assert vals[0] == 2.0 ** -127 and vals[254] == 2.0 ** 127
