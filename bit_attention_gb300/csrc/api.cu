@@ -302,9 +302,11 @@ int sage_fp4_cvt_probe(uint32_t first, uint32_t count, uint8_t* e2m1, uint8_t* e
 namespace {
 
 int mma_probe_impl(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* b_codes,
-                   const uint8_t* b_scales, int n, int K, int a_by_threads, int mx, float* d,
-                   int32_t* status, void* stream) {
+                   const uint8_t* b_scales, int n, int K, int flags, float* d, int32_t* status,
+                   void* stream) {
   if (n != 64 && n != 128) return SAGE_FP4_EINVAL;
+  if (flags & ~(SAGE_FP4_PROBE_A_BY_THREADS | SAGE_FP4_PROBE_MX | SAGE_FP4_PROBE_SF_ROWS128))
+    return SAGE_FP4_EINVAL;
   if (K != 64 && K != 128 && K != 256) return SAGE_FP4_EINVAL;
   if (!aligned(a_codes, 16) || !aligned(a_scales, 16) || !aligned(b_codes, 16) ||
       !aligned(b_scales, 16) || !aligned(d, 4) || !aligned(status, 4))
@@ -324,8 +326,9 @@ int mma_probe_impl(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_
   p.status = status;
   p.n = n;
   p.K = K;
-  p.a_by_threads = a_by_threads ? 1 : 0;
-  p.mx = mx;
+  p.a_by_threads = (flags & SAGE_FP4_PROBE_A_BY_THREADS) ? 1 : 0;
+  p.mx = (flags & SAGE_FP4_PROBE_MX) ? 1 : 0;
+  p.sf_rows128 = (flags & SAGE_FP4_PROBE_SF_ROWS128) ? 1 : 0;
   return from_cuda(launch_mma_probe(ta, tb, p, static_cast<cudaStream_t>(stream)));
 }
 
@@ -334,7 +337,14 @@ int mma_probe_impl(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_
 int sage_fp4_mma_probe(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* b_codes,
                        const uint8_t* b_scales, int n, int K, int a_by_threads, float* d,
                        int32_t* status, void* stream) {
-  return mma_probe_impl(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threads, 0, d, status, stream);
+  return mma_probe_impl(a_codes, a_scales, b_codes, b_scales, n, K,
+                        a_by_threads ? SAGE_FP4_PROBE_A_BY_THREADS : 0, d, status, stream);
+}
+
+int sage_fp4_mma_probe_ex(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* b_codes,
+                          const uint8_t* b_scales, int n, int K, int flags, float* d, int32_t* status,
+                          void* stream) {
+  return mma_probe_impl(a_codes, a_scales, b_codes, b_scales, n, K, flags, d, status, stream);
 }
 
 int sage_fp4_mma_peak(int iters, int n, int32_t* status, void* stream) {
@@ -347,7 +357,9 @@ int sage_fp4_mma_peak(int iters, int n, int32_t* status, void* stream) {
 int sage_fp4_mma_probe_mx(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* b_codes,
                           const uint8_t* b_scales, int n, int K, int a_by_threads, float* d,
                           int32_t* status, void* stream) {
-  return mma_probe_impl(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threads, 1, d, status, stream);
+  return mma_probe_impl(a_codes, a_scales, b_codes, b_scales, n, K,
+                        SAGE_FP4_PROBE_MX | (a_by_threads ? SAGE_FP4_PROBE_A_BY_THREADS : 0), d, status,
+                        stream);
 }
 
 }  // extern "C"

@@ -61,6 +61,11 @@ struct MmaProbeParams {
   int32_t* status;
   int n, K, a_by_threads;
   int mx;  // 1: MXFP4 product (kind::mxf4, UE8M0 scales, two per row per K = 64)
+  // 1: A's scale factors copied without replication, row r of the matrix to
+  // lane r (tcgen05.cp .128x256b per two K = 64 steps, .128x128b for K = 64),
+  // from a 128-row source that holds row r's scale word in word r / 32 of its
+  // 16 bytes and NaN-valued noise in the other three
+  int sf_rows128;
 };
 cudaError_t launch_mma_probe(const CUtensorMap& ta, const CUtensorMap& tb, const MmaProbeParams& p,
                              cudaStream_t st);

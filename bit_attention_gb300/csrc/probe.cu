@@ -55,8 +55,13 @@ __global__ void __launch_bounds__(128, 1)
   constexpr int KB = K / 64;         // MMAs (K = 64 each)
   constexpr uint32_t swz = (RB == 32) ? kSwizzle32B : (RB == 64) ? kSwizzle64B : kSwizzle128B;
   constexpr uint32_t sbo = 8 * RB;
-  constexpr int oA = 0, oB = 128 * RB, oSFA = 2 * 128 * RB, oSFB = oSFA + KB * 512,
-                oBar = oSFB + KB * 512, oSlot = oBar + 16;
+  // each operand's scales: KB * 512 bytes (block layout) at the start of a
+  // 48 KB region; in the 128-row mode, step kb's 128-row copy source at
+  // 4096 + 2048 kb, and noise everywhere else (the region covers every read of
+  // the 128-row copies under either reading of the descriptor's two strides)
+  constexpr int kSfRegion = 49152, kSfRows = 4096;
+  constexpr int oA = 0, oB = 128 * RB, oSFA = 2 * 128 * RB, oSFB = oSFA + kSfRegion,
+                oBar = oSFB + kSfRegion, oSlot = oBar + 16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -87,6 +92,26 @@ __global__ void __launch_bounds__(128, 1)
     bulk_load(sb + oSFA, p.a_scales, KB * 512, bar_load);
     bulk_load(sb + oSFB, p.b_scales, KB * 512, bar_load);
   }
+  // noise after the scales: every value, NaN encodings included (E4M3 0x7F,
+  // E8M0 0xFF), so that a product that read it would show
+  for (int i = KB * 512 + static_cast<int>(threadIdx.x); i < kSfRegion; i += blockDim.x) {
+    const uint8_t v = (i % 5 == 0) ? 0x7F : (i % 7 == 0) ? 0xFF : static_cast<uint8_t>(i * 37 + 11);
+    sm[oSFA + i] = v;
+    sm[oSFB + i] = static_cast<uint8_t>(v ^ 0x80);
+  }
+  __syncthreads();
+  if (p.sf_rows128) {
+    // A's 128-row copy source of step kb: row r (16 bytes) holds, in its word
+    // r / 32, the scale word of matrix row r (the block layout keeps it at row
+    // r % 32, word r / 32); its other three words stay noise
+    for (int i = threadIdx.x; i < KB * 128; i += blockDim.x) {
+      const int kb = i / 128, r = i % 128;
+      const int src = 512 * kb + (r % 32) * 16 + (r / 32) * 4;
+      const int dst = kSfRows + 2048 * kb + r * 16 + (r / 32) * 4;
+      *reinterpret_cast<uint32_t*>(sm + oSFA + dst) = *reinterpret_cast<const uint32_t*>(p.a_scales + src);
+    }
+  }
+  fence_proxy_async_smem();
   if (p.a_by_threads) {
     for (int i = threadIdx.x; i < 128 * (RB / 16); i += blockDim.x) {
       const int r = i / (RB / 16), c = i % (RB / 16);
@@ -102,9 +127,19 @@ __global__ void __launch_bounds__(128, 1)
     ok = probe_wait(bar_load, 0, err);
     if (ok) {
       tc_fence_after();
-      for (int kb = 0; kb < KB; ++kb) {
-        tc_cp_32x128b_warpx4(tmem + 128 + 4 * kb, smem_desc(sb + oSFA + 512 * kb, 0, 128, kSwizzleNone));
+      // B's scales: every lane quarter holds all rows (each quarter of the
+      // MMA's output rows reads them from its own quarter)
+      for (int kb = 0; kb < KB; ++kb)
         tc_cp_32x128b_warpx4(tmem + 160 + 4 * kb, smem_desc(sb + oSFB + 512 * kb, 0, 128, kSwizzleNone));
+      if (!p.sf_rows128) {
+        for (int kb = 0; kb < KB; ++kb)
+          tc_cp_32x128b_warpx4(tmem + 128 + 4 * kb, smem_desc(sb + oSFA + 512 * kb, 0, 128, kSwizzleNone));
+      } else if (KB == 1) {
+        tc_cp_128x128b(tmem + 128, smem_desc(sb + oSFA + kSfRows, 0, 128, kSwizzleNone));
+      } else {
+        // two steps per copy: the second 16 bytes of row r are step 2j+1's row r
+        for (int j = 0; j < KB / 2; ++j)
+          tc_cp_128x256b(tmem + 128 + 8 * j, smem_desc(sb + oSFA + kSfRows + 4096 * j, 2048, 128, kSwizzleNone));
       }
       const uint32_t n = static_cast<uint32_t>(p.n);
       for (int kb = 0; kb < KB; ++kb) {
@@ -142,7 +177,7 @@ __global__ void __launch_bounds__(128, 1)
 template <int K>
 cudaError_t launch_mma_probe_k(const CUtensorMap& ta, const CUtensorMap& tb,
                                const MmaProbeParams& p, cudaStream_t st) {
-  const int smem = 2 * 128 * (K / 2) + 2 * (K / 64) * 512 + 64 + 1024;
+  const int smem = 2 * 128 * (K / 2) + 2 * 49152 + 64 + 1024;
   cudaError_t e =
       cudaFuncSetAttribute(mma_probe_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

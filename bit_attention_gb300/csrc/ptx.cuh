@@ -157,6 +157,17 @@ __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sd
                : "memory");
 }
 
+// Copy 128 rows x 16 / 32 bytes from shared memory (descriptor: 8-row groups
+// sbo bytes apart; in the 32-byte form the second 16 bytes of every row lbo
+// bytes after the first) into tensor memory columns [col, col+4) / [col, col+8)
+// of lanes 0-127, row r to lane r.
+__device__ __forceinline__ void tc_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Each thread of the warp reads 16 / 32 consecutive 32-bit columns of its lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(

@@ -76,6 +76,7 @@ def load(build: bool = True) -> ctypes.CDLL:
                 "sage_fp4_cvt_probe": (i, [u32, u32, vp, vp, vp]),
                 "sage_fp4_mma_probe": (i, [vp, vp, vp, vp, i, i, i, vp, vp, vp]),
                 "sage_fp4_mma_probe_mx": (i, [vp, vp, vp, vp, i, i, i, vp, vp, vp]),
+                "sage_fp4_mma_probe_ex": (i, [vp, vp, vp, vp, i, i, i, vp, vp, vp]),
                 "sage_fp4_mma_peak": (i, [i, i, vp, vp]),
                 "sage_fp4_attention_noalloc": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, vp]),
                 "sage_fp4_host_workspace_bytes": (sz, [i, i, i, i]),
@@ -165,6 +166,15 @@ def sage_fp4_mma_probe(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threads,
 def sage_fp4_mma_probe_mx(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threads, d, status,
                           stream) -> int:
     return load().sage_fp4_mma_probe_mx(a_codes, a_scales, b_codes, b_scales, n, K, a_by_threads, d,
+                                        status, stream)
+
+
+PROBE_A_BY_THREADS, PROBE_MX, PROBE_SF_ROWS128 = 1, 2, 4
+
+
+def sage_fp4_mma_probe_ex(a_codes, a_scales, b_codes, b_scales, n, K, flags, d, status,
+                          stream) -> int:
+    return load().sage_fp4_mma_probe_ex(a_codes, a_scales, b_codes, b_scales, n, K, int(flags), d,
                                         status, stream)
 
 

@@ -294,6 +294,26 @@ int sage_fp4_mma_probe_mx(const uint8_t *a_codes, const uint8_t *a_scales, const
                           const uint8_t *b_scales, int n, int K, int a_by_threads, float *d,
                           int32_t *status, void *stream);
 
+/* sage_fp4_mma_probe / sage_fp4_mma_probe_mx with options as flags:
+ *   SAGE_FP4_PROBE_A_BY_THREADS  a_by_threads = 1 above;
+ *   SAGE_FP4_PROBE_MX            the MXFP4 product of sage_fp4_mma_probe_mx;
+ *   SAGE_FP4_PROBE_SF_ROWS128    A's scale factors reach tensor memory by
+ *       128-lane copies (one per two K = 64 steps, or per step when K = 64),
+ *       matrix row r to lane r, from a 128-row source that holds row r's scale
+ *       word of a step in word r / 32 of the row's 16 bytes and NaN-valued
+ *       noise in the other three (B's stay replicated in all four lane
+ *       quarters).  The product is exact only if the MMA reads A row r's scales
+ *       from lane r, column (step base) + r / 32, and nothing else of those
+ *       columns: the layout in which the attention kernel's softmax writes P's
+ *       scales.
+ * Other bits: SAGE_FP4_EINVAL.  Arguments and errors otherwise as above. */
+#define SAGE_FP4_PROBE_A_BY_THREADS 1
+#define SAGE_FP4_PROBE_MX 2
+#define SAGE_FP4_PROBE_SF_ROWS128 4
+int sage_fp4_mma_probe_ex(const uint8_t *a_codes, const uint8_t *a_scales, const uint8_t *b_codes,
+                          const uint8_t *b_scales, int n, int K, int flags, float *d,
+                          int32_t *status, void *stream);
+
 /* The tensor-core rate of the attention kernel's MMA instruction, for the
  * roofline: one block per SM, each with one thread issuing iters
  * back-to-back block-scaled FP4 MMAs (M = 128, N = n, K = 64, E4M3 scales,

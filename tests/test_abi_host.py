@@ -88,6 +88,8 @@ def test_probe_argument_checks():
     assert S.sage_fp4_mma_probe(0x1000, 0x2000, 0x3000, 0x4000, 96, 64, 0, 0x5000, 0x6000, None) == S.EINVAL
     assert S.sage_fp4_mma_probe(0x1000, 0x2000, 0x3000, 0x4000, 64, 32, 0, 0x5000, 0x6000, None) == S.EINVAL
     assert S.sage_fp4_cvt_probe(0, 16, None, None, None) == S.EINVAL
+    # unknown option bits
+    assert S.sage_fp4_mma_probe_ex(0x1000, 0x2000, 0x3000, 0x4000, 64, 64, 8, 0x5000, 0x6000, None) == S.EINVAL
 
 
 def test_strerror():

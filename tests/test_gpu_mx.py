@@ -61,7 +61,8 @@ def _mx_plain(block, R, C):
 @pytest.mark.parametrize("K", [64, 128, 256])
 @pytest.mark.parametrize("n", [64, 128])
 @pytest.mark.parametrize("a_by_threads", [0, 1])
-def test_mx_mma_probe_exact_product(K, n, a_by_threads):
+@pytest.mark.parametrize("sf_rows128", [0, 1])
+def test_mx_mma_probe_exact_product(K, n, a_by_threads, sf_rows128):
     rng = np.random.default_rng(K * 3 + n + a_by_threads)
 
     def operand(rows):
@@ -75,8 +76,9 @@ def test_mx_mma_probe_exact_product(K, n, a_by_threads):
     ta, tsa, tb, tsb = _dev(ac), _dev(asf), _dev(bc), _dev(bsf)
     d = torch.full((128, n), float("nan"), dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = S.sage_fp4_mma_probe_mx(ta.data_ptr(), tsa.data_ptr(), tb.data_ptr(), tsb.data_ptr(), n, K,
-                                 a_by_threads, d.data_ptr(), status.data_ptr(),
+    flags = S.PROBE_MX | (S.PROBE_A_BY_THREADS if a_by_threads else 0) | (S.PROBE_SF_ROWS128 if sf_rows128 else 0)
+    rc = S.sage_fp4_mma_probe_ex(ta.data_ptr(), tsa.data_ptr(), tb.data_ptr(), tsb.data_ptr(), n, K,
+                                 flags, d.data_ptr(), status.data_ptr(),
                                  torch.cuda.current_stream().cuda_stream)
     assert rc == 0
     torch.cuda.synchronize()

@@ -61,7 +61,9 @@ def _rand_operand(rng, rows, K, rows_pad=128):
 @pytest.mark.parametrize("K", [64, 128, 256])
 @pytest.mark.parametrize("n", [64, 128])
 @pytest.mark.parametrize("a_by_threads", [0, 1])
-def test_mma_probe_exact_product(K, n, a_by_threads):
+@pytest.mark.parametrize("sf_rows128", [0, 1])
+def test_mma_probe_exact_product(K, n, a_by_threads, sf_rows128):
+    # sf_rows128: A row r's scales in lane r alone (column base + r / 32), noise elsewhere
     rng = np.random.default_rng(K * 7 + n + a_by_threads)
     a_codes, a_sf, a_dec = _rand_operand(rng, 128, K)
     b_codes, b_sf, b_dec = _rand_operand(rng, n, K)
@@ -69,9 +71,10 @@ def test_mma_probe_exact_product(K, n, a_by_threads):
     ta, tsa, tb, tsb = dev(a_codes), dev(a_sf), dev(b_codes), dev(b_sf)
     d = torch.full((128, n), float("nan"), dtype=torch.float32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = S.sage_fp4_mma_probe(ta.data_ptr(), tsa.data_ptr(), tb.data_ptr(), tsb.data_ptr(), n, K,
-                              a_by_threads, d.data_ptr(), status.data_ptr(),
-                              torch.cuda.current_stream().cuda_stream)
+    flags = (S.PROBE_A_BY_THREADS if a_by_threads else 0) | (S.PROBE_SF_ROWS128 if sf_rows128 else 0)
+    rc = S.sage_fp4_mma_probe_ex(ta.data_ptr(), tsa.data_ptr(), tb.data_ptr(), tsb.data_ptr(), n, K,
+                                 flags, d.data_ptr(), status.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
     assert rc == 0
     torch.cuda.synchronize()
     assert int(status.item()) == 0
