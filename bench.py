@@ -31,11 +31,11 @@ FP4_OVER_BF16 = 6.0  # nominal dense FP4 / BF16 tensor rate (13.5 / 2.25 PFLOP/s
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one attn_fwd_kernel launch,
-# captured with ncu on this build of the kernel (reads 113.62 MB = the
-# compulsory Q, K, V codes and scales; writes 78.97 MB of the 134.2 MB O, the
-# rest leaves L2 after the launch).  Workloads without a capture report null.
+# captured with ncu on this build of the kernel, mean of five launches (reads
+# 113.39 MB = the compulsory Q, K, V codes and scales; writes 78.75 MB of the
+# 134.2 MB O, the rest leaves L2 after the launch).  Workloads without a capture report null.
 ATTN_TRAFFIC = {
-    "attn_fwd B4 H32 N4096 D128 k-channel-outliers": 113.62e6 + 78.97e6,
+    "attn_fwd B4 H32 N4096 D128 k-channel-outliers": 113.39e6 + 78.75e6,
 }
 
 
