@@ -1,8 +1,9 @@
 """Quantize kernel parity: codes and scales bit-exact with the oracle.
 
 Shapes span several 128-row tiles and ragged tails (N not a multiple of 16 or
-128), both head dims, the workloads' value patterns, and the full LLM-prefill
-workload (B4 H32 N4096 D128) compared in full.
+128), both head dims and the workloads' value patterns; every benchmark
+workload (up to B4 H32 N8192 D128 and B2 H48 N17776 D64) is compared in full,
+in the launch configuration the benchmark times.
 """
 import numpy as np
 import pytest
@@ -68,7 +69,8 @@ def test_quantize_special_values():
     check_quant(t, t.clone(), t.clone())
 
 
-def test_quantize_full_llm_workload():
-    w = WORKLOADS["llm"]
+@pytest.mark.parametrize("name", ["small", "llm", "llm_causal", "dit", "dit_long"])
+def test_quantize_full_workload(name):
+    w = WORKLOADS[name]
     q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.pattern, seed=0)
     check_quant(q, k, v)
