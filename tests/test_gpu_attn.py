@@ -69,6 +69,21 @@ def test_attention_matches_oracle(B, H, N, D, causal, pattern):
     compare(q, k, v, causal, label=f"B{B} H{H} N{N} D{D} causal={causal} {pattern}")
 
 
+def _fuzz_cases(n=12, seed=2024):
+    rng = np.random.default_rng(seed)
+    pats = ["iid", "k_channel_outliers", "k_head_mean", "sparse_outliers"]
+    return [(int(rng.integers(1, 3)), int(rng.integers(1, 4)), int(rng.integers(1, 700)),
+             int(rng.choice([64, 128])), bool(rng.integers(0, 2)), pats[int(rng.integers(0, 4))])
+            for _ in range(n)]
+
+
+@pytest.mark.parametrize("B,H,N,D,causal,pattern", _fuzz_cases())
+def test_attention_random_shapes(B, H, N, D, causal, pattern):
+    # seeded random shapes: ragged tails at every offset inside a tile
+    q, k, v = make_qkv(B, H, N, D, pattern, seed=7 * N + D)
+    compare(q, k, v, causal, label=f"fuzz B{B} H{H} N{N} D{D} causal={causal} {pattern}")
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_all_keys_equal_gives_mean_of_v(causal):
     # every score of a row is equal, so P quantizes exactly and O is the mean of

@@ -143,6 +143,23 @@ def test_mx_attention_matches_oracle(B, H, N, D, causal, pattern):
     assert np.isfinite(got).all() and e <= 5e-3 and c >= 0.999, (e, c)
 
 
+def _mx_fuzz_cases(n=6, seed=77):
+    rng = np.random.default_rng(seed)
+    pats = ["iid", "k_channel_outliers", "k_head_mean", "sparse_outliers"]
+    return [(int(rng.integers(1, 3)), int(rng.integers(1, 3)), int(rng.integers(1, 600)),
+             int(rng.choice([64, 128])), bool(rng.integers(0, 2)), pats[int(rng.integers(0, 4))])
+            for _ in range(n)]
+
+
+@pytest.mark.parametrize("B,H,N,D,causal,pattern", _mx_fuzz_cases())
+def test_mx_attention_random_shapes(B, H, N, D, causal, pattern):
+    q, k, v = make_qkv(B, H, N, D, pattern, seed=5 * N + D)
+    got = _mx_attention(q, k, v, causal).float().cpu().numpy().reshape(B * H * N, D)
+    ref = oracle.attention(oracle.Quantized(q, k, v, B * H, N, D, fmt="mxfp4"), causal)[0]
+    e, c = rel_l1(got, ref), cosine(got, ref)
+    assert np.isfinite(got).all() and e <= 5e-3 and c >= 0.999, (e, c)
+
+
 def test_mx_attention_llm_workload_sampled_rows():
     w = WORKLOADS["llm"]
     q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.pattern, seed=0)
