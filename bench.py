@@ -182,10 +182,12 @@ def run_reference(args, w, world, rank):
     value = statistics.mean(tops)
     sample = (f"oracle attention (FP64 C, OpenMP) on ~{rows_total // max(args.steps, 1)} random "
               f"query rows per step of one (b,h) of the workload, full N={w.N}; "
-              f"quantization excluded")
+              f"quantization excluded; ms_per_step extrapolated: the whole workload at the "
+              f"sampled rate")
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
-           "ms_per_step": None, "dtype": "f64", "data": "synthetic",
+           "ms_per_step": w.ops / (value * 1e12) * 1e3 if value > 0 else None,
+           "dtype": "f64", "data": "synthetic",
            "config": dict(w.describe(), format=args.fmt),
            "cpu_baseline": {"value": value, "unit": "TOPS", "cores": threads, "kind": "oracle",
                             "sample": sample},
