@@ -130,8 +130,11 @@ int sage_fp4_qkv_from_workspace(void *workspace, size_t workspace_bytes, int B, 
 /* Quantize bf16 Q, K, V ([B,H,N,D], contiguous, 16-byte aligned device memory)
  * into the NVFP4 operands of *out (layouts above): Q and K along D, V along
  * tokens into V^T.  Codes and scales are bit-exact with the rule above.
- * Two kernel launches on `stream`.  out->status (zero-initialised) is set to
- * SAGE_FP4_ETIMEOUT if a bounded device wait for a tile copy gives up. */
+ * Two kernel launches on `stream`; the second (V) is a programmatic dependent of
+ * the first and may start while the first drains, and it completes only after
+ * the first, so work queued after this call sees both.  out->status
+ * (zero-initialised) is set to SAGE_FP4_ETIMEOUT if a bounded device wait for
+ * a tile copy gives up. */
 int sage_fp4_quantize_qkv(const void *q, const void *k, const void *v, const sage_fp4_qkv *out,
                           int B, int H, int N, int D, void *stream);
 
