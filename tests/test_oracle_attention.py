@@ -10,6 +10,10 @@ The pages print no worked example, so the oracle is pinned by mathematics:
 * the online-softmax identity l = sum_j exp((S_j - m)/sqrt(D)) with S from a
   numpy matmul of the decoded operands;
 * TILE and RUNNING level-1 modes coincide when there is one KV tile;
+* both modes reproduce float64 softmax exactly on constructed inputs whose
+  tiles have different maxima and whose running-maximum ratios are powers
+  of two (softmax scale ln(2)/3), so RUNNING's level 1 (P2 below 2688,
+  sP1 = 1/2688) is exercised where it differs from TILE's;
 * the softmax scale enters only as a factor on S: attending to 2Q (whose
   quantization is Q's with every scale doubled, exactly) at scale c gives the
   same bits as attending to Q at scale 2c, and the exact path matches numpy
@@ -46,7 +50,7 @@ def softmax_attention(q, k, v, causal, scale=None):
     return np.einsum("bij,bjd->bid", p, v)
 
 
-def exact_case(BH, N, D, seed):
+def exact_case(BH, N, D, seed, hit_choices=(6.0, 4.0, 3.0, 2.0, 1.5)):
     """Inputs on which the oracle's quantization is exact.
 
     Each 16-element group holds values of the E2M1 grid with one element of
@@ -66,7 +70,7 @@ def exact_case(BH, N, D, seed):
     k = np.zeros((BH, N, D))
     k[:, :, 1] = 6.0
     ntile = (N + 127) // 128
-    hit_vals = rng.choice([6.0, 4.0, 3.0, 2.0, 1.5], size=(BH, ntile))
+    hit_vals = rng.choice(list(hit_choices), size=(BH, ntile))
     hit = rng.random((BH, N)) < 0.35
     hit[:, ::128] = True
     for t in range(ntile):
@@ -96,6 +100,41 @@ def test_exactly_quantizable_inputs_reproduce_softmax(N, causal):
     ref = softmax_attention(q, k, v, causal).reshape(BH * N, D)
     err = np.abs(o - ref).max() / np.abs(ref).max()
     assert err < 1e-12, err
+
+
+# Level 1 in RUNNING mode maps each tile against the running maximum m, so a
+# tile whose maximum t lies below m gets P2 = 2688 * exp((t - m) * scale) < 2688
+# and sP1 = 1/2688.  With hit scores q0 * h, q0 in {3, 6} and h in {6, 4, 3, 2},
+# every difference t - m within a row is a multiple of 3; at the softmax scale
+# ln(2)/3 each exp((t - m) * scale) is a power of two 2^-k (k <= 8), so P2 of a
+# hit is 2688 * 2^-k: an exact E4M3 scale 448 * 2^-k with code 6.  Quantization
+# of P stays exact in both modes, tiles have different maxima, and both modes
+# must reproduce float64 softmax attention at that scale.
+RUNNING_SCALE = np.log(2.0) / 3.0
+
+
+@pytest.mark.parametrize("pmode", ["tile", "running"])
+@pytest.mark.parametrize("N,causal", [(513, False), (513, True), (300, False)])
+def test_exactly_quantizable_inputs_with_differing_tile_maxima(N, causal, pmode):
+    BH, D = 2, 64
+    q, k, v = exact_case(BH, N, D, seed=3 * N + causal, hit_choices=(6.0, 4.0, 3.0, 2.0))
+    qz = oracle.Quantized(bf16(q), bf16(k), bf16(v), BH, N, D)
+    o, l, m = oracle.attention(qz, causal, pmode, scale=RUNNING_SCALE)
+    ref = softmax_attention(q, k, v, causal, scale=RUNNING_SCALE).reshape(BH * N, D)
+    err = np.abs(o - ref).max() / np.abs(ref).max()
+    assert err < 1e-12, (pmode, err)
+    if not causal:
+        # the case does what it is for: some rows see a later tile whose
+        # maximum exceeds every earlier one, and later tiles whose maximum is
+        # below the running one (where RUNNING's level 1 differs from TILE's)
+        qd = oracle.decode_rows(qz.qc, qz.qs)[:, :N]
+        kd = oracle.decode_rows(qz.kc, qz.ks)[:, :N]
+        s = np.einsum("bid,bjd->bij", qd, kd)
+        ntile = (N + 127) // 128
+        tmax = np.stack([s[:, :, 128 * t:128 * t + 128].max(-1) for t in range(ntile)], -1)
+        running = np.maximum.accumulate(tmax, axis=-1)
+        assert (tmax[..., 1:] < running[..., 1:]).any()
+        assert (tmax[..., 1:] > running[..., :-1]).any()
 
 
 def decoded(qz):
@@ -257,6 +296,9 @@ MUTATIONS = {
                      "  if (!(idx & 1))\n    row[idx >> 1] = (uint8_t)((row[idx >> 1] & 0x0F) | (code << 4));"),
     "dot_drops_element": ("for (int k = GS * g; k < GS * g + GS; k++)", "for (int k = GS * g + 1; k < GS * g + GS; k++)"),
     "e4m3_subnormal_step": ("return sign | (int)rint(a * 512.0);", "return sign | (int)rint(a * 256.0);"),
+    "running_sP1_as_tile": ("double sP1 = (pmode == 0) ? exp((t - m_new) * isd) / R : 1.0 / R;",
+                            "double sP1 = exp((t - m_new) * isd) / R;"),
+    "running_ref_is_tile_max": ("double ref = (pmode == 0) ? t : m_new;", "double ref = t;"),
     "scale_ignored": ("double *out_m) {\n  const double isd = scale;",
                       "double *out_m) {\n  const double isd = 1.0 / sqrt((double)D);"),
 }
@@ -275,6 +317,8 @@ def all_pins():
         ("group", lambda: __import__("test_oracle_codecs").test_group_quantizer_bruteforce_and_invariants()),
         ("unquantized", lambda: test_against_unquantized_attention("iid")),
         ("scale", lambda: test_scale_is_a_factor_on_scores(64, False)),
+        ("exact_running", lambda: test_exactly_quantizable_inputs_with_differing_tile_maxima(
+            513, False, "running")),
     ]
     for name, fn in checks:
         try:
