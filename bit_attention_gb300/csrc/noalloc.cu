@@ -10,105 +10,91 @@
 // quantized operands, which the two-call API keeps in a caller-allocated
 // workspace, live here in a fixed file-scope device array instead.
 //
+// The call is the two-call API run over that array: the array is carved by
+// sage_fp4_qkv_from_workspace, the caller's status word replaces the
+// workspace's, and sage_fp4_quantize_qkv and sage_fp4_attn_fwd do the rest,
+// so every argument check and launch is theirs.
+//
 // That array is reserved on every GPU that loads this module and is held
 // until the process exits.  Every call uses the same array: calls whose work
 // overlaps on the GPU (different streams, or different host threads, without
 // ordering between them) race on it and give undefined results.
-#include <cudaTypedefs.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
-#include <limits.h>
-#include <math.h>
+
+#include <mutex>
 
 #include "../../include/sage_fp4.h"
-#include "kernels.h"
-#include "layout.cuh"
-
-using namespace sagefp4;
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(64) << 20;  // SAGE_FP4_NOALLOC_SCRATCH_BYTES
+constexpr size_t kScratchBytes = size_t(SAGE_FP4_NOALLOC_SCRATCH_BYTES);
 
-// Quantized Q, K, V^T of the current call.
+// Quantized Q, K, V^T of the current call (and the workspace's unused status slot).
 static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
-
-static_assert(kScratchBytes == SAGE_FP4_NOALLOC_SCRATCH_BYTES, "header and array size disagree");
-
-struct Parts {
-  size_t qc, qs, kc, ks, vc, vs, total;
-};
-
-bool dims_ok(int B, int H, int N, int D) {
-  if (B < 0 || H < 0 || N < 0) return false;
-  if (D != 64 && D != 128) return false;
-  const long long BH = static_cast<long long>(B) * H;
-  const long long Np = (static_cast<long long>(N) + 127) / 128 * 128;
-  if (Np > (1LL << 30)) return false;
-  if (BH * Np > INT_MAX) return false;
-  return true;
-}
-
-Parts parts(int B, int H, int N, int D) {
-  const size_t BH = static_cast<size_t>(B) * H;
-  const OperandSizes os = operand_sizes(N, D);
-  Parts p;
-  size_t off = 0;
-  p.qc = off;
-  off += align256(BH * os.q_codes);
-  p.qs = off;
-  off += align256(BH * os.q_scales);
-  p.kc = off;
-  off += align256(BH * os.q_codes);
-  p.ks = off;
-  off += align256(BH * os.q_scales);
-  p.vc = off;
-  off += align256(BH * os.vt_codes);
-  p.vs = off;
-  off += align256(BH * os.vt_scales);
-  p.total = off;
-  return p;
-}
 
 bool aligned(const void* p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Device address of g_scratch, looked up once per device with that device
-// current.  In host code g_scratch names a host-side stand-in, not device
-// memory, so kernels must be given this address instead.
-uint8_t* scratch_address(int dev) {
-  static uint8_t* addr[64];
-  if (dev < 0 || dev >= 64) return nullptr;
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<uint8_t*>(p);
-  }
-  return addr[dev];
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+// The unique ID of the calling thread's current CUDA context (CUDA 12.0
+// driver API, reached through the runtime's entry-point query).  IDs are never
+// reused within a process, so a context created after cudaDeviceReset, or a
+// second context on the same device, has an ID of its own.  False when no
+// context is current or the query is unavailable.
+bool current_context_id(unsigned long long* id) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+    looked_up = true;
   }
-  return fn;
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
 }
 
-bool byte_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-              uint32_t box_rows, CUtensorMapSwizzle swz) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner};
-  cuuint32_t box[2] = {box_inner, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+// Device address of g_scratch in the current context.  In host code g_scratch
+// names a host-side stand-in, not device memory, so kernels must be given
+// this address.  It is looked up with cudaGetSymbolAddress the first time a
+// context calls (once per device in the usual one-context-per-device
+// program) and kept, keyed by the context's unique ID, under a lock so that
+// two threads' first calls do not race.
+uint8_t* scratch_address() {
+  struct Entry {
+    unsigned long long ctx_id;
+    uint8_t* addr;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int used = 0, next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  unsigned long long id = 0;
+  bool have_id = current_context_id(&id);
+  if (have_id)
+    for (int i = 0; i < used; ++i)
+      if (cache[i].ctx_id == id) return cache[i].addr;
+  // The lookup also makes the device's primary context current when the
+  // runtime has not done so on this thread yet.
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return nullptr;
+  if (!have_id) have_id = current_context_id(&id);
+  if (have_id) {
+    cache[next] = Entry{id, static_cast<uint8_t*>(p)};
+    next = (next + 1) % 64;
+    if (used < 64) ++used;
+  }
+  return static_cast<uint8_t*>(p);
 }
 
 }  // namespace
@@ -116,55 +102,22 @@ bool byte_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, u
 extern "C" int sage_fp4_attention_noalloc(const void* q, const void* k, const void* v, void* o,
                                           int32_t* status, int B, int H, int N, int D, int causal,
                                           void* stream) {
-  if (!dims_ok(B, H, N, D) || (causal != 0 && causal != 1)) return SAGE_FP4_EINVAL;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
-      !aligned(status, 4))
+  // Sizes first: 0 means invalid sizes, anything above the array is too large.
+  const size_t need = sage_fp4_workspace_bytes(B, H, N, D);
+  if (need == 0 || (causal != 0 && causal != 1)) return SAGE_FP4_EINVAL;
+  if (need > kScratchBytes) return SAGE_FP4_ETOOLARGE;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(status, 4))
     return SAGE_FP4_EINVAL;
-  const Parts pt = parts(B, H, N, D);
-  if (pt.total > kScratchBytes) return SAGE_FP4_ETOOLARGE;
   if (static_cast<long long>(B) * H * N == 0) return SAGE_FP4_OK;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SAGE_FP4_ECUDA;
-  int major = 0, minor = 0;
-  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-  if (major != 10 || minor != 3) return SAGE_FP4_EUNSUPPORTED;
-  uint8_t* base = scratch_address(dev);
+  uint8_t* base = scratch_address();
   if (!base) return SAGE_FP4_ECUDA;
-
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int BH = B * H;
-  const int Np = round_up_int(N, 128);
+  sage_fp4_qkv ops;
+  int rc = sage_fp4_qkv_from_workspace(base, kScratchBytes, B, H, N, D, &ops);
+  if (rc != SAGE_FP4_OK) return rc;
+  ops.status = status;
   // Every byte of the quantized operands, padding included, is rewritten by
   // the quantize kernels, so nothing left by an earlier call is read.
-  const Strides dense = contiguous_bhnd(H, N, D);
-  if (launch_quant_rows(q, k, dense, dense, base + pt.qc, base + pt.qs, base + pt.kc, base + pt.ks, H,
-                        BH, N, D, false, st) != cudaSuccess ||
-      launch_quant_v(v, dense, base + pt.vc, base + pt.vs, H, BH, N, D, false, status, st) != cudaSuccess)
-    return SAGE_FP4_ECUDA;
-  CUtensorMap tq, tk, tv;
-  const CUtensorMapSwizzle qk_swz = (D == 128) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
-  if (!byte_map(&tq, base + pt.qc, D / 2, static_cast<uint64_t>(BH) * Np, D / 2, 128, qk_swz) ||
-      !byte_map(&tk, base + pt.kc, D / 2, static_cast<uint64_t>(BH) * Np, D / 2, 128, qk_swz) ||
-      !byte_map(&tv, base + pt.vc, Np / 2, static_cast<uint64_t>(BH) * D, 64, D,
-                CU_TENSOR_MAP_SWIZZLE_64B))
-    return SAGE_FP4_ECUDA;
-  AttnParams p;
-  p.sfq = base + pt.qs;
-  p.sfk = base + pt.ks;
-  p.sfv = base + pt.vs;
-  p.o = o;
-  p.os = dense;
-  p.status = status;
-  p.H = H;
-  p.BH = BH;
-  p.N = N;
-  p.Np = Np;
-  p.causal = causal;
-  p.n_qt = Np / 128;
-  p.a = static_cast<float>(1.4426950408889634 / sqrt(static_cast<double>(D)));
-  p.mx = 0;
-  p.flags = 0;
-  p.wait_ns = kAttnWaitNs;
-  return launch_attn(tq, tk, tv, p, D, st) == cudaSuccess ? SAGE_FP4_OK : SAGE_FP4_ECUDA;
+  rc = sage_fp4_quantize_qkv(q, k, v, &ops, B, H, N, D, stream);
+  if (rc != SAGE_FP4_OK) return rc;
+  return sage_fp4_attn_fwd(&ops, o, B, H, N, D, causal, stream);
 }

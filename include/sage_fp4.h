@@ -206,21 +206,26 @@ const char *sage_fp4_strerror(int status);
  * framework's operator without access to its allocator, plugins whose host
  * owns every device allocation, code that must not allocate after start-up.
  *
- * The quantized operands live in one file-scope device array of
- * SAGE_FP4_NOALLOC_SCRATCH_BYTES (64 MiB) instead of a caller workspace.
- * Every GPU that loads the library's module holds that array until the
- * process exits.  Problems whose operands need more (sage_fp4_workspace_bytes
- * minus 256) are rejected with SAGE_FP4_ETOOLARGE before anything runs; the
- * LLM prefill shape B1 H32 N8192 D128 (~54 MiB) fits, B4 H32 N4096 D128 does
- * not.
+ * The call is sage_fp4_quantize_qkv followed by sage_fp4_attn_fwd over a
+ * workspace carved from one file-scope device array of
+ * SAGE_FP4_NOALLOC_SCRATCH_BYTES (64 MiB), with the caller's status word in
+ * place of the workspace's; their argument checks and results apply
+ * unchanged.  Every GPU that loads the library's module holds that array
+ * until the process exits.  Problems whose workspace
+ * (sage_fp4_workspace_bytes) exceeds the array are rejected with
+ * SAGE_FP4_ETOOLARGE before anything runs; the LLM prefill shape B1 H32 N8192
+ * D128 (~54 MiB) fits, B4 H32 N4096 D128 (~108 MiB) does not.
  *
  * status: one int32 of device memory, zero-initialised by the caller, set to
  * SAGE_FP4_ETIMEOUT if a bounded device wait gives up (as in
  * sage_fp4_attn_fwd; launches skip their work while it is nonzero).
  *
  * The first call on each device looks up the array's device address (with
- * that device current) and caches it; make that first call before any stream
- * capture.  All calls share the array and it keeps the last call's contents;
+ * that device current) and keeps it, keyed by the current CUDA context's
+ * unique ID, so that a context created after cudaDeviceReset, or a second
+ * context on the device, gets a lookup of its own; make that first call
+ * before any stream capture.  All calls share the array and it keeps the last
+ * call's contents;
  * each call rewrites every byte it reads, so nothing has to be cleared
  * between calls.  Calls whose work overlaps on the GPU (unordered streams or
  * host threads) race on the array: order them.  Asynchronous on `stream`;

@@ -179,3 +179,18 @@ def test_binding_argument_counts_match_the_header():
     for name, args in decls.items():
         n = len([a for a in args.replace("\n", " ").split(",") if a.strip() and a.strip() != "void"])
         assert len(getattr(lib, name).argtypes) == n, name
+
+
+def test_noalloc_rejects_before_touching_the_device():
+    # sizes are checked first (EINVAL for invalid ones, ETOOLARGE above the
+    # fixed scratch array), then pointers; none of these reaches the device
+    f = S.sage_fp4_attention_noalloc
+    good = (0x1000, 0x2000, 0x3000, 0x4000, 0x5000)
+    assert f(*good, 1, 2, 512, 96, 0, None) == S.EINVAL
+    assert f(*good, -1, 2, 512, 128, 0, None) == S.EINVAL
+    assert f(*good, 1, 2, 512, 128, 2, None) == S.EINVAL
+    assert f(*good, 4, 32, 4096, 128, 0, None) == S.ETOOLARGE
+    assert f(0x1008, *good[1:], 1, 2, 512, 128, 0, None) == S.EINVAL
+    assert f(*good[:4], 0x5002, 1, 2, 512, 128, 0, None) == S.EINVAL
+    assert f(*good[:4], 0, 1, 2, 512, 128, 0, None) == S.EINVAL
+    assert f(*good, 0, 2, 512, 128, 0, None) == S.OK  # empty: a no-op

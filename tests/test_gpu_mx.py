@@ -21,7 +21,7 @@ import torch
 import oracle
 from bit_attention_gb300 import sage_fp4 as S
 from bit_attention_gb300.synth import WORKLOADS, make_qkv
-from helpers import block_offsets, cosine, rel_l1, sample_rows
+from helpers import block_offsets, check_o, cosine, rel_l1, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -122,7 +122,7 @@ def test_mx_quantization_is_bit_exact(B, H, N, D, pattern, nhd):
 
 def _mx_attention(q, k, v, causal):
     z = S.quantize_qkv(q.cuda(), k.cuda(), v.cuda(), fmt="mxfp4")
-    o = S.attn_fwd(z, causal)
+    o = S.attn_fwd(z, causal, out=torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device="cuda"))
     torch.cuda.synchronize()
     assert z.get_status() == 0
     return o
@@ -139,8 +139,7 @@ def test_mx_attention_matches_oracle(B, H, N, D, causal, pattern):
     q, k, v = make_qkv(B, H, N, D, pattern, seed=31 + N)
     got = _mx_attention(q, k, v, causal).float().cpu().numpy().reshape(B * H * N, D)
     ref = oracle.attention(oracle.Quantized(q, k, v, B * H, N, D, fmt="mxfp4"), causal)[0]
-    e, c = rel_l1(got, ref), cosine(got, ref)
-    assert np.isfinite(got).all() and e <= 5e-3 and c >= 0.999, (e, c)
+    check_o(got, ref, f"mx B{B} H{H} N{N} D{D} causal={causal} {pattern}")
 
 
 def _mx_fuzz_cases(n=6, seed=77):
@@ -156,8 +155,7 @@ def test_mx_attention_random_shapes(B, H, N, D, causal, pattern):
     q, k, v = make_qkv(B, H, N, D, pattern, seed=5 * N + D)
     got = _mx_attention(q, k, v, causal).float().cpu().numpy().reshape(B * H * N, D)
     ref = oracle.attention(oracle.Quantized(q, k, v, B * H, N, D, fmt="mxfp4"), causal)[0]
-    e, c = rel_l1(got, ref), cosine(got, ref)
-    assert np.isfinite(got).all() and e <= 5e-3 and c >= 0.999, (e, c)
+    check_o(got, ref, f"mx fuzz B{B} H{H} N{N} D{D} causal={causal} {pattern}")
 
 
 def test_mx_attention_llm_workload_sampled_rows():
@@ -167,8 +165,8 @@ def test_mx_attention_llm_workload_sampled_rows():
     rows = sample_rows(w.B * w.H, w.N, per_head=4)
     ref = oracle.attention(oracle.Quantized(q, k, v, w.B * w.H, w.N, w.D, fmt="mxfp4"), w.causal,
                            rows=rows)[0]
-    e, c = rel_l1(got[rows], ref), cosine(got[rows], ref)
-    assert e <= 5e-3 and c >= 0.999, (e, c)
+    assert np.isfinite(got).all()
+    check_o(got[rows], ref, "mx llm sampled rows")
 
 
 @pytest.mark.parametrize("name", ["llm", "dit", "dit_long"])

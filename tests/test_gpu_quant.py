@@ -74,3 +74,28 @@ def test_quantize_full_workload(name):
     w = WORKLOADS[name]
     q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.pattern, seed=0)
     check_quant(q, k, v)
+
+
+def test_every_bf16_magnitude_as_group_absmax():
+    # Every non-negative finite bf16 value (bit patterns 0x0000-0x7F7F, 32640
+    # of them, subnormals included) is the absmax of exactly one group, in Q
+    # and K (groups along D) and in V (groups along tokens).  The kernels take
+    # amax/6 as amax*RN(1/6) plus one FMA residual step, which must equal the
+    # correctly rounded quotient the oracle computes for every one of them;
+    # the other 15 elements of a group are random fractions of its absmax, of
+    # either sign, so the codes are checked across the whole range as well.
+    amax = (np.arange(0x7F80, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+    G = amax.size
+    rng = np.random.default_rng(4)
+    frac = rng.uniform(-1.0, 1.0, size=(G, 16))
+    frac[np.arange(G), rng.integers(0, 16, size=G)] = rng.choice([-1.0, 1.0], size=G)
+    # float64 -> float32 -> bf16, each rounding to nearest: |x| <= amax stays true
+    groups = torch.from_numpy((amax[:, None] * frac).astype(np.float32)).to(torch.bfloat16)
+    got_amax = groups.float().abs().amax(1).numpy()
+    assert np.array_equal(got_amax, amax.astype(np.float32))
+    D, N = 128, G * 16 // 128  # 4080 rows of 8 groups
+    q = groups.reshape(1, 1, N, D)
+    k = q.flip(2).contiguous()
+    # V: group g of channel d is tokens 16g..16g+15 of channel d
+    v = groups.reshape(D, N // 16, 16).reshape(D, N).t().contiguous().reshape(1, 1, N, D)
+    check_quant(q, k, v)
