@@ -57,16 +57,18 @@ def sample_rows(BH: int, N: int, per_head: int, seed: int = 0) -> np.ndarray:
 
 # Tolerances of the GPU attention output against the oracle.  The whole
 # tensor: relative L1 <= 5e-3 and cosine >= 0.999 (the target's).  Each row on
-# its own: cosine >= 0.99, and max |got - ref| <= ROW_MAXABS_K * max |ref| of
+# its own: cosine >= 0.9995, and max |got - ref| <= ROW_MAXABS_K * max |ref| of
 # that row, so that one bad row (left unwritten, stale, or from the wrong tile)
 # cannot hide in the whole-tensor figures.  The two sides differ by bf16
 # rounding of O (2^-9 relative) and by P codes at an E2M1 rounding boundary,
 # where the kernel's FP32 exp2 and the oracle's FP64 exp can pick neighbouring
-# codes.
+# codes.  Measured over every attention test case on GB300 (NVFP4 and MXFP4,
+# all shapes): the worst row has max |diff| = 0.0055 of its largest value and
+# cosine 0.99999; the bounds leave a margin of about 3.6x and 50x.
 REL_L1_MAX = 5e-3
 COS_MIN = 0.999
-ROW_COS_MIN = 0.99
-ROW_MAXABS_K = 0.06
+ROW_COS_MIN = 0.9995
+ROW_MAXABS_K = 0.02
 
 
 def row_stats(got: np.ndarray, ref: np.ndarray):
