@@ -354,6 +354,13 @@ int sage_fp4_mma_peak(int iters, int n, int32_t* status, void* stream) {
   return from_cuda(launch_mma_peak(iters, n, status, static_cast<cudaStream_t>(stream)));
 }
 
+int sage_fp4_tmem_max_probe(const float* in, float* vals, float* maxes, void* stream) {
+  if (!aligned(in, 16) || !aligned(vals, 16) || !aligned(maxes, 16)) return SAGE_FP4_EINVAL;
+  int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  return from_cuda(launch_tmem_max_probe(in, vals, maxes, static_cast<cudaStream_t>(stream)));
+}
+
 int sage_fp4_mma_probe_mx(const uint8_t* a_codes, const uint8_t* a_scales, const uint8_t* b_codes,
                           const uint8_t* b_scales, int n, int K, int a_by_threads, float* d,
                           int32_t* status, void* stream) {

@@ -192,6 +192,13 @@ __device__ __forceinline__ void cta_bar_sync() {
 }
 
 constexpr float kLog2of2688 = 11.392317422778761f;  // log2(448 * 6)
+constexpr float kLog2of448 = 8.807354922057604f;    // log2(448)
+
+__device__ __forceinline__ float2 lds_f32x2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
 constexpr float kLog2of6 = 2.5849625007211563f;     // log2(6): the MXFP4 level-1 target
 
 __device__ __forceinline__ float max16(const uint32_t* s) {
@@ -486,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float a = p.a;
       const uint64_t a2 = pack2(a, a);
       const int sw = (r >> 1) & 3;  // 64-byte swizzle: 16-byte chunk c lives at c ^ ((r/2) % 4)
-      const float2* lut = reinterpret_cast<const float2*>(sm + L::oLut);
+      const uint32_t lut = sb + L::oLut;
       bool ok = true;
       int g0 = 0;  // stream index of the current item's first tile
       for (int it = item0; ok && it < n_items; it += istep) {
@@ -506,21 +513,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t tb = tmem + kColS + par * 128 + lane_base;
             // pass 1: the 16-element group maxima, whose maximum is the tile
-            // maximum; the second 64 keys stay in registers for pass 2
+            // maximum; the second 64 keys stay in registers for pass 2.  Where
+            // no key is masked, each group's maximum comes with its load from
+            // tensor memory (the reducing form of tcgen05.ld), with no
+            // comparisons in the thread.
             float gm[8];
             uint32_t s64[64];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              tmem_ld32(tb + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&s64[0]));
-              tmem_ld32(tb + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&s64[32]));
-              tmem_wait_ld();
-              if (kMasked && lim < kTileKV) {
+              if constexpr (kMasked) {
+                tmem_ld32(tb + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&s64[0]));
+                tmem_ld32(tb + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&s64[32]));
+                tmem_wait_ld();
+                if (lim < kTileKV) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j)
-                  if (64 * h + j >= lim) s64[j] = __float_as_uint(-INFINITY);
+                  for (int j = 0; j < 64; ++j)
+                    if (64 * h + j >= lim) s64[j] = __float_as_uint(-INFINITY);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) gm[4 * h + q] = max16(&s64[16 * q]);
+              } else {
+                // groups whose maximum comes with the load: all eight at D = 64;
+                // at D = 128 the first three (with four or more the kernel
+                // spills registers and runs 7-12% slower; with three it gains
+                // 2.7%, measured), the others by comparisons in the thread
+                constexpr int kRedFirst = (D == 64) ? 4 : 3, kRedSecond = (D == 64) ? 4 : 0;
+                const int nred = (h == 0) ? kRedFirst : kRedSecond;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  if (q < nred)
+                    tmem_ld16_max(tb + 64 * h + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(&s64[16 * q]),
+                                  gm[4 * h + q]);
+                  else
+                    tmem_ld16(tb + 64 * h + 16 * q, *reinterpret_cast<uint32_t(*)[16]>(&s64[16 * q]));
+                }
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  if (q >= nred) gm[4 * h + q] = max16(&s64[16 * q]);
               }
-#pragma unroll
-              for (int q = 0; q < 4; ++q) gm[4 * h + q] = max16(&s64[16 * q]);
             }
             const float t = max3f(max3f(gm[0], gm[1], gm[2]), max3f(gm[3], gm[4], gm[5]),
                                   fmaxf(gm[6], gm[7]));
@@ -549,12 +580,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               s2[2] = e8[2] | (e8[3] << 8);
               s2[3] = 0u;
             } else {
+              const float nbs = nb + kLog2of448;  // 448 e^(c(g - t)) as one exponential
 #pragma unroll
               for (int q = 0; q < 8; q += 2) {
-                const float e0 = ex2_approx(fmaf(gm[q], a, nb));
-                const float e1 = ex2_approx(fmaf(gm[q + 1], a, nb));
-                s2[q / 2] = cvt_e4m3x2(448.0f * e0, 448.0f * e1);
-                const float2 t0 = lut[s2[q / 2] & 0xFFu], t1 = lut[s2[q / 2] >> 8];
+                const float e0 = ex2_approx(fmaf(gm[q], a, nbs));
+                const float e1 = ex2_approx(fmaf(gm[q + 1], a, nbs));
+                s2[q / 2] = cvt_e4m3x2(e0, e1);
+                const float2 t0 = lds_f32x2(lut + 8 * (s2[q / 2] & 0xFFu)), t1 = lds_f32x2(lut + 8 * (s2[q / 2] >> 8));
                 bias[q] = nb + t0.x;
                 lsc[q] = t0.y;
                 bias[q + 1] = nb + t1.x;

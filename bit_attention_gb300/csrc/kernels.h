@@ -70,5 +70,6 @@ struct MmaProbeParams {
 cudaError_t launch_mma_probe(const CUtensorMap& ta, const CUtensorMap& tb, const MmaProbeParams& p,
                              cudaStream_t st);
 cudaError_t launch_mma_peak(int iters, int n, int32_t* status, cudaStream_t st);
+cudaError_t launch_tmem_max_probe(const float* in, float* vals, float* maxes, cudaStream_t st);
 
 }  // namespace sagefp4

@@ -3,7 +3,9 @@
 //   * the FP32 -> E2M1 / E4M3 conversions, over any range of bit patterns;
 //   * one block-scaled FP4 tensor-core product of a 128-row tile, with its
 //     operands staged exactly as the attention kernel stages Q/K/V (TMA with
-//     hardware swizzle) or P (thread stores into the swizzled layout).
+//     hardware swizzle) or P (thread stores into the swizzled layout);
+//   * the reducing tensor-memory load (values and their maximum per 16
+//     columns) the attention kernel takes its group maxima from.
 #include <cuda_fp16.h>
 
 #include "../../include/sage_fp4.h"
@@ -235,7 +237,56 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int n, int3
   }
 }
 
+// The reducing tensor-memory load the attention kernel uses for group
+// maxima: one CTA of 128 threads stores in[r][0..127] (FP32, row r = lane r)
+// into 128 tensor-memory columns, reads them back in eight 16-column groups
+// with tcgen05.ld.red ... max, and writes the values it got to vals[r][..]
+// and the reported maxima to maxes[r][0..7].
+__global__ void __launch_bounds__(128, 1)
+    tmem_max_probe_kernel(const float* __restrict__ in, float* __restrict__ vals, float* __restrict__ maxes) {
+  __shared__ uint32_t slot;
+  const int warp = threadIdx.x >> 5, r = threadIdx.x;
+  if (warp == 0) {
+    tmem_alloc(smem_addr(&slot), 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tb = slot + lane_base;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = __float_as_uint(in[r * 128 + 8 * c + j]);
+    tmem_st8(tb + 8 * c, w);
+  }
+  tmem_wait_st();
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    uint32_t v[16];
+    float mx;
+    tmem_ld16_max(tb + 16 * g, v, mx);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) vals[r * 128 + 16 * g + j] = __uint_as_float(v[j]);
+    maxes[r * 8 + g] = mx;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(slot, 128);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_tmem_max_probe(const float* in, float* vals, float* maxes, cudaStream_t st) {
+  tmem_max_probe_kernel<<<1, 128, 0, st>>>(in, vals, maxes);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_cvt_probe(uint32_t first, uint32_t count, uint8_t* e2m1, uint8_t* e4m3,
                              cudaStream_t st) {

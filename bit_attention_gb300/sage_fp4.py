@@ -78,6 +78,7 @@ def load(build: bool = True) -> ctypes.CDLL:
                 "sage_fp4_mma_probe_mx": (i, [vp, vp, vp, vp, i, i, i, vp, vp, vp]),
                 "sage_fp4_mma_probe_ex": (i, [vp, vp, vp, vp, i, i, i, vp, vp, vp]),
                 "sage_fp4_mma_peak": (i, [i, i, vp, vp]),
+                "sage_fp4_tmem_max_probe": (i, [vp, vp, vp, vp]),
                 "sage_fp4_attention_noalloc": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, vp]),
                 "sage_fp4_host_workspace_bytes": (sz, [i, i, i, i]),
                 "sage_fp4_attention_host": (i, [vp, vp, vp, vp, i, i, i, i, i, vp, sz, vp, vp]),
@@ -180,6 +181,10 @@ def sage_fp4_mma_probe_ex(a_codes, a_scales, b_codes, b_scales, n, K, flags, d, 
 
 def sage_fp4_mma_peak(iters, n, status_ptr, stream) -> int:
     return load().sage_fp4_mma_peak(iters, n, status_ptr, stream)
+
+
+def sage_fp4_tmem_max_probe(in_ptr, vals_ptr, maxes_ptr, stream) -> int:
+    return load().sage_fp4_tmem_max_probe(in_ptr, vals_ptr, maxes_ptr, stream)
 
 
 def mma_peak_tflops(n: int = 256, iters: int = 20000, repeats: int = 3) -> float:

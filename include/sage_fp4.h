@@ -332,6 +332,18 @@ int sage_fp4_mma_probe_ex(const uint8_t *a_codes, const uint8_t *a_scales, const
  * pages. */
 int sage_fp4_mma_peak(int iters, int n, int32_t *status, void *stream);
 
+/* The reducing tensor-memory load from which the attention kernel takes the
+ * 16-key group maxima of a tile row (the fusion of the group maxima with the
+ * row maximum, senqingzn.com article, "FP4 attention inference acceleration
+ * and hardware implementation/optimisation"): one block of 128 threads stores
+ * in[r][c] (FP32, 128 x 128, row-major, r = tensor-memory lane) into tensor
+ * memory, reads each row back in eight 16-column groups with
+ * tcgen05.ld.red.max, and writes the values read to vals[r][c] and the
+ * maximum the instruction reported for group g to maxes[r][g] (128 x 8).
+ * All three are device pointers, 16-byte aligned.  No counterpart in the
+ * pages. */
+int sage_fp4_tmem_max_probe(const float *in, float *vals, float *maxes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

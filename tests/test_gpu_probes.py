@@ -93,3 +93,30 @@ def test_mma_peak_rate(n):
     tflops = S.mma_peak_tflops(n=n, iters=4000)
     print(f"FP4 MMA rate, N={n}: {tflops:.0f} TFLOP/s")
     assert 3000 < tflops < 20000, tflops
+
+
+def test_tmem_reducing_load_gives_group_maxima():
+    # The attention kernel takes each 16-key group's maximum of a score row
+    # from the load that brings the scores out of tensor memory.  Pin what it
+    # returns: the values unchanged, and per 16 columns their maximum --
+    # including -inf (masked keys), groups of equal values, +-0 and values of
+    # every magnitude a score can take.
+    rng = np.random.default_rng(17)
+    x = (rng.standard_normal((128, 128)) * np.exp(rng.uniform(-20, 20, (128, 1)))).astype(np.float32)
+    x[1, :16] = -np.inf                # a fully masked group
+    x[2, 5:16] = -np.inf               # a partly masked group
+    x[3, 16:32] = 2.5                  # equal values
+    x[4, 32:48] = -0.0
+    x[5, 48:64] = -rng.uniform(1, 2, 16).astype(np.float32)  # all negative
+    x[6, 64] = 3.0e38
+    xin = torch.from_numpy(x).cuda()
+    vals = torch.full((128, 128), float("nan"), device="cuda")
+    maxes = torch.full((128, 8), float("nan"), device="cuda")
+    rc = S.sage_fp4_tmem_max_probe(xin.data_ptr(), vals.data_ptr(), maxes.data_ptr(),
+                                   torch.cuda.current_stream().cuda_stream)
+    assert rc == S.OK, S.strerror(rc)
+    torch.cuda.synchronize()
+    v, m = vals.cpu().numpy(), maxes.cpu().numpy()
+    assert np.array_equal(v.view(np.uint32), x.view(np.uint32))
+    want = x.reshape(128, 8, 16).max(-1)
+    assert np.array_equal(m, want), np.argwhere(m != want)[:5]
