@@ -164,10 +164,12 @@ int sage_fp4_qkv_from_workspace(void* workspace, size_t workspace_bytes, int B, 
   return SAGE_FP4_OK;
 }
 
-int sage_fp4_quantize_qkv_strided(const void* q, const sage_fp4_strides* q_strides, const void* k,
-                                  const sage_fp4_strides* k_strides, const void* v,
-                                  const sage_fp4_strides* v_strides, const sage_fp4_qkv* out, int B,
-                                  int H, int N, int D, int format, void* stream) {
+namespace {
+
+int quantize_impl(const void* q, const sage_fp4_strides* q_strides, const void* k,
+                  const sage_fp4_strides* k_strides, const void* v, const sage_fp4_strides* v_strides,
+                  const sage_fp4_qkv* out, int B, int H, int N, int D, int format, uint64_t wait_ns,
+                  int withhold, void* stream) {
   if (!dims_ok(B, H, N, D) || !out || !format_ok(format)) return SAGE_FP4_EINVAL;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return SAGE_FP4_EINVAL;
   if (!tensor_ok(out->q) || !tensor_ok(out->k) || !tensor_ok(out->vt) || !aligned(out->status, 4))
@@ -185,7 +187,25 @@ int sage_fp4_quantize_qkv_strided(const void* q, const sage_fp4_strides* q_strid
   cudaError_t e = launch_quant_rows(q, k, sq, sk, out->q.codes, out->q.scales, out->k.codes,
                                     out->k.scales, H, BH, N, D, mx, st);
   if (e != cudaSuccess) return SAGE_FP4_ECUDA;
-  return from_cuda(launch_quant_v(v, sv, out->vt.codes, out->vt.scales, H, BH, N, D, mx, out->status, st));
+  return from_cuda(
+      launch_quant_v(v, sv, out->vt.codes, out->vt.scales, H, BH, N, D, mx, out->status, wait_ns, withhold, st));
+}
+
+}  // namespace
+
+int sage_fp4_quantize_qkv_strided(const void* q, const sage_fp4_strides* q_strides, const void* k,
+                                  const sage_fp4_strides* k_strides, const void* v,
+                                  const sage_fp4_strides* v_strides, const sage_fp4_qkv* out, int B,
+                                  int H, int N, int D, int format, void* stream) {
+  return quantize_impl(q, q_strides, k, k_strides, v, v_strides, out, B, H, N, D, format, kAttnWaitNs, 0,
+                       stream);
+}
+
+int sage_fp4_quantize_qkv_stall_test(const void* q, const void* k, const void* v, const sage_fp4_qkv* out,
+                                     int B, int H, int N, int D, uint64_t wait_limit_ns, void* stream) {
+  if (wait_limit_ns < 1000000ull || wait_limit_ns > kAttnWaitNs) return SAGE_FP4_EINVAL;
+  return quantize_impl(q, nullptr, k, nullptr, v, nullptr, out, B, H, N, D, SAGE_FP4_FORMAT_NVFP4,
+                       wait_limit_ns, 1, stream);
 }
 
 int sage_fp4_quantize_qkv(const void* q, const void* k, const void* v, const sage_fp4_qkv* out,

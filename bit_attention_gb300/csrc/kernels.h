@@ -23,8 +23,11 @@ inline Strides contiguous_bhnd(int H, int N, int D) {
 cudaError_t launch_quant_rows(const void* q, const void* k, Strides sq, Strides sk, uint8_t* qc,
                               uint8_t* qs, uint8_t* kc, uint8_t* ks, int H, int BH, int N, int D,
                               bool mx, cudaStream_t st);
+// wait_ns bounds every wait for a tile; withhold: failure-detection test (block
+// 0 never issues its first tile).
 cudaError_t launch_quant_v(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, int H, int BH, int N,
-                           int D, bool mx, int32_t* status, cudaStream_t st);
+                           int D, bool mx, int32_t* status, uint64_t wait_ns, int withhold,
+                           cudaStream_t st);
 
 struct AttnParams {
   const uint8_t* sfq;  // Q scales (block layout), per (b,h) N_pad*D/16 bytes

@@ -172,11 +172,17 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
 // 32 tokens are one group; its E8M0 byte goes to byte `seg` of the tile's
 // scale word (a 64-token tile is one K = 64 step), and seg 0 zeroes the
 // word's upper half.
+// Every wait for a tile is bounded by wait_ns; a wait that gives up sets
+// *status to SAGE_FP4_ETIMEOUT and the whole block leaves together (one vote
+// of all its threads decides), after the copies it still has in flight have
+// landed.  withhold (failure-detection test only): block 0 never issues its
+// first tile, so its wait for that tile runs out.
 template <int D, int TT, int NS, bool MX>
 __global__ void __launch_bounds__(128) quant_v_kernel(const uint8_t* __restrict__ v, Strides sv,
                                                       uint8_t* __restrict__ vc,
                                                       uint8_t* __restrict__ vs, int H, int BH,
-                                                      int N, int Np, int32_t* status) {
+                                                      int N, int Np, int32_t* status, uint64_t wait_ns,
+                                                      int withhold) {
   static_assert(TT == 64 || TT == 128, "tile of 64 or 128 tokens");
   static_assert(!MX || TT == 64, "MX scale words follow 64-token tiles");
   constexpr int TILE_BYTES = TT * D * 2;
@@ -223,7 +229,7 @@ __global__ void __launch_bounds__(128) quant_v_kernel(const uint8_t* __restrict_
   if (threadIdx.x < 32)
     for (int s = 0; s < NS - 1; ++s) {
       const long long ws = blockIdx.x + static_cast<long long>(s) * gridDim.x;
-      if (ws < work) issue(ws, s);
+      if (ws < work && !(withhold && blockIdx.x == 0 && s == 0)) issue(ws, s);
     }
   const size_t vt_row = static_cast<size_t>(Np) / 2;
   long long w = blockIdx.x;
@@ -232,39 +238,40 @@ __global__ void __launch_bounds__(128) quant_v_kernel(const uint8_t* __restrict_
     // refill the slot that the last iteration released at its closing barrier
     const long long wn = w + static_cast<long long>(NS - 1) * gridDim.x;
     if (threadIdx.x < 32 && wn < work) issue(wn, (it + NS - 1) % NS);
-    // wait for this tile (bounded: a copy that never lands sets the status)
+    // wait for this tile: every thread's wait is bounded
+    bool ok = true;
     {
       const uint64_t t0 = globaltimer_ns();
-      bool ok = true;
       while (!mbar_try_wait(bar0 + 8 * buf, (it / NS) & 1)) {
-        if (globaltimer_ns() - t0 > 1500000000ull) {
+        if (globaltimer_ns() - t0 > wait_ns) {
           ok = false;
           break;
         }
-      }
-      if (!ok) {
-        if (threadIdx.x == 0) {
-          atomicCAS(status, 0, -3);  // SAGE_FP4_ETIMEOUT
-          // let the copies already issued into the other slots land before exiting
-          const uint64_t t1 = globaltimer_ns();
-          for (int s = 1; s < NS; ++s) {
-            const long long ws = w + static_cast<long long>(s) * gridDim.x;
-            if (ws >= work) break;
-            const int j = it + s;
-            while (!mbar_try_wait(bar0 + 8 * (j % NS), (j / NS) & 1) &&
-                   globaltimer_ns() - t1 < 1500000000ull) {
-            }
-          }
-        }
-        griddep_wait();
-        return;
       }
     }
     const int bh = static_cast<int>(w / ntiles), tb = static_cast<int>(w % ntiles);
     uint32_t* tile = tiles + buf * (TILE_BYTES / 4);
     const int rows = tile_rows(w);
-    for (int i = rows * (D / 2) + threadIdx.x; i < TT * (D / 2); i += 128) tile[i] = 0u;
-    __syncthreads();
+    if (ok)
+      for (int i = rows * (D / 2) + threadIdx.x; i < TT * (D / 2); i += 128) tile[i] = 0u;
+    // one vote of the whole block (it also publishes the zeroed rows): if any
+    // thread's wait gave up, every thread leaves
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) {
+        atomicCAS(status, 0, -3);  // SAGE_FP4_ETIMEOUT
+        // let the copies already issued into the other slots land before exiting
+        const uint64_t t1 = globaltimer_ns();
+        for (int s = 1; s < NS; ++s) {
+          const long long ws = w + static_cast<long long>(s) * gridDim.x;
+          if (ws >= work) break;
+          const int j = it + s;
+          while (!mbar_try_wait(bar0 + 8 * (j % NS), (j / NS) & 1) && globaltimer_ns() - t1 < wait_ns) {
+          }
+        }
+      }
+      griddep_wait();
+      return;
+    }
 
     uint8_t* __restrict__ vs_bh = vs + static_cast<size_t>(bh) * 8 * Np;
     for (int item = threadIdx.x; item < ITEMS; item += 128) {
@@ -396,7 +403,8 @@ cudaError_t launch_quant_rows(const void* q, const void* k, Strides sq, Strides 
 
 template <int D, int TT, int NS, bool MX>
 cudaError_t launch_quant_v_cfg(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, int H, int BH,
-                               int Np, int N, int32_t* status, int blocks_per_sm, cudaStream_t st) {
+                               int Np, int N, int32_t* status, int blocks_per_sm, uint64_t wait_ns,
+                               int withhold, cudaStream_t st) {
   const long long work = static_cast<long long>(Np / TT) * BH;
   const int smem = NS * TT * D * 2;
   long long blocks = static_cast<long long>(num_sms()) * blocks_per_sm;
@@ -420,11 +428,11 @@ cudaError_t launch_quant_v_cfg(const void* v, Strides sv, uint8_t* vc, uint8_t* 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, quant_v_kernel<D, TT, NS, MX>, static_cast<const uint8_t*>(v), sv, vc, vs,
-                            H, BH, N, Np, status);
+                            H, BH, N, Np, status, wait_ns, withhold);
 }
 
 cudaError_t launch_quant_v(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, int H, int BH, int N,
-                           int D, bool mx, int32_t* status, cudaStream_t st) {
+                           int D, bool mx, int32_t* status, uint64_t wait_ns, int withhold, cudaStream_t st) {
   const int Np = round_up_int(N, 128);
   // 64-token tiles, double-buffered: 32 KB (D = 128) or 16 KB (D = 64) of
   // shared memory per block.  The per-tile arithmetic, not the copy latency,
@@ -432,10 +440,10 @@ cudaError_t launch_quant_v(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, 
   // GB300: 5.3-5.8 TB/s at D = 128 with six blocks per SM, against 4.0-4.9 TB/s
   // with four-deep rings and two or three blocks).
   if (D == 128)
-    return mx ? launch_quant_v_cfg<128, 64, 2, true>(v, sv, vc, vs, H, BH, Np, N, status, 6, st)
-              : launch_quant_v_cfg<128, 64, 2, false>(v, sv, vc, vs, H, BH, Np, N, status, 6, st);
-  return mx ? launch_quant_v_cfg<64, 64, 2, true>(v, sv, vc, vs, H, BH, Np, N, status, 8, st)
-            : launch_quant_v_cfg<64, 64, 2, false>(v, sv, vc, vs, H, BH, Np, N, status, 8, st);
+    return mx ? launch_quant_v_cfg<128, 64, 2, true>(v, sv, vc, vs, H, BH, Np, N, status, 6, wait_ns, withhold, st)
+              : launch_quant_v_cfg<128, 64, 2, false>(v, sv, vc, vs, H, BH, Np, N, status, 6, wait_ns, withhold, st);
+  return mx ? launch_quant_v_cfg<64, 64, 2, true>(v, sv, vc, vs, H, BH, Np, N, status, 8, wait_ns, withhold, st)
+            : launch_quant_v_cfg<64, 64, 2, false>(v, sv, vc, vs, H, BH, Np, N, status, 8, wait_ns, withhold, st);
 }
 
 }  // namespace sagefp4

@@ -71,6 +71,7 @@ def load(build: bool = True) -> ctypes.CDLL:
                 "sage_fp4_quantize_qkv_strided": (i, [vp, sp, vp, sp, vp, sp, qp, i, i, i, i, i, vp]),
                 "sage_fp4_attn_fwd_ex": (i, [qp, vp, sp, i, i, i, i, i, ctypes.c_float, i, vp]),
                 "sage_fp4_attn_fwd_stall_test": (i, [qp, vp, i, i, i, i, i, ctypes.c_uint64, vp]),
+                "sage_fp4_quantize_qkv_stall_test": (i, [vp, vp, vp, qp, i, i, i, i, ctypes.c_uint64, vp]),
                 "sage_fp4_get_status": (i, [qp, vp]),
                 "sage_fp4_strerror": (ctypes.c_char_p, [i]),
                 "sage_fp4_cvt_probe": (i, [u32, u32, vp, vp, vp]),
@@ -144,6 +145,12 @@ def sage_fp4_attn_fwd_stall_test(qkv: sage_fp4_qkv, o_ptr, B, H, N, D, causal, w
                                  stream) -> int:
     return load().sage_fp4_attn_fwd_stall_test(ctypes.byref(qkv), o_ptr, B, H, N, D, int(causal),
                                                int(wait_limit_ns), stream)
+
+
+def sage_fp4_quantize_qkv_stall_test(q_ptr, k_ptr, v_ptr, qkv: sage_fp4_qkv, B, H, N, D, wait_limit_ns,
+                                     stream) -> int:
+    return load().sage_fp4_quantize_qkv_stall_test(q_ptr, k_ptr, v_ptr, ctypes.byref(qkv), B, H, N, D,
+                                                   int(wait_limit_ns), stream)
 
 
 def sage_fp4_get_status(qkv: sage_fp4_qkv, stream) -> int:

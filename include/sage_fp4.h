@@ -186,6 +186,19 @@ int sage_fp4_attn_fwd_ex(const sage_fp4_qkv *qkv, void *o, const sage_fp4_stride
 int sage_fp4_attn_fwd_stall_test(const sage_fp4_qkv *qkv, void *o, int B, int H, int N, int D,
                                  int causal, uint64_t wait_limit_ns, void *stream);
 
+/* No counterpart in the pages: the failure-detection test of the V
+ * quantizer's bounded waits.  The same launch as sage_fp4_quantize_qkv,
+ * except that one block of the V kernel never issues the copy of its first
+ * tile and every wait for a tile gives up after wait_limit_ns (1 ms to 1.5 s;
+ * sage_fp4_quantize_qkv uses 1.5 s).  That block then leaves as a whole, after
+ * the copies it still has in flight have landed; nothing faults, and
+ * *out->status becomes SAGE_FP4_ETIMEOUT.  The V^T operands are left partly
+ * written.  Returns SAGE_FP4_EINVAL for a limit out of range, else as
+ * sage_fp4_quantize_qkv; read the outcome with sage_fp4_get_status. */
+int sage_fp4_quantize_qkv_stall_test(const void *q, const void *k, const void *v,
+                                     const sage_fp4_qkv *out, int B, int H, int N, int D,
+                                     uint64_t wait_limit_ns, void *stream);
+
 /* Synchronise `stream`, read the status word of `qkv`, reset it to 0 and
  * return it (SAGE_FP4_OK, SAGE_FP4_ETIMEOUT) or SAGE_FP4_ECUDA if the copy
  * itself failed. */
