@@ -30,6 +30,9 @@ _lock = threading.Lock()
 _lib = None
 
 PMODE = {"tile": 0, "running": 1}
+# normaliser l: from the unquantized probabilities (the method's reading), or
+# from the rounded probabilities that enter PV (Direct-P)
+LNORM = {"exp": 0, "rounded": 1}
 
 
 def build(force: bool = False) -> str:
@@ -110,6 +113,11 @@ def _declare(L):
     for fn in (L.sor_quantize_rows_fmt, L.sor_quantize_v_fmt):
         fn.restype = None
         fn.argtypes = [u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p, u8p]
+    L.sor_attention_ex.restype = ctypes.c_int
+    L.sor_attention_ex.argtypes = [u8p, u8p, u8p, u8p, u8p, u8p, ctypes.c_int, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int64,
+                                   f64p, f64p, f64p]
     L.sor_attention.restype = ctypes.c_int
     L.sor_attention.argtypes = [u8p, u8p, u8p, u8p, u8p, u8p, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
@@ -232,8 +240,9 @@ def default_scale(D: int) -> float:
 
 
 def attention(qz: Quantized, causal: bool, pmode: str = "tile", rows=None, kv_tile: int = 128,
-              scale: float | None = None):
-    """Tiled FP4 attention. Returns (O [nrows,D] float64, l [nrows], m [nrows])."""
+              scale: float | None = None, lnorm: str = "exp"):
+    """Tiled FP4 attention. Returns (O [nrows,D] float64, l [nrows], m [nrows]).
+    lnorm: "exp" (l from the unquantized probabilities) or "rounded" (Direct-P)."""
     BH, N, D = qz.BH, qz.N, qz.D
     scale = default_scale(D) if scale is None else float(scale)
     if rows is None:
@@ -245,10 +254,10 @@ def attention(qz: Quantized, causal: bool, pmode: str = "tile", rows=None, kv_ti
     out = np.empty((nrows, D), np.float64)
     ol = np.empty(nrows, np.float64)
     om = np.empty(nrows, np.float64)
-    rc = lib().sor_attention(
+    rc = lib().sor_attention_ex(
         _p(qz.qc, ctypes.c_uint8), _p(qz.qs, ctypes.c_uint8), _p(qz.kc, ctypes.c_uint8),
         _p(qz.ks, ctypes.c_uint8), _p(qz.vc, ctypes.c_uint8), _p(qz.vs, ctypes.c_uint8),
-        BH, N, D, int(bool(causal)), FORMATS[qz.fmt], scale, PMODE[pmode], kv_tile,
+        BH, N, D, int(bool(causal)), FORMATS[qz.fmt], scale, PMODE[pmode], LNORM[lnorm], kv_tile,
         _p(rows_a, ctypes.c_int64) if rows_a is not None else None, nrows,
         _p(out, ctypes.c_double), _p(ol, ctypes.c_double), _p(om, ctypes.c_double))
     if rc != 0:

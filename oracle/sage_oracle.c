@@ -310,10 +310,15 @@ static void init_tables(void) {
  * with its range, and 6 keeps each row's tile maximum exactly representable
  * (scale 2^0, code 6), as 2688 does for NVFP4 (scale 448, code 6).
  *   acc    = acc * exp((m_old - m_new)/sqrt(D)) + sP1 * sum_j dec(P2_j) * dec(V_j)
- * and finally O = acc / l. */
+ * and finally O = acc / l.
+ * lnorm 1 (Direct-P, the rit.work summary of "Hardware-Aware FP4
+ * FlashAttention-4", "Что сделали"): the normaliser is summed from the same
+ * rounded probabilities that enter PV, sP1 * dec(P2_j) for each key, instead
+ * of the unquantized exp((S_j - m_new)/sqrt(D)); the page defines no other
+ * arithmetic, so the codes are still those of level 2 above. */
 static void attend_row(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const uint8_t *ks,
                        const uint8_t *vc, const uint8_t *vs, int N, int N_pad, int D, int causal,
-                       int fmt, double scale, int pmode, int kv_tile, int i, double *out,
+                       int fmt, double scale, int pmode, int lnorm, int kv_tile, int i, double *out,
                        double *out_l, double *out_m) {
   const double isd = scale;
   const int GS = group_size(fmt);                            /* elements per scale */
@@ -357,7 +362,6 @@ static void attend_row(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, 
     double alpha = exp((m - m_new) * isd);
     double lt = 0.0;
     for (int jj = 0; jj < T; jj++) lt += exp((S[jj] - m_new) * isd);
-    l = l * alpha + lt;
 
     /* level 1 */
     double ref = (pmode == 0) ? t : m_new;
@@ -365,6 +369,18 @@ static void attend_row(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, 
     for (int jj = 0; jj < T; jj++) P2[jj] = (float)(R * exp((S[jj] - ref) * isd));
     /* level 2 */
     for (int g = 0; g < T / GS; g++) quant_group(fmt, &P2[GS * g], &pc[GS * g], &ps[g]);
+
+    if (lnorm == 1) {
+      /* Direct-P: the tile's share of l from the rounded probabilities */
+      double rounded = 0.0;
+      for (int g = 0; g < T / GS; g++) {
+        double part = 0.0;
+        for (int k = 0; k < GS; k++) part += g_e2m1[pc[GS * g + k]];
+        rounded += sc[ps[g]] * part;
+      }
+      lt = sP1 * rounded;
+    }
+    l = l * alpha + lt;
 
     /* O update */
     for (int d = 0; d < D; d++) {
@@ -388,11 +404,12 @@ static void attend_row(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, 
   if (out_m) *out_m = m;
 }
 
-int sor_attention(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const uint8_t *ks,
-                  const uint8_t *vc, const uint8_t *vs, int BH, int N, int D, int causal,
-                  int fmt, double scale, int pmode, int kv_tile, const int64_t *rows,
-                  int64_t nrows, double *out, double *out_l, double *out_m) {
+int sor_attention_ex(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const uint8_t *ks,
+                     const uint8_t *vc, const uint8_t *vs, int BH, int N, int D, int causal,
+                     int fmt, double scale, int pmode, int lnorm, int kv_tile, const int64_t *rows,
+                     int64_t nrows, double *out, double *out_l, double *out_m) {
   if (fmt != SOR_FMT_NVFP4 && fmt != SOR_FMT_MXFP4) return -1;
+  if (lnorm != 0 && lnorm != 1) return -1;
   const int GS = group_size(fmt);
   if (D % GS || D > SOR_MAX_D || kv_tile % GS || kv_tile > SOR_MAX_TILE || kv_tile <= 0 || N < 1 ||
       !(scale > 0.0) || isinf(scale))
@@ -408,10 +425,18 @@ int sor_attention(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const
     attend_row(qc + (size_t)bh * N_pad * (D / 2), qs + (size_t)bh * N_pad * (D / GS),
                kc + (size_t)bh * N_pad * (D / 2), ks + (size_t)bh * N_pad * (D / GS),
                vc + (size_t)bh * D * (N_pad / 2), vs + (size_t)bh * D * (N_pad / GS), N, N_pad, D,
-               causal, fmt, scale, pmode, kv_tile, i, out + (size_t)r * D, out_l ? out_l + r : 0,
+               causal, fmt, scale, pmode, lnorm, kv_tile, i, out + (size_t)r * D, out_l ? out_l + r : 0,
                out_m ? out_m + r : 0);
   }
   return 0;
+}
+
+int sor_attention(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const uint8_t *ks,
+                  const uint8_t *vc, const uint8_t *vs, int BH, int N, int D, int causal,
+                  int fmt, double scale, int pmode, int kv_tile, const int64_t *rows,
+                  int64_t nrows, double *out, double *out_l, double *out_m) {
+  return sor_attention_ex(qc, qs, kc, ks, vc, vs, BH, N, D, causal, fmt, scale, pmode, 0, kv_tile,
+                          rows, nrows, out, out_l, out_m);
 }
 
 /* Exact softmax(scale * Q K^T) V in double, from the bf16 inputs. */

@@ -79,6 +79,15 @@ int sor_attention(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const
                   int fmt, double scale, int pmode, int kv_tile, const int64_t *rows,
                   int64_t nrows, double *out, double *out_l, double *out_m);
 
+/* sor_attention with the normaliser chosen: lnorm 0 = l from the unquantized
+ * probabilities (the method's reading; sor_attention), lnorm 1 = l from the
+ * rounded probabilities that enter PV (Direct-P, the rit.work summary of
+ * "Hardware-Aware FP4 FlashAttention-4"). */
+int sor_attention_ex(const uint8_t *qc, const uint8_t *qs, const uint8_t *kc, const uint8_t *ks,
+                     const uint8_t *vc, const uint8_t *vs, int BH, int N, int D, int causal,
+                     int fmt, double scale, int pmode, int lnorm, int kv_tile, const int64_t *rows,
+                     int64_t nrows, double *out, double *out_l, double *out_m);
+
 /* Exact attention softmax(scale * Q K^T) V, unquantized, from the bf16
  * inputs, in double. */
 int sor_attention_exact(const uint16_t *q, const uint16_t *k, const uint16_t *v, int BH, int N,

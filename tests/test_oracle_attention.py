@@ -299,6 +299,11 @@ MUTATIONS = {
     "running_sP1_as_tile": ("double sP1 = (pmode == 0) ? exp((t - m_new) * isd) / R : 1.0 / R;",
                             "double sP1 = exp((t - m_new) * isd) / R;"),
     "running_ref_is_tile_max": ("double ref = (pmode == 0) ? t : m_new;", "double ref = t;"),
+    "directp_drops_group_scale": ("        rounded += sc[ps[g]] * part;", "        rounded += part;"),
+    "directp_omits_sP1": ("      lt = sP1 * rounded;", "      lt = rounded / R;"),
+    "directp_normaliser_unused": ("    if (lnorm == 1) {", "    if (lnorm == 2) {"),
+    "directp_drops_code": ("for (int k = 0; k < GS; k++) part += g_e2m1[pc[GS * g + k]];",
+                           "for (int k = 1; k < GS; k++) part += g_e2m1[pc[GS * g + k]];"),
     "scale_ignored": ("double *out_m) {\n  const double isd = scale;",
                       "double *out_m) {\n  const double isd = 1.0 / sqrt((double)D);"),
 }
@@ -319,6 +324,11 @@ def all_pins():
         ("scale", lambda: test_scale_is_a_factor_on_scores(64, False)),
         ("exact_running", lambda: test_exactly_quantizable_inputs_with_differing_tile_maxima(
             513, False, "running")),
+        ("directp_exact", lambda: __import__("test_oracle_directp")
+         .test_exactly_quantizable_mx_inputs_give_softmax_with_either_normaliser(513, False)),
+        ("directp_two_keys", lambda: __import__("test_oracle_directp").test_two_visible_keys_closed_form("mxfp4")),
+        ("directp_constant_v", lambda: __import__("test_oracle_directp")
+         .test_constant_v_is_returned_exactly("mxfp4", False)),
     ]
     for name, fn in checks:
         try:
