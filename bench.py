@@ -169,8 +169,9 @@ def cpu_oracle_sample(w, target_s: float, seed: int = 0, fmt: str = "nvfp4"):
     from bit_attention_gb300.synth import make_qkv
     # a reduced batch with the same per-row work (full N, same D and pattern)
     q, k, v = make_qkv(1, 1, w.N, w.D, w.pattern, seed=seed)
+    lnorm = "rounded" if fmt == "mxfp4_directp" else "exp"  # Direct-P: MXFP4, rounded normaliser
     t0 = time.perf_counter()
-    qz = oracle.Quantized(q, k, v, 1, w.N, w.D, fmt=fmt)
+    qz = oracle.Quantized(q, k, v, 1, w.N, w.D, fmt="mxfp4" if fmt == "mxfp4_directp" else fmt)
     quant_s = time.perf_counter() - t0
     rng = np.random.default_rng(seed)
     rows_done, secs, ops = 0, 0.0, 0.0
@@ -178,7 +179,7 @@ def cpu_oracle_sample(w, target_s: float, seed: int = 0, fmt: str = "nvfp4"):
     while secs < target_s:
         rows = rng.integers(0, w.N, size=batch)
         t0 = time.perf_counter()
-        oracle.attention(qz, w.causal, rows=rows)
+        oracle.attention(qz, w.causal, rows=rows, lnorm=lnorm)
         secs += time.perf_counter() - t0
         keys = (rows + 1) if w.causal else np.full(batch, w.N)
         ops += float((4.0 * keys * w.D).sum())
@@ -292,8 +293,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--causal", type=int, default=None)
     ap.add_argument("--shape", default=None, help="B,H,N,D override (profiling cases)")
-    ap.add_argument("--fmt", default="nvfp4", choices=["nvfp4", "mxfp4"],
-                    help="microscaling format (mxfp4: the variant the pages set aside)")
+    ap.add_argument("--fmt", default="nvfp4", choices=["nvfp4", "mxfp4", "mxfp4_directp"],
+                    help="microscaling format (mxfp4: the variant the pages set aside; "
+                         "mxfp4_directp: MXFP4 with the normaliser from the rounded P)")
     ap.add_argument("--partition", default="heads", choices=["heads", "batch"],
                     help="with several ranks: split one problem's heads (strong scaling) or run "
                          "one batch per rank (weak scaling)")
@@ -457,7 +459,8 @@ def main():
             "higher_is_better": True, "scaling": "strong" if strong else "weak",
             "vs_baseline": None,
             "dtype": ("nvfp4 (e2m1 codes, e4m3 scales)" if args.fmt == "nvfp4"
-                      else "mxfp4 (e2m1 codes, e8m0 scales)") + " / fp32 accumulate",
+                      else "mxfp4 (e2m1 codes, e8m0 scales)") + " / fp32 accumulate" +
+                     (", normaliser from the rounded P (Direct-P)" if args.fmt == "mxfp4_directp" else ""),
             "data": "synthetic (seeded, bit_attention_gb300.synth)",
             "config": dict(w.describe(), format=args.fmt, l2="bf16 inputs 3x larger than L2; no flush",
                            parallelism=par),

@@ -137,7 +137,9 @@ bool strides_of(const sage_fp4_strides* in, int B, int H, int N, int D, Strides*
 
 bool scale_ok(float s) { return s > 0.0f && s <= 1.0e30f; }
 
-bool format_ok(int f) { return f == SAGE_FP4_FORMAT_NVFP4 || f == SAGE_FP4_FORMAT_MXFP4; }
+bool format_ok(int f) {
+  return f == SAGE_FP4_FORMAT_NVFP4 || f == SAGE_FP4_FORMAT_MXFP4 || f == SAGE_FP4_FORMAT_MXFP4_DIRECTP;
+}
 
 }  // namespace
 
@@ -183,7 +185,7 @@ int quantize_impl(const void* q, const sage_fp4_strides* q_strides, const void* 
   if (dev != SAGE_FP4_OK) return dev;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int BH = B * H;
-  const bool mx = format == SAGE_FP4_FORMAT_MXFP4;
+  const bool mx = format != SAGE_FP4_FORMAT_NVFP4;  // Direct-P operands are MXFP4
   cudaError_t e = launch_quant_rows(q, k, sq, sk, out->q.codes, out->q.scales, out->k.codes,
                                     out->k.scales, H, BH, N, D, mx, st);
   if (e != cudaSuccess) return SAGE_FP4_ECUDA;
@@ -223,6 +225,10 @@ int attn_fwd_impl(const sage_fp4_qkv* qkv, void* o, const sage_fp4_strides* o_st
   if (causal != 0 && causal != 1) return SAGE_FP4_EINVAL;
   Strides so;
   if (!strides_of(o_strides, B, H, N, D, &so) || !scale_ok(scale)) return SAGE_FP4_EINVAL;
+  if (format == SAGE_FP4_FORMAT_MXFP4_DIRECTP) {
+    const Strides dense = contiguous_bhnd(H, N, D);
+    if (so.b != dense.b || so.h != dense.h || so.n != dense.n) return SAGE_FP4_EINVAL;
+  }
   if (is_empty(B, H, N)) return SAGE_FP4_OK;
   int dev = check_device();
   if (dev != SAGE_FP4_OK) return dev;
@@ -249,7 +255,7 @@ int attn_fwd_impl(const sage_fp4_qkv* qkv, void* o, const sage_fp4_strides* o_st
   p.causal = causal;
   p.n_qt = Np / 128;
   p.a = static_cast<float>(1.4426950408889634 * static_cast<double>(scale));
-  p.mx = format == SAGE_FP4_FORMAT_MXFP4 ? 1 : 0;
+  p.mx = format == SAGE_FP4_FORMAT_MXFP4 ? 1 : format == SAGE_FP4_FORMAT_MXFP4_DIRECTP ? 2 : 0;
   p.flags = flags;
   p.wait_ns = wait_ns;
   return from_cuda(launch_attn(tq, tk, tv, p, D, static_cast<cudaStream_t>(stream)));

@@ -209,6 +209,37 @@ __device__ __forceinline__ float max16(const uint32_t* s) {
   return max3f(max3f(m0, m1, m2), max3f(m3, m4, f(15)), m0);
 }
 
+// Direct-P normaliser: the eight E2M1 codes of a word decoded (two per
+// instruction) and summed as an f16 pair, lanes = even / odd codes.  Exact:
+// the values are multiples of 1/2 and at most 6, so a lane's sum is a
+// multiple of 1/2 no larger than 24.
+__device__ __forceinline__ uint32_t e2m1x8_sum_h2(uint32_t w) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .b32 h0, h1, h2, h3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h3, b3;\n\t"
+      "add.rn.f16x2 h0, h0, h1;\n\t"
+      "add.rn.f16x2 h2, h2, h3;\n\t"
+      "add.rn.f16x2 %0, h0, h2;\n\t}"
+      : "=r"(r)
+      : "r"(w));
+  return r;
+}
+
+// The sum of the two f16 halves of a pair, as FP32 (exact for the sums above).
+__device__ __forceinline__ float h2_total(uint32_t a, uint32_t b) {
+  uint32_t s;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(s) : "r"(a), "r"(b));
+  float lo, hi;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(s));
+  return lo + hi;
+}
+
 // A work item: 128 query rows (tile qt) of head bh and its nkv KV tiles.
 // Causal lists start with the longest rows so that the static round-robin
 // over CTAs stays balanced.
@@ -231,7 +262,11 @@ __device__ __forceinline__ Item item_at(const AttnParams& p, int it) {
 }
 
 // kMx: operands and P in MXFP4 (groups of 32, E8M0 scales) instead of NVFP4.
-template <int D, bool kDenseO, bool kMx>
+// kDirectP (with kMx): the row sum l is summed from the rounded P, the
+// decoded codes times their scales, the same values PV uses (Direct-P, the
+// rit.work summary of "Hardware-Aware FP4 FlashAttention-4", "Что
+// сделали"), instead of from the unquantized exponentials.
+template <int D, bool kDenseO, bool kMx, bool kDirectP = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -600,6 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             uint8_t* prow = sm + L::oP + ps * L::PBYTES + r * 64;
             uint64_t acc[2] = {0ull, 0ull};  // row sum, two FP32x2 chains
+            float rsum = 0.0f;               // Direct-P: row sum of the rounded P
             // pass 2: exponentials, row sum and codes, 64 keys per tensor-memory
             // wait.  Where registers allow (D = 64), keys 64-127 are still in
             // registers from pass 1 and go first; otherwise both halves are read
@@ -640,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         a2, bb);
                     y[2 * e] = ex2_approx(lo2(x));
                     y[2 * e + 1] = ex2_approx(hi2(x));
-                    acc[e & 1] = fma2(pack2(y[2 * e], y[2 * e + 1]), l2, acc[e & 1]);
+                    if constexpr (!kDirectP) acc[e & 1] = fma2(pack2(y[2 * e], y[2 * e + 1]), l2, acc[e & 1]);
                   }
                   float y8[8];
 #pragma unroll
@@ -649,6 +685,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                   for (int e = 0; e < 8; ++e) y8[e] = y[8 + e];
                   w[2 * gg + 1] = cvt_e2m1x8(y8);
+                  if constexpr (kDirectP)
+                    rsum = fmaf(lsc[q], h2_total(e2m1x8_sum_h2(w[2 * gg]), e2m1x8_sum_h2(w[2 * gg + 1])), rsum);
                 }
                 *reinterpret_cast<uint4*>(prow + ((c ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
               }
@@ -659,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint32_t*>(sfp + kRowB) = __byte_perm(s2[2], s2[3], 0x5410);
             const uint64_t acc2 = add2(acc[0], acc[1]);
             reinterpret_cast<float2*>(sm + L::oStat + (g % kEvRing) * 1024)[r] =
-                make_float2(t, lo2(acc2) + hi2(acc2));
+                make_float2(t, kDirectP ? rsum : lo2(acc2) + hi2(acc2));
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B_PFULL + g % kEvRing));
@@ -786,7 +824,7 @@ int num_sms_attn() {
   return sms > 0 ? sms : 1;
 }
 
-template <int D, bool kDenseO, bool kMx>
+template <int D, bool kDenseO, bool kMx, bool kDirectP = false>
 cudaError_t launch_attn_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const AttnParams& p, cudaStream_t st) {
   static int configured_mask = 0;  // one bit per device ordinal (< 32)
@@ -797,10 +835,10 @@ cudaError_t launch_attn_d(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     // thread at launch; with any other launch allocation the increases would
     // never be granted, so refuse to launch.
     cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, attn_fwd_kernel<D, kDenseO, kMx>);
+    cudaError_t e = cudaFuncGetAttributes(&attr, attn_fwd_kernel<D, kDenseO, kMx, kDirectP>);
     if (e != cudaSuccess) return e;
     if (attr.numRegs != 65536 / kThreads) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D, kDenseO, kMx>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, kDenseO, kMx, kDirectP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem<D>::kAlloc);
     if (e != cudaSuccess) return e;
     if (dev < 32) configured_mask |= (1 << dev);
@@ -810,7 +848,7 @@ cudaError_t launch_attn_d(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   const long long items = static_cast<long long>(p.BH) * p.n_qt;
   const long long sms = num_sms_attn();
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
-  attn_fwd_kernel<D, kDenseO, kMx><<<grid, kThreads, Smem<D>::kAlloc, st>>>(tq, tk, tv, p);
+  attn_fwd_kernel<D, kDenseO, kMx, kDirectP><<<grid, kThreads, Smem<D>::kAlloc, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -820,6 +858,12 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
                         const AttnParams& p, int D, cudaStream_t st) {
   const Strides dense = contiguous_bhnd(p.H, p.N, D);
   const bool dense_o = p.os.b == dense.b && p.os.h == dense.h && p.os.n == dense.n;
+  if (p.mx == 2) {
+    // Direct-P (MXFP4): dense O only (the API checks it)
+    if (!dense_o) return cudaErrorInvalidValue;
+    return D == 128 ? launch_attn_d<128, true, true, true>(tq, tk, tv, p, st)
+                    : launch_attn_d<64, true, true, true>(tq, tk, tv, p, st);
+  }
   if (p.mx) {
     if (D == 128)
       return dense_o ? launch_attn_d<128, true, true>(tq, tk, tv, p, st)

@@ -38,7 +38,8 @@ struct AttnParams {
   int32_t* status;
   int H, BH, N, Np, causal, n_qt;
   float a;  // log2(e) * softmax scale: the scale folded into exp2
-  int mx;   // 1: operands are MXFP4 (groups of 32, E8M0 scales), P quantized the same way
+  int mx;   // 1: operands are MXFP4 (groups of 32, E8M0 scales), P quantized the same way;
+            // 2: the same with the row sum from the rounded P (Direct-P; dense O only)
   int flags;           // kAttnWithholdK: failure-detection test (see below)
   uint64_t wait_ns;    // limit of every bounded wait in the kernel
 };

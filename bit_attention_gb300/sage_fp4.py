@@ -19,7 +19,9 @@ import threading
 from . import build as _build
 
 OK, EINVAL, ECUDA, ETIMEOUT, EUNSUPPORTED, ETOOLARGE = 0, -1, -2, -3, -4, -5
-FORMATS = {"nvfp4": 0, "mxfp4": 1}  # SAGE_FP4_FORMAT_*
+# SAGE_FP4_FORMAT_*; "mxfp4_directp": MXFP4 with the softmax normaliser summed
+# from the rounded P (Direct-P); its operands are MXFP4
+FORMATS = {"nvfp4": 0, "mxfp4": 1, "mxfp4_directp": 2}
 
 _HEADER = os.path.join(_build.ROOT, "include", "sage_fp4.h")
 _lock = threading.Lock()

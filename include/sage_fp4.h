@@ -94,6 +94,14 @@ extern "C" {
  * exact). */
 #define SAGE_FP4_FORMAT_NVFP4 0
 #define SAGE_FP4_FORMAT_MXFP4 1
+/* Direct-P (the rit.work summary of "Hardware-Aware FP4 FlashAttention-4",
+ * "Что сделали"): MXFP4 operands and P as SAGE_FP4_FORMAT_MXFP4, but the
+ * softmax normaliser l is summed from the rounded P (decoded codes times
+ * their scales, the values PV uses) instead of from the unquantized
+ * exponentials.  Quantization treats it as SAGE_FP4_FORMAT_MXFP4;
+ * sage_fp4_attn_fwd_ex takes it with contiguous O only (SAGE_FP4_EINVAL for
+ * other strides). */
+#define SAGE_FP4_FORMAT_MXFP4_DIRECTP 2
 
 typedef struct sage_fp4_tensor {
   uint8_t *codes;  /* packed E2M1, 16-byte aligned */
@@ -169,7 +177,8 @@ int sage_fp4_attn_fwd(const sage_fp4_qkv *qkv, void *o, int B, int H, int N, int
  * the first P-quantization level (the pages give the method no scale; this is
  * the one a drop-in attention takes).  format: the format the operands were
  * quantized in (SAGE_FP4_FORMAT_NVFP4 or SAGE_FP4_FORMAT_MXFP4); P is
- * quantized in the same one. */
+ * quantized in the same one.  SAGE_FP4_FORMAT_MXFP4_DIRECTP: MXFP4 with the
+ * Direct-P normaliser (contiguous O only). */
 int sage_fp4_attn_fwd_ex(const sage_fp4_qkv *qkv, void *o, const sage_fp4_strides *o_strides, int B,
                          int H, int N, int D, int causal, float softmax_scale, int format,
                          void *stream);

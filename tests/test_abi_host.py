@@ -147,7 +147,7 @@ def test_strided_quantize_and_scaled_attention_reject_bad_arguments():
                 S.sage_fp4_strides(N * H * D, 1 << 62, H * D)):  # offsets past 2^62
         assert quant(sq=bad) == S.EINVAL
         assert quant(sv=bad) == S.EINVAL
-    assert quant(fmt=2) == S.EINVAL and quant(fmt=-1) == S.EINVAL
+    assert quant(fmt=3) == S.EINVAL and quant(fmt=-1) == S.EINVAL
     assert S.sage_fp4_quantize_qkv_strided(0x1000, nhd, 0x2000, nhd, 0x3000, nhd, q, 0, H, N, D, None) == S.OK
 
     def attn(scale, so=None, causal=0, fmt=0):
@@ -194,3 +194,12 @@ def test_noalloc_rejects_before_touching_the_device():
     assert f(*good[:4], 0x5002, 1, 2, 512, 128, 0, None) == S.EINVAL
     assert f(*good[:4], 0, 1, 2, 512, 128, 0, None) == S.EINVAL
     assert f(*good, 0, 2, 512, 128, 0, None) == S.OK  # empty: a no-op
+
+
+def test_directp_format_takes_contiguous_o_only():
+    # SAGE_FP4_FORMAT_MXFP4_DIRECTP (2) with O through other strides is
+    # refused before anything touches the device; a format past it is too
+    q = _qkv()
+    nhd = S.sage_fp4_strides(512 * 2 * 128, 128, 2 * 128)  # [B,N,H,D] strides of B1 H2 N512 D128
+    assert S.sage_fp4_attn_fwd_ex(q, 0x1000, nhd, 1, 2, 512, 128, 0, 0.1, None, 2) == S.EINVAL
+    assert S.sage_fp4_attn_fwd_ex(q, 0x1000, None, 1, 2, 512, 128, 0, 0.1, None, 3) == S.EINVAL

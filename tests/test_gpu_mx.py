@@ -177,7 +177,7 @@ def test_nvfp4_beats_mxfp4_at_full_size(name):
     exact = oracle.attention_exact(q, k, v, w.B * w.H, w.N, w.D, w.causal, rows=rows)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     res = {}
-    for fmt in ("nvfp4", "mxfp4"):
+    for fmt in ("nvfp4", "mxfp4", "mxfp4_directp"):
         o = S.attn_fwd(S.quantize_qkv(qd, kd, vd, fmt=fmt), w.causal)
         got = o.float().cpu().numpy().reshape(-1, w.D)[rows]
         res[fmt] = (cosine(got, exact), rel_l1(got, exact))
@@ -196,3 +196,51 @@ def test_mx_strided_layout_matches_contiguous(D, causal):
     got = S.attention(qn, kn, vn, causal, layout="NHD", fmt="mxfp4")
     torch.cuda.synchronize()
     assert torch.equal(got.transpose(1, 2), want)
+
+
+# ------------------------------------------------------------------ Direct-P
+def _dp_attention(q, k, v, causal):
+    z = S.quantize_qkv(q.cuda(), k.cuda(), v.cuda(), fmt="mxfp4_directp")
+    o = S.attn_fwd(z, causal, out=torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    assert z.get_status() == 0
+    return o
+
+
+@pytest.mark.parametrize("B,H,N,D,causal,pattern", [
+    (1, 2, 512, 128, False, "iid"),
+    (1, 2, 300, 128, True, "k_channel_outliers"),
+    (2, 2, 300, 64, False, "k_head_mean"),
+    (1, 1, 17, 64, True, "iid"),
+    (1, 2, 1100, 128, False, "sparse_outliers"),
+])
+def test_directp_attention_matches_oracle(B, H, N, D, causal, pattern):
+    # Direct-P: MXFP4 with l summed from the rounded P, against the oracle's
+    # rounded normaliser (same tolerance and row checks as every attention test)
+    q, k, v = make_qkv(B, H, N, D, pattern, seed=41 + N)
+    got = _dp_attention(q, k, v, causal).float().cpu().numpy().reshape(B * H * N, D)
+    qz = oracle.Quantized(q, k, v, B * H, N, D, fmt="mxfp4")
+    ref = oracle.attention(qz, causal, lnorm="rounded")[0]
+    check_o(got, ref, f"directp B{B} H{H} N{N} D{D} causal={causal} {pattern}")
+
+
+def test_directp_llm_workload_sampled_rows():
+    w = WORKLOADS["llm"]
+    q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.pattern, seed=0)
+    got = _dp_attention(q, k, v, w.causal).float().cpu().numpy().reshape(-1, w.D)
+    rows = sample_rows(w.B * w.H, w.N, per_head=4)
+    qz = oracle.Quantized(q, k, v, w.B * w.H, w.N, w.D, fmt="mxfp4")
+    ref = oracle.attention(qz, w.causal, rows=rows, lnorm="rounded")[0]
+    assert np.isfinite(got).all()
+    check_o(got[rows], ref, "directp llm sampled rows")
+
+
+@pytest.mark.parametrize("D,causal", [(128, False), (64, True)])
+def test_directp_constant_v_is_returned(D, causal):
+    # l and PV sum the same rounded P, so V = 1.5 everywhere gives O = 1.5
+    # up to the FP32 sums' order and the bf16 rounding of O
+    B, H, N = 1, 2, 700
+    q, k, _ = make_qkv(B, H, N, D, "k_channel_outliers", seed=D)
+    v = torch.full((B, H, N, D), 1.5, dtype=torch.bfloat16)
+    o = _dp_attention(q, k, v, causal).float()
+    assert (o - 1.5).abs().max().item() <= 2 ** -8 * 1.5
