@@ -111,6 +111,28 @@ CUtensorMapSwizzle swizzle_for_row(int row_bytes) {
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? SAGE_FP4_OK : SAGE_FP4_ECUDA; }
 
+// bf16 elements addressable through a [B,H,N,D] tensor with strides s: its
+// largest element offset + 1 (the strides were checked not to overflow)
+long long tensor_extent(const Strides& s, int B, int H, int N, int D) {
+  return static_cast<long long>(B - 1) * s.b + static_cast<long long>(H - 1) * s.h +
+         static_cast<long long>(N - 1) * s.n + D;
+}
+
+// The sizes the debug build checks kernel indexes against (x[] and o as given).
+Extents operand_extents(int32_t* status, int B, int H, int N, int D) {
+  const OperandSizes os = operand_sizes(N, D);
+  const long long BH = static_cast<long long>(B) * H;
+  Extents e;
+  e.status = status;
+  e.x[0] = e.x[1] = e.x[2] = 0;
+  e.o = 0;
+  e.codes = BH * static_cast<long long>(os.q_codes);
+  e.scales = BH * static_cast<long long>(os.q_scales);
+  e.vt_codes = BH * static_cast<long long>(os.vt_codes);
+  e.vt_scales = BH * static_cast<long long>(os.vt_scales);
+  return e;
+}
+
 // Strides of one tensor: NULL means the contiguous [B,H,N,D] layout.  Each
 // stride is >= 0 and a multiple of 8 elements (16-byte rows for the vector
 // loads, bulk copies and stores), and the largest element offset fits in 62
@@ -186,11 +208,15 @@ int quantize_impl(const void* q, const sage_fp4_strides* q_strides, const void* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int BH = B * H;
   const bool mx = format != SAGE_FP4_FORMAT_NVFP4;  // Direct-P operands are MXFP4
+  Extents ext = operand_extents(out->status, B, H, N, D);
+  ext.x[0] = tensor_extent(sq, B, H, N, D);
+  ext.x[1] = tensor_extent(sk, B, H, N, D);
+  ext.x[2] = tensor_extent(sv, B, H, N, D);
   cudaError_t e = launch_quant_rows(q, k, sq, sk, out->q.codes, out->q.scales, out->k.codes,
-                                    out->k.scales, H, BH, N, D, mx, st);
+                                    out->k.scales, H, BH, N, D, mx, ext, st);
   if (e != cudaSuccess) return SAGE_FP4_ECUDA;
-  return from_cuda(
-      launch_quant_v(v, sv, out->vt.codes, out->vt.scales, H, BH, N, D, mx, out->status, wait_ns, withhold, st));
+  return from_cuda(launch_quant_v(v, sv, out->vt.codes, out->vt.scales, H, BH, N, D, mx, out->status, wait_ns,
+                                  withhold, ext, st));
 }
 
 }  // namespace
@@ -258,6 +284,10 @@ int attn_fwd_impl(const sage_fp4_qkv* qkv, void* o, const sage_fp4_strides* o_st
   p.mx = format == SAGE_FP4_FORMAT_MXFP4 ? 1 : format == SAGE_FP4_FORMAT_MXFP4_DIRECTP ? 2 : 0;
   p.flags = flags;
   p.wait_ns = wait_ns;
+#if SAGE_FP4_DEBUG_BOUNDS
+  p.ext = operand_extents(qkv->status, B, H, N, D);
+  p.ext.o = tensor_extent(so, B, H, N, D);
+#endif
   return from_cuda(launch_attn(tq, tk, tv, p, D, static_cast<cudaStream_t>(stream)));
 }
 
@@ -311,6 +341,8 @@ const char* sage_fp4_strerror(int status) {
       return "device is not sm_103 (kernels are built for sm_103a)";
     case SAGE_FP4_ETOOLARGE:
       return "problem needs more than the no-allocation entry's fixed 64 MiB scratch";
+    case SAGE_FP4_EBOUNDS:
+      return "debug build: a kernel computed an index outside its buffer (the access was skipped)";
     default:
       return "unknown status";
   }

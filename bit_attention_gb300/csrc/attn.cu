@@ -339,9 +339,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i >= 2 && !wait1(bar(B_QEMPTY + s), ((i >> 1) - 1) & 1, ctl)) return false;
         mbar_arrive_expect_tx(bar(B_QFULL + s), L::QBYTES + L::SFQK);
         tma_load_2d(sb + L::oQ + s * L::QBYTES, &tm_q, 0, it.bh * p.Np + it.qt * kTileQ, bar(B_QFULL + s));
+#if SAGE_FP4_DEBUG_BOUNDS
+        // debug build: a copy that would leave its buffer is skipped; the wait
+        // for it then runs out after the bounds failure was recorded
+        const long long qso = static_cast<long long>(it.bh) * p.Np * (D / 16) + static_cast<long long>(it.qt) * L::SFQK;
+        if (in_bounds(p.ext, qso, L::SFQK, p.ext.scales))
+          bulk_load(sb + L::oSFQ + s * L::SFQK, p.sfq + qso, L::SFQK, bar(B_QFULL + s));
+#else
         bulk_load(sb + L::oSFQ + s * L::SFQK,
                   p.sfq + static_cast<size_t>(it.bh) * p.Np * (D / 16) + static_cast<size_t>(it.qt) * L::SFQK,
                   L::SFQK, bar(B_QFULL + s));
+#endif
         nq = i + 1;
         return true;
       };
@@ -359,8 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (g >= kStages && !(ok = wait1(bar(B_SDONE + s), ((g / kStages) - 1) & 1, ctl))) break;
           mbar_arrive_expect_tx(bar(B_KFULL + s), L::QBYTES + L::SFQK);
           tma_load_2d(sb + L::oK + s * L::QBYTES, &tm_k, 0, I.bh * p.Np + k * kTileKV, bar(B_KFULL + s));
-          bulk_load(sb + L::oSFK + s * L::SFQK, sfk + static_cast<size_t>(k) * L::SFQK, L::SFQK,
-                    bar(B_KFULL + s));
+#if SAGE_FP4_DEBUG_BOUNDS
+          if (in_bounds(p.ext, (sfk - p.sfk) + static_cast<long long>(k) * L::SFQK, L::SFQK, p.ext.scales))
+#endif
+            bulk_load(sb + L::oSFK + s * L::SFQK, sfk + static_cast<size_t>(k) * L::SFQK, L::SFQK,
+                      bar(B_KFULL + s));
           nk = g + 1;
           // the next item's Q goes out once a few of this item's tiles are
           // queued (by then the item before this one has finished its S)
@@ -392,8 +403,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(bar(B_VFULL + s), L::VBYTES + L::SFVB);
           tma_load_2d(sb + L::oV + s * L::VBYTES, &tm_v, k * (kTileKV / 2), I.bh * D, bar(B_VFULL + s));
-          bulk_load(sb + L::oSFV + s * L::SFVB, sfv + static_cast<size_t>(k) * L::SFVB, L::SFVB,
-                    bar(B_VFULL + s));
+#if SAGE_FP4_DEBUG_BOUNDS
+          if (in_bounds(p.ext, (sfv - p.sfv) + static_cast<long long>(k) * L::SFVB, L::SFVB, p.ext.vt_scales))
+#endif
+            bulk_load(sb + L::oSFV + s * L::SFVB, sfv + static_cast<size_t>(k) * L::SFVB, L::SFVB,
+                      bar(B_VFULL + s));
           nv = g + 1;
         }
       }
@@ -798,8 +812,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                   static_cast<size_t>(gi) * static_cast<size_t>(p.os.n);
           }
           uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + row);
+#if SAGE_FP4_DEBUG_BOUNDS
+          if (!in_bounds(p.ext, static_cast<long long>(row), D, p.ext.o)) orow = nullptr;
+#pragma unroll
+          for (int c = 0; c < D / 8 && orow; ++c) {
+#else
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) {
+#endif
             uint32_t w4[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {

@@ -6,7 +6,38 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#ifndef SAGE_FP4_DEBUG_BOUNDS
+#define SAGE_FP4_DEBUG_BOUNDS 0
+#endif
+
 namespace sagefp4 {
+
+// The sizes every computed global-memory index is checked against in the
+// debug build (SAGE_FP4_DEBUG_BOUNDS=1); the release build ignores them.
+struct Extents {
+  int32_t* status;        // where a failed check is recorded (SAGE_FP4_EBOUNDS)
+  long long x[3];         // bf16 elements addressable through q, k, v (largest offset + 1)
+  long long o;            // bf16 elements addressable through o
+  long long codes, scales;          // bytes of one Q or K code / scale buffer
+  long long vt_codes, vt_scales;    // bytes of the V^T code / scale buffer
+};
+
+// True if [off, off + len) lies in [0, extent).  Debug build: otherwise the
+// first failure is recorded in *e.status and the caller skips the access.
+// Release build: always true, so the check and its arithmetic compile away.
+__device__ __forceinline__ bool in_bounds(const Extents& e, long long off, long long len, long long extent) {
+#if SAGE_FP4_DEBUG_BOUNDS
+  if (off >= 0 && off + len <= extent) return true;
+  atomicCAS(e.status, 0, -6);  // SAGE_FP4_EBOUNDS
+  return false;
+#else
+  (void)e;
+  (void)off;
+  (void)len;
+  (void)extent;
+  return true;
+#endif
+}
 
 // Element strides of a bf16 [B,H,N,D] tensor between batches, heads and
 // tokens; D is contiguous.  All three are multiples of 8 (16 bytes).
@@ -22,12 +53,12 @@ inline Strides contiguous_bhnd(int H, int N, int D) {
 // mx: MXFP4 (groups of 32, E8M0 scales) instead of NVFP4.
 cudaError_t launch_quant_rows(const void* q, const void* k, Strides sq, Strides sk, uint8_t* qc,
                               uint8_t* qs, uint8_t* kc, uint8_t* ks, int H, int BH, int N, int D,
-                              bool mx, cudaStream_t st);
+                              bool mx, const Extents& ext, cudaStream_t st);
 // wait_ns bounds every wait for a tile; withhold: failure-detection test (block
 // 0 never issues its first tile).
 cudaError_t launch_quant_v(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, int H, int BH, int N,
                            int D, bool mx, int32_t* status, uint64_t wait_ns, int withhold,
-                           cudaStream_t st);
+                           const Extents& ext, cudaStream_t st);
 
 struct AttnParams {
   const uint8_t* sfq;  // Q scales (block layout), per (b,h) N_pad*D/16 bytes
@@ -42,6 +73,9 @@ struct AttnParams {
             // 2: the same with the row sum from the rounded P (Direct-P; dense O only)
   int flags;           // kAttnWithholdK: failure-detection test (see below)
   uint64_t wait_ns;    // limit of every bounded wait in the kernel
+#if SAGE_FP4_DEBUG_BOUNDS
+  Extents ext;         // sizes the scale copies and O stores are checked against
+#endif
 };
 
 // Failure-detection test: the K producer issues the first KV tile of its

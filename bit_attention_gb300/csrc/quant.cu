@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
                                                          uint8_t* __restrict__ s0,
                                                          uint8_t* __restrict__ c1,
                                                          uint8_t* __restrict__ s1, int H, int BH,
-                                                         int N, int Np) {
+                                                         int N, int Np, const Extents ext) {
   constexpr int LPR = D / 8;      // lanes per row
   constexpr int RPW = 32 / LPR;   // rows per warp step
   constexpr int U = 8;            // row-steps per chunk
@@ -119,16 +119,20 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
     const int r0 = (chunk - bh * chunks_per_head) * CHUNK;
     const int n0 = r0 + rsub;
     const int b = bh / H, h = bh - b * H;
-    const uint4* __restrict__ src =
-        x + static_cast<size_t>((b * t.b + h * t.h + static_cast<long long>(n0) * t.n) / 8) + sub;
+    const long long off0 = b * t.b + h * t.h + static_cast<long long>(n0) * t.n + sub * 8;  // elements
+    const uint4* __restrict__ src = x + static_cast<size_t>(off0 / 8);
+    const long long xext = ext.x[blockIdx.y];
     uint4 raw[U];
     if (r0 + CHUNK <= N) {
 #pragma unroll
-      for (int u = 0; u < U; ++u) raw[u] = __ldcs(src + u * step);
+      for (int u = 0; u < U; ++u)
+        raw[u] = in_bounds(ext, off0 + u * RPW * t.n, 8, xext) ? __ldcs(src + u * step)
+                                                               : make_uint4(0u, 0u, 0u, 0u);
     } else {
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        raw[u] = (n0 + u * RPW < N) ? __ldcs(src + u * step) : make_uint4(0u, 0u, 0u, 0u);
+        raw[u] = (n0 + u * RPW < N && in_bounds(ext, off0 + u * RPW * t.n, 8, xext)) ? __ldcs(src + u * step)
+                                                                                     : make_uint4(0u, 0u, 0u, 0u);
     }
     uint8_t* __restrict__ cdst = codes + (static_cast<size_t>(bh) * Np + n0) * (D / 2) + sub * 4;
     uint8_t* __restrict__ sdst =
@@ -155,8 +159,10 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint4* __restrict
         sw = pack4_bytes(sb, __shfl_down_sync(kFull, sb, 2), __shfl_down_sync(kFull, sb, 4),
                          __shfl_down_sync(kFull, sb, 6));
       }
-      *reinterpret_cast<uint32_t*>(cdst + u * RPW * (D / 2)) = word;
-      if ((sub & 7) == 0) *reinterpret_cast<uint32_t*>(sdst + u * RPW * 16) = sw;
+      if (in_bounds(ext, (cdst + u * RPW * (D / 2)) - codes, 4, ext.codes))
+        *reinterpret_cast<uint32_t*>(cdst + u * RPW * (D / 2)) = word;
+      if ((sub & 7) == 0 && in_bounds(ext, (sdst + u * RPW * 16) - scales, 4, ext.scales))
+        *reinterpret_cast<uint32_t*>(sdst + u * RPW * 16) = sw;
     }
   }
 }
@@ -182,7 +188,7 @@ __global__ void __launch_bounds__(128) quant_v_kernel(const uint8_t* __restrict_
                                                       uint8_t* __restrict__ vc,
                                                       uint8_t* __restrict__ vs, int H, int BH,
                                                       int N, int Np, int32_t* status, uint64_t wait_ns,
-                                                      int withhold) {
+                                                      int withhold, const Extents ext) {
   static_assert(TT == 64 || TT == 128, "tile of 64 or 128 tokens");
   static_assert(!MX || TT == 64, "MX scale words follow 64-token tiles");
   constexpr int TILE_BYTES = TT * D * 2;
@@ -214,16 +220,20 @@ __global__ void __launch_bounds__(128) quant_v_kernel(const uint8_t* __restrict_
     const int bh = static_cast<int>(w / ntiles), tb = static_cast<int>(w % ntiles);
     const int b = bh / H, h = bh - b * H;
     const int rows = tile_rows(w);
-    const uint8_t* src =
-        v + (b * sv.b + h * sv.h + static_cast<long long>(tb) * TT * sv.n) * 2;
+    const long long off = b * sv.b + h * sv.h + static_cast<long long>(tb) * TT * sv.n;  // elements
+    const uint8_t* src = v + off * 2;
     const uint32_t dst = smem_addr(qv_smem + buf * TILE_BYTES);
     if (lane == 0) mbar_arrive_expect_tx(bar0 + 8 * buf, static_cast<uint32_t>(rows) * D * 2);
     __syncwarp();
+    // (debug build: a copy that would leave V is skipped; its tile's wait then
+    // runs out, after the bounds failure has been recorded)
     if (sv.n == D) {
-      if (lane == 0 && rows > 0) bulk_load(dst, src, static_cast<uint32_t>(rows) * D * 2, bar0 + 8 * buf);
+      if (lane == 0 && rows > 0 && in_bounds(ext, off, static_cast<long long>(rows) * D, ext.x[2]))
+        bulk_load(dst, src, static_cast<uint32_t>(rows) * D * 2, bar0 + 8 * buf);
     } else {
       for (int r = lane; r < rows; r += 32)
-        bulk_load(dst + r * D * 2, src + static_cast<long long>(r) * sv.n * 2, D * 2, bar0 + 8 * buf);
+        if (in_bounds(ext, off + static_cast<long long>(r) * sv.n, D, ext.x[2]))
+          bulk_load(dst + r * D * 2, src + static_cast<long long>(r) * sv.n * 2, D * 2, bar0 + 8 * buf);
     }
   };
   if (threadIdx.x < 32)
@@ -299,15 +309,22 @@ __global__ void __launch_bounds__(128) quant_v_kernel(const uint8_t* __restrict_
         }
         const int d0 = 2 * pch, d1 = 2 * pch + 1;
         const size_t col = static_cast<size_t>(tb) * (TT / 2) + seg * 16;
-        *reinterpret_cast<uint4*>(vc + (static_cast<size_t>(bh) * D + d0) * vt_row + col) =
-            make_uint4(clo[0], clo[1], clo[2], clo[3]);
-        *reinterpret_cast<uint4*>(vc + (static_cast<size_t>(bh) * D + d1) * vt_row + col) =
-            make_uint4(chi[0], chi[1], chi[2], chi[3]);
-        vs_bh[sf_offset(d0, tb * 4 + seg, Np / 16)] = static_cast<uint8_t>(elo);
-        vs_bh[sf_offset(d1, tb * 4 + seg, Np / 16)] = static_cast<uint8_t>(ehi);
+        const long long c0 = (static_cast<long long>(bh) * D + d0) * vt_row + col;
+        const long long c1 = (static_cast<long long>(bh) * D + d1) * vt_row + col;
+        const long long sbase = static_cast<long long>(bh) * 8 * Np;
+        if (in_bounds(ext, c0, 16, ext.vt_codes))
+          *reinterpret_cast<uint4*>(vc + c0) = make_uint4(clo[0], clo[1], clo[2], clo[3]);
+        if (in_bounds(ext, c1, 16, ext.vt_codes))
+          *reinterpret_cast<uint4*>(vc + c1) = make_uint4(chi[0], chi[1], chi[2], chi[3]);
+        if (in_bounds(ext, sbase + sf_offset(d0, tb * 4 + seg, Np / 16), 1, ext.vt_scales))
+          vs_bh[sf_offset(d0, tb * 4 + seg, Np / 16)] = static_cast<uint8_t>(elo);
+        if (in_bounds(ext, sbase + sf_offset(d1, tb * 4 + seg, Np / 16), 1, ext.vt_scales))
+          vs_bh[sf_offset(d1, tb * 4 + seg, Np / 16)] = static_cast<uint8_t>(ehi);
         if (seg == 0) {
-          *reinterpret_cast<uint16_t*>(vs_bh + sf_offset(d0, tb * 4 + 2, Np / 16)) = 0;
-          *reinterpret_cast<uint16_t*>(vs_bh + sf_offset(d1, tb * 4 + 2, Np / 16)) = 0;
+          if (in_bounds(ext, sbase + sf_offset(d0, tb * 4 + 2, Np / 16), 2, ext.vt_scales))
+            *reinterpret_cast<uint16_t*>(vs_bh + sf_offset(d0, tb * 4 + 2, Np / 16)) = 0;
+          if (in_bounds(ext, sbase + sf_offset(d1, tb * 4 + 2, Np / 16), 2, ext.vt_scales))
+            *reinterpret_cast<uint16_t*>(vs_bh + sf_offset(d1, tb * 4 + 2, Np / 16)) = 0;
         }
         continue;
       }
@@ -342,20 +359,27 @@ __global__ void __launch_bounds__(128) quant_v_kernel(const uint8_t* __restrict_
       }
       const int d0 = 2 * pch, d1 = 2 * pch + 1;
       const size_t col = static_cast<size_t>(tb) * (TT / 2) + seg * 16;
-      *reinterpret_cast<uint4*>(vc + (static_cast<size_t>(bh) * D + d0) * vt_row + col) =
-          make_uint4(clo[0], clo[1], clo[2], clo[3]);
-      *reinterpret_cast<uint4*>(vc + (static_cast<size_t>(bh) * D + d1) * vt_row + col) =
-          make_uint4(chi[0], chi[1], chi[2], chi[3]);
+      const long long c0 = (static_cast<long long>(bh) * D + d0) * vt_row + col;
+      const long long c1 = (static_cast<long long>(bh) * D + d1) * vt_row + col;
+      const long long sbase = static_cast<long long>(bh) * 8 * Np;
+      if (in_bounds(ext, c0, 16, ext.vt_codes))
+        *reinterpret_cast<uint4*>(vc + c0) = make_uint4(clo[0], clo[1], clo[2], clo[3]);
+      if (in_bounds(ext, c1, 16, ext.vt_codes))
+        *reinterpret_cast<uint4*>(vc + c1) = make_uint4(chi[0], chi[1], chi[2], chi[3]);
       const int g0 = tb * (TT / 16) + seg * 2;  // even: the two groups share a 16-bit half
-      *reinterpret_cast<uint16_t*>(vs_bh + sf_offset(d0, g0, Np / 16)) =
-          static_cast<uint16_t>(sbl[0] | (sbl[1] << 8));
-      *reinterpret_cast<uint16_t*>(vs_bh + sf_offset(d1, g0, Np / 16)) =
-          static_cast<uint16_t>(sbh[0] | (sbh[1] << 8));
+      if (in_bounds(ext, sbase + sf_offset(d0, g0, Np / 16), 2, ext.vt_scales))
+        *reinterpret_cast<uint16_t*>(vs_bh + sf_offset(d0, g0, Np / 16)) =
+            static_cast<uint16_t>(sbl[0] | (sbl[1] << 8));
+      if (in_bounds(ext, sbase + sf_offset(d1, g0, Np / 16), 2, ext.vt_scales))
+        *reinterpret_cast<uint16_t*>(vs_bh + sf_offset(d1, g0, Np / 16)) =
+            static_cast<uint16_t>(sbh[0] | (sbh[1] << 8));
     }
     // scale rows of the padding channels D..127 of the 128-row block are zero
     for (int i = threadIdx.x; i < (128 - D) * (TT / 64); i += 128) {
       const int d = D + i / (TT / 64), h = i % (TT / 64);
-      *reinterpret_cast<uint32_t*>(vs_bh + sf_offset(d, tb * (TT / 16) + h * 4, Np / 16)) = 0u;
+      if (in_bounds(ext, static_cast<long long>(bh) * 8 * Np + sf_offset(d, tb * (TT / 16) + h * 4, Np / 16), 4,
+                    ext.vt_scales))
+        *reinterpret_cast<uint32_t*>(vs_bh + sf_offset(d, tb * (TT / 16) + h * 4, Np / 16)) = 0u;
     }
     // this slot is refilled by a bulk copy (async proxy) after the barrier
     fence_proxy_async_smem();
@@ -377,7 +401,7 @@ int num_sms() {
 
 cudaError_t launch_quant_rows(const void* q, const void* k, Strides sq, Strides sk, uint8_t* qc,
                               uint8_t* qs, uint8_t* kc, uint8_t* ks, int H, int BH, int N, int D,
-                              bool mx, cudaStream_t st) {
+                              bool mx, const Extents& ext, cudaStream_t st) {
   const int Np = round_up_int(N, 128);
   const long long chunks = static_cast<long long>(BH) * Np / (D == 128 ? 16 : 32);  // one warp each
   long long blocks = (chunks + 7) / 8;
@@ -389,14 +413,14 @@ cudaError_t launch_quant_rows(const void* q, const void* k, Strides sq, Strides 
   const uint4* x1 = static_cast<const uint4*>(k);
   if (D == 128) {
     if (mx)
-      quant_rows_kernel<128, true><<<grid, 256, 0, st>>>(x0, x1, sq, sk, qc, qs, kc, ks, H, BH, N, Np);
+      quant_rows_kernel<128, true><<<grid, 256, 0, st>>>(x0, x1, sq, sk, qc, qs, kc, ks, H, BH, N, Np, ext);
     else
-      quant_rows_kernel<128, false><<<grid, 256, 0, st>>>(x0, x1, sq, sk, qc, qs, kc, ks, H, BH, N, Np);
+      quant_rows_kernel<128, false><<<grid, 256, 0, st>>>(x0, x1, sq, sk, qc, qs, kc, ks, H, BH, N, Np, ext);
   } else {
     if (mx)
-      quant_rows_kernel<64, true><<<grid, 256, 0, st>>>(x0, x1, sq, sk, qc, qs, kc, ks, H, BH, N, Np);
+      quant_rows_kernel<64, true><<<grid, 256, 0, st>>>(x0, x1, sq, sk, qc, qs, kc, ks, H, BH, N, Np, ext);
     else
-      quant_rows_kernel<64, false><<<grid, 256, 0, st>>>(x0, x1, sq, sk, qc, qs, kc, ks, H, BH, N, Np);
+      quant_rows_kernel<64, false><<<grid, 256, 0, st>>>(x0, x1, sq, sk, qc, qs, kc, ks, H, BH, N, Np, ext);
   }
   return cudaGetLastError();
 }
@@ -404,7 +428,7 @@ cudaError_t launch_quant_rows(const void* q, const void* k, Strides sq, Strides 
 template <int D, int TT, int NS, bool MX>
 cudaError_t launch_quant_v_cfg(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, int H, int BH,
                                int Np, int N, int32_t* status, int blocks_per_sm, uint64_t wait_ns,
-                               int withhold, cudaStream_t st) {
+                               int withhold, const Extents& ext, cudaStream_t st) {
   const long long work = static_cast<long long>(Np / TT) * BH;
   const int smem = NS * TT * D * 2;
   long long blocks = static_cast<long long>(num_sms()) * blocks_per_sm;
@@ -428,11 +452,12 @@ cudaError_t launch_quant_v_cfg(const void* v, Strides sv, uint8_t* vc, uint8_t* 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, quant_v_kernel<D, TT, NS, MX>, static_cast<const uint8_t*>(v), sv, vc, vs,
-                            H, BH, N, Np, status, wait_ns, withhold);
+                            H, BH, N, Np, status, wait_ns, withhold, ext);
 }
 
 cudaError_t launch_quant_v(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, int H, int BH, int N,
-                           int D, bool mx, int32_t* status, uint64_t wait_ns, int withhold, cudaStream_t st) {
+                           int D, bool mx, int32_t* status, uint64_t wait_ns, int withhold,
+                           const Extents& ext, cudaStream_t st) {
   const int Np = round_up_int(N, 128);
   // 64-token tiles, double-buffered: 32 KB (D = 128) or 16 KB (D = 64) of
   // shared memory per block.  The per-tile arithmetic, not the copy latency,
@@ -440,10 +465,10 @@ cudaError_t launch_quant_v(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, 
   // GB300: 5.3-5.8 TB/s at D = 128 with six blocks per SM, against 4.0-4.9 TB/s
   // with four-deep rings and two or three blocks).
   if (D == 128)
-    return mx ? launch_quant_v_cfg<128, 64, 2, true>(v, sv, vc, vs, H, BH, Np, N, status, 6, wait_ns, withhold, st)
-              : launch_quant_v_cfg<128, 64, 2, false>(v, sv, vc, vs, H, BH, Np, N, status, 6, wait_ns, withhold, st);
-  return mx ? launch_quant_v_cfg<64, 64, 2, true>(v, sv, vc, vs, H, BH, Np, N, status, 8, wait_ns, withhold, st)
-            : launch_quant_v_cfg<64, 64, 2, false>(v, sv, vc, vs, H, BH, Np, N, status, 8, wait_ns, withhold, st);
+    return mx ? launch_quant_v_cfg<128, 64, 2, true>(v, sv, vc, vs, H, BH, Np, N, status, 6, wait_ns, withhold, ext, st)
+              : launch_quant_v_cfg<128, 64, 2, false>(v, sv, vc, vs, H, BH, Np, N, status, 6, wait_ns, withhold, ext, st);
+  return mx ? launch_quant_v_cfg<64, 64, 2, true>(v, sv, vc, vs, H, BH, Np, N, status, 8, wait_ns, withhold, ext, st)
+            : launch_quant_v_cfg<64, 64, 2, false>(v, sv, vc, vs, H, BH, Np, N, status, 8, wait_ns, withhold, ext, st);
 }
 
 }  // namespace sagefp4

@@ -11,6 +11,7 @@ conveniences built on them.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import re
@@ -18,14 +19,15 @@ import threading
 
 from . import build as _build
 
-OK, EINVAL, ECUDA, ETIMEOUT, EUNSUPPORTED, ETOOLARGE = 0, -1, -2, -3, -4, -5
+OK, EINVAL, ECUDA, ETIMEOUT, EUNSUPPORTED, ETOOLARGE, EBOUNDS = 0, -1, -2, -3, -4, -5, -6
 # SAGE_FP4_FORMAT_*; "mxfp4_directp": MXFP4 with the softmax normaliser summed
 # from the rounded P (Direct-P); its operands are MXFP4
 FORMATS = {"nvfp4": 0, "mxfp4": 1, "mxfp4_directp": 2}
 
 _HEADER = os.path.join(_build.ROOT, "include", "sage_fp4.h")
 _lock = threading.Lock()
-_lib = None
+_libs = {}             # loaded libraries: False = release, True = bounds-checking debug build
+_use_debug = False     # which one the calls below go to (debug_bounds_library())
 
 
 class SageFp4Error(RuntimeError):
@@ -53,12 +55,16 @@ def header_functions() -> list:
     return sorted(set(re.findall(r"^[a-z_ 0-9\*]+?\b(sage_fp4_[a-z_0-9]+)\s*\(", text, re.M)))
 
 
-def load(build: bool = True) -> ctypes.CDLL:
-    """Load the library, building it first when it is missing or stale."""
-    global _lib
+def load(build: bool = True, debug_bounds: bool | None = None) -> ctypes.CDLL:
+    """Load the library, building it first when it is missing or stale.
+
+    debug_bounds: the build whose kernels check every computed index against
+    its buffer (SAGE_FP4_EBOUNDS); None = the one debug_bounds_library()
+    selects (the release library outside it)."""
+    dbg = _use_debug if debug_bounds is None else bool(debug_bounds)
     with _lock:
-        if _lib is None:
-            path = _build.build() if build else _build.LIB
+        if dbg not in _libs:
+            path = _build.build(debug_bounds=dbg) if build else (_build.LIB_DEBUG if dbg else _build.LIB)
             if not os.path.exists(path):
                 raise RuntimeError(f"CUDA library not built: {path}")
             L = ctypes.CDLL(path)
@@ -89,8 +95,21 @@ def load(build: bool = True) -> ctypes.CDLL:
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
                 fn.restype, fn.argtypes = res, args
-            _lib = L
-    return _lib
+            _libs[dbg] = L
+    return _libs[dbg]
+
+
+@contextlib.contextmanager
+def debug_bounds_library():
+    """Route every call of this module to the bounds-checking debug build of
+    the library while the block runs (for tests; not thread-safe)."""
+    global _use_debug
+    prev = _use_debug
+    _use_debug = True
+    try:
+        yield load()
+    finally:
+        _use_debug = prev
 
 
 def strerror(code: int) -> str:

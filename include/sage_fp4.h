@@ -77,7 +77,10 @@ extern "C" {
 #define SAGE_FP4_ECUDA (-2)       /* CUDA runtime/driver error at launch or copy */
 #define SAGE_FP4_ETIMEOUT (-3)    /* a kernel's bounded wait gave up (see sage_fp4_get_status) */
 #define SAGE_FP4_EUNSUPPORTED (-4) /* device is not sm_103 (the kernels are built for sm_103a) */
-#define SAGE_FP4_ETOOLARGE (-5)   /* problem needs more than the no-allocation entry's fixed scratch */
+#define SAGE_FP4_ETOOLARGE (-5)
+/* debug build only (SAGE_FP4_DEBUG_BOUNDS=1, libsagefp4_debug.so): a kernel
+ * computed a global-memory index outside its buffer; the access was skipped */
+#define SAGE_FP4_EBOUNDS (-6)   /* problem needs more than the no-allocation entry's fixed scratch */
 
 /* Microscaling formats of the quantized operands.  NVFP4 is the method's:
  * E2M1 codes with one E4M3 scale per 16 elements.  MXFP4 is the alternative

@@ -203,3 +203,12 @@ def test_directp_format_takes_contiguous_o_only():
     nhd = S.sage_fp4_strides(512 * 2 * 128, 128, 2 * 128)  # [B,N,H,D] strides of B1 H2 N512 D128
     assert S.sage_fp4_attn_fwd_ex(q, 0x1000, nhd, 1, 2, 512, 128, 0, 0.1, None, 2) == S.EINVAL
     assert S.sage_fp4_attn_fwd_ex(q, 0x1000, None, 1, 2, 512, 128, 0, 0.1, None, 3) == S.EINVAL
+
+
+def test_debug_build_loads_and_exports_every_header_function():
+    # the bounds-checking build of the same sources (SAGE_FP4_DEBUG_BOUNDS=1)
+    lib = S.load(debug_bounds=True)
+    for n in S.header_functions():
+        assert hasattr(lib, n), n
+    assert lib is not S.load()
+    assert "debug build" in S.load(debug_bounds=True).sage_fp4_strerror(S.EBOUNDS).decode()
