@@ -26,6 +26,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _SRC = os.path.join(_HERE, "sage_oracle.c")
+_SRC_BWD = os.path.join(_HERE, "sagebwd_oracle.c")  # SageBwd, the 8-bit attention for training
 _lock = threading.Lock()
 _lib = None
 
@@ -38,12 +39,14 @@ LNORM = {"exp": 0, "rounded": 1}
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (no fast-math, no FP contraction)."""
     os.makedirs(_BUILD, exist_ok=True)
+    srcs = [_SRC, _SRC_BWD]
+    deps = srcs + [s[:-2] + ".h" for s in srcs]
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(f) for f in deps)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
-           "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+           "-fPIC", "-shared", *srcs, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -122,6 +125,19 @@ def _declare(L):
     L.sor_attention.argtypes = [u8p, u8p, u8p, u8p, u8p, u8p, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
                                 ctypes.c_int, ctypes.c_int, i64p, ctypes.c_int64, f64p, f64p, f64p]
+    # SageBwd (absent from the one-file builds the mutation tests make)
+    if hasattr(L, "sbo_attention_train"):
+        L.sbo_int8_code.restype = ctypes.c_int
+        L.sbo_int8_code.argtypes = [ctypes.c_float, ctypes.c_float]
+        L.sbo_int8_scale.restype = ctypes.c_float
+        L.sbo_int8_scale.argtypes = [ctypes.c_float]
+        L.sbo_quantize_blocks.restype = None
+        L.sbo_quantize_blocks.argtypes = [u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_int8), f32p]
+        L.sbo_attention_train.restype = ctypes.c_int
+        L.sbo_attention_train.argtypes = [u16p, u16p, u16p, u16p, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                                          f64p, f64p, f64p, f64p, f64p]
     L.sor_attention_exact.restype = ctypes.c_int
     L.sor_attention_exact.argtypes = [u16p, u16p, u16p, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_double, i64p,
@@ -301,3 +317,43 @@ def decode_rows(codes: np.ndarray, scales: np.ndarray, fmt: str = "nvfp4") -> np
     vals = e2[el]
     sc = np.repeat(sv[scales], GROUP[fmt], axis=-1)
     return vals * sc
+
+
+# ------------------------------------------------------------------ SageBwd
+SAGEBWD_BLOCK = 128  # token block of the INT8 operands Q, K, V, dO; key edge of a P / dS block
+SAGEBWD_QBLOCK = 64  # query edge of a P / dS block
+
+
+def int8_code(x: float, amax: float) -> int:
+    return lib().sbo_int8_code(x, amax)
+
+
+def int8_scale(amax: float) -> float:
+    return lib().sbo_int8_scale(amax)
+
+
+def sagebwd_quantize(x, BH: int, N: int, D: int):
+    """bf16 [.., N, D] -> (INT8 codes [BH, N, D], float scales [BH, ceil(N/128)])."""
+    xb = _u16(x)
+    nb = (N + SAGEBWD_BLOCK - 1) // SAGEBWD_BLOCK
+    codes = np.empty((BH, N, D), np.int8)
+    scales = np.empty((BH, nb), np.float32)
+    lib().sbo_quantize_blocks(_p(xb, ctypes.c_uint16), BH, N, D, _p(codes, ctypes.c_int8),
+                              _p(scales, ctypes.c_float))
+    return codes, scales
+
+
+def sagebwd(q, k, v, dout, BH: int, N: int, D: int, causal: bool, scale: float | None = None,
+            quant: bool = True):
+    """SageBwd forward and backward. Returns (o, lse, dq, dk, dv), float64,
+    [BH, N, D] (lse [BH, N]).  quant=False: exact attention and its gradient."""
+    scale = default_scale(D) if scale is None else float(scale)
+    bufs = [_u16(t) for t in (q, k, v, dout)]
+    o = np.empty((BH, N, D), np.float64)
+    lse = np.empty((BH, N), np.float64)
+    dq, dk, dv = (np.empty((BH, N, D), np.float64) for _ in range(3))
+    rc = lib().sbo_attention_train(*(_p(b, ctypes.c_uint16) for b in bufs), BH, N, D, int(bool(causal)),
+                                   scale, int(bool(quant)), *(_p(a, ctypes.c_double) for a in (o, lse, dq, dk, dv)))
+    if rc != 0:
+        raise ValueError(f"SageBwd oracle failed ({rc})")
+    return o, lse, dq, dk, dv

@@ -9,6 +9,7 @@
 #include <string.h>
 
 #include "sage_oracle.h"
+#include "sagebwd_oracle.h"
 
 static unsigned long long rng_state = 0x9E3779B97F4A7C15ull;
 
@@ -102,6 +103,38 @@ static int run_shape(int BH, int N, int D, int fmt) {
   return 0;
 }
 
+/* SageBwd forward and backward, both modes, causal and not */
+static int run_train(int BH, int N, int D) {
+  const size_t elems = (size_t)BH * N * D;
+  unsigned short *x[4];
+  for (int t = 0; t < 4; t++) {
+    x[t] = malloc(elems * 2);
+    for (size_t i = 0; i < elems; i++) x[t][i] = bf16_rand(3);
+  }
+  double *out[5];
+  for (int t = 0; t < 5; t++) out[t] = malloc(sizeof(double) * (t == 1 ? (size_t)BH * N : elems));
+  int8_t *codes = malloc(elems);
+  float *scales = malloc(sizeof(float) * BH * ((N + 127) / 128));
+  sbo_quantize_blocks(x[0], BH, N, D, codes, scales);
+  for (int quant = 0; quant < 2; quant++)
+    for (int causal = 0; causal < 2; causal++) {
+      if (sbo_attention_train(x[0], x[1], x[2], x[3], BH, N, D, causal, 0.125, quant, out[0], out[1], out[2],
+                              out[3], out[4]))
+        return fail("SageBwd oracle rejected valid arguments");
+      for (int t = 0; t < 5; t++)
+        for (size_t i = 0; i < (t == 1 ? (size_t)BH * N : elems); i++)
+          if (!isfinite(out[t][i])) return fail("non-finite SageBwd output");
+    }
+  if (sbo_attention_train(x[0], x[1], x[2], x[3], BH, 0, D, 0, 0.125, 1, out[0], out[1], out[2], out[3],
+                          out[4]) != -1)
+    return fail("SageBwd oracle accepted N = 0");
+  for (int t = 0; t < 4; t++) free(x[t]);
+  for (int t = 0; t < 5; t++) free(out[t]);
+  free(codes);
+  free(scales);
+  return 0;
+}
+
 int main(void) {
   /* codecs over a range of float32 patterns, and every E4M3 / E8M0 byte */
   enum { R = 1 << 16 };
@@ -128,6 +161,9 @@ int main(void) {
   for (unsigned s = 0; s < sizeof shapes / sizeof shapes[0]; s++)
     for (int fmt = 0; fmt < 2; fmt++)
       if (run_shape(shapes[s][0], shapes[s][1], shapes[s][2], fmt)) return 1;
+  const int train_shapes[][3] = {{1, 1, 64}, {2, 65, 64}, {1, 200, 128}};
+  for (unsigned s = 0; s < sizeof train_shapes / sizeof train_shapes[0]; s++)
+    if (run_train(train_shapes[s][0], train_shapes[s][1], train_shapes[s][2])) return 1;
   printf("oracle driver: ok\n");
   return 0;
 }

@@ -36,7 +36,8 @@ def _run(cmd, **kw):
 def test_oracle_under_sanitizers(tmp_path):
     exe = tmp_path / "oracle_driver"
     _run(["gcc", "-O1", "-std=c11", "-fopenmp", "-ffp-contract=off", *SAN, "-I", os.path.join(ROOT, "oracle"),
-          os.path.join(ROOT, "oracle", "sage_oracle.c"), os.path.join(ROOT, "tests", "sanitize", "oracle_driver.c"),
+          os.path.join(ROOT, "oracle", "sage_oracle.c"), os.path.join(ROOT, "oracle", "sagebwd_oracle.c"),
+          os.path.join(ROOT, "tests", "sanitize", "oracle_driver.c"),
           "-o", str(exe), "-lm"])
     r = _run([str(exe)], env=ENV, timeout=600)
     assert "oracle driver: ok" in r.stdout
