@@ -165,142 +165,174 @@ static void quant_block(const double *m, int N, int i0, int i1, int j0, int j1, 
 
 /* The whole [N][N] matrix, block by block (64 queries x 128 keys). */
 static void quant_blocks_nn(const double *m, int N, int quant, double *out) {
+#pragma omp parallel for schedule(static)
   for (int i0 = 0; i0 < N; i0 += QBLK)
     for (int j0 = 0; j0 < N; j0 += TOK)
       quant_block(m, N, i0, (i0 + QBLK < N) ? i0 + QBLK : N, j0, (j0 + TOK < N) ? j0 + TOK : N, quant, out);
 }
 
+/* dst[j][d] = sum over i (ascending) of M[i][j] * X[i][d], for the [N][N]
+ * matrix M and [N][D] X: the transposed products dV and dK.  Threads take
+ * disjoint ranges of j; each sum keeps its order. */
+static void mt_times(const double *M, const double *X, int N, int D, double *dst) {
+#pragma omp parallel for schedule(static)
+  for (int jb = 0; jb < N; jb += 32) {
+    const int je = (jb + 32 < N) ? jb + 32 : N;
+    for (int j = jb; j < je; j++)
+      for (int d = 0; d < D; d++) dst[(size_t)j * D + d] = 0.0;
+    for (int i = 0; i < N; i++)
+      for (int j = jb; j < je; j++)
+        for (int d = 0; d < D; d++) dst[(size_t)j * D + d] += M[(size_t)i * N + j] * X[(size_t)i * D + d];
+  }
+}
+
+/* One head.  The heads run one after another; the loops inside run their
+ * independent rows (or row blocks) in parallel, every sum in a fixed order. */
+static int train_head(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout, int N, int D,
+                      int causal, double scale, int quant, double *O, double *lse, double *dq, double *dk,
+                      double *dv) {
+  double *Qd = malloc(sizeof(double) * N * D), *Kd = malloc(sizeof(double) * N * D);
+  double *Vd = malloc(sizeof(double) * N * D), *dOd = malloc(sizeof(double) * N * D);
+  double *S = malloc(sizeof(double) * N * N), *P = malloc(sizeof(double) * N * N);
+  double *Pq = malloc(sizeof(double) * N * N), *L = malloc(sizeof(double) * N);
+  double *Dr = malloc(sizeof(double) * N), *m = malloc(sizeof(double) * N);
+  double *l = malloc(sizeof(double) * N);
+  double *dOh = malloc(sizeof(double) * N * D), *Vh = malloc(sizeof(double) * N * D);
+  int rc = 0;
+  if (!Qd || !Kd || !Vd || !dOd || !S || !P || !Pq || !L || !Dr || !m || !l || !dOh || !Vh) {
+    rc = -2;
+    goto out;
+  }
+  dequant_head(q, N, D, quant, Qd);
+  dequant_head(k, N, D, quant, Kd);
+  dequant_head(v, N, D, quant, Vd);
+  dequant_head(dout, N, D, quant, dOd);
+  /* scale * S = scale * Q^ K^^T (an INT8 product; exact here), masked -inf */
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < N; i++)
+    for (int j = 0; j < N; j++) {
+      double s = 0.0;
+      for (int d = 0; d < D; d++) s += Qd[(size_t)i * D + d] * Kd[(size_t)j * D + d];
+      S[(size_t)i * N + j] = (causal && j > i) ? -INFINITY : scale * s;
+    }
+  /* forward: online softmax over key tiles; P~ of each tile into P */
+  for (size_t x = 0; x < (size_t)N * D; x++) O[x] = 0.0;
+  for (int i = 0; i < N; i++) {
+    m[i] = -INFINITY;
+    l[i] = 0.0;
+  }
+  for (int j0 = 0; j0 < N; j0 += TOK) {
+    const int j1 = (j0 + TOK < N) ? j0 + TOK : N;
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < N; i++) {
+      double mt = -INFINITY;
+      for (int j = j0; j < j1; j++)
+        if (S[(size_t)i * N + j] > mt) mt = S[(size_t)i * N + j];
+      const double mn = (mt > m[i]) ? mt : m[i];
+      const double alpha = (m[i] == -INFINITY) ? 0.0 : exp(m[i] - mn);
+      double rs = 0.0;
+      for (int j = j0; j < j1; j++) {
+        double s = S[(size_t)i * N + j];
+        double p = (s == -INFINITY) ? 0.0 : exp(s - mn);
+        if (quant) p = (double)(float)p;
+        P[(size_t)i * N + j] = p;
+        rs += p;
+      }
+      l[i] = l[i] * alpha + rs;
+      for (int d = 0; d < D; d++) O[(size_t)i * D + d] *= alpha;
+      m[i] = mn;
+    }
+    /* O += P~^ V^ for this key tile, P~ quantized per (64 x 128) block; each
+     * sum runs over j in ascending order */
+#pragma omp parallel for schedule(static)
+    for (int i0 = 0; i0 < N; i0 += QBLK) {
+      const int i1 = (i0 + QBLK < N) ? i0 + QBLK : N;
+      double acc[D];
+      quant_block(P, N, i0, i1, j0, j1, quant, Pq);
+      for (int i = i0; i < i1; i++) {
+        for (int d = 0; d < D; d++) acc[d] = 0.0;
+        for (int j = j0; j < j1; j++)
+          for (int d = 0; d < D; d++) acc[d] += Pq[(size_t)i * N + j] * Vd[(size_t)j * D + d];
+        for (int d = 0; d < D; d++) O[(size_t)i * D + d] += acc[d];
+      }
+    }
+  }
+  for (int i = 0; i < N; i++) {
+    L[i] = m[i] + log(l[i]);
+    lse[i] = L[i];
+    for (int d = 0; d < D; d++) O[(size_t)i * D + d] /= l[i];
+  }
+  /* backward: exact P from L (the forward's quantized Q and K) */
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < N; i++)
+    for (int j = 0; j < N; j++) {
+      double s = S[(size_t)i * N + j];
+      P[(size_t)i * N + j] = (s == -INFINITY) ? 0.0 : exp(s - L[i]);
+    }
+  /* dV = P^^T dO^ (INT8) */
+  quant_blocks_nn(P, N, quant, Pq);
+  mt_times(Pq, dOd, N, D, dv);
+  /* D_i = rowsum(dO o O), O as the forward returns it */
+  for (int i = 0; i < N; i++) {
+    double r = 0.0;
+    for (int d = 0; d < D; d++) {
+      double od = O[(size_t)i * D + d];
+      r += (double)bf16f(dout[(size_t)i * D + d]) * (quant ? bf16_round(od) : od);
+    }
+    Dr[i] = r;
+  }
+  /* dP = dO V^T in FP16 (inputs rounded to FP16); dS = P o (dP - D) into S */
+  for (size_t x = 0; x < (size_t)N * D; x++) {
+    float a = bf16f(dout[x]), b = bf16f(v[x]);
+    dOh[x] = quant ? fp16_round(a) : (double)a;
+    Vh[x] = quant ? fp16_round(b) : (double)b;
+  }
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < N; i++)
+    for (int j = 0; j < N; j++) {
+      double dp = 0.0;
+      for (int d = 0; d < D; d++) dp += dOh[(size_t)i * D + d] * Vh[(size_t)j * D + d];
+      S[(size_t)i * N + j] = P[(size_t)i * N + j] * (dp - Dr[i]);
+    }
+  /* dQ = scale * dS^ K^, dK = scale * dS^^T Q^ (INT8) */
+  quant_blocks_nn(S, N, quant, Pq);
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < N; i++) {
+    double acc[D];
+    for (int d = 0; d < D; d++) acc[d] = 0.0;
+    for (int j = 0; j < N; j++)
+      for (int d = 0; d < D; d++) acc[d] += Pq[(size_t)i * N + j] * Kd[(size_t)j * D + d];
+    for (int d = 0; d < D; d++) dq[(size_t)i * D + d] = scale * acc[d];
+  }
+  mt_times(Pq, Qd, N, D, dk);
+  for (size_t x = 0; x < (size_t)N * D; x++) dk[x] *= scale;
+out:
+  free(Qd);
+  free(Kd);
+  free(Vd);
+  free(dOd);
+  free(S);
+  free(P);
+  free(Pq);
+  free(L);
+  free(Dr);
+  free(m);
+  free(l);
+  free(dOh);
+  free(Vh);
+  return rc;
+}
+
 int sbo_attention_train(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
                         int BH, int N, int D, int causal, double scale, int quant, double *o,
                         double *lse, double *dq, double *dk, double *dv) {
-  if (BH < 0 || N < 1 || D < 1 || !(scale > 0.0) || isinf(scale) || (quant != 0 && quant != 1)) return -1;
-  int failed = 0;
-#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+  if (BH < 0 || N < 1 || D < 1 || D > 4096 || !(scale > 0.0) || isinf(scale) || (quant != 0 && quant != 1))
+    return -1;
   for (int64_t bh = 0; bh < BH; bh++) {
     const size_t hoff = (size_t)bh * N * D;
-    double *Qd = malloc(sizeof(double) * N * D), *Kd = malloc(sizeof(double) * N * D);
-    double *Vd = malloc(sizeof(double) * N * D), *dOd = malloc(sizeof(double) * N * D);
-    double *S = malloc(sizeof(double) * N * N), *P = malloc(sizeof(double) * N * N);
-    double *Pq = malloc(sizeof(double) * N * N), *L = malloc(sizeof(double) * N);
-    double *Dr = malloc(sizeof(double) * N), *m = malloc(sizeof(double) * N);
-    double *l = malloc(sizeof(double) * N);
-    if (!Qd || !Kd || !Vd || !dOd || !S || !P || !Pq || !L || !Dr || !m || !l) {
-      failed = 1;
-    } else {
-      dequant_head(q + hoff, N, D, quant, Qd);
-      dequant_head(k + hoff, N, D, quant, Kd);
-      dequant_head(v + hoff, N, D, quant, Vd);
-      dequant_head(dout + hoff, N, D, quant, dOd);
-      /* scale * S = scale * Q^ K^^T (an INT8 product; exact here), masked -inf */
-      for (int i = 0; i < N; i++)
-        for (int j = 0; j < N; j++) {
-          double s = 0.0;
-          for (int d = 0; d < D; d++) s += Qd[(size_t)i * D + d] * Kd[(size_t)j * D + d];
-          S[(size_t)i * N + j] = (causal && j > i) ? -INFINITY : scale * s;
-        }
-      /* forward: online softmax over key tiles; P~ of each tile into P */
-      double *O = o + hoff;
-      for (size_t x = 0; x < (size_t)N * D; x++) O[x] = 0.0;
-      for (int i = 0; i < N; i++) {
-        m[i] = -INFINITY;
-        l[i] = 0.0;
-      }
-      for (int j0 = 0; j0 < N; j0 += TOK) {
-        const int j1 = (j0 + TOK < N) ? j0 + TOK : N;
-        for (int i = 0; i < N; i++) {
-          double mt = -INFINITY;
-          for (int j = j0; j < j1; j++)
-            if (S[(size_t)i * N + j] > mt) mt = S[(size_t)i * N + j];
-          const double mn = (mt > m[i]) ? mt : m[i];
-          const double alpha = (m[i] == -INFINITY) ? 0.0 : exp(m[i] - mn);
-          double rs = 0.0;
-          for (int j = j0; j < j1; j++) {
-            double s = S[(size_t)i * N + j];
-            double p = (s == -INFINITY) ? 0.0 : exp(s - mn);
-            if (quant) p = (double)(float)p;
-            P[(size_t)i * N + j] = p;
-            rs += p;
-          }
-          l[i] = l[i] * alpha + rs;
-          for (int d = 0; d < D; d++) O[(size_t)i * D + d] *= alpha;
-          m[i] = mn;
-        }
-        /* O += P~^ V^ for this key tile, P~ quantized per (64 x 128) block */
-        for (int i0 = 0; i0 < N; i0 += QBLK) {
-          const int i1 = (i0 + QBLK < N) ? i0 + QBLK : N;
-          quant_block(P, N, i0, i1, j0, j1, quant, Pq);
-          for (int i = i0; i < i1; i++)
-            for (int d = 0; d < D; d++) {
-              double acc = 0.0;
-              for (int j = j0; j < j1; j++) acc += Pq[(size_t)i * N + j] * Vd[(size_t)j * D + d];
-              O[(size_t)i * D + d] += acc;
-            }
-        }
-      }
-      for (int i = 0; i < N; i++) {
-        L[i] = m[i] + log(l[i]);
-        lse[(size_t)bh * N + i] = L[i];
-        for (int d = 0; d < D; d++) O[(size_t)i * D + d] /= l[i];
-      }
-      /* backward: exact P from L (the forward's quantized Q and K) */
-      for (int i = 0; i < N; i++)
-        for (int j = 0; j < N; j++) {
-          double s = S[(size_t)i * N + j];
-          P[(size_t)i * N + j] = (s == -INFINITY) ? 0.0 : exp(s - L[i]);
-        }
-      /* dV = P^^T dO^ (INT8) */
-      quant_blocks_nn(P, N, quant, Pq);
-      for (int j = 0; j < N; j++)
-        for (int d = 0; d < D; d++) {
-          double acc = 0.0;
-          for (int i = 0; i < N; i++) acc += Pq[(size_t)i * N + j] * dOd[(size_t)i * D + d];
-          dv[hoff + (size_t)j * D + d] = acc;
-        }
-      /* D_i = rowsum(dO o O), O as the forward returns it */
-      for (int i = 0; i < N; i++) {
-        double r = 0.0;
-        for (int d = 0; d < D; d++) {
-          double od = O[(size_t)i * D + d];
-          r += (double)bf16f(dout[hoff + (size_t)i * D + d]) * (quant ? bf16_round(od) : od);
-        }
-        Dr[i] = r;
-      }
-      /* dP = dO V^T in FP16 (inputs rounded to FP16); dS = P o (dP - D) into S */
-      for (int i = 0; i < N; i++)
-        for (int j = 0; j < N; j++) {
-          double dp = 0.0;
-          for (int d = 0; d < D; d++) {
-            float a = bf16f(dout[hoff + (size_t)i * D + d]), b = bf16f(v[hoff + (size_t)j * D + d]);
-            dp += quant ? fp16_round(a) * fp16_round(b) : (double)a * (double)b;
-          }
-          S[(size_t)i * N + j] = P[(size_t)i * N + j] * (dp - Dr[i]);
-        }
-      /* dQ = scale * dS^ K^, dK = scale * dS^^T Q^ (INT8) */
-      quant_blocks_nn(S, N, quant, Pq);
-      for (int i = 0; i < N; i++)
-        for (int d = 0; d < D; d++) {
-          double acc = 0.0;
-          for (int j = 0; j < N; j++) acc += Pq[(size_t)i * N + j] * Kd[(size_t)j * D + d];
-          dq[hoff + (size_t)i * D + d] = scale * acc;
-        }
-      for (int j = 0; j < N; j++)
-        for (int d = 0; d < D; d++) {
-          double acc = 0.0;
-          for (int i = 0; i < N; i++) acc += Pq[(size_t)i * N + j] * Qd[(size_t)i * D + d];
-          dk[hoff + (size_t)j * D + d] = scale * acc;
-        }
-    }
-    free(Qd);
-    free(Kd);
-    free(Vd);
-    free(dOd);
-    free(S);
-    free(P);
-    free(Pq);
-    free(L);
-    free(Dr);
-    free(m);
-    free(l);
+    int rc = train_head(q + hoff, k + hoff, v + hoff, dout + hoff, N, D, causal, scale, quant, o + hoff,
+                        lse + (size_t)bh * N, dq + hoff, dk + hoff, dv + hoff);
+    if (rc) return rc;
   }
-  return failed ? -2 : 0;
+  return 0;
 }

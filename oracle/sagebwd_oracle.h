@@ -23,8 +23,8 @@ void sbo_quantize_blocks(const uint16_t *x, int BH, int N, int D, int8_t *codes,
  * v and the output gradient dout ([BH][N][D] each).  Writes o, the row
  * log-sum-exp lse [BH][N], and dq, dk, dv ([BH][N][D], double).  quant = 1:
  * SageBwd's INT8 and FP16 products; quant = 0: exact float64 attention and
- * its exact gradient.  Returns 0, -1 for invalid arguments, -2 if memory ran
- * out. */
+ * its exact gradient.  Returns 0, -1 for invalid arguments (N < 1, D outside
+ * [1, 4096], a scale that is not positive and finite), -2 if memory ran out. */
 int sbo_attention_train(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *dout,
                         int BH, int N, int D, int causal, double scale, int quant, double *o,
                         double *lse, double *dq, double *dk, double *dv);

@@ -13,6 +13,8 @@ training, forward and backward (senqingzn.com article on SageAttention3,
 * that the products use the quantized operands: a V block (or dO block) with
   one outlier quantizes every other entry of that block to zero, so channels
   without the outlier must come out exactly zero;
+* FP16 rounding of dP's operands: a power-of-two scaling of dO scales every
+  gradient exactly until dO reaches FP16's subnormal range, and dQ not after;
 * the shape of the P and dS blocks (64 queries x 128 keys): query rows in
   different 64-row blocks never interact (changing rows 64-127 leaves O,
   lse, dQ of rows 0-63 and every dK, dV entry bit-identical when their dO
@@ -128,6 +130,22 @@ def test_scale_identities(causal):
     assert np.array_equal(dv3, 2 * base[4])
 
 
+def test_dp_operands_are_rounded_to_fp16():
+    """Scaling dO by a power of two is exact for the INT8 blocks, D and bf16;
+    only dP's FP16 operands break it, once dO falls into FP16's subnormal
+    range (below 2^-14): dQ then stops scaling by exactly 2^-18."""
+    BH, N, D = 2, 200, 64
+    q, k, v, do = rand_inputs(BH, N, D, seed=7)
+    small = (do.float() * 2.0 ** -18).to(torch.bfloat16)
+    base = oracle.sagebwd(q, k, v, do, BH, N, D, False)
+    tiny = oracle.sagebwd(q, k, v, small, BH, N, D, False)
+    assert np.array_equal(tiny[4], base[4] * 2.0 ** -18)          # dV: INT8 dO only
+    assert not np.array_equal(tiny[2], base[2] * 2.0 ** -18)      # dQ: through dP
+    ex = oracle.sagebwd(q, k, v, do, BH, N, D, False, quant=False)
+    ex_tiny = oracle.sagebwd(q, k, v, small, BH, N, D, False, quant=False)
+    assert np.array_equal(ex_tiny[2], ex[2] * 2.0 ** -18)
+
+
 def test_products_use_the_quantized_v_and_do():
     # Every V (and dO) entry is 1 except one outlier of 1000 in channel 0 of
     # token 0: per 128-token block the scale is 1000/127, so the 1s quantize
@@ -205,16 +223,16 @@ MUTATIONS = {
                 "S[(size_t)i * N + j] = P[(size_t)i * N + j] * (Dr[i] - dp);"),
     "ds_drops_D": ("S[(size_t)i * N + j] = P[(size_t)i * N + j] * (dp - Dr[i]);",
                    "S[(size_t)i * N + j] = P[(size_t)i * N + j] * dp;"),
-    "dq_without_scale": ("dq[hoff + (size_t)i * D + d] = scale * acc;", "dq[hoff + (size_t)i * D + d] = acc;"),
-    "dk_not_transposed": ("for (int i = 0; i < N; i++) acc += Pq[(size_t)i * N + j] * Qd[(size_t)i * D + d];",
-                          "for (int i = 0; i < N; i++) acc += Pq[(size_t)j * N + i] * Qd[(size_t)i * D + d];"),
-    "dv_from_v": ("acc += Pq[(size_t)i * N + j] * dOd[(size_t)i * D + d];",
-                  "acc += Pq[(size_t)i * N + j] * Vd[(size_t)i * D + d];"),
-    "o_from_unquantized_v": ("dequant_head(v + hoff, N, D, quant, Vd);", "dequant_head(v + hoff, N, D, 0, Vd);"),
-    "dv_from_unquantized_do": ("dequant_head(dout + hoff, N, D, quant, dOd);",
-                               "dequant_head(dout + hoff, N, D, 0, dOd);"),
+    "dq_without_scale": ("dq[(size_t)i * D + d] = scale * acc[d];", "dq[(size_t)i * D + d] = acc[d];"),
+    "dk_not_transposed": ("mt_times(Pq, Qd, N, D, dk);", "mt_times(Pq, Kd, N, D, dk);"),
+    "dv_from_v": ("mt_times(Pq, dOd, N, D, dv);", "mt_times(Pq, Vd, N, D, dv);"),
+    "mt_not_transposed": ("dst[(size_t)j * D + d] += M[(size_t)i * N + j] * X[(size_t)i * D + d];",
+                          "dst[(size_t)j * D + d] += M[(size_t)j * N + i] * X[(size_t)i * D + d];"),
+    "o_from_unquantized_v": ("dequant_head(v, N, D, quant, Vd);", "dequant_head(v, N, D, 0, Vd);"),
+    "dv_from_unquantized_do": ("dequant_head(dout, N, D, quant, dOd);", "dequant_head(dout, N, D, 0, dOd);"),
     "lse_without_max": ("L[i] = m[i] + log(l[i]);", "L[i] = log(l[i]);"),
     "o_not_rescaled": ("for (int d = 0; d < D; d++) O[(size_t)i * D + d] *= alpha;", ""),
+    "dp_unrounded_operands": ("dOh[x] = quant ? fp16_round(a) : (double)a;", "dOh[x] = (double)a;"),
     "l_not_rescaled": ("l[i] = l[i] * alpha + rs;", "l[i] = l[i] + rs;"),
     "p_block_128_queries": ("#define QBLK 64", "#define QBLK 128"),
     "p_block_one_row": ("#define QBLK 64", "#define QBLK 1"),
@@ -230,6 +248,7 @@ def all_pins():
         ("scales", lambda: test_scale_identities(False)),
         ("outliers", test_products_use_the_quantized_v_and_do),
         ("blocks", test_p_blocks_are_64_queries_by_128_keys),
+        ("fp16", test_dp_operands_are_rounded_to_fp16),
     ]
     failed = []
     for name, fn in checks:
