@@ -25,7 +25,7 @@ OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libsagefp4.so")
 OUT_DEBUG = os.path.join(HERE, "_build_debug")
 LIB_DEBUG = os.path.join(OUT_DEBUG, "libsagefp4_debug.so")
-SOURCES = ["quant.cu", "attn.cu", "probe.cu", "api.cu", "noalloc.cu", "host_pipe.cu"]
+SOURCES = ["quant.cu", "attn.cu", "probe.cu", "api.cu", "noalloc.cu", "host_pipe.cu", "sagebwd.cu"]
 HEADERS = ["ptx.cuh", "layout.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -40,6 +40,7 @@ def nvcc() -> str:
 def _inputs():
     files = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
     files.append(os.path.join(ROOT, "include", "sage_fp4.h"))
+    files.append(os.path.join(ROOT, "include", "sagebwd.h"))
     files.append(os.path.abspath(__file__))
     return files
 

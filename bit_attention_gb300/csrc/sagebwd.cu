@@ -1,0 +1,1139 @@
+// sagebwd.cu -- SageBwd, the 8-bit attention for training: forward and
+// backward kernels and the C ABI of include/sagebwd.h (senqingzn.com article
+// on SageAttention3, "INT8 attention for training" and "Solving two obstacles
+// and one difficulty", difficulty 3; abstract of "SageAttention3: Microscaling
+// FP4 Attention for Inference and An Exploration of 8-Bit Training").
+//
+// Six of the seven products run on the INT8 tensor path (mma.sync m16n8k32,
+// exact s32 accumulation): S = Q K^T (forward, and again in the backward),
+// O = P V, dV = P^T dO, dQ = dS K, dK = dS^T Q.  dP = dO V^T, the product
+// that forms the attention-map gradient, runs in FP16 (mma.sync m16n8k16,
+// FP32 accumulation).  Quantization: Q, K, V, dO per head in blocks of 128
+// tokens, P and dS per block of 64 queries x 128 keys, scale amax / 127, codes
+// rint(x * (127 / amax)).  The forward is FlashAttention's online softmax
+// (P~ = exp(S - running max) quantized per block, the normaliser summed from
+// the unquantized P~); the backward recomputes P = exp(S - L) from the saved
+// log-sum-exp.  (sm_103a has no INT8 form of tcgen05.mma, so the warp-level
+// INT8 MMA is the tensor path here.)
+//
+// Layout.  Every quantized operand is written by the quantizer kernels as
+// tiles that are contiguous in global memory (one bulk copy each) and
+// already swizzled for conflict-free ldmatrix (16-byte chunks XOR-permuted by
+// row).  Transposed tiles ([D][tokens]) hold the tokens of each 32-token
+// chunk in the order in which a thread's MMA accumulator values become its A
+// fragment for the next product (pi32 below), so P and dS go from one MMA to
+// the next without a shuffle; dQ's key order (rho32) lets each thread stage
+// its dS codes with 16-bit stores.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sagebwd.h"
+#include "ptx.cuh"
+
+namespace sagebwd {
+
+using sagefp4::bulk_load;
+using sagefp4::globaltimer_ns;
+using sagefp4::mbar_arrive_expect_tx;
+using sagefp4::mbar_fence_init;
+using sagefp4::mbar_init;
+using sagefp4::mbar_try_wait;
+using sagefp4::smem_addr;
+
+constexpr int kTok = 128;  // token block of Q, K, V, dO; key tile; key edge of a P / dS block
+constexpr int kQ = 64;     // query tile of the backward; query edge of a P / dS block
+constexpr int kThreads = 256;
+constexpr unsigned kFull = 0xffffffffu;
+constexpr uint64_t kWaitNs = 1500ull * 1000ull * 1000ull;  // bounded copy waits: 1.5 s
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------- layout
+// Byte offset of logical (row, byte) in a tile of rows W bytes wide.  The
+// 16-byte chunk index is XORed with a function of the row so that the eight
+// rows one ldmatrix reads at the same logical chunk fall in eight different
+// bank groups.
+__host__ __device__ __forceinline__ int swz(int row, int byte, int W) {
+  const int sw = (W == 64) ? ((row >> 1) & 3) : (row & 7);
+  return row * W + ((((byte >> 4) ^ sw)) << 4) + (byte & 15);
+}
+
+// Stored position k (0..31) of a 32-token chunk -> token offset in the chunk.
+// Positions 4t..4t+3 hold tokens 2t, 2t+1, 8+2t, 9+2t (and +16 for the upper
+// half): the accumulator columns that thread t of each quad holds in the two
+// n8 blocks of the previous MMA.
+__host__ __device__ __forceinline__ int pi32(int k) {
+  return (k & 16) | (((k >> 1) & 1) << 3) | (((k >> 2) & 3) << 1) | (k & 1);
+}
+// dQ's key order: position 16u + 2g + h holds key 16u + g + 8h.
+__host__ __device__ __forceinline__ int rho32(int k) { return (k & 16) | ((k >> 1) & 7) | ((k & 1) << 3); }
+
+// ---------------------------------------------------------------- helpers
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_s8(int (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// rint(x) saturated to [-128, 127], as an int (its low byte is the s8 code).
+__device__ __forceinline__ int cvt_s8(float x) {
+  int r;
+  asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+// Low bytes of four ints -> one register, byte 0 from a.
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
+  const uint32_t lo = __byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(b), 0x0040);
+  const uint32_t hi = __byte_perm(static_cast<uint32_t>(c), static_cast<uint32_t>(d), 0x0040);
+  return __byte_perm(lo, hi, 0x5410);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void red_add_v2(float* p, float a, float b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
+}
+
+struct Ctl {
+  int32_t* status;
+  uint64_t limit;
+};
+
+// Bounded wait by a whole warp for an mbarrier phase.  False: the copy never
+// completed; the status word holds SAGEBWD_ETIMEOUT.
+__device__ __forceinline__ bool waitw(uint32_t bar, uint32_t parity, const Ctl& c) {
+  if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+    int stop = 0;
+    if ((threadIdx.x & 31) == 0 && globaltimer_ns() - t0 > c.limit) {
+      atomicCAS(c.status, 0, SAGE_FP4_ETIMEOUT);
+      stop = 1;
+    }
+    if (__shfl_sync(kFull, stop, 0)) return false;
+  }
+}
+
+// Wait used only while abandoning work, so that no copy is still writing
+// shared memory when the CTA exits: bounded, result ignored.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const Ctl& c) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < c.limit) {
+  }
+}
+
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+// bf16 -> FP16 bits, rounded to nearest even, saturated to +-65504.
+__device__ __forceinline__ uint16_t f2h_sat(float x) {
+  x = fminf(fmaxf(x, -65504.0f), 65504.0f);
+  return __half_as_ushort(__float2half_rn(x));
+}
+
+// ---------------------------------------------------------------- workspace
+struct Ws {
+  int8_t *qr, *qt, *kr, *kt, *vt, *dot;
+  uint16_t *vh, *doh;
+  float *sq, *sk, *sv, *sdo, *l2, *dd, *dqacc;
+  int32_t* status;
+};
+
+// ---------------------------------------------------------------- quantizer
+// One CTA per (128-token block, head).  kind 0: Q (row tiles [64][D] and
+// transposed tiles [D][64]); 1: K ([128][D] and [D][128] in dQ's key order);
+// 2: V ([D][128] and FP16 [128][D]); 3: dO ([D][64] and FP16 [64][D]), with
+// D_i = sum_d dO_id O_id, the log2-domain log-sum-exp, and dQ's accumulator
+// rows zeroed.
+template <int D>
+__global__ void __launch_bounds__(kThreads) quant_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+                                                         const uint16_t* __restrict__ v, const uint16_t* __restrict__ o,
+                                                         const float* __restrict__ lse, int N, int kind0, Ws ws) {
+  __shared__ __align__(16) uint16_t xs[kTok * D];
+  __shared__ float red[kThreads / 32];
+  const int kind = kind0 + blockIdx.z;
+  const int blk = blockIdx.x, bh = blockIdx.y;
+  const int nb = (N + kTok - 1) / kTok;
+  const int Np = nb * kTok;
+  const int n0 = blk * kTok;
+  const int rows = min(kTok, N - n0);
+  const uint16_t* x = (kind == 0 ? q : kind == 1 ? k : kind == 2 ? v : q) + (static_cast<size_t>(bh) * N + n0) * D;
+  const int tid = threadIdx.x;
+
+  // load the block (zeros past N) and find its largest magnitude
+  float amax = 0.0f;
+  constexpr int kVec = kTok * D / 8;  // 16-byte vectors
+  for (int i = tid; i < kVec; i += kThreads) {
+    const int r = i / (D / 8);
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (r < rows) val = __ldg(reinterpret_cast<const uint4*>(x) + i);
+    reinterpret_cast<uint4*>(xs)[i] = val;
+    const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[j] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[j] & 0xffff0000u)));
+    }
+  }
+  amax = warp_max(amax);
+  if ((tid & 31) == 0) red[tid >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; w++) amax = fmaxf(amax, red[w]);
+  const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+  const float sc = __fdiv_rn(amax, 127.0f);
+  const size_t hb = static_cast<size_t>(bh) * Np * D;  // this head's first byte of a code array
+  if (tid == 0) {
+    float* s = kind == 0 ? ws.sq : kind == 1 ? ws.sk : kind == 2 ? ws.sv : ws.sdo;
+    s[static_cast<size_t>(bh) * nb + blk] = sc;
+  }
+  auto code = [&](int r, int d) { return cvt_s8(__fmul_rn(bf2f(xs[r * D + d]), inv)); };
+
+  // row-major INT8 tiles of T tokens: [T][D], one 16-byte chunk per step
+  auto rows_out = [&](int8_t* dst, int T) {
+    for (int i = tid; i < kTok * D / 16; i += kThreads) {
+      const int r = i / (D / 16), c = i % (D / 16);
+      int b[16];
+#pragma unroll
+      for (int j = 0; j < 16; j++) b[j] = code(r, 16 * c + j);
+      uint4 out = make_uint4(pack4(b[0], b[1], b[2], b[3]), pack4(b[4], b[5], b[6], b[7]),
+                             pack4(b[8], b[9], b[10], b[11]), pack4(b[12], b[13], b[14], b[15]));
+      const size_t tile = (n0 + r) / T;
+      *reinterpret_cast<uint4*>(dst + hb + tile * T * D + swz(r % T, 16 * c, D)) = out;
+    }
+  };
+  // transposed INT8 tiles of T tokens: [D][T], tokens of each 32-chunk in the
+  // order perm (pi32 or rho32)
+  auto cols_out = [&](int8_t* dst, int T, bool rho) {
+    constexpr int kChunks = kTok / 16;
+    for (int i = tid; i < D * kChunks; i += kThreads) {
+      const int d = i % D, c = i / D;  // consecutive threads: consecutive d
+      const int t0 = 16 * c;           // first stored position in the 128-token block
+      int b[16];
+#pragma unroll
+      for (int j = 0; j < 16; j++) {
+        const int p = t0 + j;
+        const int tok = (p & ~31) | (rho ? rho32(p & 31) : pi32(p & 31));
+        b[j] = code(tok, d);
+      }
+      uint4 out = make_uint4(pack4(b[0], b[1], b[2], b[3]), pack4(b[4], b[5], b[6], b[7]),
+                             pack4(b[8], b[9], b[10], b[11]), pack4(b[12], b[13], b[14], b[15]));
+      const int tile = (n0 + t0) / T, within = (n0 + t0) % T;
+      *reinterpret_cast<uint4*>(dst + hb + static_cast<size_t>(tile) * T * D + swz(d, within, T)) = out;
+    }
+  };
+  // row-major FP16 tiles of T tokens: [T][D] halves, rows 2D bytes wide
+  auto half_out = [&](uint16_t* dst, int T) {
+    for (int i = tid; i < kTok * D / 8; i += kThreads) {
+      const int r = i / (D / 8), c = i % (D / 8);
+      uint32_t h[4];
+#pragma unroll
+      for (int j = 0; j < 4; j++)
+        h[j] = static_cast<uint32_t>(f2h_sat(bf2f(xs[r * D + 8 * c + 2 * j]))) |
+               (static_cast<uint32_t>(f2h_sat(bf2f(xs[r * D + 8 * c + 2 * j + 1]))) << 16);
+      const size_t tile = (n0 + r) / T;
+      char* base = reinterpret_cast<char*>(dst + hb + tile * T * D);
+      *reinterpret_cast<uint4*>(base + swz(r % T, 16 * c, 2 * D)) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+  };
+
+  if (kind == 0) {
+    rows_out(ws.qr, kQ);
+    cols_out(ws.qt, kQ, false);
+  } else if (kind == 1) {
+    rows_out(ws.kr, kTok);
+    cols_out(ws.kt, kTok, true);
+  } else if (kind == 2) {
+    cols_out(ws.vt, kTok, false);
+    half_out(ws.vh, kTok);
+  } else {
+    cols_out(ws.dot, kQ, false);
+    half_out(ws.doh, kQ);
+    // D_i = sum_d dO_id O_id and L in log2 units: one warp per row
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int r = warp; r < kTok; r += kThreads / 32) {
+      float acc = 0.0f;
+      if (r < rows) {
+        const uint16_t* orow = o + (static_cast<size_t>(bh) * N + n0 + r) * D;
+        for (int d = lane; d < D; d += 32) acc = fmaf(bf2f(xs[r * D + d]), bf2f(orow[d]), acc);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+      if (lane == 0) {
+        const size_t ix = static_cast<size_t>(bh) * Np + n0 + r;
+        ws.dd[ix] = acc;
+        ws.l2[ix] = r < rows ? lse[static_cast<size_t>(bh) * N + n0 + r] * kLog2e : 0.0f;
+      }
+    }
+    float4* acc = reinterpret_cast<float4*>(ws.dqacc + (static_cast<size_t>(bh) * Np + n0) * D);
+    for (int i = tid; i < kTok * D / 4; i += kThreads) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// ---------------------------------------------------------------- forward
+// One CTA of 8 warps per (128 queries, head).  Warp w owns query rows
+// 16w..16w+15; warps 0-3 and 4-7 form the two 64-query P blocks.  Key tiles
+// of 128 (K^ row tile and V^ transposed tile) stream through two stages of
+// shared memory by bulk copy.
+template <int D>
+struct FwdSmem {
+  static constexpr int kQBytes = 2 * kQ * D;
+  static constexpr int kKBytes = kTok * D;
+  static constexpr int kStage = 2 * kKBytes;
+  static constexpr int kQOff = 0;
+  static constexpr int kStageOff = kQBytes;
+  static constexpr int kBarOff = kStageOff + 2 * kStage;  // 3 mbarriers: q, full[2]
+  static constexpr int kRedOff = kBarOff + 64;            // [2][8] floats
+  static constexpr int kBytes = kRedOff + 2 * 8 * 4;
+};
+
+template <int D, bool kCausal>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(Ws ws, uint16_t* __restrict__ out, float* __restrict__ lse, int N, float scale_log2e) {
+  using L = FwdSmem<D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int nqt = (N + kTok - 1) / kTok;
+  const int Np = nqt * kTok;
+  // causal: the longest rows first
+  const int qt = kCausal ? (nqt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int bh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int grp = warp >> 2;
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t qbar = sbase + L::kBarOff, full0 = qbar + 8;
+  float* redp = reinterpret_cast<float*>(smem + L::kRedOff);
+  const Ctl ctl{ws.status, kWaitNs};
+  const int nkt = kCausal ? qt + 1 : nqt;
+  const size_t hb = static_cast<size_t>(bh) * Np * D;
+
+  if (threadIdx.x == 0) {
+    mbar_init(qbar, 1);
+    mbar_init(full0, 1);
+    mbar_init(full0 + 8, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  auto issue_tile = [&](int kt) {
+    const int s = kt & 1;
+    const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+    mbar_arrive_expect_tx(full0 + 8 * s, L::kStage);
+    bulk_load(st, ws.kr + hb + static_cast<size_t>(kt) * kTok * D, L::kKBytes, full0 + 8 * s);
+    bulk_load(st + L::kKBytes, ws.vt + hb + static_cast<size_t>(kt) * kTok * D, L::kKBytes, full0 + 8 * s);
+  };
+  int issued = 0;  // key tiles whose copies thread 0 has issued
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(qbar, L::kQBytes);
+    bulk_load(sbase + L::kQOff, ws.qr + hb + static_cast<size_t>(qt) * kTok * D, L::kQBytes, qbar);
+    for (; issued < 2 && issued < nkt; issued++) issue_tile(issued);
+  }
+  // every wait's outcome is voted on by the whole CTA, so that all warps
+  // carry on or all give up together
+  bool ok = __syncthreads_and(waitw(qbar, 0, ctl));
+
+  // Q^ fragments of this warp's 16 rows (A operand of S = Q K^T)
+  uint32_t qa[D / 32][4];
+  {
+    const int j = lane >> 3;
+    const int r = 16 * (warp & 3) + ((j & 1) << 3) + (lane & 7);
+    const uint32_t tq = sbase + L::kQOff + grp * kQ * D;
+#pragma unroll
+    for (int kc = 0; kc < D / 32; kc++)
+      ldsm_x4(tq + swz(r, 32 * kc + ((j >> 1) << 4), D), qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3]);
+  }
+  const float sqk = ws.sq[static_cast<size_t>(bh) * nqt + qt] * scale_log2e;
+  const int row0 = qt * kTok + 16 * warp + g;  // this thread's rows: row0, row0 + 8
+  const bool valid0 = row0 < N, valid1 = row0 + 8 < N;
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+
+  for (int kt = 0; kt < nkt && ok; kt++) {
+    const int s = kt & 1;
+    const uint32_t kst = sbase + L::kStageOff + s * L::kStage, vst = kst + L::kKBytes;
+    ok = __syncthreads_and(waitw(full0 + 8 * s, (kt >> 1) & 1, ctl));
+    if (!ok) break;
+    // every warp is done with tile kt - 1: its stage takes tile kt + 1
+    if (threadIdx.x == 0 && kt >= 1 && kt + 1 < nkt) issue_tile(issued++);
+    // S = Q^ K^^T for 16 rows x 128 keys
+    int sacc[16][4];
+#pragma unroll
+    for (int nb = 0; nb < 16; nb++) sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0;
+    {
+      const int j = lane >> 3;
+#pragma unroll
+      for (int nb = 0; nb < 16; nb += 2) {
+        const int key = 8 * (nb + (j >> 1)) + (lane & 7);
+#pragma unroll
+        for (int kc = 0; kc < D / 32; kc++) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kst + swz(key, 32 * kc + ((j & 1) << 4), D), b0, b1, b2, b3);
+          mma_s8(sacc[nb], qa[kc], b0, b1);
+          mma_s8(sacc[nb + 1], qa[kc], b2, b3);
+        }
+      }
+    }
+    // scale to log2 units, mask, row maxima
+    const float c2 = sqk * ws.sk[static_cast<size_t>(bh) * nqt + kt];
+    const bool edge = (kCausal && kt == qt) || (kt == nqt - 1 && (N % kTok) != 0);
+    float x[16][4];
+    float tm0 = -INFINITY, tm1 = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < 16; nb++) {
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        float v = static_cast<float>(sacc[nb][e]) * c2;
+        if (edge) {
+          const int key = kt * kTok + 8 * nb + 2 * t + (e & 1);
+          const int row = row0 + ((e >> 1) << 3);
+          if (key >= N || (kCausal && key > row)) v = -INFINITY;
+        }
+        x[nb][e] = v;
+      }
+      tm0 = fmaxf(tm0, fmaxf(x[nb][0], x[nb][1]));
+      tm1 = fmaxf(tm1, fmaxf(x[nb][2], x[nb][3]));
+    }
+    tm0 = fmaxf(tm0, __shfl_xor_sync(kFull, tm0, 1));
+    tm0 = fmaxf(tm0, __shfl_xor_sync(kFull, tm0, 2));
+    tm1 = fmaxf(tm1, __shfl_xor_sync(kFull, tm1, 1));
+    tm1 = fmaxf(tm1, __shfl_xor_sync(kFull, tm1, 2));
+    const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
+    const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);  // m = -inf on the first tile: 0
+    m0 = mn0;
+    m1 = mn1;
+    // P~ = exp2(x - m); rows past N take no part in the block maximum
+    float pmax = 0.0f, rs0 = 0.0f, rs1 = 0.0f;
+#pragma unroll
+    for (int nb = 0; nb < 16; nb++) {
+      x[nb][0] = valid0 ? ex2(x[nb][0] - mn0) : 0.0f;
+      x[nb][1] = valid0 ? ex2(x[nb][1] - mn0) : 0.0f;
+      x[nb][2] = valid1 ? ex2(x[nb][2] - mn1) : 0.0f;
+      x[nb][3] = valid1 ? ex2(x[nb][3] - mn1) : 0.0f;
+      rs0 += x[nb][0] + x[nb][1];
+      rs1 += x[nb][2] + x[nb][3];
+      pmax = fmaxf(pmax, fmaxf(fmaxf(x[nb][0], x[nb][1]), fmaxf(x[nb][2], x[nb][3])));
+    }
+    l0 = l0 * al0 + rs0;
+    l1 = l1 * al1 + rs1;
+    // block maximum over the 64-query group (named barrier per group)
+    pmax = warp_max(pmax);
+    if (lane == 0) redp[s * 8 + warp] = pmax;
+    named_bar(1 + grp, 128);
+    float amax = redp[s * 8 + 4 * grp];
+#pragma unroll
+    for (int w = 1; w < 4; w++) amax = fmaxf(amax, redp[s * 8 + 4 * grp + w]);
+    const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    const float spv = __fdiv_rn(amax, 127.0f) * ws.sv[static_cast<size_t>(bh) * nqt + kt];
+    // P^ codes as A fragments (keys in pi32 order)
+    uint32_t pa[4][4];
+#pragma unroll
+    for (int kc = 0; kc < 4; kc++) {
+      const int b = 4 * kc;
+#pragma unroll
+      for (int h = 0; h < 2; h++) {
+        pa[kc][2 * h + 0] = pack4(cvt_s8(__fmul_rn(x[b + 2 * h][0], inv)), cvt_s8(__fmul_rn(x[b + 2 * h][1], inv)),
+                                  cvt_s8(__fmul_rn(x[b + 2 * h + 1][0], inv)),
+                                  cvt_s8(__fmul_rn(x[b + 2 * h + 1][1], inv)));
+        pa[kc][2 * h + 1] = pack4(cvt_s8(__fmul_rn(x[b + 2 * h][2], inv)), cvt_s8(__fmul_rn(x[b + 2 * h][3], inv)),
+                                  cvt_s8(__fmul_rn(x[b + 2 * h + 1][2], inv)),
+                                  cvt_s8(__fmul_rn(x[b + 2 * h + 1][3], inv)));
+      }
+    }
+    // O = O * alpha + s_P s_V (P^ V^)
+    {
+      const int j = lane >> 3;
+#pragma unroll
+      for (int nd = 0; nd < D / 8; nd += 2) {
+        int acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+        const int drow = 8 * (nd + (j >> 1)) + (lane & 7);
+#pragma unroll
+        for (int kc = 0; kc < 4; kc++) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(vst + swz(drow, 32 * kc + ((j & 1) << 4), kTok), b0, b1, b2, b3);
+          mma_s8(acc[0], pa[kc], b0, b1);
+          mma_s8(acc[1], pa[kc], b2, b3);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+          o[nd + h][0] = fmaf(static_cast<float>(acc[h][0]), spv, o[nd + h][0] * al0);
+          o[nd + h][1] = fmaf(static_cast<float>(acc[h][1]), spv, o[nd + h][1] * al0);
+          o[nd + h][2] = fmaf(static_cast<float>(acc[h][2]), spv, o[nd + h][2] * al1);
+          o[nd + h][3] = fmaf(static_cast<float>(acc[h][3]), spv, o[nd + h][3] * al1);
+        }
+      }
+    }
+  }
+  if (!ok) {
+    // abandoning: let every copy this CTA issued land before exiting (the
+    // newest phase armed on each stage's barrier)
+    if (threadIdx.x == 0) {
+      drain_wait(qbar, 0, ctl);
+      for (int last = issued - 1; last >= 0 && last >= issued - 2; last--)
+        drain_wait(full0 + 8 * (last & 1), (last >> 1) & 1, ctl);
+    }
+    return;
+  }
+  // epilogue: O / l, lse = ln(l) + m ln 2
+  l0 += __shfl_xor_sync(kFull, l0, 1);
+  l0 += __shfl_xor_sync(kFull, l0, 2);
+  l1 += __shfl_xor_sync(kFull, l1, 1);
+  l1 += __shfl_xor_sync(kFull, l1, 2);
+  const float il0 = 1.0f / l0, il1 = 1.0f / l1;
+  uint16_t* orow0 = out + (static_cast<size_t>(bh) * N + row0) * D;
+  uint16_t* orow1 = orow0 + 8 * D;
+#pragma unroll
+  for (int nd = 0; nd < D / 8; nd++) {
+    const int d = 8 * nd + 2 * t;
+    if (valid0) {
+      __nv_bfloat162 v = __floats2bfloat162_rn(o[nd][0] * il0, o[nd][1] * il0);
+      *reinterpret_cast<__nv_bfloat162*>(orow0 + d) = v;
+    }
+    if (valid1) {
+      __nv_bfloat162 v = __floats2bfloat162_rn(o[nd][2] * il1, o[nd][3] * il1);
+      *reinterpret_cast<__nv_bfloat162*>(orow1 + d) = v;
+    }
+  }
+  if (t == 0) {
+    if (valid0) lse[static_cast<size_t>(bh) * N + row0] = (m0 + __log2f(l0)) * kLn2;
+    if (valid1) lse[static_cast<size_t>(bh) * N + row0 + 8] = (m1 + __log2f(l1)) * kLn2;
+  }
+}
+
+// ---------------------------------------------------------------- backward
+// One CTA of 8 warps per (128 keys, head); warp w owns keys 16w..16w+15.  The
+// CTA's K^ (row and dQ-ordered transposed tiles) and FP16 V stay in shared
+// memory; query tiles of 64 (Q^ row and transposed tiles, dO^ transposed
+// tile, FP16 dO, L and D) stream through two stages.  Per query tile: S^T,
+// P^T, dV += P^^T dO^, dP^T (FP16), dS^T, dK += dS^^T Q^, and this key
+// tile's share of dQ = dS^ K^ added to an FP32 accumulator with vector
+// reductions.
+template <int D>
+struct BwdSmem {
+  static constexpr int kKr = 0;
+  static constexpr int kKt = kKr + kTok * D;
+  static constexpr int kVh = kKt + kTok * D;
+  static constexpr int kFixedBytes = 2 * kTok * D + 2 * kTok * D;
+  static constexpr int kQr = 0, kQt = kQr + kQ * D, kDot = kQt + kQ * D, kDoh = kDot + kQ * D;
+  static constexpr int kL = kDoh + 2 * kQ * D, kDd = kL + 4 * kQ;
+  static constexpr int kStage = kDd + 4 * kQ;
+  static constexpr int kStageOff = kFixedBytes;
+  static constexpr int kDs = kStageOff + 2 * kStage;  // staged dS^ codes [64][128]
+  static constexpr int kBarOff = kDs + kQ * kTok;     // fixed, full[2]
+  static constexpr int kRedOff = kBarOff + 64;        // [2 kinds][8] floats
+  static constexpr int kBytes = kRedOff + 2 * 8 * 4;
+};
+
+template <int D, bool kCausal>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv_kernel(Ws ws, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int N, float scale) {
+  using L = BwdSmem<D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int nkt = (N + kTok - 1) / kTok;
+  const int Np = nkt * kTok;
+  const int nqt = Np / kQ;
+  const int kb = blockIdx.x, bh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3, j = lane >> 3;
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t fbar = sbase + L::kBarOff, full0 = fbar + 8;
+  float* redp = reinterpret_cast<float*>(smem + L::kRedOff);
+  const Ctl ctl{ws.status, kWaitNs};
+  const size_t hb = static_cast<size_t>(bh) * Np * D;
+  const size_t hrow = static_cast<size_t>(bh) * Np;
+  const int q0 = kCausal ? 2 * kb : 0;  // first query tile that sees these keys
+  const int niter = nqt - q0;
+
+  auto issue_stage = [&](int it) {
+    const int qtile = q0 + it, s = it & 1;
+    const uint32_t st = sbase + L::kStageOff + s * L::kStage, bar = full0 + 8 * s;
+    mbar_arrive_expect_tx(bar, L::kStage);
+    const size_t off = hb + static_cast<size_t>(qtile) * kQ * D;
+    bulk_load(st + L::kQr, ws.qr + off, kQ * D, bar);
+    bulk_load(st + L::kQt, ws.qt + off, kQ * D, bar);
+    bulk_load(st + L::kDot, ws.dot + off, kQ * D, bar);
+    bulk_load(st + L::kDoh, ws.doh + off, 2 * kQ * D, bar);
+    bulk_load(st + L::kL, ws.l2 + hrow + static_cast<size_t>(qtile) * kQ, 4 * kQ, bar);
+    bulk_load(st + L::kDd, ws.dd + hrow + static_cast<size_t>(qtile) * kQ, 4 * kQ, bar);
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(fbar, 1);
+    mbar_init(full0, 1);
+    mbar_init(full0 + 8, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  int issued = 0;  // query tiles whose copies thread 0 has issued
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(fbar, L::kFixedBytes);
+    const size_t off = hb + static_cast<size_t>(kb) * kTok * D;
+    bulk_load(sbase + L::kKr, ws.kr + off, kTok * D, fbar);
+    bulk_load(sbase + L::kKt, ws.kt + off, kTok * D, fbar);
+    bulk_load(sbase + L::kVh, ws.vh + off, 2 * kTok * D, fbar);
+    for (; issued < 2 && issued < niter; issued++) issue_stage(issued);
+  }
+  // every wait's outcome is voted on by the whole CTA
+  bool ok = __syncthreads_and(waitw(fbar, 0, ctl));
+
+  const float sk = ws.sk[static_cast<size_t>(bh) * nkt + kb];
+  const int key0 = kb * kTok + 16 * warp + g;  // this thread's keys: key0, key0 + 8
+  const float c2base = sk * scale * kLog2e;
+  float dka[D / 8][4], dva[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; i++)
+#pragma unroll
+    for (int e = 0; e < 4; e++) dka[i][e] = dva[i][e] = 0.0f;
+
+  for (int it = 0; it < niter && ok; it++) {
+    const int qtile = q0 + it, s = it & 1;
+    const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+    ok = __syncthreads_and(waitw(full0 + 8 * s, (it >> 1) & 1, ctl));
+    if (!ok) break;
+    const float sq = ws.sq[static_cast<size_t>(bh) * nkt + (qtile >> 1)];
+    const float sdo = ws.sdo[static_cast<size_t>(bh) * nkt + (qtile >> 1)];
+    // S^T = K^ Q^^T: 16 keys x 64 queries
+    int sacc[8][4];
+#pragma unroll
+    for (int nb = 0; nb < 8; nb++) sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0;
+#pragma unroll
+    for (int kc = 0; kc < D / 32; kc++) {
+      uint32_t ka[4];
+      ldsm_x4(sbase + L::kKr + swz(16 * warp + ((j & 1) << 3) + (lane & 7), 32 * kc + ((j >> 1) << 4), D), ka[0],
+              ka[1], ka[2], ka[3]);
+#pragma unroll
+      for (int nb = 0; nb < 8; nb += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(st + L::kQr + swz(8 * (nb + (j >> 1)) + (lane & 7), 32 * kc + ((j & 1) << 4), D), b0, b1, b2, b3);
+        mma_s8(sacc[nb], ka, b0, b1);
+        mma_s8(sacc[nb + 1], ka, b2, b3);
+      }
+    }
+    // P^T = exp2(S^T c - L); masked and padded entries 0
+    const float c2 = c2base * sq;
+    const float* Ls = reinterpret_cast<const float*>(smem + (st - sbase) + L::kL);
+    const float* Ds = reinterpret_cast<const float*>(smem + (st - sbase) + L::kDd);
+    const bool edge = (kCausal && qtile <= 2 * kb + 1) || (qtile * kQ + kQ > N) || (kb * kTok + kTok > N);
+    float p[8][4];
+    float pmax = 0.0f;
+#pragma unroll
+    for (int nb = 0; nb < 8; nb++) {
+      const int qc = 8 * nb + 2 * t;  // query column within the tile
+      const float2 lq = *reinterpret_cast<const float2*>(Ls + qc);
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        float v = ex2(fmaf(static_cast<float>(sacc[nb][e]), c2, -((e & 1) ? lq.y : lq.x)));
+        if (edge) {
+          const int query = qtile * kQ + qc + (e & 1);
+          const int key = key0 + ((e >> 1) << 3);
+          if (query >= N || key >= N || (kCausal && key > query)) v = 0.0f;
+        }
+        p[nb][e] = v;
+        pmax = fmaxf(pmax, v);
+      }
+    }
+    pmax = warp_max(pmax);
+    if (lane == 0) redp[warp] = pmax;
+    __syncthreads();
+    float amax = redp[0];
+#pragma unroll
+    for (int w = 1; w < 8; w++) amax = fmaxf(amax, redp[w]);
+    float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    // P^^T as A fragments (queries in pi32 order)
+    uint32_t pa[2][4];
+#pragma unroll
+    for (int kc = 0; kc < 2; kc++) {
+      const int b = 4 * kc;
+#pragma unroll
+      for (int h = 0; h < 2; h++) {
+        pa[kc][2 * h + 0] = pack4(cvt_s8(__fmul_rn(p[b + 2 * h][0], inv)), cvt_s8(__fmul_rn(p[b + 2 * h][1], inv)),
+                                  cvt_s8(__fmul_rn(p[b + 2 * h + 1][0], inv)),
+                                  cvt_s8(__fmul_rn(p[b + 2 * h + 1][1], inv)));
+        pa[kc][2 * h + 1] = pack4(cvt_s8(__fmul_rn(p[b + 2 * h][2], inv)), cvt_s8(__fmul_rn(p[b + 2 * h][3], inv)),
+                                  cvt_s8(__fmul_rn(p[b + 2 * h + 1][2], inv)),
+                                  cvt_s8(__fmul_rn(p[b + 2 * h + 1][3], inv)));
+      }
+    }
+    // dV += s_P s_dO (P^^T dO^)
+    {
+      const float f = __fdiv_rn(amax, 127.0f) * sdo;
+#pragma unroll
+      for (int nd = 0; nd < D / 8; nd += 2) {
+        int acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+        const int drow = 8 * (nd + (j >> 1)) + (lane & 7);
+#pragma unroll
+        for (int kc = 0; kc < 2; kc++) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(st + L::kDot + swz(drow, 32 * kc + ((j & 1) << 4), kQ), b0, b1, b2, b3);
+          mma_s8(acc[0], pa[kc], b0, b1);
+          mma_s8(acc[1], pa[kc], b2, b3);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; h++)
+#pragma unroll
+          for (int e = 0; e < 4; e++) dva[nd + h][e] = fmaf(static_cast<float>(acc[h][e]), f, dva[nd + h][e]);
+      }
+    }
+    // dP^T = V dO^T in FP16, then dS^T = P^T o (dP^T - D)
+    float dp[8][4];
+#pragma unroll
+    for (int nb = 0; nb < 8; nb++) dp[nb][0] = dp[nb][1] = dp[nb][2] = dp[nb][3] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ks++) {
+      uint32_t va[4];
+      ldsm_x4(sbase + L::kVh + swz(16 * warp + ((j & 1) << 3) + (lane & 7), 32 * ks + ((j >> 1) << 4), 2 * D),
+              va[0], va[1], va[2], va[3]);
+#pragma unroll
+      for (int nb = 0; nb < 8; nb += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(st + L::kDoh + swz(8 * (nb + (j >> 1)) + (lane & 7), 32 * ks + ((j & 1) << 4), 2 * D), b0, b1, b2,
+                b3);
+        mma_f16(dp[nb], va, b0, b1);
+        mma_f16(dp[nb + 1], va, b2, b3);
+      }
+    }
+    float smax = 0.0f;
+#pragma unroll
+    for (int nb = 0; nb < 8; nb++) {
+      const float2 dq2 = *reinterpret_cast<const float2*>(Ds + 8 * nb + 2 * t);
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        p[nb][e] = p[nb][e] * (dp[nb][e] - ((e & 1) ? dq2.y : dq2.x));
+        smax = fmaxf(smax, fabsf(p[nb][e]));
+      }
+    }
+    smax = warp_max(smax);
+    if (lane == 0) redp[8 + warp] = smax;
+    __syncthreads();
+    amax = redp[8];
+#pragma unroll
+    for (int w = 1; w < 8; w++) amax = fmaxf(amax, redp[8 + w]);
+    inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    const float sds = __fdiv_rn(amax, 127.0f);
+    // dS^ codes: A fragments for dK, and 16-bit stores in dQ's key order
+    int cd[8][4];
+#pragma unroll
+    for (int nb = 0; nb < 8; nb++)
+#pragma unroll
+      for (int e = 0; e < 4; e++) cd[nb][e] = cvt_s8(__fmul_rn(p[nb][e], inv));
+    {
+      uint8_t* dsb = smem + L::kDs;
+#pragma unroll
+      for (int nb = 0; nb < 8; nb++)
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+          const int row = 8 * nb + 2 * t + e;
+          const uint16_t v = static_cast<uint16_t>((cd[nb][e] & 0xff) | ((cd[nb][2 + e] & 0xff) << 8));
+          *reinterpret_cast<uint16_t*>(dsb + swz(row, 16 * warp + 2 * g, kTok)) = v;
+        }
+    }
+    uint32_t da[2][4];
+#pragma unroll
+    for (int kc = 0; kc < 2; kc++) {
+      const int b = 4 * kc;
+#pragma unroll
+      for (int h = 0; h < 2; h++) {
+        da[kc][2 * h + 0] = pack4(cd[b + 2 * h][0], cd[b + 2 * h][1], cd[b + 2 * h + 1][0], cd[b + 2 * h + 1][1]);
+        da[kc][2 * h + 1] = pack4(cd[b + 2 * h][2], cd[b + 2 * h][3], cd[b + 2 * h + 1][2], cd[b + 2 * h + 1][3]);
+      }
+    }
+    // dK += s_dS s_Q (dS^^T Q^)
+    {
+      const float f = sds * sq;
+#pragma unroll
+      for (int nd = 0; nd < D / 8; nd += 2) {
+        int acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+        const int drow = 8 * (nd + (j >> 1)) + (lane & 7);
+#pragma unroll
+        for (int kc = 0; kc < 2; kc++) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(st + L::kQt + swz(drow, 32 * kc + ((j & 1) << 4), kQ), b0, b1, b2, b3);
+          mma_s8(acc[0], da[kc], b0, b1);
+          mma_s8(acc[1], da[kc], b2, b3);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; h++)
+#pragma unroll
+          for (int e = 0; e < 4; e++) dka[nd + h][e] = fmaf(static_cast<float>(acc[h][e]), f, dka[nd + h][e]);
+      }
+    }
+    // every warp's dS^ is staged and every warp is done with stage s
+    __syncthreads();
+    if (threadIdx.x == 0 && it + 2 < niter) issue_stage(issued++);
+    // dQ[64 x D] += scale s_dS s_K (dS^ K^): warp w takes rows 16 (w & 3) and
+    // half of the D columns
+    {
+      const float f = sds * sk * scale;
+      const int r0 = 16 * (warp & 3);
+      const int dh = (warp >> 2) * (D / 2);
+      int acc[D / 16][4];
+#pragma unroll
+      for (int i = 0; i < D / 16; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0;
+#pragma unroll
+      for (int kc = 0; kc < 4; kc++) {
+        uint32_t a[4];
+        ldsm_x4(sbase + L::kDs + swz(r0 + ((j & 1) << 3) + (lane & 7), 32 * kc + ((j >> 1) << 4), kTok), a[0], a[1],
+                a[2], a[3]);
+#pragma unroll
+        for (int nd = 0; nd < D / 16; nd += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(sbase + L::kKt + swz(dh + 8 * (nd + (j >> 1)) + (lane & 7), 32 * kc + ((j & 1) << 4), kTok), b0,
+                  b1, b2, b3);
+          mma_s8(acc[nd], a, b0, b1);
+          mma_s8(acc[nd + 1], a, b2, b3);
+        }
+      }
+      float* dq0 = ws.dqacc + (hrow + static_cast<size_t>(qtile) * kQ + r0 + g) * D + dh + 2 * t;
+#pragma unroll
+      for (int nd = 0; nd < D / 16; nd++) {
+        red_add_v2(dq0 + 8 * nd, static_cast<float>(acc[nd][0]) * f, static_cast<float>(acc[nd][1]) * f);
+        red_add_v2(dq0 + 8 * D + 8 * nd, static_cast<float>(acc[nd][2]) * f, static_cast<float>(acc[nd][3]) * f);
+      }
+    }
+  }
+  if (!ok) {
+    if (threadIdx.x == 0) {
+      drain_wait(fbar, 0, ctl);
+      for (int last = issued - 1; last >= 0 && last >= issued - 2; last--)
+        drain_wait(full0 + 8 * (last & 1), (last >> 1) & 1, ctl);
+    }
+    return;
+  }
+  // dK = scale * sum, dV: bf16 rows (keys) below N
+  const int key1 = key0 + 8;
+#pragma unroll
+  for (int nd = 0; nd < D / 8; nd++) {
+    const int d = 8 * nd + 2 * t;
+    if (key0 < N) {
+      const size_t ix = (static_cast<size_t>(bh) * N + key0) * D + d;
+      *reinterpret_cast<__nv_bfloat162*>(dk + ix) = __floats2bfloat162_rn(dka[nd][0] * scale, dka[nd][1] * scale);
+      *reinterpret_cast<__nv_bfloat162*>(dv + ix) = __floats2bfloat162_rn(dva[nd][0], dva[nd][1]);
+    }
+    if (key1 < N) {
+      const size_t ix = (static_cast<size_t>(bh) * N + key1) * D + d;
+      *reinterpret_cast<__nv_bfloat162*>(dk + ix) = __floats2bfloat162_rn(dka[nd][2] * scale, dka[nd][3] * scale);
+      *reinterpret_cast<__nv_bfloat162*>(dv + ix) = __floats2bfloat162_rn(dva[nd][2], dva[nd][3]);
+    }
+  }
+}
+
+// dQ accumulator (FP32, padded rows) -> bf16 [BH][N][D]
+template <int D>
+__global__ void __launch_bounds__(kThreads) dq_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq, int N,
+                                                      int BH) {
+  const int Np = (N + kTok - 1) / kTok * kTok;
+  const size_t total = static_cast<size_t>(BH) * N * D / 4;
+  for (size_t i = blockIdx.x * static_cast<size_t>(kThreads) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * kThreads) {
+    const size_t e = 4 * i;
+    const size_t row = e / D, d = e % D;
+    const size_t bh = row / N, n = row % N;
+    const float4 v = *reinterpret_cast<const float4*>(acc + (bh * Np + n) * D + d);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 w;
+    w.x = *reinterpret_cast<uint32_t*>(&lo);
+    w.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dq + e) = w;
+  }
+}
+
+// ---------------------------------------------------------------- peak probe
+// Throughput of the two warp-level MMA forms this path uses, on register
+// operands: kind 0 INT8 m16n8k32, kind 1 FP16 m16n8k16 with FP32
+// accumulation.  Eight independent accumulators per warp.
+template <int kKind>
+__global__ void __launch_bounds__(kThreads) mma_peak_kernel(int iters, int* out) {
+  uint32_t a[4], b0, b1;
+  const uint32_t seed = threadIdx.x * 0x9E3779B9u + blockIdx.x;
+  a[0] = seed;
+  a[1] = seed ^ 0x5bd1e995u;
+  a[2] = seed * 3u;
+  a[3] = seed + 0x1234567u;
+  b0 = seed ^ 0xabcdefu;
+  b1 = seed * 7u;
+  if (kKind == 0) {
+    int c[8][4] = {};
+    for (int i = 0; i < iters; i++)
+#pragma unroll
+      for (int u = 0; u < 8; u++) mma_s8(c[u], a, b0, b1);
+    int s = 0;
+#pragma unroll
+    for (int u = 0; u < 8; u++) s += c[u][0] + c[u][1] + c[u][2] + c[u][3];
+    if (s == 0x7fffffff) out[0] = s;
+  } else {
+    // small FP16 values so the sums stay finite
+    a[0] = a[1] = a[2] = a[3] = 0x3c003c00u & (seed | 0x3c003c00u);
+    b0 = b1 = 0x1c001c00u;
+    float c[8][4] = {};
+    for (int i = 0; i < iters; i++)
+#pragma unroll
+      for (int u = 0; u < 8; u++) mma_f16(c[u], a, b0, b1);
+    float s = 0.0f;
+#pragma unroll
+    for (int u = 0; u < 8; u++) s += c[u][0] + c[u][1] + c[u][2] + c[u][3];
+    if (s == -1.0f) out[0] = 1;
+  }
+}
+
+// ---------------------------------------------------------------- host side
+struct Layout {
+  size_t off[SAGEBWD_WS_FIELDS];
+  size_t total;
+};
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+Layout layout(int B, int H, int N, int D) {
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t Np = (static_cast<size_t>(N) + kTok - 1) / kTok * kTok;
+  const size_t nb = Np / kTok;
+  const size_t sizes[SAGEBWD_WS_FIELDS] = {
+      BH * Np * D,      // Q^ row tiles
+      BH * Np * D,      // Q^ transposed tiles
+      BH * Np * D,      // K^ row tiles
+      BH * Np * D,      // K^ transposed tiles (dQ order)
+      BH * Np * D,      // V^ transposed tiles
+      BH * Np * D,      // dO^ transposed tiles
+      2 * BH * Np * D,  // V, FP16 row tiles
+      2 * BH * Np * D,  // dO, FP16 row tiles
+      4 * BH * nb,      // Q scales
+      4 * BH * nb,      // K scales
+      4 * BH * nb,      // V scales
+      4 * BH * nb,      // dO scales
+      4 * BH * Np,      // L, log2 units
+      4 * BH * Np,      // D = rowsum(dO o O)
+      4 * BH * Np * D,  // dQ accumulator
+      256,              // status word
+  };
+  Layout l;
+  size_t off = 0;
+  for (int i = 0; i < SAGEBWD_WS_FIELDS; i++) {
+    l.off[i] = off;
+    off += align256(sizes[i]);
+  }
+  l.total = off;
+  return l;
+}
+
+Ws carve(void* base, const Layout& l) {
+  char* b = static_cast<char*>(base);
+  Ws w;
+  w.qr = reinterpret_cast<int8_t*>(b + l.off[0]);
+  w.qt = reinterpret_cast<int8_t*>(b + l.off[1]);
+  w.kr = reinterpret_cast<int8_t*>(b + l.off[2]);
+  w.kt = reinterpret_cast<int8_t*>(b + l.off[3]);
+  w.vt = reinterpret_cast<int8_t*>(b + l.off[4]);
+  w.dot = reinterpret_cast<int8_t*>(b + l.off[5]);
+  w.vh = reinterpret_cast<uint16_t*>(b + l.off[6]);
+  w.doh = reinterpret_cast<uint16_t*>(b + l.off[7]);
+  w.sq = reinterpret_cast<float*>(b + l.off[8]);
+  w.sk = reinterpret_cast<float*>(b + l.off[9]);
+  w.sv = reinterpret_cast<float*>(b + l.off[10]);
+  w.sdo = reinterpret_cast<float*>(b + l.off[11]);
+  w.l2 = reinterpret_cast<float*>(b + l.off[12]);
+  w.dd = reinterpret_cast<float*>(b + l.off[13]);
+  w.dqacc = reinterpret_cast<float*>(b + l.off[14]);
+  w.status = reinterpret_cast<int32_t*>(b + l.off[15]);
+  return w;
+}
+
+bool dims_ok(int B, int H, int N, int D) {
+  if (B < 0 || H < 0 || N < 0 || (D != 64 && D != 128)) return false;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long Np = (static_cast<long long>(N) + kTok - 1) / kTok * kTok;
+  if (BH > 65535) return false;                    // gridDim.y
+  if (Np / kTok > (1LL << 20)) return false;       // gridDim.x, with room
+  if (BH * Np * D > (1LL << 40)) return false;     // workspace offsets stay sane
+  return true;
+}
+
+bool aligned(const void* p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool scale_ok(float s) { return s > 0.0f && s < 1e30f; }  // false for NaN
+
+int check_device() {
+  static int cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SAGE_FP4_ECUDA;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev] == 1 ? SAGE_FP4_OK : SAGE_FP4_EUNSUPPORTED;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return SAGE_FP4_ECUDA;
+  const bool ok = (major == 10 && minor == 3);
+  if (dev >= 0 && dev < 64) cache[dev] = ok ? 1 : 2;
+  return ok ? SAGE_FP4_OK : SAGE_FP4_EUNSUPPORTED;
+}
+
+template <int D, bool C>
+cudaError_t launch_fwd(const Ws& w, uint16_t* o, float* lse, int BH, int N, float scale, cudaStream_t st) {
+  const int smem = FwdSmem<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((N + kTok - 1) / kTok, BH);
+  fwd_kernel<D, C><<<grid, kThreads, smem, st>>>(w, o, lse, N, scale * kLog2e);
+  return cudaGetLastError();
+}
+
+template <int D, bool C>
+cudaError_t launch_dkdv(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int N, float scale, cudaStream_t st) {
+  const int smem = BwdSmem<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((N + kTok - 1) / kTok, BH);
+  dkdv_kernel<D, C><<<grid, kThreads, smem, st>>>(w, dk, dv, N, scale);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_quant(const Ws& w, const void* a, const void* b, const void* c, const void* o, const float* lse,
+                         int BH, int N, int kind0, int nkinds, cudaStream_t st) {
+  const dim3 grid((N + kTok - 1) / kTok, BH, nkinds);
+  quant_kernel<D><<<grid, kThreads, 0, st>>>(static_cast<const uint16_t*>(a), static_cast<const uint16_t*>(b),
+                                             static_cast<const uint16_t*>(c), static_cast<const uint16_t*>(o), lse, N,
+                                             kind0, w);
+  return cudaGetLastError();
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? SAGE_FP4_OK : SAGE_FP4_ECUDA; }
+
+}  // namespace sagebwd
+
+using namespace sagebwd;
+
+extern "C" {
+
+size_t sagebwd_workspace_bytes(int B, int H, int N, int D) {
+  if (!dims_ok(B, H, N, D)) return 0;
+  return layout(B, H, N, D).total;
+}
+
+int sagebwd_workspace_layout(int B, int H, int N, int D, size_t* offsets) {
+  if (!dims_ok(B, H, N, D) || !offsets) return SAGE_FP4_EINVAL;
+  const Layout l = layout(B, H, N, D);
+  for (int i = 0; i < SAGEBWD_WS_FIELDS; i++) offsets[i] = l.off[i];
+  return SAGE_FP4_OK;
+}
+
+int sagebwd_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+                int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!dims_ok(B, H, N, D) || (causal != 0 && causal != 1) || !scale_ok(scale)) return SAGE_FP4_EINVAL;
+  if (!aligned(workspace, 256)) return SAGE_FP4_EINVAL;
+  const Layout l = layout(B, H, N, D);
+  if (workspace_bytes < l.total) return SAGE_FP4_EINVAL;
+  if (static_cast<long long>(B) * H * N == 0) return SAGE_FP4_OK;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return SAGE_FP4_EINVAL;
+  const int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  const Ws w = carve(workspace, l);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  uint16_t* ob = static_cast<uint16_t*>(o);
+  cudaError_t e = D == 64 ? launch_quant<64>(w, q, k, v, nullptr, nullptr, BH, N, 0, 3, st)
+                          : launch_quant<128>(w, q, k, v, nullptr, nullptr, BH, N, 0, 3, st);
+  if (e != cudaSuccess) return SAGE_FP4_ECUDA;
+  if (D == 64)
+    e = causal ? launch_fwd<64, true>(w, ob, lse, BH, N, scale, st) : launch_fwd<64, false>(w, ob, lse, BH, N, scale, st);
+  else
+    e = causal ? launch_fwd<128, true>(w, ob, lse, BH, N, scale, st)
+               : launch_fwd<128, false>(w, ob, lse, BH, N, scale, st);
+  return from_cuda(e);
+}
+
+int sagebwd_bwd(const void* dout, const void* o, const float* lse, void* dq, void* dk, void* dv, int B, int H, int N,
+                int D, int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!dims_ok(B, H, N, D) || (causal != 0 && causal != 1) || !scale_ok(scale)) return SAGE_FP4_EINVAL;
+  if (!aligned(workspace, 256)) return SAGE_FP4_EINVAL;
+  const Layout l = layout(B, H, N, D);
+  if (workspace_bytes < l.total) return SAGE_FP4_EINVAL;
+  if (static_cast<long long>(B) * H * N == 0) return SAGE_FP4_OK;
+  if (!aligned(dout, 16) || !aligned(o, 16) || !aligned(lse, 4) || !aligned(dq, 16) || !aligned(dk, 16) ||
+      !aligned(dv, 16))
+    return SAGE_FP4_EINVAL;
+  const int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  const Ws w = carve(workspace, l);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  uint16_t *dkb = static_cast<uint16_t*>(dk), *dvb = static_cast<uint16_t*>(dv);
+  cudaError_t e = D == 64 ? launch_quant<64>(w, dout, nullptr, nullptr, o, lse, BH, N, 3, 1, st)
+                          : launch_quant<128>(w, dout, nullptr, nullptr, o, lse, BH, N, 3, 1, st);
+  if (e != cudaSuccess) return SAGE_FP4_ECUDA;
+  if (D == 64)
+    e = causal ? launch_dkdv<64, true>(w, dkb, dvb, BH, N, scale, st)
+               : launch_dkdv<64, false>(w, dkb, dvb, BH, N, scale, st);
+  else
+    e = causal ? launch_dkdv<128, true>(w, dkb, dvb, BH, N, scale, st)
+               : launch_dkdv<128, false>(w, dkb, dvb, BH, N, scale, st);
+  if (e != cudaSuccess) return SAGE_FP4_ECUDA;
+  const size_t total = static_cast<size_t>(BH) * N * D / 4;
+  const int blocks = static_cast<int>((total + kThreads - 1) / kThreads < 152 * 16 ? (total + kThreads - 1) / kThreads
+                                                                                   : 152 * 16);
+  if (D == 64)
+    dq_kernel<64><<<blocks, kThreads, 0, st>>>(w.dqacc, static_cast<uint16_t*>(dq), N, BH);
+  else
+    dq_kernel<128><<<blocks, kThreads, 0, st>>>(w.dqacc, static_cast<uint16_t*>(dq), N, BH);
+  return from_cuda(cudaGetLastError());
+}
+
+int sagebwd_get_status(void* workspace, int B, int H, int N, int D, void* stream) {
+  if (!dims_ok(B, H, N, D) || !aligned(workspace, 256)) return SAGE_FP4_EINVAL;
+  const Layout l = layout(B, H, N, D);
+  int32_t* status = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + l.off[SAGEBWD_WS_FIELDS - 1]);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SAGE_FP4_ECUDA;
+  int32_t h = 0;
+  if (cudaMemcpy(&h, status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return SAGE_FP4_ECUDA;
+  if (h != 0 && cudaMemset(status, 0, sizeof(h)) != cudaSuccess) return SAGE_FP4_ECUDA;
+  return h;
+}
+
+int sagebwd_mma_peak(int kind, int ctas, int iters, void* scratch, void* stream) {
+  if ((kind != 0 && kind != 1) || ctas < 1 || ctas > 65535 || iters < 1 || !aligned(scratch, 4))
+    return SAGE_FP4_EINVAL;
+  const int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (kind == 0)
+    mma_peak_kernel<0><<<ctas, kThreads, 0, st>>>(iters, static_cast<int*>(scratch));
+  else
+    mma_peak_kernel<1><<<ctas, kThreads, 0, st>>>(iters, static_cast<int*>(scratch));
+  return from_cuda(cudaGetLastError());
+}
+
+}  // extern "C"

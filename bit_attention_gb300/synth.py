@@ -54,6 +54,18 @@ WORKLOADS = {
                          "sparse_outliers"),
 }
 
+# SageBwd (8-bit attention for training) shapes: the pages fine-tune Llama3.2
+# (1B: 32 query heads of 64) and Qwen2.5 (3B: 16 query heads of 128) and time
+# Llama-1B training on 8K/16K-token micro-batches.  One 8K-token sequence per
+# micro-batch, causal; grouped K/V heads are taken as one K/V head per query
+# head.
+TRAIN_WORKLOADS = {
+    "train_small": Workload("attn_train B1 H2 N512 D64 iid", 1, 2, 512, 64, False, "iid"),
+    "train_llama1b": Workload("attn_train B1 H32 N8192 D64 causal iid", 1, 32, 8192, 64, True, "iid"),
+    "train_qwen3b": Workload("attn_train B1 H16 N8192 D128 causal k-channel-outliers", 1, 16, 8192, 128, True,
+                             "k_channel_outliers"),
+}
+
 
 def make_qkv(B: int, H: int, N: int, D: int, pattern: str = "iid", seed: int = 0):
     """Return bf16 CPU tensors q, k, v of shape [B, H, N, D] (contiguous)."""
@@ -94,3 +106,12 @@ def make_qkv(B: int, H: int, N: int, D: int, pattern: str = "iid", seed: int = 0
 
 def make_workload(w: Workload, seed: int = 0):
     return make_qkv(w.B, w.H, w.N, w.D, w.pattern, seed)
+
+
+def make_dout(B: int, H: int, N: int, D: int, seed: int = 0, std: float = 0.01):
+    """Output gradient dO for the training shapes: bf16 N(0, std) of shape
+    [B, H, N, D], from its own generator (seed + 7919) so that Q, K, V stay
+    those of make_qkv with the same seed."""
+    g = torch.Generator("cpu").manual_seed(seed + 7919)
+    d = torch.randn((B, H, N, D), generator=g, dtype=torch.float32) * std
+    return d.to(torch.bfloat16).contiguous()

@@ -1,0 +1,98 @@
+/* sagebwd.h -- C ABI of SageBwd, the 8-bit attention for training, on
+ * sm_103a (libsagefp4.so).
+ *
+ * The method: the senqingzn.com article on SageAttention3, "INT8 attention
+ * for training" (six of the seven matrix products of attention's forward and
+ * backward passes run in INT8) and "Solving two obstacles and one
+ * difficulty", difficulty 3 (the attention-map gradient accumulates
+ * quantization error, so the most precision-sensitive backward product stays
+ * at FP16); the abstract of "SageAttention3: Microscaling FP4 Attention for
+ * Inference and An Exploration of 8-Bit Training" (an 8-bit attention for
+ * both forward and backward propagation).
+ *
+ * What the library computes (the pages leave the granularity open; these
+ * are the readings the kernels and the test oracle share):
+ *   forward   S = Q^ K^^T (INT8), FlashAttention's online softmax over key
+ *             tiles of 128 with the tile probabilities P~ = exp(scale*S - m)
+ *             quantized to INT8 per block of 64 queries x 128 keys,
+ *             O = sum P~^ V^ / l (INT8 product, l from the unquantized P~);
+ *             saves L = log-sum-exp per row.
+ *   backward  P = exp(scale*S - L); dV = P^^T dO^ (INT8); dP = dO V^T (FP16
+ *             operands, FP32 accumulation); D = rowsum(dO o O);
+ *             dS = P o (dP - D); dQ = scale dS^ K^, dK = scale dS^^T Q^ (INT8,
+ *             dS quantized per block of 64 queries x 128 keys).
+ *   INT8      symmetric per block: scale = amax / 127, code =
+ *             rint(x * (127 / amax)) in float arithmetic.  Q, K, V and dO are
+ *             quantized per head in blocks of 128 tokens over all D channels.
+ *   causal    key j is visible from query i when j <= i.
+ *
+ * Tensors: q, k, v, o, dout, dq, dk, dv are bf16, contiguous [B][H][N][D],
+ * 16-byte aligned, on the current device; lse is float [B][H][N], 4-byte
+ * aligned.  D is 64 or 128; N >= 0 (N = 0 or B*H = 0 is a successful no-op).
+ * scale is the softmax scale (positive, finite).
+ *
+ * Workspace: caller-owned device memory of sagebwd_workspace_bytes(B, H, N, D)
+ * bytes, 256-byte aligned.  sagebwd_fwd writes the quantized Q, K, V there;
+ * sagebwd_bwd reads them back (with the forward's o and lse) and uses the rest
+ * as scratch, so the same workspace, untouched in between, must be passed to
+ * the backward of the same forward.  Calls on one workspace must be ordered
+ * (one stream, or events); the library allocates nothing.
+ *
+ * Errors: return values are the SAGE_FP4_* codes of sage_fp4.h.  Argument
+ * errors (SAGE_FP4_EINVAL) are found before anything touches the device;
+ * SAGE_FP4_EUNSUPPORTED on a device other than sm_103; SAGE_FP4_ECUDA when a
+ * launch fails.  The kernels run asynchronously on `stream` (a cudaStream_t,
+ * NULL for the legacy default stream); a copy that never completes makes the
+ * kernels give up after 1.5 s and record SAGE_FP4_ETIMEOUT in the
+ * workspace's status word, which sagebwd_get_status reads.
+ */
+#ifndef SAGEBWD_H
+#define SAGEBWD_H
+
+#include <stddef.h>
+
+#include "sage_fp4.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Number of regions in the workspace (see sagebwd_workspace_layout). */
+#define SAGEBWD_WS_FIELDS 16
+
+/* Bytes of workspace for these sizes; 0 when the sizes are invalid. */
+size_t sagebwd_workspace_bytes(int B, int H, int N, int D);
+
+/* Byte offsets of the workspace's regions, in this order: Q^ row tiles, Q^
+ * transposed tiles, K^ row tiles, K^ transposed tiles, V^ transposed tiles,
+ * dO^ transposed tiles, V FP16 tiles, dO FP16 tiles, Q/K/V/dO scales (four
+ * regions, float [B*H][ceil(N/128)]), L (log2 units) and D (float
+ * [B*H][N padded to 128]), the dQ accumulator, the status word.  For tests
+ * and inspection; offsets must hold SAGEBWD_WS_FIELDS values. */
+int sagebwd_workspace_layout(int B, int H, int N, int D, size_t *offsets);
+
+/* Forward: quantizes q, k, v into the workspace and writes o (bf16) and lse
+ * (natural-log log-sum-exp of scale * S per row). */
+int sagebwd_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int D,
+                int causal, float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward: given dout and the forward's o and lse (and its workspace),
+ * writes dq, dk, dv (bf16). */
+int sagebwd_bwd(const void *dout, const void *o, const float *lse, void *dq, void *dk, void *dv, int B, int H,
+                int N, int D, int causal, float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronizes `stream`, returns the workspace's status word (0 or a
+ * negative SAGE_FP4_* code) and clears it. */
+int sagebwd_get_status(void *workspace, int B, int H, int N, int D, void *stream);
+
+/* Throughput probe of the two warp-level MMA forms the kernels use, on
+ * register operands (the roofline's denominators): kind 0 INT8 m16n8k32,
+ * kind 1 FP16 m16n8k16 with FP32 accumulation.  Each of `ctas` CTAs of 256
+ * threads runs iters x 8 MMAs per warp; scratch is 4 device bytes it may
+ * write. */
+int sagebwd_mma_peak(int kind, int ctas, int iters, void *scratch, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
