@@ -4,26 +4,32 @@
 // and one difficulty", difficulty 3; abstract of "SageAttention3: Microscaling
 // FP4 Attention for Inference and An Exploration of 8-Bit Training").
 //
-// Six of the seven products run on the INT8 tensor path (mma.sync m16n8k32,
-// exact s32 accumulation): S = Q K^T (forward, and again in the backward),
-// O = P V, dV = P^T dO, dQ = dS K, dK = dS^T Q.  dP = dO V^T, the product
-// that forms the attention-map gradient, runs in FP16 (mma.sync m16n8k16,
-// FP32 accumulation).  Quantization: Q, K, V, dO per head in blocks of 128
-// tokens, P and dS per block of 64 queries x 128 keys, scale amax / 127, codes
+// Six of the seven products take INT8 operands: S = Q K^T (forward, and again
+// in the backward), O = P V, dV = P^T dO, dQ = dS K, dK = dS^T Q.  dP = dO V^T,
+// the product that forms the attention-map gradient, takes FP16 operands.
+// Quantization: Q, K, V, dO per head in blocks of 128 tokens, P and dS per
+// block of 64 queries x 128 keys, scale amax / 127, codes
 // rint(x * (127 / amax)).  The forward is FlashAttention's online softmax
 // (P~ = exp(S - running max) quantized per block, the normaliser summed from
 // the unquantized P~); the backward recomputes P = exp(S - L) from the saved
-// log-sum-exp.  (sm_103a has no INT8 form of tcgen05.mma, so the warp-level
-// INT8 MMA is the tensor path here.)
+// log-sum-exp.
 //
-// Layout.  Every quantized operand is written by the quantizer kernels as
-// tiles that are contiguous in global memory (one bulk copy each) and
-// already swizzled for conflict-free ldmatrix (16-byte chunks XOR-permuted by
-// row).  Transposed tiles ([D][tokens]) hold the tokens of each 32-token
-// chunk in the order in which a thread's MMA accumulator values become its A
-// fragment for the next product (pi32 below), so P and dS go from one MMA to
-// the next without a shuffle; dQ's key order (rho32) lets each thread stage
-// its dS codes with 16-bit stores.
+// The INT8 products on sm_103a.  This GPU has no INT8 form of tcgen05.mma,
+// and its warp-level INT8 MMA (m16n8k32) runs at a quarter of the FP16 one
+// (m16n8k16, FP32 accumulation).  An INT8 code is an integer in [-127, 127],
+// exact in FP16; the product of two is exact in FP32, and so is every sum of
+// such products below 2^24 (127^2 * 128 < 2^21 here).  So the six INT8
+// products run on the FP16 MMA with the codes stored as FP16 values, and give
+// the integer results an INT8 MMA would (sagebwd_int_mma_probe checks this on
+// the hardware).  Each block's integer sum is then scaled by its two block
+// scales in FP32.
+//
+// Layout.  Every operand lives in the workspace as FP16 rows [token][D] whose
+// 16-byte chunks are XOR-permuted by (row & 7): any 8-row-aligned run of rows
+// is a bank-conflict-free shared-memory tile for ldmatrix after one bulk copy.
+// Operands needed transposed are read with ldmatrix.trans, and an MMA's FP32
+// accumulator fragment is, pairwise converted, the A fragment of the next MMA,
+// so no operand is stored twice.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -51,24 +57,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // ---------------------------------------------------------------- layout
-// Byte offset of logical (row, byte) in a tile of rows W bytes wide.  The
-// 16-byte chunk index is XORed with a function of the row so that the eight
-// rows one ldmatrix reads at the same logical chunk fall in eight different
-// bank groups.
+// Byte offset of logical (row, byte) in rows W bytes wide (W = 2D: 128 or
+// 256): the 16-byte chunk index is XORed with row & 7, so the eight rows one
+// ldmatrix reads at the same logical chunk fall in eight bank groups.
 __host__ __device__ __forceinline__ int swz(int row, int byte, int W) {
-  const int sw = (W == 64) ? ((row >> 1) & 3) : (row & 7);
-  return row * W + ((((byte >> 4) ^ sw)) << 4) + (byte & 15);
+  return row * W + ((((byte >> 4) ^ (row & 7))) << 4) + (byte & 15);
 }
-
-// Stored position k (0..31) of a 32-token chunk -> token offset in the chunk.
-// Positions 4t..4t+3 hold tokens 2t, 2t+1, 8+2t, 9+2t (and +16 for the upper
-// half): the accumulator columns that thread t of each quad holds in the two
-// n8 blocks of the previous MMA.
-__host__ __device__ __forceinline__ int pi32(int k) {
-  return (k & 16) | (((k >> 1) & 1) << 3) | (((k >> 2) & 3) << 1) | (k & 1);
-}
-// dQ's key order: position 16u + 2g + h holds key 16u + g + 8h.
-__host__ __device__ __forceinline__ int rho32(int k) { return (k & 16) | ((k >> 1) & 7) | ((k & 1) << 3); }
 
 // ---------------------------------------------------------------- helpers
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -76,13 +70,10 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-
-__device__ __forceinline__ void mma_s8(int (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
 }
 
 __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -93,19 +84,25 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], u
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// rint(x) saturated to [-128, 127], as an int (its low byte is the s8 code).
-__device__ __forceinline__ int cvt_s8(float x) {
-  int r;
-  asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(r) : "f"(x));
+__device__ __forceinline__ void mma_s8(int (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two floats -> FP16x2 (lo in the low half), rounded to nearest; exact for
+// the integer codes.
+__device__ __forceinline__ uint32_t h2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 
-// Low bytes of four ints -> one register, byte 0 from a.
-__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d) {
-  const uint32_t lo = __byte_perm(static_cast<uint32_t>(a), static_cast<uint32_t>(b), 0x0040);
-  const uint32_t hi = __byte_perm(static_cast<uint32_t>(c), static_cast<uint32_t>(d), 0x0040);
-  return __byte_perm(lo, hi, 0x5410);
-}
+// INT8 code of x in a block with 127 / amax = inv: rint(x * inv) as a float
+// (|x| <= amax keeps it within [-127, 127]).
+__device__ __forceinline__ float code(float x, float inv) { return rintf(__fmul_rn(x, inv)); }
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -127,13 +124,17 @@ __device__ __forceinline__ void red_add_v2(float* p, float a, float b) {
   asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
 }
 
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 struct Ctl {
   int32_t* status;
   uint64_t limit;
 };
 
 // Bounded wait by a whole warp for an mbarrier phase.  False: the copy never
-// completed; the status word holds SAGEBWD_ETIMEOUT.
+// completed; the status word holds SAGE_FP4_ETIMEOUT.
 __device__ __forceinline__ bool waitw(uint32_t bar, uint32_t parity, const Ctl& c) {
   if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -158,7 +159,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 
 __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 
-// bf16 -> FP16 bits, rounded to nearest even, saturated to +-65504.
+// -> FP16 bits, rounded to nearest even, saturated to +-65504.
 __device__ __forceinline__ uint16_t f2h_sat(float x) {
   x = fminf(fmaxf(x, -65504.0f), 65504.0f);
   return __half_as_ushort(__float2half_rn(x));
@@ -166,18 +167,16 @@ __device__ __forceinline__ uint16_t f2h_sat(float x) {
 
 // ---------------------------------------------------------------- workspace
 struct Ws {
-  int8_t *qr, *qt, *kr, *kt, *vt, *dot;
-  uint16_t *vh, *doh;
+  uint16_t *qc, *kc, *vc, *doc;  // INT8 codes as FP16 values, swizzled rows
+  uint16_t *vh, *doh;            // V and dO as FP16 values, swizzled rows
   float *sq, *sk, *sv, *sdo, *l2, *dd, *dqacc;
   int32_t* status;
 };
 
 // ---------------------------------------------------------------- quantizer
-// One CTA per (128-token block, head).  kind 0: Q (row tiles [64][D] and
-// transposed tiles [D][64]); 1: K ([128][D] and [D][128] in dQ's key order);
-// 2: V ([D][128] and FP16 [128][D]); 3: dO ([D][64] and FP16 [64][D]), with
-// D_i = sum_d dO_id O_id, the log2-domain log-sum-exp, and dQ's accumulator
-// rows zeroed.
+// One CTA per (128-token block, head).  kind 0: Q, 1: K, 2: V (codes and the
+// FP16 values), 3: dO (codes and FP16 values), with D_i = sum_d dO_id O_id,
+// the log2-domain log-sum-exp, and dQ's accumulator rows zeroed.
 template <int D>
 __global__ void __launch_bounds__(kThreads) quant_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                                                          const uint16_t* __restrict__ v, const uint16_t* __restrict__ o,
@@ -190,7 +189,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const uint16_t* __restr
   const int Np = nb * kTok;
   const int n0 = blk * kTok;
   const int rows = min(kTok, N - n0);
-  const uint16_t* x = (kind == 0 ? q : kind == 1 ? k : kind == 2 ? v : q) + (static_cast<size_t>(bh) * N + n0) * D;
+  const uint16_t* x = (kind == 1 ? k : kind == 2 ? v : q) + (static_cast<size_t>(bh) * N + n0) * D;
   const int tid = threadIdx.x;
 
   // load the block (zeros past N) and find its largest magnitude
@@ -215,74 +214,30 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const uint16_t* __restr
 #pragma unroll
   for (int w = 1; w < kThreads / 32; w++) amax = fmaxf(amax, red[w]);
   const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
-  const float sc = __fdiv_rn(amax, 127.0f);
-  const size_t hb = static_cast<size_t>(bh) * Np * D;  // this head's first byte of a code array
+  const size_t hb = static_cast<size_t>(bh) * Np * D;  // this head's first element
   if (tid == 0) {
     float* s = kind == 0 ? ws.sq : kind == 1 ? ws.sk : kind == 2 ? ws.sv : ws.sdo;
-    s[static_cast<size_t>(bh) * nb + blk] = sc;
+    s[static_cast<size_t>(bh) * nb + blk] = __fdiv_rn(amax, 127.0f);
   }
-  auto code = [&](int r, int d) { return cvt_s8(__fmul_rn(bf2f(xs[r * D + d]), inv)); };
-
-  // row-major INT8 tiles of T tokens: [T][D], one 16-byte chunk per step
-  auto rows_out = [&](int8_t* dst, int T) {
-    for (int i = tid; i < kTok * D / 16; i += kThreads) {
-      const int r = i / (D / 16), c = i % (D / 16);
-      int b[16];
+  uint16_t* codes = kind == 0 ? ws.qc : kind == 1 ? ws.kc : kind == 2 ? ws.vc : ws.doc;
+  uint16_t* vals = kind == 2 ? ws.vh : ws.doh;
+  char* cbase = reinterpret_cast<char*>(codes + hb + static_cast<size_t>(n0) * D);
+  char* vbase = reinterpret_cast<char*>(vals + hb + static_cast<size_t>(n0) * D);
+  // one 16-byte chunk (8 channels of one row) per step
+  for (int i = tid; i < kTok * D / 8; i += kThreads) {
+    const int r = i / (D / 8), c = i % (D / 8);
+    uint32_t hc[4], hv[4];
 #pragma unroll
-      for (int j = 0; j < 16; j++) b[j] = code(r, 16 * c + j);
-      uint4 out = make_uint4(pack4(b[0], b[1], b[2], b[3]), pack4(b[4], b[5], b[6], b[7]),
-                             pack4(b[8], b[9], b[10], b[11]), pack4(b[12], b[13], b[14], b[15]));
-      const size_t tile = (n0 + r) / T;
-      *reinterpret_cast<uint4*>(dst + hb + tile * T * D + swz(r % T, 16 * c, D)) = out;
+    for (int j = 0; j < 4; j++) {
+      const float a = bf2f(xs[r * D + 8 * c + 2 * j]), b = bf2f(xs[r * D + 8 * c + 2 * j + 1]);
+      hc[j] = h2(code(a, inv), code(b, inv));
+      hv[j] = static_cast<uint32_t>(f2h_sat(a)) | (static_cast<uint32_t>(f2h_sat(b)) << 16);
     }
-  };
-  // transposed INT8 tiles of T tokens: [D][T], tokens of each 32-chunk in the
-  // order perm (pi32 or rho32)
-  auto cols_out = [&](int8_t* dst, int T, bool rho) {
-    constexpr int kChunks = kTok / 16;
-    for (int i = tid; i < D * kChunks; i += kThreads) {
-      const int d = i % D, c = i / D;  // consecutive threads: consecutive d
-      const int t0 = 16 * c;           // first stored position in the 128-token block
-      int b[16];
-#pragma unroll
-      for (int j = 0; j < 16; j++) {
-        const int p = t0 + j;
-        const int tok = (p & ~31) | (rho ? rho32(p & 31) : pi32(p & 31));
-        b[j] = code(tok, d);
-      }
-      uint4 out = make_uint4(pack4(b[0], b[1], b[2], b[3]), pack4(b[4], b[5], b[6], b[7]),
-                             pack4(b[8], b[9], b[10], b[11]), pack4(b[12], b[13], b[14], b[15]));
-      const int tile = (n0 + t0) / T, within = (n0 + t0) % T;
-      *reinterpret_cast<uint4*>(dst + hb + static_cast<size_t>(tile) * T * D + swz(d, within, T)) = out;
-    }
-  };
-  // row-major FP16 tiles of T tokens: [T][D] halves, rows 2D bytes wide
-  auto half_out = [&](uint16_t* dst, int T) {
-    for (int i = tid; i < kTok * D / 8; i += kThreads) {
-      const int r = i / (D / 8), c = i % (D / 8);
-      uint32_t h[4];
-#pragma unroll
-      for (int j = 0; j < 4; j++)
-        h[j] = static_cast<uint32_t>(f2h_sat(bf2f(xs[r * D + 8 * c + 2 * j]))) |
-               (static_cast<uint32_t>(f2h_sat(bf2f(xs[r * D + 8 * c + 2 * j + 1]))) << 16);
-      const size_t tile = (n0 + r) / T;
-      char* base = reinterpret_cast<char*>(dst + hb + tile * T * D);
-      *reinterpret_cast<uint4*>(base + swz(r % T, 16 * c, 2 * D)) = make_uint4(h[0], h[1], h[2], h[3]);
-    }
-  };
-
-  if (kind == 0) {
-    rows_out(ws.qr, kQ);
-    cols_out(ws.qt, kQ, false);
-  } else if (kind == 1) {
-    rows_out(ws.kr, kTok);
-    cols_out(ws.kt, kTok, true);
-  } else if (kind == 2) {
-    cols_out(ws.vt, kTok, false);
-    half_out(ws.vh, kTok);
-  } else {
-    cols_out(ws.dot, kQ, false);
-    half_out(ws.doh, kQ);
+    const int off = swz(r, 16 * c, 2 * D);
+    *reinterpret_cast<uint4*>(cbase + off) = make_uint4(hc[0], hc[1], hc[2], hc[3]);
+    if (kind >= 2) *reinterpret_cast<uint4*>(vbase + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+  }
+  if (kind == 3) {
     // D_i = sum_d dO_id O_id and L in log2 units: one warp per row
     const int warp = tid >> 5, lane = tid & 31;
     for (int r = warp; r < kTok; r += kThreads / 32) {
@@ -307,15 +262,15 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const uint16_t* __restr
 // ---------------------------------------------------------------- forward
 // One CTA of 8 warps per (128 queries, head).  Warp w owns query rows
 // 16w..16w+15; warps 0-3 and 4-7 form the two 64-query P blocks.  Key tiles
-// of 128 (K^ row tile and V^ transposed tile) stream through two stages of
-// shared memory by bulk copy.
+// of 128 (K^ and V^ codes) stream through two shared-memory stages by bulk
+// copy.
 template <int D>
 struct FwdSmem {
-  static constexpr int kQBytes = 2 * kQ * D;
-  static constexpr int kKBytes = kTok * D;
-  static constexpr int kStage = 2 * kKBytes;
+  static constexpr int kRow = 2 * D;         // bytes per FP16 row
+  static constexpr int kTile = kTok * kRow;  // one 128-row tile
   static constexpr int kQOff = 0;
-  static constexpr int kStageOff = kQBytes;
+  static constexpr int kStageOff = kTile;
+  static constexpr int kStage = 2 * kTile;                // K^ then V^
   static constexpr int kBarOff = kStageOff + 2 * kStage;  // 3 mbarriers: q, full[2]
   static constexpr int kRedOff = kBarOff + 64;            // [2][8] floats
   static constexpr int kBytes = kRedOff + 2 * 8 * 4;
@@ -332,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qt = kCausal ? (nqt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
   const int bh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
+  const int g = lane >> 2, t = lane & 3, j = lane >> 3;
   const int grp = warp >> 2;
   const uint32_t sbase = smem_addr(smem);
   const uint32_t qbar = sbase + L::kBarOff, full0 = qbar + 8;
@@ -352,32 +307,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int s = kt & 1;
     const uint32_t st = sbase + L::kStageOff + s * L::kStage;
     mbar_arrive_expect_tx(full0 + 8 * s, L::kStage);
-    bulk_load(st, ws.kr + hb + static_cast<size_t>(kt) * kTok * D, L::kKBytes, full0 + 8 * s);
-    bulk_load(st + L::kKBytes, ws.vt + hb + static_cast<size_t>(kt) * kTok * D, L::kKBytes, full0 + 8 * s);
+    bulk_load(st, ws.kc + hb + static_cast<size_t>(kt) * kTok * D, L::kTile, full0 + 8 * s);
+    bulk_load(st + L::kTile, ws.vc + hb + static_cast<size_t>(kt) * kTok * D, L::kTile, full0 + 8 * s);
   };
   int issued = 0;  // key tiles whose copies thread 0 has issued
   if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(qbar, L::kQBytes);
-    bulk_load(sbase + L::kQOff, ws.qr + hb + static_cast<size_t>(qt) * kTok * D, L::kQBytes, qbar);
+    mbar_arrive_expect_tx(qbar, L::kTile);
+    bulk_load(sbase + L::kQOff, ws.qc + hb + static_cast<size_t>(qt) * kTok * D, L::kTile, qbar);
     for (; issued < 2 && issued < nkt; issued++) issue_tile(issued);
   }
   // every wait's outcome is voted on by the whole CTA, so that all warps
   // carry on or all give up together
   bool ok = __syncthreads_and(waitw(qbar, 0, ctl));
 
-  // Q^ fragments of this warp's 16 rows (A operand of S = Q K^T)
-  uint32_t qa[D / 32][4];
-  {
-    const int j = lane >> 3;
-    const int r = 16 * (warp & 3) + ((j & 1) << 3) + (lane & 7);
-    const uint32_t tq = sbase + L::kQOff + grp * kQ * D;
-#pragma unroll
-    for (int kc = 0; kc < D / 32; kc++)
-      ldsm_x4(tq + swz(r, 32 * kc + ((j >> 1) << 4), D), qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3]);
-  }
   const float sqk = ws.sq[static_cast<size_t>(bh) * nqt + qt] * scale_log2e;
   const int row0 = qt * kTok + 16 * warp + g;  // this thread's rows: row0, row0 + 8
   const bool valid0 = row0 < N, valid1 = row0 + 8 < N;
+  const uint32_t qrow = sbase + L::kQOff;
+  const int arow = 16 * warp + ((j & 1) << 3) + (lane & 7);  // A-fragment row this lane addresses
 
   float o[D / 8][4];
 #pragma unroll
@@ -386,39 +333,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   for (int kt = 0; kt < nkt && ok; kt++) {
     const int s = kt & 1;
-    const uint32_t kst = sbase + L::kStageOff + s * L::kStage, vst = kst + L::kKBytes;
+    const uint32_t kst = sbase + L::kStageOff + s * L::kStage, vst = kst + L::kTile;
     ok = __syncthreads_and(waitw(full0 + 8 * s, (kt >> 1) & 1, ctl));
     if (!ok) break;
     // every warp is done with tile kt - 1: its stage takes tile kt + 1
     if (threadIdx.x == 0 && kt >= 1 && kt + 1 < nkt) issue_tile(issued++);
-    // S = Q^ K^^T for 16 rows x 128 keys
-    int sacc[16][4];
+    // S = Q^ K^^T for 16 rows x 128 keys (integer sums in FP32)
+    float x[16][4];
 #pragma unroll
-    for (int nb = 0; nb < 16; nb++) sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0;
-    {
-      const int j = lane >> 3;
+    for (int nb = 0; nb < 16; nb++) x[nb][0] = x[nb][1] = x[nb][2] = x[nb][3] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ks++) {
+      uint32_t qa[4];
+      ldsm_x4(qrow + swz(arow, 32 * ks + ((j >> 1) << 4), L::kRow), qa[0], qa[1], qa[2], qa[3]);
 #pragma unroll
       for (int nb = 0; nb < 16; nb += 2) {
-        const int key = 8 * (nb + (j >> 1)) + (lane & 7);
-#pragma unroll
-        for (int kc = 0; kc < D / 32; kc++) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kst + swz(key, 32 * kc + ((j & 1) << 4), D), b0, b1, b2, b3);
-          mma_s8(sacc[nb], qa[kc], b0, b1);
-          mma_s8(sacc[nb + 1], qa[kc], b2, b3);
-        }
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kst + swz(8 * (nb + (j >> 1)) + (lane & 7), 32 * ks + ((j & 1) << 4), L::kRow), b0, b1, b2, b3);
+        mma_f16(x[nb], qa, b0, b1);
+        mma_f16(x[nb + 1], qa, b2, b3);
       }
     }
     // scale to log2 units, mask, row maxima
     const float c2 = sqk * ws.sk[static_cast<size_t>(bh) * nqt + kt];
     const bool edge = (kCausal && kt == qt) || (kt == nqt - 1 && (N % kTok) != 0);
-    float x[16][4];
     float tm0 = -INFINITY, tm1 = -INFINITY;
 #pragma unroll
     for (int nb = 0; nb < 16; nb++) {
 #pragma unroll
       for (int e = 0; e < 4; e++) {
-        float v = static_cast<float>(sacc[nb][e]) * c2;
+        float v = x[nb][e] * c2;
         if (edge) {
           const int key = kt * kTok + 8 * nb + 2 * t + (e & 1);
           const int row = row0 + ((e >> 1) << 3);
@@ -460,42 +404,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = 1; w < 4; w++) amax = fmaxf(amax, redp[s * 8 + 4 * grp + w]);
     const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
     const float spv = __fdiv_rn(amax, 127.0f) * ws.sv[static_cast<size_t>(bh) * nqt + kt];
-    // P^ codes as A fragments (keys in pi32 order)
-    uint32_t pa[4][4];
+    // P^ codes: the accumulator fragments of n-blocks 2kc, 2kc+1 are the A
+    // fragment of k-step kc
+    uint32_t pa[8][4];
 #pragma unroll
-    for (int kc = 0; kc < 4; kc++) {
-      const int b = 4 * kc;
+    for (int kc = 0; kc < 8; kc++) {
+      pa[kc][0] = h2(code(x[2 * kc][0], inv), code(x[2 * kc][1], inv));
+      pa[kc][1] = h2(code(x[2 * kc][2], inv), code(x[2 * kc][3], inv));
+      pa[kc][2] = h2(code(x[2 * kc + 1][0], inv), code(x[2 * kc + 1][1], inv));
+      pa[kc][3] = h2(code(x[2 * kc + 1][2], inv), code(x[2 * kc + 1][3], inv));
+    }
+    // O = O * alpha + s_P s_V (P^ V^); V^ read transposed by ldmatrix.trans
+#pragma unroll
+    for (int nd = 0; nd < D / 8; nd += 2) {
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kc = 0; kc < 8; kc++) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vst + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 16 * (nd + (j >> 1)), L::kRow), b0, b1, b2, b3);
+        mma_f16(acc[0], pa[kc], b0, b1);
+        mma_f16(acc[1], pa[kc], b2, b3);
+      }
 #pragma unroll
       for (int h = 0; h < 2; h++) {
-        pa[kc][2 * h + 0] = pack4(cvt_s8(__fmul_rn(x[b + 2 * h][0], inv)), cvt_s8(__fmul_rn(x[b + 2 * h][1], inv)),
-                                  cvt_s8(__fmul_rn(x[b + 2 * h + 1][0], inv)),
-                                  cvt_s8(__fmul_rn(x[b + 2 * h + 1][1], inv)));
-        pa[kc][2 * h + 1] = pack4(cvt_s8(__fmul_rn(x[b + 2 * h][2], inv)), cvt_s8(__fmul_rn(x[b + 2 * h][3], inv)),
-                                  cvt_s8(__fmul_rn(x[b + 2 * h + 1][2], inv)),
-                                  cvt_s8(__fmul_rn(x[b + 2 * h + 1][3], inv)));
-      }
-    }
-    // O = O * alpha + s_P s_V (P^ V^)
-    {
-      const int j = lane >> 3;
-#pragma unroll
-      for (int nd = 0; nd < D / 8; nd += 2) {
-        int acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
-        const int drow = 8 * (nd + (j >> 1)) + (lane & 7);
-#pragma unroll
-        for (int kc = 0; kc < 4; kc++) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(vst + swz(drow, 32 * kc + ((j & 1) << 4), kTok), b0, b1, b2, b3);
-          mma_s8(acc[0], pa[kc], b0, b1);
-          mma_s8(acc[1], pa[kc], b2, b3);
-        }
-#pragma unroll
-        for (int h = 0; h < 2; h++) {
-          o[nd + h][0] = fmaf(static_cast<float>(acc[h][0]), spv, o[nd + h][0] * al0);
-          o[nd + h][1] = fmaf(static_cast<float>(acc[h][1]), spv, o[nd + h][1] * al0);
-          o[nd + h][2] = fmaf(static_cast<float>(acc[h][2]), spv, o[nd + h][2] * al1);
-          o[nd + h][3] = fmaf(static_cast<float>(acc[h][3]), spv, o[nd + h][3] * al1);
-        }
+        o[nd + h][0] = fmaf(acc[h][0], spv, o[nd + h][0] * al0);
+        o[nd + h][1] = fmaf(acc[h][1], spv, o[nd + h][1] * al0);
+        o[nd + h][2] = fmaf(acc[h][2], spv, o[nd + h][2] * al1);
+        o[nd + h][3] = fmaf(acc[h][3], spv, o[nd + h][3] * al1);
       }
     }
   }
@@ -520,14 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
   for (int nd = 0; nd < D / 8; nd++) {
     const int d = 8 * nd + 2 * t;
-    if (valid0) {
-      __nv_bfloat162 v = __floats2bfloat162_rn(o[nd][0] * il0, o[nd][1] * il0);
-      *reinterpret_cast<__nv_bfloat162*>(orow0 + d) = v;
-    }
-    if (valid1) {
-      __nv_bfloat162 v = __floats2bfloat162_rn(o[nd][2] * il1, o[nd][3] * il1);
-      *reinterpret_cast<__nv_bfloat162*>(orow1 + d) = v;
-    }
+    if (valid0) *reinterpret_cast<__nv_bfloat162*>(orow0 + d) = __floats2bfloat162_rn(o[nd][0] * il0, o[nd][1] * il0);
+    if (valid1) *reinterpret_cast<__nv_bfloat162*>(orow1 + d) = __floats2bfloat162_rn(o[nd][2] * il1, o[nd][3] * il1);
   }
   if (t == 0) {
     if (valid0) lse[static_cast<size_t>(bh) * N + row0] = (m0 + __log2f(l0)) * kLn2;
@@ -537,25 +466,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- backward
 // One CTA of 8 warps per (128 keys, head); warp w owns keys 16w..16w+15.  The
-// CTA's K^ (row and dQ-ordered transposed tiles) and FP16 V stay in shared
-// memory; query tiles of 64 (Q^ row and transposed tiles, dO^ transposed
-// tile, FP16 dO, L and D) stream through two stages.  Per query tile: S^T,
-// P^T, dV += P^^T dO^, dP^T (FP16), dS^T, dK += dS^^T Q^, and this key
-// tile's share of dQ = dS^ K^ added to an FP32 accumulator with vector
+// CTA's K^ codes and FP16 V stay in shared memory; query tiles of 64 (Q^ and
+// dO^ codes, FP16 dO, L and D) stream through two stages.  Per query tile:
+// S^T, P^T, dV += P^^T dO^, dP^T (FP16), dS^T, dK += dS^^T Q^, and this key
+// tile's share of dQ = dS^ K^, added to an FP32 accumulator with vector
 // reductions.
 template <int D>
 struct BwdSmem {
-  static constexpr int kKr = 0;
-  static constexpr int kKt = kKr + kTok * D;
-  static constexpr int kVh = kKt + kTok * D;
-  static constexpr int kFixedBytes = 2 * kTok * D + 2 * kTok * D;
-  static constexpr int kQr = 0, kQt = kQr + kQ * D, kDot = kQt + kQ * D, kDoh = kDot + kQ * D;
-  static constexpr int kL = kDoh + 2 * kQ * D, kDd = kL + 4 * kQ;
+  static constexpr int kRow = 2 * D;
+  static constexpr int kKc = 0;
+  static constexpr int kVh = kKc + kTok * kRow;
+  static constexpr int kFixedBytes = 2 * kTok * kRow;
+  static constexpr int kQc = 0, kDoc = kQc + kQ * kRow, kDoh = kDoc + kQ * kRow;
+  static constexpr int kL = kDoh + kQ * kRow, kDd = kL + 4 * kQ;
   static constexpr int kStage = kDd + 4 * kQ;
   static constexpr int kStageOff = kFixedBytes;
-  static constexpr int kDs = kStageOff + 2 * kStage;  // staged dS^ codes [64][128]
-  static constexpr int kBarOff = kDs + kQ * kTok;     // fixed, full[2]
-  static constexpr int kRedOff = kBarOff + 64;        // [2 kinds][8] floats
+  static constexpr int kDs = kStageOff + 2 * kStage;   // staged dS^ codes, [128 keys][64 queries] FP16
+  static constexpr int kBarOff = kDs + kTok * kQ * 2;  // fixed, full[2]
+  static constexpr int kRedOff = kBarOff + 64;         // [2 kinds][8] floats
   static constexpr int kBytes = kRedOff + 2 * 8 * 4;
 };
 
@@ -584,10 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t st = sbase + L::kStageOff + s * L::kStage, bar = full0 + 8 * s;
     mbar_arrive_expect_tx(bar, L::kStage);
     const size_t off = hb + static_cast<size_t>(qtile) * kQ * D;
-    bulk_load(st + L::kQr, ws.qr + off, kQ * D, bar);
-    bulk_load(st + L::kQt, ws.qt + off, kQ * D, bar);
-    bulk_load(st + L::kDot, ws.dot + off, kQ * D, bar);
-    bulk_load(st + L::kDoh, ws.doh + off, 2 * kQ * D, bar);
+    bulk_load(st + L::kQc, ws.qc + off, kQ * L::kRow, bar);
+    bulk_load(st + L::kDoc, ws.doc + off, kQ * L::kRow, bar);
+    bulk_load(st + L::kDoh, ws.doh + off, kQ * L::kRow, bar);
     bulk_load(st + L::kL, ws.l2 + hrow + static_cast<size_t>(qtile) * kQ, 4 * kQ, bar);
     bulk_load(st + L::kDd, ws.dd + hrow + static_cast<size_t>(qtile) * kQ, 4 * kQ, bar);
   };
@@ -602,9 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(fbar, L::kFixedBytes);
     const size_t off = hb + static_cast<size_t>(kb) * kTok * D;
-    bulk_load(sbase + L::kKr, ws.kr + off, kTok * D, fbar);
-    bulk_load(sbase + L::kKt, ws.kt + off, kTok * D, fbar);
-    bulk_load(sbase + L::kVh, ws.vh + off, 2 * kTok * D, fbar);
+    bulk_load(sbase + L::kKc, ws.kc + off, kTok * L::kRow, fbar);
+    bulk_load(sbase + L::kVh, ws.vh + off, kTok * L::kRow, fbar);
     for (; issued < 2 && issued < niter; issued++) issue_stage(issued);
   }
   // every wait's outcome is voted on by the whole CTA
@@ -613,6 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float sk = ws.sk[static_cast<size_t>(bh) * nkt + kb];
   const int key0 = kb * kTok + 16 * warp + g;  // this thread's keys: key0, key0 + 8
   const float c2base = sk * scale * kLog2e;
+  const int arow = 16 * warp + ((j & 1) << 3) + (lane & 7);  // A-fragment row (key) this lane addresses
+  const uint32_t dsb = sbase + L::kDs;
   float dka[D / 8][4], dva[D / 8][4];
 #pragma unroll
   for (int i = 0; i < D / 8; i++)
@@ -627,20 +555,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sq = ws.sq[static_cast<size_t>(bh) * nkt + (qtile >> 1)];
     const float sdo = ws.sdo[static_cast<size_t>(bh) * nkt + (qtile >> 1)];
     // S^T = K^ Q^^T: 16 keys x 64 queries
-    int sacc[8][4];
+    float p[8][4];
 #pragma unroll
-    for (int nb = 0; nb < 8; nb++) sacc[nb][0] = sacc[nb][1] = sacc[nb][2] = sacc[nb][3] = 0;
+    for (int nb = 0; nb < 8; nb++) p[nb][0] = p[nb][1] = p[nb][2] = p[nb][3] = 0.0f;
 #pragma unroll
-    for (int kc = 0; kc < D / 32; kc++) {
+    for (int ks = 0; ks < D / 16; ks++) {
       uint32_t ka[4];
-      ldsm_x4(sbase + L::kKr + swz(16 * warp + ((j & 1) << 3) + (lane & 7), 32 * kc + ((j >> 1) << 4), D), ka[0],
-              ka[1], ka[2], ka[3]);
+      ldsm_x4(sbase + L::kKc + swz(arow, 32 * ks + ((j >> 1) << 4), L::kRow), ka[0], ka[1], ka[2], ka[3]);
 #pragma unroll
       for (int nb = 0; nb < 8; nb += 2) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(st + L::kQr + swz(8 * (nb + (j >> 1)) + (lane & 7), 32 * kc + ((j & 1) << 4), D), b0, b1, b2, b3);
-        mma_s8(sacc[nb], ka, b0, b1);
-        mma_s8(sacc[nb + 1], ka, b2, b3);
+        ldsm_x4(st + L::kQc + swz(8 * (nb + (j >> 1)) + (lane & 7), 32 * ks + ((j & 1) << 4), L::kRow), b0, b1, b2,
+                b3);
+        mma_f16(p[nb], ka, b0, b1);
+        mma_f16(p[nb + 1], ka, b2, b3);
       }
     }
     // P^T = exp2(S^T c - L); masked and padded entries 0
@@ -648,7 +576,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* Ls = reinterpret_cast<const float*>(smem + (st - sbase) + L::kL);
     const float* Ds = reinterpret_cast<const float*>(smem + (st - sbase) + L::kDd);
     const bool edge = (kCausal && qtile <= 2 * kb + 1) || (qtile * kQ + kQ > N) || (kb * kTok + kTok > N);
-    float p[8][4];
     float pmax = 0.0f;
 #pragma unroll
     for (int nb = 0; nb < 8; nb++) {
@@ -656,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 lq = *reinterpret_cast<const float2*>(Ls + qc);
 #pragma unroll
       for (int e = 0; e < 4; e++) {
-        float v = ex2(fmaf(static_cast<float>(sacc[nb][e]), c2, -((e & 1) ? lq.y : lq.x)));
+        float v = ex2(fmaf(p[nb][e], c2, -((e & 1) ? lq.y : lq.x)));
         if (edge) {
           const int query = qtile * kQ + qc + (e & 1);
           const int key = key0 + ((e >> 1) << 3);
@@ -673,39 +600,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int w = 1; w < 8; w++) amax = fmaxf(amax, redp[w]);
     float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
-    // P^^T as A fragments (queries in pi32 order)
-    uint32_t pa[2][4];
+    // P^^T codes as A fragments (k = queries)
+    uint32_t pa[4][4];
 #pragma unroll
-    for (int kc = 0; kc < 2; kc++) {
-      const int b = 4 * kc;
-#pragma unroll
-      for (int h = 0; h < 2; h++) {
-        pa[kc][2 * h + 0] = pack4(cvt_s8(__fmul_rn(p[b + 2 * h][0], inv)), cvt_s8(__fmul_rn(p[b + 2 * h][1], inv)),
-                                  cvt_s8(__fmul_rn(p[b + 2 * h + 1][0], inv)),
-                                  cvt_s8(__fmul_rn(p[b + 2 * h + 1][1], inv)));
-        pa[kc][2 * h + 1] = pack4(cvt_s8(__fmul_rn(p[b + 2 * h][2], inv)), cvt_s8(__fmul_rn(p[b + 2 * h][3], inv)),
-                                  cvt_s8(__fmul_rn(p[b + 2 * h + 1][2], inv)),
-                                  cvt_s8(__fmul_rn(p[b + 2 * h + 1][3], inv)));
-      }
+    for (int kc = 0; kc < 4; kc++) {
+      pa[kc][0] = h2(code(p[2 * kc][0], inv), code(p[2 * kc][1], inv));
+      pa[kc][1] = h2(code(p[2 * kc][2], inv), code(p[2 * kc][3], inv));
+      pa[kc][2] = h2(code(p[2 * kc + 1][0], inv), code(p[2 * kc + 1][1], inv));
+      pa[kc][3] = h2(code(p[2 * kc + 1][2], inv), code(p[2 * kc + 1][3], inv));
     }
-    // dV += s_P s_dO (P^^T dO^)
+    // dV += s_P s_dO (P^^T dO^); dO^ read transposed
     {
       const float f = __fdiv_rn(amax, 127.0f) * sdo;
 #pragma unroll
       for (int nd = 0; nd < D / 8; nd += 2) {
-        int acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
-        const int drow = 8 * (nd + (j >> 1)) + (lane & 7);
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-        for (int kc = 0; kc < 2; kc++) {
+        for (int kc = 0; kc < 4; kc++) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(st + L::kDot + swz(drow, 32 * kc + ((j & 1) << 4), kQ), b0, b1, b2, b3);
-          mma_s8(acc[0], pa[kc], b0, b1);
-          mma_s8(acc[1], pa[kc], b2, b3);
+          ldsm_x4_t(st + L::kDoc + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 16 * (nd + (j >> 1)), L::kRow), b0,
+                    b1, b2, b3);
+          mma_f16(acc[0], pa[kc], b0, b1);
+          mma_f16(acc[1], pa[kc], b2, b3);
         }
 #pragma unroll
         for (int h = 0; h < 2; h++)
 #pragma unroll
-          for (int e = 0; e < 4; e++) dva[nd + h][e] = fmaf(static_cast<float>(acc[h][e]), f, dva[nd + h][e]);
+          for (int e = 0; e < 4; e++) dva[nd + h][e] = fmaf(acc[h][e], f, dva[nd + h][e]);
       }
     }
     // dP^T = V dO^T in FP16, then dS^T = P^T o (dP^T - D)
@@ -715,13 +636,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int ks = 0; ks < D / 16; ks++) {
       uint32_t va[4];
-      ldsm_x4(sbase + L::kVh + swz(16 * warp + ((j & 1) << 3) + (lane & 7), 32 * ks + ((j >> 1) << 4), 2 * D),
-              va[0], va[1], va[2], va[3]);
+      ldsm_x4(sbase + L::kVh + swz(arow, 32 * ks + ((j >> 1) << 4), L::kRow), va[0], va[1], va[2], va[3]);
 #pragma unroll
       for (int nb = 0; nb < 8; nb += 2) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(st + L::kDoh + swz(8 * (nb + (j >> 1)) + (lane & 7), 32 * ks + ((j & 1) << 4), 2 * D), b0, b1, b2,
-                b3);
+        ldsm_x4(st + L::kDoh + swz(8 * (nb + (j >> 1)) + (lane & 7), 32 * ks + ((j & 1) << 4), L::kRow), b0, b1,
+                b2, b3);
         mma_f16(dp[nb], va, b0, b1);
         mma_f16(dp[nb + 1], va, b2, b3);
       }
@@ -744,84 +664,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = 1; w < 8; w++) amax = fmaxf(amax, redp[8 + w]);
     inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
     const float sds = __fdiv_rn(amax, 127.0f);
-    // dS^ codes: A fragments for dK, and 16-bit stores in dQ's key order
-    int cd[8][4];
+    // dS^^T codes: A fragments for dK, and staged ([key][query]) for dQ
+    uint32_t da[4][4];
 #pragma unroll
-    for (int nb = 0; nb < 8; nb++)
-#pragma unroll
-      for (int e = 0; e < 4; e++) cd[nb][e] = cvt_s8(__fmul_rn(p[nb][e], inv));
-    {
-      uint8_t* dsb = smem + L::kDs;
-#pragma unroll
-      for (int nb = 0; nb < 8; nb++)
-#pragma unroll
-        for (int e = 0; e < 2; e++) {
-          const int row = 8 * nb + 2 * t + e;
-          const uint16_t v = static_cast<uint16_t>((cd[nb][e] & 0xff) | ((cd[nb][2 + e] & 0xff) << 8));
-          *reinterpret_cast<uint16_t*>(dsb + swz(row, 16 * warp + 2 * g, kTok)) = v;
-        }
+    for (int kc = 0; kc < 4; kc++) {
+      da[kc][0] = h2(code(p[2 * kc][0], inv), code(p[2 * kc][1], inv));
+      da[kc][1] = h2(code(p[2 * kc][2], inv), code(p[2 * kc][3], inv));
+      da[kc][2] = h2(code(p[2 * kc + 1][0], inv), code(p[2 * kc + 1][1], inv));
+      da[kc][3] = h2(code(p[2 * kc + 1][2], inv), code(p[2 * kc + 1][3], inv));
+      // rows key 16w+g and 16w+g+8; queries 16kc+2t (+1) and 16kc+8+2t (+1)
+      sts32(dsb + swz(16 * warp + g, 2 * (16 * kc + 2 * t), 2 * kQ), da[kc][0]);
+      sts32(dsb + swz(16 * warp + g + 8, 2 * (16 * kc + 2 * t), 2 * kQ), da[kc][1]);
+      sts32(dsb + swz(16 * warp + g, 2 * (16 * kc + 8 + 2 * t), 2 * kQ), da[kc][2]);
+      sts32(dsb + swz(16 * warp + g + 8, 2 * (16 * kc + 8 + 2 * t), 2 * kQ), da[kc][3]);
     }
-    uint32_t da[2][4];
-#pragma unroll
-    for (int kc = 0; kc < 2; kc++) {
-      const int b = 4 * kc;
-#pragma unroll
-      for (int h = 0; h < 2; h++) {
-        da[kc][2 * h + 0] = pack4(cd[b + 2 * h][0], cd[b + 2 * h][1], cd[b + 2 * h + 1][0], cd[b + 2 * h + 1][1]);
-        da[kc][2 * h + 1] = pack4(cd[b + 2 * h][2], cd[b + 2 * h][3], cd[b + 2 * h + 1][2], cd[b + 2 * h + 1][3]);
-      }
-    }
-    // dK += s_dS s_Q (dS^^T Q^)
+    // dK += s_dS s_Q (dS^^T Q^); Q^ read transposed
     {
       const float f = sds * sq;
 #pragma unroll
       for (int nd = 0; nd < D / 8; nd += 2) {
-        int acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
-        const int drow = 8 * (nd + (j >> 1)) + (lane & 7);
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-        for (int kc = 0; kc < 2; kc++) {
+        for (int kc = 0; kc < 4; kc++) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(st + L::kQt + swz(drow, 32 * kc + ((j & 1) << 4), kQ), b0, b1, b2, b3);
-          mma_s8(acc[0], da[kc], b0, b1);
-          mma_s8(acc[1], da[kc], b2, b3);
+          ldsm_x4_t(st + L::kQc + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 16 * (nd + (j >> 1)), L::kRow), b0, b1,
+                    b2, b3);
+          mma_f16(acc[0], da[kc], b0, b1);
+          mma_f16(acc[1], da[kc], b2, b3);
         }
 #pragma unroll
         for (int h = 0; h < 2; h++)
 #pragma unroll
-          for (int e = 0; e < 4; e++) dka[nd + h][e] = fmaf(static_cast<float>(acc[h][e]), f, dka[nd + h][e]);
+          for (int e = 0; e < 4; e++) dka[nd + h][e] = fmaf(acc[h][e], f, dka[nd + h][e]);
       }
     }
     // every warp's dS^ is staged and every warp is done with stage s
     __syncthreads();
     if (threadIdx.x == 0 && it + 2 < niter) issue_stage(issued++);
-    // dQ[64 x D] += scale s_dS s_K (dS^ K^): warp w takes rows 16 (w & 3) and
-    // half of the D columns
+    // dQ[64 x D] += scale s_dS s_K (dS^ K^): warp w takes query rows
+    // 16 (w & 3) and half of the D columns; dS^ and K^ read transposed
     {
       const float f = sds * sk * scale;
       const int r0 = 16 * (warp & 3);
       const int dh = (warp >> 2) * (D / 2);
-      int acc[D / 16][4];
+      float acc[D / 16][4];
 #pragma unroll
-      for (int i = 0; i < D / 16; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0;
+      for (int i = 0; i < D / 16; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
 #pragma unroll
-      for (int kc = 0; kc < 4; kc++) {
+      for (int kc = 0; kc < kTok / 16; kc++) {
         uint32_t a[4];
-        ldsm_x4(sbase + L::kDs + swz(r0 + ((j & 1) << 3) + (lane & 7), 32 * kc + ((j >> 1) << 4), kTok), a[0], a[1],
-                a[2], a[3]);
+        ldsm_x4_t(dsb + swz(16 * kc + ((j >> 1) << 3) + (lane & 7), 2 * (r0 + ((j & 1) << 3)), 2 * kQ), a[0], a[1],
+                  a[2], a[3]);
 #pragma unroll
         for (int nd = 0; nd < D / 16; nd += 2) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(sbase + L::kKt + swz(dh + 8 * (nd + (j >> 1)) + (lane & 7), 32 * kc + ((j & 1) << 4), kTok), b0,
-                  b1, b2, b3);
-          mma_s8(acc[nd], a, b0, b1);
-          mma_s8(acc[nd + 1], a, b2, b3);
+          ldsm_x4_t(sbase + L::kKc + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 2 * dh + 16 * (nd + (j >> 1)), L::kRow),
+                    b0, b1, b2, b3);
+          mma_f16(acc[nd], a, b0, b1);
+          mma_f16(acc[nd + 1], a, b2, b3);
         }
       }
       float* dq0 = ws.dqacc + (hrow + static_cast<size_t>(qtile) * kQ + r0 + g) * D + dh + 2 * t;
 #pragma unroll
       for (int nd = 0; nd < D / 16; nd++) {
-        red_add_v2(dq0 + 8 * nd, static_cast<float>(acc[nd][0]) * f, static_cast<float>(acc[nd][1]) * f);
-        red_add_v2(dq0 + 8 * D + 8 * nd, static_cast<float>(acc[nd][2]) * f, static_cast<float>(acc[nd][3]) * f);
+        red_add_v2(dq0 + 8 * nd, acc[nd][0] * f, acc[nd][1] * f);
+        red_add_v2(dq0 + 8 * D + 8 * nd, acc[nd][2] * f, acc[nd][3] * f);
       }
     }
   }
@@ -871,10 +778,35 @@ __global__ void __launch_bounds__(kThreads) dq_kernel(const float* __restrict__ 
   }
 }
 
-// ---------------------------------------------------------------- peak probe
-// Throughput of the two warp-level MMA forms this path uses, on register
-// operands: kind 0 INT8 m16n8k32, kind 1 FP16 m16n8k16 with FP32
-// accumulation.  Eight independent accumulators per warp.
+// ---------------------------------------------------------------- probes
+// Integer products on the FP16 MMA: one warp computes the 16 x 8 product of
+// INT8 matrices a [16][K] and b [8][K] (both row-major, K a multiple of 16)
+// with the codes as FP16 values and FP32 accumulation, chained over K / 16
+// MMAs like the kernels' sums, and writes it as float [16][8].
+__global__ void int_mma_probe_kernel(const int8_t* __restrict__ a, const int8_t* __restrict__ b, int K,
+                                     float* __restrict__ out) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int ks = 0; ks < K / 16; ks++) {
+    const int k0 = 16 * ks + 2 * t;
+    uint32_t fa[4];
+    fa[0] = h2(a[g * K + k0], a[g * K + k0 + 1]);
+    fa[1] = h2(a[(g + 8) * K + k0], a[(g + 8) * K + k0 + 1]);
+    fa[2] = h2(a[g * K + k0 + 8], a[g * K + k0 + 9]);
+    fa[3] = h2(a[(g + 8) * K + k0 + 8], a[(g + 8) * K + k0 + 9]);
+    const uint32_t b0 = h2(b[g * K + k0], b[g * K + k0 + 1]);
+    const uint32_t b1 = h2(b[g * K + k0 + 8], b[g * K + k0 + 9]);
+    mma_f16(c, fa, b0, b1);
+  }
+  out[g * 8 + 2 * t] = c[0];
+  out[g * 8 + 2 * t + 1] = c[1];
+  out[(g + 8) * 8 + 2 * t] = c[2];
+  out[(g + 8) * 8 + 2 * t + 1] = c[3];
+}
+
+// Throughput of the warp-level MMA forms on register operands: kind 0 INT8
+// m16n8k32, kind 1 FP16 m16n8k16 with FP32 accumulation (the one the kernels
+// use).  Eight independent accumulators per warp.
 template <int kKind>
 __global__ void __launch_bounds__(kThreads) mma_peak_kernel(int iters, int* out) {
   uint32_t a[4], b0, b1;
@@ -921,23 +853,14 @@ Layout layout(int B, int H, int N, int D) {
   const size_t BH = static_cast<size_t>(B) * H;
   const size_t Np = (static_cast<size_t>(N) + kTok - 1) / kTok * kTok;
   const size_t nb = Np / kTok;
+  const size_t rows = 2 * BH * Np * D;  // FP16 [BH][Np][D]
   const size_t sizes[SAGEBWD_WS_FIELDS] = {
-      BH * Np * D,      // Q^ row tiles
-      BH * Np * D,      // Q^ transposed tiles
-      BH * Np * D,      // K^ row tiles
-      BH * Np * D,      // K^ transposed tiles (dQ order)
-      BH * Np * D,      // V^ transposed tiles
-      BH * Np * D,      // dO^ transposed tiles
-      2 * BH * Np * D,  // V, FP16 row tiles
-      2 * BH * Np * D,  // dO, FP16 row tiles
-      4 * BH * nb,      // Q scales
-      4 * BH * nb,      // K scales
-      4 * BH * nb,      // V scales
-      4 * BH * nb,      // dO scales
-      4 * BH * Np,      // L, log2 units
-      4 * BH * Np,      // D = rowsum(dO o O)
-      4 * BH * Np * D,  // dQ accumulator
-      256,              // status word
+      rows,        rows,        rows,        rows,         // Q^, K^, V^, dO^ codes
+      rows,        rows,                                   // V, dO as FP16
+      4 * BH * nb, 4 * BH * nb, 4 * BH * nb, 4 * BH * nb,  // Q, K, V, dO block scales
+      4 * BH * Np, 4 * BH * Np,                            // L (log2 units), D = rowsum(dO o O)
+      4 * BH * Np * D,                                     // dQ accumulator
+      256,                                                 // status word
   };
   Layout l;
   size_t off = 0;
@@ -952,22 +875,20 @@ Layout layout(int B, int H, int N, int D) {
 Ws carve(void* base, const Layout& l) {
   char* b = static_cast<char*>(base);
   Ws w;
-  w.qr = reinterpret_cast<int8_t*>(b + l.off[0]);
-  w.qt = reinterpret_cast<int8_t*>(b + l.off[1]);
-  w.kr = reinterpret_cast<int8_t*>(b + l.off[2]);
-  w.kt = reinterpret_cast<int8_t*>(b + l.off[3]);
-  w.vt = reinterpret_cast<int8_t*>(b + l.off[4]);
-  w.dot = reinterpret_cast<int8_t*>(b + l.off[5]);
-  w.vh = reinterpret_cast<uint16_t*>(b + l.off[6]);
-  w.doh = reinterpret_cast<uint16_t*>(b + l.off[7]);
-  w.sq = reinterpret_cast<float*>(b + l.off[8]);
-  w.sk = reinterpret_cast<float*>(b + l.off[9]);
-  w.sv = reinterpret_cast<float*>(b + l.off[10]);
-  w.sdo = reinterpret_cast<float*>(b + l.off[11]);
-  w.l2 = reinterpret_cast<float*>(b + l.off[12]);
-  w.dd = reinterpret_cast<float*>(b + l.off[13]);
-  w.dqacc = reinterpret_cast<float*>(b + l.off[14]);
-  w.status = reinterpret_cast<int32_t*>(b + l.off[15]);
+  w.qc = reinterpret_cast<uint16_t*>(b + l.off[0]);
+  w.kc = reinterpret_cast<uint16_t*>(b + l.off[1]);
+  w.vc = reinterpret_cast<uint16_t*>(b + l.off[2]);
+  w.doc = reinterpret_cast<uint16_t*>(b + l.off[3]);
+  w.vh = reinterpret_cast<uint16_t*>(b + l.off[4]);
+  w.doh = reinterpret_cast<uint16_t*>(b + l.off[5]);
+  w.sq = reinterpret_cast<float*>(b + l.off[6]);
+  w.sk = reinterpret_cast<float*>(b + l.off[7]);
+  w.sv = reinterpret_cast<float*>(b + l.off[8]);
+  w.sdo = reinterpret_cast<float*>(b + l.off[9]);
+  w.l2 = reinterpret_cast<float*>(b + l.off[10]);
+  w.dd = reinterpret_cast<float*>(b + l.off[11]);
+  w.dqacc = reinterpret_cast<float*>(b + l.off[12]);
+  w.status = reinterpret_cast<int32_t*>(b + l.off[13]);
   return w;
 }
 
@@ -975,9 +896,9 @@ bool dims_ok(int B, int H, int N, int D) {
   if (B < 0 || H < 0 || N < 0 || (D != 64 && D != 128)) return false;
   const long long BH = static_cast<long long>(B) * H;
   const long long Np = (static_cast<long long>(N) + kTok - 1) / kTok * kTok;
-  if (BH > 65535) return false;                    // gridDim.y
-  if (Np / kTok > (1LL << 20)) return false;       // gridDim.x, with room
-  if (BH * Np * D > (1LL << 40)) return false;     // workspace offsets stay sane
+  if (BH > 65535) return false;                 // gridDim.y
+  if (Np / kTok > (1LL << 20)) return false;    // gridDim.x, with room
+  if (BH * Np * D > (1LL << 40)) return false;  // workspace offsets stay sane
   return true;
 }
 
@@ -1102,8 +1023,8 @@ int sagebwd_bwd(const void* dout, const void* o, const float* lse, void* dq, voi
                : launch_dkdv<128, false>(w, dkb, dvb, BH, N, scale, st);
   if (e != cudaSuccess) return SAGE_FP4_ECUDA;
   const size_t total = static_cast<size_t>(BH) * N * D / 4;
-  const int blocks = static_cast<int>((total + kThreads - 1) / kThreads < 152 * 16 ? (total + kThreads - 1) / kThreads
-                                                                                   : 152 * 16);
+  const size_t want = (total + kThreads - 1) / kThreads;
+  const int blocks = static_cast<int>(want < 152 * 16 ? want : 152 * 16);
   if (D == 64)
     dq_kernel<64><<<blocks, kThreads, 0, st>>>(w.dqacc, static_cast<uint16_t*>(dq), N, BH);
   else
@@ -1121,6 +1042,15 @@ int sagebwd_get_status(void* workspace, int B, int H, int N, int D, void* stream
   if (cudaMemcpy(&h, status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return SAGE_FP4_ECUDA;
   if (h != 0 && cudaMemset(status, 0, sizeof(h)) != cudaSuccess) return SAGE_FP4_ECUDA;
   return h;
+}
+
+int sagebwd_int_mma_probe(const int8_t* a, const int8_t* b, int K, float* out, void* stream) {
+  if (K < 16 || K > 4096 || K % 16 != 0 || !aligned(a, 4) || !aligned(b, 4) || !aligned(out, 4))
+    return SAGE_FP4_EINVAL;
+  const int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  int_mma_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(a, b, K, out);
+  return from_cuda(cudaGetLastError());
 }
 
 int sagebwd_mma_peak(int kind, int ctas, int iters, void* scratch, void* stream) {

@@ -21,10 +21,10 @@ from . import sage_fp4 as _fp4
 from .sage_fp4 import EINVAL, OK, SageFp4Error
 
 _HEADER = os.path.join(os.path.dirname(_fp4._HEADER), "sagebwd.h")
-WS_FIELDS = 16
-WS_NAMES = ("q_rows", "q_cols", "k_rows", "k_cols", "v_cols", "do_cols", "v_half", "do_half",
+WS_FIELDS = 14
+WS_NAMES = ("q_codes", "k_codes", "v_codes", "do_codes", "v_half", "do_half",
             "q_scales", "k_scales", "v_scales", "do_scales", "l2", "drow", "dq_acc", "status")
-TOK, QTILE = 128, 64  # token block / key tile; query tile and query edge of a P / dS block
+TOK = 128  # token block of the INT8 operands; rows padded to a multiple of it
 _lock = threading.Lock()
 _declared = set()
 
@@ -47,6 +47,7 @@ def lib() -> ctypes.CDLL:
                 "sagebwd_bwd": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]),
                 "sagebwd_get_status": (i, [vp, i, i, i, i, vp]),
                 "sagebwd_mma_peak": (i, [i, i, i, vp, vp]),
+                "sagebwd_int_mma_probe": (i, [vp, vp, i, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -84,6 +85,10 @@ def sagebwd_get_status(ws_ptr, B, H, N, D, stream) -> int:
 
 def sagebwd_mma_peak(kind: int, ctas: int, iters: int, scratch_ptr, stream) -> int:
     return lib().sagebwd_mma_peak(kind, ctas, iters, scratch_ptr, stream)
+
+
+def sagebwd_int_mma_probe(a_ptr, b_ptr, K: int, out_ptr, stream) -> int:
+    return lib().sagebwd_int_mma_probe(a_ptr, b_ptr, K, out_ptr, stream)
 
 
 # ------------------------------------------------------------- torch conveniences

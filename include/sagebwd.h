@@ -24,6 +24,11 @@
  *   INT8      symmetric per block: scale = amax / 127, code =
  *             rint(x * (127 / amax)) in float arithmetic.  Q, K, V and dO are
  *             quantized per head in blocks of 128 tokens over all D channels.
+ *             The INT8 products run on the FP16 tensor path with the codes
+ *             held as FP16 values: integer codes, exact products and exact
+ *             integer sums (below 2^24), the results of an INT8 MMA, at the
+ *             FP16 rate (sm_103a's INT8 MMA runs at a quarter of it;
+ *             sagebwd_int_mma_probe checks the exactness on the device).
  *   causal    key j is visible from query i when j <= i.
  *
  * Tensors: q, k, v, o, dout, dq, dk, dv are bf16, contiguous [B][H][N][D],
@@ -50,6 +55,7 @@
 #define SAGEBWD_H
 
 #include <stddef.h>
+#include <stdint.h>
 
 #include "sage_fp4.h"
 
@@ -58,17 +64,18 @@ extern "C" {
 #endif
 
 /* Number of regions in the workspace (see sagebwd_workspace_layout). */
-#define SAGEBWD_WS_FIELDS 16
+#define SAGEBWD_WS_FIELDS 14
 
 /* Bytes of workspace for these sizes; 0 when the sizes are invalid. */
 size_t sagebwd_workspace_bytes(int B, int H, int N, int D);
 
-/* Byte offsets of the workspace's regions, in this order: Q^ row tiles, Q^
- * transposed tiles, K^ row tiles, K^ transposed tiles, V^ transposed tiles,
- * dO^ transposed tiles, V FP16 tiles, dO FP16 tiles, Q/K/V/dO scales (four
- * regions, float [B*H][ceil(N/128)]), L (log2 units) and D (float
- * [B*H][N padded to 128]), the dQ accumulator, the status word.  For tests
- * and inspection; offsets must hold SAGEBWD_WS_FIELDS values. */
+/* Byte offsets of the workspace's regions, in this order: the INT8 codes of
+ * Q, K, V, dO (as FP16 values), V and dO as FP16 (each [B*H][N padded to
+ * 128][D], the 16-byte chunks of row r XOR-permuted by r & 7); the Q/K/V/dO
+ * block scales (float [B*H][ceil(N/128)] each); L in log2 units and
+ * D = rowsum(dO o O) (float [B*H][N padded to 128]); the dQ accumulator
+ * (float [B*H][N padded][D]); the status word.  For tests and inspection;
+ * offsets must hold SAGEBWD_WS_FIELDS values. */
 int sagebwd_workspace_layout(int B, int H, int N, int D, size_t *offsets);
 
 /* Forward: quantizes q, k, v into the workspace and writes o (bf16) and lse
@@ -85,12 +92,17 @@ int sagebwd_bwd(const void *dout, const void *o, const float *lse, void *dq, voi
  * negative SAGE_FP4_* code) and clears it. */
 int sagebwd_get_status(void *workspace, int B, int H, int N, int D, void *stream);
 
-/* Throughput probe of the two warp-level MMA forms the kernels use, on
- * register operands (the roofline's denominators): kind 0 INT8 m16n8k32,
- * kind 1 FP16 m16n8k16 with FP32 accumulation.  Each of `ctas` CTAs of 256
- * threads runs iters x 8 MMAs per warp; scratch is 4 device bytes it may
- * write. */
+/* Throughput probe of two warp-level MMA forms on register operands (the
+ * roofline's denominator is the second): kind 0 INT8 m16n8k32, kind 1 FP16
+ * m16n8k16 with FP32 accumulation.  Each of `ctas` CTAs of 256 threads runs
+ * iters x 8 MMAs per warp; scratch is 4 device bytes it may write. */
 int sagebwd_mma_peak(int kind, int ctas, int iters, void *scratch, void *stream);
+
+/* Exactness probe of the INT8 products: the 16 x 8 product of INT8 device
+ * matrices a [16][K] and b [8][K] (row-major, K a multiple of 16 up to 4096)
+ * computed the kernels' way (codes as FP16 values, FP32 accumulation chained
+ * over K/16 MMAs), written to out, float [16][8] on the device. */
+int sagebwd_int_mma_probe(const int8_t *a, const int8_t *b, int K, float *out, void *stream);
 
 #ifdef __cplusplus
 }

@@ -11,7 +11,7 @@ from bit_attention_gb300 import sagebwd as SB
 def test_library_exports_every_header_function():
     lib = SB.lib()
     names = SB.header_functions()
-    assert len(names) == 6
+    assert len(names) == 7
     text = open(SB._HEADER).read()
     decls = dict(re.findall(r"^(?:int|size_t)\s*(sagebwd_\w+)\(([^;]*)\);", text, re.M))
     assert set(decls) == set(names)
@@ -26,7 +26,7 @@ def test_workspace_layout():
     rc, offs = SB.sagebwd_workspace_layout(B, H, N, D)
     assert rc == S.OK and len(offs) == SB.WS_FIELDS
     total = SB.sagebwd_workspace_bytes(B, H, N, D)
-    sizes = [BH * Np * D] * 6 + [2 * BH * Np * D] * 2 + [4 * BH * 3] * 4 + [4 * BH * Np] * 2 + [4 * BH * Np * D, 256]
+    sizes = [2 * BH * Np * D] * 6 + [4 * BH * 3] * 4 + [4 * BH * Np] * 2 + [4 * BH * Np * D, 256]
     assert offs[0] == 0
     for i, sz in enumerate(sizes):
         assert offs[i] % 256 == 0
@@ -66,3 +66,6 @@ def test_probe_and_status_argument_checks():
     assert SB.sagebwd_mma_peak(0, 1, 0, 0x1000, None) == S.EINVAL
     assert SB.sagebwd_get_status(0x1010, 1, 1, 128, 64, None) == S.EINVAL
     assert SB.sagebwd_get_status(0x1000, 1, 1, 128, 96, None) == S.EINVAL
+    assert SB.sagebwd_int_mma_probe(0x1000, 0x2000, 24, 0x3000, None) == S.EINVAL
+    assert SB.sagebwd_int_mma_probe(0x1000, 0x2000, 8192, 0x3000, None) == S.EINVAL
+    assert SB.sagebwd_int_mma_probe(0x1001, 0x2000, 32, 0x3000, None) == S.EINVAL

@@ -1,9 +1,12 @@
 """SageBwd (8-bit attention for training) on the GPU against the oracle.
 
-* Quantization, bit-exact: the INT8 codes of Q, K, V, dO in every layout the
-  workspace holds (row tiles, transposed tiles in both token orders), their
-  block scales, and the FP16 copies of V and dO, decoded from the workspace
-  and compared with oracle.sagebwd_quantize and with FP16 rounding.
+* Quantization, bit-exact: the INT8 codes of Q, K, V, dO as the workspace
+  holds them (FP16 values in swizzled rows), their block scales, and the
+  FP16 copies of V and dO, decoded and compared with oracle.sagebwd_quantize
+  and with FP16 rounding.
+* The INT8 products on the FP16 tensor path are exact: integer matrices
+  through sagebwd_int_mma_probe give numpy's int64 products bit for bit,
+  including sums of 256 products of 127 * 127 (4.1e6) and mixed signs.
 * Outputs, within tolerance: O and lse of the forward, dQ, dK, dV of the
   backward, element by element against oracle.sagebwd on the same seeded
   inputs.  The two sides follow the same readings; they differ by FP32
@@ -36,7 +39,7 @@ import torch
 import oracle
 from bit_attention_gb300 import sagebwd as SB
 from bit_attention_gb300.synth import TRAIN_WORKLOADS, make_dout, make_qkv
-from sagebwd_layout import decode_cols, decode_half, decode_rows, pi32, rho32
+from sagebwd_layout import decode_codes, decode_half
 
 pytestmark = pytest.mark.gpu
 
@@ -121,25 +124,37 @@ def test_quantized_operands_are_bit_exact(N, D):
     def region(name):
         return ws.region(name).cpu().numpy()
 
-    def padded(codes):
-        out = np.zeros((BH, Np, D), np.int8)
-        out[:, :N] = codes
-        return out
-
-    for name, x, rows, cols, perm, T in (("q", q, "q_rows", "q_cols", pi32, 64), ("k", k, "k_rows", "k_cols", rho32, 128),
-                                         ("v", v, None, "v_cols", pi32, 128), ("do", do, None, "do_cols", pi32, 64)):
+    for name, x in (("q", q), ("k", k), ("v", v), ("do", do)):
         codes, scales = oracle.sagebwd_quantize(x, BH, N, D)
-        want = padded(codes)
-        if rows:
-            assert np.array_equal(decode_rows(region(rows), BH, Np, D, T), want), name
-        assert np.array_equal(decode_cols(region(cols), BH, Np, D, T, perm), want), name
+        want = np.zeros((BH, Np, D), np.int8)
+        want[:, :N] = codes
+        assert np.array_equal(decode_codes(region(f"{name}_codes"), BH, Np, D), want), name
         got_s = region(f"{name}_scales")[:BH * (Np // 128) * 4].view(np.float32).reshape(BH, Np // 128)
         assert np.array_equal(got_s, scales), name
-    for name, x, T in (("v_half", v, 128), ("do_half", do, 64)):
+    for name, x in (("v_half", v), ("do_half", do)):
         want = np.zeros((BH, Np, D), np.float16)
         want[:, :N] = np.clip(x.float().numpy().reshape(BH, N, D), -65504, 65504).astype(np.float16)
-        got = decode_half(region(name), BH, Np, D, T)
+        got = decode_half(region(name), BH, Np, D)
         assert np.array_equal(got.view(np.uint16), want.view(np.uint16)), name
+
+
+@pytest.mark.parametrize("K", [16, 64, 128, 256])
+def test_int8_products_on_the_fp16_path_are_exact(K):
+    rng = np.random.default_rng(K)
+    cases = [rng.integers(-127, 128, size=(24, K)), np.full((24, K), 127), np.full((24, K), -127)]
+    alt = np.full((24, K), 127)
+    alt[:, 1::2] = -127
+    cases.append(alt)
+    mix = rng.choice([-127, -1, 0, 1, 126, 127], size=(24, K))
+    cases.append(mix)
+    for m in cases:
+        a = torch.tensor(m[:16], dtype=torch.int8, device="cuda")
+        b = torch.tensor(m[16:] if m is not alt else -m[16:], dtype=torch.int8, device="cuda")
+        out = torch.empty((16, 8), dtype=torch.float32, device="cuda")
+        assert SB.sagebwd_int_mma_probe(a.data_ptr(), b.data_ptr(), K, out.data_ptr(), None) == 0
+        torch.cuda.synchronize()
+        want = a.cpu().numpy().astype(np.int64) @ b.cpu().numpy().astype(np.int64).T
+        assert np.array_equal(out.cpu().numpy().astype(np.int64), want), (K, np.abs(out.cpu().numpy() - want).max())
 
 
 def test_row_terms_of_the_backward():
