@@ -13,7 +13,16 @@ Prints one JSON line (rank 0).  Under torchrun the ranks split one problem's
 B*H heads between them (--partition heads, the default: strong scaling, no
 data-path collective), or each rank runs its own batch of the workload
 (--partition batch: weak scaling).  With one GPU the line also carries a
-per_workload block: the same kernels timed on every benchmark workload.
+per_workload block: the same kernels timed on every benchmark workload, and
+a sagebwd block: the 8-bit training attention (forward + backward) on its
+two training shapes.
+
+  python bench.py --path sagebwd [--workload train_llama1b|train_qwen3b]
+
+times SageBwd alone: one step = quantize Q, K, V, the forward, the backward
+preparation (dO), the backward (dK, dV, dQ) and dQ's output, on the seeded
+synthetic training inputs; metric TOPS = 3.5 * 4*B*H*N^2*D / t (the
+backward's five products counted as 2.5 forwards; causal at half).
 """
 from __future__ import annotations
 
@@ -36,6 +45,10 @@ FP4_OVER_BF16 = 6.0  # nominal dense FP4 / BF16 tensor rate (13.5 / 2.25 PFLOP/s
 FP4_PUBLISHED_TFLOPS = 15000.0
 HBM_NOMINAL_GBS = 8000.0  # the "~8 TB/s" HBM3e figure the quantize target is quoted against
 
+
+TRAIN_METRIC = ("SageBwd 8-bit attention fwd+bwd TOPS (3.5*4*B*H*N^2*D/t, causal at half) on 1 GB300; "
+                "% of the measured FP16 mma.sync peak")
+SAGEBWD_CALLS = ("quantize_qkv", "attn_fwd", "bwd_prep", "attn_bwd", "dq_out")
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one attn_fwd_kernel launch,
 # captured with ncu on this build of the kernel, mean of two launches (reads
@@ -284,6 +297,201 @@ def per_workload(S, names, fmt, steps, warmup, dev, stream, fp4_peak, hbm_gbs):
     return out
 
 
+class SageBwdRun:
+    """Device buffers of one SageBwd training step on workload w, and its
+    five C-ABI step calls on `stream`."""
+
+    def __init__(self, SB, w, dev, seed=0):
+        import torch
+        from bit_attention_gb300.synth import make_dout, make_qkv
+        self.SB, self.w = SB, w
+        q, k, v = make_qkv(w.B, w.H, w.N, w.D, w.pattern, seed)
+        do = make_dout(w.B, w.H, w.N, w.D, seed)
+        self.host = (q, k, v, do)
+        self.q, self.k, self.v, self.do = (t.to(dev) for t in self.host)
+        self.ws = SB.Workspace(w.B, w.H, w.N, w.D, dev)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        self.scale = w.D ** -0.5
+
+    def calls(self, stream):
+        SB, w, ws = self.SB, self.w, self.ws
+        dims = (w.B, w.H, w.N, w.D)
+        wsa = (ws.buf.data_ptr(), ws.nbytes, stream.cuda_stream)
+        c, sc = int(w.causal), self.scale
+        p = lambda t: t.data_ptr()
+        return (
+            lambda: SB.sagebwd_quantize_qkv(p(self.q), p(self.k), p(self.v), *dims, *wsa),
+            lambda: SB.sagebwd_attn_fwd(p(self.o), p(self.lse), *dims, c, sc, *wsa),
+            lambda: SB.sagebwd_bwd_prep(p(self.do), p(self.o), p(self.lse), *dims, *wsa),
+            lambda: SB.sagebwd_attn_bwd(p(self.dk), p(self.dv), *dims, c, sc, *wsa),
+            lambda: SB.sagebwd_dq_out(p(self.dq), *dims, *wsa),
+        )
+
+    def time(self, steps, warmup, stream):
+        """Time `steps` steps, each of the five calls between CUDA events.
+        Returns (total ms, {call: [ms per step]})."""
+        import torch
+        calls = self.calls(stream)
+        for _ in range(warmup):
+            for fn in calls:
+                if fn() != 0:
+                    raise RuntimeError("SageBwd call failed")
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(steps)]
+        for i in range(steps):
+            ev[i][0].record(stream)
+            for j, fn in enumerate(calls):
+                fn()
+                ev[i][j + 1].record(stream)
+        torch.cuda.synchronize()
+        status = self.ws.get_status(stream)
+        if status != 0:
+            raise RuntimeError(f"SageBwd kernel status {status}")
+        per = {nm: [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)]
+               for j, nm in enumerate(SAGEBWD_CALLS)}
+        return ev[0][0].elapsed_time(ev[-1][-1]), per
+
+
+def sagebwd_summary(w, per, fp16_peak):
+    """Per-call means and the roofline figures of the two attention kernels."""
+    m = {nm: statistics.mean(v) for nm, v in per.items()}
+    ops = w.ops
+    fwd_tops = ops / (m["attn_fwd"] * 1e-3) / 1e12
+    bwd_tops = 2.5 * ops / (m["attn_bwd"] * 1e-3) / 1e12
+    step = sum(m.values())
+    return {"workload": w.name, "ms": m, "ms_per_step": step,
+            "attn_fwd_tops": fwd_tops, "attn_bwd_tops": bwd_tops,
+            "attn_fwd_frac_of_fp16_mma": fwd_tops / fp16_peak,
+            "attn_bwd_frac_of_fp16_mma": bwd_tops / fp16_peak,
+            "step_tops": 3.5 * ops / (step * 1e-3) / 1e12}
+
+
+def sagebwd_cpu_sample(w, seed=0):
+    """The SageBwd oracle (FP64 C, OpenMP) on one head of workload w at its
+    full N: forward and backward.  Returns (TOPS, seconds, threads)."""
+    import oracle
+    from bit_attention_gb300.synth import make_dout, make_qkv
+    q, k, v = make_qkv(1, 1, w.N, w.D, w.pattern, seed)
+    do = make_dout(1, 1, w.N, w.D, seed)
+    t0 = time.perf_counter()
+    oracle.sagebwd(q, k, v, do, 1, w.N, w.D, w.causal)
+    secs = time.perf_counter() - t0
+    head_ops = 3.5 * w.ops / (w.B * w.H)
+    return head_ops / secs / 1e12, secs, oracle.num_threads()
+
+
+def run_sagebwd(args, world, rank, local):
+    """--path sagebwd: the SageBwd training step alone (one GPU; under
+    torchrun every rank runs its own batch: weak scaling)."""
+    from bit_attention_gb300.synth import TRAIN_WORKLOADS
+    w = TRAIN_WORKLOADS[args.workload if args.workload in TRAIN_WORKLOADS else "train_llama1b"]
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        vals, secs_all, threads = [], [], 1
+        for i in range(args.warmup + args.steps):
+            v, secs, threads = sagebwd_cpu_sample(w, seed=i)
+            if i >= args.warmup:
+                vals.append(v)
+                secs_all.append(secs)
+        value = statistics.mean(vals)
+        sample = (f"SageBwd oracle (FP64 C, OpenMP) per step: forward and backward of one (b,h) of the "
+                  f"workload at full N={w.N} ({statistics.mean(secs_all):.1f} s); ms_per_step "
+                  f"extrapolated: the whole workload at that rate")
+        print(json.dumps({
+            "impl": "reference", "metric": TRAIN_METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "ms_per_step": 3.5 * w.ops / (value * 1e12) * 1e3, "extrapolated": True,
+            "extrapolated_fields": ["ms_per_step"], "dtype": "f64", "data": "synthetic",
+            "config": w.describe(),
+            "cpu_baseline": {"value": value, "unit": "TOPS", "cores": threads, "kind": "oracle",
+                             "sample": sample, "extrapolated": True},
+            "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
+
+    import torch
+    from bit_attention_gb300 import sagebwd as SB
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    run = SageBwdRun(SB, w, dev, seed=rank)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        total_ms, per = run.time(args.steps, args.warmup, stream)
+    barrier(world)
+    total_ms = max_over_ranks(total_ms, world)
+    ms_step = total_ms / args.steps
+    value = job_throughput(3.5 * w.ops, world, ms_step)
+    fp16_peak = SB.mma_peak_tops(1)
+    summ = sagebwd_summary(w, per, fp16_peak)
+
+    # end to end through the public API with host buffers: every step copies
+    # q, k, v, dout from pinned host memory, runs forward and backward, and
+    # copies o, dq, dk, dv back
+    e2e = None
+    if not args.no_e2e:
+        hin = [t.pin_memory() for t in run.host]
+        hout = [torch.empty(run.o.shape, dtype=run.o.dtype, pin_memory=True) for _ in range(4)]
+        calls = run.calls(stream)
+        dins = (run.q, run.k, run.v, run.do)
+        douts = (run.o, run.dq, run.dk, run.dv)
+
+        def e2e_step():
+            for d, h in zip(dins, hin):
+                d.copy_(h, non_blocking=True)
+            for fn in calls:
+                fn()
+            for h, d in zip(hout, douts):
+                h.copy_(d, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(s0.elapsed_time(s1), world) / args.steps
+        elems = w.B * w.H * w.N * w.D
+        e2e = {"value": job_throughput(3.5 * w.ops, world, e2e_ms), "unit": "TOPS", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": 4 * elems * 2, "d2h_bytes_per_step": 4 * elems * 2,
+               "call": "sagebwd_quantize_qkv, _attn_fwd, _bwd_prep, _attn_bwd, _dq_out with pinned-host copies"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v_cpu, secs, threads = sagebwd_cpu_sample(w)
+        cpu = {"value": v_cpu, "unit": "TOPS", "cores": threads, "kind": "oracle", "extrapolated": False,
+               "sample": f"SageBwd oracle: forward and backward of one (b,h) of the workload at full N={w.N}, "
+                         f"{secs:.1f} s; the value is the rate on that head"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": TRAIN_METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "int8 codes (per-block scales) on the fp16 tensor path, exact integer sums / fp16 dP / "
+                     "fp32 accumulate",
+            "data": "synthetic (seeded, bit_attention_gb300.synth)",
+            "config": dict(w.describe(), l2="bf16 inputs 4x32 MiB+ per tensor set; no flush",
+                           parallelism=f"weak, {world} independent batch(es)"),
+            "kernels": summ,
+            "roofline": {"bound": "tensor", "kernel": "attn_bwd (dkdv_kernel)",
+                         "achieved": summ["attn_bwd_tops"], "peak": fp16_peak, "unit": "TFLOP/s",
+                         "frac": summ["attn_bwd_frac_of_fp16_mma"], "traffic": None,
+                         "peak_src": "measured live: FP16 mma.sync m16n8k16 (FP32 accumulate) probe, "
+                                     "the instruction the kernels issue",
+                         "bf16_tcgen05_measured_tflops": peaks()["bf16_tflops"]},
+            "e2e": e2e, "cpu_baseline": cpu, "clocks": clk.summary(),
+            "gpu_launches": len(SAGEBWD_CALLS) * args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -304,11 +512,23 @@ def main():
     ap.add_argument("--no-sdpa", action="store_true", help="skip the bf16 SDPA context timing")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip the per-workload block (one GPU only)")
+    ap.add_argument("--path", default="fp4", choices=["fp4", "sagebwd"],
+                    help="fp4: the NVFP4 inference attention (the headline); sagebwd: the 8-bit "
+                         "training attention, forward + backward")
+    ap.add_argument("--no-sagebwd", action="store_true", help="skip the sagebwd block (one GPU only)")
     ap.add_argument("--ref-seconds", type=float, default=6.0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
+
+    if args.path == "sagebwd":
+        world, rank, local = dist_init()
+        run_sagebwd(args, world, rank, local)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
 
     from bit_attention_gb300.synth import WORKLOADS, Workload
     w = WORKLOADS[args.workload]
@@ -440,6 +660,21 @@ def main():
                              "quant_frac_of_hbm_8tbs": quant_gbs / HBM_NOMINAL_GBS,
                              "step_tops": ops / ((a_ms + q_ms) * 1e-3) / 1e12, "headline": True}
 
+    # the 8-bit training attention on its two training shapes (one GPU only)
+    sbw = None
+    if world == 1 and not args.no_sagebwd and args.shape is None and args.causal is None:
+        from bit_attention_gb300 import sagebwd as SB
+        from bit_attention_gb300.synth import TRAIN_WORKLOADS
+        torch.cuda.empty_cache()
+        fp16_peak = SB.mma_peak_tops(1)
+        sbw = {"fp16_mma_measured_tflops": fp16_peak, "metric": TRAIN_METRIC}
+        for name in ("train_llama1b", "train_qwen3b"):
+            run = SageBwdRun(SB, TRAIN_WORKLOADS[name], dev)
+            _, per = run.time(5, 3, stream)
+            sbw[name] = sagebwd_summary(run.w, per, fp16_peak)
+            del run
+            torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         v_cpu, secs, rows, threads, quant_s = cpu_oracle_sample(w, args.cpu_seconds, fmt=args.fmt)
@@ -480,7 +715,7 @@ def main():
                          "frac_of_published": attn_tops / FP4_PUBLISHED_TFLOPS,
                          "fp4_mma_measured_tflops": fp4_mma,
                          "frac_of_fp4_mma_measured": attn_tops / fp4_mma},
-            "per_workload": pw,
+            "per_workload": pw, "sagebwd": sbw,
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk.summary(),
             "gpu_launches": 3 * args.steps,
         }

@@ -970,24 +970,43 @@ int sagebwd_workspace_layout(int B, int H, int N, int D, size_t* offsets) {
   return SAGE_FP4_OK;
 }
 
-int sagebwd_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
-                int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+// Common checks of the step calls: sizes, causal flag, scale, workspace.
+// Returns SAGE_FP4_OK (carry on), a negative code, or 1 for an empty problem.
+static int check_common(int B, int H, int N, int D, int causal, float scale, const void* workspace,
+                        size_t workspace_bytes, Layout* l) {
   if (!dims_ok(B, H, N, D) || (causal != 0 && causal != 1) || !scale_ok(scale)) return SAGE_FP4_EINVAL;
   if (!aligned(workspace, 256)) return SAGE_FP4_EINVAL;
-  const Layout l = layout(B, H, N, D);
-  if (workspace_bytes < l.total) return SAGE_FP4_EINVAL;
-  if (static_cast<long long>(B) * H * N == 0) return SAGE_FP4_OK;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
-    return SAGE_FP4_EINVAL;
-  const int dev = check_device();
-  if (dev != SAGE_FP4_OK) return dev;
+  *l = layout(B, H, N, D);
+  if (workspace_bytes < l->total) return SAGE_FP4_EINVAL;
+  if (static_cast<long long>(B) * H * N == 0) return 1;
+  return SAGE_FP4_OK;
+}
+
+int sagebwd_quantize_qkv(const void* q, const void* k, const void* v, int B, int H, int N, int D, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  Layout l;
+  int rc = check_common(B, H, N, D, 0, 1.0f, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_OK : rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return SAGE_FP4_EINVAL;
+  if ((rc = check_device()) != SAGE_FP4_OK) return rc;
   const Ws w = carve(workspace, l);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int BH = B * H;
+  return from_cuda(D == 64 ? launch_quant<64>(w, q, k, v, nullptr, nullptr, B * H, N, 0, 3, st)
+                           : launch_quant<128>(w, q, k, v, nullptr, nullptr, B * H, N, 0, 3, st));
+}
+
+int sagebwd_attn_fwd(void* o, float* lse, int B, int H, int N, int D, int causal, float scale, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  Layout l;
+  int rc = check_common(B, H, N, D, causal, scale, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_OK : rc;
+  if (!aligned(o, 16) || !aligned(lse, 4)) return SAGE_FP4_EINVAL;
+  if ((rc = check_device()) != SAGE_FP4_OK) return rc;
+  const Ws w = carve(workspace, l);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint16_t* ob = static_cast<uint16_t*>(o);
-  cudaError_t e = D == 64 ? launch_quant<64>(w, q, k, v, nullptr, nullptr, BH, N, 0, 3, st)
-                          : launch_quant<128>(w, q, k, v, nullptr, nullptr, BH, N, 0, 3, st);
-  if (e != cudaSuccess) return SAGE_FP4_ECUDA;
+  const int BH = B * H;
+  cudaError_t e;
   if (D == 64)
     e = causal ? launch_fwd<64, true>(w, ob, lse, BH, N, scale, st) : launch_fwd<64, false>(w, ob, lse, BH, N, scale, st);
   else
@@ -996,32 +1015,49 @@ int sagebwd_fwd(const void* q, const void* k, const void* v, void* o, float* lse
   return from_cuda(e);
 }
 
-int sagebwd_bwd(const void* dout, const void* o, const float* lse, void* dq, void* dk, void* dv, int B, int H, int N,
-                int D, int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
-  if (!dims_ok(B, H, N, D) || (causal != 0 && causal != 1) || !scale_ok(scale)) return SAGE_FP4_EINVAL;
-  if (!aligned(workspace, 256)) return SAGE_FP4_EINVAL;
-  const Layout l = layout(B, H, N, D);
-  if (workspace_bytes < l.total) return SAGE_FP4_EINVAL;
-  if (static_cast<long long>(B) * H * N == 0) return SAGE_FP4_OK;
-  if (!aligned(dout, 16) || !aligned(o, 16) || !aligned(lse, 4) || !aligned(dq, 16) || !aligned(dk, 16) ||
-      !aligned(dv, 16))
-    return SAGE_FP4_EINVAL;
-  const int dev = check_device();
-  if (dev != SAGE_FP4_OK) return dev;
+int sagebwd_bwd_prep(const void* dout, const void* o, const float* lse, int B, int H, int N, int D, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  Layout l;
+  int rc = check_common(B, H, N, D, 0, 1.0f, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_OK : rc;
+  if (!aligned(dout, 16) || !aligned(o, 16) || !aligned(lse, 4)) return SAGE_FP4_EINVAL;
+  if ((rc = check_device()) != SAGE_FP4_OK) return rc;
   const Ws w = carve(workspace, l);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int BH = B * H;
+  return from_cuda(D == 64 ? launch_quant<64>(w, dout, nullptr, nullptr, o, lse, B * H, N, 3, 1, st)
+                           : launch_quant<128>(w, dout, nullptr, nullptr, o, lse, B * H, N, 3, 1, st));
+}
+
+int sagebwd_attn_bwd(void* dk, void* dv, int B, int H, int N, int D, int causal, float scale, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  Layout l;
+  int rc = check_common(B, H, N, D, causal, scale, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_OK : rc;
+  if (!aligned(dk, 16) || !aligned(dv, 16)) return SAGE_FP4_EINVAL;
+  if ((rc = check_device()) != SAGE_FP4_OK) return rc;
+  const Ws w = carve(workspace, l);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint16_t *dkb = static_cast<uint16_t*>(dk), *dvb = static_cast<uint16_t*>(dv);
-  cudaError_t e = D == 64 ? launch_quant<64>(w, dout, nullptr, nullptr, o, lse, BH, N, 3, 1, st)
-                          : launch_quant<128>(w, dout, nullptr, nullptr, o, lse, BH, N, 3, 1, st);
-  if (e != cudaSuccess) return SAGE_FP4_ECUDA;
+  const int BH = B * H;
+  cudaError_t e;
   if (D == 64)
     e = causal ? launch_dkdv<64, true>(w, dkb, dvb, BH, N, scale, st)
                : launch_dkdv<64, false>(w, dkb, dvb, BH, N, scale, st);
   else
     e = causal ? launch_dkdv<128, true>(w, dkb, dvb, BH, N, scale, st)
                : launch_dkdv<128, false>(w, dkb, dvb, BH, N, scale, st);
-  if (e != cudaSuccess) return SAGE_FP4_ECUDA;
+  return from_cuda(e);
+}
+
+int sagebwd_dq_out(void* dq, int B, int H, int N, int D, void* workspace, size_t workspace_bytes, void* stream) {
+  Layout l;
+  int rc = check_common(B, H, N, D, 0, 1.0f, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_OK : rc;
+  if (!aligned(dq, 16)) return SAGE_FP4_EINVAL;
+  if ((rc = check_device()) != SAGE_FP4_OK) return rc;
+  const Ws w = carve(workspace, l);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
   const size_t total = static_cast<size_t>(BH) * N * D / 4;
   const size_t want = (total + kThreads - 1) / kThreads;
   const int blocks = static_cast<int>(want < 152 * 16 ? want : 152 * 16);
@@ -1030,6 +1066,31 @@ int sagebwd_bwd(const void* dout, const void* o, const float* lse, void* dq, voi
   else
     dq_kernel<128><<<blocks, kThreads, 0, st>>>(w.dqacc, static_cast<uint16_t*>(dq), N, BH);
   return from_cuda(cudaGetLastError());
+}
+
+int sagebwd_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+                int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  // every argument checked before the first launch
+  Layout l;
+  int rc = check_common(B, H, N, D, causal, scale, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_OK : rc;
+  if (!aligned(o, 16) || !aligned(lse, 4)) return SAGE_FP4_EINVAL;
+  rc = sagebwd_quantize_qkv(q, k, v, B, H, N, D, workspace, workspace_bytes, stream);
+  if (rc != SAGE_FP4_OK) return rc;
+  return sagebwd_attn_fwd(o, lse, B, H, N, D, causal, scale, workspace, workspace_bytes, stream);
+}
+
+int sagebwd_bwd(const void* dout, const void* o, const float* lse, void* dq, void* dk, void* dv, int B, int H, int N,
+                int D, int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  Layout l;
+  int rc = check_common(B, H, N, D, causal, scale, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_OK : rc;
+  if (!aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16)) return SAGE_FP4_EINVAL;
+  rc = sagebwd_bwd_prep(dout, o, lse, B, H, N, D, workspace, workspace_bytes, stream);
+  if (rc != SAGE_FP4_OK) return rc;
+  rc = sagebwd_attn_bwd(dk, dv, B, H, N, D, causal, scale, workspace, workspace_bytes, stream);
+  if (rc != SAGE_FP4_OK) return rc;
+  return sagebwd_dq_out(dq, B, H, N, D, workspace, workspace_bytes, stream);
 }
 
 int sagebwd_get_status(void* workspace, int B, int H, int N, int D, void* stream) {

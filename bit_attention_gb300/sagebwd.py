@@ -48,6 +48,11 @@ def lib() -> ctypes.CDLL:
                 "sagebwd_get_status": (i, [vp, i, i, i, i, vp]),
                 "sagebwd_mma_peak": (i, [i, i, i, vp, vp]),
                 "sagebwd_int_mma_probe": (i, [vp, vp, i, vp, vp]),
+                "sagebwd_quantize_qkv": (i, [vp, vp, vp, i, i, i, i, vp, sz, vp]),
+                "sagebwd_attn_fwd": (i, [vp, vp, i, i, i, i, i, f, vp, sz, vp]),
+                "sagebwd_bwd_prep": (i, [vp, vp, vp, i, i, i, i, vp, sz, vp]),
+                "sagebwd_attn_bwd": (i, [vp, vp, i, i, i, i, i, f, vp, sz, vp]),
+                "sagebwd_dq_out": (i, [vp, i, i, i, i, vp, sz, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -77,6 +82,26 @@ def sagebwd_bwd(do_ptr, o_ptr, lse_ptr, dq_ptr, dk_ptr, dv_ptr, B, H, N, D, caus
                 ws_bytes, stream) -> int:
     return lib().sagebwd_bwd(do_ptr, o_ptr, lse_ptr, dq_ptr, dk_ptr, dv_ptr, B, H, N, D, int(causal),
                              float(scale), ws_ptr, ws_bytes, stream)
+
+
+def sagebwd_quantize_qkv(q_ptr, k_ptr, v_ptr, B, H, N, D, ws_ptr, ws_bytes, stream) -> int:
+    return lib().sagebwd_quantize_qkv(q_ptr, k_ptr, v_ptr, B, H, N, D, ws_ptr, ws_bytes, stream)
+
+
+def sagebwd_attn_fwd(o_ptr, lse_ptr, B, H, N, D, causal, scale, ws_ptr, ws_bytes, stream) -> int:
+    return lib().sagebwd_attn_fwd(o_ptr, lse_ptr, B, H, N, D, int(causal), float(scale), ws_ptr, ws_bytes, stream)
+
+
+def sagebwd_bwd_prep(do_ptr, o_ptr, lse_ptr, B, H, N, D, ws_ptr, ws_bytes, stream) -> int:
+    return lib().sagebwd_bwd_prep(do_ptr, o_ptr, lse_ptr, B, H, N, D, ws_ptr, ws_bytes, stream)
+
+
+def sagebwd_attn_bwd(dk_ptr, dv_ptr, B, H, N, D, causal, scale, ws_ptr, ws_bytes, stream) -> int:
+    return lib().sagebwd_attn_bwd(dk_ptr, dv_ptr, B, H, N, D, int(causal), float(scale), ws_ptr, ws_bytes, stream)
+
+
+def sagebwd_dq_out(dq_ptr, B, H, N, D, ws_ptr, ws_bytes, stream) -> int:
+    return lib().sagebwd_dq_out(dq_ptr, B, H, N, D, ws_ptr, ws_bytes, stream)
 
 
 def sagebwd_get_status(ws_ptr, B, H, N, D, stream) -> int:

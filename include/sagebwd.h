@@ -79,14 +79,33 @@ size_t sagebwd_workspace_bytes(int B, int H, int N, int D);
 int sagebwd_workspace_layout(int B, int H, int N, int D, size_t *offsets);
 
 /* Forward: quantizes q, k, v into the workspace and writes o (bf16) and lse
- * (natural-log log-sum-exp of scale * S per row). */
+ * (natural-log log-sum-exp of scale * S per row).  The same as
+ * sagebwd_quantize_qkv followed by sagebwd_attn_fwd. */
 int sagebwd_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int D,
                 int causal, float scale, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Backward: given dout and the forward's o and lse (and its workspace),
- * writes dq, dk, dv (bf16). */
+ * writes dq, dk, dv (bf16).  The same as sagebwd_bwd_prep, sagebwd_attn_bwd
+ * and sagebwd_dq_out in turn. */
 int sagebwd_bwd(const void *dout, const void *o, const float *lse, void *dq, void *dk, void *dv, int B, int H,
                 int N, int D, int causal, float scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* The steps, one kernel launch each, on the same arguments and workspace:
+ *   quantize_qkv  Q, K, V -> INT8 codes and block scales, and V as FP16;
+ *   attn_fwd      the forward attention from those codes -> o, lse;
+ *   bwd_prep      dO -> codes, scales and FP16 copy; D = rowsum(dout o o);
+ *                 L from lse; zeroes the dQ accumulator;
+ *   attn_bwd      dK, dV (bf16), and dQ into the FP32 accumulator;
+ *   dq_out        the accumulator -> dq (bf16). */
+int sagebwd_quantize_qkv(const void *q, const void *k, const void *v, int B, int H, int N, int D, void *workspace,
+                         size_t workspace_bytes, void *stream);
+int sagebwd_attn_fwd(void *o, float *lse, int B, int H, int N, int D, int causal, float scale, void *workspace,
+                     size_t workspace_bytes, void *stream);
+int sagebwd_bwd_prep(const void *dout, const void *o, const float *lse, int B, int H, int N, int D, void *workspace,
+                     size_t workspace_bytes, void *stream);
+int sagebwd_attn_bwd(void *dk, void *dv, int B, int H, int N, int D, int causal, float scale, void *workspace,
+                     size_t workspace_bytes, void *stream);
+int sagebwd_dq_out(void *dq, int B, int H, int N, int D, void *workspace, size_t workspace_bytes, void *stream);
 
 /* Synchronizes `stream`, returns the workspace's status word (0 or a
  * negative SAGE_FP4_* code) and clears it. */

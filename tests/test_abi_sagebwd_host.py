@@ -11,7 +11,7 @@ from bit_attention_gb300 import sagebwd as SB
 def test_library_exports_every_header_function():
     lib = SB.lib()
     names = SB.header_functions()
-    assert len(names) == 7
+    assert len(names) == 12
     text = open(SB._HEADER).read()
     decls = dict(re.findall(r"^(?:int|size_t)\s*(sagebwd_\w+)\(([^;]*)\);", text, re.M))
     assert set(decls) == set(names)
@@ -58,6 +58,16 @@ def test_fwd_and_bwd_reject_bad_arguments():
     assert bwd(*q, B, H, N, D, 0, 0.125, ws, nb - 256, None) == S.EINVAL
     assert bwd(*q[:5], 0x6008, B, H, N, D, 0, 0.125, ws, nb, None) == S.EINVAL
     assert bwd(*q, 0, H, N, D, 1, 0.125, ws, SB.sagebwd_workspace_bytes(0, H, N, D), None) == S.OK
+    # the step calls check the same way
+    assert SB.sagebwd_quantize_qkv(0x1008, 0x2000, 0x3000, B, H, N, D, ws, nb, None) == S.EINVAL
+    assert SB.sagebwd_quantize_qkv(*p[:3], B, H, N, 80, ws, nb, None) == S.EINVAL
+    assert SB.sagebwd_attn_fwd(0x4000, 0x5002, B, H, N, D, 0, 0.125, ws, nb, None) == S.EINVAL
+    assert SB.sagebwd_attn_fwd(0x4000, 0x5000, B, H, N, D, 3, 0.125, ws, nb, None) == S.EINVAL
+    assert SB.sagebwd_bwd_prep(0x1000, 0x2000, 0x3000, B, H, N, D, ws, nb - 1, None) == S.EINVAL
+    assert SB.sagebwd_attn_bwd(0x1000, 0x2008, B, H, N, D, 1, 0.125, ws, nb, None) == S.EINVAL
+    assert SB.sagebwd_attn_bwd(0x1000, 0x2000, B, H, N, D, 1, float("inf"), ws, nb, None) == S.EINVAL
+    assert SB.sagebwd_dq_out(0x1000, B, H, N, D, ws + 128, nb, None) == S.EINVAL
+    assert SB.sagebwd_dq_out(0x1000, B, H, 0, D, ws, SB.sagebwd_workspace_bytes(B, H, 0, D), None) == S.OK
 
 
 def test_probe_and_status_argument_checks():
