@@ -330,8 +330,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
   for (int i = 0; i < D / 8; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+  // this key tile's block scales, read one tile ahead
+  float sk_next = ws.sk[static_cast<size_t>(bh) * nqt], sv_next = ws.sv[static_cast<size_t>(bh) * nqt];
 
   for (int kt = 0; kt < nkt && ok; kt++) {
+    const float sk_cur = sk_next, sv_cur = sv_next;
     const int s = kt & 1;
     const uint32_t kst = sbase + L::kStageOff + s * L::kStage, vst = kst + L::kTile;
     ok = __syncthreads_and(waitw(full0 + 8 * s, (kt >> 1) & 1, ctl));
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // scale to log2 units, mask, row maxima
-    const float c2 = sqk * ws.sk[static_cast<size_t>(bh) * nqt + kt];
+    const float c2 = sqk * sk_cur;
     const bool edge = (kCausal && kt == qt) || (kt == nqt - 1 && (N % kTok) != 0);
     float tm0 = -INFINITY, tm1 = -INFINITY;
 #pragma unroll
@@ -403,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int w = 1; w < 4; w++) amax = fmaxf(amax, redp[s * 8 + 4 * grp + w]);
     const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
-    const float spv = __fdiv_rn(amax, 127.0f) * ws.sv[static_cast<size_t>(bh) * nqt + kt];
+    const float spv = __fdiv_rn(amax, 127.0f) * sv_cur;
     // P^ codes: the accumulator fragments of n-blocks 2kc, 2kc+1 are the A
     // fragment of k-step kc
     uint32_t pa[8][4];
@@ -414,25 +417,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       pa[kc][2] = h2(code(x[2 * kc + 1][0], inv), code(x[2 * kc + 1][1], inv));
       pa[kc][3] = h2(code(x[2 * kc + 1][2], inv), code(x[2 * kc + 1][3], inv));
     }
-    // O = O * alpha + s_P s_V (P^ V^); V^ read transposed by ldmatrix.trans
+    // O = O * alpha + s_P s_V (P^ V^); V^ read transposed by ldmatrix.trans.
+    // Eight output n-blocks at a time, k outermost, so that eight
+    // independent MMA chains are in flight.
 #pragma unroll
-    for (int nd = 0; nd < D / 8; nd += 2) {
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    for (int ng = 0; ng < D / 64; ng++) {
+      float acc[8][4];
+#pragma unroll
+      for (int i = 0; i < 8; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
 #pragma unroll
       for (int kc = 0; kc < 8; kc++) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vst + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 16 * (nd + (j >> 1)), L::kRow), b0, b1, b2, b3);
-        mma_f16(acc[0], pa[kc], b0, b1);
-        mma_f16(acc[1], pa[kc], b2, b3);
+#pragma unroll
+        for (int np = 0; np < 8; np += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vst + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 16 * (8 * ng + np + (j >> 1)), L::kRow), b0, b1,
+                    b2, b3);
+          mma_f16(acc[np], pa[kc], b0, b1);
+          mma_f16(acc[np + 1], pa[kc], b2, b3);
+        }
       }
 #pragma unroll
-      for (int h = 0; h < 2; h++) {
-        o[nd + h][0] = fmaf(acc[h][0], spv, o[nd + h][0] * al0);
-        o[nd + h][1] = fmaf(acc[h][1], spv, o[nd + h][1] * al0);
-        o[nd + h][2] = fmaf(acc[h][2], spv, o[nd + h][2] * al1);
-        o[nd + h][3] = fmaf(acc[h][3], spv, o[nd + h][3] * al1);
+      for (int i = 0; i < 8; i++) {
+        float* oo = o[8 * ng + i];
+        oo[0] = fmaf(acc[i][0], spv, oo[0] * al0);
+        oo[1] = fmaf(acc[i][1], spv, oo[1] * al0);
+        oo[2] = fmaf(acc[i][2], spv, oo[2] * al1);
+        oo[3] = fmaf(acc[i][3], spv, oo[3] * al1);
       }
     }
+    sk_next = kt + 1 < nkt ? ws.sk[static_cast<size_t>(bh) * nqt + kt + 1] : 0.0f;
+    sv_next = kt + 1 < nkt ? ws.sv[static_cast<size_t>(bh) * nqt + kt + 1] : 0.0f;
   }
   if (!ok) {
     // abandoning: let every copy this CTA issued land before exiting (the
@@ -487,6 +501,36 @@ struct BwdSmem {
   static constexpr int kBytes = kRedOff + 2 * 8 * 4;
 };
 
+// acc[D/8][4] += f * (A B): A the warp's 16-key x 64-query code fragments
+// (k = queries), B a 64-query x D tile of FP16 rows read transposed.  Eight
+// output n-blocks at a time with k outermost: eight independent MMA chains.
+template <int D>
+__device__ __forceinline__ void mma_fold(float (&acc)[D / 8][4], const uint32_t (&a)[4][4], uint32_t tile, float f,
+                                         int lane) {
+  const int j = lane >> 3;
+#pragma unroll
+  for (int ng = 0; ng < D / 64; ng++) {
+    float t[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; i++) t[i][0] = t[i][1] = t[i][2] = t[i][3] = 0.0f;
+#pragma unroll
+    for (int kc = 0; kc < 4; kc++) {
+#pragma unroll
+      for (int np = 0; np < 8; np += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(tile + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 16 * (8 * ng + np + (j >> 1)), 2 * D), b0, b1,
+                  b2, b3);
+        mma_f16(t[np], a[kc], b0, b1);
+        mma_f16(t[np + 1], a[kc], b2, b3);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+#pragma unroll
+      for (int e = 0; e < 4; e++) acc[8 * ng + i][e] = fmaf(t[i][e], f, acc[8 * ng + i][e]);
+  }
+}
+
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(Ws ws, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int N, float scale) {
@@ -533,8 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bulk_load(sbase + L::kVh, ws.vh + off, kTok * L::kRow, fbar);
     for (; issued < 2 && issued < niter; issued++) issue_stage(issued);
   }
-  // every wait's outcome is voted on by the whole CTA
-  bool ok = __syncthreads_and(waitw(fbar, 0, ctl));
+  // every wait's outcome is voted on by the whole CTA: here the fixed tiles
+  // and the first query tile; each later tile's vote rides on the barrier
+  // that ends the previous tile's dK
+  bool ok = __syncthreads_and(waitw(fbar, 0, ctl) && waitw(full0, 0, ctl));
 
   const float sk = ws.sk[static_cast<size_t>(bh) * nkt + kb];
   const int key0 = kb * kTok + 16 * warp + g;  // this thread's keys: key0, key0 + 8
@@ -547,13 +593,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int e = 0; e < 4; e++) dka[i][e] = dva[i][e] = 0.0f;
 
+  // the query tile's block scales, read one tile ahead
+  float sq_next = ws.sq[static_cast<size_t>(bh) * nkt + (q0 >> 1)];
+  float sdo_next = ws.sdo[static_cast<size_t>(bh) * nkt + (q0 >> 1)];
   for (int it = 0; it < niter && ok; it++) {
     const int qtile = q0 + it, s = it & 1;
     const uint32_t st = sbase + L::kStageOff + s * L::kStage;
-    ok = __syncthreads_and(waitw(full0 + 8 * s, (it >> 1) & 1, ctl));
-    if (!ok) break;
-    const float sq = ws.sq[static_cast<size_t>(bh) * nkt + (qtile >> 1)];
-    const float sdo = ws.sdo[static_cast<size_t>(bh) * nkt + (qtile >> 1)];
+    const float sq = sq_next, sdo = sdo_next;
+    if (it + 1 < niter) {
+      sq_next = ws.sq[static_cast<size_t>(bh) * nkt + ((qtile + 1) >> 1)];
+      sdo_next = ws.sdo[static_cast<size_t>(bh) * nkt + ((qtile + 1) >> 1)];
+    }
     // S^T = K^ Q^^T: 16 keys x 64 queries
     float p[8][4];
 #pragma unroll
@@ -610,25 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pa[kc][3] = h2(code(p[2 * kc + 1][2], inv), code(p[2 * kc + 1][3], inv));
     }
     // dV += s_P s_dO (P^^T dO^); dO^ read transposed
-    {
-      const float f = __fdiv_rn(amax, 127.0f) * sdo;
-#pragma unroll
-      for (int nd = 0; nd < D / 8; nd += 2) {
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-        for (int kc = 0; kc < 4; kc++) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(st + L::kDoc + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 16 * (nd + (j >> 1)), L::kRow), b0,
-                    b1, b2, b3);
-          mma_f16(acc[0], pa[kc], b0, b1);
-          mma_f16(acc[1], pa[kc], b2, b3);
-        }
-#pragma unroll
-        for (int h = 0; h < 2; h++)
-#pragma unroll
-          for (int e = 0; e < 4; e++) dva[nd + h][e] = fmaf(acc[h][e], f, dva[nd + h][e]);
-      }
-    }
+    mma_fold<D>(dva, pa, st + L::kDoc, __fdiv_rn(amax, 127.0f) * sdo, lane);
     // dP^T = V dO^T in FP16, then dS^T = P^T o (dP^T - D)
     float dp[8][4];
 #pragma unroll
@@ -679,28 +711,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       sts32(dsb + swz(16 * warp + g + 8, 2 * (16 * kc + 8 + 2 * t), 2 * kQ), da[kc][3]);
     }
     // dK += s_dS s_Q (dS^^T Q^); Q^ read transposed
-    {
-      const float f = sds * sq;
-#pragma unroll
-      for (int nd = 0; nd < D / 8; nd += 2) {
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-        for (int kc = 0; kc < 4; kc++) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(st + L::kQc + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 16 * (nd + (j >> 1)), L::kRow), b0, b1,
-                    b2, b3);
-          mma_f16(acc[0], da[kc], b0, b1);
-          mma_f16(acc[1], da[kc], b2, b3);
-        }
-#pragma unroll
-        for (int h = 0; h < 2; h++)
-#pragma unroll
-          for (int e = 0; e < 4; e++) dka[nd + h][e] = fmaf(acc[h][e], f, dka[nd + h][e]);
-      }
-    }
-    // every warp's dS^ is staged and every warp is done with stage s
-    __syncthreads();
-    if (threadIdx.x == 0 && it + 2 < niter) issue_stage(issued++);
+    mma_fold<D>(dka, da, st + L::kQc, sds * sq, lane);
+    // every warp's dS^ is staged and every warp is done with stage s; the
+    // same barrier votes on the next query tile's copy (issued a tile ago)
+    const bool next_ok = it + 1 >= niter || waitw(full0 + 8 * (s ^ 1), ((it + 1) >> 1) & 1, ctl);
+    ok = __syncthreads_and(next_ok);
+    if (threadIdx.x == 0 && ok && it + 2 < niter) issue_stage(issued++);
     // dQ[64 x D] += scale s_dS s_K (dS^ K^): warp w takes query rows
     // 16 (w & 3) and half of the D columns; dS^ and K^ read transposed
     {
