@@ -52,10 +52,17 @@ __device__ __forceinline__ void fill_rtab(float* rtab) {
   }
 }
 
+// Eight values times the group's reciprocal scale, then E2M1.  The products
+// are taken two at a time (mul.rn.f32x2: each lane rounded like __fmul_rn).
 __device__ __forceinline__ uint32_t encode8(const float (&v)[8], float r) {
+  const uint64_t rr = pack2(r, r);
   float y[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(v[i], r);
+  for (int i = 0; i < 8; i += 2) {
+    const uint64_t p = mul2(pack2(v[i], v[i + 1]), rr);
+    y[i] = lo2(p);
+    y[i + 1] = hi2(p);
+  }
   return cvt_e2m1x8(y);
 }
 
