@@ -278,7 +278,8 @@ struct FwdSmem {
 
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
-    fwd_kernel(Ws ws, uint16_t* __restrict__ out, float* __restrict__ lse, int N, float scale_log2e) {
+    fwd_kernel(Ws ws, uint16_t* __restrict__ out, float* __restrict__ lse, int N, float scale_log2e, uint64_t wait_ns,
+               int withhold) {
   using L = FwdSmem<D>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int nqt = (N + kTok - 1) / kTok;
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_addr(smem);
   const uint32_t qbar = sbase + L::kBarOff, full0 = qbar + 8;
   float* redp = reinterpret_cast<float*>(smem + L::kRedOff);
-  const Ctl ctl{ws.status, kWaitNs};
+  const Ctl ctl{ws.status, wait_ns};
   const int nkt = kCausal ? qt + 1 : nqt;
   const size_t hb = static_cast<size_t>(bh) * Np * D;
 
@@ -314,6 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(qbar, L::kTile);
     bulk_load(sbase + L::kQOff, ws.qc + hb + static_cast<size_t>(qt) * kTok * D, L::kTile, qbar);
+    // withhold (failure-detection test only): CTA 0 never issues key tile 0,
+    // so its wait for that tile runs out
+    if (withhold && blockIdx.x == 0 && blockIdx.y == 0) issued = 1;
     for (; issued < 2 && issued < nkt; issued++) issue_tile(issued);
   }
   // every wait's outcome is voted on by the whole CTA, so that all warps
@@ -454,7 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
       drain_wait(qbar, 0, ctl);
       for (int last = issued - 1; last >= 0 && last >= issued - 2; last--)
-        drain_wait(full0 + 8 * (last & 1), (last >> 1) & 1, ctl);
+        if (!(withhold && blockIdx.x == 0 && blockIdx.y == 0 && last == 0))
+          drain_wait(full0 + 8 * (last & 1), (last >> 1) & 1, ctl);
     }
     return;
   }
@@ -533,7 +538,8 @@ __device__ __forceinline__ void mma_fold(float (&acc)[D / 8][4], const uint32_t 
 
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
-    dkdv_kernel(Ws ws, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int N, float scale) {
+    dkdv_kernel(Ws ws, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int N, float scale, uint64_t wait_ns,
+                int withhold) {
   using L = BwdSmem<D>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int nkt = (N + kTok - 1) / kTok;
@@ -545,9 +551,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_addr(smem);
   const uint32_t fbar = sbase + L::kBarOff, full0 = fbar + 8;
   float* redp = reinterpret_cast<float*>(smem + L::kRedOff);
-  const Ctl ctl{ws.status, kWaitNs};
+  const Ctl ctl{ws.status, wait_ns};
   const size_t hb = static_cast<size_t>(bh) * Np * D;
   const size_t hrow = static_cast<size_t>(bh) * Np;
+  // withhold (failure-detection test only): CTA 0 never issues its first
+  // query tile, so its wait for that tile runs out
+  const bool held = withhold && blockIdx.x == 0 && blockIdx.y == 0;
   const int q0 = kCausal ? 2 * kb : 0;  // first query tile that sees these keys
   const int niter = nqt - q0;
 
@@ -575,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t off = hb + static_cast<size_t>(kb) * kTok * D;
     bulk_load(sbase + L::kKc, ws.kc + off, kTok * L::kRow, fbar);
     bulk_load(sbase + L::kVh, ws.vh + off, kTok * L::kRow, fbar);
+    if (held) issued = 1;
     for (; issued < 2 && issued < niter; issued++) issue_stage(issued);
   }
   // every wait's outcome is voted on by the whole CTA: here the fixed tiles
@@ -752,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
       drain_wait(fbar, 0, ctl);
       for (int last = issued - 1; last >= 0 && last >= issued - 2; last--)
-        drain_wait(full0 + 8 * (last & 1), (last >> 1) & 1, ctl);
+        if (!(held && last == 0)) drain_wait(full0 + 8 * (last & 1), (last >> 1) & 1, ctl);
     }
     return;
   }
@@ -937,22 +947,24 @@ int check_device() {
 }
 
 template <int D, bool C>
-cudaError_t launch_fwd(const Ws& w, uint16_t* o, float* lse, int BH, int N, float scale, cudaStream_t st) {
+cudaError_t launch_fwd(const Ws& w, uint16_t* o, float* lse, int BH, int N, float scale, cudaStream_t st,
+                       uint64_t wait_ns = kWaitNs, int withhold = 0) {
   const int smem = FwdSmem<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((N + kTok - 1) / kTok, BH);
-  fwd_kernel<D, C><<<grid, kThreads, smem, st>>>(w, o, lse, N, scale * kLog2e);
+  fwd_kernel<D, C><<<grid, kThreads, smem, st>>>(w, o, lse, N, scale * kLog2e, wait_ns, withhold);
   return cudaGetLastError();
 }
 
 template <int D, bool C>
-cudaError_t launch_dkdv(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int N, float scale, cudaStream_t st) {
+cudaError_t launch_dkdv(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int N, float scale, cudaStream_t st,
+                        uint64_t wait_ns = kWaitNs, int withhold = 0) {
   const int smem = BwdSmem<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((N + kTok - 1) / kTok, BH);
-  dkdv_kernel<D, C><<<grid, kThreads, smem, st>>>(w, dk, dv, N, scale);
+  dkdv_kernel<D, C><<<grid, kThreads, smem, st>>>(w, dk, dv, N, scale, wait_ns, withhold);
   return cudaGetLastError();
 }
 
@@ -1119,6 +1131,31 @@ int sagebwd_get_status(void* workspace, int B, int H, int N, int D, void* stream
   if (cudaMemcpy(&h, status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return SAGE_FP4_ECUDA;
   if (h != 0 && cudaMemset(status, 0, sizeof(h)) != cudaSuccess) return SAGE_FP4_ECUDA;
   return h;
+}
+
+int sagebwd_stall_test(int kernel, void* out0, void* out1, int B, int H, int N, int D, float scale,
+                       uint64_t wait_limit_ns, void* workspace, size_t workspace_bytes, void* stream) {
+  Layout l;
+  int rc = check_common(B, H, N, D, 0, scale, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_EINVAL : rc;
+  if ((kernel != 0 && kernel != 1) || wait_limit_ns < 1000000ull || wait_limit_ns > kWaitNs) return SAGE_FP4_EINVAL;
+  if (!aligned(out0, 16) || !aligned(out1, kernel == 0 ? 4 : 16)) return SAGE_FP4_EINVAL;
+  if ((rc = check_device()) != SAGE_FP4_OK) return rc;
+  const Ws w = carve(workspace, l);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  cudaError_t e;
+  if (kernel == 0) {
+    uint16_t* o = static_cast<uint16_t*>(out0);
+    float* lse = static_cast<float*>(out1);
+    e = D == 64 ? launch_fwd<64, false>(w, o, lse, BH, N, scale, st, wait_limit_ns, 1)
+                : launch_fwd<128, false>(w, o, lse, BH, N, scale, st, wait_limit_ns, 1);
+  } else {
+    uint16_t *dkb = static_cast<uint16_t*>(out0), *dvb = static_cast<uint16_t*>(out1);
+    e = D == 64 ? launch_dkdv<64, false>(w, dkb, dvb, BH, N, scale, st, wait_limit_ns, 1)
+                : launch_dkdv<128, false>(w, dkb, dvb, BH, N, scale, st, wait_limit_ns, 1);
+  }
+  return from_cuda(e);
 }
 
 int sagebwd_int_mma_probe(const int8_t* a, const int8_t* b, int K, float* out, void* stream) {

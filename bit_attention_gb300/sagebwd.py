@@ -53,6 +53,7 @@ def lib() -> ctypes.CDLL:
                 "sagebwd_bwd_prep": (i, [vp, vp, vp, i, i, i, i, vp, sz, vp]),
                 "sagebwd_attn_bwd": (i, [vp, vp, i, i, i, i, i, f, vp, sz, vp]),
                 "sagebwd_dq_out": (i, [vp, i, i, i, i, vp, sz, vp]),
+                "sagebwd_stall_test": (i, [i, vp, vp, i, i, i, i, f, ctypes.c_uint64, vp, sz, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -102,6 +103,12 @@ def sagebwd_attn_bwd(dk_ptr, dv_ptr, B, H, N, D, causal, scale, ws_ptr, ws_bytes
 
 def sagebwd_dq_out(dq_ptr, B, H, N, D, ws_ptr, ws_bytes, stream) -> int:
     return lib().sagebwd_dq_out(dq_ptr, B, H, N, D, ws_ptr, ws_bytes, stream)
+
+
+def sagebwd_stall_test(kernel, out0_ptr, out1_ptr, B, H, N, D, scale, wait_limit_ns, ws_ptr, ws_bytes,
+                       stream) -> int:
+    return lib().sagebwd_stall_test(kernel, out0_ptr, out1_ptr, B, H, N, D, float(scale), wait_limit_ns, ws_ptr,
+                                    ws_bytes, stream)
 
 
 def sagebwd_get_status(ws_ptr, B, H, N, D, stream) -> int:

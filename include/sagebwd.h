@@ -117,6 +117,17 @@ int sagebwd_get_status(void *workspace, int B, int H, int N, int D, void *stream
  * iters x 8 MMAs per warp; scratch is 4 device bytes it may write. */
 int sagebwd_mma_peak(int kind, int ctas, int iters, void *scratch, void *stream);
 
+/* Failure-detection test: runs the forward attention (kernel 0; out0 = o,
+ * out1 = lse) or the backward attention (kernel 1; out0 = dk, out1 = dv),
+ * non-causal, on a workspace already filled by sagebwd_quantize_qkv (and, for
+ * kernel 1, sagebwd_bwd_prep), with one copy withheld: the first CTA never
+ * issues its first streamed tile, so its bounded wait runs out after
+ * wait_limit_ns (1 ms to 1.5 s) and the kernel records SAGE_FP4_ETIMEOUT in
+ * the status word; every other CTA completes.  The outputs are then
+ * incomplete.  EINVAL for an empty problem. */
+int sagebwd_stall_test(int kernel, void *out0, void *out1, int B, int H, int N, int D, float scale,
+                       uint64_t wait_limit_ns, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Exactness probe of the INT8 products: the 16 x 8 product of INT8 device
  * matrices a [16][K] and b [8][K] (row-major, K a multiple of 16 up to 4096)
  * computed the kernels' way (codes as FP16 values, FP32 accumulation chained

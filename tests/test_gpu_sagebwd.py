@@ -212,3 +212,34 @@ def test_mma_peaks_are_measurable():
     f16 = SB.mma_peak_tops(1)
     print(f"mma.sync peaks: INT8 m16n8k32 {i8:.1f} TOP/s, FP16 m16n8k16 (FP32 acc) {f16:.1f} TFLOP/s")
     assert i8 > 0 and f16 > 0
+
+
+@pytest.mark.parametrize("kernel,D", [(0, 64), (1, 64), (0, 128), (1, 128)])
+def test_stalled_copy_sets_timeout_and_the_context_survives(kernel, D):
+    """Failure detection without a fault: the first CTA of the forward
+    (kernel 0) or backward (kernel 1) attention never gets its first streamed
+    tile; its bounded wait (20 ms here) runs out, the kernel records
+    SAGE_FP4_ETIMEOUT and returns, and the next calls run normally."""
+    import time
+    from bit_attention_gb300 import sage_fp4 as S
+    B, H, N = 1, 2, 384
+    q, k, v, do = (t.cuda() for t in inputs(B, H, N, D, seed=21))
+    o, lse, ws = SB.forward(q, k, v, False)
+    dq, dk, dv = SB.backward(do, o, lse, ws, False)  # the workspace now holds every operand
+    torch.cuda.synchronize()
+    assert ws.get_status() == 0
+    out0 = torch.empty_like(q)
+    out1 = torch.empty((B, H, N), dtype=torch.float32, device="cuda") if kernel == 0 else torch.empty_like(q)
+    t0 = time.time()
+    rc = SB.sagebwd_stall_test(kernel, out0.data_ptr(), out1.data_ptr(), B, H, N, D, D ** -0.5, 20_000_000,
+                               ws.buf.data_ptr(), ws.nbytes, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 5.0
+    assert ws.get_status() == S.ETIMEOUT
+    assert ws.get_status() == 0  # read and cleared
+    o2, lse2, ws2 = SB.forward(q, k, v, False)
+    dq2, dk2, dv2 = SB.backward(do, o2, lse2, ws2, False)
+    torch.cuda.synchronize()
+    assert ws2.get_status() == 0
+    assert torch.equal(o2, o) and torch.equal(lse2, lse) and torch.equal(dk2, dk) and torch.equal(dv2, dv)
