@@ -12,6 +12,7 @@
 #include <string.h>
 
 #include "sage_fp4.h"
+#include "sagebwd.h"
 
 static int failures = 0;
 
@@ -124,6 +125,41 @@ int main(void) {
          SAGE_FP4_EINVAL, "mma probe unknown flag");
   expect(sage_fp4_mma_peak(0, 128, P(0x5000), NULL), SAGE_FP4_EINVAL, "mma peak, no iterations");
   expect(sage_fp4_tmem_max_probe(NULL, P(0x2000), P(0x3000), NULL), SAGE_FP4_EINVAL, "tmem probe, no input");
+
+  /* SageBwd (include/sagebwd.h): workspace layout and argument rejections */
+  {
+    size_t offs[SAGEBWD_WS_FIELDS];
+    const size_t sb = sagebwd_workspace_bytes(2, 3, 300, 64);
+    if (sb == 0 || sagebwd_workspace_layout(2, 3, 300, 64, offs) != SAGE_FP4_OK) expect(0, 1, "sagebwd layout");
+    for (int i = 1; i < SAGEBWD_WS_FIELDS; i++)
+      if (offs[i] <= offs[i - 1] || offs[i] % 256 || offs[i] >= sb) expect(i, -1, "sagebwd offsets increase");
+    expect((int)sagebwd_workspace_bytes(INT_MAX, INT_MAX, INT_MAX, 128), 0, "sagebwd workspace, overflow");
+    expect((int)sagebwd_workspace_bytes(1, 1, 17, 96), 0, "sagebwd workspace, D = 96");
+    expect(sagebwd_workspace_layout(1, 1, 17, 64, NULL), SAGE_FP4_EINVAL, "sagebwd layout, no output");
+    void *w = P(0x100000);
+    expect(sagebwd_fwd(P(0x1000), P(0x2000), P(0x3000), P(0x4000), (float *)P(0x5000), 2, 3, 300, 64, 2, 0.125f,
+                       w, sb, NULL),
+           SAGE_FP4_EINVAL, "sagebwd_fwd causal = 2");
+    expect(sagebwd_fwd(P(0x1000), P(0x2000), P(0x3000), P(0x4000), (float *)P(0x5000), 2, 3, 300, 64, 0, -1.0f, w,
+                       sb, NULL),
+           SAGE_FP4_EINVAL, "sagebwd_fwd scale < 0");
+    expect(sagebwd_fwd(P(0x1000), P(0x2000), P(0x3000), P(0x4000), (float *)P(0x5000), 2, 3, 300, 64, 0, 0.125f, w,
+                       sb - 1, NULL),
+           SAGE_FP4_EINVAL, "sagebwd_fwd short workspace");
+    expect(sagebwd_bwd(P(0x1000), P(0x2000), (float *)P(0x3000), P(0x4008), P(0x5000), P(0x6000), 2, 3, 300, 64, 0,
+                       0.125f, w, sb, NULL),
+           SAGE_FP4_EINVAL, "sagebwd_bwd misaligned dq");
+    expect(sagebwd_attn_bwd(P(0x1000), P(0x2000), 2, 3, 300, 64, 1, 0.125f, P(0x100010), sb, NULL), SAGE_FP4_EINVAL,
+           "sagebwd_attn_bwd misaligned workspace");
+    expect(sagebwd_quantize_qkv(P(0x1000), P(0x2000), P(0x3000), 0, 3, 300, 64, w,
+                                sagebwd_workspace_bytes(0, 3, 300, 64), NULL),
+           SAGE_FP4_OK, "sagebwd empty problem");
+    expect(sagebwd_stall_test(0, P(0x1000), P(0x2000), 2, 3, 300, 64, 0.125f, 10, w, sb, NULL), SAGE_FP4_EINVAL,
+           "sagebwd stall test, limit too short");
+    expect(sagebwd_int_mma_probe((const int8_t *)P(0x1000), (const int8_t *)P(0x2000), 20, (float *)P(0x3000), NULL),
+           SAGE_FP4_EINVAL, "sagebwd probe K = 20");
+    expect(sagebwd_mma_peak(3, 1, 1, P(0x1000), NULL), SAGE_FP4_EINVAL, "sagebwd peak kind");
+  }
 
   /* every status code has a string */
   for (int c = -8; c <= 1; c++)

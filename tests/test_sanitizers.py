@@ -2,7 +2,8 @@
 
 compute-sanitizer is not available on the GPU pool, so the host side is
 checked here instead: the CPU oracle, and the library's argument checking,
-workspace carving and one-call paths (api.cu, noalloc.cu, host_pipe.cu),
+workspace carving and one-call paths (api.cu, noalloc.cu, host_pipe.cu,
+and SageBwd's sagebwd.cu),
 built with -fsanitize=address,undefined and driven by the two C programs in
 tests/sanitize/ through every path that needs no device.  Any memory error or
 undefined behaviour aborts the program, and the test fails.
@@ -57,7 +58,7 @@ def test_abi_argument_checks_under_sanitizers(tmp_path):
               "-fno-omit-frame-pointer", "-g"]:
         flags += ["-Xcompiler", s]
     procs, objs = [], []
-    for name in ("api", "noalloc", "host_pipe"):
+    for name in ("api", "noalloc", "host_pipe", "sagebwd"):
         obj = tmp_path / f"{name}.o"
         objs.append(str(obj))
         procs.append(subprocess.Popen([nvcc, *flags, "-c", os.path.join(csrc, name + ".cu"), "-o", str(obj)],
