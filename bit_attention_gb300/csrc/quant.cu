@@ -412,7 +412,10 @@ cudaError_t launch_quant_rows(const void* q, const void* k, Strides sq, Strides 
   const int Np = round_up_int(N, 128);
   const long long chunks = static_cast<long long>(BH) * Np / (D == 128 ? 16 : 32);  // one warp each
   long long blocks = (chunks + 7) / 8;
-  const long long cap = static_cast<long long>(num_sms()) * 8;
+  // D = 128: one wave of 8 resident blocks per SM (4 per tensor), so that the
+  // V grid queued behind may start at once (measured on GB300: +3% on the LLM
+  // shape over two waves); D = 64: 8 per tensor (two waves), measured best
+  const long long cap = static_cast<long long>(num_sms()) * (D == 128 ? 4 : 8);
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   dim3 grid(static_cast<unsigned>(blocks), 2);
@@ -468,12 +471,14 @@ cudaError_t launch_quant_v(const void* v, Strides sv, uint8_t* vc, uint8_t* vs, 
   const int Np = round_up_int(N, 128);
   // 64-token tiles, double-buffered: 32 KB (D = 128) or 16 KB (D = 64) of
   // shared memory per block.  The per-tile arithmetic, not the copy latency,
-  // sets the pace, so more resident blocks beat deeper rings (measured on
+  // sets the pace, so several resident blocks beat deeper rings (measured on
   // GB300: 5.3-5.8 TB/s at D = 128 with six blocks per SM, against 4.0-4.9 TB/s
-  // with four-deep rings and two or three blocks).
+  // with four-deep rings and two or three blocks).  Five blocks per SM at
+  // D = 128 leave room for the Q/K grid's last blocks: 1-3% faster than six
+  // on every D = 128 workload.
   if (D == 128)
-    return mx ? launch_quant_v_cfg<128, 64, 2, true>(v, sv, vc, vs, H, BH, Np, N, status, 6, wait_ns, withhold, ext, st)
-              : launch_quant_v_cfg<128, 64, 2, false>(v, sv, vc, vs, H, BH, Np, N, status, 6, wait_ns, withhold, ext, st);
+    return mx ? launch_quant_v_cfg<128, 64, 2, true>(v, sv, vc, vs, H, BH, Np, N, status, 5, wait_ns, withhold, ext, st)
+              : launch_quant_v_cfg<128, 64, 2, false>(v, sv, vc, vs, H, BH, Np, N, status, 5, wait_ns, withhold, ext, st);
   return mx ? launch_quant_v_cfg<64, 64, 2, true>(v, sv, vc, vs, H, BH, Np, N, status, 8, wait_ns, withhold, ext, st)
             : launch_quant_v_cfg<64, 64, 2, false>(v, sv, vc, vs, H, BH, Np, N, status, 8, wait_ns, withhold, ext, st);
 }
