@@ -57,6 +57,10 @@ SAGEBWD_CALLS = ("quantize_qkv", "attn_fwd", "bwd_prep", "attn_bwd", "dq_out")
 ATTN_TRAFFIC = {
     "attn_fwd B4 H32 N4096 D128 k-channel-outliers": 113.32e6 + 80.14e6,
 }
+# the same for one SageBwd dkdv_kernel launch (attn_bwd), one ncu capture
+SAGEBWD_BWD_TRAFFIC = {
+    "attn_train B1 H32 N8192 D64 causal iid": 237.57e6 + 96.61e6,
+}
 
 
 def peaks():
@@ -484,7 +488,8 @@ def run_sagebwd(args, world, rank, local):
             "kernels": summ,
             "roofline": {"bound": "tensor", "kernel": "attn_bwd (dkdv_kernel)",
                          "achieved": summ["attn_bwd_tops"], "peak": fp16_peak, "unit": "TFLOP/s",
-                         "frac": summ["attn_bwd_frac_of_fp16_mma"], "traffic": None,
+                         "frac": summ["attn_bwd_frac_of_fp16_mma"], "traffic": SAGEBWD_BWD_TRAFFIC.get(w.name),
+                         "traffic_unit": "DRAM bytes (read + write) per attn_bwd launch, from ncu",
                          "peak_src": "measured live: FP16 mma.sync m16n8k16 (FP32 accumulate) probe, "
                                      "the instruction the kernels issue",
                          "bf16_tcgen05_measured_tflops": peaks()["bf16_tflops"]},
