@@ -47,6 +47,16 @@ using sagefp4::mbar_fence_init;
 using sagefp4::mbar_init;
 using sagefp4::mbar_try_wait;
 using sagefp4::smem_addr;
+using sagefp4::smem_desc;
+using sagefp4::tc_commit;
+using sagefp4::tc_fence_after;
+using sagefp4::tc_fence_before;
+using sagefp4::tmem_alloc;
+using sagefp4::tmem_dealloc;
+using sagefp4::tmem_ld32;
+using sagefp4::tmem_relinquish;
+using sagefp4::tmem_wait_ld;
+using sagefp4::kSwizzle128B;
 
 constexpr int kTok = 128;  // token block of Q, K, V, dO; key tile; key edge of a P / dS block
 constexpr int kQ = 64;     // query tile of the backward; query edge of a P / dS block
@@ -804,7 +814,92 @@ __global__ void __launch_bounds__(kThreads) dq_kernel(const float* __restrict__ 
   }
 }
 
+// ---------------------------------------------------------------- tcgen05
+// Instruction descriptor of tcgen05.mma kind::f16: FP16 A and B (formats 0),
+// FP32 accumulator (bits 4-5 = 1), both operands K-major, N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D[tmem] (+)= A x B^T, FP16 operands in shared memory (descriptors), K = 16.
+__device__ __forceinline__ void mma_f16_tc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Descriptor of a K-major FP16 operand whose rows are 128 bytes (64 values)
+// with the 128-byte swizzle (16-byte chunk ^ row & 7), rows of 8 at 1024-byte
+// strides, starting k0 values into the row (k0 a multiple of 16); the tile
+// must start on a 1024-byte boundary.
+__device__ __forceinline__ uint64_t desc_k64(uint32_t tile, int k0) {
+  return smem_desc(tile + 2 * k0, 16, 1024, kSwizzle128B);
+}
+
 // ---------------------------------------------------------------- probes
+// tcgen05 kind::f16 with the layouts the kernels use: one CTA of 4 warps
+// computes C [128][N] = A [128][64] x B [N][64]^T (FP16 in, FP32 out) from
+// row-major global inputs staged into swizzled shared memory.
+__global__ void __launch_bounds__(128) umma_probe_kernel(const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,
+                                                         int N, float* __restrict__ c, int32_t* status) {
+  __shared__ __align__(1024) uint8_t sa[128 * 128];
+  __shared__ __align__(1024) uint8_t sb[128 * 128];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tslot;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  for (int i = tid; i < 128 * 8; i += 128) {  // 16-byte chunks of A
+    const int r = i / 8, ch = i % 8;
+    *reinterpret_cast<uint4*>(sa + swz(r, 16 * ch, 128)) = *reinterpret_cast<const uint4*>(a + r * 64 + 8 * ch);
+  }
+  for (int i = tid; i < N * 8; i += 128) {
+    const int r = i / 8, ch = i % 8;
+    *reinterpret_cast<uint4*>(sb + swz(r, 16 * ch, 128)) = *reinterpret_cast<const uint4*>(b + r * 64 + 8 * ch);
+  }
+  if (tid == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_addr(&tslot), 128);
+    tmem_relinquish();
+  }
+  // generic-proxy writes of the operands -> visible to the tensor core
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tslot;
+  if (tid == 0) {
+    const uint32_t id = idesc_f16(128, N);
+#pragma unroll
+    for (int k = 0; k < 4; k++)
+      mma_f16_tc(tmem, desc_k64(smem_addr(sa), 16 * k), desc_k64(smem_addr(sb), 16 * k), id, k > 0);
+    tc_commit(smem_addr(&bar));
+  }
+  const Ctl ctl{status, 100ull * 1000ull * 1000ull};
+  const bool ok = waitw(smem_addr(&bar), 0, ctl);
+  tc_fence_after();
+  if (ok) {
+    const int row = 32 * warp + (tid & 31);
+    for (int c0 = 0; c0 < N; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + c0, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; j++) c[row * N + c0 + j] = __uint_as_float(r[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+
 // Integer products on the FP16 MMA: one warp computes the 16 x 8 product of
 // INT8 matrices a [16][K] and b [8][K] (both row-major, K a multiple of 16)
 // with the codes as FP16 values and FP32 accumulation, chained over K / 16
@@ -1156,6 +1251,15 @@ int sagebwd_stall_test(int kernel, void* out0, void* out1, int B, int H, int N, 
                 : launch_dkdv<128, false>(w, dkb, dvb, BH, N, scale, st, wait_limit_ns, 1);
   }
   return from_cuda(e);
+}
+
+int sagebwd_umma_probe(const uint16_t* a, const uint16_t* b, int N, float* c, int32_t* status, void* stream) {
+  if ((N != 64 && N != 128) || !aligned(a, 16) || !aligned(b, 16) || !aligned(c, 4) || !aligned(status, 4))
+    return SAGE_FP4_EINVAL;
+  const int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  umma_probe_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(a, b, N, c, status);
+  return from_cuda(cudaGetLastError());
 }
 
 int sagebwd_int_mma_probe(const int8_t* a, const int8_t* b, int K, float* out, void* stream) {

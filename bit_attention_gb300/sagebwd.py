@@ -54,6 +54,7 @@ def lib() -> ctypes.CDLL:
                 "sagebwd_attn_bwd": (i, [vp, vp, i, i, i, i, i, f, vp, sz, vp]),
                 "sagebwd_dq_out": (i, [vp, i, i, i, i, vp, sz, vp]),
                 "sagebwd_stall_test": (i, [i, vp, vp, i, i, i, i, f, ctypes.c_uint64, vp, sz, vp]),
+                "sagebwd_umma_probe": (i, [vp, vp, i, vp, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -117,6 +118,10 @@ def sagebwd_get_status(ws_ptr, B, H, N, D, stream) -> int:
 
 def sagebwd_mma_peak(kind: int, ctas: int, iters: int, scratch_ptr, stream) -> int:
     return lib().sagebwd_mma_peak(kind, ctas, iters, scratch_ptr, stream)
+
+
+def sagebwd_umma_probe(a_ptr, b_ptr, N: int, c_ptr, status_ptr, stream) -> int:
+    return lib().sagebwd_umma_probe(a_ptr, b_ptr, N, c_ptr, status_ptr, stream)
 
 
 def sagebwd_int_mma_probe(a_ptr, b_ptr, K: int, out_ptr, stream) -> int:

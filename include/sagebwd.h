@@ -128,6 +128,13 @@ int sagebwd_mma_peak(int kind, int ctas, int iters, void *scratch, void *stream)
 int sagebwd_stall_test(int kernel, void *out0, void *out1, int B, int H, int N, int D, float scale,
                        uint64_t wait_limit_ns, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Probe of the 5th-generation tensor-core form the backward uses (tcgen05.mma
+ * kind::f16 with the 128-byte-swizzled K-major operand layout): one CTA
+ * computes c [128][N] = a [128][64] x b [N][64]^T (FP16 in, FP32 out; all
+ * row-major device arrays; N = 64 or 128).  status: a device int32 that a
+ * wait that runs out sets to SAGE_FP4_ETIMEOUT. */
+int sagebwd_umma_probe(const uint16_t *a, const uint16_t *b, int N, float *c, int32_t *status, void *stream);
+
 /* Exactness probe of the INT8 products: the 16 x 8 product of INT8 device
  * matrices a [16][K] and b [8][K] (row-major, K a multiple of 16 up to 4096)
  * computed the kernels' way (codes as FP16 values, FP32 accumulation chained
