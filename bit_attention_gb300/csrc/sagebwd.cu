@@ -179,6 +179,7 @@ __device__ __forceinline__ uint16_t f2h_sat(float x) {
 struct Ws {
   uint16_t *qc, *kc, *vc, *doc;  // INT8 codes as FP16 values, swizzled rows
   uint16_t *vh, *doh;            // V and dO as FP16 values, swizzled rows
+  uint16_t *qct, *doct;          // Q^ and dO^ codes transposed: [64-token tile][D][64], swizzled rows
   float *sq, *sk, *sv, *sdo, *l2, *dd, *dqacc;
   int32_t* status;
 };
@@ -246,6 +247,21 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const uint16_t* __restr
     const int off = swz(r, 16 * c, 2 * D);
     *reinterpret_cast<uint4*>(cbase + off) = make_uint4(hc[0], hc[1], hc[2], hc[3]);
     if (kind >= 2) *reinterpret_cast<uint4*>(vbase + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+  }
+  if (kind == 0 || kind == 3) {
+    // the same codes transposed, per 64-token tile: [D rows][64 tokens], the
+    // K-major B operand of dK = dS^T Q and dV = P^T dO
+    uint16_t* tdst = kind == 0 ? ws.qct : ws.doct;
+    for (int i = tid; i < D * (kTok / 8); i += kThreads) {
+      const int d = i % D, c = i / D;  // c: 8-token chunk of the block
+      uint32_t h[4];
+#pragma unroll
+      for (int j = 0; j < 4; j++)
+        h[j] = h2(code(bf2f(xs[(8 * c + 2 * j) * D + d]), inv), code(bf2f(xs[(8 * c + 2 * j + 1) * D + d]), inv));
+      const int tile = (n0 + 8 * c) / kQ, within = (8 * c) % kQ;
+      char* tb = reinterpret_cast<char*>(tdst + hb + static_cast<size_t>(tile) * kQ * D);
+      *reinterpret_cast<uint4*>(tb + swz(d, 2 * within, 2 * kQ)) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
   }
   if (kind == 3) {
     // D_i = sum_d dO_id O_id and L in log2 units: one warp per row
@@ -794,26 +810,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// dQ accumulator (FP32, padded rows) -> bf16 [BH][N][D]
-template <int D>
-__global__ void __launch_bounds__(kThreads) dq_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq, int N,
-                                                      int BH) {
-  const int Np = (N + kTok - 1) / kTok * kTok;
-  const size_t total = static_cast<size_t>(BH) * N * D / 4;
-  for (size_t i = blockIdx.x * static_cast<size_t>(kThreads) + threadIdx.x; i < total;
-       i += static_cast<size_t>(gridDim.x) * kThreads) {
-    const size_t e = 4 * i;
-    const size_t row = e / D, d = e % D;
-    const size_t bh = row / N, n = row % N;
-    const float4 v = *reinterpret_cast<const float4*>(acc + (bh * Np + n) * D + d);
-    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-    uint2 w;
-    w.x = *reinterpret_cast<uint32_t*>(&lo);
-    w.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(dq + e) = w;
-  }
-}
-
 // ---------------------------------------------------------------- tcgen05
 // Instruction descriptor of tcgen05.mma kind::f16: FP16 A and B (formats 0),
 // FP32 accumulator (bits 4-5 = 1), both operands K-major, N >> 3 in bits
@@ -839,6 +835,491 @@ __device__ __forceinline__ void mma_f16_tc(uint32_t d_tmem, uint64_t a_desc, uin
 // must start on a 1024-byte boundary.
 __device__ __forceinline__ uint64_t desc_k64(uint32_t tile, int k0) {
   return smem_desc(tile + 2 * k0, 16, 1024, kSwizzle128B);
+}
+
+// ---------------------------------------------------------------- backward, tcgen05 (D = 64)
+// The same backward with the four products that have 128 keys as rows --
+// S^T = K^ Q^^T, dP^T = V dO^T, dV = P^^T dO^ and dK = dS^^T Q^ -- on the
+// 5th-generation tensor cores: one thread issues them asynchronously into
+// tensor memory (M = 128 keys, N = 64, K = 16 per instruction) while other
+// warps work.  The warpgroups of the CTA:
+//   0  warp 0: bulk copies; warp 1: tensor-memory allocation and MMA issue
+//   1, 2  softmax: each thread owns one key row and half of the tile's 64
+//      query columns; P^T and dS^T from the S^T and dP^T rows in tensor
+//      memory, their block maxima (one vote of the eight warps each), their
+//      INT8 codes written to shared memory as the A operands of dV and dK
+//      (and dS^T read again by dQ)
+//   3  folds each tile's dV and dK partials (tensor memory) into registers
+//      with the tile's block scales, and computes dQ (16 query rows a warp)
+// dQ = dS^ K^ (64 queries as rows) stays on the warp-level MMA, from the
+// staged dS^ codes and the resident K^ tile, added to the FP32 accumulator.
+// Tensor memory: S^T, dP^T, dV and dK partials, each double-buffered (512
+// columns).  Every wait is bounded; a wait that runs out sets the status
+// word and an abort flag that ends every role's loop.
+constexpr int kTcThreads = 512;
+constexpr int kTcStages = 3;
+struct TcRegs {
+  static constexpr uint32_t kCtl = 48, kSoft = 128, kFold = 208;
+};
+static_assert(TcRegs::kCtl * 128 + TcRegs::kSoft * 256 + TcRegs::kFold * 128 == 65536, "register split");
+
+struct TcSmem {
+  static constexpr int kTile = 128 * 128;  // 128 rows of 128 bytes
+  static constexpr int kK = 0;             // K^ codes [128 keys][64]
+  static constexpr int kV = kTile;         // FP16 V [128 keys][64]
+  static constexpr int kStageOff = 2 * kTile;
+  // stage: Q^ [64 q][64], FP16 dO [64 q][64], Q^T [64 d][64 q], dO^T [64 d][64 q], L, D
+  static constexpr int kSQ = 0, kSDoh = 8192, kSQt = 16384, kSDot = 24576, kSL = 32768, kSD = 33024;
+  static constexpr int kStage = 33792;  // a multiple of 1024
+  static constexpr int kCodesOff = kStageOff + kTcStages * kStage;
+  // codes buffer: P^T [128 keys][64 q], dS^T [128 keys][64 q]
+  static constexpr int kCP = 0, kCS = kTile, kCodes = 2 * kTile;
+  static constexpr int kBarOff = kCodesOff + 2 * kCodes;
+  static constexpr int kNumBars = 32;
+  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // tmem slot, abort flag, red[2][2][8], scal[2][4]
+  static constexpr int kBytes = kMiscOff + 256;
+  static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
+};
+// mbarrier indices
+enum {
+  TB_FIXED = 0,
+  TB_FULL = 1,             // + stage
+  TB_EMPTY = 1 + kTcStages,  // + stage
+  TB_SDONE = 1 + 2 * kTcStages,  // + buffer (2)
+  TB_SFREE = TB_SDONE + 2,
+  TB_CFULL = TB_SFREE + 2,
+  TB_CEMPTY = TB_CFULL + 2,
+  TB_PDONE = TB_CEMPTY + 2,
+  TB_PFREE = TB_PDONE + 2,
+  TB_DRAIN = TB_PFREE + 2,
+  TB_COUNT
+};
+static_assert(TB_COUNT <= TcSmem::kNumBars, "barriers");
+// tensor-memory columns
+constexpr uint32_t kTcS = 0, kTcDp = 128, kTcDv = 256, kTcDk = 384;
+
+// Bounded warp-wide wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool waitw_ab(uint32_t bar, uint32_t parity, const Ctl& c, volatile int* abort) {
+  if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+    int stop = 0;
+    if ((threadIdx.x & 31) == 0) {
+      if (*abort) {
+        stop = 1;
+      } else if (globaltimer_ns() - t0 > c.limit) {
+        *abort = 1;
+        atomicCAS(c.status, 0, SAGE_FP4_ETIMEOUT);
+        stop = 1;
+      }
+    }
+    if (__shfl_sync(kFull, stop, 0)) return false;
+  }
+}
+
+// The same for a single thread.
+__device__ __forceinline__ bool wait1_ab(uint32_t bar, uint32_t parity, const Ctl& c, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > c.limit) {
+      *abort = 1;
+      atomicCAS(c.status, 0, SAGE_FP4_ETIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive1(uint32_t bar) { sagefp4::mbar_arrive(bar); }
+
+// All 256 threads of the two softmax warpgroups: AND of `ok` over them
+// (named barrier 1).
+__device__ __forceinline__ bool group_and(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.and.pred q, 1, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(ok))
+      : "memory");
+  return r != 0;
+}
+
+// Each thread of the warp reads 16 consecutive FP32 columns of its lane.
+__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  sagefp4::tmem_ld16(taddr, r);
+  tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+
+template <bool kCausal>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    dkdv_tc_kernel(Ws ws, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int N, float scale, uint64_t wait_ns,
+                   int withhold) {
+  constexpr int D = 64;
+  using L = TcSmem;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte aligned base, by pointer arithmetic on the shared array (so
+  // that the compiler keeps its accesses in the shared state space)
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_addr(smem);
+  const int nkt = (N + kTok - 1) / kTok;
+  const int Np = nkt * kTok;
+  const int nqt = Np / kQ;
+  const int kb = blockIdx.x, bh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wg = warp >> 2;
+  const size_t hb = static_cast<size_t>(bh) * Np * D;
+  const size_t hrow = static_cast<size_t>(bh) * Np;
+  const int q0 = kCausal ? 2 * kb : 0;
+  const int niter = nqt - q0;
+  const Ctl ctl{ws.status, wait_ns};
+  auto bar = [&](int i) { return sbase + L::kBarOff + 8 * i; };
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  float* red = reinterpret_cast<float*>(smem + L::kMiscOff + 16);    // [2 parity][2 kinds][8 warps]
+  float* scal = reinterpret_cast<float*>(smem + L::kMiscOff + 160);  // [2 buffers][4]
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(TB_FIXED), 1);
+    for (int s = 0; s < kTcStages; s++) {
+      mbar_init(bar(TB_FULL + s), 1);
+      mbar_init(bar(TB_EMPTY + s), 1 + 8);  // the MMA commit + the softmax warps
+    }
+    for (int b = 0; b < 2; b++) {
+      mbar_init(bar(TB_SDONE + b), 1);
+      mbar_init(bar(TB_SFREE + b), 8);
+      mbar_init(bar(TB_CFULL + b), 8);
+      mbar_init(bar(TB_CEMPTY + b), 1 + 4);  // the MMA commit + the dQ warps
+      mbar_init(bar(TB_PDONE + b), 1);
+      mbar_init(bar(TB_PFREE + b), 4);
+    }
+    mbar_init(bar(TB_DRAIN), 1);
+    *abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tslot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (wg == 0) {
+    sagefp4::regs_dec<TcRegs::kCtl>();
+    if (warp == 0 && lane == 0) {
+      // ---- producer
+      const size_t off = hb + static_cast<size_t>(kb) * kTok * D;
+      mbar_arrive_expect_tx(bar(TB_FIXED), 2 * L::kTile);
+      bulk_load(sbase + L::kK, ws.kc + off, L::kTile, bar(TB_FIXED));
+      bulk_load(sbase + L::kV, ws.vh + off, L::kTile, bar(TB_FIXED));
+      const bool held = withhold && blockIdx.x == 0 && blockIdx.y == 0;
+      int issued = 0;
+      for (int it = 0; it < niter; it++) {
+        const int s = it % kTcStages;
+        if (it >= kTcStages && !wait1_ab(bar(TB_EMPTY + s), ((it / kTcStages) - 1) & 1, ctl, abort)) break;
+        if (held && it == 0) continue;  // failure-detection test: this tile never arrives
+        const int qtile = q0 + it;
+        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+        const size_t qo = hb + static_cast<size_t>(qtile) * kQ * D;
+        mbar_arrive_expect_tx(bar(TB_FULL + s), 4 * 8192 + 512);
+        bulk_load(st + L::kSQ, ws.qc + qo, 8192, bar(TB_FULL + s));
+        bulk_load(st + L::kSDoh, ws.doh + qo, 8192, bar(TB_FULL + s));
+        bulk_load(st + L::kSQt, ws.qct + qo, 8192, bar(TB_FULL + s));
+        bulk_load(st + L::kSDot, ws.doct + qo, 8192, bar(TB_FULL + s));
+        bulk_load(st + L::kSL, ws.l2 + hrow + static_cast<size_t>(qtile) * kQ, 256, bar(TB_FULL + s));
+        bulk_load(st + L::kSD, ws.dd + hrow + static_cast<size_t>(qtile) * kQ, 256, bar(TB_FULL + s));
+        issued = it + 1;
+      }
+      if (*abort) {
+        // let every copy this thread issued land before the CTA exits
+        for (int last = issued - 1; last >= 0 && last >= issued - kTcStages; last--)
+          if (!(held && last == 0)) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar(TB_FULL + last % kTcStages), (last / kTcStages) & 1) &&
+                   globaltimer_ns() - t0 < ctl.limit) {
+            }
+          }
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar(TB_FIXED), 0) && globaltimer_ns() - t0 < ctl.limit) {
+        }
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---- MMA issue
+      const uint32_t id = idesc_f16(128, 64);
+      bool ok = wait1_ab(bar(TB_FIXED), 0, ctl, abort);
+      auto issue_sdp = [&](int it) {
+        const int s = it % kTcStages, b = it & 1;
+        if (!wait1_ab(bar(TB_FULL + s), (it / kTcStages) & 1, ctl, abort)) return false;
+        if (it >= 2 && !wait1_ab(bar(TB_SFREE + b), ((it >> 1) - 1) & 1, ctl, abort)) return false;
+        tc_fence_after();
+        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          mma_f16_tc(tmem + kTcS + 64 * b, desc_k64(sbase + L::kK, 16 * k), desc_k64(st + L::kSQ, 16 * k), id, k > 0);
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          mma_f16_tc(tmem + kTcDp + 64 * b, desc_k64(sbase + L::kV, 16 * k), desc_k64(st + L::kSDoh, 16 * k), id,
+                     k > 0);
+        tc_commit(bar(TB_SDONE + b));
+        return true;
+      };
+      if (ok) ok = issue_sdp(0);
+      for (int it = 0; ok && it < niter; it++) {
+        const int s = it % kTcStages, b = it & 1;
+        if (it + 1 < niter && !(ok = issue_sdp(it + 1))) break;
+        if (!(ok = wait1_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort))) break;
+        if (it >= 2 && !(ok = wait1_ab(bar(TB_PFREE + b), ((it >> 1) - 1) & 1, ctl, abort))) break;
+        tc_fence_after();
+        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+        const uint32_t cb = sbase + L::kCodesOff + b * L::kCodes;
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          mma_f16_tc(tmem + kTcDv + 64 * b, desc_k64(cb + L::kCP, 16 * k), desc_k64(st + L::kSDot, 16 * k), id,
+                     k > 0);
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          mma_f16_tc(tmem + kTcDk + 64 * b, desc_k64(cb + L::kCS, 16 * k), desc_k64(st + L::kSQt, 16 * k), id,
+                     k > 0);
+        tc_commit(bar(TB_PDONE + b));
+        tc_commit(bar(TB_EMPTY + s));
+        tc_commit(bar(TB_CEMPTY + b));
+      }
+      // every MMA issued has completed before tensor memory is released
+      tc_commit(bar(TB_DRAIN));
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar(TB_DRAIN), 0) && globaltimer_ns() - t0 < ctl.limit) {
+      }
+    }
+  } else if (wg == 1 || wg == 2) {
+    // ---- softmax: this thread's key row, query columns 32h..32h+31
+    sagefp4::regs_inc<TcRegs::kSoft>();
+    const int h = wg - 1;
+    const int row = 32 * (warp & 3) + lane;     // 0..127
+    const int sw = 4 * h + (warp & 3);          // softmax warp 0..7
+    const uint32_t lanebase = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int key = kb * kTok + row;
+    const float sk = ws.sk[static_cast<size_t>(bh) * nkt + kb];
+    const float c2base = sk * scale * kLog2e;
+    // the query tile's block scales, read one tile ahead
+    float sq_next = ws.sq[static_cast<size_t>(bh) * nkt + (q0 >> 1)];
+    float sdo_next = ws.sdo[static_cast<size_t>(bh) * nkt + (q0 >> 1)];
+    for (int it = 0; it < niter; it++) {
+      const int s = it % kTcStages, b = it & 1, qtile = q0 + it;
+      const float sq = sq_next, sdo = sdo_next;
+      if (it + 1 < niter) {
+        sq_next = ws.sq[static_cast<size_t>(bh) * nkt + ((qtile + 1) >> 1)];
+        sdo_next = ws.sdo[static_cast<size_t>(bh) * nkt + ((qtile + 1) >> 1)];
+      }
+      bool ok = waitw_ab(bar(TB_SDONE + b), (it >> 1) & 1, ctl, abort) &&
+                waitw_ab(bar(TB_FULL + s), (it / kTcStages) & 1, ctl, abort);
+      if (!group_and(ok)) break;
+      tc_fence_after();
+      // this half of the S^T and dP^T rows: two loads in flight, one wait
+      uint32_t ru[2][32];
+      tmem_ld32(tmem + lanebase + kTcS + 64 * b + 32 * h, ru[0]);
+      tmem_ld32(tmem + lanebase + kTcDp + 64 * b + 32 * h, ru[1]);
+      tmem_wait_ld();
+      float p[32], dp[32];
+#pragma unroll
+      for (int i = 0; i < 32; i++) {
+        p[i] = __uint_as_float(ru[0][i]);
+        dp[i] = __uint_as_float(ru[1][i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(TB_SFREE + b));
+      // P^T = exp2(S^T c - L); masked and padded entries 0; dS^T = P^T o (dP^T - D)
+      const float* Ls = reinterpret_cast<const float*>(smem + L::kStageOff + s * L::kStage + L::kSL) + 32 * h;
+      const float* Ds = reinterpret_cast<const float*>(smem + L::kStageOff + s * L::kStage + L::kSD) + 32 * h;
+      const float c2 = c2base * sq;
+      const bool edge = (kCausal && qtile <= 2 * kb + 1) || (qtile * kQ + kQ > N) || (kb * kTok + kTok > N);
+      float pmax = 0.0f, smax = 0.0f;
+#pragma unroll
+      for (int q4 = 0; q4 < 8; q4++) {
+        const float4 l4 = reinterpret_cast<const float4*>(Ls)[q4];
+        const float4 d4 = reinterpret_cast<const float4*>(Ds)[q4];
+        const float lq[4] = {l4.x, l4.y, l4.z, l4.w}, dq[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+          const int q = 4 * q4 + e;
+          float v = ex2(fmaf(p[q], c2, -lq[e]));
+          if (edge) {
+            const int query = qtile * kQ + 32 * h + q;
+            if (query >= N || key >= N || (kCausal && key > query)) v = 0.0f;
+          }
+          p[q] = v;
+          pmax = fmaxf(pmax, v);
+          dp[q] = v * (dp[q] - dq[e]);
+          smax = fmaxf(smax, fabsf(dp[q]));
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(TB_EMPTY + s));  // L and D read
+      pmax = warp_max(pmax);
+      smax = warp_max(smax);
+      if (lane == 0) {
+        red[(b * 2 + 0) * 8 + sw] = pmax;
+        red[(b * 2 + 1) * 8 + sw] = smax;
+      }
+      // the codes buffer is free once dV, dK (tile it - 2) and dQ have read it
+      ok = it < 2 || waitw_ab(bar(TB_CEMPTY + b), ((it >> 1) - 1) & 1, ctl, abort);
+      if (!group_and(ok)) break;  // also publishes red[]
+      float pa = red[(b * 2) * 8], sa = red[(b * 2 + 1) * 8];
+#pragma unroll
+      for (int w = 1; w < 8; w++) {
+        pa = fmaxf(pa, red[(b * 2) * 8 + w]);
+        sa = fmaxf(sa, red[(b * 2 + 1) * 8 + w]);
+      }
+      const float pinv = pa > 0.0f ? __fdiv_rn(127.0f, pa) : 0.0f;
+      const float sinv = sa > 0.0f ? __fdiv_rn(127.0f, sa) : 0.0f;
+      uint8_t* cbuf = smem + L::kCodesOff + b * L::kCodes;
+#pragma unroll
+      for (int ch = 0; ch < 4; ch++) {
+        uint4 wp, wsd;
+        wp.x = h2(code(p[8 * ch + 0], pinv), code(p[8 * ch + 1], pinv));
+        wp.y = h2(code(p[8 * ch + 2], pinv), code(p[8 * ch + 3], pinv));
+        wp.z = h2(code(p[8 * ch + 4], pinv), code(p[8 * ch + 5], pinv));
+        wp.w = h2(code(p[8 * ch + 6], pinv), code(p[8 * ch + 7], pinv));
+        wsd.x = h2(code(dp[8 * ch + 0], sinv), code(dp[8 * ch + 1], sinv));
+        wsd.y = h2(code(dp[8 * ch + 2], sinv), code(dp[8 * ch + 3], sinv));
+        wsd.z = h2(code(dp[8 * ch + 4], sinv), code(dp[8 * ch + 5], sinv));
+        wsd.w = h2(code(dp[8 * ch + 6], sinv), code(dp[8 * ch + 7], sinv));
+        *reinterpret_cast<uint4*>(cbuf + L::kCP + swz(row, 64 * h + 16 * ch, 128)) = wp;
+        *reinterpret_cast<uint4*>(cbuf + L::kCS + swz(row, 64 * h + 16 * ch, 128)) = wsd;
+      }
+      if (threadIdx.x == 128) {
+        const float sp = __fdiv_rn(pa, 127.0f), sds = __fdiv_rn(sa, 127.0f);
+        scal[4 * b + 0] = sp * sdo;          // dV
+        scal[4 * b + 1] = sds * sq;          // dK (the softmax scale comes at the end)
+        scal[4 * b + 2] = sds * sk * scale;  // dQ
+      }
+      // the codes (generic-proxy writes) -> visible to the tensor core
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(TB_CFULL + b));
+    }
+  } else {
+    // ---- dV and dK folds, and dQ (warpgroup 3)
+    sagefp4::regs_inc<TcRegs::kFold>();
+    const int row = 32 * (warp & 3) + lane;  // key row of the folds
+    const uint32_t lanebase = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int g = lane >> 2, t = lane & 3, j = lane >> 3;
+    const int r0 = 16 * (warp & 3);  // this warp's 16 dQ rows
+    float accv[64], acck[64];
+#pragma unroll
+    for (int i = 0; i < 64; i++) accv[i] = acck[i] = 0.0f;
+    for (int it = 0; it < niter; it++) {
+      const int b = it & 1, qtile = q0 + it;
+      if (!waitw_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort)) break;
+      const float f_dv = scal[4 * b + 0], f_dk = scal[4 * b + 1], f_dq = scal[4 * b + 2];
+      // dQ[64 x 64] += f_dq (dS^ K^): this warp's 16 rows, 32 columns at a
+      // time; dS^ and K^ read transposed
+      const uint32_t dsb = sbase + L::kCodesOff + b * L::kCodes + L::kCS;
+#pragma unroll
+      for (int dh = 0; dh < D; dh += 32) {
+        float q4[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) q4[i][0] = q4[i][1] = q4[i][2] = q4[i][3] = 0.0f;
+#pragma unroll
+        for (int kc = 0; kc < kTok / 16; kc++) {
+          uint32_t a[4];
+          ldsm_x4_t(dsb + swz(16 * kc + ((j >> 1) << 3) + (lane & 7), 2 * (r0 + ((j & 1) << 3)), 128), a[0], a[1],
+                    a[2], a[3]);
+#pragma unroll
+          for (int nd = 0; nd < 4; nd += 2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(sbase + L::kK + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 2 * dh + 16 * (nd + (j >> 1)), 128),
+                      b0, b1, b2, b3);
+            mma_f16(q4[nd], a, b0, b1);
+            mma_f16(q4[nd + 1], a, b2, b3);
+          }
+        }
+        float* dq0 = ws.dqacc + (hrow + static_cast<size_t>(qtile) * kQ + r0 + g) * D + dh + 2 * t;
+#pragma unroll
+        for (int nd = 0; nd < 4; nd++) {
+          red_add_v2(dq0 + 8 * nd, q4[nd][0] * f_dq, q4[nd][1] * f_dq);
+          red_add_v2(dq0 + 8 * D + 8 * nd, q4[nd][2] * f_dq, q4[nd][3] * f_dq);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(TB_CEMPTY + b));
+      // fold this tile's partials
+      if (!waitw_ab(bar(TB_PDONE + b), (it >> 1) & 1, ctl, abort)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int qc = 0; qc < 4; qc++) {
+        uint32_t rv[16], rk[16];
+        sagefp4::tmem_ld16(tmem + lanebase + kTcDv + 64 * b + 16 * qc, rv);
+        sagefp4::tmem_ld16(tmem + lanebase + kTcDk + 64 * b + 16 * qc, rk);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+          accv[16 * qc + i] = fmaf(__uint_as_float(rv[i]), f_dv, accv[16 * qc + i]);
+          acck[16 * qc + i] = fmaf(__uint_as_float(rk[i]), f_dk, acck[16 * qc + i]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(TB_PFREE + b));
+    }
+    if (!*abort) {
+      const int key = kb * kTok + row;
+      if (key < N) {
+#pragma unroll
+        for (int which = 0; which < 2; which++) {
+          uint16_t* dst = (which == 0 ? dv : dk) + (static_cast<size_t>(bh) * N + key) * D;
+          const float f = which == 0 ? 1.0f : scale;
+          const float* acc = which == 0 ? accv : acck;
+#pragma unroll
+          for (int c = 0; c < 8; c++) {
+            uint4 w;
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(acc[8 * c + 0] * f, acc[8 * c + 1] * f);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(acc[8 * c + 2] * f, acc[8 * c + 3] * f);
+            __nv_bfloat162 h2v = __floats2bfloat162_rn(acc[8 * c + 4] * f, acc[8 * c + 5] * f);
+            __nv_bfloat162 h3 = __floats2bfloat162_rn(acc[8 * c + 6] * f, acc[8 * c + 7] * f);
+            w.x = *reinterpret_cast<uint32_t*>(&h0);
+            w.y = *reinterpret_cast<uint32_t*>(&h1);
+            w.z = *reinterpret_cast<uint32_t*>(&h2v);
+            w.w = *reinterpret_cast<uint32_t*>(&h3);
+            *reinterpret_cast<uint4*>(dst + 8 * c) = w;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// dQ accumulator (FP32, padded rows) -> bf16 [BH][N][D]
+template <int D>
+__global__ void __launch_bounds__(kThreads) dq_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq, int N,
+                                                      int BH) {
+  const int Np = (N + kTok - 1) / kTok * kTok;
+  const size_t total = static_cast<size_t>(BH) * N * D / 4;
+  for (size_t i = blockIdx.x * static_cast<size_t>(kThreads) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * kThreads) {
+    const size_t e = 4 * i;
+    const size_t row = e / D, d = e % D;
+    const size_t bh = row / N, n = row % N;
+    const float4 v = *reinterpret_cast<const float4*>(acc + (bh * Np + n) * D + d);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 w;
+    w.x = *reinterpret_cast<uint32_t*>(&lo);
+    w.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dq + e) = w;
+  }
 }
 
 // ---------------------------------------------------------------- probes
@@ -978,6 +1459,7 @@ Layout layout(int B, int H, int N, int D) {
   const size_t sizes[SAGEBWD_WS_FIELDS] = {
       rows,        rows,        rows,        rows,         // Q^, K^, V^, dO^ codes
       rows,        rows,                                   // V, dO as FP16
+      rows,        rows,                                   // Q^, dO^ codes transposed per 64-token tile
       4 * BH * nb, 4 * BH * nb, 4 * BH * nb, 4 * BH * nb,  // Q, K, V, dO block scales
       4 * BH * Np, 4 * BH * Np,                            // L (log2 units), D = rowsum(dO o O)
       4 * BH * Np * D,                                     // dQ accumulator
@@ -1002,14 +1484,16 @@ Ws carve(void* base, const Layout& l) {
   w.doc = reinterpret_cast<uint16_t*>(b + l.off[3]);
   w.vh = reinterpret_cast<uint16_t*>(b + l.off[4]);
   w.doh = reinterpret_cast<uint16_t*>(b + l.off[5]);
-  w.sq = reinterpret_cast<float*>(b + l.off[6]);
-  w.sk = reinterpret_cast<float*>(b + l.off[7]);
-  w.sv = reinterpret_cast<float*>(b + l.off[8]);
-  w.sdo = reinterpret_cast<float*>(b + l.off[9]);
-  w.l2 = reinterpret_cast<float*>(b + l.off[10]);
-  w.dd = reinterpret_cast<float*>(b + l.off[11]);
-  w.dqacc = reinterpret_cast<float*>(b + l.off[12]);
-  w.status = reinterpret_cast<int32_t*>(b + l.off[13]);
+  w.qct = reinterpret_cast<uint16_t*>(b + l.off[6]);
+  w.doct = reinterpret_cast<uint16_t*>(b + l.off[7]);
+  w.sq = reinterpret_cast<float*>(b + l.off[8]);
+  w.sk = reinterpret_cast<float*>(b + l.off[9]);
+  w.sv = reinterpret_cast<float*>(b + l.off[10]);
+  w.sdo = reinterpret_cast<float*>(b + l.off[11]);
+  w.l2 = reinterpret_cast<float*>(b + l.off[12]);
+  w.dd = reinterpret_cast<float*>(b + l.off[13]);
+  w.dqacc = reinterpret_cast<float*>(b + l.off[14]);
+  w.status = reinterpret_cast<int32_t*>(b + l.off[15]);
   return w;
 }
 
@@ -1060,6 +1544,23 @@ cudaError_t launch_dkdv(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int N, 
   if (e != cudaSuccess) return e;
   const dim3 grid((N + kTok - 1) / kTok, BH);
   dkdv_kernel<D, C><<<grid, kThreads, smem, st>>>(w, dk, dv, N, scale, wait_ns, withhold);
+  return cudaGetLastError();
+}
+
+// The tcgen05 backward (D = 64).  Its warpgroups' setmaxnreg budgets add up
+// to exactly 128 registers per thread at launch; with any other allocation
+// an increase would never be granted, so it refuses to launch.
+template <bool C>
+cudaError_t launch_dkdv_tc(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int N, float scale, cudaStream_t st,
+                           uint64_t wait_ns, int withhold) {
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, dkdv_tc_kernel<C>);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs != 65536 / kTcThreads) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(dkdv_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::kAlloc);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((N + kTok - 1) / kTok, BH);
+  dkdv_tc_kernel<C><<<grid, kTcThreads, TcSmem::kAlloc, st>>>(w, dk, dv, N, scale, wait_ns, withhold);
   return cudaGetLastError();
 }
 
@@ -1164,8 +1665,8 @@ int sagebwd_attn_bwd(void* dk, void* dv, int B, int H, int N, int D, int causal,
   const int BH = B * H;
   cudaError_t e;
   if (D == 64)
-    e = causal ? launch_dkdv<64, true>(w, dkb, dvb, BH, N, scale, st)
-               : launch_dkdv<64, false>(w, dkb, dvb, BH, N, scale, st);
+    e = causal ? launch_dkdv_tc<true>(w, dkb, dvb, BH, N, scale, st, kWaitNs, 0)
+               : launch_dkdv_tc<false>(w, dkb, dvb, BH, N, scale, st, kWaitNs, 0);
   else
     e = causal ? launch_dkdv<128, true>(w, dkb, dvb, BH, N, scale, st)
                : launch_dkdv<128, false>(w, dkb, dvb, BH, N, scale, st);
@@ -1247,7 +1748,7 @@ int sagebwd_stall_test(int kernel, void* out0, void* out1, int B, int H, int N, 
                 : launch_fwd<128, false>(w, o, lse, BH, N, scale, st, wait_limit_ns, 1);
   } else {
     uint16_t *dkb = static_cast<uint16_t*>(out0), *dvb = static_cast<uint16_t*>(out1);
-    e = D == 64 ? launch_dkdv<64, false>(w, dkb, dvb, BH, N, scale, st, wait_limit_ns, 1)
+    e = D == 64 ? launch_dkdv_tc<false>(w, dkb, dvb, BH, N, scale, st, wait_limit_ns, 1)
                 : launch_dkdv<128, false>(w, dkb, dvb, BH, N, scale, st, wait_limit_ns, 1);
   }
   return from_cuda(e);

@@ -28,3 +28,13 @@ def decode_codes(region: np.ndarray, BH: int, Np: int, D: int) -> np.ndarray:
     h = decode_half(region, BH, Np, D).astype(np.float64)
     assert np.all(h == np.rint(h)) and np.abs(h).max() <= 127
     return h.astype(np.int8)
+
+
+def decode_codes_t(region: np.ndarray, BH: int, Np: int, D: int) -> np.ndarray:
+    """Transposed code tiles ([64-token tile][D][64], rows of 128 bytes,
+    swizzled) -> int8 [BH, Np, D] in token order."""
+    t = region[:BH * Np * D * 2].reshape(BH, Np // 64, D * 128)
+    h = np.ascontiguousarray(t[:, :, _swz_index(D, 128)]).view(np.float16).reshape(BH, Np // 64, D, 64)
+    h = h.astype(np.float64)
+    assert np.all(h == np.rint(h)) and np.abs(h).max() <= 127
+    return h.transpose(0, 1, 3, 2).reshape(BH, Np, D).astype(np.int8)

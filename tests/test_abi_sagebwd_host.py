@@ -26,7 +26,7 @@ def test_workspace_layout():
     rc, offs = SB.sagebwd_workspace_layout(B, H, N, D)
     assert rc == S.OK and len(offs) == SB.WS_FIELDS
     total = SB.sagebwd_workspace_bytes(B, H, N, D)
-    sizes = [2 * BH * Np * D] * 6 + [4 * BH * 3] * 4 + [4 * BH * Np] * 2 + [4 * BH * Np * D, 256]
+    sizes = [2 * BH * Np * D] * 8 + [4 * BH * 3] * 4 + [4 * BH * Np] * 2 + [4 * BH * Np * D, 256]
     assert offs[0] == 0
     for i, sz in enumerate(sizes):
         assert offs[i] % 256 == 0

@@ -39,7 +39,7 @@ import torch
 import oracle
 from bit_attention_gb300 import sagebwd as SB
 from bit_attention_gb300.synth import TRAIN_WORKLOADS, make_dout, make_qkv
-from sagebwd_layout import decode_codes, decode_half
+from sagebwd_layout import decode_codes, decode_codes_t, decode_half
 
 pytestmark = pytest.mark.gpu
 
@@ -129,6 +129,8 @@ def test_quantized_operands_are_bit_exact(N, D):
         want = np.zeros((BH, Np, D), np.int8)
         want[:, :N] = codes
         assert np.array_equal(decode_codes(region(f"{name}_codes"), BH, Np, D), want), name
+        if name in ("q", "do"):
+            assert np.array_equal(decode_codes_t(region(f"{name}_codes_t"), BH, Np, D), want), name
         got_s = region(f"{name}_scales")[:BH * (Np // 128) * 4].view(np.float32).reshape(BH, Np // 128)
         assert np.array_equal(got_s, scales), name
     for name, x in (("v_half", v), ("do_half", do)):
