@@ -48,6 +48,13 @@ using sagefp4::mbar_init;
 using sagefp4::mbar_try_wait;
 using sagefp4::smem_addr;
 using sagefp4::smem_desc;
+using sagefp4::add2;
+using sagefp4::fma2;
+using sagefp4::hi2;
+using sagefp4::lo2;
+using sagefp4::max3f;
+using sagefp4::mul2;
+using sagefp4::pack2;
 using sagefp4::tc_commit;
 using sagefp4::tc_fence_after;
 using sagefp4::tc_fence_before;
@@ -187,7 +194,7 @@ struct Ws {
 // ---------------------------------------------------------------- quantizer
 // One CTA per (128-token block, head).  kind 0: Q, 1: K, 2: V (codes and the
 // FP16 values), 3: dO (codes and FP16 values), with D_i = sum_d dO_id O_id,
-// the log2-domain log-sum-exp, and dQ's accumulator rows zeroed.
+// the negated log-sum-exp in log2 units, and dQ's accumulator rows zeroed.
 template <int D>
 __global__ void __launch_bounds__(kThreads) quant_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                                                          const uint16_t* __restrict__ v, const uint16_t* __restrict__ o,
@@ -264,7 +271,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const uint16_t* __restr
     }
   }
   if (kind == 3) {
-    // D_i = sum_d dO_id O_id and L in log2 units: one warp per row
+    // D_i = sum_d dO_id O_id and -L in log2 units: one warp per row
     const int warp = tid >> 5, lane = tid & 31;
     for (int r = warp; r < kTok; r += kThreads / 32) {
       float acc = 0.0f;
@@ -277,7 +284,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const uint16_t* __restr
       if (lane == 0) {
         const size_t ix = static_cast<size_t>(bh) * Np + n0 + r;
         ws.dd[ix] = acc;
-        ws.l2[ix] = r < rows ? lse[static_cast<size_t>(bh) * N + n0 + r] * kLog2e : 0.0f;
+        ws.l2[ix] = r < rows ? -lse[static_cast<size_t>(bh) * N + n0 + r] * kLog2e : 0.0f;
       }
     }
     float4* acc = reinterpret_cast<float4*>(ws.dqacc + (static_cast<size_t>(bh) * Np + n0) * D);
@@ -669,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 lq = *reinterpret_cast<const float2*>(Ls + qc);
 #pragma unroll
       for (int e = 0; e < 4; e++) {
-        float v = ex2(fmaf(p[nb][e], c2, -((e & 1) ? lq.y : lq.x)));
+        float v = ex2(fmaf(p[nb][e], c2, (e & 1) ? lq.y : lq.x));  // lq holds -L
         if (edge) {
           const int query = qtile * kQ + qc + (e & 1);
           const int key = key0 + ((e >> 1) << 3);
@@ -1142,26 +1149,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float* Ds = reinterpret_cast<const float*>(smem + L::kStageOff + s * L::kStage + L::kSD) + 32 * h;
       const float c2 = c2base * sq;
       const bool edge = (kCausal && qtile <= 2 * kb + 1) || (qtile * kQ + kQ > N) || (kb * kTok + kTok > N);
-      float pmax = 0.0f, smax = 0.0f;
+      // (pairs of columns through the packed FP32 forms, each lane rounded
+      // like its scalar form; Ls holds -L)
+      float pmax = 0.0f, smax = 0.0f, smin = 0.0f;
+      const uint64_t cc = pack2(c2, c2);
 #pragma unroll
       for (int q4 = 0; q4 < 8; q4++) {
         const float4 l4 = reinterpret_cast<const float4*>(Ls)[q4];
         const float4 d4 = reinterpret_cast<const float4*>(Ds)[q4];
-        const float lq[4] = {l4.x, l4.y, l4.z, l4.w}, dq[4] = {d4.x, d4.y, d4.z, d4.w};
+        const uint64_t l01 = pack2(l4.x, l4.y), l23 = pack2(l4.z, l4.w);
+        const int q = 4 * q4;
+        const uint64_t x01 = fma2(pack2(p[q], p[q + 1]), cc, l01), x23 = fma2(pack2(p[q + 2], p[q + 3]), cc, l23);
+        float v[4] = {ex2(lo2(x01)), ex2(hi2(x01)), ex2(lo2(x23)), ex2(hi2(x23))};
+        if (edge) {
 #pragma unroll
-        for (int e = 0; e < 4; e++) {
-          const int q = 4 * q4 + e;
-          float v = ex2(fmaf(p[q], c2, -lq[e]));
-          if (edge) {
-            const int query = qtile * kQ + 32 * h + q;
-            if (query >= N || key >= N || (kCausal && key > query)) v = 0.0f;
+          for (int e = 0; e < 4; e++) {
+            const int query = qtile * kQ + 32 * h + q + e;
+            if (query >= N || key >= N || (kCausal && key > query)) v[e] = 0.0f;
           }
-          p[q] = v;
-          pmax = fmaxf(pmax, v);
-          dp[q] = v * (dp[q] - dq[e]);
-          smax = fmaxf(smax, fabsf(dp[q]));
         }
+        const uint64_t s01 = mul2(pack2(v[0], v[1]), add2(pack2(dp[q], dp[q + 1]), pack2(-d4.x, -d4.y)));
+        const uint64_t s23 = mul2(pack2(v[2], v[3]), add2(pack2(dp[q + 2], dp[q + 3]), pack2(-d4.z, -d4.w)));
+        p[q] = v[0];
+        p[q + 1] = v[1];
+        p[q + 2] = v[2];
+        p[q + 3] = v[3];
+        dp[q] = lo2(s01);
+        dp[q + 1] = hi2(s01);
+        dp[q + 2] = lo2(s23);
+        dp[q + 3] = hi2(s23);
+        pmax = max3f(pmax, max3f(v[0], v[1], v[2]), v[3]);
+        smax = max3f(smax, max3f(dp[q], dp[q + 1], dp[q + 2]), dp[q + 3]);
+        smin = fminf(fminf(smin, fminf(dp[q], dp[q + 1])), fminf(dp[q + 2], dp[q + 3]));
       }
+      smax = fmaxf(smax, -smin);
       __syncwarp();
       if (lane == 0) mbar_arrive1(bar(TB_EMPTY + s));  // L and D read
       pmax = warp_max(pmax);
@@ -1182,17 +1203,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float pinv = pa > 0.0f ? __fdiv_rn(127.0f, pa) : 0.0f;
       const float sinv = sa > 0.0f ? __fdiv_rn(127.0f, sa) : 0.0f;
       uint8_t* cbuf = smem + L::kCodesOff + b * L::kCodes;
+      const uint64_t pp = pack2(pinv, pinv), ss = pack2(sinv, sinv);
+      // rint(x * inv) for a pair, as FP16x2 (the products rounded per lane)
+      auto code2 = [](float a, float b, uint64_t inv2) {
+        const uint64_t y = mul2(pack2(a, b), inv2);
+        return h2(rintf(lo2(y)), rintf(hi2(y)));
+      };
 #pragma unroll
       for (int ch = 0; ch < 4; ch++) {
         uint4 wp, wsd;
-        wp.x = h2(code(p[8 * ch + 0], pinv), code(p[8 * ch + 1], pinv));
-        wp.y = h2(code(p[8 * ch + 2], pinv), code(p[8 * ch + 3], pinv));
-        wp.z = h2(code(p[8 * ch + 4], pinv), code(p[8 * ch + 5], pinv));
-        wp.w = h2(code(p[8 * ch + 6], pinv), code(p[8 * ch + 7], pinv));
-        wsd.x = h2(code(dp[8 * ch + 0], sinv), code(dp[8 * ch + 1], sinv));
-        wsd.y = h2(code(dp[8 * ch + 2], sinv), code(dp[8 * ch + 3], sinv));
-        wsd.z = h2(code(dp[8 * ch + 4], sinv), code(dp[8 * ch + 5], sinv));
-        wsd.w = h2(code(dp[8 * ch + 6], sinv), code(dp[8 * ch + 7], sinv));
+        wp.x = code2(p[8 * ch + 0], p[8 * ch + 1], pp);
+        wp.y = code2(p[8 * ch + 2], p[8 * ch + 3], pp);
+        wp.z = code2(p[8 * ch + 4], p[8 * ch + 5], pp);
+        wp.w = code2(p[8 * ch + 6], p[8 * ch + 7], pp);
+        wsd.x = code2(dp[8 * ch + 0], dp[8 * ch + 1], ss);
+        wsd.y = code2(dp[8 * ch + 2], dp[8 * ch + 3], ss);
+        wsd.z = code2(dp[8 * ch + 4], dp[8 * ch + 5], ss);
+        wsd.w = code2(dp[8 * ch + 6], dp[8 * ch + 7], ss);
         *reinterpret_cast<uint4*>(cbuf + L::kCP + swz(row, 64 * h + 16 * ch, 128)) = wp;
         *reinterpret_cast<uint4*>(cbuf + L::kCS + swz(row, 64 * h + 16 * ch, 128)) = wsd;
       }
@@ -1221,33 +1248,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int b = it & 1, qtile = q0 + it;
       if (!waitw_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort)) break;
       const float f_dv = scal[4 * b + 0], f_dk = scal[4 * b + 1], f_dq = scal[4 * b + 2];
-      // dQ[64 x 64] += f_dq (dS^ K^): this warp's 16 rows, 32 columns at a
-      // time; dS^ and K^ read transposed
+      // dQ[64 x 64] += f_dq (dS^ K^): this warp's 16 rows, all 64 columns
+      // (eight independent accumulators); dS^ and K^ read transposed
       const uint32_t dsb = sbase + L::kCodesOff + b * L::kCodes + L::kCS;
+      {
+        float q8[8][4];
 #pragma unroll
-      for (int dh = 0; dh < D; dh += 32) {
-        float q4[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; i++) q4[i][0] = q4[i][1] = q4[i][2] = q4[i][3] = 0.0f;
+        for (int i = 0; i < 8; i++) q8[i][0] = q8[i][1] = q8[i][2] = q8[i][3] = 0.0f;
 #pragma unroll
         for (int kc = 0; kc < kTok / 16; kc++) {
           uint32_t a[4];
           ldsm_x4_t(dsb + swz(16 * kc + ((j >> 1) << 3) + (lane & 7), 2 * (r0 + ((j & 1) << 3)), 128), a[0], a[1],
                     a[2], a[3]);
 #pragma unroll
-          for (int nd = 0; nd < 4; nd += 2) {
+          for (int nd = 0; nd < 8; nd += 2) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(sbase + L::kK + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 2 * dh + 16 * (nd + (j >> 1)), 128),
-                      b0, b1, b2, b3);
-            mma_f16(q4[nd], a, b0, b1);
-            mma_f16(q4[nd + 1], a, b2, b3);
+            ldsm_x4_t(sbase + L::kK + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 16 * (nd + (j >> 1)), 128), b0, b1,
+                      b2, b3);
+            mma_f16(q8[nd], a, b0, b1);
+            mma_f16(q8[nd + 1], a, b2, b3);
           }
         }
-        float* dq0 = ws.dqacc + (hrow + static_cast<size_t>(qtile) * kQ + r0 + g) * D + dh + 2 * t;
+        float* dq0 = ws.dqacc + (hrow + static_cast<size_t>(qtile) * kQ + r0 + g) * D + 2 * t;
 #pragma unroll
-        for (int nd = 0; nd < 4; nd++) {
-          red_add_v2(dq0 + 8 * nd, q4[nd][0] * f_dq, q4[nd][1] * f_dq);
-          red_add_v2(dq0 + 8 * D + 8 * nd, q4[nd][2] * f_dq, q4[nd][3] * f_dq);
+        for (int nd = 0; nd < 8; nd++) {
+          red_add_v2(dq0 + 8 * nd, q8[nd][0] * f_dq, q8[nd][1] * f_dq);
+          red_add_v2(dq0 + 8 * D + 8 * nd, q8[nd][2] * f_dq, q8[nd][3] * f_dq);
         }
       }
       __syncwarp();

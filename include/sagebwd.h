@@ -74,7 +74,7 @@ size_t sagebwd_workspace_bytes(int B, int H, int N, int D);
  * 128][D], the 16-byte chunks of row r XOR-permuted by r & 7); the codes of Q
  * and dO transposed per 64-token tile ([B*H][N/64][D][64], swizzled the same
  * way); the Q/K/V/dO
- * block scales (float [B*H][ceil(N/128)] each); L in log2 units and
+ * block scales (float [B*H][ceil(N/128)] each); -L in log2 units and
  * D = rowsum(dO o O) (float [B*H][N padded to 128]); the dQ accumulator
  * (float [B*H][N padded][D]); the status word.  For tests and inspection;
  * offsets must hold SAGEBWD_WS_FIELDS values. */

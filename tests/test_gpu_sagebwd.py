@@ -160,7 +160,7 @@ def test_int8_products_on_the_fp16_path_are_exact(K):
 
 
 def test_row_terms_of_the_backward():
-    """D = rowsum(dO o O) over the returned O, and L in log2 units."""
+    """D = rowsum(dO o O) over the returned O, and -L in log2 units."""
     B, H, N, D = 1, 2, 300, 64
     q, k, v, do = inputs(B, H, N, D, seed=9)
     ws, (o, lse, *_) = run(q, k, v, do, False)
@@ -170,7 +170,7 @@ def test_row_terms_of_the_backward():
     want = (do.double().numpy().reshape(B * H, N, D) * o.reshape(B * H, N, D).astype(np.float64)).sum(-1)
     assert np.allclose(drow[:, :N], want, rtol=1e-5, atol=1e-7)
     assert np.all(drow[:, N:] == 0) and np.all(l2[:, N:] == 0)
-    assert np.allclose(l2[:, :N], lse.reshape(B * H, N) / np.log(2), rtol=1e-6)
+    assert np.allclose(l2[:, :N], -lse.reshape(B * H, N) / np.log(2), rtol=1e-6)
 
 
 def test_autograd_function_matches_explicit_calls():
