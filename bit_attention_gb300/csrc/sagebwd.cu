@@ -187,6 +187,7 @@ struct Ws {
   uint16_t *qc, *kc, *vc, *doc;  // INT8 codes as FP16 values, swizzled rows
   uint16_t *vh, *doh;            // V and dO as FP16 values, swizzled rows
   uint16_t *qct, *doct;          // Q^ and dO^ codes transposed: [64-token tile][D][64], swizzled rows
+  uint16_t* vct;                 // V^ codes transposed: [128-token tile][2 key halves][D][64], swizzled rows
   float *sq, *sk, *sv, *sdo, *l2, *dd, *dqacc;
   int32_t* status;
 };
@@ -255,10 +256,11 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const uint16_t* __restr
     *reinterpret_cast<uint4*>(cbase + off) = make_uint4(hc[0], hc[1], hc[2], hc[3]);
     if (kind >= 2) *reinterpret_cast<uint4*>(vbase + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
   }
-  if (kind == 0 || kind == 3) {
+  if (kind == 0 || kind == 2 || kind == 3) {
     // the same codes transposed, per 64-token tile: [D rows][64 tokens], the
-    // K-major B operand of dK = dS^T Q and dV = P^T dO
-    uint16_t* tdst = kind == 0 ? ws.qct : ws.doct;
+    // K-major B operand of dK = dS^T Q and dV = P^T dO, and for V of PV (the
+    // two 64-token halves of a 128-token tile are consecutive: [2][D][64])
+    uint16_t* tdst = kind == 0 ? ws.qct : kind == 2 ? ws.vct : ws.doct;
     for (int i = tid; i < D * (kTok / 8); i += kThreads) {
       const int d = i % D, c = i / D;  // c: 8-token chunk of the block
       uint32_t h[4];
@@ -1328,6 +1330,326 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+// ---------------------------------------------------------------- forward, tcgen05 (D = 64)
+// The forward with S = Q^ K^^T and O_t = P~^ V^ on the 5th-generation tensor
+// cores (M = 128 query rows; S: N = 128 keys; PV: N = 64), issued by one
+// thread into double-buffered tensor memory.  The warpgroups:
+//   0  warp 0: bulk copies; warp 1: tensor-memory allocation and MMA issue
+//   1, 2  softmax: each thread owns one query row and 64 of the tile's 128
+//      keys; the row maximum and the 64-row block maxima are exchanged
+//      through shared memory; P~'s INT8 codes go to shared memory as the A
+//      operand of PV (each warpgroup writes one 64-key slab)
+//   3  correction: O in registers, rescaled by each row's factor and
+//      accumulated with each tile's PV times its block scales; the epilogue
+// P~ blocks are 64 query rows x 128 keys, as in the warp-level forward.
+struct TfSmem {
+  static constexpr int kQ = 0;                    // Q^ [128][64]: 16 KB
+  static constexpr int kStageOff = 16384;
+  static constexpr int kSK = 0, kSV = 16384;      // K^ [128][64]; V^T [2][64 d][64 keys]
+  static constexpr int kStage = 32768;
+  static constexpr int kPOff = kStageOff + kTcStages * kStage;  // P^ [2 bufs][2 key slabs][128][64]
+  static constexpr int kP = 32768;
+  static constexpr int kBarOff = kPOff + 2 * kP;
+  static constexpr int kMiscOff = kBarOff + 8 * 32;
+  // misc: tmem slot, abort, row max halves [2][128], alpha [2][128], block max
+  // [2 parity][8 warps], beta [2][2], final l halves [2][128], m [128]
+  static constexpr int kXm = kMiscOff + 16, kAl = kXm + 1024, kBm = kAl + 1024, kBeta = kBm + 64,
+                       kLf = kBeta + 16, kMf = kLf + 1024;
+  static constexpr int kBytes = kMf + 512;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+enum {
+  FB_Q = 0,
+  FB_FULL = 1,
+  FB_EMPTY = 1 + kTcStages,
+  FB_SDONE = 1 + 2 * kTcStages,  // + buffer
+  FB_SFREE = FB_SDONE + 2,
+  FB_PFULL = FB_SFREE + 2,
+  FB_PEMPTY = FB_PFULL + 2,
+  FB_PVDONE = FB_PEMPTY + 2,
+  FB_PVFREE = FB_PVDONE + 2,
+  FB_DRAIN = FB_PVFREE + 2,
+  FB_COUNT
+};
+static_assert(FB_COUNT <= 32, "barriers");
+constexpr uint32_t kTfS = 0, kTfPv = 256;
+
+template <bool kCausal>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    fwd_tc_kernel(Ws ws, uint16_t* __restrict__ out, float* __restrict__ lse, int N, float scale_log2e, uint64_t wait_ns,
+                  int withhold) {
+  constexpr int D = 64;
+  using L = TfSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_addr(smem);
+  const int nqt = (N + kTok - 1) / kTok;
+  const int Np = nqt * kTok;
+  const int qt = kCausal ? (nqt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int bh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wg = warp >> 2;
+  const int nkt = kCausal ? qt + 1 : nqt;
+  const size_t hb = static_cast<size_t>(bh) * Np * D;
+  const Ctl ctl{ws.status, wait_ns};
+  auto bar = [&](int i) { return sbase + L::kBarOff + 8 * i; };
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  float* xm = reinterpret_cast<float*>(smem + L::kXm);     // [2 halves][128 rows]
+  float* al = reinterpret_cast<float*>(smem + L::kAl);     // [2 buffers][128 rows]
+  float* bm = reinterpret_cast<float*>(smem + L::kBm);     // [2 parity][8 softmax warps]
+  float* beta = reinterpret_cast<float*>(smem + L::kBeta); // [2 buffers][2 row blocks]
+  float* lf = reinterpret_cast<float*>(smem + L::kLf);     // [2 halves][128 rows]
+  float* mf = reinterpret_cast<float*>(smem + L::kMf);     // [128 rows]
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(FB_Q), 1);
+    for (int s = 0; s < kTcStages; s++) {
+      mbar_init(bar(FB_FULL + s), 1);
+      mbar_init(bar(FB_EMPTY + s), 1);  // the MMA commit after PV
+    }
+    for (int b = 0; b < 2; b++) {
+      mbar_init(bar(FB_SDONE + b), 1);
+      mbar_init(bar(FB_SFREE + b), 8);
+      mbar_init(bar(FB_PFULL + b), 8);
+      mbar_init(bar(FB_PEMPTY + b), 1);
+      mbar_init(bar(FB_PVDONE + b), 1);
+      mbar_init(bar(FB_PVFREE + b), 4);
+    }
+    mbar_init(bar(FB_DRAIN), 1);
+    *abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tslot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (wg == 0) {
+    sagefp4::regs_dec<TcRegs::kCtl>();
+    if (warp == 0 && lane == 0) {
+      // ---- producer
+      mbar_arrive_expect_tx(bar(FB_Q), 16384);
+      bulk_load(sbase + L::kQ, ws.qc + hb + static_cast<size_t>(qt) * kTok * D, 16384, bar(FB_Q));
+      const bool held = withhold && blockIdx.x == 0 && blockIdx.y == 0;
+      int issued = 0;
+      for (int kt = 0; kt < nkt; kt++) {
+        const int s = kt % kTcStages;
+        if (kt >= kTcStages && !wait1_ab(bar(FB_EMPTY + s), ((kt / kTcStages) - 1) & 1, ctl, abort)) break;
+        if (held && kt == 0) continue;  // failure-detection test: this tile never arrives
+        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+        const size_t ko = hb + static_cast<size_t>(kt) * kTok * D;
+        mbar_arrive_expect_tx(bar(FB_FULL + s), 32768);
+        bulk_load(st + L::kSK, ws.kc + ko, 16384, bar(FB_FULL + s));
+        bulk_load(st + L::kSV, ws.vct + ko, 16384, bar(FB_FULL + s));
+        issued = kt + 1;
+      }
+      if (*abort) {
+        for (int last = issued - 1; last >= 0 && last >= issued - kTcStages; last--)
+          if (!(held && last == 0)) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar(FB_FULL + last % kTcStages), (last / kTcStages) & 1) &&
+                   globaltimer_ns() - t0 < ctl.limit) {
+            }
+          }
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar(FB_Q), 0) && globaltimer_ns() - t0 < ctl.limit) {
+        }
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---- MMA issue
+      const uint32_t idS = idesc_f16(128, 128), idPV = idesc_f16(128, 64);
+      bool ok = wait1_ab(bar(FB_Q), 0, ctl, abort);
+      auto issue_s = [&](int kt) {
+        const int s = kt % kTcStages, b = kt & 1;
+        if (!wait1_ab(bar(FB_FULL + s), (kt / kTcStages) & 1, ctl, abort)) return false;
+        if (kt >= 2 && !wait1_ab(bar(FB_SFREE + b), ((kt >> 1) - 1) & 1, ctl, abort)) return false;
+        tc_fence_after();
+        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+          mma_f16_tc(tmem + kTfS + 128 * b, desc_k64(sbase + L::kQ, 16 * k), desc_k64(st + L::kSK, 16 * k), idS,
+                     k > 0);
+        tc_commit(bar(FB_SDONE + b));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int kt = 0; ok && kt < nkt; kt++) {
+        const int s = kt % kTcStages, b = kt & 1;
+        if (kt + 1 < nkt && !(ok = issue_s(kt + 1))) break;
+        if (!(ok = wait1_ab(bar(FB_PFULL + b), (kt >> 1) & 1, ctl, abort))) break;
+        if (kt >= 2 && !(ok = wait1_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort))) break;
+        tc_fence_after();
+        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+        const uint32_t pb = sbase + L::kPOff + b * L::kP;
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+          mma_f16_tc(tmem + kTfPv + 64 * b, desc_k64(pb + (k >> 2) * 16384, 16 * (k & 3)),
+                     desc_k64(st + L::kSV + (k >> 2) * 8192, 16 * (k & 3)), idPV, k > 0);
+        tc_commit(bar(FB_PVDONE + b));
+        tc_commit(bar(FB_EMPTY + s));
+        tc_commit(bar(FB_PEMPTY + b));
+      }
+      tc_commit(bar(FB_DRAIN));
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar(FB_DRAIN), 0) && globaltimer_ns() - t0 < ctl.limit) {
+      }
+    }
+    // end of the CTA: every role arrives from its own code path (barrier 2)
+    __syncwarp();
+    named_bar(2, kTcThreads);
+    if (warp == 1) tmem_dealloc(tmem, 512);
+  } else if (wg == 1 || wg == 2) {
+    // ---- softmax: this thread's query row, keys 64h..64h+63 of each tile
+    sagefp4::regs_inc<TcRegs::kSoft>();
+    const int h = wg - 1;
+    const int row = 32 * (warp & 3) + lane;
+    const int sw = 4 * h + (warp & 3);
+    const int blk = (warp & 3) >> 1;  // 64-row block of this row
+    const uint32_t lanebase = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int qrow = qt * kTok + row;
+    const bool valid = qrow < N;
+    const float sqk = ws.sq[static_cast<size_t>(bh) * nqt + qt] * scale_log2e;
+    float m = -INFINITY, l = 0.0f;
+    float sk_next = ws.sk[static_cast<size_t>(bh) * nqt], sv_next = ws.sv[static_cast<size_t>(bh) * nqt];
+    for (int kt = 0; kt < nkt; kt++) {
+      const int b = kt & 1;
+      const float sk_cur = sk_next, sv_cur = sv_next;
+      if (kt + 1 < nkt) {
+        sk_next = ws.sk[static_cast<size_t>(bh) * nqt + kt + 1];
+        sv_next = ws.sv[static_cast<size_t>(bh) * nqt + kt + 1];
+      }
+      bool ok = waitw_ab(bar(FB_SDONE + b), (kt >> 1) & 1, ctl, abort);
+      if (!group_and(ok)) break;
+      tc_fence_after();
+      uint32_t ru[2][32];
+      tmem_ld32(tmem + lanebase + kTfS + 128 * b + 64 * h, ru[0]);
+      tmem_ld32(tmem + lanebase + kTfS + 128 * b + 64 * h + 32, ru[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(FB_SFREE + b));
+      const float c2 = sqk * sk_cur;
+      const bool edge = (kCausal && kt == qt) || (kt == nqt - 1 && (N % kTok) != 0);
+      float x[64];
+      float hm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; i++) {
+        float v = __uint_as_float(ru[i >> 5][i & 31]) * c2;
+        if (edge) {
+          const int key = kt * kTok + 64 * h + i;
+          if (key >= N || (kCausal && key > qrow)) v = -INFINITY;
+        }
+        x[i] = v;
+        hm = fmaxf(hm, v);
+      }
+      // the row's maximum over both halves of the tile
+      xm[h * 128 + row] = hm;
+      ok = kt < 2 || waitw_ab(bar(FB_PEMPTY + b), ((kt >> 1) - 1) & 1, ctl, abort);
+      // alpha and beta of buffer b were read by the correction (tile kt - 2)
+      ok = ok && (kt < 2 || waitw_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort));
+      if (!group_and(ok)) break;  // also publishes xm
+      const float mt = fmaxf(hm, xm[(1 - h) * 128 + row]);
+      const float mn = fmaxf(m, mt);
+      const float alpha = ex2(m - mn);  // m = -inf on the first tile: 0
+      m = mn;
+      float pmax = 0.0f, rs = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 64; i++) {
+        const float v = valid ? ex2(x[i] - mn) : 0.0f;
+        x[i] = v;
+        rs += v;
+        pmax = fmaxf(pmax, v);
+      }
+      l = l * alpha + rs;
+      if (h == 0) al[b * 128 + row] = alpha;
+      pmax = warp_max(pmax);
+      if (lane == 0) bm[b * 8 + sw] = pmax;
+      group_and(true);  // publishes bm
+      // block maximum: rows of this block are warps 2 blk, 2 blk + 1 of both halves
+      const float amax = fmaxf(fmaxf(bm[b * 8 + 2 * blk], bm[b * 8 + 2 * blk + 1]),
+                               fmaxf(bm[b * 8 + 4 + 2 * blk], bm[b * 8 + 4 + 2 * blk + 1]));
+      const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+      if (threadIdx.x == 128 + 64 * blk && (warp & 3) == 2 * blk)  // lane 0 of the block's first warp, half 0
+        beta[b * 2 + blk] = __fdiv_rn(amax, 127.0f) * sv_cur;
+      uint8_t* pbuf = smem + L::kPOff + b * L::kP + h * 16384;
+      const uint64_t ii = pack2(inv, inv);
+#pragma unroll
+      for (int ch = 0; ch < 8; ch++) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+          const uint64_t y = mul2(pack2(x[8 * ch + 2 * u], x[8 * ch + 2 * u + 1]), ii);
+          wv[u] = h2(rintf(lo2(y)), rintf(hi2(y)));
+        }
+        *reinterpret_cast<uint4*>(pbuf + swz(row, 16 * ch, 128)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(FB_PFULL + b));
+    }
+    // the row's statistics for the epilogue
+    lf[h * 128 + row] = l;
+    if (h == 0) mf[row] = m;
+    tc_fence_before();
+    named_bar(2, kTcThreads);
+  } else {
+    // ---- correction: O of this thread's row
+    sagefp4::regs_inc<TcRegs::kFold>();
+    const int row = 32 * (warp & 3) + lane;
+    const int blk = (warp & 3) >> 1;
+    const uint32_t lanebase = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    float o[64];
+#pragma unroll
+    for (int i = 0; i < 64; i++) o[i] = 0.0f;
+    for (int kt = 0; kt < nkt; kt++) {
+      const int b = kt & 1;
+      // PFULL: the softmax's alpha and beta of this tile (its release); PVDONE: the product
+      if (!waitw_ab(bar(FB_PFULL + b), (kt >> 1) & 1, ctl, abort)) break;
+      if (!waitw_ab(bar(FB_PVDONE + b), (kt >> 1) & 1, ctl, abort)) break;
+      tc_fence_after();
+      const float alpha = al[b * 128 + row], bt = beta[b * 2 + blk];
+      uint32_t ru[2][32];
+      tmem_ld32(tmem + lanebase + kTfPv + 64 * b, ru[0]);
+      tmem_ld32(tmem + lanebase + kTfPv + 64 * b + 32, ru[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(FB_PVFREE + b));
+#pragma unroll
+      for (int i = 0; i < 64; i++) o[i] = fmaf(__uint_as_float(ru[i >> 5][i & 31]), bt, o[i] * alpha);
+    }
+    // epilogue, once the softmax has published l and m
+    tc_fence_before();
+    named_bar(2, kTcThreads);
+    if (!*abort) {
+      const int qrow = qt * kTok + row;
+      if (qrow < N) {
+        const float lt = lf[row] + lf[128 + row];
+        const float il = 1.0f / lt;
+        uint16_t* orow = out + (static_cast<size_t>(bh) * N + qrow) * D;
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+          __nv_bfloat162 h0 = __floats2bfloat162_rn(o[8 * c + 0] * il, o[8 * c + 1] * il);
+          __nv_bfloat162 h1 = __floats2bfloat162_rn(o[8 * c + 2] * il, o[8 * c + 3] * il);
+          __nv_bfloat162 hh2 = __floats2bfloat162_rn(o[8 * c + 4] * il, o[8 * c + 5] * il);
+          __nv_bfloat162 h3 = __floats2bfloat162_rn(o[8 * c + 6] * il, o[8 * c + 7] * il);
+          uint4 w;
+          w.x = *reinterpret_cast<uint32_t*>(&h0);
+          w.y = *reinterpret_cast<uint32_t*>(&h1);
+          w.z = *reinterpret_cast<uint32_t*>(&hh2);
+          w.w = *reinterpret_cast<uint32_t*>(&h3);
+          *reinterpret_cast<uint4*>(orow + 8 * c) = w;
+        }
+        lse[static_cast<size_t>(bh) * N + qrow] = (mf[row] + __log2f(lt)) * kLn2;
+      }
+    }
+  }
+}
+
 // dQ accumulator (FP32, padded rows) -> bf16 [BH][N][D]
 template <int D>
 __global__ void __launch_bounds__(kThreads) dq_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq, int N,
@@ -1486,6 +1808,7 @@ Layout layout(int B, int H, int N, int D) {
       rows,        rows,        rows,        rows,         // Q^, K^, V^, dO^ codes
       rows,        rows,                                   // V, dO as FP16
       rows,        rows,                                   // Q^, dO^ codes transposed per 64-token tile
+      rows,                                                // V^ codes transposed per 64-token half tile
       4 * BH * nb, 4 * BH * nb, 4 * BH * nb, 4 * BH * nb,  // Q, K, V, dO block scales
       4 * BH * Np, 4 * BH * Np,                            // L (log2 units), D = rowsum(dO o O)
       4 * BH * Np * D,                                     // dQ accumulator
@@ -1512,14 +1835,15 @@ Ws carve(void* base, const Layout& l) {
   w.doh = reinterpret_cast<uint16_t*>(b + l.off[5]);
   w.qct = reinterpret_cast<uint16_t*>(b + l.off[6]);
   w.doct = reinterpret_cast<uint16_t*>(b + l.off[7]);
-  w.sq = reinterpret_cast<float*>(b + l.off[8]);
-  w.sk = reinterpret_cast<float*>(b + l.off[9]);
-  w.sv = reinterpret_cast<float*>(b + l.off[10]);
-  w.sdo = reinterpret_cast<float*>(b + l.off[11]);
-  w.l2 = reinterpret_cast<float*>(b + l.off[12]);
-  w.dd = reinterpret_cast<float*>(b + l.off[13]);
-  w.dqacc = reinterpret_cast<float*>(b + l.off[14]);
-  w.status = reinterpret_cast<int32_t*>(b + l.off[15]);
+  w.vct = reinterpret_cast<uint16_t*>(b + l.off[8]);
+  w.sq = reinterpret_cast<float*>(b + l.off[9]);
+  w.sk = reinterpret_cast<float*>(b + l.off[10]);
+  w.sv = reinterpret_cast<float*>(b + l.off[11]);
+  w.sdo = reinterpret_cast<float*>(b + l.off[12]);
+  w.l2 = reinterpret_cast<float*>(b + l.off[13]);
+  w.dd = reinterpret_cast<float*>(b + l.off[14]);
+  w.dqacc = reinterpret_cast<float*>(b + l.off[15]);
+  w.status = reinterpret_cast<int32_t*>(b + l.off[16]);
   return w;
 }
 
@@ -1587,6 +1911,20 @@ cudaError_t launch_dkdv_tc(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int 
   if (e != cudaSuccess) return e;
   const dim3 grid((N + kTok - 1) / kTok, BH);
   dkdv_tc_kernel<C><<<grid, kTcThreads, TcSmem::kAlloc, st>>>(w, dk, dv, N, scale, wait_ns, withhold);
+  return cudaGetLastError();
+}
+
+template <bool C>
+cudaError_t launch_fwd_tc(const Ws& w, uint16_t* o, float* lse, int BH, int N, float scale, cudaStream_t st,
+                          uint64_t wait_ns, int withhold) {
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, fwd_tc_kernel<C>);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs != 65536 / kTcThreads) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(fwd_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, TfSmem::kAlloc);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((N + kTok - 1) / kTok, BH);
+  fwd_tc_kernel<C><<<grid, kTcThreads, TfSmem::kAlloc, st>>>(w, o, lse, N, scale * kLog2e, wait_ns, withhold);
   return cudaGetLastError();
 }
 
@@ -1658,7 +1996,8 @@ int sagebwd_attn_fwd(void* o, float* lse, int B, int H, int N, int D, int causal
   const int BH = B * H;
   cudaError_t e;
   if (D == 64)
-    e = causal ? launch_fwd<64, true>(w, ob, lse, BH, N, scale, st) : launch_fwd<64, false>(w, ob, lse, BH, N, scale, st);
+    e = causal ? launch_fwd_tc<true>(w, ob, lse, BH, N, scale, st, kWaitNs, 0)
+               : launch_fwd_tc<false>(w, ob, lse, BH, N, scale, st, kWaitNs, 0);
   else
     e = causal ? launch_fwd<128, true>(w, ob, lse, BH, N, scale, st)
                : launch_fwd<128, false>(w, ob, lse, BH, N, scale, st);
@@ -1770,7 +2109,7 @@ int sagebwd_stall_test(int kernel, void* out0, void* out1, int B, int H, int N, 
   if (kernel == 0) {
     uint16_t* o = static_cast<uint16_t*>(out0);
     float* lse = static_cast<float*>(out1);
-    e = D == 64 ? launch_fwd<64, false>(w, o, lse, BH, N, scale, st, wait_limit_ns, 1)
+    e = D == 64 ? launch_fwd_tc<false>(w, o, lse, BH, N, scale, st, wait_limit_ns, 1)
                 : launch_fwd<128, false>(w, o, lse, BH, N, scale, st, wait_limit_ns, 1);
   } else {
     uint16_t *dkb = static_cast<uint16_t*>(out0), *dvb = static_cast<uint16_t*>(out1);

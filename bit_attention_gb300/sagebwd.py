@@ -21,8 +21,8 @@ from . import sage_fp4 as _fp4
 from .sage_fp4 import EINVAL, OK, SageFp4Error
 
 _HEADER = os.path.join(os.path.dirname(_fp4._HEADER), "sagebwd.h")
-WS_FIELDS = 16
-WS_NAMES = ("q_codes", "k_codes", "v_codes", "do_codes", "v_half", "do_half", "q_codes_t", "do_codes_t",
+WS_FIELDS = 17
+WS_NAMES = ("q_codes", "k_codes", "v_codes", "do_codes", "v_half", "do_half", "q_codes_t", "do_codes_t", "v_codes_t",
             "q_scales", "k_scales", "v_scales", "do_scales", "l2", "drow", "dq_acc", "status")
 TOK = 128  # token block of the INT8 operands; rows padded to a multiple of it
 _lock = threading.Lock()

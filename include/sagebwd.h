@@ -64,16 +64,16 @@ extern "C" {
 #endif
 
 /* Number of regions in the workspace (see sagebwd_workspace_layout). */
-#define SAGEBWD_WS_FIELDS 16
+#define SAGEBWD_WS_FIELDS 17
 
 /* Bytes of workspace for these sizes; 0 when the sizes are invalid. */
 size_t sagebwd_workspace_bytes(int B, int H, int N, int D);
 
 /* Byte offsets of the workspace's regions, in this order: the INT8 codes of
  * Q, K, V, dO (as FP16 values), V and dO as FP16 (each [B*H][N padded to
- * 128][D], the 16-byte chunks of row r XOR-permuted by r & 7); the codes of Q
- * and dO transposed per 64-token tile ([B*H][N/64][D][64], swizzled the same
- * way); the Q/K/V/dO
+ * 128][D], the 16-byte chunks of row r XOR-permuted by r & 7); the codes of Q,
+ * dO and V transposed per 64-token tile ([B*H][N/64][D][64], swizzled the
+ * same way); the Q/K/V/dO
  * block scales (float [B*H][ceil(N/128)] each); -L in log2 units and
  * D = rowsum(dO o O) (float [B*H][N padded to 128]); the dQ accumulator
  * (float [B*H][N padded][D]); the status word.  For tests and inspection;

@@ -11,7 +11,7 @@ from bit_attention_gb300 import sagebwd as SB
 def test_library_exports_every_header_function():
     lib = SB.lib()
     names = SB.header_functions()
-    assert len(names) == 13
+    assert len(names) == 14
     text = open(SB._HEADER).read()
     decls = dict(re.findall(r"^(?:int|size_t)\s*(sagebwd_\w+)\(([^;]*)\);", text, re.M))
     assert set(decls) == set(names)
@@ -26,7 +26,7 @@ def test_workspace_layout():
     rc, offs = SB.sagebwd_workspace_layout(B, H, N, D)
     assert rc == S.OK and len(offs) == SB.WS_FIELDS
     total = SB.sagebwd_workspace_bytes(B, H, N, D)
-    sizes = [2 * BH * Np * D] * 8 + [4 * BH * 3] * 4 + [4 * BH * Np] * 2 + [4 * BH * Np * D, 256]
+    sizes = [2 * BH * Np * D] * 9 + [4 * BH * 3] * 4 + [4 * BH * Np] * 2 + [4 * BH * Np * D, 256]
     assert offs[0] == 0
     for i, sz in enumerate(sizes):
         assert offs[i] % 256 == 0

@@ -129,7 +129,7 @@ def test_quantized_operands_are_bit_exact(N, D):
         want = np.zeros((BH, Np, D), np.int8)
         want[:, :N] = codes
         assert np.array_equal(decode_codes(region(f"{name}_codes"), BH, Np, D), want), name
-        if name in ("q", "do"):
+        if name in ("q", "do", "v"):
             assert np.array_equal(decode_codes_t(region(f"{name}_codes_t"), BH, Np, D), want), name
         got_s = region(f"{name}_scales")[:BH * (Np // 128) * 4].view(np.float32).reshape(BH, Np // 128)
         assert np.array_equal(got_s, scales), name
