@@ -127,6 +127,17 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// rint by FP32 arithmetic: (z + 1.5 * 2^23) - 1.5 * 2^23 is z rounded to the
+// nearest integer, ties to even, exactly, for |z| < 2^22.
+constexpr float kRintMagic = 12582912.0f;
+
+// Warp-wide maximum of unsigned words (every lane gets it).
+__device__ __forceinline__ uint32_t redux_max_u32(uint32_t v) {
+  uint32_t r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
@@ -1351,9 +1362,9 @@ struct TfSmem {
   static constexpr int kP = 32768;
   static constexpr int kBarOff = kPOff + 2 * kP;
   static constexpr int kMiscOff = kBarOff + 8 * 32;
-  // misc: tmem slot, abort, row max halves [2][128], alpha [2][128], block max
-  // [2 parity][8 warps], beta [2][2], final l halves [2][128], m [128]
-  static constexpr int kXm = kMiscOff + 16, kAl = kXm + 1024, kBm = kAl + 1024, kBeta = kBm + 64,
+  // misc: tmem slot, abort, row max halves [2 parity][2][128], alpha [2][128],
+  // block max [2 parity][8 warps], beta [2][2], final l halves [2][128], m [128]
+  static constexpr int kXm = kMiscOff + 16, kAl = kXm + 2048, kBm = kAl + 1024, kBeta = kBm + 64,
                        kLf = kBeta + 16, kMf = kLf + 1024;
   static constexpr int kBytes = kMf + 512;
   static constexpr int kAlloc = kBytes + 1024;
@@ -1503,16 +1514,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     named_bar(2, kTcThreads);
     if (warp == 1) tmem_dealloc(tmem, 512);
   } else if (wg == 1 || wg == 2) {
-    // ---- softmax: this thread's query row, keys 64h..64h+63 of each tile
+    // ---- softmax: this thread's query row, keys 64h..64h+63 of each tile.
+    // The scores arrive as exact integers (Q^.K^ code products); the scale
+    // sq sk scale log2(e) enters only the exponent's argument.
     sagefp4::regs_inc<TcRegs::kSoft>();
     const int h = wg - 1;
-    const int row = 32 * (warp & 3) + lane;
-    const int sw = 4 * h + (warp & 3);
-    const int blk = (warp & 3) >> 1;  // 64-row block of this row
-    const uint32_t lanebase = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int wq = warp & 3;
+    const int row = 32 * wq + lane;
+    const int sw = 4 * h + wq;
+    const int blk = wq >> 1;  // 64-row block of this row
+    const uint32_t lanebase = static_cast<uint32_t>(32 * wq) << 16;
     const int qrow = qt * kTok + row;
     const bool valid = qrow < N;
     const float sqk = ws.sq[static_cast<size_t>(bh) * nqt + qt] * scale_log2e;
+    const uint64_t magic2 = pack2(kRintMagic, kRintMagic), nmagic2 = pack2(-kRintMagic, -kRintMagic);
     float m = -INFINITY, l = 0.0f;
     float sk_next = ws.sk[static_cast<size_t>(bh) * nqt], sv_next = ws.sv[static_cast<size_t>(bh) * nqt];
     for (int kt = 0; kt < nkt; kt++) {
@@ -1523,7 +1538,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         sv_next = ws.sv[static_cast<size_t>(bh) * nqt + kt + 1];
       }
       bool ok = waitw_ab(bar(FB_SDONE + b), (kt >> 1) & 1, ctl, abort);
-      if (!group_and(ok)) break;
       tc_fence_after();
       uint32_t ru[2][32];
       tmem_ld32(tmem + lanebase + kTfS + 128 * b + 64 * h, ru[0]);
@@ -1532,49 +1546,66 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive1(bar(FB_SFREE + b));
-      const float c2 = sqk * sk_cur;
-      const bool edge = (kCausal && kt == qt) || (kt == nqt - 1 && (N % kTok) != 0);
-      float x[64];
-      float hm = -INFINITY;
+      if ((kCausal && kt == qt) || (kt == nqt - 1 && (N % kTok) != 0)) {
+        // keys past N, and (causal) past this row, do not take part
+        const int k0 = kt * kTok + 64 * h;
+        const int last = kCausal ? min(N - 1, qrow) : N - 1;
 #pragma unroll
-      for (int i = 0; i < 64; i++) {
-        float v = __uint_as_float(ru[i >> 5][i & 31]) * c2;
-        if (edge) {
-          const int key = kt * kTok + 64 * h + i;
-          if (key >= N || (kCausal && key > qrow)) v = -INFINITY;
-        }
-        x[i] = v;
-        hm = fmaxf(hm, v);
+        for (int i = 0; i < 64; i++)
+          if (k0 + i > last) ru[i >> 5][i & 31] = __float_as_uint(-INFINITY);
       }
-      // the row's maximum over both halves of the tile
-      xm[h * 128 + row] = hm;
-      ok = kt < 2 || waitw_ab(bar(FB_PEMPTY + b), ((kt >> 1) - 1) & 1, ctl, abort);
-      // alpha and beta of buffer b were read by the correction (tile kt - 2)
+      float hm;
+      {
+        float t[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+          const uint32_t* r = &ru[j >> 2][(j & 3) * 8];
+          t[j] = max3f(max3f(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2])),
+                       max3f(__uint_as_float(r[3]), __uint_as_float(r[4]), __uint_as_float(r[5])),
+                       fmaxf(__uint_as_float(r[6]), __uint_as_float(r[7])));
+        }
+        hm = max3f(max3f(t[0], t[1], t[2]), max3f(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
+      }
+      // the row's maximum over both halves of the tile (xm by tile parity)
+      xm[(2 * b + h) * 128 + row] = hm;
+      // P buffer b: PV of tile kt - 2 has read it; alpha and beta of buffer b:
+      // the correction has read them
+      ok = ok && (kt < 2 || waitw_ab(bar(FB_PEMPTY + b), ((kt >> 1) - 1) & 1, ctl, abort));
       ok = ok && (kt < 2 || waitw_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort));
       if (!group_and(ok)) break;  // also publishes xm
-      const float mt = fmaxf(hm, xm[(1 - h) * 128 + row]);
-      const float mn = fmaxf(m, mt);
+      const float mt = fmaxf(hm, xm[(2 * b + 1 - h) * 128 + row]);
+      // c2 > 0 keeps masked keys at -inf (c2 = 0 only when every score is 0)
+      const float c2 = fmaxf(sqk * sk_cur, 1e-30f);
+      const float mn = fmaxf(m, mt * c2);
       const float alpha = ex2(m - mn);  // m = -inf on the first tile: 0
       m = mn;
-      float pmax = 0.0f, rs = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 64; i++) {
-        const float v = valid ? ex2(x[i] - mn) : 0.0f;
-        x[i] = v;
-        rs += v;
-        pmax = fmaxf(pmax, v);
-      }
-      l = l * alpha + rs;
+      // The block's largest P~ is the largest of its rows' maxima, each the
+      // exponential of the same argument as the row's largest score (rows past
+      // N excluded); both halves of a row compute it alike.
+      const float rp = valid ? ex2(fmaf(mt, c2, -mn)) : 0.0f;
+      const uint32_t wmax = redux_max_u32(__float_as_uint(rp));  // rp >= 0: bit order is value order
+      if (lane == 0) bm[b * 8 + sw] = __uint_as_float(wmax);
       if (h == 0) al[b * 128 + row] = alpha;
-      pmax = warp_max(pmax);
-      if (lane == 0) bm[b * 8 + sw] = pmax;
-      group_and(true);  // publishes bm
-      // block maximum: rows of this block are warps 2 blk, 2 blk + 1 of both halves
-      const float amax = fmaxf(fmaxf(bm[b * 8 + 2 * blk], bm[b * 8 + 2 * blk + 1]),
-                               fmaxf(bm[b * 8 + 4 + 2 * blk], bm[b * 8 + 4 + 2 * blk + 1]));
+      const uint64_t c22 = pack2(c2, c2), nm2 = pack2(-mn, -mn);
+      uint64_t acc0 = 0, acc1 = 0;
+#pragma unroll
+      for (int j = 0; j < 32; j++) {
+        uint32_t* r = &ru[j >> 4][(j & 15) * 2];
+        const uint64_t y = fma2(pack2(__uint_as_float(r[0]), __uint_as_float(r[1])), c22, nm2);
+        const float x0 = ex2(lo2(y)), x1 = ex2(hi2(y));
+        r[0] = __float_as_uint(x0);
+        r[1] = __float_as_uint(x1);
+        if (j & 1)
+          acc1 = add2(acc1, pack2(x0, x1));
+        else
+          acc0 = add2(acc0, pack2(x0, x1));
+      }
+      const uint64_t acc = add2(acc0, acc1);
+      l = fmaf(l, alpha, lo2(acc) + hi2(acc));
+      named_bar(3 + 2 * h + blk, 64);  // publishes bm to the block's other warp of this half
+      const float amax = fmaxf(bm[b * 8 + 4 * h + 2 * blk], bm[b * 8 + 4 * h + 2 * blk + 1]);
       const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
-      if (threadIdx.x == 128 + 64 * blk && (warp & 3) == 2 * blk)  // lane 0 of the block's first warp, half 0
-        beta[b * 2 + blk] = __fdiv_rn(amax, 127.0f) * sv_cur;
+      if (h == 0 && wq == 2 * blk && lane == 0) beta[b * 2 + blk] = __fdiv_rn(amax, 127.0f) * sv_cur;
       uint8_t* pbuf = smem + L::kPOff + b * L::kP + h * 16384;
       const uint64_t ii = pack2(inv, inv);
 #pragma unroll
@@ -1582,8 +1613,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t wv[4];
 #pragma unroll
         for (int u = 0; u < 4; u++) {
-          const uint64_t y = mul2(pack2(x[8 * ch + 2 * u], x[8 * ch + 2 * u + 1]), ii);
-          wv[u] = h2(rintf(lo2(y)), rintf(hi2(y)));
+          const uint32_t* r = &ru[ch >> 2][(ch & 3) * 8 + 2 * u];
+          // rint(x * inv): the product rounded to FP32, then to an integer by
+          // adding and subtracting 1.5 * 2^23 (exact below 2^22)
+          const uint64_t z = mul2(pack2(__uint_as_float(r[0]), __uint_as_float(r[1])), ii);
+          const uint64_t n = add2(add2(z, magic2), nmagic2);
+          wv[u] = h2(lo2(n), hi2(n));
         }
         *reinterpret_cast<uint4*>(pbuf + swz(row, 16 * ch, 128)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
       }
@@ -1597,14 +1632,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before();
     named_bar(2, kTcThreads);
   } else {
-    // ---- correction: O of this thread's row
+    // ---- correction: O of this thread's row, as FP32 pairs
     sagefp4::regs_inc<TcRegs::kFold>();
     const int row = 32 * (warp & 3) + lane;
     const int blk = (warp & 3) >> 1;
     const uint32_t lanebase = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    float o[64];
+    uint64_t o[32];
 #pragma unroll
-    for (int i = 0; i < 64; i++) o[i] = 0.0f;
+    for (int i = 0; i < 32; i++) o[i] = 0;
     for (int kt = 0; kt < nkt; kt++) {
       const int b = kt & 1;
       // PFULL: the softmax's alpha and beta of this tile (its release); PVDONE: the product
@@ -1619,8 +1654,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive1(bar(FB_PVFREE + b));
+      // o = pv * beta + o * alpha; o * 1 is o, so rows whose maximum held skip it
+      const uint64_t bt2 = pack2(bt, bt);
+      if (__all_sync(kFull, alpha == 1.0f)) {
 #pragma unroll
-      for (int i = 0; i < 64; i++) o[i] = fmaf(__uint_as_float(ru[i >> 5][i & 31]), bt, o[i] * alpha);
+        for (int j = 0; j < 32; j++)
+          o[j] = fma2(pack2(__uint_as_float(ru[j >> 4][(j & 15) * 2]), __uint_as_float(ru[j >> 4][(j & 15) * 2 + 1])),
+                      bt2, o[j]);
+      } else {
+        const uint64_t al2 = pack2(alpha, alpha);
+#pragma unroll
+        for (int j = 0; j < 32; j++)
+          o[j] = fma2(pack2(__uint_as_float(ru[j >> 4][(j & 15) * 2]), __uint_as_float(ru[j >> 4][(j & 15) * 2 + 1])),
+                      bt2, mul2(o[j], al2));
+      }
     }
     // epilogue, once the softmax has published l and m
     tc_fence_before();
@@ -1633,10 +1680,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint16_t* orow = out + (static_cast<size_t>(bh) * N + qrow) * D;
 #pragma unroll
         for (int c = 0; c < 8; c++) {
-          __nv_bfloat162 h0 = __floats2bfloat162_rn(o[8 * c + 0] * il, o[8 * c + 1] * il);
-          __nv_bfloat162 h1 = __floats2bfloat162_rn(o[8 * c + 2] * il, o[8 * c + 3] * il);
-          __nv_bfloat162 hh2 = __floats2bfloat162_rn(o[8 * c + 4] * il, o[8 * c + 5] * il);
-          __nv_bfloat162 h3 = __floats2bfloat162_rn(o[8 * c + 6] * il, o[8 * c + 7] * il);
+          __nv_bfloat162 h0 = __floats2bfloat162_rn(lo2(o[4 * c + 0]) * il, hi2(o[4 * c + 0]) * il);
+          __nv_bfloat162 h1 = __floats2bfloat162_rn(lo2(o[4 * c + 1]) * il, hi2(o[4 * c + 1]) * il);
+          __nv_bfloat162 hh2 = __floats2bfloat162_rn(lo2(o[4 * c + 2]) * il, hi2(o[4 * c + 2]) * il);
+          __nv_bfloat162 h3 = __floats2bfloat162_rn(lo2(o[4 * c + 3]) * il, hi2(o[4 * c + 3]) * il);
           uint4 w;
           w.x = *reinterpret_cast<uint32_t*>(&h0);
           w.y = *reinterpret_cast<uint32_t*>(&h1);
