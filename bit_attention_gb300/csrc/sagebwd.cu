@@ -30,6 +30,7 @@
 // Operands needed transposed are read with ldmatrix.trans, and an MMA's FP32
 // accumulator fragment is, pairwise converted, the A fragment of the next MMA,
 // so no operand is stored twice.
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -151,6 +152,21 @@ __device__ __forceinline__ void named_bar(int id, int n) {
 __device__ __forceinline__ void red_add_v2(float* p, float a, float b) {
   asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
 }
+
+// Tensor reduction by the copy engine: the box of `map` at (x, y) += the
+// shared-memory tile at ssrc (laid out with the map's swizzle), element-wise
+// in the map's type, in this thread's bulk group.  wait_read: this thread's
+// bulk operations have read their shared-memory sources; wait_all: they have
+// completed.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t ssrc, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(ssrc), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
@@ -857,12 +873,27 @@ __device__ __forceinline__ uint64_t desc_k64(uint32_t tile, int k0) {
   return smem_desc(tile + 2 * k0, 16, 1024, kSwizzle128B);
 }
 
+// The same products with MN-major operands (idesc bits 15 and 16: A and B
+// transposed), as dQ = dS^ K^ reads them: each operand is stored with its K
+// index as the 128-byte row (64 FP16 values of M or N per row, 16-byte chunks
+// XOR-permuted by row & 7).  The descriptor's leading offset is the distance
+// between 64-wide blocks of M (or N), its stride offset the distance between
+// groups of 8 K rows (1024 bytes here); a K step of 16 starts 16 rows later.
+__host__ __device__ constexpr uint32_t idesc_f16_mn(uint32_t M, uint32_t N) {
+  return idesc_f16(M, N) | (1u << 15) | (1u << 16);
+}
+__device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int k0, uint32_t block_stride) {
+  return smem_desc(tile + 128 * k0, block_stride, 1024, kSwizzle128B);
+}
+
 // ---------------------------------------------------------------- backward, tcgen05 (D = 64)
-// The same backward with the four products that have 128 keys as rows --
-// S^T = K^ Q^^T, dP^T = V dO^T, dV = P^^T dO^ and dK = dS^^T Q^ -- on the
-// 5th-generation tensor cores: one thread issues them asynchronously into
-// tensor memory (M = 128 keys, N = 64, K = 16 per instruction) while other
-// warps work.  The warpgroups of the CTA:
+// The same backward with all five products on the 5th-generation tensor
+// cores, issued asynchronously into tensor memory by one thread while other
+// warps work: per 64-query tile the four with 128 keys as rows -- S^T = K^ Q^^T,
+// dP^T = V dO^T, dV = P^^T dO^ and dK = dS^^T Q^ (M = 128 keys, N = 64, K = 16
+// per instruction) -- and per pair of query tiles dQ = dS^ K^ (M = 128
+// queries, N = 64, K = 128 keys) with both operands read MN-major from the
+// codes buffers and the resident K^ tile.  The warpgroups of the CTA:
 //   0  warp 0: bulk copies; warp 1: tensor-memory allocation and MMA issue
 //   1, 2  softmax: each thread owns one key row and half of the tile's 64
 //      query columns; P^T and dS^T from the S^T and dP^T rows in tensor
@@ -870,18 +901,18 @@ __device__ __forceinline__ uint64_t desc_k64(uint32_t tile, int k0) {
 //      INT8 codes written to shared memory as the A operands of dV and dK
 //      (and dS^T read again by dQ)
 //   3  folds each tile's dV and dK partials (tensor memory) into registers
-//      with the tile's block scales, and computes dQ (16 query rows a warp)
-// dQ = dS^ K^ (64 queries as rows) stays on the warp-level MMA, from the
-// staged dS^ codes and the resident K^ tile, added to the FP32 accumulator.
-// Tensor memory: S^T, dP^T, dV and dK partials, each double-buffered (512
-// columns).  Every wait is bounded; a wait that runs out sets the status
-// word and an abort flag that ends every role's loop.
+//      with the tile's block scales, and adds each tile pair's dQ, times its
+//      tiles' scales, to the FP32 accumulator in global memory by tensor
+//      reductions of the copy engine (staged 32 rows x 32 columns a warp)
+// Tensor memory: S^T and dP^T double-buffered, the dV and dK partials and dQ
+// single (448 of 512 columns).  Every wait is bounded; a wait that runs out
+// sets the status word and an abort flag that ends every role's loop.
 constexpr int kTcThreads = 512;
 constexpr int kTcStages = 3;
 struct TcRegs {
-  static constexpr uint32_t kCtl = 48, kSoft = 128, kFold = 208;
+  static constexpr uint32_t kCtl = 64, kSoft = 128, kFold = 192;
 };
-static_assert(TcRegs::kCtl * 128 + TcRegs::kSoft * 256 + TcRegs::kFold * 128 == 65536, "register split");
+static_assert(TcRegs::kCtl * 128 + TcRegs::kSoft * 256 + TcRegs::kFold * 128 <= 65536, "register split");
 
 struct TcSmem {
   static constexpr int kTile = 128 * 128;  // 128 rows of 128 bytes
@@ -894,9 +925,11 @@ struct TcSmem {
   static constexpr int kCodesOff = kStageOff + kTcStages * kStage;
   // codes buffer: P^T [128 keys][64 q], dS^T [128 keys][64 q]
   static constexpr int kCP = 0, kCS = kTile, kCodes = 2 * kTile;
-  static constexpr int kBarOff = kCodesOff + 2 * kCodes;
+  // dQ staging: per fold warp a [32 rows][32 FP32] tile, 128-byte swizzled
+  static constexpr int kDqOff = kCodesOff + 2 * kCodes;
+  static constexpr int kBarOff = kDqOff + 128 * 128;
   static constexpr int kNumBars = 32;
-  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // tmem slot, abort flag, red[2][2][8], scal[2][4]
+  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // tmem slot, abort flag, red[2][2][8], scal[4][4]
   static constexpr int kBytes = kMiscOff + 256;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
 };
@@ -909,14 +942,16 @@ enum {
   TB_SFREE = TB_SDONE + 2,
   TB_CFULL = TB_SFREE + 2,
   TB_CEMPTY = TB_CFULL + 2,
-  TB_PDONE = TB_CEMPTY + 2,
-  TB_PFREE = TB_PDONE + 2,
-  TB_DRAIN = TB_PFREE + 2,
+  TB_PDONE = TB_CEMPTY + 2,  // dV and dK partials (single buffer)
+  TB_PFREE = TB_PDONE + 1,
+  TB_QDONE = TB_PFREE + 1,   // dQ of a tile pair (single buffer)
+  TB_QFREE = TB_QDONE + 1,
+  TB_DRAIN = TB_QFREE + 1,
   TB_COUNT
 };
 static_assert(TB_COUNT <= TcSmem::kNumBars, "barriers");
 // tensor-memory columns
-constexpr uint32_t kTcS = 0, kTcDp = 128, kTcDv = 256, kTcDk = 384;
+constexpr uint32_t kTcS = 0, kTcDp = 128, kTcDv = 256, kTcDk = 320, kTcDq = 384;
 
 // Bounded warp-wide wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool waitw_ab(uint32_t bar, uint32_t parity, const Ctl& c, volatile int* abort) {
@@ -981,8 +1016,8 @@ __device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
 
 template <bool kCausal>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    dkdv_tc_kernel(Ws ws, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int N, float scale, uint64_t wait_ns,
-                   int withhold) {
+    dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_dq, Ws ws, uint16_t* __restrict__ dk,
+                   uint16_t* __restrict__ dv, int N, float scale, uint64_t wait_ns, int withhold) {
   constexpr int D = 64;
   using L = TcSmem;
   extern __shared__ uint8_t smem_raw[];
@@ -1004,7 +1039,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   float* red = reinterpret_cast<float*>(smem + L::kMiscOff + 16);    // [2 parity][2 kinds][8 warps]
-  float* scal = reinterpret_cast<float*>(smem + L::kMiscOff + 160);  // [2 buffers][4]
+  float* scal = reinterpret_cast<float*>(smem + L::kMiscOff + 160);  // [tile mod 4][4]
 
   if (threadIdx.x == 0) {
     mbar_init(bar(TB_FIXED), 1);
@@ -1016,10 +1051,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar(TB_SDONE + b), 1);
       mbar_init(bar(TB_SFREE + b), 8);
       mbar_init(bar(TB_CFULL + b), 8);
-      mbar_init(bar(TB_CEMPTY + b), 1 + 4);  // the MMA commit + the dQ warps
-      mbar_init(bar(TB_PDONE + b), 1);
-      mbar_init(bar(TB_PFREE + b), 4);
+      mbar_init(bar(TB_CEMPTY + b), 1);  // the MMA commit after the pair's dQ
     }
+    mbar_init(bar(TB_PDONE), 1);
+    mbar_init(bar(TB_PFREE), 4);
+    mbar_init(bar(TB_QDONE), 1);
+    mbar_init(bar(TB_QFREE), 4);
     mbar_init(bar(TB_DRAIN), 1);
     *abort = 0;
     mbar_fence_init();
@@ -1074,7 +1111,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     } else if (warp == 1 && lane == 0) {
       // ---- MMA issue
-      const uint32_t id = idesc_f16(128, 64);
+      const uint32_t id = idesc_f16(128, 64), idq = idesc_f16_mn(128, 64);
+      const uint64_t dk0 = desc_k64(sbase + L::kK, 0), dv0 = desc_k64(sbase + L::kV, 0);
+      // dQ = dS^ K^, MN-major: a K step of 16 rows moves 2048 bytes (+128)
+      const uint64_t dqa = desc_mn(sbase + L::kCodesOff + L::kCS, 0, L::kCodes), dqb = desc_mn(sbase + L::kK, 0, L::kCodes);
       bool ok = wait1_ab(bar(TB_FIXED), 0, ctl, abort);
       auto issue_sdp = [&](int it) {
         const int s = it % kTcStages, b = it & 1;
@@ -1082,13 +1122,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (it >= 2 && !wait1_ab(bar(TB_SFREE + b), ((it >> 1) - 1) & 1, ctl, abort)) return false;
         tc_fence_after();
         const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+        // descriptors built once per operand; a K step of 16 moves 32 bytes (+2)
+        const uint64_t dq = desc_k64(st + L::kSQ, 0), ddo = desc_k64(st + L::kSDoh, 0);
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-          mma_f16_tc(tmem + kTcS + 64 * b, desc_k64(sbase + L::kK, 16 * k), desc_k64(st + L::kSQ, 16 * k), id, k > 0);
+        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcS + 64 * b, dk0 + 2 * k, dq + 2 * k, id, k > 0);
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-          mma_f16_tc(tmem + kTcDp + 64 * b, desc_k64(sbase + L::kV, 16 * k), desc_k64(st + L::kSDoh, 16 * k), id,
-                     k > 0);
+        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcDp + 64 * b, dv0 + 2 * k, ddo + 2 * k, id, k > 0);
         tc_commit(bar(TB_SDONE + b));
         return true;
       };
@@ -1097,21 +1136,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int s = it % kTcStages, b = it & 1;
         if (it + 1 < niter && !(ok = issue_sdp(it + 1))) break;
         if (!(ok = wait1_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort))) break;
-        if (it >= 2 && !(ok = wait1_ab(bar(TB_PFREE + b), ((it >> 1) - 1) & 1, ctl, abort))) break;
+        // the partials' buffer: the fold has read the previous tile's
+        if (it >= 1 && !(ok = wait1_ab(bar(TB_PFREE), (it - 1) & 1, ctl, abort))) break;
         tc_fence_after();
         const uint32_t st = sbase + L::kStageOff + s * L::kStage;
         const uint32_t cb = sbase + L::kCodesOff + b * L::kCodes;
+        const uint64_t dp = desc_k64(cb + L::kCP, 0), dds = desc_k64(cb + L::kCS, 0);
+        const uint64_t ddot = desc_k64(st + L::kSDot, 0), dqt = desc_k64(st + L::kSQt, 0);
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-          mma_f16_tc(tmem + kTcDv + 64 * b, desc_k64(cb + L::kCP, 16 * k), desc_k64(st + L::kSDot, 16 * k), id,
-                     k > 0);
+        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcDv, dp + 2 * k, ddot + 2 * k, id, k > 0);
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-          mma_f16_tc(tmem + kTcDk + 64 * b, desc_k64(cb + L::kCS, 16 * k), desc_k64(st + L::kSQt, 16 * k), id,
-                     k > 0);
-        tc_commit(bar(TB_PDONE + b));
+        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcDk, dds + 2 * k, dqt + 2 * k, id, k > 0);
+        tc_commit(bar(TB_PDONE));
         tc_commit(bar(TB_EMPTY + s));
-        tc_commit(bar(TB_CEMPTY + b));
+        if (b == 1) {
+          // dQ of the pair (it - 1, it): rows 0..63 from codes buffer 0, rows
+          // 64..127 from buffer 1; the fold has read the previous pair's dQ
+          const int pr = it >> 1;
+          if (pr >= 1 && !(ok = wait1_ab(bar(TB_QFREE), (pr - 1) & 1, ctl, abort))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 8; k++) mma_f16_tc(tmem + kTcDq, dqa + 128 * k, dqb + 128 * k, idq, k > 0);
+          tc_commit(bar(TB_QDONE));
+          tc_commit(bar(TB_CEMPTY + 0));
+          tc_commit(bar(TB_CEMPTY + 1));
+        }
       }
       // every MMA issued has completed before tensor memory is released
       tc_commit(bar(TB_DRAIN));
@@ -1139,9 +1188,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         sq_next = ws.sq[static_cast<size_t>(bh) * nkt + ((qtile + 1) >> 1)];
         sdo_next = ws.sdo[static_cast<size_t>(bh) * nkt + ((qtile + 1) >> 1)];
       }
+      // a failed wait is voted on below, before anything is published
       bool ok = waitw_ab(bar(TB_SDONE + b), (it >> 1) & 1, ctl, abort) &&
                 waitw_ab(bar(TB_FULL + s), (it / kTcStages) & 1, ctl, abort);
-      if (!group_and(ok)) break;
       tc_fence_after();
       // this half of the S^T and dP^T rows: two loads in flight, one wait
       uint32_t ru[2][32];
@@ -1204,8 +1253,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         red[(b * 2 + 0) * 8 + sw] = pmax;
         red[(b * 2 + 1) * 8 + sw] = smax;
       }
-      // the codes buffer is free once dV, dK (tile it - 2) and dQ have read it
-      ok = it < 2 || waitw_ab(bar(TB_CEMPTY + b), ((it >> 1) - 1) & 1, ctl, abort);
+      // the codes buffer is free once dV, dK (tile it - 2) and the pair's dQ have read it
+      ok = ok && (it < 2 || waitw_ab(bar(TB_CEMPTY + b), ((it >> 1) - 1) & 1, ctl, abort));
       if (!group_and(ok)) break;  // also publishes red[]
       float pa = red[(b * 2) * 8], sa = red[(b * 2 + 1) * 8];
 #pragma unroll
@@ -1217,10 +1266,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float sinv = sa > 0.0f ? __fdiv_rn(127.0f, sa) : 0.0f;
       uint8_t* cbuf = smem + L::kCodesOff + b * L::kCodes;
       const uint64_t pp = pack2(pinv, pinv), ss = pack2(sinv, sinv);
-      // rint(x * inv) for a pair, as FP16x2 (the products rounded per lane)
-      auto code2 = [](float a, float b, uint64_t inv2) {
-        const uint64_t y = mul2(pack2(a, b), inv2);
-        return h2(rintf(lo2(y)), rintf(hi2(y)));
+      // rint(x * inv) for a pair, as FP16x2: the products rounded per lane to
+      // FP32, then to integers by adding and subtracting 1.5 * 2^23 (exact)
+      const uint64_t magic2 = pack2(kRintMagic, kRintMagic), nmagic2 = pack2(-kRintMagic, -kRintMagic);
+      auto code2 = [&](float a, float b, uint64_t inv2) {
+        const uint64_t y = add2(add2(mul2(pack2(a, b), inv2), magic2), nmagic2);
+        return h2(lo2(y), hi2(y));
       };
 #pragma unroll
       for (int ch = 0; ch < 4; ch++) {
@@ -1238,9 +1289,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (threadIdx.x == 128) {
         const float sp = __fdiv_rn(pa, 127.0f), sds = __fdiv_rn(sa, 127.0f);
-        scal[4 * b + 0] = sp * sdo;          // dV
-        scal[4 * b + 1] = sds * sq;          // dK (the softmax scale comes at the end)
-        scal[4 * b + 2] = sds * sk * scale;  // dQ
+        float* sc = scal + 4 * (it & 3);
+        sc[0] = sp * sdo;          // dV
+        sc[1] = sds * sq;          // dK (the softmax scale comes at the end)
+        sc[2] = sds * sk * scale;  // dQ
       }
       // the codes (generic-proxy writes) -> visible to the tensor core
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1248,68 +1300,76 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) mbar_arrive1(bar(TB_CFULL + b));
     }
   } else {
-    // ---- dV and dK folds, and dQ (warpgroup 3)
+    // ---- dV and dK folds, and dQ read out (warpgroup 3)
     sagefp4::regs_inc<TcRegs::kFold>();
-    const int row = 32 * (warp & 3) + lane;  // key row of the folds
+    const int row = 32 * (warp & 3) + lane;  // key row of the folds; query row of a tile pair's dQ
     const uint32_t lanebase = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const int g = lane >> 2, t = lane & 3, j = lane >> 3;
-    const int r0 = 16 * (warp & 3);  // this warp's 16 dQ rows
-    float accv[64], acck[64];
+    uint64_t accv[32], acck[32];  // FP32 pairs
 #pragma unroll
-    for (int i = 0; i < 64; i++) accv[i] = acck[i] = 0.0f;
+    for (int i = 0; i < 32; i++) accv[i] = acck[i] = 0;
+    float fq[2] = {0.0f, 0.0f};  // dQ scales of the pair's two tiles
     for (int it = 0; it < niter; it++) {
-      const int b = it & 1, qtile = q0 + it;
+      const int b = it & 1;
+      // CFULL: this tile's block scales are written
       if (!waitw_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort)) break;
-      const float f_dv = scal[4 * b + 0], f_dk = scal[4 * b + 1], f_dq = scal[4 * b + 2];
-      // dQ[64 x 64] += f_dq (dS^ K^): this warp's 16 rows, all 64 columns
-      // (eight independent accumulators); dS^ and K^ read transposed
-      const uint32_t dsb = sbase + L::kCodesOff + b * L::kCodes + L::kCS;
-      {
-        float q8[8][4];
-#pragma unroll
-        for (int i = 0; i < 8; i++) q8[i][0] = q8[i][1] = q8[i][2] = q8[i][3] = 0.0f;
-#pragma unroll
-        for (int kc = 0; kc < kTok / 16; kc++) {
-          uint32_t a[4];
-          ldsm_x4_t(dsb + swz(16 * kc + ((j >> 1) << 3) + (lane & 7), 2 * (r0 + ((j & 1) << 3)), 128), a[0], a[1],
-                    a[2], a[3]);
-#pragma unroll
-          for (int nd = 0; nd < 8; nd += 2) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(sbase + L::kK + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 16 * (nd + (j >> 1)), 128), b0, b1,
-                      b2, b3);
-            mma_f16(q8[nd], a, b0, b1);
-            mma_f16(q8[nd + 1], a, b2, b3);
-          }
-        }
-        float* dq0 = ws.dqacc + (hrow + static_cast<size_t>(qtile) * kQ + r0 + g) * D + 2 * t;
-#pragma unroll
-        for (int nd = 0; nd < 8; nd++) {
-          red_add_v2(dq0 + 8 * nd, q8[nd][0] * f_dq, q8[nd][1] * f_dq);
-          red_add_v2(dq0 + 8 * D + 8 * nd, q8[nd][2] * f_dq, q8[nd][3] * f_dq);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive1(bar(TB_CEMPTY + b));
-      // fold this tile's partials
-      if (!waitw_ab(bar(TB_PDONE + b), (it >> 1) & 1, ctl, abort)) break;
+      const float* sc = scal + 4 * (it & 3);
+      const uint64_t fv = pack2(sc[0], sc[0]), fk = pack2(sc[1], sc[1]);
+      fq[b] = sc[2];
+      if (!waitw_ab(bar(TB_PDONE), it & 1, ctl, abort)) break;
       tc_fence_after();
 #pragma unroll
       for (int qc = 0; qc < 4; qc++) {
         uint32_t rv[16], rk[16];
-        sagefp4::tmem_ld16(tmem + lanebase + kTcDv + 64 * b + 16 * qc, rv);
-        sagefp4::tmem_ld16(tmem + lanebase + kTcDk + 64 * b + 16 * qc, rk);
+        sagefp4::tmem_ld16(tmem + lanebase + kTcDv + 16 * qc, rv);
+        sagefp4::tmem_ld16(tmem + lanebase + kTcDk + 16 * qc, rk);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-          accv[16 * qc + i] = fmaf(__uint_as_float(rv[i]), f_dv, accv[16 * qc + i]);
-          acck[16 * qc + i] = fmaf(__uint_as_float(rk[i]), f_dk, acck[16 * qc + i]);
+        for (int i = 0; i < 8; i++) {
+          accv[8 * qc + i] = fma2(pack2(__uint_as_float(rv[2 * i]), __uint_as_float(rv[2 * i + 1])), fv, accv[8 * qc + i]);
+          acck[8 * qc + i] = fma2(pack2(__uint_as_float(rk[2 * i]), __uint_as_float(rk[2 * i + 1])), fk, acck[8 * qc + i]);
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive1(bar(TB_PFREE + b));
+      if (lane == 0) mbar_arrive1(bar(TB_PFREE));
+      if (b == 1) {
+        // dQ rows of query tiles it - 1 (rows 0..63) and it (64..127)
+        if (!waitw_ab(bar(TB_QDONE), (it >> 1) & 1, ctl, abort)) break;
+        tc_fence_after();
+        const float f = row < kQ ? fq[0] : fq[1];
+        const uint64_t f2 = pack2(f, f);
+        // this warp's rows of the pair in the accumulator viewed as [B*H*Np][64]
+        const int y0 = static_cast<int>(hrow) + (q0 + it - 1) * kQ + 32 * (warp & 3);
+        uint8_t* wt = smem + L::kDqOff + 4096 * (warp & 3);
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lanebase + kTcDq + 32 * hh, r);
+          if (lane == 0) bulk_wait_read();  // the staging tile's previous reduction has read it
+          __syncwarp();
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 8; c++) {
+            const uint64_t x01 = mul2(pack2(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1])), f2);
+            const uint64_t x23 = mul2(pack2(__uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3])), f2);
+            *reinterpret_cast<uint4*>(wt + swz(lane, 16 * c, 128)) =
+                make_uint4(static_cast<uint32_t>(x01), static_cast<uint32_t>(x01 >> 32), static_cast<uint32_t>(x23),
+                           static_cast<uint32_t>(x23 >> 32));
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_2d(&tm_dq, smem_addr(wt), 32 * hh, y0);
+            bulk_commit();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive1(bar(TB_QFREE));
+      }
     }
+    if (lane == 0) bulk_wait_all();  // the dQ reductions have read shared memory and completed
+    __syncwarp();
     if (!*abort) {
       const int key = kb * kTok + row;
       if (key < N) {
@@ -1317,14 +1377,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int which = 0; which < 2; which++) {
           uint16_t* dst = (which == 0 ? dv : dk) + (static_cast<size_t>(bh) * N + key) * D;
           const float f = which == 0 ? 1.0f : scale;
-          const float* acc = which == 0 ? accv : acck;
+          const uint64_t* acc = which == 0 ? accv : acck;
 #pragma unroll
           for (int c = 0; c < 8; c++) {
             uint4 w;
-            __nv_bfloat162 h0 = __floats2bfloat162_rn(acc[8 * c + 0] * f, acc[8 * c + 1] * f);
-            __nv_bfloat162 h1 = __floats2bfloat162_rn(acc[8 * c + 2] * f, acc[8 * c + 3] * f);
-            __nv_bfloat162 h2v = __floats2bfloat162_rn(acc[8 * c + 4] * f, acc[8 * c + 5] * f);
-            __nv_bfloat162 h3 = __floats2bfloat162_rn(acc[8 * c + 6] * f, acc[8 * c + 7] * f);
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(lo2(acc[4 * c + 0]) * f, hi2(acc[4 * c + 0]) * f);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(lo2(acc[4 * c + 1]) * f, hi2(acc[4 * c + 1]) * f);
+            __nv_bfloat162 h2v = __floats2bfloat162_rn(lo2(acc[4 * c + 2]) * f, hi2(acc[4 * c + 2]) * f);
+            __nv_bfloat162 h3 = __floats2bfloat162_rn(lo2(acc[4 * c + 3]) * f, hi2(acc[4 * c + 3]) * f);
             w.x = *reinterpret_cast<uint32_t*>(&h0);
             w.y = *reinterpret_cast<uint32_t*>(&h1);
             w.z = *reinterpret_cast<uint32_t*>(&h2v);
@@ -1473,17 +1533,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp == 1 && lane == 0) {
       // ---- MMA issue
       const uint32_t idS = idesc_f16(128, 128), idPV = idesc_f16(128, 64);
+      // descriptors built once per operand; a K step of 16 moves 32 bytes (+2)
+      const uint64_t dq0 = desc_k64(sbase + L::kQ, 0);
       bool ok = wait1_ab(bar(FB_Q), 0, ctl, abort);
       auto issue_s = [&](int kt) {
         const int s = kt % kTcStages, b = kt & 1;
         if (!wait1_ab(bar(FB_FULL + s), (kt / kTcStages) & 1, ctl, abort)) return false;
         if (kt >= 2 && !wait1_ab(bar(FB_SFREE + b), ((kt >> 1) - 1) & 1, ctl, abort)) return false;
         tc_fence_after();
-        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+        const uint64_t dks = desc_k64(sbase + L::kStageOff + s * L::kStage + L::kSK, 0);
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-          mma_f16_tc(tmem + kTfS + 128 * b, desc_k64(sbase + L::kQ, 16 * k), desc_k64(st + L::kSK, 16 * k), idS,
-                     k > 0);
+        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTfS + 128 * b, dq0 + 2 * k, dks + 2 * k, idS, k > 0);
         tc_commit(bar(FB_SDONE + b));
         return true;
       };
@@ -1494,12 +1554,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!(ok = wait1_ab(bar(FB_PFULL + b), (kt >> 1) & 1, ctl, abort))) break;
         if (kt >= 2 && !(ok = wait1_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort))) break;
         tc_fence_after();
-        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
-        const uint32_t pb = sbase + L::kPOff + b * L::kP;
+        // P^ key slabs 16 KB apart (+1024), V^T key halves 8 KB apart (+512)
+        const uint64_t dpb = desc_k64(sbase + L::kPOff + b * L::kP, 0);
+        const uint64_t dvs = desc_k64(sbase + L::kStageOff + s * L::kStage + L::kSV, 0);
 #pragma unroll
         for (int k = 0; k < 8; k++)
-          mma_f16_tc(tmem + kTfPv + 64 * b, desc_k64(pb + (k >> 2) * 16384, 16 * (k & 3)),
-                     desc_k64(st + L::kSV + (k >> 2) * 8192, 16 * (k & 3)), idPV, k > 0);
+          mma_f16_tc(tmem + kTfPv + 64 * b, dpb + 1024 * (k >> 2) + 2 * (k & 3), dvs + 512 * (k >> 2) + 2 * (k & 3),
+                     idPV, k > 0);
         tc_commit(bar(FB_PVDONE + b));
         tc_commit(bar(FB_EMPTY + s));
         tc_commit(bar(FB_PEMPTY + b));
@@ -1775,6 +1836,67 @@ __global__ void __launch_bounds__(128) umma_probe_kernel(const uint16_t* __restr
   if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
+// Probe of the MN-major form: one CTA computes c [128][64] = a [128][128] x
+// b [128][64] (FP16 in, FP32 out, row-major device arrays) with both operands
+// staged K-row by K-row, A's two 64-row blocks of M 32 KB apart (as dQ reads
+// two query tiles' dS^ codes from two buffers) and B between them.
+constexpr int kMnProbeSmem = 3 * 16384 + 1024;
+__global__ void __launch_bounds__(128) umma_mn_probe_kernel(const uint16_t* __restrict__ a,
+                                                            const uint16_t* __restrict__ b, float* __restrict__ c,
+                                                            int32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tslot;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  constexpr int kA0 = 0, kB = 16384, kA1 = 32768;
+  for (int i = tid; i < 128 * 128; i += 128) {  // a[m][k] -> row k of block m / 64
+    const int m = i >> 7, k = i & 127;
+    *reinterpret_cast<uint16_t*>(sm + (m < 64 ? kA0 : kA1) + swz(k, 2 * (m & 63), 128)) = a[i];
+  }
+  for (int i = tid; i < 128 * 64; i += 128) {  // b[k][n] -> row k
+    const int k = i >> 6, n = i & 63;
+    *reinterpret_cast<uint16_t*>(sm + kB + swz(k, 2 * n, 128)) = b[i];
+  }
+  if (tid == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_addr(&tslot), 64);
+    tmem_relinquish();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tslot;
+  const uint32_t sb = smem_addr(sm);
+  if (tid == 0) {
+    const uint32_t id = idesc_f16_mn(128, 64);
+#pragma unroll
+    for (int k = 0; k < 8; k++)
+      mma_f16_tc(tmem, desc_mn(sb + kA0, 16 * k, kA1 - kA0), desc_mn(sb + kB, 16 * k, kA1 - kA0), id, k > 0);
+    tc_commit(smem_addr(&bar));
+  }
+  const Ctl ctl{status, 100ull * 1000ull * 1000ull};
+  const bool ok = waitw(smem_addr(&bar), 0, ctl);
+  tc_fence_after();
+  if (ok) {
+    const int row = 32 * warp + (tid & 31);
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + c0, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; j++) c[row * 64 + c0 + j] = __uint_as_float(r[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
 
 // Integer products on the FP16 MMA: one warp computes the 16 x 8 product of
 // INT8 matrices a [16][K] and b [8][K] (both row-major, K a multiple of 16)
@@ -1947,9 +2069,34 @@ cudaError_t launch_dkdv(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int N, 
 // The tcgen05 backward (D = 64).  Its warpgroups' setmaxnreg budgets add up
 // to exactly 128 registers per thread at launch; with any other allocation
 // an increase would never be granted, so it refuses to launch.
+// 2-D FP32 tensor [rows][inner] (row pitch inner * 4 bytes) with boxes of
+// [box_rows][box_inner], 128-byte swizzled (box_inner * 4 <= 128).
+bool make_map_f32(CUtensorMap* m, const float* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                  uint32_t box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if (!enc) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool C>
 cudaError_t launch_dkdv_tc(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int N, float scale, cudaStream_t st,
                            uint64_t wait_ns, int withhold) {
+  const uint64_t rows = static_cast<uint64_t>(BH) * ((N + kTok - 1) / kTok * kTok);
+  CUtensorMap tm;
+  if (rows > 0x7fffffffu || !make_map_f32(&tm, w.dqacc, 64, rows, 32, 32)) return cudaErrorInvalidValue;
   cudaFuncAttributes attr;
   cudaError_t e = cudaFuncGetAttributes(&attr, dkdv_tc_kernel<C>);
   if (e != cudaSuccess) return e;
@@ -1957,7 +2104,7 @@ cudaError_t launch_dkdv_tc(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int 
   e = cudaFuncSetAttribute(dkdv_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::kAlloc);
   if (e != cudaSuccess) return e;
   const dim3 grid((N + kTok - 1) / kTok, BH);
-  dkdv_tc_kernel<C><<<grid, kTcThreads, TcSmem::kAlloc, st>>>(w, dk, dv, N, scale, wait_ns, withhold);
+  dkdv_tc_kernel<C><<<grid, kTcThreads, TcSmem::kAlloc, st>>>(tm, w, dk, dv, N, scale, wait_ns, withhold);
   return cudaGetLastError();
 }
 
@@ -2172,6 +2319,17 @@ int sagebwd_umma_probe(const uint16_t* a, const uint16_t* b, int N, float* c, in
   const int dev = check_device();
   if (dev != SAGE_FP4_OK) return dev;
   umma_probe_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(a, b, N, c, status);
+  return from_cuda(cudaGetLastError());
+}
+
+int sagebwd_umma_mn_probe(const uint16_t* a, const uint16_t* b, float* c, int32_t* status, void* stream) {
+  if (!aligned(a, 2) || !aligned(b, 2) || !aligned(c, 4) || !aligned(status, 4)) return SAGE_FP4_EINVAL;
+  const int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  cudaError_t e = cudaFuncSetAttribute(sagebwd::umma_mn_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       sagebwd::kMnProbeSmem);
+  if (e != cudaSuccess) return from_cuda(e);
+  sagebwd::umma_mn_probe_kernel<<<1, 128, sagebwd::kMnProbeSmem, static_cast<cudaStream_t>(stream)>>>(a, b, c, status);
   return from_cuda(cudaGetLastError());
 }
 

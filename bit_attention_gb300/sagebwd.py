@@ -55,6 +55,7 @@ def lib() -> ctypes.CDLL:
                 "sagebwd_dq_out": (i, [vp, i, i, i, i, vp, sz, vp]),
                 "sagebwd_stall_test": (i, [i, vp, vp, i, i, i, i, f, ctypes.c_uint64, vp, sz, vp]),
                 "sagebwd_umma_probe": (i, [vp, vp, i, vp, vp, vp]),
+                "sagebwd_umma_mn_probe": (i, [vp, vp, vp, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -122,6 +123,10 @@ def sagebwd_mma_peak(kind: int, ctas: int, iters: int, scratch_ptr, stream) -> i
 
 def sagebwd_umma_probe(a_ptr, b_ptr, N: int, c_ptr, status_ptr, stream) -> int:
     return lib().sagebwd_umma_probe(a_ptr, b_ptr, N, c_ptr, status_ptr, stream)
+
+
+def sagebwd_umma_mn_probe(a_ptr, b_ptr, c_ptr, status_ptr, stream) -> int:
+    return lib().sagebwd_umma_mn_probe(a_ptr, b_ptr, c_ptr, status_ptr, stream)
 
 
 def sagebwd_int_mma_probe(a_ptr, b_ptr, K: int, out_ptr, stream) -> int:

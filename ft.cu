@@ -1,0 +1,2383 @@
+// sagebwd.cu -- SageBwd, the 8-bit attention for training: forward and
+// backward kernels and the C ABI of include/sagebwd.h (senqingzn.com article
+// on SageAttention3, "INT8 attention for training" and "Solving two obstacles
+// and one difficulty", difficulty 3; abstract of "SageAttention3: Microscaling
+// FP4 Attention for Inference and An Exploration of 8-Bit Training").
+//
+// Six of the seven products take INT8 operands: S = Q K^T (forward, and again
+// in the backward), O = P V, dV = P^T dO, dQ = dS K, dK = dS^T Q.  dP = dO V^T,
+// the product that forms the attention-map gradient, takes FP16 operands.
+// Quantization: Q, K, V, dO per head in blocks of 128 tokens, P and dS per
+// block of 64 queries x 128 keys, scale amax / 127, codes
+// rint(x * (127 / amax)).  The forward is FlashAttention's online softmax
+// (P~ = exp(S - running max) quantized per block, the normaliser summed from
+// the unquantized P~); the backward recomputes P = exp(S - L) from the saved
+// log-sum-exp.
+//
+// The INT8 products on sm_103a.  This GPU has no INT8 form of tcgen05.mma,
+// and its warp-level INT8 MMA (m16n8k32) runs at a quarter of the FP16 one
+// (m16n8k16, FP32 accumulation).  An INT8 code is an integer in [-127, 127],
+// exact in FP16; the product of two is exact in FP32, and so is every sum of
+// such products below 2^24 (127^2 * 128 < 2^21 here).  So the six INT8
+// products run on the FP16 MMA with the codes stored as FP16 values, and give
+// the integer results an INT8 MMA would (sagebwd_int_mma_probe checks this on
+// the hardware).  Each block's integer sum is then scaled by its two block
+// scales in FP32.
+//
+// Layout.  Every operand lives in the workspace as FP16 rows [token][D] whose
+// 16-byte chunks are XOR-permuted by (row & 7): any 8-row-aligned run of rows
+// is a bank-conflict-free shared-memory tile for ldmatrix after one bulk copy.
+// Operands needed transposed are read with ldmatrix.trans, and an MMA's FP32
+// accumulator fragment is, pairwise converted, the A fragment of the next MMA,
+// so no operand is stored twice.
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sagebwd.h"
+#include "ptx.cuh"
+
+__device__ long long g_trace[16][256];
+__device__ unsigned long long g_span[4096][3];
+#define TR(slot, it) do { if (blockIdx.x == 0 && blockIdx.y == 0 && (it) < 256) g_trace[slot][it] = clock64(); } while (0)
+namespace sagebwd {
+
+using sagefp4::bulk_load;
+using sagefp4::globaltimer_ns;
+using sagefp4::mbar_arrive_expect_tx;
+using sagefp4::mbar_fence_init;
+using sagefp4::mbar_init;
+using sagefp4::mbar_try_wait;
+using sagefp4::smem_addr;
+using sagefp4::smem_desc;
+using sagefp4::add2;
+using sagefp4::fma2;
+using sagefp4::hi2;
+using sagefp4::lo2;
+using sagefp4::max3f;
+using sagefp4::mul2;
+using sagefp4::pack2;
+using sagefp4::tc_commit;
+using sagefp4::tc_fence_after;
+using sagefp4::tc_fence_before;
+using sagefp4::tmem_alloc;
+using sagefp4::tmem_dealloc;
+using sagefp4::tmem_ld32;
+using sagefp4::tmem_relinquish;
+using sagefp4::tmem_wait_ld;
+using sagefp4::kSwizzle128B;
+
+constexpr int kTok = 128;  // token block of Q, K, V, dO; key tile; key edge of a P / dS block
+constexpr int kQ = 64;     // query tile of the backward; query edge of a P / dS block
+constexpr int kThreads = 256;
+constexpr unsigned kFull = 0xffffffffu;
+constexpr uint64_t kWaitNs = 1500ull * 1000ull * 1000ull;  // bounded copy waits: 1.5 s
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------- layout
+// Byte offset of logical (row, byte) in rows W bytes wide (W = 2D: 128 or
+// 256): the 16-byte chunk index is XORed with row & 7, so the eight rows one
+// ldmatrix reads at the same logical chunk fall in eight bank groups.
+__host__ __device__ __forceinline__ int swz(int row, int byte, int W) {
+  return row * W + ((((byte >> 4) ^ (row & 7))) << 4) + (byte & 15);
+}
+
+// ---------------------------------------------------------------- helpers
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_s8(int (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+r"(c[0]), "+r"(c[1]), "+r"(c[2]), "+r"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two floats -> FP16x2 (lo in the low half), rounded to nearest; exact for
+// the integer codes.
+__device__ __forceinline__ uint32_t h2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// INT8 code of x in a block with 127 / amax = inv: rint(x * inv) as a float
+// (|x| <= amax keeps it within [-127, 127]).
+__device__ __forceinline__ float code(float x, float inv) { return rintf(__fmul_rn(x, inv)); }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// rint by FP32 arithmetic: (z + 1.5 * 2^23) - 1.5 * 2^23 is z rounded to the
+// nearest integer, ties to even, exactly, for |z| < 2^22.
+constexpr float kRintMagic = 12582912.0f;
+
+// Warp-wide maximum of unsigned words (every lane gets it).
+__device__ __forceinline__ uint32_t redux_max_u32(uint32_t v) {
+  uint32_t r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void red_add_v2(float* p, float a, float b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
+}
+
+// Tensor reduction by the copy engine: the box of `map` at (x, y) += the
+// shared-memory tile at ssrc (laid out with the map's swizzle), element-wise
+// in the map's type, in this thread's bulk group.  wait_read: this thread's
+// bulk operations have read their shared-memory sources; wait_all: they have
+// completed.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t ssrc, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(ssrc), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+struct Ctl {
+  int32_t* status;
+  uint64_t limit;
+};
+
+// Bounded wait by a whole warp for an mbarrier phase.  False: the copy never
+// completed; the status word holds SAGE_FP4_ETIMEOUT.
+__device__ __forceinline__ bool waitw(uint32_t bar, uint32_t parity, const Ctl& c) {
+  if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+    int stop = 0;
+    if ((threadIdx.x & 31) == 0 && globaltimer_ns() - t0 > c.limit) {
+      atomicCAS(c.status, 0, SAGE_FP4_ETIMEOUT);
+      stop = 1;
+    }
+    if (__shfl_sync(kFull, stop, 0)) return false;
+  }
+}
+
+// Wait used only while abandoning work, so that no copy is still writing
+// shared memory when the CTA exits: bounded, result ignored.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const Ctl& c) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < c.limit) {
+  }
+}
+
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+
+// -> FP16 bits, rounded to nearest even, saturated to +-65504.
+__device__ __forceinline__ uint16_t f2h_sat(float x) {
+  x = fminf(fmaxf(x, -65504.0f), 65504.0f);
+  return __half_as_ushort(__float2half_rn(x));
+}
+
+// ---------------------------------------------------------------- workspace
+struct Ws {
+  uint16_t *qc, *kc, *vc, *doc;  // INT8 codes as FP16 values, swizzled rows
+  uint16_t *vh, *doh;            // V and dO as FP16 values, swizzled rows
+  uint16_t *qct, *doct;          // Q^ and dO^ codes transposed: [64-token tile][D][64], swizzled rows
+  uint16_t* vct;                 // V^ codes transposed: [128-token tile][2 key halves][D][64], swizzled rows
+  float *sq, *sk, *sv, *sdo, *l2, *dd, *dqacc;
+  int32_t* status;
+};
+
+// ---------------------------------------------------------------- quantizer
+// One CTA per (128-token block, head).  kind 0: Q, 1: K, 2: V (codes and the
+// FP16 values), 3: dO (codes and FP16 values), with D_i = sum_d dO_id O_id,
+// the negated log-sum-exp in log2 units, and dQ's accumulator rows zeroed.
+template <int D>
+__global__ void __launch_bounds__(kThreads) quant_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+                                                         const uint16_t* __restrict__ v, const uint16_t* __restrict__ o,
+                                                         const float* __restrict__ lse, int N, int kind0, Ws ws) {
+  __shared__ __align__(16) uint16_t xs[kTok * D];
+  __shared__ float red[kThreads / 32];
+  const int kind = kind0 + blockIdx.z;
+  const int blk = blockIdx.x, bh = blockIdx.y;
+  const int nb = (N + kTok - 1) / kTok;
+  const int Np = nb * kTok;
+  const int n0 = blk * kTok;
+  const int rows = min(kTok, N - n0);
+  const uint16_t* x = (kind == 1 ? k : kind == 2 ? v : q) + (static_cast<size_t>(bh) * N + n0) * D;
+  const int tid = threadIdx.x;
+
+  // load the block (zeros past N) and find its largest magnitude
+  float amax = 0.0f;
+  constexpr int kVec = kTok * D / 8;  // 16-byte vectors
+  for (int i = tid; i < kVec; i += kThreads) {
+    const int r = i / (D / 8);
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (r < rows) val = __ldg(reinterpret_cast<const uint4*>(x) + i);
+    reinterpret_cast<uint4*>(xs)[i] = val;
+    const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[j] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[j] & 0xffff0000u)));
+    }
+  }
+  amax = warp_max(amax);
+  if ((tid & 31) == 0) red[tid >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; w++) amax = fmaxf(amax, red[w]);
+  const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+  const size_t hb = static_cast<size_t>(bh) * Np * D;  // this head's first element
+  if (tid == 0) {
+    float* s = kind == 0 ? ws.sq : kind == 1 ? ws.sk : kind == 2 ? ws.sv : ws.sdo;
+    s[static_cast<size_t>(bh) * nb + blk] = __fdiv_rn(amax, 127.0f);
+  }
+  uint16_t* codes = kind == 0 ? ws.qc : kind == 1 ? ws.kc : kind == 2 ? ws.vc : ws.doc;
+  uint16_t* vals = kind == 2 ? ws.vh : ws.doh;
+  char* cbase = reinterpret_cast<char*>(codes + hb + static_cast<size_t>(n0) * D);
+  char* vbase = reinterpret_cast<char*>(vals + hb + static_cast<size_t>(n0) * D);
+  // one 16-byte chunk (8 channels of one row) per step
+  for (int i = tid; i < kTok * D / 8; i += kThreads) {
+    const int r = i / (D / 8), c = i % (D / 8);
+    uint32_t hc[4], hv[4];
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const float a = bf2f(xs[r * D + 8 * c + 2 * j]), b = bf2f(xs[r * D + 8 * c + 2 * j + 1]);
+      hc[j] = h2(code(a, inv), code(b, inv));
+      hv[j] = static_cast<uint32_t>(f2h_sat(a)) | (static_cast<uint32_t>(f2h_sat(b)) << 16);
+    }
+    const int off = swz(r, 16 * c, 2 * D);
+    *reinterpret_cast<uint4*>(cbase + off) = make_uint4(hc[0], hc[1], hc[2], hc[3]);
+    if (kind >= 2) *reinterpret_cast<uint4*>(vbase + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+  }
+  if (kind == 0 || kind == 2 || kind == 3) {
+    // the same codes transposed, per 64-token tile: [D rows][64 tokens], the
+    // K-major B operand of dK = dS^T Q and dV = P^T dO, and for V of PV (the
+    // two 64-token halves of a 128-token tile are consecutive: [2][D][64])
+    uint16_t* tdst = kind == 0 ? ws.qct : kind == 2 ? ws.vct : ws.doct;
+    for (int i = tid; i < D * (kTok / 8); i += kThreads) {
+      const int d = i % D, c = i / D;  // c: 8-token chunk of the block
+      uint32_t h[4];
+#pragma unroll
+      for (int j = 0; j < 4; j++)
+        h[j] = h2(code(bf2f(xs[(8 * c + 2 * j) * D + d]), inv), code(bf2f(xs[(8 * c + 2 * j + 1) * D + d]), inv));
+      const int tile = (n0 + 8 * c) / kQ, within = (8 * c) % kQ;
+      char* tb = reinterpret_cast<char*>(tdst + hb + static_cast<size_t>(tile) * kQ * D);
+      *reinterpret_cast<uint4*>(tb + swz(d, 2 * within, 2 * kQ)) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+  }
+  if (kind == 3) {
+    // D_i = sum_d dO_id O_id and -L in log2 units: one warp per row
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int r = warp; r < kTok; r += kThreads / 32) {
+      float acc = 0.0f;
+      if (r < rows) {
+        const uint16_t* orow = o + (static_cast<size_t>(bh) * N + n0 + r) * D;
+        for (int d = lane; d < D; d += 32) acc = fmaf(bf2f(xs[r * D + d]), bf2f(orow[d]), acc);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFull, acc, off);
+      if (lane == 0) {
+        const size_t ix = static_cast<size_t>(bh) * Np + n0 + r;
+        ws.dd[ix] = acc;
+        ws.l2[ix] = r < rows ? -lse[static_cast<size_t>(bh) * N + n0 + r] * kLog2e : 0.0f;
+      }
+    }
+    float4* acc = reinterpret_cast<float4*>(ws.dqacc + (static_cast<size_t>(bh) * Np + n0) * D);
+    for (int i = tid; i < kTok * D / 4; i += kThreads) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// ---------------------------------------------------------------- forward
+// One CTA of 8 warps per (128 queries, head).  Warp w owns query rows
+// 16w..16w+15; warps 0-3 and 4-7 form the two 64-query P blocks.  Key tiles
+// of 128 (K^ and V^ codes) stream through two shared-memory stages by bulk
+// copy.
+template <int D>
+struct FwdSmem {
+  static constexpr int kRow = 2 * D;         // bytes per FP16 row
+  static constexpr int kTile = kTok * kRow;  // one 128-row tile
+  static constexpr int kQOff = 0;
+  static constexpr int kStageOff = kTile;
+  static constexpr int kStage = 2 * kTile;                // K^ then V^
+  static constexpr int kBarOff = kStageOff + 2 * kStage;  // 3 mbarriers: q, full[2]
+  static constexpr int kRedOff = kBarOff + 64;            // [2][8] floats
+  static constexpr int kBytes = kRedOff + 2 * 8 * 4;
+};
+
+template <int D, bool kCausal>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(Ws ws, uint16_t* __restrict__ out, float* __restrict__ lse, int N, float scale_log2e, uint64_t wait_ns,
+               int withhold) {
+  using L = FwdSmem<D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int nqt = (N + kTok - 1) / kTok;
+  const int Np = nqt * kTok;
+  // causal: the longest rows first
+  const int qt = kCausal ? (nqt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int bh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3, j = lane >> 3;
+  const int grp = warp >> 2;
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t qbar = sbase + L::kBarOff, full0 = qbar + 8;
+  float* redp = reinterpret_cast<float*>(smem + L::kRedOff);
+  const Ctl ctl{ws.status, wait_ns};
+  const int nkt = kCausal ? qt + 1 : nqt;
+  const size_t hb = static_cast<size_t>(bh) * Np * D;
+
+  if (threadIdx.x == 0) {
+    mbar_init(qbar, 1);
+    mbar_init(full0, 1);
+    mbar_init(full0 + 8, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  auto issue_tile = [&](int kt) {
+    const int s = kt & 1;
+    const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+    mbar_arrive_expect_tx(full0 + 8 * s, L::kStage);
+    bulk_load(st, ws.kc + hb + static_cast<size_t>(kt) * kTok * D, L::kTile, full0 + 8 * s);
+    bulk_load(st + L::kTile, ws.vc + hb + static_cast<size_t>(kt) * kTok * D, L::kTile, full0 + 8 * s);
+  };
+  int issued = 0;  // key tiles whose copies thread 0 has issued
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(qbar, L::kTile);
+    bulk_load(sbase + L::kQOff, ws.qc + hb + static_cast<size_t>(qt) * kTok * D, L::kTile, qbar);
+    // withhold (failure-detection test only): CTA 0 never issues key tile 0,
+    // so its wait for that tile runs out
+    if (withhold && blockIdx.x == 0 && blockIdx.y == 0) issued = 1;
+    for (; issued < 2 && issued < nkt; issued++) issue_tile(issued);
+  }
+  // every wait's outcome is voted on by the whole CTA, so that all warps
+  // carry on or all give up together
+  bool ok = __syncthreads_and(waitw(qbar, 0, ctl));
+
+  const float sqk = ws.sq[static_cast<size_t>(bh) * nqt + qt] * scale_log2e;
+  const int row0 = qt * kTok + 16 * warp + g;  // this thread's rows: row0, row0 + 8
+  const bool valid0 = row0 < N, valid1 = row0 + 8 < N;
+  const uint32_t qrow = sbase + L::kQOff;
+  const int arow = 16 * warp + ((j & 1) << 3) + (lane & 7);  // A-fragment row this lane addresses
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+  // this key tile's block scales, read one tile ahead
+  float sk_next = ws.sk[static_cast<size_t>(bh) * nqt], sv_next = ws.sv[static_cast<size_t>(bh) * nqt];
+
+  for (int kt = 0; kt < nkt && ok; kt++) {
+    const float sk_cur = sk_next, sv_cur = sv_next;
+    const int s = kt & 1;
+    const uint32_t kst = sbase + L::kStageOff + s * L::kStage, vst = kst + L::kTile;
+    ok = __syncthreads_and(waitw(full0 + 8 * s, (kt >> 1) & 1, ctl));
+    if (!ok) break;
+    // every warp is done with tile kt - 1: its stage takes tile kt + 1
+    if (threadIdx.x == 0 && kt >= 1 && kt + 1 < nkt) issue_tile(issued++);
+    // S = Q^ K^^T for 16 rows x 128 keys (integer sums in FP32)
+    float x[16][4];
+#pragma unroll
+    for (int nb = 0; nb < 16; nb++) x[nb][0] = x[nb][1] = x[nb][2] = x[nb][3] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ks++) {
+      uint32_t qa[4];
+      ldsm_x4(qrow + swz(arow, 32 * ks + ((j >> 1) << 4), L::kRow), qa[0], qa[1], qa[2], qa[3]);
+#pragma unroll
+      for (int nb = 0; nb < 16; nb += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kst + swz(8 * (nb + (j >> 1)) + (lane & 7), 32 * ks + ((j & 1) << 4), L::kRow), b0, b1, b2, b3);
+        mma_f16(x[nb], qa, b0, b1);
+        mma_f16(x[nb + 1], qa, b2, b3);
+      }
+    }
+    // scale to log2 units, mask, row maxima
+    const float c2 = sqk * sk_cur;
+    const bool edge = (kCausal && kt == qt) || (kt == nqt - 1 && (N % kTok) != 0);
+    float tm0 = -INFINITY, tm1 = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < 16; nb++) {
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        float v = x[nb][e] * c2;
+        if (edge) {
+          const int key = kt * kTok + 8 * nb + 2 * t + (e & 1);
+          const int row = row0 + ((e >> 1) << 3);
+          if (key >= N || (kCausal && key > row)) v = -INFINITY;
+        }
+        x[nb][e] = v;
+      }
+      tm0 = fmaxf(tm0, fmaxf(x[nb][0], x[nb][1]));
+      tm1 = fmaxf(tm1, fmaxf(x[nb][2], x[nb][3]));
+    }
+    tm0 = fmaxf(tm0, __shfl_xor_sync(kFull, tm0, 1));
+    tm0 = fmaxf(tm0, __shfl_xor_sync(kFull, tm0, 2));
+    tm1 = fmaxf(tm1, __shfl_xor_sync(kFull, tm1, 1));
+    tm1 = fmaxf(tm1, __shfl_xor_sync(kFull, tm1, 2));
+    const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
+    const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);  // m = -inf on the first tile: 0
+    m0 = mn0;
+    m1 = mn1;
+    // P~ = exp2(x - m); rows past N take no part in the block maximum
+    float pmax = 0.0f, rs0 = 0.0f, rs1 = 0.0f;
+#pragma unroll
+    for (int nb = 0; nb < 16; nb++) {
+      x[nb][0] = valid0 ? ex2(x[nb][0] - mn0) : 0.0f;
+      x[nb][1] = valid0 ? ex2(x[nb][1] - mn0) : 0.0f;
+      x[nb][2] = valid1 ? ex2(x[nb][2] - mn1) : 0.0f;
+      x[nb][3] = valid1 ? ex2(x[nb][3] - mn1) : 0.0f;
+      rs0 += x[nb][0] + x[nb][1];
+      rs1 += x[nb][2] + x[nb][3];
+      pmax = fmaxf(pmax, fmaxf(fmaxf(x[nb][0], x[nb][1]), fmaxf(x[nb][2], x[nb][3])));
+    }
+    l0 = l0 * al0 + rs0;
+    l1 = l1 * al1 + rs1;
+    // block maximum over the 64-query group (named barrier per group)
+    pmax = warp_max(pmax);
+    if (lane == 0) redp[s * 8 + warp] = pmax;
+    named_bar(1 + grp, 128);
+    float amax = redp[s * 8 + 4 * grp];
+#pragma unroll
+    for (int w = 1; w < 4; w++) amax = fmaxf(amax, redp[s * 8 + 4 * grp + w]);
+    const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    const float spv = __fdiv_rn(amax, 127.0f) * sv_cur;
+    // P^ codes: the accumulator fragments of n-blocks 2kc, 2kc+1 are the A
+    // fragment of k-step kc
+    uint32_t pa[8][4];
+#pragma unroll
+    for (int kc = 0; kc < 8; kc++) {
+      pa[kc][0] = h2(code(x[2 * kc][0], inv), code(x[2 * kc][1], inv));
+      pa[kc][1] = h2(code(x[2 * kc][2], inv), code(x[2 * kc][3], inv));
+      pa[kc][2] = h2(code(x[2 * kc + 1][0], inv), code(x[2 * kc + 1][1], inv));
+      pa[kc][3] = h2(code(x[2 * kc + 1][2], inv), code(x[2 * kc + 1][3], inv));
+    }
+    // O = O * alpha + s_P s_V (P^ V^); V^ read transposed by ldmatrix.trans.
+    // Eight output n-blocks at a time, k outermost, so that eight
+    // independent MMA chains are in flight.
+#pragma unroll
+    for (int ng = 0; ng < D / 64; ng++) {
+      float acc[8][4];
+#pragma unroll
+      for (int i = 0; i < 8; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+#pragma unroll
+      for (int kc = 0; kc < 8; kc++) {
+#pragma unroll
+        for (int np = 0; np < 8; np += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vst + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 16 * (8 * ng + np + (j >> 1)), L::kRow), b0, b1,
+                    b2, b3);
+          mma_f16(acc[np], pa[kc], b0, b1);
+          mma_f16(acc[np + 1], pa[kc], b2, b3);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        float* oo = o[8 * ng + i];
+        oo[0] = fmaf(acc[i][0], spv, oo[0] * al0);
+        oo[1] = fmaf(acc[i][1], spv, oo[1] * al0);
+        oo[2] = fmaf(acc[i][2], spv, oo[2] * al1);
+        oo[3] = fmaf(acc[i][3], spv, oo[3] * al1);
+      }
+    }
+    sk_next = kt + 1 < nkt ? ws.sk[static_cast<size_t>(bh) * nqt + kt + 1] : 0.0f;
+    sv_next = kt + 1 < nkt ? ws.sv[static_cast<size_t>(bh) * nqt + kt + 1] : 0.0f;
+  }
+  if (!ok) {
+    // abandoning: let every copy this CTA issued land before exiting (the
+    // newest phase armed on each stage's barrier)
+    if (threadIdx.x == 0) {
+      drain_wait(qbar, 0, ctl);
+      for (int last = issued - 1; last >= 0 && last >= issued - 2; last--)
+        if (!(withhold && blockIdx.x == 0 && blockIdx.y == 0 && last == 0))
+          drain_wait(full0 + 8 * (last & 1), (last >> 1) & 1, ctl);
+    }
+    return;
+  }
+  // epilogue: O / l, lse = ln(l) + m ln 2
+  l0 += __shfl_xor_sync(kFull, l0, 1);
+  l0 += __shfl_xor_sync(kFull, l0, 2);
+  l1 += __shfl_xor_sync(kFull, l1, 1);
+  l1 += __shfl_xor_sync(kFull, l1, 2);
+  const float il0 = 1.0f / l0, il1 = 1.0f / l1;
+  uint16_t* orow0 = out + (static_cast<size_t>(bh) * N + row0) * D;
+  uint16_t* orow1 = orow0 + 8 * D;
+#pragma unroll
+  for (int nd = 0; nd < D / 8; nd++) {
+    const int d = 8 * nd + 2 * t;
+    if (valid0) *reinterpret_cast<__nv_bfloat162*>(orow0 + d) = __floats2bfloat162_rn(o[nd][0] * il0, o[nd][1] * il0);
+    if (valid1) *reinterpret_cast<__nv_bfloat162*>(orow1 + d) = __floats2bfloat162_rn(o[nd][2] * il1, o[nd][3] * il1);
+  }
+  if (t == 0) {
+    if (valid0) lse[static_cast<size_t>(bh) * N + row0] = (m0 + __log2f(l0)) * kLn2;
+    if (valid1) lse[static_cast<size_t>(bh) * N + row0 + 8] = (m1 + __log2f(l1)) * kLn2;
+  }
+}
+
+// ---------------------------------------------------------------- backward
+// One CTA of 8 warps per (128 keys, head); warp w owns keys 16w..16w+15.  The
+// CTA's K^ codes and FP16 V stay in shared memory; query tiles of 64 (Q^ and
+// dO^ codes, FP16 dO, L and D) stream through two stages.  Per query tile:
+// S^T, P^T, dV += P^^T dO^, dP^T (FP16), dS^T, dK += dS^^T Q^, and this key
+// tile's share of dQ = dS^ K^, added to an FP32 accumulator with vector
+// reductions.
+template <int D>
+struct BwdSmem {
+  static constexpr int kRow = 2 * D;
+  static constexpr int kKc = 0;
+  static constexpr int kVh = kKc + kTok * kRow;
+  static constexpr int kFixedBytes = 2 * kTok * kRow;
+  static constexpr int kQc = 0, kDoc = kQc + kQ * kRow, kDoh = kDoc + kQ * kRow;
+  static constexpr int kL = kDoh + kQ * kRow, kDd = kL + 4 * kQ;
+  static constexpr int kStage = kDd + 4 * kQ;
+  static constexpr int kStageOff = kFixedBytes;
+  static constexpr int kDs = kStageOff + 2 * kStage;   // staged dS^ codes, [128 keys][64 queries] FP16
+  static constexpr int kBarOff = kDs + kTok * kQ * 2;  // fixed, full[2]
+  static constexpr int kRedOff = kBarOff + 64;         // [2 kinds][8] floats
+  static constexpr int kBytes = kRedOff + 2 * 8 * 4;
+};
+
+// acc[D/8][4] += f * (A B): A the warp's 16-key x 64-query code fragments
+// (k = queries), B a 64-query x D tile of FP16 rows read transposed.  Eight
+// output n-blocks at a time with k outermost: eight independent MMA chains.
+template <int D>
+__device__ __forceinline__ void mma_fold(float (&acc)[D / 8][4], const uint32_t (&a)[4][4], uint32_t tile, float f,
+                                         int lane) {
+  const int j = lane >> 3;
+#pragma unroll
+  for (int ng = 0; ng < D / 64; ng++) {
+    float t[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; i++) t[i][0] = t[i][1] = t[i][2] = t[i][3] = 0.0f;
+#pragma unroll
+    for (int kc = 0; kc < 4; kc++) {
+#pragma unroll
+      for (int np = 0; np < 8; np += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(tile + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 16 * (8 * ng + np + (j >> 1)), 2 * D), b0, b1,
+                  b2, b3);
+        mma_f16(t[np], a[kc], b0, b1);
+        mma_f16(t[np + 1], a[kc], b2, b3);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+#pragma unroll
+      for (int e = 0; e < 4; e++) acc[8 * ng + i][e] = fmaf(t[i][e], f, acc[8 * ng + i][e]);
+  }
+}
+
+template <int D, bool kCausal>
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv_kernel(Ws ws, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int N, float scale, uint64_t wait_ns,
+                int withhold) {
+  using L = BwdSmem<D>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int nkt = (N + kTok - 1) / kTok;
+  const int Np = nkt * kTok;
+  const int nqt = Np / kQ;
+  const int kb = blockIdx.x, bh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3, j = lane >> 3;
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t fbar = sbase + L::kBarOff, full0 = fbar + 8;
+  float* redp = reinterpret_cast<float*>(smem + L::kRedOff);
+  const Ctl ctl{ws.status, wait_ns};
+  const size_t hb = static_cast<size_t>(bh) * Np * D;
+  const size_t hrow = static_cast<size_t>(bh) * Np;
+  // withhold (failure-detection test only): CTA 0 never issues its first
+  // query tile, so its wait for that tile runs out
+  const bool held = withhold && blockIdx.x == 0 && blockIdx.y == 0;
+  const int q0 = kCausal ? 2 * kb : 0;  // first query tile that sees these keys
+  const int niter = nqt - q0;
+
+  auto issue_stage = [&](int it) {
+    const int qtile = q0 + it, s = it & 1;
+    const uint32_t st = sbase + L::kStageOff + s * L::kStage, bar = full0 + 8 * s;
+    mbar_arrive_expect_tx(bar, L::kStage);
+    const size_t off = hb + static_cast<size_t>(qtile) * kQ * D;
+    bulk_load(st + L::kQc, ws.qc + off, kQ * L::kRow, bar);
+    bulk_load(st + L::kDoc, ws.doc + off, kQ * L::kRow, bar);
+    bulk_load(st + L::kDoh, ws.doh + off, kQ * L::kRow, bar);
+    bulk_load(st + L::kL, ws.l2 + hrow + static_cast<size_t>(qtile) * kQ, 4 * kQ, bar);
+    bulk_load(st + L::kDd, ws.dd + hrow + static_cast<size_t>(qtile) * kQ, 4 * kQ, bar);
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(fbar, 1);
+    mbar_init(full0, 1);
+    mbar_init(full0 + 8, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  int issued = 0;  // query tiles whose copies thread 0 has issued
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(fbar, L::kFixedBytes);
+    const size_t off = hb + static_cast<size_t>(kb) * kTok * D;
+    bulk_load(sbase + L::kKc, ws.kc + off, kTok * L::kRow, fbar);
+    bulk_load(sbase + L::kVh, ws.vh + off, kTok * L::kRow, fbar);
+    if (held) issued = 1;
+    for (; issued < 2 && issued < niter; issued++) issue_stage(issued);
+  }
+  // every wait's outcome is voted on by the whole CTA: here the fixed tiles
+  // and the first query tile; each later tile's vote rides on the barrier
+  // that ends the previous tile's dK
+  bool ok = __syncthreads_and(waitw(fbar, 0, ctl) && waitw(full0, 0, ctl));
+
+  const float sk = ws.sk[static_cast<size_t>(bh) * nkt + kb];
+  const int key0 = kb * kTok + 16 * warp + g;  // this thread's keys: key0, key0 + 8
+  const float c2base = sk * scale * kLog2e;
+  const int arow = 16 * warp + ((j & 1) << 3) + (lane & 7);  // A-fragment row (key) this lane addresses
+  const uint32_t dsb = sbase + L::kDs;
+  float dka[D / 8][4], dva[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; i++)
+#pragma unroll
+    for (int e = 0; e < 4; e++) dka[i][e] = dva[i][e] = 0.0f;
+
+  // the query tile's block scales, read one tile ahead
+  float sq_next = ws.sq[static_cast<size_t>(bh) * nkt + (q0 >> 1)];
+  float sdo_next = ws.sdo[static_cast<size_t>(bh) * nkt + (q0 >> 1)];
+  for (int it = 0; it < niter && ok; it++) {
+    const int qtile = q0 + it, s = it & 1;
+    const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+    const float sq = sq_next, sdo = sdo_next;
+    if (it + 1 < niter) {
+      sq_next = ws.sq[static_cast<size_t>(bh) * nkt + ((qtile + 1) >> 1)];
+      sdo_next = ws.sdo[static_cast<size_t>(bh) * nkt + ((qtile + 1) >> 1)];
+    }
+    // S^T = K^ Q^^T: 16 keys x 64 queries
+    float p[8][4];
+#pragma unroll
+    for (int nb = 0; nb < 8; nb++) p[nb][0] = p[nb][1] = p[nb][2] = p[nb][3] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ks++) {
+      uint32_t ka[4];
+      ldsm_x4(sbase + L::kKc + swz(arow, 32 * ks + ((j >> 1) << 4), L::kRow), ka[0], ka[1], ka[2], ka[3]);
+#pragma unroll
+      for (int nb = 0; nb < 8; nb += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(st + L::kQc + swz(8 * (nb + (j >> 1)) + (lane & 7), 32 * ks + ((j & 1) << 4), L::kRow), b0, b1, b2,
+                b3);
+        mma_f16(p[nb], ka, b0, b1);
+        mma_f16(p[nb + 1], ka, b2, b3);
+      }
+    }
+    // P^T = exp2(S^T c - L); masked and padded entries 0
+    const float c2 = c2base * sq;
+    const float* Ls = reinterpret_cast<const float*>(smem + (st - sbase) + L::kL);
+    const float* Ds = reinterpret_cast<const float*>(smem + (st - sbase) + L::kDd);
+    const bool edge = (kCausal && qtile <= 2 * kb + 1) || (qtile * kQ + kQ > N) || (kb * kTok + kTok > N);
+    float pmax = 0.0f;
+#pragma unroll
+    for (int nb = 0; nb < 8; nb++) {
+      const int qc = 8 * nb + 2 * t;  // query column within the tile
+      const float2 lq = *reinterpret_cast<const float2*>(Ls + qc);
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        float v = ex2(fmaf(p[nb][e], c2, (e & 1) ? lq.y : lq.x));  // lq holds -L
+        if (edge) {
+          const int query = qtile * kQ + qc + (e & 1);
+          const int key = key0 + ((e >> 1) << 3);
+          if (query >= N || key >= N || (kCausal && key > query)) v = 0.0f;
+        }
+        p[nb][e] = v;
+        pmax = fmaxf(pmax, v);
+      }
+    }
+    pmax = warp_max(pmax);
+    if (lane == 0) redp[warp] = pmax;
+    __syncthreads();
+    float amax = redp[0];
+#pragma unroll
+    for (int w = 1; w < 8; w++) amax = fmaxf(amax, redp[w]);
+    float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    // P^^T codes as A fragments (k = queries)
+    uint32_t pa[4][4];
+#pragma unroll
+    for (int kc = 0; kc < 4; kc++) {
+      pa[kc][0] = h2(code(p[2 * kc][0], inv), code(p[2 * kc][1], inv));
+      pa[kc][1] = h2(code(p[2 * kc][2], inv), code(p[2 * kc][3], inv));
+      pa[kc][2] = h2(code(p[2 * kc + 1][0], inv), code(p[2 * kc + 1][1], inv));
+      pa[kc][3] = h2(code(p[2 * kc + 1][2], inv), code(p[2 * kc + 1][3], inv));
+    }
+    // dV += s_P s_dO (P^^T dO^); dO^ read transposed
+    mma_fold<D>(dva, pa, st + L::kDoc, __fdiv_rn(amax, 127.0f) * sdo, lane);
+    // dP^T = V dO^T in FP16, then dS^T = P^T o (dP^T - D)
+    float dp[8][4];
+#pragma unroll
+    for (int nb = 0; nb < 8; nb++) dp[nb][0] = dp[nb][1] = dp[nb][2] = dp[nb][3] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ks++) {
+      uint32_t va[4];
+      ldsm_x4(sbase + L::kVh + swz(arow, 32 * ks + ((j >> 1) << 4), L::kRow), va[0], va[1], va[2], va[3]);
+#pragma unroll
+      for (int nb = 0; nb < 8; nb += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(st + L::kDoh + swz(8 * (nb + (j >> 1)) + (lane & 7), 32 * ks + ((j & 1) << 4), L::kRow), b0, b1,
+                b2, b3);
+        mma_f16(dp[nb], va, b0, b1);
+        mma_f16(dp[nb + 1], va, b2, b3);
+      }
+    }
+    float smax = 0.0f;
+#pragma unroll
+    for (int nb = 0; nb < 8; nb++) {
+      const float2 dq2 = *reinterpret_cast<const float2*>(Ds + 8 * nb + 2 * t);
+#pragma unroll
+      for (int e = 0; e < 4; e++) {
+        p[nb][e] = p[nb][e] * (dp[nb][e] - ((e & 1) ? dq2.y : dq2.x));
+        smax = fmaxf(smax, fabsf(p[nb][e]));
+      }
+    }
+    smax = warp_max(smax);
+    if (lane == 0) redp[8 + warp] = smax;
+    __syncthreads();
+    amax = redp[8];
+#pragma unroll
+    for (int w = 1; w < 8; w++) amax = fmaxf(amax, redp[8 + w]);
+    inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+    const float sds = __fdiv_rn(amax, 127.0f);
+    // dS^^T codes: A fragments for dK, and staged ([key][query]) for dQ
+    uint32_t da[4][4];
+#pragma unroll
+    for (int kc = 0; kc < 4; kc++) {
+      da[kc][0] = h2(code(p[2 * kc][0], inv), code(p[2 * kc][1], inv));
+      da[kc][1] = h2(code(p[2 * kc][2], inv), code(p[2 * kc][3], inv));
+      da[kc][2] = h2(code(p[2 * kc + 1][0], inv), code(p[2 * kc + 1][1], inv));
+      da[kc][3] = h2(code(p[2 * kc + 1][2], inv), code(p[2 * kc + 1][3], inv));
+      // rows key 16w+g and 16w+g+8; queries 16kc+2t (+1) and 16kc+8+2t (+1)
+      sts32(dsb + swz(16 * warp + g, 2 * (16 * kc + 2 * t), 2 * kQ), da[kc][0]);
+      sts32(dsb + swz(16 * warp + g + 8, 2 * (16 * kc + 2 * t), 2 * kQ), da[kc][1]);
+      sts32(dsb + swz(16 * warp + g, 2 * (16 * kc + 8 + 2 * t), 2 * kQ), da[kc][2]);
+      sts32(dsb + swz(16 * warp + g + 8, 2 * (16 * kc + 8 + 2 * t), 2 * kQ), da[kc][3]);
+    }
+    // dK += s_dS s_Q (dS^^T Q^); Q^ read transposed
+    mma_fold<D>(dka, da, st + L::kQc, sds * sq, lane);
+    // every warp's dS^ is staged and every warp is done with stage s; the
+    // same barrier votes on the next query tile's copy (issued a tile ago)
+    const bool next_ok = it + 1 >= niter || waitw(full0 + 8 * (s ^ 1), ((it + 1) >> 1) & 1, ctl);
+    ok = __syncthreads_and(next_ok);
+    if (threadIdx.x == 0 && ok && it + 2 < niter) issue_stage(issued++);
+    // dQ[64 x D] += scale s_dS s_K (dS^ K^): warp w takes query rows
+    // 16 (w & 3) and half of the D columns; dS^ and K^ read transposed
+    {
+      const float f = sds * sk * scale;
+      const int r0 = 16 * (warp & 3);
+      const int dh = (warp >> 2) * (D / 2);
+      float acc[D / 16][4];
+#pragma unroll
+      for (int i = 0; i < D / 16; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+#pragma unroll
+      for (int kc = 0; kc < kTok / 16; kc++) {
+        uint32_t a[4];
+        ldsm_x4_t(dsb + swz(16 * kc + ((j >> 1) << 3) + (lane & 7), 2 * (r0 + ((j & 1) << 3)), 2 * kQ), a[0], a[1],
+                  a[2], a[3]);
+#pragma unroll
+        for (int nd = 0; nd < D / 16; nd += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(sbase + L::kKc + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 2 * dh + 16 * (nd + (j >> 1)), L::kRow),
+                    b0, b1, b2, b3);
+          mma_f16(acc[nd], a, b0, b1);
+          mma_f16(acc[nd + 1], a, b2, b3);
+        }
+      }
+      float* dq0 = ws.dqacc + (hrow + static_cast<size_t>(qtile) * kQ + r0 + g) * D + dh + 2 * t;
+#pragma unroll
+      for (int nd = 0; nd < D / 16; nd++) {
+        red_add_v2(dq0 + 8 * nd, acc[nd][0] * f, acc[nd][1] * f);
+        red_add_v2(dq0 + 8 * D + 8 * nd, acc[nd][2] * f, acc[nd][3] * f);
+      }
+    }
+  }
+  if (!ok) {
+    if (threadIdx.x == 0) {
+      drain_wait(fbar, 0, ctl);
+      for (int last = issued - 1; last >= 0 && last >= issued - 2; last--)
+        if (!(held && last == 0)) drain_wait(full0 + 8 * (last & 1), (last >> 1) & 1, ctl);
+    }
+    return;
+  }
+  // dK = scale * sum, dV: bf16 rows (keys) below N
+  const int key1 = key0 + 8;
+#pragma unroll
+  for (int nd = 0; nd < D / 8; nd++) {
+    const int d = 8 * nd + 2 * t;
+    if (key0 < N) {
+      const size_t ix = (static_cast<size_t>(bh) * N + key0) * D + d;
+      *reinterpret_cast<__nv_bfloat162*>(dk + ix) = __floats2bfloat162_rn(dka[nd][0] * scale, dka[nd][1] * scale);
+      *reinterpret_cast<__nv_bfloat162*>(dv + ix) = __floats2bfloat162_rn(dva[nd][0], dva[nd][1]);
+    }
+    if (key1 < N) {
+      const size_t ix = (static_cast<size_t>(bh) * N + key1) * D + d;
+      *reinterpret_cast<__nv_bfloat162*>(dk + ix) = __floats2bfloat162_rn(dka[nd][2] * scale, dka[nd][3] * scale);
+      *reinterpret_cast<__nv_bfloat162*>(dv + ix) = __floats2bfloat162_rn(dva[nd][2], dva[nd][3]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- tcgen05
+// Instruction descriptor of tcgen05.mma kind::f16: FP16 A and B (formats 0),
+// FP32 accumulator (bits 4-5 = 1), both operands K-major, N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D[tmem] (+)= A x B^T, FP16 operands in shared memory (descriptors), K = 16.
+__device__ __forceinline__ void mma_f16_tc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Descriptor of a K-major FP16 operand whose rows are 128 bytes (64 values)
+// with the 128-byte swizzle (16-byte chunk ^ row & 7), rows of 8 at 1024-byte
+// strides, starting k0 values into the row (k0 a multiple of 16); the tile
+// must start on a 1024-byte boundary.
+__device__ __forceinline__ uint64_t desc_k64(uint32_t tile, int k0) {
+  return smem_desc(tile + 2 * k0, 16, 1024, kSwizzle128B);
+}
+
+// The same products with MN-major operands (idesc bits 15 and 16: A and B
+// transposed), as dQ = dS^ K^ reads them: each operand is stored with its K
+// index as the 128-byte row (64 FP16 values of M or N per row, 16-byte chunks
+// XOR-permuted by row & 7).  The descriptor's leading offset is the distance
+// between 64-wide blocks of M (or N), its stride offset the distance between
+// groups of 8 K rows (1024 bytes here); a K step of 16 starts 16 rows later.
+__host__ __device__ constexpr uint32_t idesc_f16_mn(uint32_t M, uint32_t N) {
+  return idesc_f16(M, N) | (1u << 15) | (1u << 16);
+}
+__device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int k0, uint32_t block_stride) {
+  return smem_desc(tile + 128 * k0, block_stride, 1024, kSwizzle128B);
+}
+
+// ---------------------------------------------------------------- backward, tcgen05 (D = 64)
+// The same backward with all five products on the 5th-generation tensor
+// cores, issued asynchronously into tensor memory by one thread while other
+// warps work: per 64-query tile the four with 128 keys as rows -- S^T = K^ Q^^T,
+// dP^T = V dO^T, dV = P^^T dO^ and dK = dS^^T Q^ (M = 128 keys, N = 64, K = 16
+// per instruction) -- and per pair of query tiles dQ = dS^ K^ (M = 128
+// queries, N = 64, K = 128 keys) with both operands read MN-major from the
+// codes buffers and the resident K^ tile.  The warpgroups of the CTA:
+//   0  warp 0: bulk copies; warp 1: tensor-memory allocation and MMA issue
+//   1, 2  softmax: each thread owns one key row and half of the tile's 64
+//      query columns; P^T and dS^T from the S^T and dP^T rows in tensor
+//      memory, their block maxima (one vote of the eight warps each), their
+//      INT8 codes written to shared memory as the A operands of dV and dK
+//      (and dS^T read again by dQ)
+//   3  folds each tile's dV and dK partials (tensor memory) into registers
+//      with the tile's block scales, and adds each tile pair's dQ, times its
+//      tiles' scales, to the FP32 accumulator in global memory by tensor
+//      reductions of the copy engine (staged 32 rows x 32 columns a warp)
+// Tensor memory: S^T and dP^T double-buffered, the dV and dK partials and dQ
+// single (448 of 512 columns).  Every wait is bounded; a wait that runs out
+// sets the status word and an abort flag that ends every role's loop.
+constexpr int kTcThreads = 512;
+constexpr int kTcStages = 3;
+struct TcRegs {
+  static constexpr uint32_t kCtl = 64, kSoft = 128, kFold = 192;
+};
+static_assert(TcRegs::kCtl * 128 + TcRegs::kSoft * 256 + TcRegs::kFold * 128 <= 65536, "register split");
+
+struct TcSmem {
+  static constexpr int kTile = 128 * 128;  // 128 rows of 128 bytes
+  static constexpr int kK = 0;             // K^ codes [128 keys][64]
+  static constexpr int kV = kTile;         // FP16 V [128 keys][64]
+  static constexpr int kStageOff = 2 * kTile;
+  // stage: Q^ [64 q][64], FP16 dO [64 q][64], Q^T [64 d][64 q], dO^T [64 d][64 q], L, D
+  static constexpr int kSQ = 0, kSDoh = 8192, kSQt = 16384, kSDot = 24576, kSL = 32768, kSD = 33024;
+  static constexpr int kStage = 33792;  // a multiple of 1024
+  static constexpr int kCodesOff = kStageOff + kTcStages * kStage;
+  // codes buffer: P^T [128 keys][64 q], dS^T [128 keys][64 q]
+  static constexpr int kCP = 0, kCS = kTile, kCodes = 2 * kTile;
+  // dQ staging: per fold warp a [32 rows][32 FP32] tile, 128-byte swizzled
+  static constexpr int kDqOff = kCodesOff + 2 * kCodes;
+  static constexpr int kBarOff = kDqOff + 128 * 128;
+  static constexpr int kNumBars = 32;
+  static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // tmem slot, abort flag, red[2][2][8], scal[4][4]
+  static constexpr int kBytes = kMiscOff + 256;
+  static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
+};
+// mbarrier indices
+enum {
+  TB_FIXED = 0,
+  TB_FULL = 1,             // + stage
+  TB_EMPTY = 1 + kTcStages,  // + stage
+  TB_SDONE = 1 + 2 * kTcStages,  // + buffer (2)
+  TB_SFREE = TB_SDONE + 2,
+  TB_CFULL = TB_SFREE + 2,
+  TB_CEMPTY = TB_CFULL + 2,
+  TB_PDONE = TB_CEMPTY + 2,  // dV and dK partials (single buffer)
+  TB_PFREE = TB_PDONE + 1,
+  TB_QDONE = TB_PFREE + 1,   // dQ of a tile pair (single buffer)
+  TB_QFREE = TB_QDONE + 1,
+  TB_DRAIN = TB_QFREE + 1,
+  TB_COUNT
+};
+static_assert(TB_COUNT <= TcSmem::kNumBars, "barriers");
+// tensor-memory columns
+constexpr uint32_t kTcS = 0, kTcDp = 128, kTcDv = 256, kTcDk = 320, kTcDq = 384;
+
+// Bounded warp-wide wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool waitw_ab(uint32_t bar, uint32_t parity, const Ctl& c, volatile int* abort) {
+  if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+    int stop = 0;
+    if ((threadIdx.x & 31) == 0) {
+      if (*abort) {
+        stop = 1;
+      } else if (globaltimer_ns() - t0 > c.limit) {
+        *abort = 1;
+        atomicCAS(c.status, 0, SAGE_FP4_ETIMEOUT);
+        stop = 1;
+      }
+    }
+    if (__shfl_sync(kFull, stop, 0)) return false;
+  }
+}
+
+// The same for a single thread.
+__device__ __forceinline__ bool wait1_ab(uint32_t bar, uint32_t parity, const Ctl& c, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > c.limit) {
+      *abort = 1;
+      atomicCAS(c.status, 0, SAGE_FP4_ETIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive1(uint32_t bar) { sagefp4::mbar_arrive(bar); }
+
+// All 256 threads of the two softmax warpgroups: AND of `ok` over them
+// (named barrier 1).
+__device__ __forceinline__ bool group_and(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.and.pred q, 1, 256, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(ok))
+      : "memory");
+  return r != 0;
+}
+
+// Each thread of the warp reads 16 consecutive FP32 columns of its lane.
+__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  sagefp4::tmem_ld16(taddr, r);
+  tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+
+template <bool kCausal>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_dq, Ws ws, uint16_t* __restrict__ dk,
+                   uint16_t* __restrict__ dv, int N, float scale, uint64_t wait_ns, int withhold) {
+  constexpr int D = 64;
+  using L = TcSmem;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte aligned base, by pointer arithmetic on the shared array (so
+  // that the compiler keeps its accesses in the shared state space)
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_addr(smem);
+  const int nkt = (N + kTok - 1) / kTok;
+  const int Np = nkt * kTok;
+  const int nqt = Np / kQ;
+  const int kb = blockIdx.x, bh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wg = warp >> 2;
+  const size_t hb = static_cast<size_t>(bh) * Np * D;
+  const size_t hrow = static_cast<size_t>(bh) * Np;
+  const int q0 = kCausal ? 2 * kb : 0;
+  const int niter = nqt - q0;
+  const Ctl ctl{ws.status, wait_ns};
+  auto bar = [&](int i) { return sbase + L::kBarOff + 8 * i; };
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  float* red = reinterpret_cast<float*>(smem + L::kMiscOff + 16);    // [2 parity][2 kinds][8 warps]
+  float* scal = reinterpret_cast<float*>(smem + L::kMiscOff + 160);  // [tile mod 4][4]
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(TB_FIXED), 1);
+    for (int s = 0; s < kTcStages; s++) {
+      mbar_init(bar(TB_FULL + s), 1);
+      mbar_init(bar(TB_EMPTY + s), 1 + 8);  // the MMA commit + the softmax warps
+    }
+    for (int b = 0; b < 2; b++) {
+      mbar_init(bar(TB_SDONE + b), 1);
+      mbar_init(bar(TB_SFREE + b), 8);
+      mbar_init(bar(TB_CFULL + b), 8);
+      mbar_init(bar(TB_CEMPTY + b), 1);  // the MMA commit after the pair's dQ
+    }
+    mbar_init(bar(TB_PDONE), 1);
+    mbar_init(bar(TB_PFREE), 4);
+    mbar_init(bar(TB_QDONE), 1);
+    mbar_init(bar(TB_QFREE), 4);
+    mbar_init(bar(TB_DRAIN), 1);
+    *abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tslot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  if (wg == 0) {
+    sagefp4::regs_dec<TcRegs::kCtl>();
+    if (warp == 0 && lane == 0) {
+      // ---- producer
+      const size_t off = hb + static_cast<size_t>(kb) * kTok * D;
+      mbar_arrive_expect_tx(bar(TB_FIXED), 2 * L::kTile);
+      bulk_load(sbase + L::kK, ws.kc + off, L::kTile, bar(TB_FIXED));
+      bulk_load(sbase + L::kV, ws.vh + off, L::kTile, bar(TB_FIXED));
+      const bool held = withhold && blockIdx.x == 0 && blockIdx.y == 0;
+      int issued = 0;
+      for (int it = 0; it < niter; it++) {
+        const int s = it % kTcStages;
+        if (it >= kTcStages && !wait1_ab(bar(TB_EMPTY + s), ((it / kTcStages) - 1) & 1, ctl, abort)) break;
+        if (held && it == 0) continue;  // failure-detection test: this tile never arrives
+        const int qtile = q0 + it;
+        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+        const size_t qo = hb + static_cast<size_t>(qtile) * kQ * D;
+        mbar_arrive_expect_tx(bar(TB_FULL + s), 4 * 8192 + 512);
+        bulk_load(st + L::kSQ, ws.qc + qo, 8192, bar(TB_FULL + s));
+        bulk_load(st + L::kSDoh, ws.doh + qo, 8192, bar(TB_FULL + s));
+        bulk_load(st + L::kSQt, ws.qct + qo, 8192, bar(TB_FULL + s));
+        bulk_load(st + L::kSDot, ws.doct + qo, 8192, bar(TB_FULL + s));
+        bulk_load(st + L::kSL, ws.l2 + hrow + static_cast<size_t>(qtile) * kQ, 256, bar(TB_FULL + s));
+        bulk_load(st + L::kSD, ws.dd + hrow + static_cast<size_t>(qtile) * kQ, 256, bar(TB_FULL + s));
+        issued = it + 1;
+      }
+      if (*abort) {
+        // let every copy this thread issued land before the CTA exits
+        for (int last = issued - 1; last >= 0 && last >= issued - kTcStages; last--)
+          if (!(held && last == 0)) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar(TB_FULL + last % kTcStages), (last / kTcStages) & 1) &&
+                   globaltimer_ns() - t0 < ctl.limit) {
+            }
+          }
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar(TB_FIXED), 0) && globaltimer_ns() - t0 < ctl.limit) {
+        }
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---- MMA issue
+      const uint32_t id = idesc_f16(128, 64), idq = idesc_f16_mn(128, 64);
+      const uint64_t dk0 = desc_k64(sbase + L::kK, 0), dv0 = desc_k64(sbase + L::kV, 0);
+      // dQ = dS^ K^, MN-major: a K step of 16 rows moves 2048 bytes (+128)
+      const uint64_t dqa = desc_mn(sbase + L::kCodesOff + L::kCS, 0, L::kCodes), dqb = desc_mn(sbase + L::kK, 0, L::kCodes);
+      bool ok = wait1_ab(bar(TB_FIXED), 0, ctl, abort);
+      auto issue_sdp = [&](int it) {
+        const int s = it % kTcStages, b = it & 1;
+        if (!wait1_ab(bar(TB_FULL + s), (it / kTcStages) & 1, ctl, abort)) return false;
+        if (it >= 2 && !wait1_ab(bar(TB_SFREE + b), ((it >> 1) - 1) & 1, ctl, abort)) return false;
+        tc_fence_after();
+        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+        // descriptors built once per operand; a K step of 16 moves 32 bytes (+2)
+        const uint64_t dq = desc_k64(st + L::kSQ, 0), ddo = desc_k64(st + L::kSDoh, 0);
+#pragma unroll
+        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcS + 64 * b, dk0 + 2 * k, dq + 2 * k, id, k > 0);
+#pragma unroll
+        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcDp + 64 * b, dv0 + 2 * k, ddo + 2 * k, id, k > 0);
+        tc_commit(bar(TB_SDONE + b));
+        return true;
+      };
+      if (ok) ok = issue_sdp(0);
+      for (int it = 0; ok && it < niter; it++) {
+        const int s = it % kTcStages, b = it & 1;
+        if (it + 1 < niter && !(ok = issue_sdp(it + 1))) break;
+        if (!(ok = wait1_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort))) break;
+        // the partials' buffer: the fold has read the previous tile's
+        if (it >= 1 && !(ok = wait1_ab(bar(TB_PFREE), (it - 1) & 1, ctl, abort))) break;
+        tc_fence_after();
+        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+        const uint32_t cb = sbase + L::kCodesOff + b * L::kCodes;
+        const uint64_t dp = desc_k64(cb + L::kCP, 0), dds = desc_k64(cb + L::kCS, 0);
+        const uint64_t ddot = desc_k64(st + L::kSDot, 0), dqt = desc_k64(st + L::kSQt, 0);
+#pragma unroll
+        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcDv, dp + 2 * k, ddot + 2 * k, id, k > 0);
+#pragma unroll
+        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcDk, dds + 2 * k, dqt + 2 * k, id, k > 0);
+        tc_commit(bar(TB_PDONE));
+        tc_commit(bar(TB_EMPTY + s));
+        if (b == 1) {
+          // dQ of the pair (it - 1, it): rows 0..63 from codes buffer 0, rows
+          // 64..127 from buffer 1; the fold has read the previous pair's dQ
+          const int pr = it >> 1;
+          if (pr >= 1 && !(ok = wait1_ab(bar(TB_QFREE), (pr - 1) & 1, ctl, abort))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 8; k++) mma_f16_tc(tmem + kTcDq, dqa + 128 * k, dqb + 128 * k, idq, k > 0);
+          tc_commit(bar(TB_QDONE));
+          tc_commit(bar(TB_CEMPTY + 0));
+          tc_commit(bar(TB_CEMPTY + 1));
+        }
+      }
+      // every MMA issued has completed before tensor memory is released
+      tc_commit(bar(TB_DRAIN));
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar(TB_DRAIN), 0) && globaltimer_ns() - t0 < ctl.limit) {
+      }
+    }
+  } else if (wg == 1 || wg == 2) {
+    // ---- softmax: this thread's key row, query columns 32h..32h+31
+    sagefp4::regs_inc<TcRegs::kSoft>();
+    const int h = wg - 1;
+    const int row = 32 * (warp & 3) + lane;     // 0..127
+    const int sw = 4 * h + (warp & 3);          // softmax warp 0..7
+    const uint32_t lanebase = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int key = kb * kTok + row;
+    const float sk = ws.sk[static_cast<size_t>(bh) * nkt + kb];
+    const float c2base = sk * scale * kLog2e;
+    // the query tile's block scales, read one tile ahead
+    float sq_next = ws.sq[static_cast<size_t>(bh) * nkt + (q0 >> 1)];
+    float sdo_next = ws.sdo[static_cast<size_t>(bh) * nkt + (q0 >> 1)];
+    for (int it = 0; it < niter; it++) {
+      const int s = it % kTcStages, b = it & 1, qtile = q0 + it;
+      const float sq = sq_next, sdo = sdo_next;
+      if (it + 1 < niter) {
+        sq_next = ws.sq[static_cast<size_t>(bh) * nkt + ((qtile + 1) >> 1)];
+        sdo_next = ws.sdo[static_cast<size_t>(bh) * nkt + ((qtile + 1) >> 1)];
+      }
+      // a failed wait is voted on below, before anything is published
+      bool ok = waitw_ab(bar(TB_SDONE + b), (it >> 1) & 1, ctl, abort) &&
+                waitw_ab(bar(TB_FULL + s), (it / kTcStages) & 1, ctl, abort);
+      tc_fence_after();
+      // this half of the S^T and dP^T rows: two loads in flight, one wait
+      uint32_t ru[2][32];
+      tmem_ld32(tmem + lanebase + kTcS + 64 * b + 32 * h, ru[0]);
+      tmem_ld32(tmem + lanebase + kTcDp + 64 * b + 32 * h, ru[1]);
+      tmem_wait_ld();
+      float p[32], dp[32];
+#pragma unroll
+      for (int i = 0; i < 32; i++) {
+        p[i] = __uint_as_float(ru[0][i]);
+        dp[i] = __uint_as_float(ru[1][i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(TB_SFREE + b));
+      // P^T = exp2(S^T c - L); masked and padded entries 0; dS^T = P^T o (dP^T - D)
+      const float* Ls = reinterpret_cast<const float*>(smem + L::kStageOff + s * L::kStage + L::kSL) + 32 * h;
+      const float* Ds = reinterpret_cast<const float*>(smem + L::kStageOff + s * L::kStage + L::kSD) + 32 * h;
+      const float c2 = c2base * sq;
+      const bool edge = (kCausal && qtile <= 2 * kb + 1) || (qtile * kQ + kQ > N) || (kb * kTok + kTok > N);
+      // (pairs of columns through the packed FP32 forms, each lane rounded
+      // like its scalar form; Ls holds -L)
+      float pmax = 0.0f, smax = 0.0f, smin = 0.0f;
+      const uint64_t cc = pack2(c2, c2);
+#pragma unroll
+      for (int q4 = 0; q4 < 8; q4++) {
+        const float4 l4 = reinterpret_cast<const float4*>(Ls)[q4];
+        const float4 d4 = reinterpret_cast<const float4*>(Ds)[q4];
+        const uint64_t l01 = pack2(l4.x, l4.y), l23 = pack2(l4.z, l4.w);
+        const int q = 4 * q4;
+        const uint64_t x01 = fma2(pack2(p[q], p[q + 1]), cc, l01), x23 = fma2(pack2(p[q + 2], p[q + 3]), cc, l23);
+        float v[4] = {ex2(lo2(x01)), ex2(hi2(x01)), ex2(lo2(x23)), ex2(hi2(x23))};
+        if (edge) {
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            const int query = qtile * kQ + 32 * h + q + e;
+            if (query >= N || key >= N || (kCausal && key > query)) v[e] = 0.0f;
+          }
+        }
+        const uint64_t s01 = mul2(pack2(v[0], v[1]), add2(pack2(dp[q], dp[q + 1]), pack2(-d4.x, -d4.y)));
+        const uint64_t s23 = mul2(pack2(v[2], v[3]), add2(pack2(dp[q + 2], dp[q + 3]), pack2(-d4.z, -d4.w)));
+        p[q] = v[0];
+        p[q + 1] = v[1];
+        p[q + 2] = v[2];
+        p[q + 3] = v[3];
+        dp[q] = lo2(s01);
+        dp[q + 1] = hi2(s01);
+        dp[q + 2] = lo2(s23);
+        dp[q + 3] = hi2(s23);
+        pmax = max3f(pmax, max3f(v[0], v[1], v[2]), v[3]);
+        smax = max3f(smax, max3f(dp[q], dp[q + 1], dp[q + 2]), dp[q + 3]);
+        smin = fminf(fminf(smin, fminf(dp[q], dp[q + 1])), fminf(dp[q + 2], dp[q + 3]));
+      }
+      smax = fmaxf(smax, -smin);
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(TB_EMPTY + s));  // L and D read
+      pmax = warp_max(pmax);
+      smax = warp_max(smax);
+      if (lane == 0) {
+        red[(b * 2 + 0) * 8 + sw] = pmax;
+        red[(b * 2 + 1) * 8 + sw] = smax;
+      }
+      // the codes buffer is free once dV, dK (tile it - 2) and the pair's dQ have read it
+      ok = ok && (it < 2 || waitw_ab(bar(TB_CEMPTY + b), ((it >> 1) - 1) & 1, ctl, abort));
+      if (!group_and(ok)) break;  // also publishes red[]
+      float pa = red[(b * 2) * 8], sa = red[(b * 2 + 1) * 8];
+#pragma unroll
+      for (int w = 1; w < 8; w++) {
+        pa = fmaxf(pa, red[(b * 2) * 8 + w]);
+        sa = fmaxf(sa, red[(b * 2 + 1) * 8 + w]);
+      }
+      const float pinv = pa > 0.0f ? __fdiv_rn(127.0f, pa) : 0.0f;
+      const float sinv = sa > 0.0f ? __fdiv_rn(127.0f, sa) : 0.0f;
+      uint8_t* cbuf = smem + L::kCodesOff + b * L::kCodes;
+      const uint64_t pp = pack2(pinv, pinv), ss = pack2(sinv, sinv);
+      // rint(x * inv) for a pair, as FP16x2: the products rounded per lane to
+      // FP32, then to integers by adding and subtracting 1.5 * 2^23 (exact)
+      const uint64_t magic2 = pack2(kRintMagic, kRintMagic), nmagic2 = pack2(-kRintMagic, -kRintMagic);
+      auto code2 = [&](float a, float b, uint64_t inv2) {
+        const uint64_t y = add2(add2(mul2(pack2(a, b), inv2), magic2), nmagic2);
+        return h2(lo2(y), hi2(y));
+      };
+#pragma unroll
+      for (int ch = 0; ch < 4; ch++) {
+        uint4 wp, wsd;
+        wp.x = code2(p[8 * ch + 0], p[8 * ch + 1], pp);
+        wp.y = code2(p[8 * ch + 2], p[8 * ch + 3], pp);
+        wp.z = code2(p[8 * ch + 4], p[8 * ch + 5], pp);
+        wp.w = code2(p[8 * ch + 6], p[8 * ch + 7], pp);
+        wsd.x = code2(dp[8 * ch + 0], dp[8 * ch + 1], ss);
+        wsd.y = code2(dp[8 * ch + 2], dp[8 * ch + 3], ss);
+        wsd.z = code2(dp[8 * ch + 4], dp[8 * ch + 5], ss);
+        wsd.w = code2(dp[8 * ch + 6], dp[8 * ch + 7], ss);
+        *reinterpret_cast<uint4*>(cbuf + L::kCP + swz(row, 64 * h + 16 * ch, 128)) = wp;
+        *reinterpret_cast<uint4*>(cbuf + L::kCS + swz(row, 64 * h + 16 * ch, 128)) = wsd;
+      }
+      if (threadIdx.x == 128) {
+        const float sp = __fdiv_rn(pa, 127.0f), sds = __fdiv_rn(sa, 127.0f);
+        float* sc = scal + 4 * (it & 3);
+        sc[0] = sp * sdo;          // dV
+        sc[1] = sds * sq;          // dK (the softmax scale comes at the end)
+        sc[2] = sds * sk * scale;  // dQ
+      }
+      // the codes (generic-proxy writes) -> visible to the tensor core
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(TB_CFULL + b));
+    }
+  } else {
+    // ---- dV and dK folds, and dQ read out (warpgroup 3)
+    sagefp4::regs_inc<TcRegs::kFold>();
+    const int row = 32 * (warp & 3) + lane;  // key row of the folds; query row of a tile pair's dQ
+    const uint32_t lanebase = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    uint64_t accv[32], acck[32];  // FP32 pairs
+#pragma unroll
+    for (int i = 0; i < 32; i++) accv[i] = acck[i] = 0;
+    float fq[2] = {0.0f, 0.0f};  // dQ scales of the pair's two tiles
+    for (int it = 0; it < niter; it++) {
+      const int b = it & 1;
+      // CFULL: this tile's block scales are written
+      if (!waitw_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort)) break;
+      const float* sc = scal + 4 * (it & 3);
+      const uint64_t fv = pack2(sc[0], sc[0]), fk = pack2(sc[1], sc[1]);
+      fq[b] = sc[2];
+      if (!waitw_ab(bar(TB_PDONE), it & 1, ctl, abort)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int qc = 0; qc < 4; qc++) {
+        uint32_t rv[16], rk[16];
+        sagefp4::tmem_ld16(tmem + lanebase + kTcDv + 16 * qc, rv);
+        sagefp4::tmem_ld16(tmem + lanebase + kTcDk + 16 * qc, rk);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+          accv[8 * qc + i] = fma2(pack2(__uint_as_float(rv[2 * i]), __uint_as_float(rv[2 * i + 1])), fv, accv[8 * qc + i]);
+          acck[8 * qc + i] = fma2(pack2(__uint_as_float(rk[2 * i]), __uint_as_float(rk[2 * i + 1])), fk, acck[8 * qc + i]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(TB_PFREE));
+      if (b == 1) {
+        // dQ rows of query tiles it - 1 (rows 0..63) and it (64..127)
+        if (!waitw_ab(bar(TB_QDONE), (it >> 1) & 1, ctl, abort)) break;
+        tc_fence_after();
+        const float f = row < kQ ? fq[0] : fq[1];
+        const uint64_t f2 = pack2(f, f);
+        // this warp's rows of the pair in the accumulator viewed as [B*H*Np][64]
+        const int y0 = static_cast<int>(hrow) + (q0 + it - 1) * kQ + 32 * (warp & 3);
+        uint8_t* wt = smem + L::kDqOff + 4096 * (warp & 3);
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lanebase + kTcDq + 32 * hh, r);
+          if (lane == 0) bulk_wait_read();  // the staging tile's previous reduction has read it
+          __syncwarp();
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 8; c++) {
+            const uint64_t x01 = mul2(pack2(__uint_as_float(r[4 * c]), __uint_as_float(r[4 * c + 1])), f2);
+            const uint64_t x23 = mul2(pack2(__uint_as_float(r[4 * c + 2]), __uint_as_float(r[4 * c + 3])), f2);
+            *reinterpret_cast<uint4*>(wt + swz(lane, 16 * c, 128)) =
+                make_uint4(static_cast<uint32_t>(x01), static_cast<uint32_t>(x01 >> 32), static_cast<uint32_t>(x23),
+                           static_cast<uint32_t>(x23 >> 32));
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_2d(&tm_dq, smem_addr(wt), 32 * hh, y0);
+            bulk_commit();
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive1(bar(TB_QFREE));
+      }
+    }
+    if (lane == 0) bulk_wait_all();  // the dQ reductions have read shared memory and completed
+    __syncwarp();
+    if (!*abort) {
+      const int key = kb * kTok + row;
+      if (key < N) {
+#pragma unroll
+        for (int which = 0; which < 2; which++) {
+          uint16_t* dst = (which == 0 ? dv : dk) + (static_cast<size_t>(bh) * N + key) * D;
+          const float f = which == 0 ? 1.0f : scale;
+          const uint64_t* acc = which == 0 ? accv : acck;
+#pragma unroll
+          for (int c = 0; c < 8; c++) {
+            uint4 w;
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(lo2(acc[4 * c + 0]) * f, hi2(acc[4 * c + 0]) * f);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(lo2(acc[4 * c + 1]) * f, hi2(acc[4 * c + 1]) * f);
+            __nv_bfloat162 h2v = __floats2bfloat162_rn(lo2(acc[4 * c + 2]) * f, hi2(acc[4 * c + 2]) * f);
+            __nv_bfloat162 h3 = __floats2bfloat162_rn(lo2(acc[4 * c + 3]) * f, hi2(acc[4 * c + 3]) * f);
+            w.x = *reinterpret_cast<uint32_t*>(&h0);
+            w.y = *reinterpret_cast<uint32_t*>(&h1);
+            w.z = *reinterpret_cast<uint32_t*>(&h2v);
+            w.w = *reinterpret_cast<uint32_t*>(&h3);
+            *reinterpret_cast<uint4*>(dst + 8 * c) = w;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------- forward, tcgen05 (D = 64)
+// The forward with S = Q^ K^^T and O_t = P~^ V^ on the 5th-generation tensor
+// cores (M = 128 query rows; S: N = 128 keys; PV: N = 64), issued by one
+// thread into double-buffered tensor memory.  The warpgroups:
+//   0  warp 0: bulk copies; warp 1: tensor-memory allocation and MMA issue
+//   1, 2  softmax: each thread owns one query row and 64 of the tile's 128
+//      keys; the row maximum and the 64-row block maxima are exchanged
+//      through shared memory; P~'s INT8 codes go to shared memory as the A
+//      operand of PV (each warpgroup writes one 64-key slab)
+//   3  correction: O in registers, rescaled by each row's factor and
+//      accumulated with each tile's PV times its block scales; the epilogue
+// P~ blocks are 64 query rows x 128 keys, as in the warp-level forward.
+struct TfSmem {
+  static constexpr int kQ = 0;                    // Q^ [128][64]: 16 KB
+  static constexpr int kStageOff = 16384;
+  static constexpr int kSK = 0, kSV = 16384;      // K^ [128][64]; V^T [2][64 d][64 keys]
+  static constexpr int kStage = 32768;
+  static constexpr int kPOff = kStageOff + kTcStages * kStage;  // P^ [2 bufs][2 key slabs][128][64]
+  static constexpr int kP = 32768;
+  static constexpr int kBarOff = kPOff + 2 * kP;
+  static constexpr int kMiscOff = kBarOff + 8 * 32;
+  // misc: tmem slot, abort, row max halves [2 parity][2][128], alpha [2][128],
+  // block max [2 parity][8 warps], beta [2][2], final l halves [2][128], m [128]
+  static constexpr int kXm = kMiscOff + 16, kAl = kXm + 2048, kBm = kAl + 1024, kBeta = kBm + 64,
+                       kLf = kBeta + 16, kMf = kLf + 1024;
+  static constexpr int kBytes = kMf + 512;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+enum {
+  FB_Q = 0,
+  FB_FULL = 1,
+  FB_EMPTY = 1 + kTcStages,
+  FB_SDONE = 1 + 2 * kTcStages,  // + buffer
+  FB_SFREE = FB_SDONE + 2,
+  FB_PFULL = FB_SFREE + 2,
+  FB_PEMPTY = FB_PFULL + 2,
+  FB_PVDONE = FB_PEMPTY + 2,
+  FB_PVFREE = FB_PVDONE + 2,
+  FB_DRAIN = FB_PVFREE + 2,
+  FB_COUNT
+};
+static_assert(FB_COUNT <= 32, "barriers");
+constexpr uint32_t kTfS = 0, kTfPv = 256;
+
+template <bool kCausal>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    fwd_tc_kernel(Ws ws, uint16_t* __restrict__ out, float* __restrict__ lse, int N, float scale_log2e, uint64_t wait_ns,
+                  int withhold) {
+  constexpr int D = 64;
+  using L = TfSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_addr(smem);
+  const int nqt = (N + kTok - 1) / kTok;
+  const int Np = nqt * kTok;
+  const int qt = kCausal ? (nqt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int bh = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wg = warp >> 2;
+  const int nkt = kCausal ? qt + 1 : nqt;
+  const size_t hb = static_cast<size_t>(bh) * Np * D;
+  const Ctl ctl{ws.status, wait_ns};
+  auto bar = [&](int i) { return sbase + L::kBarOff + 8 * i; };
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  float* xm = reinterpret_cast<float*>(smem + L::kXm);     // [2 halves][128 rows]
+  float* al = reinterpret_cast<float*>(smem + L::kAl);     // [2 buffers][128 rows]
+  float* bm = reinterpret_cast<float*>(smem + L::kBm);     // [2 parity][8 softmax warps]
+  float* beta = reinterpret_cast<float*>(smem + L::kBeta); // [2 buffers][2 row blocks]
+  float* lf = reinterpret_cast<float*>(smem + L::kLf);     // [2 halves][128 rows]
+  float* mf = reinterpret_cast<float*>(smem + L::kMf);     // [128 rows]
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(FB_Q), 1);
+    for (int s = 0; s < kTcStages; s++) {
+      mbar_init(bar(FB_FULL + s), 1);
+      mbar_init(bar(FB_EMPTY + s), 1);  // the MMA commit after PV
+    }
+    for (int b = 0; b < 2; b++) {
+      mbar_init(bar(FB_SDONE + b), 1);
+      mbar_init(bar(FB_SFREE + b), 8);
+      mbar_init(bar(FB_PFULL + b), 8);
+      mbar_init(bar(FB_PEMPTY + b), 1);
+      mbar_init(bar(FB_PVDONE + b), 1);
+      mbar_init(bar(FB_PVFREE + b), 4);
+    }
+    mbar_init(bar(FB_DRAIN), 1);
+    *abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tslot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (threadIdx.x == 0) { unsigned smid; asm volatile("mov.u32 %0, %%smid;" : "=r"(smid)); const int cid = blockIdx.y * gridDim.x + blockIdx.x; if (cid < 4096) { g_span[cid][0] = globaltimer_ns(); g_span[cid][2] = smid; } }
+
+  if (wg == 0) {
+    sagefp4::regs_dec<TcRegs::kCtl>();
+    if (warp == 0 && lane == 0) {
+      // ---- producer
+      mbar_arrive_expect_tx(bar(FB_Q), 16384);
+      bulk_load(sbase + L::kQ, ws.qc + hb + static_cast<size_t>(qt) * kTok * D, 16384, bar(FB_Q));
+      const bool held = withhold && blockIdx.x == 0 && blockIdx.y == 0;
+      int issued = 0;
+      for (int kt = 0; kt < nkt; kt++) {
+        const int s = kt % kTcStages;
+        if (kt >= kTcStages && !wait1_ab(bar(FB_EMPTY + s), ((kt / kTcStages) - 1) & 1, ctl, abort)) break;
+        if (held && kt == 0) continue;  // failure-detection test: this tile never arrives
+        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+        const size_t ko = hb + static_cast<size_t>(kt) * kTok * D;
+        mbar_arrive_expect_tx(bar(FB_FULL + s), 32768);
+        bulk_load(st + L::kSK, ws.kc + ko, 16384, bar(FB_FULL + s));
+        bulk_load(st + L::kSV, ws.vct + ko, 16384, bar(FB_FULL + s));
+        issued = kt + 1;
+      }
+      if (*abort) {
+        for (int last = issued - 1; last >= 0 && last >= issued - kTcStages; last--)
+          if (!(held && last == 0)) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(bar(FB_FULL + last % kTcStages), (last / kTcStages) & 1) &&
+                   globaltimer_ns() - t0 < ctl.limit) {
+            }
+          }
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar(FB_Q), 0) && globaltimer_ns() - t0 < ctl.limit) {
+        }
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---- MMA issue
+      const uint32_t idS = idesc_f16(128, 128), idPV = idesc_f16(128, 64);
+      // descriptors built once per operand; a K step of 16 moves 32 bytes (+2)
+      const uint64_t dq0 = desc_k64(sbase + L::kQ, 0);
+      bool ok = wait1_ab(bar(FB_Q), 0, ctl, abort);
+      auto issue_s = [&](int kt) {
+        const int s = kt % kTcStages, b = kt & 1;
+        if (!wait1_ab(bar(FB_FULL + s), (kt / kTcStages) & 1, ctl, abort)) return false;
+        if (kt >= 2 && !wait1_ab(bar(FB_SFREE + b), ((kt >> 1) - 1) & 1, ctl, abort)) return false;
+        tc_fence_after();
+        const uint64_t dks = desc_k64(sbase + L::kStageOff + s * L::kStage + L::kSK, 0);
+#pragma unroll
+        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTfS + 128 * b, dq0 + 2 * k, dks + 2 * k, idS, k > 0);
+        tc_commit(bar(FB_SDONE + b));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int kt = 0; ok && kt < nkt; kt++) {
+        const int s = kt % kTcStages, b = kt & 1;
+        if (kt + 1 < nkt && !(ok = issue_s(kt + 1))) break;
+        TR(8, kt);
+        if (!(ok = wait1_ab(bar(FB_PFULL + b), (kt >> 1) & 1, ctl, abort))) break;
+        TR(9, kt);
+        if (kt >= 2 && !(ok = wait1_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort))) break;
+        tc_fence_after();
+        // P^ key slabs 16 KB apart (+1024), V^T key halves 8 KB apart (+512)
+        const uint64_t dpb = desc_k64(sbase + L::kPOff + b * L::kP, 0);
+        const uint64_t dvs = desc_k64(sbase + L::kStageOff + s * L::kStage + L::kSV, 0);
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+          mma_f16_tc(tmem + kTfPv + 64 * b, dpb + 1024 * (k >> 2) + 2 * (k & 3), dvs + 512 * (k >> 2) + 2 * (k & 3),
+                     idPV, k > 0);
+        tc_commit(bar(FB_PVDONE + b));
+        tc_commit(bar(FB_EMPTY + s));
+        tc_commit(bar(FB_PEMPTY + b));
+        TR(10, kt);
+      }
+      tc_commit(bar(FB_DRAIN));
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar(FB_DRAIN), 0) && globaltimer_ns() - t0 < ctl.limit) {
+      }
+    }
+    // end of the CTA: every role arrives from its own code path (barrier 2)
+    __syncwarp();
+    named_bar(2, kTcThreads);
+    if (warp == 1) tmem_dealloc(tmem, 512);
+  } else if (wg == 1 || wg == 2) {
+    // ---- softmax: this thread's query row, keys 64h..64h+63 of each tile.
+    // The scores arrive as exact integers (Q^.K^ code products); the scale
+    // sq sk scale log2(e) enters only the exponent's argument.
+    sagefp4::regs_inc<TcRegs::kSoft>();
+    const int h = wg - 1;
+    const int wq = warp & 3;
+    const int row = 32 * wq + lane;
+    const int sw = 4 * h + wq;
+    const int blk = wq >> 1;  // 64-row block of this row
+    const uint32_t lanebase = static_cast<uint32_t>(32 * wq) << 16;
+    const int qrow = qt * kTok + row;
+    const bool valid = qrow < N;
+    const float sqk = ws.sq[static_cast<size_t>(bh) * nqt + qt] * scale_log2e;
+    const uint64_t magic2 = pack2(kRintMagic, kRintMagic), nmagic2 = pack2(-kRintMagic, -kRintMagic);
+    float m = -INFINITY, l = 0.0f;
+    float sk_next = ws.sk[static_cast<size_t>(bh) * nqt], sv_next = ws.sv[static_cast<size_t>(bh) * nqt];
+    for (int kt = 0; kt < nkt; kt++) {
+      const int b = kt & 1;
+      const float sk_cur = sk_next, sv_cur = sv_next;
+      if (kt + 1 < nkt) {
+        sk_next = ws.sk[static_cast<size_t>(bh) * nqt + kt + 1];
+        sv_next = ws.sv[static_cast<size_t>(bh) * nqt + kt + 1];
+      }
+      bool ok = waitw_ab(bar(FB_SDONE + b), (kt >> 1) & 1, ctl, abort);
+      if (threadIdx.x == 128) TR(0, kt); if (threadIdx.x == 256) TR(6, kt);
+      tc_fence_after();
+      uint32_t ru[2][32];
+      tmem_ld32(tmem + lanebase + kTfS + 128 * b + 64 * h, ru[0]);
+      tmem_ld32(tmem + lanebase + kTfS + 128 * b + 64 * h + 32, ru[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(FB_SFREE + b));
+      if (threadIdx.x == 128) TR(1, kt);
+      if ((kCausal && kt == qt) || (kt == nqt - 1 && (N % kTok) != 0)) {
+        // keys past N, and (causal) past this row, do not take part
+        const int k0 = kt * kTok + 64 * h;
+        const int last = kCausal ? min(N - 1, qrow) : N - 1;
+#pragma unroll
+        for (int i = 0; i < 64; i++)
+          if (k0 + i > last) ru[i >> 5][i & 31] = __float_as_uint(-INFINITY);
+      }
+      float hm;
+      {
+        float t[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+          const uint32_t* r = &ru[j >> 2][(j & 3) * 8];
+          t[j] = max3f(max3f(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2])),
+                       max3f(__uint_as_float(r[3]), __uint_as_float(r[4]), __uint_as_float(r[5])),
+                       fmaxf(__uint_as_float(r[6]), __uint_as_float(r[7])));
+        }
+        hm = max3f(max3f(t[0], t[1], t[2]), max3f(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
+      }
+      // the row's maximum over both halves of the tile (xm by tile parity)
+      xm[(2 * b + h) * 128 + row] = hm;
+      // P buffer b: PV of tile kt - 2 has read it; alpha and beta of buffer b:
+      // the correction has read them
+      ok = ok && (kt < 2 || waitw_ab(bar(FB_PEMPTY + b), ((kt >> 1) - 1) & 1, ctl, abort));
+      ok = ok && (kt < 2 || waitw_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort));
+      if (threadIdx.x == 128) TR(11, kt);
+      if (!group_and(ok)) break;  // also publishes xm
+      if (threadIdx.x == 128) TR(2, kt);
+      const float mt = fmaxf(hm, xm[(2 * b + 1 - h) * 128 + row]);
+      // c2 > 0 keeps masked keys at -inf (c2 = 0 only when every score is 0)
+      const float c2 = fmaxf(sqk * sk_cur, 1e-30f);
+      const float mn = fmaxf(m, mt * c2);
+      const float alpha = ex2(m - mn);  // m = -inf on the first tile: 0
+      m = mn;
+      // The block's largest P~ is the largest of its rows' maxima, each the
+      // exponential of the same argument as the row's largest score (rows past
+      // N excluded); both halves of a row compute it alike.
+      const float rp = valid ? ex2(fmaf(mt, c2, -mn)) : 0.0f;
+      const uint32_t wmax = redux_max_u32(__float_as_uint(rp));  // rp >= 0: bit order is value order
+      if (lane == 0) bm[b * 8 + sw] = __uint_as_float(wmax);
+      if (h == 0) al[b * 128 + row] = alpha;
+      const uint64_t c22 = pack2(c2, c2), nm2 = pack2(-mn, -mn);
+      uint64_t acc0 = 0, acc1 = 0;
+#pragma unroll
+      for (int j = 0; j < 32; j++) {
+        uint32_t* r = &ru[j >> 4][(j & 15) * 2];
+        const uint64_t y = fma2(pack2(__uint_as_float(r[0]), __uint_as_float(r[1])), c22, nm2);
+        const float x0 = ex2(lo2(y)), x1 = ex2(hi2(y));
+        r[0] = __float_as_uint(x0);
+        r[1] = __float_as_uint(x1);
+        if (j & 1)
+          acc1 = add2(acc1, pack2(x0, x1));
+        else
+          acc0 = add2(acc0, pack2(x0, x1));
+      }
+      const uint64_t acc = add2(acc0, acc1);
+      l = fmaf(l, alpha, lo2(acc) + hi2(acc));
+      if (threadIdx.x == 128) TR(3, kt);
+      named_bar(3 + 2 * h + blk, 64);  // publishes bm to the block's other warp of this half
+      if (threadIdx.x == 128) TR(4, kt);
+      const float amax = fmaxf(bm[b * 8 + 4 * h + 2 * blk], bm[b * 8 + 4 * h + 2 * blk + 1]);
+      const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+      if (h == 0 && wq == 2 * blk && lane == 0) beta[b * 2 + blk] = __fdiv_rn(amax, 127.0f) * sv_cur;
+      uint8_t* pbuf = smem + L::kPOff + b * L::kP + h * 16384;
+      const uint64_t ii = pack2(inv, inv);
+#pragma unroll
+      for (int ch = 0; ch < 8; ch++) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+          const uint32_t* r = &ru[ch >> 2][(ch & 3) * 8 + 2 * u];
+          // rint(x * inv): the product rounded to FP32, then to an integer by
+          // adding and subtracting 1.5 * 2^23 (exact below 2^22)
+          const uint64_t z = mul2(pack2(__uint_as_float(r[0]), __uint_as_float(r[1])), ii);
+          const uint64_t n = add2(add2(z, magic2), nmagic2);
+          wv[u] = h2(lo2(n), hi2(n));
+        }
+        *reinterpret_cast<uint4*>(pbuf + swz(row, 16 * ch, 128)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(FB_PFULL + b));
+      if (threadIdx.x == 128) TR(5, kt); if (threadIdx.x == 256) TR(7, kt);
+    }
+    // the row's statistics for the epilogue
+    lf[h * 128 + row] = l;
+    if (h == 0) mf[row] = m;
+    tc_fence_before();
+    named_bar(2, kTcThreads);
+  } else {
+    // ---- correction: O of this thread's row, as FP32 pairs
+    sagefp4::regs_inc<TcRegs::kFold>();
+    const int row = 32 * (warp & 3) + lane;
+    const int blk = (warp & 3) >> 1;
+    const uint32_t lanebase = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    uint64_t o[32];
+#pragma unroll
+    for (int i = 0; i < 32; i++) o[i] = 0;
+    for (int kt = 0; kt < nkt; kt++) {
+      const int b = kt & 1;
+      // PFULL: the softmax's alpha and beta of this tile (its release); PVDONE: the product
+      if (!waitw_ab(bar(FB_PFULL + b), (kt >> 1) & 1, ctl, abort)) break;
+      if (!waitw_ab(bar(FB_PVDONE + b), (kt >> 1) & 1, ctl, abort)) break;
+      if (threadIdx.x == 384) TR(12, kt);
+      tc_fence_after();
+      const float alpha = al[b * 128 + row], bt = beta[b * 2 + blk];
+      uint32_t ru[2][32];
+      tmem_ld32(tmem + lanebase + kTfPv + 64 * b, ru[0]);
+      tmem_ld32(tmem + lanebase + kTfPv + 64 * b + 32, ru[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(FB_PVFREE + b));
+      // o = pv * beta + o * alpha; o * 1 is o, so rows whose maximum held skip it
+      const uint64_t bt2 = pack2(bt, bt);
+      if (__all_sync(kFull, alpha == 1.0f)) {
+#pragma unroll
+        for (int j = 0; j < 32; j++)
+          o[j] = fma2(pack2(__uint_as_float(ru[j >> 4][(j & 15) * 2]), __uint_as_float(ru[j >> 4][(j & 15) * 2 + 1])),
+                      bt2, o[j]);
+      } else {
+        const uint64_t al2 = pack2(alpha, alpha);
+#pragma unroll
+        for (int j = 0; j < 32; j++)
+          o[j] = fma2(pack2(__uint_as_float(ru[j >> 4][(j & 15) * 2]), __uint_as_float(ru[j >> 4][(j & 15) * 2 + 1])),
+                      bt2, mul2(o[j], al2));
+      }
+      if (threadIdx.x == 384) TR(13, kt);
+    }
+    // epilogue, once the softmax has published l and m
+    tc_fence_before();
+    named_bar(2, kTcThreads);
+    if (!*abort) {
+      const int qrow = qt * kTok + row;
+      if (qrow < N) {
+        const float lt = lf[row] + lf[128 + row];
+        const float il = 1.0f / lt;
+        uint16_t* orow = out + (static_cast<size_t>(bh) * N + qrow) * D;
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+          __nv_bfloat162 h0 = __floats2bfloat162_rn(lo2(o[4 * c + 0]) * il, hi2(o[4 * c + 0]) * il);
+          __nv_bfloat162 h1 = __floats2bfloat162_rn(lo2(o[4 * c + 1]) * il, hi2(o[4 * c + 1]) * il);
+          __nv_bfloat162 hh2 = __floats2bfloat162_rn(lo2(o[4 * c + 2]) * il, hi2(o[4 * c + 2]) * il);
+          __nv_bfloat162 h3 = __floats2bfloat162_rn(lo2(o[4 * c + 3]) * il, hi2(o[4 * c + 3]) * il);
+          uint4 w;
+          w.x = *reinterpret_cast<uint32_t*>(&h0);
+          w.y = *reinterpret_cast<uint32_t*>(&h1);
+          w.z = *reinterpret_cast<uint32_t*>(&hh2);
+          w.w = *reinterpret_cast<uint32_t*>(&h3);
+          *reinterpret_cast<uint4*>(orow + 8 * c) = w;
+        }
+        lse[static_cast<size_t>(bh) * N + qrow] = (mf[row] + __log2f(lt)) * kLn2;
+      }
+    }
+    if (threadIdx.x == 384) { const int cid = blockIdx.y * gridDim.x + blockIdx.x; if (cid < 4096) g_span[cid][1] = globaltimer_ns(); }
+  }
+}
+
+// dQ accumulator (FP32, padded rows) -> bf16 [BH][N][D]
+template <int D>
+__global__ void __launch_bounds__(kThreads) dq_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq, int N,
+                                                      int BH) {
+  const int Np = (N + kTok - 1) / kTok * kTok;
+  const size_t total = static_cast<size_t>(BH) * N * D / 4;
+  for (size_t i = blockIdx.x * static_cast<size_t>(kThreads) + threadIdx.x; i < total;
+       i += static_cast<size_t>(gridDim.x) * kThreads) {
+    const size_t e = 4 * i;
+    const size_t row = e / D, d = e % D;
+    const size_t bh = row / N, n = row % N;
+    const float4 v = *reinterpret_cast<const float4*>(acc + (bh * Np + n) * D + d);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 w;
+    w.x = *reinterpret_cast<uint32_t*>(&lo);
+    w.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dq + e) = w;
+  }
+}
+
+// ---------------------------------------------------------------- probes
+// tcgen05 kind::f16 with the layouts the kernels use: one CTA of 4 warps
+// computes C [128][N] = A [128][64] x B [N][64]^T (FP16 in, FP32 out) from
+// row-major global inputs staged into swizzled shared memory.
+__global__ void __launch_bounds__(128) umma_probe_kernel(const uint16_t* __restrict__ a, const uint16_t* __restrict__ b,
+                                                         int N, float* __restrict__ c, int32_t* status) {
+  __shared__ __align__(1024) uint8_t sa[128 * 128];
+  __shared__ __align__(1024) uint8_t sb[128 * 128];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tslot;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  for (int i = tid; i < 128 * 8; i += 128) {  // 16-byte chunks of A
+    const int r = i / 8, ch = i % 8;
+    *reinterpret_cast<uint4*>(sa + swz(r, 16 * ch, 128)) = *reinterpret_cast<const uint4*>(a + r * 64 + 8 * ch);
+  }
+  for (int i = tid; i < N * 8; i += 128) {
+    const int r = i / 8, ch = i % 8;
+    *reinterpret_cast<uint4*>(sb + swz(r, 16 * ch, 128)) = *reinterpret_cast<const uint4*>(b + r * 64 + 8 * ch);
+  }
+  if (tid == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_addr(&tslot), 128);
+    tmem_relinquish();
+  }
+  // generic-proxy writes of the operands -> visible to the tensor core
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tslot;
+  if (tid == 0) {
+    const uint32_t id = idesc_f16(128, N);
+#pragma unroll
+    for (int k = 0; k < 4; k++)
+      mma_f16_tc(tmem, desc_k64(smem_addr(sa), 16 * k), desc_k64(smem_addr(sb), 16 * k), id, k > 0);
+    tc_commit(smem_addr(&bar));
+  }
+  const Ctl ctl{status, 100ull * 1000ull * 1000ull};
+  const bool ok = waitw(smem_addr(&bar), 0, ctl);
+  tc_fence_after();
+  if (ok) {
+    const int row = 32 * warp + (tid & 31);
+    for (int c0 = 0; c0 < N; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + c0, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; j++) c[row * N + c0 + j] = __uint_as_float(r[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// Probe of the MN-major form: one CTA computes c [128][64] = a [128][128] x
+// b [128][64] (FP16 in, FP32 out, row-major device arrays) with both operands
+// staged K-row by K-row, A's two 64-row blocks of M 32 KB apart (as dQ reads
+// two query tiles' dS^ codes from two buffers) and B between them.
+constexpr int kMnProbeSmem = 3 * 16384 + 1024;
+__global__ void __launch_bounds__(128) umma_mn_probe_kernel(const uint16_t* __restrict__ a,
+                                                            const uint16_t* __restrict__ b, float* __restrict__ c,
+                                                            int32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tslot;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  constexpr int kA0 = 0, kB = 16384, kA1 = 32768;
+  for (int i = tid; i < 128 * 128; i += 128) {  // a[m][k] -> row k of block m / 64
+    const int m = i >> 7, k = i & 127;
+    *reinterpret_cast<uint16_t*>(sm + (m < 64 ? kA0 : kA1) + swz(k, 2 * (m & 63), 128)) = a[i];
+  }
+  for (int i = tid; i < 128 * 64; i += 128) {  // b[k][n] -> row k
+    const int k = i >> 6, n = i & 63;
+    *reinterpret_cast<uint16_t*>(sm + kB + swz(k, 2 * n, 128)) = b[i];
+  }
+  if (tid == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_addr(&tslot), 64);
+    tmem_relinquish();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tslot;
+  const uint32_t sb = smem_addr(sm);
+  if (tid == 0) {
+    const uint32_t id = idesc_f16_mn(128, 64);
+#pragma unroll
+    for (int k = 0; k < 8; k++)
+      mma_f16_tc(tmem, desc_mn(sb + kA0, 16 * k, kA1 - kA0), desc_mn(sb + kB, 16 * k, kA1 - kA0), id, k > 0);
+    tc_commit(smem_addr(&bar));
+  }
+  const Ctl ctl{status, 100ull * 1000ull * 1000ull};
+  const bool ok = waitw(smem_addr(&bar), 0, ctl);
+  tc_fence_after();
+  if (ok) {
+    const int row = 32 * warp + (tid & 31);
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + c0, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; j++) c[row * 64 + c0 + j] = __uint_as_float(r[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
+
+// Integer products on the FP16 MMA: one warp computes the 16 x 8 product of
+// INT8 matrices a [16][K] and b [8][K] (both row-major, K a multiple of 16)
+// with the codes as FP16 values and FP32 accumulation, chained over K / 16
+// MMAs like the kernels' sums, and writes it as float [16][8].
+__global__ void int_mma_probe_kernel(const int8_t* __restrict__ a, const int8_t* __restrict__ b, int K,
+                                     float* __restrict__ out) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int ks = 0; ks < K / 16; ks++) {
+    const int k0 = 16 * ks + 2 * t;
+    uint32_t fa[4];
+    fa[0] = h2(a[g * K + k0], a[g * K + k0 + 1]);
+    fa[1] = h2(a[(g + 8) * K + k0], a[(g + 8) * K + k0 + 1]);
+    fa[2] = h2(a[g * K + k0 + 8], a[g * K + k0 + 9]);
+    fa[3] = h2(a[(g + 8) * K + k0 + 8], a[(g + 8) * K + k0 + 9]);
+    const uint32_t b0 = h2(b[g * K + k0], b[g * K + k0 + 1]);
+    const uint32_t b1 = h2(b[g * K + k0 + 8], b[g * K + k0 + 9]);
+    mma_f16(c, fa, b0, b1);
+  }
+  out[g * 8 + 2 * t] = c[0];
+  out[g * 8 + 2 * t + 1] = c[1];
+  out[(g + 8) * 8 + 2 * t] = c[2];
+  out[(g + 8) * 8 + 2 * t + 1] = c[3];
+}
+
+// Throughput of the warp-level MMA forms on register operands: kind 0 INT8
+// m16n8k32, kind 1 FP16 m16n8k16 with FP32 accumulation (the one the kernels
+// use).  Eight independent accumulators per warp.
+template <int kKind>
+__global__ void __launch_bounds__(kThreads) mma_peak_kernel(int iters, int* out) {
+  uint32_t a[4], b0, b1;
+  const uint32_t seed = threadIdx.x * 0x9E3779B9u + blockIdx.x;
+  a[0] = seed;
+  a[1] = seed ^ 0x5bd1e995u;
+  a[2] = seed * 3u;
+  a[3] = seed + 0x1234567u;
+  b0 = seed ^ 0xabcdefu;
+  b1 = seed * 7u;
+  if (kKind == 0) {
+    int c[8][4] = {};
+    for (int i = 0; i < iters; i++)
+#pragma unroll
+      for (int u = 0; u < 8; u++) mma_s8(c[u], a, b0, b1);
+    int s = 0;
+#pragma unroll
+    for (int u = 0; u < 8; u++) s += c[u][0] + c[u][1] + c[u][2] + c[u][3];
+    if (s == 0x7fffffff) out[0] = s;
+  } else {
+    // small FP16 values so the sums stay finite
+    a[0] = a[1] = a[2] = a[3] = 0x3c003c00u & (seed | 0x3c003c00u);
+    b0 = b1 = 0x1c001c00u;
+    float c[8][4] = {};
+    for (int i = 0; i < iters; i++)
+#pragma unroll
+      for (int u = 0; u < 8; u++) mma_f16(c[u], a, b0, b1);
+    float s = 0.0f;
+#pragma unroll
+    for (int u = 0; u < 8; u++) s += c[u][0] + c[u][1] + c[u][2] + c[u][3];
+    if (s == -1.0f) out[0] = 1;
+  }
+}
+
+// ---------------------------------------------------------------- host side
+struct Layout {
+  size_t off[SAGEBWD_WS_FIELDS];
+  size_t total;
+};
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+Layout layout(int B, int H, int N, int D) {
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t Np = (static_cast<size_t>(N) + kTok - 1) / kTok * kTok;
+  const size_t nb = Np / kTok;
+  const size_t rows = 2 * BH * Np * D;  // FP16 [BH][Np][D]
+  const size_t sizes[SAGEBWD_WS_FIELDS] = {
+      rows,        rows,        rows,        rows,         // Q^, K^, V^, dO^ codes
+      rows,        rows,                                   // V, dO as FP16
+      rows,        rows,                                   // Q^, dO^ codes transposed per 64-token tile
+      rows,                                                // V^ codes transposed per 64-token half tile
+      4 * BH * nb, 4 * BH * nb, 4 * BH * nb, 4 * BH * nb,  // Q, K, V, dO block scales
+      4 * BH * Np, 4 * BH * Np,                            // L (log2 units), D = rowsum(dO o O)
+      4 * BH * Np * D,                                     // dQ accumulator
+      256,                                                 // status word
+  };
+  Layout l;
+  size_t off = 0;
+  for (int i = 0; i < SAGEBWD_WS_FIELDS; i++) {
+    l.off[i] = off;
+    off += align256(sizes[i]);
+  }
+  l.total = off;
+  return l;
+}
+
+Ws carve(void* base, const Layout& l) {
+  char* b = static_cast<char*>(base);
+  Ws w;
+  w.qc = reinterpret_cast<uint16_t*>(b + l.off[0]);
+  w.kc = reinterpret_cast<uint16_t*>(b + l.off[1]);
+  w.vc = reinterpret_cast<uint16_t*>(b + l.off[2]);
+  w.doc = reinterpret_cast<uint16_t*>(b + l.off[3]);
+  w.vh = reinterpret_cast<uint16_t*>(b + l.off[4]);
+  w.doh = reinterpret_cast<uint16_t*>(b + l.off[5]);
+  w.qct = reinterpret_cast<uint16_t*>(b + l.off[6]);
+  w.doct = reinterpret_cast<uint16_t*>(b + l.off[7]);
+  w.vct = reinterpret_cast<uint16_t*>(b + l.off[8]);
+  w.sq = reinterpret_cast<float*>(b + l.off[9]);
+  w.sk = reinterpret_cast<float*>(b + l.off[10]);
+  w.sv = reinterpret_cast<float*>(b + l.off[11]);
+  w.sdo = reinterpret_cast<float*>(b + l.off[12]);
+  w.l2 = reinterpret_cast<float*>(b + l.off[13]);
+  w.dd = reinterpret_cast<float*>(b + l.off[14]);
+  w.dqacc = reinterpret_cast<float*>(b + l.off[15]);
+  w.status = reinterpret_cast<int32_t*>(b + l.off[16]);
+  return w;
+}
+
+bool dims_ok(int B, int H, int N, int D) {
+  if (B < 0 || H < 0 || N < 0 || (D != 64 && D != 128)) return false;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long Np = (static_cast<long long>(N) + kTok - 1) / kTok * kTok;
+  if (BH > 65535) return false;                 // gridDim.y
+  if (Np / kTok > (1LL << 20)) return false;    // gridDim.x, with room
+  if (BH * Np * D > (1LL << 40)) return false;  // workspace offsets stay sane
+  return true;
+}
+
+bool aligned(const void* p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool scale_ok(float s) { return s > 0.0f && s < 1e30f; }  // false for NaN
+
+int check_device() {
+  static int cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SAGE_FP4_ECUDA;
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev] == 1 ? SAGE_FP4_OK : SAGE_FP4_EUNSUPPORTED;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return SAGE_FP4_ECUDA;
+  const bool ok = (major == 10 && minor == 3);
+  if (dev >= 0 && dev < 64) cache[dev] = ok ? 1 : 2;
+  return ok ? SAGE_FP4_OK : SAGE_FP4_EUNSUPPORTED;
+}
+
+template <int D, bool C>
+cudaError_t launch_fwd(const Ws& w, uint16_t* o, float* lse, int BH, int N, float scale, cudaStream_t st,
+                       uint64_t wait_ns = kWaitNs, int withhold = 0) {
+  const int smem = FwdSmem<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((N + kTok - 1) / kTok, BH);
+  fwd_kernel<D, C><<<grid, kThreads, smem, st>>>(w, o, lse, N, scale * kLog2e, wait_ns, withhold);
+  return cudaGetLastError();
+}
+
+template <int D, bool C>
+cudaError_t launch_dkdv(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int N, float scale, cudaStream_t st,
+                        uint64_t wait_ns = kWaitNs, int withhold = 0) {
+  const int smem = BwdSmem<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((N + kTok - 1) / kTok, BH);
+  dkdv_kernel<D, C><<<grid, kThreads, smem, st>>>(w, dk, dv, N, scale, wait_ns, withhold);
+  return cudaGetLastError();
+}
+
+// The tcgen05 backward (D = 64).  Its warpgroups' setmaxnreg budgets add up
+// to exactly 128 registers per thread at launch; with any other allocation
+// an increase would never be granted, so it refuses to launch.
+// 2-D FP32 tensor [rows][inner] (row pitch inner * 4 bytes) with boxes of
+// [box_rows][box_inner], 128-byte swizzled (box_inner * 4 <= 128).
+bool make_map_f32(CUtensorMap* m, const float* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                  uint32_t box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if (!enc) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool C>
+cudaError_t launch_dkdv_tc(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int N, float scale, cudaStream_t st,
+                           uint64_t wait_ns, int withhold) {
+  const uint64_t rows = static_cast<uint64_t>(BH) * ((N + kTok - 1) / kTok * kTok);
+  CUtensorMap tm;
+  if (rows > 0x7fffffffu || !make_map_f32(&tm, w.dqacc, 64, rows, 32, 32)) return cudaErrorInvalidValue;
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, dkdv_tc_kernel<C>);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs != 65536 / kTcThreads) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(dkdv_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::kAlloc);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((N + kTok - 1) / kTok, BH);
+  dkdv_tc_kernel<C><<<grid, kTcThreads, TcSmem::kAlloc, st>>>(tm, w, dk, dv, N, scale, wait_ns, withhold);
+  return cudaGetLastError();
+}
+
+template <bool C>
+cudaError_t launch_fwd_tc(const Ws& w, uint16_t* o, float* lse, int BH, int N, float scale, cudaStream_t st,
+                          uint64_t wait_ns, int withhold) {
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, fwd_tc_kernel<C>);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs != 65536 / kTcThreads) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(fwd_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, TfSmem::kAlloc);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((N + kTok - 1) / kTok, BH);
+  fwd_tc_kernel<C><<<grid, kTcThreads, TfSmem::kAlloc, st>>>(w, o, lse, N, scale * kLog2e, wait_ns, withhold);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_quant(const Ws& w, const void* a, const void* b, const void* c, const void* o, const float* lse,
+                         int BH, int N, int kind0, int nkinds, cudaStream_t st) {
+  const dim3 grid((N + kTok - 1) / kTok, BH, nkinds);
+  quant_kernel<D><<<grid, kThreads, 0, st>>>(static_cast<const uint16_t*>(a), static_cast<const uint16_t*>(b),
+                                             static_cast<const uint16_t*>(c), static_cast<const uint16_t*>(o), lse, N,
+                                             kind0, w);
+  return cudaGetLastError();
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? SAGE_FP4_OK : SAGE_FP4_ECUDA; }
+
+}  // namespace sagebwd
+
+using namespace sagebwd;
+
+extern "C" {
+
+size_t sagebwd_workspace_bytes(int B, int H, int N, int D) {
+  if (!dims_ok(B, H, N, D)) return 0;
+  return layout(B, H, N, D).total;
+}
+
+int sagebwd_workspace_layout(int B, int H, int N, int D, size_t* offsets) {
+  if (!dims_ok(B, H, N, D) || !offsets) return SAGE_FP4_EINVAL;
+  const Layout l = layout(B, H, N, D);
+  for (int i = 0; i < SAGEBWD_WS_FIELDS; i++) offsets[i] = l.off[i];
+  return SAGE_FP4_OK;
+}
+
+// Common checks of the step calls: sizes, causal flag, scale, workspace.
+// Returns SAGE_FP4_OK (carry on), a negative code, or 1 for an empty problem.
+static int check_common(int B, int H, int N, int D, int causal, float scale, const void* workspace,
+                        size_t workspace_bytes, Layout* l) {
+  if (!dims_ok(B, H, N, D) || (causal != 0 && causal != 1) || !scale_ok(scale)) return SAGE_FP4_EINVAL;
+  if (!aligned(workspace, 256)) return SAGE_FP4_EINVAL;
+  *l = layout(B, H, N, D);
+  if (workspace_bytes < l->total) return SAGE_FP4_EINVAL;
+  if (static_cast<long long>(B) * H * N == 0) return 1;
+  return SAGE_FP4_OK;
+}
+
+int sagebwd_quantize_qkv(const void* q, const void* k, const void* v, int B, int H, int N, int D, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  Layout l;
+  int rc = check_common(B, H, N, D, 0, 1.0f, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_OK : rc;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return SAGE_FP4_EINVAL;
+  if ((rc = check_device()) != SAGE_FP4_OK) return rc;
+  const Ws w = carve(workspace, l);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return from_cuda(D == 64 ? launch_quant<64>(w, q, k, v, nullptr, nullptr, B * H, N, 0, 3, st)
+                           : launch_quant<128>(w, q, k, v, nullptr, nullptr, B * H, N, 0, 3, st));
+}
+
+int sagebwd_attn_fwd(void* o, float* lse, int B, int H, int N, int D, int causal, float scale, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  Layout l;
+  int rc = check_common(B, H, N, D, causal, scale, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_OK : rc;
+  if (!aligned(o, 16) || !aligned(lse, 4)) return SAGE_FP4_EINVAL;
+  if ((rc = check_device()) != SAGE_FP4_OK) return rc;
+  const Ws w = carve(workspace, l);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint16_t* ob = static_cast<uint16_t*>(o);
+  const int BH = B * H;
+  cudaError_t e;
+  if (D == 64)
+    e = causal ? launch_fwd_tc<true>(w, ob, lse, BH, N, scale, st, kWaitNs, 0)
+               : launch_fwd_tc<false>(w, ob, lse, BH, N, scale, st, kWaitNs, 0);
+  else
+    e = causal ? launch_fwd<128, true>(w, ob, lse, BH, N, scale, st)
+               : launch_fwd<128, false>(w, ob, lse, BH, N, scale, st);
+  return from_cuda(e);
+}
+
+int sagebwd_bwd_prep(const void* dout, const void* o, const float* lse, int B, int H, int N, int D, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  Layout l;
+  int rc = check_common(B, H, N, D, 0, 1.0f, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_OK : rc;
+  if (!aligned(dout, 16) || !aligned(o, 16) || !aligned(lse, 4)) return SAGE_FP4_EINVAL;
+  if ((rc = check_device()) != SAGE_FP4_OK) return rc;
+  const Ws w = carve(workspace, l);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return from_cuda(D == 64 ? launch_quant<64>(w, dout, nullptr, nullptr, o, lse, B * H, N, 3, 1, st)
+                           : launch_quant<128>(w, dout, nullptr, nullptr, o, lse, B * H, N, 3, 1, st));
+}
+
+int sagebwd_attn_bwd(void* dk, void* dv, int B, int H, int N, int D, int causal, float scale, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  Layout l;
+  int rc = check_common(B, H, N, D, causal, scale, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_OK : rc;
+  if (!aligned(dk, 16) || !aligned(dv, 16)) return SAGE_FP4_EINVAL;
+  if ((rc = check_device()) != SAGE_FP4_OK) return rc;
+  const Ws w = carve(workspace, l);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint16_t *dkb = static_cast<uint16_t*>(dk), *dvb = static_cast<uint16_t*>(dv);
+  const int BH = B * H;
+  cudaError_t e;
+  if (D == 64)
+    e = causal ? launch_dkdv_tc<true>(w, dkb, dvb, BH, N, scale, st, kWaitNs, 0)
+               : launch_dkdv_tc<false>(w, dkb, dvb, BH, N, scale, st, kWaitNs, 0);
+  else
+    e = causal ? launch_dkdv<128, true>(w, dkb, dvb, BH, N, scale, st)
+               : launch_dkdv<128, false>(w, dkb, dvb, BH, N, scale, st);
+  return from_cuda(e);
+}
+
+int sagebwd_dq_out(void* dq, int B, int H, int N, int D, void* workspace, size_t workspace_bytes, void* stream) {
+  Layout l;
+  int rc = check_common(B, H, N, D, 0, 1.0f, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_OK : rc;
+  if (!aligned(dq, 16)) return SAGE_FP4_EINVAL;
+  if ((rc = check_device()) != SAGE_FP4_OK) return rc;
+  const Ws w = carve(workspace, l);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  const size_t total = static_cast<size_t>(BH) * N * D / 4;
+  const size_t want = (total + kThreads - 1) / kThreads;
+  const int blocks = static_cast<int>(want < 152 * 16 ? want : 152 * 16);
+  if (D == 64)
+    dq_kernel<64><<<blocks, kThreads, 0, st>>>(w.dqacc, static_cast<uint16_t*>(dq), N, BH);
+  else
+    dq_kernel<128><<<blocks, kThreads, 0, st>>>(w.dqacc, static_cast<uint16_t*>(dq), N, BH);
+  return from_cuda(cudaGetLastError());
+}
+
+int sagebwd_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+                int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  // every argument checked before the first launch
+  Layout l;
+  int rc = check_common(B, H, N, D, causal, scale, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_OK : rc;
+  if (!aligned(o, 16) || !aligned(lse, 4)) return SAGE_FP4_EINVAL;
+  rc = sagebwd_quantize_qkv(q, k, v, B, H, N, D, workspace, workspace_bytes, stream);
+  if (rc != SAGE_FP4_OK) return rc;
+  return sagebwd_attn_fwd(o, lse, B, H, N, D, causal, scale, workspace, workspace_bytes, stream);
+}
+
+int sagebwd_bwd(const void* dout, const void* o, const float* lse, void* dq, void* dk, void* dv, int B, int H, int N,
+                int D, int causal, float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  Layout l;
+  int rc = check_common(B, H, N, D, causal, scale, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_OK : rc;
+  if (!aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16)) return SAGE_FP4_EINVAL;
+  rc = sagebwd_bwd_prep(dout, o, lse, B, H, N, D, workspace, workspace_bytes, stream);
+  if (rc != SAGE_FP4_OK) return rc;
+  rc = sagebwd_attn_bwd(dk, dv, B, H, N, D, causal, scale, workspace, workspace_bytes, stream);
+  if (rc != SAGE_FP4_OK) return rc;
+  return sagebwd_dq_out(dq, B, H, N, D, workspace, workspace_bytes, stream);
+}
+
+int sagebwd_get_status(void* workspace, int B, int H, int N, int D, void* stream) {
+  if (!dims_ok(B, H, N, D) || !aligned(workspace, 256)) return SAGE_FP4_EINVAL;
+  const Layout l = layout(B, H, N, D);
+  int32_t* status = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + l.off[SAGEBWD_WS_FIELDS - 1]);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SAGE_FP4_ECUDA;
+  int32_t h = 0;
+  if (cudaMemcpy(&h, status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return SAGE_FP4_ECUDA;
+  if (h != 0 && cudaMemset(status, 0, sizeof(h)) != cudaSuccess) return SAGE_FP4_ECUDA;
+  return h;
+}
+
+int sagebwd_stall_test(int kernel, void* out0, void* out1, int B, int H, int N, int D, float scale,
+                       uint64_t wait_limit_ns, void* workspace, size_t workspace_bytes, void* stream) {
+  Layout l;
+  int rc = check_common(B, H, N, D, 0, scale, workspace, workspace_bytes, &l);
+  if (rc != SAGE_FP4_OK) return rc == 1 ? SAGE_FP4_EINVAL : rc;
+  if ((kernel != 0 && kernel != 1) || wait_limit_ns < 1000000ull || wait_limit_ns > kWaitNs) return SAGE_FP4_EINVAL;
+  if (!aligned(out0, 16) || !aligned(out1, kernel == 0 ? 4 : 16)) return SAGE_FP4_EINVAL;
+  if ((rc = check_device()) != SAGE_FP4_OK) return rc;
+  const Ws w = carve(workspace, l);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  cudaError_t e;
+  if (kernel == 0) {
+    uint16_t* o = static_cast<uint16_t*>(out0);
+    float* lse = static_cast<float*>(out1);
+    e = D == 64 ? launch_fwd_tc<false>(w, o, lse, BH, N, scale, st, wait_limit_ns, 1)
+                : launch_fwd<128, false>(w, o, lse, BH, N, scale, st, wait_limit_ns, 1);
+  } else {
+    uint16_t *dkb = static_cast<uint16_t*>(out0), *dvb = static_cast<uint16_t*>(out1);
+    e = D == 64 ? launch_dkdv_tc<false>(w, dkb, dvb, BH, N, scale, st, wait_limit_ns, 1)
+                : launch_dkdv<128, false>(w, dkb, dvb, BH, N, scale, st, wait_limit_ns, 1);
+  }
+  return from_cuda(e);
+}
+
+int sagebwd_umma_probe(const uint16_t* a, const uint16_t* b, int N, float* c, int32_t* status, void* stream) {
+  if ((N != 64 && N != 128) || !aligned(a, 16) || !aligned(b, 16) || !aligned(c, 4) || !aligned(status, 4))
+    return SAGE_FP4_EINVAL;
+  const int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  umma_probe_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(a, b, N, c, status);
+  return from_cuda(cudaGetLastError());
+}
+
+int sagebwd_umma_mn_probe(const uint16_t* a, const uint16_t* b, float* c, int32_t* status, void* stream) {
+  if (!aligned(a, 2) || !aligned(b, 2) || !aligned(c, 4) || !aligned(status, 4)) return SAGE_FP4_EINVAL;
+  const int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  cudaError_t e = cudaFuncSetAttribute(sagebwd::umma_mn_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       sagebwd::kMnProbeSmem);
+  if (e != cudaSuccess) return from_cuda(e);
+  sagebwd::umma_mn_probe_kernel<<<1, 128, sagebwd::kMnProbeSmem, static_cast<cudaStream_t>(stream)>>>(a, b, c, status);
+  return from_cuda(cudaGetLastError());
+}
+
+int sagebwd_int_mma_probe(const int8_t* a, const int8_t* b, int K, float* out, void* stream) {
+  if (K < 16 || K > 4096 || K % 16 != 0 || !aligned(a, 4) || !aligned(b, 4) || !aligned(out, 4))
+    return SAGE_FP4_EINVAL;
+  const int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  int_mma_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(a, b, K, out);
+  return from_cuda(cudaGetLastError());
+}
+
+int sagebwd_mma_peak(int kind, int ctas, int iters, void* scratch, void* stream) {
+  if ((kind != 0 && kind != 1) || ctas < 1 || ctas > 65535 || iters < 1 || !aligned(scratch, 4))
+    return SAGE_FP4_EINVAL;
+  const int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (kind == 0)
+    mma_peak_kernel<0><<<ctas, kThreads, 0, st>>>(iters, static_cast<int*>(scratch));
+  else
+    mma_peak_kernel<1><<<ctas, kThreads, 0, st>>>(iters, static_cast<int*>(scratch));
+  return from_cuda(cudaGetLastError());
+}
+
+}  // extern "C"
+
+extern "C" int sagebwd_span_read(unsigned long long* host) {
+  return cudaMemcpyFromSymbol(host, g_span, sizeof(g_span)) == cudaSuccess ? 0 : -2;
+}
+
+extern "C" int sagebwd_trace_read(long long* host) {
+  return cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace)) == cudaSuccess ? 0 : -2;
+}

@@ -137,6 +137,13 @@ int sagebwd_stall_test(int kernel, void *out0, void *out1, int B, int H, int N, 
  * wait that runs out sets to SAGE_FP4_ETIMEOUT. */
 int sagebwd_umma_probe(const uint16_t *a, const uint16_t *b, int N, float *c, int32_t *status, void *stream);
 
+/* Probe of the MN-major operand form dQ = dS^ K^ uses (tcgen05.mma kind::f16,
+ * both operands stored with the K index as the 128-byte row, A's two 64-row
+ * blocks of M 32 KB apart): one CTA computes c [128][64] = a [128][128] x
+ * b [128][64] (FP16 in, FP32 out; row-major device arrays).  status: a device
+ * int32 that a wait that runs out sets to SAGE_FP4_ETIMEOUT. */
+int sagebwd_umma_mn_probe(const uint16_t *a, const uint16_t *b, float *c, int32_t *status, void *stream);
+
 /* Exactness probe of the INT8 products: the 16 x 8 product of INT8 device
  * matrices a [16][K] and b [8][K] (row-major, K a multiple of 16 up to 4096)
  * computed the kernels' way (codes as FP16 values, FP32 accumulation chained

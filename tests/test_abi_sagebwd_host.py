@@ -11,7 +11,7 @@ from bit_attention_gb300 import sagebwd as SB
 def test_library_exports_every_header_function():
     lib = SB.lib()
     names = SB.header_functions()
-    assert len(names) == 14
+    assert len(names) == 15
     text = open(SB._HEADER).read()
     decls = dict(re.findall(r"^(?:int|size_t)\s*(sagebwd_\w+)\(([^;]*)\);", text, re.M))
     assert set(decls) == set(names)
@@ -79,6 +79,8 @@ def test_probe_and_status_argument_checks():
     assert SB.sagebwd_int_mma_probe(0x1000, 0x2000, 24, 0x3000, None) == S.EINVAL
     assert SB.sagebwd_int_mma_probe(0x1000, 0x2000, 8192, 0x3000, None) == S.EINVAL
     assert SB.sagebwd_int_mma_probe(0x1001, 0x2000, 32, 0x3000, None) == S.EINVAL
+    assert SB.sagebwd_umma_mn_probe(0x1001, 0x2000, 0x3000, 0x4000, None) == S.EINVAL
+    assert SB.sagebwd_umma_mn_probe(0x1000, 0x2000, 0x3002, 0x4000, None) == S.EINVAL
     nb = SB.sagebwd_workspace_bytes(1, 2, 256, 64)
     st = SB.sagebwd_stall_test
     assert st(2, 0x1000, 0x2000, 1, 2, 256, 64, 0.125, 10 ** 7, 0x100000, nb, None) == S.EINVAL     # kernel

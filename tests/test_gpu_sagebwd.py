@@ -247,6 +247,36 @@ def test_stalled_copy_sets_timeout_and_the_context_survives(kernel, D):
     assert torch.equal(o2, o) and torch.equal(lse2, lse) and torch.equal(dk2, dk) and torch.equal(dv2, dv)
 
 
+def test_tcgen05_f16_mn_major_operands():
+    """tcgen05.mma kind::f16 with both operands MN-major (the K index as the
+    128-byte row), A's two blocks of 64 rows 32 KB apart, as dQ = dS^ K^ reads
+    them: integer codes give the exact integer product, FP16 values the
+    float64 product within FP32 accumulation."""
+    rng = np.random.default_rng(7)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for kind in ("codes", "values"):
+        if kind == "codes":
+            a = rng.integers(-127, 128, size=(128, 128)).astype(np.float16)
+            b = rng.integers(-127, 128, size=(128, 64)).astype(np.float16)
+            a[5, :] = 127
+            b[:, 3] = 127
+        else:
+            a = rng.standard_normal((128, 128)).astype(np.float16)
+            b = rng.standard_normal((128, 64)).astype(np.float16)
+        ad = torch.from_numpy(a.view(np.uint16).astype(np.int32)).to(torch.int16).cuda()
+        bd = torch.from_numpy(b.view(np.uint16).astype(np.int32)).to(torch.int16).cuda()
+        c = torch.full((128, 64), float("nan"), dtype=torch.float32, device="cuda")
+        assert SB.sagebwd_umma_mn_probe(ad.data_ptr(), bd.data_ptr(), c.data_ptr(), status.data_ptr(), None) == 0
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        want = a.astype(np.float64) @ b.astype(np.float64)
+        got = c.cpu().numpy().astype(np.float64)
+        if kind == "codes":
+            assert np.array_equal(got, want), np.abs(got - want).max()
+        else:
+            assert np.abs(got - want).max() <= 1e-5 * np.abs(want).max() + 1e-5
+
+
 @pytest.mark.parametrize("N", [64, 128])
 def test_tcgen05_f16_operands_and_readback(N):
     """tcgen05.mma kind::f16 with the 128-byte-swizzled K-major layout the
