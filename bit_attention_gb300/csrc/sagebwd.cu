@@ -869,6 +869,32 @@ __device__ __forceinline__ void mma_f16_tc(uint32_t d_tmem, uint64_t a_desc, uin
 // with the 128-byte swizzle (16-byte chunk ^ row & 7), rows of 8 at 1024-byte
 // strides, starting k0 values into the row (k0 a multiple of 16); the tile
 // must start on a 1024-byte boundary.
+// The same with A in tensor memory (M = 128 rows in lanes 0..127; a row's
+// K = 16 FP16 values of one step in 8 consecutive 32-bit columns, the lower
+// K index in the low half of each column).
+__device__ __forceinline__ void mma_f16_tc_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Each thread of the warp writes 32 consecutive 32-bit columns of its lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t desc_k64(uint32_t tile, int k0) {
   return smem_desc(tile + 2 * k0, 16, 1024, kSwizzle128B);
 }
@@ -1960,6 +1986,117 @@ __global__ void __launch_bounds__(kThreads) mma_peak_kernel(int iters, int* out)
   }
 }
 
+// Throughput of the 5th-generation form the kernels use (tcgen05.mma
+// kind::f16, M = 128, K = 16, N = kN): one thread per CTA issues iters x 8
+// MMAs back to back into one tensor-memory accumulator from zero-filled
+// 128-byte-swizzled operands, then waits (bounded) for their completion; a
+// wait that runs out writes SAGE_FP4_ETIMEOUT to out[0].
+template <int kN>
+__global__ void __launch_bounds__(128, 1) umma_peak_kernel(int iters, int* out) {
+  // A (128 rows) and B (kN rows) share one zero-filled buffer
+  __shared__ __align__(1024) uint8_t sb[(kN > 128 ? kN : 128) * 128];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tslot;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  uint8_t* sa = sb;
+  for (int i = tid; i < (kN > 128 ? kN : 128) * 8; i += 128) reinterpret_cast<uint4*>(sb)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_addr(&tslot), 256);
+    tmem_relinquish();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tslot;
+  if (tid == 0) {
+    const uint32_t id = idesc_f16(128, kN);
+    const uint64_t da = desc_k64(smem_addr(sa), 0), db = desc_k64(smem_addr(sb), 0);
+    for (int i = 0; i < iters; i++)
+#pragma unroll
+      for (int k = 0; k < 8; k++) mma_f16_tc(tmem, da + 2 * (k & 3), db + 2 * (k & 3), id, (i | k) != 0);
+    tc_commit(smem_addr(&bar));
+    const uint64_t t0 = globaltimer_ns();
+    bool done = false;
+    while (!(done = mbar_try_wait(smem_addr(&bar), 0)) && globaltimer_ns() - t0 < 1000000000ull) {
+    }
+    if (!done) out[0] = SAGE_FP4_ETIMEOUT;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// Probe of the A-in-tensor-memory form: one CTA computes c [128][N] =
+// a [128][64] x b [N][64]^T (FP16 in, FP32 out, row-major device arrays) with
+// A written to tensor memory by tcgen05.st (thread = row) and B in shared
+// memory (128-byte-swizzled K-major).
+__global__ void __launch_bounds__(128) umma_ta_probe_kernel(const uint16_t* __restrict__ a,
+                                                            const uint16_t* __restrict__ b, int N,
+                                                            float* __restrict__ c, int32_t* status) {
+  __shared__ __align__(1024) uint8_t sb[128 * 128];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tslot;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  for (int i = tid; i < N * 8; i += 128) {
+    const int r = i / 8, ch = i % 8;
+    *reinterpret_cast<uint4*>(sb + swz(r, 16 * ch, 128)) = *reinterpret_cast<const uint4*>(b + r * 64 + 8 * ch);
+  }
+  if (tid == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_addr(&tslot), 256);
+    tmem_relinquish();
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tslot;
+  const uint32_t lanebase = static_cast<uint32_t>(32 * warp) << 16;
+  {
+    uint32_t r[32];
+#pragma unroll
+    for (int j = 0; j < 32; j++)
+      r[j] = static_cast<uint32_t>(a[tid * 64 + 2 * j]) | (static_cast<uint32_t>(a[tid * 64 + 2 * j + 1]) << 16);
+    tmem_st32(tmem + lanebase + 128, r);  // A in columns 128..159
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) {
+    const uint32_t id = idesc_f16(128, N);
+    const uint64_t db = desc_k64(smem_addr(sb), 0);
+#pragma unroll
+    for (int k = 0; k < 4; k++) mma_f16_tc_ta(tmem, tmem + 128 + 8 * k, db + 2 * k, id, k > 0);
+    tc_commit(smem_addr(&bar));
+  }
+  const Ctl ctl{status, 100ull * 1000ull * 1000ull};
+  const bool ok = waitw(smem_addr(&bar), 0, ctl);
+  tc_fence_after();
+  if (ok) {
+    const int row = 32 * warp + (tid & 31);
+    for (int c0 = 0; c0 < N; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(tmem + lanebase + c0, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; j++) c[row * N + c0 + j] = __uint_as_float(r[j]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
 // ---------------------------------------------------------------- host side
 struct Layout {
   size_t off[SAGEBWD_WS_FIELDS];
@@ -2322,6 +2459,15 @@ int sagebwd_umma_probe(const uint16_t* a, const uint16_t* b, int N, float* c, in
   return from_cuda(cudaGetLastError());
 }
 
+int sagebwd_umma_ta_probe(const uint16_t* a, const uint16_t* b, int N, float* c, int32_t* status, void* stream) {
+  if ((N != 64 && N != 128) || !aligned(a, 2) || !aligned(b, 16) || !aligned(c, 4) || !aligned(status, 4))
+    return SAGE_FP4_EINVAL;
+  const int dev = check_device();
+  if (dev != SAGE_FP4_OK) return dev;
+  umma_ta_probe_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(a, b, N, c, status);
+  return from_cuda(cudaGetLastError());
+}
+
 int sagebwd_umma_mn_probe(const uint16_t* a, const uint16_t* b, float* c, int32_t* status, void* stream) {
   if (!aligned(a, 2) || !aligned(b, 2) || !aligned(c, 4) || !aligned(status, 4)) return SAGE_FP4_EINVAL;
   const int dev = check_device();
@@ -2343,15 +2489,19 @@ int sagebwd_int_mma_probe(const int8_t* a, const int8_t* b, int K, float* out, v
 }
 
 int sagebwd_mma_peak(int kind, int ctas, int iters, void* scratch, void* stream) {
-  if ((kind != 0 && kind != 1) || ctas < 1 || ctas > 65535 || iters < 1 || !aligned(scratch, 4))
+  if (kind < 0 || kind > 4 || ctas < 1 || ctas > 65535 || iters < 1 || iters > (1 << 20) || !aligned(scratch, 4))
     return SAGE_FP4_EINVAL;
   const int dev = check_device();
   if (dev != SAGE_FP4_OK) return dev;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (kind == 0)
-    mma_peak_kernel<0><<<ctas, kThreads, 0, st>>>(iters, static_cast<int*>(scratch));
-  else
-    mma_peak_kernel<1><<<ctas, kThreads, 0, st>>>(iters, static_cast<int*>(scratch));
+  int* out = static_cast<int*>(scratch);
+  switch (kind) {
+    case 0: mma_peak_kernel<0><<<ctas, kThreads, 0, st>>>(iters, out); break;
+    case 1: mma_peak_kernel<1><<<ctas, kThreads, 0, st>>>(iters, out); break;
+    case 2: umma_peak_kernel<64><<<ctas, 128, 0, st>>>(iters, out); break;
+    case 3: umma_peak_kernel<128><<<ctas, 128, 0, st>>>(iters, out); break;
+    default: umma_peak_kernel<256><<<ctas, 128, 0, st>>>(iters, out); break;
+  }
   return from_cuda(cudaGetLastError());
 }
 

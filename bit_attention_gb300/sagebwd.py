@@ -56,6 +56,7 @@ def lib() -> ctypes.CDLL:
                 "sagebwd_stall_test": (i, [i, vp, vp, i, i, i, i, f, ctypes.c_uint64, vp, sz, vp]),
                 "sagebwd_umma_probe": (i, [vp, vp, i, vp, vp, vp]),
                 "sagebwd_umma_mn_probe": (i, [vp, vp, vp, vp, vp]),
+                "sagebwd_umma_ta_probe": (i, [vp, vp, i, vp, vp, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -123,6 +124,10 @@ def sagebwd_mma_peak(kind: int, ctas: int, iters: int, scratch_ptr, stream) -> i
 
 def sagebwd_umma_probe(a_ptr, b_ptr, N: int, c_ptr, status_ptr, stream) -> int:
     return lib().sagebwd_umma_probe(a_ptr, b_ptr, N, c_ptr, status_ptr, stream)
+
+
+def sagebwd_umma_ta_probe(a_ptr, b_ptr, N: int, c_ptr, status_ptr, stream) -> int:
+    return lib().sagebwd_umma_ta_probe(a_ptr, b_ptr, N, c_ptr, status_ptr, stream)
 
 
 def sagebwd_umma_mn_probe(a_ptr, b_ptr, c_ptr, status_ptr, stream) -> int:
@@ -242,10 +247,11 @@ def attention(q, k, v, causal: bool = False, scale=None):
 
 def mma_peak_tops(kind: int, ctas: int | None = None, iters: int = 4096, repeats: int = 3) -> float:
     """Best of `repeats` timed probe launches, in TOP/s (INT8, kind 0) or
-    TFLOP/s (FP16 with FP32 accumulation, kind 1)."""
+    TFLOP/s (FP16 with FP32 accumulation: kind 1 warp-level, kinds 2-4
+    tcgen05 with N = 64, 128, 256)."""
     import torch
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    ctas = ctas or 4 * sms
+    ctas = ctas or (4 * sms if kind < 2 else sms)
     scratch = torch.zeros(1, dtype=torch.int32, device="cuda")
     st = torch.cuda.current_stream()
     _fp4._check(sagebwd_mma_peak(kind, ctas, iters, scratch.data_ptr(), st.cuda_stream), "sagebwd_mma_peak")
@@ -257,6 +263,11 @@ def mma_peak_tops(kind: int, ctas: int | None = None, iters: int = 4096, repeats
         e1.record(st)
         e1.synchronize()
         best = min(best, e0.elapsed_time(e1))
+    if kind >= 2:
+        if int(scratch.item()) != 0:
+            raise SageFp4Error(int(scratch.item()), "sagebwd_mma_peak: tcgen05 completion wait ran out")
+        n = (64, 128, 256)[kind - 2]
+        return 2.0 * 128 * n * 16 * 8 * iters * ctas / (best * 1e-3) / 1e12
     macs = (16 * 8 * 32) if kind == 0 else (16 * 8 * 16)
     warps = 256 // 32
     return 2.0 * macs * 8 * iters * warps * ctas / (best * 1e-3) / 1e12

@@ -113,10 +113,14 @@ int sagebwd_dq_out(void *dq, int B, int H, int N, int D, void *workspace, size_t
  * negative SAGE_FP4_* code) and clears it. */
 int sagebwd_get_status(void *workspace, int B, int H, int N, int D, void *stream);
 
-/* Throughput probe of two warp-level MMA forms on register operands (the
- * roofline's denominator is the second): kind 0 INT8 m16n8k32, kind 1 FP16
- * m16n8k16 with FP32 accumulation.  Each of `ctas` CTAs of 256 threads runs
- * iters x 8 MMAs per warp; scratch is 4 device bytes it may write. */
+/* Throughput probe of the MMA forms the kernels use.  Kinds 0 and 1: warp-level
+ * MMAs on register operands, INT8 m16n8k32 and FP16 m16n8k16 with FP32
+ * accumulation; each of `ctas` CTAs of 256 threads runs iters x 8 MMAs per
+ * warp.  Kinds 2, 3, 4: tcgen05.mma kind::f16 with M = 128, K = 16 and N = 64,
+ * 128, 256 (shared-memory operands, FP32 accumulation in tensor memory); one
+ * thread of each of `ctas` CTAs issues iters x 8 of them (iters <= 2^20).
+ * scratch is 4 device bytes it may write (SAGE_FP4_ETIMEOUT when a tcgen05
+ * completion wait runs out). */
 int sagebwd_mma_peak(int kind, int ctas, int iters, void *scratch, void *stream);
 
 /* Failure-detection test: runs the forward attention (kernel 0; out0 = o,
@@ -136,6 +140,14 @@ int sagebwd_stall_test(int kernel, void *out0, void *out1, int B, int H, int N, 
  * row-major device arrays; N = 64 or 128).  status: a device int32 that a
  * wait that runs out sets to SAGE_FP4_ETIMEOUT. */
 int sagebwd_umma_probe(const uint16_t *a, const uint16_t *b, int N, float *c, int32_t *status, void *stream);
+
+/* Probe of the tensor-memory A operand (tcgen05.mma kind::f16 with A written to
+ * tensor memory by tcgen05.st, 128 rows in lanes, two FP16 values per 32-bit
+ * column, the lower K index in the low half; B 128-byte-swizzled K-major in
+ * shared memory): one CTA computes c [128][N] = a [128][64] x b [N][64]^T
+ * (FP16 in, FP32 out; row-major device arrays; N = 64 or 128).  status: a
+ * device int32 that a wait that runs out sets to SAGE_FP4_ETIMEOUT. */
+int sagebwd_umma_ta_probe(const uint16_t *a, const uint16_t *b, int N, float *c, int32_t *status, void *stream);
 
 /* Probe of the MN-major operand form dQ = dS^ K^ uses (tcgen05.mma kind::f16,
  * both operands stored with the K index as the 128-byte row, A's two 64-row

@@ -11,7 +11,7 @@ from bit_attention_gb300 import sagebwd as SB
 def test_library_exports_every_header_function():
     lib = SB.lib()
     names = SB.header_functions()
-    assert len(names) == 15
+    assert len(names) == 16
     text = open(SB._HEADER).read()
     decls = dict(re.findall(r"^(?:int|size_t)\s*(sagebwd_\w+)\(([^;]*)\);", text, re.M))
     assert set(decls) == set(names)
@@ -71,7 +71,9 @@ def test_fwd_and_bwd_reject_bad_arguments():
 
 
 def test_probe_and_status_argument_checks():
-    assert SB.sagebwd_mma_peak(2, 1, 1, 0x1000, None) == S.EINVAL
+    assert SB.sagebwd_mma_peak(5, 1, 1, 0x1000, None) == S.EINVAL
+    assert SB.sagebwd_mma_peak(-1, 1, 1, 0x1000, None) == S.EINVAL
+    assert SB.sagebwd_mma_peak(2, 1, (1 << 20) + 1, 0x1000, None) == S.EINVAL
     assert SB.sagebwd_mma_peak(0, 0, 1, 0x1000, None) == S.EINVAL
     assert SB.sagebwd_mma_peak(0, 1, 0, 0x1000, None) == S.EINVAL
     assert SB.sagebwd_get_status(0x1010, 1, 1, 128, 64, None) == S.EINVAL
@@ -80,6 +82,8 @@ def test_probe_and_status_argument_checks():
     assert SB.sagebwd_int_mma_probe(0x1000, 0x2000, 8192, 0x3000, None) == S.EINVAL
     assert SB.sagebwd_int_mma_probe(0x1001, 0x2000, 32, 0x3000, None) == S.EINVAL
     assert SB.sagebwd_umma_mn_probe(0x1001, 0x2000, 0x3000, 0x4000, None) == S.EINVAL
+    assert SB.sagebwd_umma_ta_probe(0x1000, 0x2000, 96, 0x3000, 0x4000, None) == S.EINVAL
+    assert SB.sagebwd_umma_ta_probe(0x1000, 0x2008, 64, 0x3000, 0x4000, None) == S.EINVAL
     assert SB.sagebwd_umma_mn_probe(0x1000, 0x2000, 0x3002, 0x4000, None) == S.EINVAL
     nb = SB.sagebwd_workspace_bytes(1, 2, 256, 64)
     st = SB.sagebwd_stall_test

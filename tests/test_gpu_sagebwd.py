@@ -214,6 +214,9 @@ def test_mma_peaks_are_measurable():
     f16 = SB.mma_peak_tops(1)
     print(f"mma.sync peaks: INT8 m16n8k32 {i8:.1f} TOP/s, FP16 m16n8k16 (FP32 acc) {f16:.1f} TFLOP/s")
     assert i8 > 0 and f16 > 0
+    tc = {n: SB.mma_peak_tops(kind, iters=2048) for kind, n in ((2, 64), (3, 128), (4, 256))}
+    print("tcgen05 kind::f16 M=128 K=16: " + ", ".join(f"N={n} {t:.0f} TFLOP/s" for n, t in tc.items()))
+    assert all(t > f16 for t in tc.values())
 
 
 @pytest.mark.parametrize("kernel,D", [(0, 64), (1, 64), (0, 128), (1, 128)])
@@ -245,6 +248,35 @@ def test_stalled_copy_sets_timeout_and_the_context_survives(kernel, D):
     torch.cuda.synchronize()
     assert ws2.get_status() == 0
     assert torch.equal(o2, o) and torch.equal(lse2, lse) and torch.equal(dk2, dk) and torch.equal(dv2, dv)
+
+
+@pytest.mark.parametrize("N", [64, 128])
+def test_tcgen05_f16_a_from_tensor_memory(N):
+    """tcgen05.mma kind::f16 with A written to tensor memory by tcgen05.st
+    (two FP16 values per column, the lower K index low) and B in shared
+    memory: integer codes give the exact integer product, FP16 values the
+    float64 product within FP32 accumulation."""
+    rng = np.random.default_rng(11 + N)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for kind in ("codes", "values"):
+        if kind == "codes":
+            a = rng.integers(-127, 128, size=(128, 64)).astype(np.float16)
+            b = rng.integers(-127, 128, size=(N, 64)).astype(np.float16)
+        else:
+            a = rng.standard_normal((128, 64)).astype(np.float16)
+            b = rng.standard_normal((N, 64)).astype(np.float16)
+        ad = torch.from_numpy(a.view(np.uint16).astype(np.int32)).to(torch.int16).cuda()
+        bd = torch.from_numpy(b.view(np.uint16).astype(np.int32)).to(torch.int16).cuda()
+        c = torch.full((128, N), float("nan"), dtype=torch.float32, device="cuda")
+        assert SB.sagebwd_umma_ta_probe(ad.data_ptr(), bd.data_ptr(), N, c.data_ptr(), status.data_ptr(), None) == 0
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        want = a.astype(np.float64) @ b.astype(np.float64).T
+        got = c.cpu().numpy().astype(np.float64)
+        if kind == "codes":
+            assert np.array_equal(got, want), np.abs(got - want).max()
+        else:
+            assert np.abs(got - want).max() <= 1e-5 * np.abs(want).max() + 1e-5
 
 
 def test_tcgen05_f16_mn_major_operands():
