@@ -1434,8 +1434,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 //   0  warp 0: bulk copies; warp 1: tensor-memory allocation and MMA issue
 //   1, 2  softmax: each thread owns one query row and 64 of the tile's 128
 //      keys; the row maximum and the 64-row block maxima are exchanged
-//      through shared memory; P~'s INT8 codes go to shared memory as the A
-//      operand of PV (each warpgroup writes one 64-key slab)
+//      through shared memory; P~'s INT8 codes go to tensor memory (tcgen05.st)
+//      as the A operand of PV, each warpgroup writing its 64 keys
 //   3  correction: O in registers, rescaled by each row's factor and
 //      accumulated with each tile's PV times its block scales; the epilogue
 // P~ blocks are 64 query rows x 128 keys, as in the warp-level forward.
@@ -1444,9 +1444,7 @@ struct TfSmem {
   static constexpr int kStageOff = 16384;
   static constexpr int kSK = 0, kSV = 16384;      // K^ [128][64]; V^T [2][64 d][64 keys]
   static constexpr int kStage = 32768;
-  static constexpr int kPOff = kStageOff + kTcStages * kStage;  // P^ [2 bufs][2 key slabs][128][64]
-  static constexpr int kP = 32768;
-  static constexpr int kBarOff = kPOff + 2 * kP;
+  static constexpr int kBarOff = kStageOff + kTcStages * kStage;
   static constexpr int kMiscOff = kBarOff + 8 * 32;
   // misc: tmem slot, abort, row max halves [2 parity][2][128], alpha [2][128],
   // block max [2 parity][8 warps], beta [2][2], final l halves [2][128], m [128]
@@ -1462,14 +1460,14 @@ enum {
   FB_SDONE = 1 + 2 * kTcStages,  // + buffer
   FB_SFREE = FB_SDONE + 2,
   FB_PFULL = FB_SFREE + 2,
-  FB_PEMPTY = FB_PFULL + 2,
-  FB_PVDONE = FB_PEMPTY + 2,
+  FB_PVDONE = FB_PFULL + 2,
   FB_PVFREE = FB_PVDONE + 2,
   FB_DRAIN = FB_PVFREE + 2,
   FB_COUNT
 };
 static_assert(FB_COUNT <= 32, "barriers");
-constexpr uint32_t kTfS = 0, kTfPv = 256;
+// tensor-memory columns: S (FP32) [2][128], P^ (FP16 pairs) [2][64], PV (FP32) [2][64]
+constexpr uint32_t kTfS = 0, kTfP = 256, kTfPv = 384;
 
 template <bool kCausal>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -1508,7 +1506,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar(FB_SDONE + b), 1);
       mbar_init(bar(FB_SFREE + b), 8);
       mbar_init(bar(FB_PFULL + b), 8);
-      mbar_init(bar(FB_PEMPTY + b), 1);
       mbar_init(bar(FB_PVDONE + b), 1);
       mbar_init(bar(FB_PVFREE + b), 4);
     }
@@ -1580,16 +1577,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!(ok = wait1_ab(bar(FB_PFULL + b), (kt >> 1) & 1, ctl, abort))) break;
         if (kt >= 2 && !(ok = wait1_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort))) break;
         tc_fence_after();
-        // P^ key slabs 16 KB apart (+1024), V^T key halves 8 KB apart (+512)
-        const uint64_t dpb = desc_k64(sbase + L::kPOff + b * L::kP, 0);
+        // P^ from tensor memory (8 columns a K step); V^T key halves 8 KB apart (+512)
         const uint64_t dvs = desc_k64(sbase + L::kStageOff + s * L::kStage + L::kSV, 0);
 #pragma unroll
         for (int k = 0; k < 8; k++)
-          mma_f16_tc(tmem + kTfPv + 64 * b, dpb + 1024 * (k >> 2) + 2 * (k & 3), dvs + 512 * (k >> 2) + 2 * (k & 3),
-                     idPV, k > 0);
+          mma_f16_tc_ta(tmem + kTfPv + 64 * b, tmem + kTfP + 64 * b + 8 * k, dvs + 512 * (k >> 2) + 2 * (k & 3), idPV,
+                        k > 0);
         tc_commit(bar(FB_PVDONE + b));
         tc_commit(bar(FB_EMPTY + s));
-        tc_commit(bar(FB_PEMPTY + b));
       }
       tc_commit(bar(FB_DRAIN));
       const uint64_t t0 = globaltimer_ns();
@@ -1655,9 +1650,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // the row's maximum over both halves of the tile (xm by tile parity)
       xm[(2 * b + h) * 128 + row] = hm;
-      // P buffer b: PV of tile kt - 2 has read it; alpha and beta of buffer b:
-      // the correction has read them
-      ok = ok && (kt < 2 || waitw_ab(bar(FB_PEMPTY + b), ((kt >> 1) - 1) & 1, ctl, abort));
+      // alpha, beta and the P^ buffer b: the correction has read tile kt - 2's
+      // alpha and beta and, after PV of tile kt - 2 completed, its product
       ok = ok && (kt < 2 || waitw_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort));
       if (!group_and(ok)) break;  // also publishes xm
       const float mt = fmaxf(hm, xm[(2 * b + 1 - h) * 128 + row]);
@@ -1668,48 +1662,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       m = mn;
       // The block's largest P~ is the largest of its rows' maxima, each the
       // exponential of the same argument as the row's largest score (rows past
-      // N excluded); both halves of a row compute it alike.
+      // N excluded); both halves of a row compute it alike, so each half takes
+      // the block maximum over its own two warps.
       const float rp = valid ? ex2(fmaf(mt, c2, -mn)) : 0.0f;
       const uint32_t wmax = redux_max_u32(__float_as_uint(rp));  // rp >= 0: bit order is value order
       if (lane == 0) bm[b * 8 + sw] = __uint_as_float(wmax);
       if (h == 0) al[b * 128 + row] = alpha;
-      const uint64_t c22 = pack2(c2, c2), nm2 = pack2(-mn, -mn);
-      uint64_t acc0 = 0, acc1 = 0;
-#pragma unroll
-      for (int j = 0; j < 32; j++) {
-        uint32_t* r = &ru[j >> 4][(j & 15) * 2];
-        const uint64_t y = fma2(pack2(__uint_as_float(r[0]), __uint_as_float(r[1])), c22, nm2);
-        const float x0 = ex2(lo2(y)), x1 = ex2(hi2(y));
-        r[0] = __float_as_uint(x0);
-        r[1] = __float_as_uint(x1);
-        if (j & 1)
-          acc1 = add2(acc1, pack2(x0, x1));
-        else
-          acc0 = add2(acc0, pack2(x0, x1));
-      }
-      const uint64_t acc = add2(acc0, acc1);
-      l = fmaf(l, alpha, lo2(acc) + hi2(acc));
       named_bar(3 + 2 * h + blk, 64);  // publishes bm to the block's other warp of this half
       const float amax = fmaxf(bm[b * 8 + 4 * h + 2 * blk], bm[b * 8 + 4 * h + 2 * blk + 1]);
       const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
       if (h == 0 && wq == 2 * blk && lane == 0) beta[b * 2 + blk] = __fdiv_rn(amax, 127.0f) * sv_cur;
-      uint8_t* pbuf = smem + L::kPOff + b * L::kP + h * 16384;
-      const uint64_t ii = pack2(inv, inv);
+      // one pass: P~ = exp2(s c2 - m), its row sum, and its codes
+      // rint(P~ * inv) (the product rounded to FP32, then to an integer by
+      // adding and subtracting 1.5 * 2^23, exact below 2^22)
+      const uint64_t c22 = pack2(c2, c2), nm2 = pack2(-mn, -mn), ii = pack2(inv, inv);
+      uint64_t acc0 = 0, acc1 = 0;
+      uint32_t pw[32];  // keys 2j, 2j + 1 of this half as FP16 codes
 #pragma unroll
-      for (int ch = 0; ch < 8; ch++) {
-        uint32_t wv[4];
-#pragma unroll
-        for (int u = 0; u < 4; u++) {
-          const uint32_t* r = &ru[ch >> 2][(ch & 3) * 8 + 2 * u];
-          // rint(x * inv): the product rounded to FP32, then to an integer by
-          // adding and subtracting 1.5 * 2^23 (exact below 2^22)
-          const uint64_t z = mul2(pack2(__uint_as_float(r[0]), __uint_as_float(r[1])), ii);
-          const uint64_t n = add2(add2(z, magic2), nmagic2);
-          wv[u] = h2(lo2(n), hi2(n));
-        }
-        *reinterpret_cast<uint4*>(pbuf + swz(row, 16 * ch, 128)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      for (int j = 0; j < 32; j++) {
+        const uint32_t* r = &ru[j >> 4][(j & 15) * 2];
+        const uint64_t y = fma2(pack2(__uint_as_float(r[0]), __uint_as_float(r[1])), c22, nm2);
+        const uint64_t x = pack2(ex2(lo2(y)), ex2(hi2(y)));
+        if (j & 1)
+          acc1 = add2(acc1, x);
+        else
+          acc0 = add2(acc0, x);
+        const uint64_t n = add2(add2(mul2(x, ii), magic2), nmagic2);
+        pw[j] = h2(lo2(n), hi2(n));
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      const uint64_t acc = add2(acc0, acc1);
+      l = fmaf(l, alpha, lo2(acc) + hi2(acc));
+      tmem_st32(tmem + lanebase + kTfP + 64 * b + 32 * h, pw);
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive1(bar(FB_PFULL + b));
     }
