@@ -931,7 +931,8 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int k0, uint32_t bloc
 //      tiles' scales, to the FP32 accumulator in global memory by tensor
 //      reductions of the copy engine (staged 32 rows x 32 columns a warp)
 // Tensor memory: S^T and dP^T double-buffered, the dV and dK partials and dQ
-// single (448 of 512 columns).  Every wait is bounded; a wait that runs out
+// single, and the resident K^ and V as the A operands of S^T and dP^T (512
+// columns); dV and dK read dO^ and Q^ MN-major from their row tiles.  Every wait is bounded; a wait that runs out
 // sets the status word and an abort flag that ends every role's loop.
 constexpr int kTcThreads = 512;
 constexpr int kTcStages = 3;
@@ -945,9 +946,9 @@ struct TcSmem {
   static constexpr int kK = 0;             // K^ codes [128 keys][64]
   static constexpr int kV = kTile;         // FP16 V [128 keys][64]
   static constexpr int kStageOff = 2 * kTile;
-  // stage: Q^ [64 q][64], FP16 dO [64 q][64], Q^T [64 d][64 q], dO^T [64 d][64 q], L, D
-  static constexpr int kSQ = 0, kSDoh = 8192, kSQt = 16384, kSDot = 24576, kSL = 32768, kSD = 33024;
-  static constexpr int kStage = 33792;  // a multiple of 1024
+  // stage: Q^ [64 q][64], FP16 dO [64 q][64], dO^ [64 q][64], -L, D
+  static constexpr int kSQ = 0, kSDoh = 8192, kSDoc = 16384, kSL = 24576, kSD = 24832;
+  static constexpr int kStage = 25600;  // a multiple of 1024
   static constexpr int kCodesOff = kStageOff + kTcStages * kStage;
   // codes buffer: P^T [128 keys][64 q], dS^T [128 keys][64 q]
   static constexpr int kCP = 0, kCS = kTile, kCodes = 2 * kTile;
@@ -972,12 +973,13 @@ enum {
   TB_PFREE = TB_PDONE + 1,
   TB_QDONE = TB_PFREE + 1,   // dQ of a tile pair (single buffer)
   TB_QFREE = TB_QDONE + 1,
-  TB_DRAIN = TB_QFREE + 1,
+  TB_KVT = TB_QFREE + 1,     // K^ and V copied into tensor memory
+  TB_DRAIN = TB_KVT + 1,
   TB_COUNT
 };
 static_assert(TB_COUNT <= TcSmem::kNumBars, "barriers");
 // tensor-memory columns
-constexpr uint32_t kTcS = 0, kTcDp = 128, kTcDv = 256, kTcDk = 320, kTcDq = 384;
+constexpr uint32_t kTcS = 0, kTcDp = 128, kTcDv = 256, kTcDk = 320, kTcDq = 384, kTcK = 448, kTcV = 480;
 
 // Bounded warp-wide wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool waitw_ab(uint32_t bar, uint32_t parity, const Ctl& c, volatile int* abort) {
@@ -1083,6 +1085,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(bar(TB_PFREE), 4);
     mbar_init(bar(TB_QDONE), 1);
     mbar_init(bar(TB_QFREE), 4);
+    mbar_init(bar(TB_KVT), 4);
     mbar_init(bar(TB_DRAIN), 1);
     *abort = 0;
     mbar_fence_init();
@@ -1113,11 +1116,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int qtile = q0 + it;
         const uint32_t st = sbase + L::kStageOff + s * L::kStage;
         const size_t qo = hb + static_cast<size_t>(qtile) * kQ * D;
-        mbar_arrive_expect_tx(bar(TB_FULL + s), 4 * 8192 + 512);
+        mbar_arrive_expect_tx(bar(TB_FULL + s), 3 * 8192 + 512);
         bulk_load(st + L::kSQ, ws.qc + qo, 8192, bar(TB_FULL + s));
         bulk_load(st + L::kSDoh, ws.doh + qo, 8192, bar(TB_FULL + s));
-        bulk_load(st + L::kSQt, ws.qct + qo, 8192, bar(TB_FULL + s));
-        bulk_load(st + L::kSDot, ws.doct + qo, 8192, bar(TB_FULL + s));
+        bulk_load(st + L::kSDoc, ws.doc + qo, 8192, bar(TB_FULL + s));
         bulk_load(st + L::kSL, ws.l2 + hrow + static_cast<size_t>(qtile) * kQ, 256, bar(TB_FULL + s));
         bulk_load(st + L::kSD, ws.dd + hrow + static_cast<size_t>(qtile) * kQ, 256, bar(TB_FULL + s));
         issued = it + 1;
@@ -1137,11 +1139,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     } else if (warp == 1 && lane == 0) {
       // ---- MMA issue
-      const uint32_t id = idesc_f16(128, 64), idq = idesc_f16_mn(128, 64);
-      const uint64_t dk0 = desc_k64(sbase + L::kK, 0), dv0 = desc_k64(sbase + L::kV, 0);
+      // B MN-major for dV and dK (dO^ and Q^ as [64 q][64 d] rows)
+      const uint32_t id = idesc_f16(128, 64), idb = idesc_f16(128, 64) | (1u << 16), idq = idesc_f16_mn(128, 64);
       // dQ = dS^ K^, MN-major: a K step of 16 rows moves 2048 bytes (+128)
       const uint64_t dqa = desc_mn(sbase + L::kCodesOff + L::kCS, 0, L::kCodes), dqb = desc_mn(sbase + L::kK, 0, L::kCodes);
-      bool ok = wait1_ab(bar(TB_FIXED), 0, ctl, abort);
+      bool ok = wait1_ab(bar(TB_FIXED), 0, ctl, abort) && wait1_ab(bar(TB_KVT), 0, ctl, abort);
       auto issue_sdp = [&](int it) {
         const int s = it % kTcStages, b = it & 1;
         if (!wait1_ab(bar(TB_FULL + s), (it / kTcStages) & 1, ctl, abort)) return false;
@@ -1151,9 +1153,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // descriptors built once per operand; a K step of 16 moves 32 bytes (+2)
         const uint64_t dq = desc_k64(st + L::kSQ, 0), ddo = desc_k64(st + L::kSDoh, 0);
 #pragma unroll
-        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcS + 64 * b, dk0 + 2 * k, dq + 2 * k, id, k > 0);
+        for (int k = 0; k < 4; k++) mma_f16_tc_ta(tmem + kTcS + 64 * b, tmem + kTcK + 8 * k, dq + 2 * k, id, k > 0);
 #pragma unroll
-        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcDp + 64 * b, dv0 + 2 * k, ddo + 2 * k, id, k > 0);
+        for (int k = 0; k < 4; k++) mma_f16_tc_ta(tmem + kTcDp + 64 * b, tmem + kTcV + 8 * k, ddo + 2 * k, id, k > 0);
         tc_commit(bar(TB_SDONE + b));
         return true;
       };
@@ -1162,22 +1164,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int s = it % kTcStages, b = it & 1;
         if (it + 1 < niter && !(ok = issue_sdp(it + 1))) break;
         if (!(ok = wait1_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort))) break;
-        // the partials' buffer: the fold has read the previous tile's
-        if (it >= 1 && !(ok = wait1_ab(bar(TB_PFREE), (it - 1) & 1, ctl, abort))) break;
-        tc_fence_after();
-        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
-        const uint32_t cb = sbase + L::kCodesOff + b * L::kCodes;
-        const uint64_t dp = desc_k64(cb + L::kCP, 0), dds = desc_k64(cb + L::kCS, 0);
-        const uint64_t ddot = desc_k64(st + L::kSDot, 0), dqt = desc_k64(st + L::kSQt, 0);
-#pragma unroll
-        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcDv, dp + 2 * k, ddot + 2 * k, id, k > 0);
-#pragma unroll
-        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcDk, dds + 2 * k, dqt + 2 * k, id, k > 0);
-        tc_commit(bar(TB_PDONE));
-        tc_commit(bar(TB_EMPTY + s));
         if (b == 1) {
-          // dQ of the pair (it - 1, it): rows 0..63 from codes buffer 0, rows
-          // 64..127 from buffer 1; the fold has read the previous pair's dQ
+          // dQ of the pair (it - 1, it) first -- rows 0..63 from codes buffer
+          // 0, rows 64..127 from buffer 1 -- so that buffer 0 (its dV and dK
+          // were issued before) is released for the next tile's codes; the
+          // fold has read the previous pair's dQ
           const int pr = it >> 1;
           if (pr >= 1 && !(ok = wait1_ab(bar(TB_QFREE), (pr - 1) & 1, ctl, abort))) break;
           tc_fence_after();
@@ -1185,8 +1176,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int k = 0; k < 8; k++) mma_f16_tc(tmem + kTcDq, dqa + 128 * k, dqb + 128 * k, idq, k > 0);
           tc_commit(bar(TB_QDONE));
           tc_commit(bar(TB_CEMPTY + 0));
-          tc_commit(bar(TB_CEMPTY + 1));
         }
+        // the partials' buffer: the fold has read the previous tile's
+        if (it >= 1 && !(ok = wait1_ab(bar(TB_PFREE), (it - 1) & 1, ctl, abort))) break;
+        tc_fence_after();
+        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+        const uint32_t cb = sbase + L::kCodesOff + b * L::kCodes;
+        const uint64_t dp = desc_k64(cb + L::kCP, 0), dds = desc_k64(cb + L::kCS, 0);
+        const uint64_t ddoc = desc_mn(st + L::kSDoc, 0, 8192), dqm = desc_mn(st + L::kSQ, 0, 8192);
+#pragma unroll
+        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcDv, dp + 2 * k, ddoc + 128 * k, idb, k > 0);
+#pragma unroll
+        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcDk, dds + 2 * k, dqm + 128 * k, idb, k > 0);
+        tc_commit(bar(TB_PDONE));
+        tc_commit(bar(TB_EMPTY + s));
+        if (b == 1) tc_commit(bar(TB_CEMPTY + 1));  // after dV and dK have read buffer 1
       }
       // every MMA issued has completed before tensor memory is released
       tc_commit(bar(TB_DRAIN));
@@ -1273,21 +1277,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       smax = fmaxf(smax, -smin);
       __syncwarp();
       if (lane == 0) mbar_arrive1(bar(TB_EMPTY + s));  // L and D read
-      pmax = warp_max(pmax);
-      smax = warp_max(smax);
+      // both maxima are >= 0 (or -0): the warp maximum of their bit patterns
+      // with the sign bit cleared
+      const uint32_t pm = redux_max_u32(__float_as_uint(pmax) & 0x7fffffffu);
+      const uint32_t sm = redux_max_u32(__float_as_uint(smax) & 0x7fffffffu);
       if (lane == 0) {
-        red[(b * 2 + 0) * 8 + sw] = pmax;
-        red[(b * 2 + 1) * 8 + sw] = smax;
+        red[(b * 2 + 0) * 8 + sw] = __uint_as_float(pm);
+        red[(b * 2 + 1) * 8 + sw] = __uint_as_float(sm);
       }
       // the codes buffer is free once dV, dK (tile it - 2) and the pair's dQ have read it
       ok = ok && (it < 2 || waitw_ab(bar(TB_CEMPTY + b), ((it >> 1) - 1) & 1, ctl, abort));
       if (!group_and(ok)) break;  // also publishes red[]
-      float pa = red[(b * 2) * 8], sa = red[(b * 2 + 1) * 8];
-#pragma unroll
-      for (int w = 1; w < 8; w++) {
-        pa = fmaxf(pa, red[(b * 2) * 8 + w]);
-        sa = fmaxf(sa, red[(b * 2 + 1) * 8 + w]);
-      }
+      const float4* r4 = reinterpret_cast<const float4*>(red + b * 16);
+      const float4 p0 = r4[0], p1 = r4[1], s0 = r4[2], s1 = r4[3];
+      const float pa = fmaxf(max3f(max3f(p0.x, p0.y, p0.z), max3f(p0.w, p1.x, p1.y), p1.z), p1.w);
+      const float sa = fmaxf(max3f(max3f(s0.x, s0.y, s0.z), max3f(s0.w, s1.x, s1.y), s1.z), s1.w);
       const float pinv = pa > 0.0f ? __fdiv_rn(127.0f, pa) : 0.0f;
       const float sinv = sa > 0.0f ? __fdiv_rn(127.0f, sa) : 0.0f;
       uint8_t* cbuf = smem + L::kCodesOff + b * L::kCodes;
@@ -1334,7 +1338,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
     for (int i = 0; i < 32; i++) accv[i] = acck[i] = 0;
     float fq[2] = {0.0f, 0.0f};  // dQ scales of the pair's two tiles
-    for (int it = 0; it < niter; it++) {
+    // K^ and V rows (this thread's key) into tensor memory, the A operands of
+    // S^T and dP^T for the CTA's whole life
+    bool kv_ok = waitw_ab(bar(TB_FIXED), 0, ctl, abort);
+    if (kv_ok) {
+#pragma unroll
+      for (int which = 0; which < 2; which++) {
+        uint32_t w[32];
+        const uint8_t* src = smem + (which == 0 ? L::kK : L::kV);
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+          const uint4 v4 = *reinterpret_cast<const uint4*>(src + swz(row, 16 * c, 128));
+          w[4 * c] = v4.x;
+          w[4 * c + 1] = v4.y;
+          w[4 * c + 2] = v4.z;
+          w[4 * c + 3] = v4.w;
+        }
+        tmem_st32(tmem + lanebase + (which == 0 ? kTcK : kTcV), w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(TB_KVT));
+    }
+    for (int it = 0; kv_ok && it < niter; it++) {
       const int b = it & 1;
       // CFULL: this tile's block scales are written
       if (!waitw_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort)) break;
@@ -1665,7 +1692,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // N excluded); both halves of a row compute it alike, so each half takes
       // the block maximum over its own two warps.
       const float rp = valid ? ex2(fmaf(mt, c2, -mn)) : 0.0f;
-      const uint32_t wmax = redux_max_u32(__float_as_uint(rp));  // rp >= 0: bit order is value order
+      const uint32_t wmax = redux_max_u32(__float_as_uint(rp) & 0x7fffffffu);  // rp >= 0: bit order is value order
       if (lane == 0) bm[b * 8 + sw] = __uint_as_float(wmax);
       if (h == 0) al[b * 128 + row] = alpha;
       named_bar(3 + 2 * h + blk, 64);  // publishes bm to the block's other warp of this half
