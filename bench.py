@@ -57,9 +57,12 @@ SAGEBWD_CALLS = ("quantize_qkv", "attn_fwd", "bwd_prep", "attn_bwd", "dq_out")
 ATTN_TRAFFIC = {
     "attn_fwd B4 H32 N4096 D128 k-channel-outliers": 113.32e6 + 80.14e6,
 }
-# the same for one SageBwd dkdv_kernel launch (attn_bwd), one ncu capture
+# the same for one SageBwd attn_bwd launch (dkdv_tc_kernel at D = 64), from one
+# ncu capture of the half-head case (B1 H16 N8192 D64 causal: 118.55 MB read,
+# 27.35 MB written) scaled by the heads (the traffic is per head)
 SAGEBWD_BWD_TRAFFIC = {
-    "attn_train B1 H32 N8192 D64 causal iid": 237.57e6 + 96.61e6,
+    "attn_train B1 H32 N8192 D64 causal iid": 2 * (118.55e6 + 27.35e6),
+    "attn_train B1 H16 N8192 D64 causal iid": 118.55e6 + 27.35e6,
 }
 
 
@@ -358,17 +361,30 @@ class SageBwdRun:
         return ev[0][0].elapsed_time(ev[-1][-1]), per
 
 
-def sagebwd_summary(w, per, fp16_peak):
+def sagebwd_peak(w, fp16_mma_peak):
+    """The tensor peak the SageBwd attention kernels of workload w are judged
+    against: at D = 64 they issue tcgen05.mma kind::f16 (the measured dense
+    16-bit GEMM peak; FP16 and BF16 share the nominal rate), at D = 128 the
+    warp-level FP16 mma.sync (its measured rate)."""
+    if w.D == 64:
+        pk = peaks()
+        return pk["bf16_tflops"], f"{pk['src']} bf16 GEMM (burst), the tcgen05 kind::f16 rate"
+    return fp16_mma_peak, "measured live: FP16 mma.sync m16n8k16 (FP32 accumulate) probe, the instruction issued"
+
+
+def sagebwd_summary(w, per, fp16_mma_peak):
     """Per-call means and the roofline figures of the two attention kernels."""
     m = {nm: statistics.mean(v) for nm, v in per.items()}
     ops = w.ops
     fwd_tops = ops / (m["attn_fwd"] * 1e-3) / 1e12
     bwd_tops = 2.5 * ops / (m["attn_bwd"] * 1e-3) / 1e12
     step = sum(m.values())
+    peak, src = sagebwd_peak(w, fp16_mma_peak)
     return {"workload": w.name, "ms": m, "ms_per_step": step,
             "attn_fwd_tops": fwd_tops, "attn_bwd_tops": bwd_tops,
-            "attn_fwd_frac_of_fp16_mma": fwd_tops / fp16_peak,
-            "attn_bwd_frac_of_fp16_mma": bwd_tops / fp16_peak,
+            "peak_tflops": peak, "peak_src": src,
+            "attn_fwd_frac_of_peak": fwd_tops / peak,
+            "attn_bwd_frac_of_peak": bwd_tops / peak,
             "step_tops": 3.5 * ops / (step * 1e-3) / 1e12}
 
 
@@ -486,13 +502,12 @@ def run_sagebwd(args, world, rank, local):
             "config": dict(w.describe(), l2="bf16 inputs 4x32 MiB+ per tensor set; no flush",
                            parallelism=f"weak, {world} independent batch(es)"),
             "kernels": summ,
-            "roofline": {"bound": "tensor", "kernel": "attn_bwd (dkdv_kernel)",
-                         "achieved": summ["attn_bwd_tops"], "peak": fp16_peak, "unit": "TFLOP/s",
-                         "frac": summ["attn_bwd_frac_of_fp16_mma"], "traffic": SAGEBWD_BWD_TRAFFIC.get(w.name),
+            "roofline": {"bound": "tensor",
+                         "kernel": "attn_bwd (" + ("dkdv_tc_kernel" if w.D == 64 else "dkdv_kernel") + ")",
+                         "achieved": summ["attn_bwd_tops"], "peak": summ["peak_tflops"], "unit": "TFLOP/s",
+                         "frac": summ["attn_bwd_frac_of_peak"], "traffic": SAGEBWD_BWD_TRAFFIC.get(w.name),
                          "traffic_unit": "DRAM bytes (read + write) per attn_bwd launch, from ncu",
-                         "peak_src": "measured live: FP16 mma.sync m16n8k16 (FP32 accumulate) probe, "
-                                     "the instruction the kernels issue",
-                         "bf16_tcgen05_measured_tflops": peaks()["bf16_tflops"]},
+                         "peak_src": summ["peak_src"], "fp16_mma_sync_measured_tflops": fp16_peak},
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk.summary(),
             "gpu_launches": len(SAGEBWD_CALLS) * args.steps}), flush=True)
 

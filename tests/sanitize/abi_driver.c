@@ -158,7 +158,17 @@ int main(void) {
            "sagebwd stall test, limit too short");
     expect(sagebwd_int_mma_probe((const int8_t *)P(0x1000), (const int8_t *)P(0x2000), 20, (float *)P(0x3000), NULL),
            SAGE_FP4_EINVAL, "sagebwd probe K = 20");
-    expect(sagebwd_mma_peak(3, 1, 1, P(0x1000), NULL), SAGE_FP4_EINVAL, "sagebwd peak kind");
+    expect(sagebwd_mma_peak(5, 1, 1, P(0x1000), NULL), SAGE_FP4_EINVAL, "sagebwd peak kind");
+    expect(sagebwd_mma_peak(2, 1, (1 << 20) + 1, P(0x1000), NULL), SAGE_FP4_EINVAL, "sagebwd peak iterations");
+    expect(sagebwd_umma_probe((const uint16_t *)P(0x1000), (const uint16_t *)P(0x2000), 96, (float *)P(0x3000),
+                              (int32_t *)P(0x4000), NULL),
+           SAGE_FP4_EINVAL, "sagebwd tcgen05 probe N = 96");
+    expect(sagebwd_umma_mn_probe((const uint16_t *)P(0x1001), (const uint16_t *)P(0x2000), (float *)P(0x3000),
+                                 (int32_t *)P(0x4000), NULL),
+           SAGE_FP4_EINVAL, "sagebwd MN-major probe misaligned a");
+    expect(sagebwd_umma_ta_probe((const uint16_t *)P(0x1000), (const uint16_t *)P(0x2008), 64, (float *)P(0x3000),
+                                 (int32_t *)P(0x4000), NULL),
+           SAGE_FP4_EINVAL, "sagebwd tensor-memory probe misaligned b");
   }
 
   /* every status code has a string */
