@@ -47,7 +47,8 @@ HBM_NOMINAL_GBS = 8000.0  # the "~8 TB/s" HBM3e figure the quantize target is qu
 
 
 TRAIN_METRIC = ("SageBwd 8-bit attention fwd+bwd TOPS (3.5*4*B*H*N^2*D/t, causal at half) on 1 GB300; "
-                "% of the measured FP16 mma.sync peak")
+                "fraction of the measured 16-bit tensor peak of the instruction issued (D=64: tcgen05, "
+                "D=128: mma.sync)")
 SAGEBWD_CALLS = ("quantize_qkv", "attn_fwd", "bwd_prep", "attn_bwd", "dq_out")
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one attn_fwd_kernel launch,
