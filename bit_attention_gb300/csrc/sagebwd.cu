@@ -1243,7 +1243,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool edge = (kCausal && qtile <= 2 * kb + 1) || (qtile * kQ + kQ > N) || (kb * kTok + kTok > N);
       // (pairs of columns through the packed FP32 forms, each lane rounded
       // like its scalar form; Ls holds -L)
-      float pmax = 0.0f, smax = 0.0f, smin = 0.0f;
+      float pmax = 0.0f, smax = 0.0f;
       const uint64_t cc = pack2(c2, c2);
 #pragma unroll
       for (int q4 = 0; q4 < 8; q4++) {
@@ -1271,10 +1271,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         dp[q + 2] = lo2(s23);
         dp[q + 3] = hi2(s23);
         pmax = max3f(pmax, max3f(v[0], v[1], v[2]), v[3]);
-        smax = max3f(smax, max3f(dp[q], dp[q + 1], dp[q + 2]), dp[q + 3]);
-        smin = fminf(fminf(smin, fminf(dp[q], dp[q + 1])), fminf(dp[q + 2], dp[q + 3]));
+        smax = max3f(smax, max3f(fabsf(dp[q]), fabsf(dp[q + 1]), fabsf(dp[q + 2])), fabsf(dp[q + 3]));
       }
-      smax = fmaxf(smax, -smin);
       __syncwarp();
       if (lane == 0) mbar_arrive1(bar(TB_EMPTY + s));  // L and D read
       // both maxima are >= 0 (or -0): the warp maximum of their bit patterns
@@ -1296,11 +1294,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float sinv = sa > 0.0f ? __fdiv_rn(127.0f, sa) : 0.0f;
       uint8_t* cbuf = smem + L::kCodesOff + b * L::kCodes;
       const uint64_t pp = pack2(pinv, pinv), ss = pack2(sinv, sinv);
-      // rint(x * inv) for a pair, as FP16x2: the products rounded per lane to
-      // FP32, then to integers by adding and subtracting 1.5 * 2^23 (exact)
+      // rint(x * inv) for a pair, as FP16x2: x * inv + 1.5 * 2^23 in one FMA
+      // rounds the exact product to an integer (ties to even), and
+      // subtracting 1.5 * 2^23 is exact
       const uint64_t magic2 = pack2(kRintMagic, kRintMagic), nmagic2 = pack2(-kRintMagic, -kRintMagic);
       auto code2 = [&](float a, float b, uint64_t inv2) {
-        const uint64_t y = add2(add2(mul2(pack2(a, b), inv2), magic2), nmagic2);
+        const uint64_t y = add2(fma2(pack2(a, b), inv2, magic2), nmagic2);
         return h2(lo2(y), hi2(y));
       };
 #pragma unroll
@@ -1700,8 +1699,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
       if (h == 0 && wq == 2 * blk && lane == 0) beta[b * 2 + blk] = __fdiv_rn(amax, 127.0f) * sv_cur;
       // one pass: P~ = exp2(s c2 - m), its row sum, and its codes
-      // rint(P~ * inv) (the product rounded to FP32, then to an integer by
-      // adding and subtracting 1.5 * 2^23, exact below 2^22)
+      // rint(P~ * inv): P~ * inv + 1.5 * 2^23 in one FMA rounds the exact
+      // product to an integer (ties to even), and subtracting 1.5 * 2^23 is
+      // exact
       const uint64_t c22 = pack2(c2, c2), nm2 = pack2(-mn, -mn), ii = pack2(inv, inv);
       uint64_t acc0 = 0, acc1 = 0;
       uint32_t pw[32];  // keys 2j, 2j + 1 of this half as FP16 codes
@@ -1714,7 +1714,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           acc1 = add2(acc1, x);
         else
           acc0 = add2(acc0, x);
-        const uint64_t n = add2(add2(mul2(x, ii), magic2), nmagic2);
+        const uint64_t n = add2(fma2(x, ii, magic2), nmagic2);
         pw[j] = h2(lo2(n), hi2(n));
       }
       const uint64_t acc = add2(acc0, acc1);

@@ -24,6 +24,10 @@
  *   INT8      symmetric per block: scale = amax / 127, code =
  *             rint(x * (127 / amax)) in float arithmetic.  Q, K, V and dO are
  *             quantized per head in blocks of 128 tokens over all D channels.
+ *             Inside the attention kernels P's and dS's codes round the exact
+ *             product x * (127 / amax) (one fused multiply-add); that differs
+ *             from rounding the FP32 product only when the product lies within
+ *             half an FP32 unit in the last place of a half-integer.
  *             The INT8 products run on the FP16 tensor path with the codes
  *             held as FP16 values: integer codes, exact products and exact
  *             integer sums (below 2^24), the results of an INT8 MMA, at the
