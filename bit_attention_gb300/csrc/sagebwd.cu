@@ -894,6 +894,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
 
 __device__ __forceinline__ uint64_t desc_k64(uint32_t tile, int k0) {
   return smem_desc(tile + 2 * k0, 16, 1024, kSwizzle128B);
@@ -924,15 +932,17 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int k0, uint32_t bloc
 //   1, 2  softmax: each thread owns one key row and half of the tile's 64
 //      query columns; P^T and dS^T from the S^T and dP^T rows in tensor
 //      memory, their block maxima (one vote of the eight warps each), their
-//      INT8 codes written to shared memory as the A operands of dV and dK
-//      (and dS^T read again by dQ)
+//      INT8 codes written back over S^T and dP^T in tensor memory as the A
+//      operands of dV and dK, and dS^T's also to shared memory for dQ
 //   3  folds each tile's dV and dK partials (tensor memory) into registers
 //      with the tile's block scales, and adds each tile pair's dQ, times its
 //      tiles' scales, to the FP32 accumulator in global memory by tensor
 //      reductions of the copy engine (staged 32 rows x 32 columns a warp)
-// Tensor memory: S^T and dP^T double-buffered, the dV and dK partials and dQ
-// single, and the resident K^ and V as the A operands of S^T and dP^T (512
-// columns); dV and dK read dO^ and Q^ MN-major from their row tiles.  Every wait is bounded; a wait that runs out
+// Tensor memory: S^T and dP^T double-buffered (then P^^T and dS^^T in their
+// first 32 columns), the dV and dK partials and dQ single, and the resident K^
+// and V as the A operands of S^T and dP^T (512 columns); dV and dK read dO^
+// and Q^ MN-major from their row tiles.  S^T and dP^T of tile t + 2 are issued
+// once dV and dK of tile t have completed.  Every wait is bounded; a wait that runs out
 // sets the status word and an abort flag that ends every role's loop.
 constexpr int kTcThreads = 512;
 constexpr int kTcStages = 3;
@@ -950,8 +960,8 @@ struct TcSmem {
   static constexpr int kSQ = 0, kSDoh = 8192, kSDoc = 16384, kSL = 24576, kSD = 24832;
   static constexpr int kStage = 25600;  // a multiple of 1024
   static constexpr int kCodesOff = kStageOff + kTcStages * kStage;
-  // codes buffer: P^T [128 keys][64 q], dS^T [128 keys][64 q]
-  static constexpr int kCP = 0, kCS = kTile, kCodes = 2 * kTile;
+  // codes buffer: dS^T [128 keys][64 q] (dQ's A operand, read MN-major)
+  static constexpr int kCS = 0, kCodes = kTile;
   // dQ staging: per fold warp a [32 rows][32 FP32] tile, 128-byte swizzled
   static constexpr int kDqOff = kCodesOff + 2 * kCodes;
   static constexpr int kBarOff = kDqOff + 128 * 128;
@@ -966,8 +976,7 @@ enum {
   TB_FULL = 1,             // + stage
   TB_EMPTY = 1 + kTcStages,  // + stage
   TB_SDONE = 1 + 2 * kTcStages,  // + buffer (2)
-  TB_SFREE = TB_SDONE + 2,
-  TB_CFULL = TB_SFREE + 2,
+  TB_CFULL = TB_SDONE + 2,
   TB_CEMPTY = TB_CFULL + 2,
   TB_PDONE = TB_CEMPTY + 2,  // dV and dK partials (single buffer)
   TB_PFREE = TB_PDONE + 1,
@@ -1077,7 +1086,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(bar(TB_SDONE + b), 1);
-      mbar_init(bar(TB_SFREE + b), 8);
       mbar_init(bar(TB_CFULL + b), 8);
       mbar_init(bar(TB_CEMPTY + b), 1);  // the MMA commit after the pair's dQ
     }
@@ -1147,7 +1155,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       auto issue_sdp = [&](int it) {
         const int s = it % kTcStages, b = it & 1;
         if (!wait1_ab(bar(TB_FULL + s), (it / kTcStages) & 1, ctl, abort)) return false;
-        if (it >= 2 && !wait1_ab(bar(TB_SFREE + b), ((it >> 1) - 1) & 1, ctl, abort)) return false;
+        // buffer b: dV and dK of tile it - 2 have read its P^^T and dS^^T (the
+        // latest completion of PDONE can be tile it - 2's: tile it - 1's dV and
+        // dK are issued after this)
+        if (it >= 2 && !wait1_ab(bar(TB_PDONE), (it - 2) & 1, ctl, abort)) return false;
         tc_fence_after();
         const uint32_t st = sbase + L::kStageOff + s * L::kStage;
         // descriptors built once per operand; a K step of 16 moves 32 bytes (+2)
@@ -1166,9 +1177,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!(ok = wait1_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort))) break;
         if (b == 1) {
           // dQ of the pair (it - 1, it) first -- rows 0..63 from codes buffer
-          // 0, rows 64..127 from buffer 1 -- so that buffer 0 (its dV and dK
-          // were issued before) is released for the next tile's codes; the
-          // fold has read the previous pair's dQ
+          // 0, rows 64..127 from buffer 1, their only reader -- so that both
+          // buffers are released for the next tiles' codes; the fold has read
+          // the previous pair's dQ
           const int pr = it >> 1;
           if (pr >= 1 && !(ok = wait1_ab(bar(TB_QFREE), (pr - 1) & 1, ctl, abort))) break;
           tc_fence_after();
@@ -1176,21 +1187,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int k = 0; k < 8; k++) mma_f16_tc(tmem + kTcDq, dqa + 128 * k, dqb + 128 * k, idq, k > 0);
           tc_commit(bar(TB_QDONE));
           tc_commit(bar(TB_CEMPTY + 0));
+          tc_commit(bar(TB_CEMPTY + 1));
         }
         // the partials' buffer: the fold has read the previous tile's
         if (it >= 1 && !(ok = wait1_ab(bar(TB_PFREE), (it - 1) & 1, ctl, abort))) break;
         tc_fence_after();
         const uint32_t st = sbase + L::kStageOff + s * L::kStage;
-        const uint32_t cb = sbase + L::kCodesOff + b * L::kCodes;
-        const uint64_t dp = desc_k64(cb + L::kCP, 0), dds = desc_k64(cb + L::kCS, 0);
         const uint64_t ddoc = desc_mn(st + L::kSDoc, 0, 8192), dqm = desc_mn(st + L::kSQ, 0, 8192);
+        // A: P^^T and dS^^T in tensor memory (8 columns a K step of 16 queries)
 #pragma unroll
-        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcDv, dp + 2 * k, ddoc + 128 * k, idb, k > 0);
+        for (int k = 0; k < 4; k++)
+          mma_f16_tc_ta(tmem + kTcDv, tmem + kTcS + 64 * b + 8 * k, ddoc + 128 * k, idb, k > 0);
 #pragma unroll
-        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTcDk, dds + 2 * k, dqm + 128 * k, idb, k > 0);
+        for (int k = 0; k < 4; k++)
+          mma_f16_tc_ta(tmem + kTcDk, tmem + kTcDp + 64 * b + 8 * k, dqm + 128 * k, idb, k > 0);
         tc_commit(bar(TB_PDONE));
         tc_commit(bar(TB_EMPTY + s));
-        if (b == 1) tc_commit(bar(TB_CEMPTY + 1));  // after dV and dK have read buffer 1
       }
       // every MMA issued has completed before tensor memory is released
       tc_commit(bar(TB_DRAIN));
@@ -1233,9 +1245,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         p[i] = __uint_as_float(ru[0][i]);
         dp[i] = __uint_as_float(ru[1][i]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive1(bar(TB_SFREE + b));
       // P^T = exp2(S^T c - L); masked and padded entries 0; dS^T = P^T o (dP^T - D)
       const float* Ls = reinterpret_cast<const float*>(smem + L::kStageOff + s * L::kStage + L::kSL) + 32 * h;
       const float* Ds = reinterpret_cast<const float*>(smem + L::kStageOff + s * L::kStage + L::kSD) + 32 * h;
@@ -1283,7 +1292,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         red[(b * 2 + 0) * 8 + sw] = __uint_as_float(pm);
         red[(b * 2 + 1) * 8 + sw] = __uint_as_float(sm);
       }
-      // the codes buffer is free once dV, dK (tile it - 2) and the pair's dQ have read it
+      // the codes buffer is free once the pair's dQ (tiles it - 2, it - 1) has read it; the vote
+      // below also orders both halves' tensor-memory loads before the codes overwrite them
       ok = ok && (it < 2 || waitw_ab(bar(TB_CEMPTY + b), ((it >> 1) - 1) & 1, ctl, abort));
       if (!group_and(ok)) break;  // also publishes red[]
       const float4* r4 = reinterpret_cast<const float4*>(red + b * 16);
@@ -1302,20 +1312,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint64_t y = add2(fma2(pack2(a, b), inv2, magic2), nmagic2);
         return h2(lo2(y), hi2(y));
       };
+      // codes of query columns 2j, 2j + 1 of this half in word j: P^^T and
+      // dS^^T over the first 32 columns of S^T and dP^T (tensor memory),
+      // dS^^T also to shared memory
+      uint32_t wp[16], wsd[16];
 #pragma unroll
-      for (int ch = 0; ch < 4; ch++) {
-        uint4 wp, wsd;
-        wp.x = code2(p[8 * ch + 0], p[8 * ch + 1], pp);
-        wp.y = code2(p[8 * ch + 2], p[8 * ch + 3], pp);
-        wp.z = code2(p[8 * ch + 4], p[8 * ch + 5], pp);
-        wp.w = code2(p[8 * ch + 6], p[8 * ch + 7], pp);
-        wsd.x = code2(dp[8 * ch + 0], dp[8 * ch + 1], ss);
-        wsd.y = code2(dp[8 * ch + 2], dp[8 * ch + 3], ss);
-        wsd.z = code2(dp[8 * ch + 4], dp[8 * ch + 5], ss);
-        wsd.w = code2(dp[8 * ch + 6], dp[8 * ch + 7], ss);
-        *reinterpret_cast<uint4*>(cbuf + L::kCP + swz(row, 64 * h + 16 * ch, 128)) = wp;
-        *reinterpret_cast<uint4*>(cbuf + L::kCS + swz(row, 64 * h + 16 * ch, 128)) = wsd;
+      for (int j = 0; j < 16; j++) {
+        wp[j] = code2(p[2 * j], p[2 * j + 1], pp);
+        wsd[j] = code2(dp[2 * j], dp[2 * j + 1], ss);
       }
+      tmem_st16(tmem + lanebase + kTcS + 64 * b + 16 * h, wp);
+      tmem_st16(tmem + lanebase + kTcDp + 64 * b + 16 * h, wsd);
+#pragma unroll
+      for (int ch = 0; ch < 4; ch++)
+        *reinterpret_cast<uint4*>(cbuf + L::kCS + swz(row, 64 * h + 16 * ch, 128)) =
+            make_uint4(wsd[4 * ch], wsd[4 * ch + 1], wsd[4 * ch + 2], wsd[4 * ch + 3]);
+      tmem_wait_st();
       if (threadIdx.x == 128) {
         const float sp = __fdiv_rn(pa, 127.0f), sds = __fdiv_rn(sa, 127.0f);
         float* sc = scal + 4 * (it & 3);
@@ -1323,7 +1335,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         sc[1] = sds * sq;          // dK (the softmax scale comes at the end)
         sc[2] = sds * sk * scale;  // dQ
       }
-      // the codes (generic-proxy writes) -> visible to the tensor core
+      // the codes (tensor-memory stores; generic-proxy shared-memory writes) ->
+      // visible to the tensor core
+      tc_fence_before();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive1(bar(TB_CFULL + b));
