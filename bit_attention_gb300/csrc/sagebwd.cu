@@ -2012,12 +2012,13 @@ __global__ void __launch_bounds__(kThreads) mma_peak_kernel(int iters, int* out)
   }
 }
 
-// Throughput of the 5th-generation form the kernels use (tcgen05.mma
+// Throughput of the 5th-generation forms the kernels use (tcgen05.mma
 // kind::f16, M = 128, K = 16, N = kN): one thread per CTA issues iters x 8
 // MMAs back to back into one tensor-memory accumulator from zero-filled
 // 128-byte-swizzled operands, then waits (bounded) for their completion; a
-// wait that runs out writes SAGE_FP4_ETIMEOUT to out[0].
-template <int kN>
+// wait that runs out writes SAGE_FP4_ETIMEOUT to out[0].  kForm 0: A and B
+// K-major in shared memory; 1: A in tensor memory; 2: B MN-major.
+template <int kN, int kForm>
 __global__ void __launch_bounds__(128, 1) umma_peak_kernel(int iters, int* out) {
   // A (128 rows) and B (kN rows) share one zero-filled buffer
   __shared__ __align__(1024) uint8_t sb[(kN > 128 ? kN : 128) * 128];
@@ -2040,11 +2041,19 @@ __global__ void __launch_bounds__(128, 1) umma_peak_kernel(int iters, int* out) 
   tc_fence_after();
   const uint32_t tmem = tslot;
   if (tid == 0) {
-    const uint32_t id = idesc_f16(128, kN);
-    const uint64_t da = desc_k64(smem_addr(sa), 0), db = desc_k64(smem_addr(sb), 0);
+    const uint32_t id = kForm == 2 ? (idesc_f16(128, kN) | (1u << 16)) : idesc_f16(128, kN);
+    const uint64_t da = desc_k64(smem_addr(sa), 0);
+    const uint64_t db = kForm == 2 ? desc_mn(smem_addr(sb), 0, 8192) : desc_k64(smem_addr(sb), 0);
     for (int i = 0; i < iters; i++)
 #pragma unroll
-      for (int k = 0; k < 8; k++) mma_f16_tc(tmem, da + 2 * (k & 3), db + 2 * (k & 3), id, (i | k) != 0);
+      for (int k = 0; k < 8; k++) {
+        if (kForm == 1)
+          mma_f16_tc_ta(tmem, tmem + 128 + 8 * (k & 3), db + 2 * (k & 3), id, (i | k) != 0);
+        else if (kForm == 2)
+          mma_f16_tc(tmem, da + 2 * (k & 3), db + 128 * (k & 3), id, (i | k) != 0);
+        else
+          mma_f16_tc(tmem, da + 2 * (k & 3), db + 2 * (k & 3), id, (i | k) != 0);
+      }
     tc_commit(smem_addr(&bar));
     const uint64_t t0 = globaltimer_ns();
     bool done = false;
@@ -2515,7 +2524,7 @@ int sagebwd_int_mma_probe(const int8_t* a, const int8_t* b, int K, float* out, v
 }
 
 int sagebwd_mma_peak(int kind, int ctas, int iters, void* scratch, void* stream) {
-  if (kind < 0 || kind > 4 || ctas < 1 || ctas > 65535 || iters < 1 || iters > (1 << 20) || !aligned(scratch, 4))
+  if (kind < 0 || kind > 6 || ctas < 1 || ctas > 65535 || iters < 1 || iters > (1 << 20) || !aligned(scratch, 4))
     return SAGE_FP4_EINVAL;
   const int dev = check_device();
   if (dev != SAGE_FP4_OK) return dev;
@@ -2524,9 +2533,11 @@ int sagebwd_mma_peak(int kind, int ctas, int iters, void* scratch, void* stream)
   switch (kind) {
     case 0: mma_peak_kernel<0><<<ctas, kThreads, 0, st>>>(iters, out); break;
     case 1: mma_peak_kernel<1><<<ctas, kThreads, 0, st>>>(iters, out); break;
-    case 2: umma_peak_kernel<64><<<ctas, 128, 0, st>>>(iters, out); break;
-    case 3: umma_peak_kernel<128><<<ctas, 128, 0, st>>>(iters, out); break;
-    default: umma_peak_kernel<256><<<ctas, 128, 0, st>>>(iters, out); break;
+    case 2: umma_peak_kernel<64, 0><<<ctas, 128, 0, st>>>(iters, out); break;
+    case 3: umma_peak_kernel<128, 0><<<ctas, 128, 0, st>>>(iters, out); break;
+    case 4: umma_peak_kernel<256, 0><<<ctas, 128, 0, st>>>(iters, out); break;
+    case 5: umma_peak_kernel<64, 1><<<ctas, 128, 0, st>>>(iters, out); break;
+    default: umma_peak_kernel<64, 2><<<ctas, 128, 0, st>>>(iters, out); break;
   }
   return from_cuda(cudaGetLastError());
 }

@@ -248,7 +248,8 @@ def attention(q, k, v, causal: bool = False, scale=None):
 def mma_peak_tops(kind: int, ctas: int | None = None, iters: int = 4096, repeats: int = 3) -> float:
     """Best of `repeats` timed probe launches, in TOP/s (INT8, kind 0) or
     TFLOP/s (FP16 with FP32 accumulation: kind 1 warp-level, kinds 2-4
-    tcgen05 with N = 64, 128, 256)."""
+    tcgen05 with N = 64, 128, 256, kind 5 N = 64 with A in tensor memory,
+    kind 6 N = 64 with B MN-major)."""
     import torch
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     ctas = ctas or (4 * sms if kind < 2 else sms)
@@ -266,7 +267,7 @@ def mma_peak_tops(kind: int, ctas: int | None = None, iters: int = 4096, repeats
     if kind >= 2:
         if int(scratch.item()) != 0:
             raise SageFp4Error(int(scratch.item()), "sagebwd_mma_peak: tcgen05 completion wait ran out")
-        n = (64, 128, 256)[kind - 2]
+        n = (64, 128, 256, 64, 64)[kind - 2]
         return 2.0 * 128 * n * 16 * 8 * iters * ctas / (best * 1e-3) / 1e12
     macs = (16 * 8 * 32) if kind == 0 else (16 * 8 * 16)
     warps = 256 // 32

@@ -121,8 +121,10 @@ int sagebwd_get_status(void *workspace, int B, int H, int N, int D, void *stream
  * MMAs on register operands, INT8 m16n8k32 and FP16 m16n8k16 with FP32
  * accumulation; each of `ctas` CTAs of 256 threads runs iters x 8 MMAs per
  * warp.  Kinds 2, 3, 4: tcgen05.mma kind::f16 with M = 128, K = 16 and N = 64,
- * 128, 256 (shared-memory operands, FP32 accumulation in tensor memory); one
- * thread of each of `ctas` CTAs issues iters x 8 of them (iters <= 2^20).
+ * 128, 256 (K-major shared-memory operands, FP32 accumulation in tensor
+ * memory); kind 5: N = 64 with A in tensor memory; kind 6: N = 64 with B
+ * MN-major.  One thread of each of `ctas` CTAs issues iters x 8 of them
+ * (iters <= 2^20).
  * scratch is 4 device bytes it may write (SAGE_FP4_ETIMEOUT when a tcgen05
  * completion wait runs out). */
 int sagebwd_mma_peak(int kind, int ctas, int iters, void *scratch, void *stream);

@@ -158,7 +158,7 @@ int main(void) {
            "sagebwd stall test, limit too short");
     expect(sagebwd_int_mma_probe((const int8_t *)P(0x1000), (const int8_t *)P(0x2000), 20, (float *)P(0x3000), NULL),
            SAGE_FP4_EINVAL, "sagebwd probe K = 20");
-    expect(sagebwd_mma_peak(5, 1, 1, P(0x1000), NULL), SAGE_FP4_EINVAL, "sagebwd peak kind");
+    expect(sagebwd_mma_peak(7, 1, 1, P(0x1000), NULL), SAGE_FP4_EINVAL, "sagebwd peak kind");
     expect(sagebwd_mma_peak(2, 1, (1 << 20) + 1, P(0x1000), NULL), SAGE_FP4_EINVAL, "sagebwd peak iterations");
     expect(sagebwd_umma_probe((const uint16_t *)P(0x1000), (const uint16_t *)P(0x2000), 96, (float *)P(0x3000),
                               (int32_t *)P(0x4000), NULL),

@@ -71,7 +71,7 @@ def test_fwd_and_bwd_reject_bad_arguments():
 
 
 def test_probe_and_status_argument_checks():
-    assert SB.sagebwd_mma_peak(5, 1, 1, 0x1000, None) == S.EINVAL
+    assert SB.sagebwd_mma_peak(7, 1, 1, 0x1000, None) == S.EINVAL
     assert SB.sagebwd_mma_peak(-1, 1, 1, 0x1000, None) == S.EINVAL
     assert SB.sagebwd_mma_peak(2, 1, (1 << 20) + 1, 0x1000, None) == S.EINVAL
     assert SB.sagebwd_mma_peak(0, 0, 1, 0x1000, None) == S.EINVAL

@@ -214,8 +214,9 @@ def test_mma_peaks_are_measurable():
     f16 = SB.mma_peak_tops(1)
     print(f"mma.sync peaks: INT8 m16n8k32 {i8:.1f} TOP/s, FP16 m16n8k16 (FP32 acc) {f16:.1f} TFLOP/s")
     assert i8 > 0 and f16 > 0
-    tc = {n: SB.mma_peak_tops(kind, iters=2048) for kind, n in ((2, 64), (3, 128), (4, 256))}
-    print("tcgen05 kind::f16 M=128 K=16: " + ", ".join(f"N={n} {t:.0f} TFLOP/s" for n, t in tc.items()))
+    forms = ((2, "N=64"), (3, "N=128"), (4, "N=256"), (5, "N=64 A in TMEM"), (6, "N=64 B MN-major"))
+    tc = {nm: SB.mma_peak_tops(kind, iters=2048) for kind, nm in forms}
+    print("tcgen05 kind::f16 M=128 K=16: " + ", ".join(f"{nm} {t:.0f} TFLOP/s" for nm, t in tc.items()))
     assert all(t > f16 for t in tc.values())
 
 
