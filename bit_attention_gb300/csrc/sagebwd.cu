@@ -1027,6 +1027,15 @@ __device__ __forceinline__ bool wait1_ab(uint32_t bar, uint32_t parity, const Ct
 
 __device__ __forceinline__ void mbar_arrive1(uint32_t bar) { sagefp4::mbar_arrive(bar); }
 
+// One lane of the (converged) warp: true there, false elsewhere.  The MMA
+// issuers run as whole warps, so their descriptors and loop state are
+// warp-uniform, and the elected lane issues.
+__device__ __forceinline__ bool elect1() {
+  uint32_t p;
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
+  return p != 0;
+}
+
 // All 256 threads of the two softmax warpgroups: AND of `ok` over them
 // (named barrier 1).
 __device__ __forceinline__ bool group_and(bool ok) {
@@ -1145,67 +1154,78 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         while (!mbar_try_wait(bar(TB_FIXED), 0) && globaltimer_ns() - t0 < ctl.limit) {
         }
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---- MMA issue
+    } else if (warp == 1) {
+      // ---- MMA issue: the whole warp, one elected lane issues
       // B MN-major for dV and dK (dO^ and Q^ as [64 q][64 d] rows)
       const uint32_t id = idesc_f16(128, 64), idb = idesc_f16(128, 64) | (1u << 16), idq = idesc_f16_mn(128, 64);
       // dQ = dS^ K^, MN-major: a K step of 16 rows moves 2048 bytes (+128)
       const uint64_t dqa = desc_mn(sbase + L::kCodesOff + L::kCS, 0, L::kCodes), dqb = desc_mn(sbase + L::kK, 0, L::kCodes);
-      bool ok = wait1_ab(bar(TB_FIXED), 0, ctl, abort) && wait1_ab(bar(TB_KVT), 0, ctl, abort);
+      bool ok = waitw_ab(bar(TB_FIXED), 0, ctl, abort) && waitw_ab(bar(TB_KVT), 0, ctl, abort);
       auto issue_sdp = [&](int it) {
         const int s = it % kTcStages, b = it & 1;
-        if (!wait1_ab(bar(TB_FULL + s), (it / kTcStages) & 1, ctl, abort)) return false;
+        if (!waitw_ab(bar(TB_FULL + s), (it / kTcStages) & 1, ctl, abort)) return false;
         // buffer b: dV and dK of tile it - 2 have read its P^^T and dS^^T (the
         // latest completion of PDONE can be tile it - 2's: tile it - 1's dV and
         // dK are issued after this)
-        if (it >= 2 && !wait1_ab(bar(TB_PDONE), (it - 2) & 1, ctl, abort)) return false;
+        if (it >= 2 && !waitw_ab(bar(TB_PDONE), (it - 2) & 1, ctl, abort)) return false;
         tc_fence_after();
         const uint32_t st = sbase + L::kStageOff + s * L::kStage;
         // descriptors built once per operand; a K step of 16 moves 32 bytes (+2)
         const uint64_t dq = desc_k64(st + L::kSQ, 0), ddo = desc_k64(st + L::kSDoh, 0);
+        if (elect1()) {
 #pragma unroll
-        for (int k = 0; k < 4; k++) mma_f16_tc_ta(tmem + kTcS + 64 * b, tmem + kTcK + 8 * k, dq + 2 * k, id, k > 0);
+          for (int k = 0; k < 4; k++) mma_f16_tc_ta(tmem + kTcS + 64 * b, tmem + kTcK + 8 * k, dq + 2 * k, id, k > 0);
 #pragma unroll
-        for (int k = 0; k < 4; k++) mma_f16_tc_ta(tmem + kTcDp + 64 * b, tmem + kTcV + 8 * k, ddo + 2 * k, id, k > 0);
-        tc_commit(bar(TB_SDONE + b));
+          for (int k = 0; k < 4; k++)
+            mma_f16_tc_ta(tmem + kTcDp + 64 * b, tmem + kTcV + 8 * k, ddo + 2 * k, id, k > 0);
+          tc_commit(bar(TB_SDONE + b));
+        }
+        __syncwarp();
         return true;
       };
       if (ok) ok = issue_sdp(0);
       for (int it = 0; ok && it < niter; it++) {
         const int s = it % kTcStages, b = it & 1;
         if (it + 1 < niter && !(ok = issue_sdp(it + 1))) break;
-        if (!(ok = wait1_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort))) break;
+        if (!(ok = waitw_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort))) break;
         if (b == 1) {
           // dQ of the pair (it - 1, it) first -- rows 0..63 from codes buffer
           // 0, rows 64..127 from buffer 1, their only reader -- so that both
           // buffers are released for the next tiles' codes; the fold has read
           // the previous pair's dQ
           const int pr = it >> 1;
-          if (pr >= 1 && !(ok = wait1_ab(bar(TB_QFREE), (pr - 1) & 1, ctl, abort))) break;
+          if (pr >= 1 && !(ok = waitw_ab(bar(TB_QFREE), (pr - 1) & 1, ctl, abort))) break;
           tc_fence_after();
+          if (elect1()) {
 #pragma unroll
-          for (int k = 0; k < 8; k++) mma_f16_tc(tmem + kTcDq, dqa + 128 * k, dqb + 128 * k, idq, k > 0);
-          tc_commit(bar(TB_QDONE));
-          tc_commit(bar(TB_CEMPTY + 0));
-          tc_commit(bar(TB_CEMPTY + 1));
+            for (int k = 0; k < 8; k++) mma_f16_tc(tmem + kTcDq, dqa + 128 * k, dqb + 128 * k, idq, k > 0);
+            tc_commit(bar(TB_QDONE));
+            tc_commit(bar(TB_CEMPTY + 0));
+            tc_commit(bar(TB_CEMPTY + 1));
+          }
+          __syncwarp();
         }
         // the partials' buffer: the fold has read the previous tile's
-        if (it >= 1 && !(ok = wait1_ab(bar(TB_PFREE), (it - 1) & 1, ctl, abort))) break;
+        if (it >= 1 && !(ok = waitw_ab(bar(TB_PFREE), (it - 1) & 1, ctl, abort))) break;
         tc_fence_after();
         const uint32_t st = sbase + L::kStageOff + s * L::kStage;
         const uint64_t ddoc = desc_mn(st + L::kSDoc, 0, 8192), dqm = desc_mn(st + L::kSQ, 0, 8192);
         // A: P^^T and dS^^T in tensor memory (8 columns a K step of 16 queries)
+        if (elect1()) {
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-          mma_f16_tc_ta(tmem + kTcDv, tmem + kTcS + 64 * b + 8 * k, ddoc + 128 * k, idb, k > 0);
+          for (int k = 0; k < 4; k++)
+            mma_f16_tc_ta(tmem + kTcDv, tmem + kTcS + 64 * b + 8 * k, ddoc + 128 * k, idb, k > 0);
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-          mma_f16_tc_ta(tmem + kTcDk, tmem + kTcDp + 64 * b + 8 * k, dqm + 128 * k, idb, k > 0);
-        tc_commit(bar(TB_PDONE));
-        tc_commit(bar(TB_EMPTY + s));
+          for (int k = 0; k < 4; k++)
+            mma_f16_tc_ta(tmem + kTcDk, tmem + kTcDp + 64 * b + 8 * k, dqm + 128 * k, idb, k > 0);
+          tc_commit(bar(TB_PDONE));
+          tc_commit(bar(TB_EMPTY + s));
+        }
+        __syncwarp();
       }
       // every MMA issued has completed before tensor memory is released
-      tc_commit(bar(TB_DRAIN));
+      if (elect1()) tc_commit(bar(TB_DRAIN));
+      __syncwarp();
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(bar(TB_DRAIN), 0) && globaltimer_ns() - t0 < ctl.limit) {
       }
@@ -1593,40 +1613,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         while (!mbar_try_wait(bar(FB_Q), 0) && globaltimer_ns() - t0 < ctl.limit) {
         }
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---- MMA issue
+    } else if (warp == 1) {
+      // ---- MMA issue: the whole warp, one elected lane issues
       const uint32_t idS = idesc_f16(128, 128), idPV = idesc_f16(128, 64);
       // descriptors built once per operand; a K step of 16 moves 32 bytes (+2)
       const uint64_t dq0 = desc_k64(sbase + L::kQ, 0);
-      bool ok = wait1_ab(bar(FB_Q), 0, ctl, abort);
+      bool ok = waitw_ab(bar(FB_Q), 0, ctl, abort);
       auto issue_s = [&](int kt) {
         const int s = kt % kTcStages, b = kt & 1;
-        if (!wait1_ab(bar(FB_FULL + s), (kt / kTcStages) & 1, ctl, abort)) return false;
-        if (kt >= 2 && !wait1_ab(bar(FB_SFREE + b), ((kt >> 1) - 1) & 1, ctl, abort)) return false;
+        if (!waitw_ab(bar(FB_FULL + s), (kt / kTcStages) & 1, ctl, abort)) return false;
+        if (kt >= 2 && !waitw_ab(bar(FB_SFREE + b), ((kt >> 1) - 1) & 1, ctl, abort)) return false;
         tc_fence_after();
         const uint64_t dks = desc_k64(sbase + L::kStageOff + s * L::kStage + L::kSK, 0);
+        if (elect1()) {
 #pragma unroll
-        for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTfS + 128 * b, dq0 + 2 * k, dks + 2 * k, idS, k > 0);
-        tc_commit(bar(FB_SDONE + b));
+          for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTfS + 128 * b, dq0 + 2 * k, dks + 2 * k, idS, k > 0);
+          tc_commit(bar(FB_SDONE + b));
+        }
+        __syncwarp();
         return true;
       };
       if (ok) ok = issue_s(0);
       for (int kt = 0; ok && kt < nkt; kt++) {
         const int s = kt % kTcStages, b = kt & 1;
         if (kt + 1 < nkt && !(ok = issue_s(kt + 1))) break;
-        if (!(ok = wait1_ab(bar(FB_PFULL + b), (kt >> 1) & 1, ctl, abort))) break;
-        if (kt >= 2 && !(ok = wait1_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort))) break;
+        if (!(ok = waitw_ab(bar(FB_PFULL + b), (kt >> 1) & 1, ctl, abort))) break;
+        if (kt >= 2 && !(ok = waitw_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort))) break;
         tc_fence_after();
         // P^ from tensor memory (8 columns a K step); V^T key halves 8 KB apart (+512)
         const uint64_t dvs = desc_k64(sbase + L::kStageOff + s * L::kStage + L::kSV, 0);
+        if (elect1()) {
 #pragma unroll
-        for (int k = 0; k < 8; k++)
-          mma_f16_tc_ta(tmem + kTfPv + 64 * b, tmem + kTfP + 64 * b + 8 * k, dvs + 512 * (k >> 2) + 2 * (k & 3), idPV,
-                        k > 0);
-        tc_commit(bar(FB_PVDONE + b));
-        tc_commit(bar(FB_EMPTY + s));
+          for (int k = 0; k < 8; k++)
+            mma_f16_tc_ta(tmem + kTfPv + 64 * b, tmem + kTfP + 64 * b + 8 * k, dvs + 512 * (k >> 2) + 2 * (k & 3),
+                          idPV, k > 0);
+          tc_commit(bar(FB_PVDONE + b));
+          tc_commit(bar(FB_EMPTY + s));
+        }
+        __syncwarp();
       }
-      tc_commit(bar(FB_DRAIN));
+      if (elect1()) tc_commit(bar(FB_DRAIN));
+      __syncwarp();
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(bar(FB_DRAIN), 0) && globaltimer_ns() - t0 < ctl.limit) {
       }
