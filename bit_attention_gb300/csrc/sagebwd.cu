@@ -321,230 +321,6 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const uint16_t* __restr
   }
 }
 
-// ---------------------------------------------------------------- forward
-// One CTA of 8 warps per (128 queries, head).  Warp w owns query rows
-// 16w..16w+15; warps 0-3 and 4-7 form the two 64-query P blocks.  Key tiles
-// of 128 (K^ and V^ codes) stream through two shared-memory stages by bulk
-// copy.
-template <int D>
-struct FwdSmem {
-  static constexpr int kRow = 2 * D;         // bytes per FP16 row
-  static constexpr int kTile = kTok * kRow;  // one 128-row tile
-  static constexpr int kQOff = 0;
-  static constexpr int kStageOff = kTile;
-  static constexpr int kStage = 2 * kTile;                // K^ then V^
-  static constexpr int kBarOff = kStageOff + 2 * kStage;  // 3 mbarriers: q, full[2]
-  static constexpr int kRedOff = kBarOff + 64;            // [2][8] floats
-  static constexpr int kBytes = kRedOff + 2 * 8 * 4;
-};
-
-template <int D, bool kCausal>
-__global__ void __launch_bounds__(kThreads, 1)
-    fwd_kernel(Ws ws, uint16_t* __restrict__ out, float* __restrict__ lse, int N, float scale_log2e, uint64_t wait_ns,
-               int withhold) {
-  using L = FwdSmem<D>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int nqt = (N + kTok - 1) / kTok;
-  const int Np = nqt * kTok;
-  // causal: the longest rows first
-  const int qt = kCausal ? (nqt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
-  const int bh = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3, j = lane >> 3;
-  const int grp = warp >> 2;
-  const uint32_t sbase = smem_addr(smem);
-  const uint32_t qbar = sbase + L::kBarOff, full0 = qbar + 8;
-  float* redp = reinterpret_cast<float*>(smem + L::kRedOff);
-  const Ctl ctl{ws.status, wait_ns};
-  const int nkt = kCausal ? qt + 1 : nqt;
-  const size_t hb = static_cast<size_t>(bh) * Np * D;
-
-  if (threadIdx.x == 0) {
-    mbar_init(qbar, 1);
-    mbar_init(full0, 1);
-    mbar_init(full0 + 8, 1);
-    mbar_fence_init();
-  }
-  __syncthreads();
-  auto issue_tile = [&](int kt) {
-    const int s = kt & 1;
-    const uint32_t st = sbase + L::kStageOff + s * L::kStage;
-    mbar_arrive_expect_tx(full0 + 8 * s, L::kStage);
-    bulk_load(st, ws.kc + hb + static_cast<size_t>(kt) * kTok * D, L::kTile, full0 + 8 * s);
-    bulk_load(st + L::kTile, ws.vc + hb + static_cast<size_t>(kt) * kTok * D, L::kTile, full0 + 8 * s);
-  };
-  int issued = 0;  // key tiles whose copies thread 0 has issued
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(qbar, L::kTile);
-    bulk_load(sbase + L::kQOff, ws.qc + hb + static_cast<size_t>(qt) * kTok * D, L::kTile, qbar);
-    // withhold (failure-detection test only): CTA 0 never issues key tile 0,
-    // so its wait for that tile runs out
-    if (withhold && blockIdx.x == 0 && blockIdx.y == 0) issued = 1;
-    for (; issued < 2 && issued < nkt; issued++) issue_tile(issued);
-  }
-  // every wait's outcome is voted on by the whole CTA, so that all warps
-  // carry on or all give up together
-  bool ok = __syncthreads_and(waitw(qbar, 0, ctl));
-
-  const float sqk = ws.sq[static_cast<size_t>(bh) * nqt + qt] * scale_log2e;
-  const int row0 = qt * kTok + 16 * warp + g;  // this thread's rows: row0, row0 + 8
-  const bool valid0 = row0 < N, valid1 = row0 + 8 < N;
-  const uint32_t qrow = sbase + L::kQOff;
-  const int arow = 16 * warp + ((j & 1) << 3) + (lane & 7);  // A-fragment row this lane addresses
-
-  float o[D / 8][4];
-#pragma unroll
-  for (int i = 0; i < D / 8; i++) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.0f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-  // this key tile's block scales, read one tile ahead
-  float sk_next = ws.sk[static_cast<size_t>(bh) * nqt], sv_next = ws.sv[static_cast<size_t>(bh) * nqt];
-
-  for (int kt = 0; kt < nkt && ok; kt++) {
-    const float sk_cur = sk_next, sv_cur = sv_next;
-    const int s = kt & 1;
-    const uint32_t kst = sbase + L::kStageOff + s * L::kStage, vst = kst + L::kTile;
-    ok = __syncthreads_and(waitw(full0 + 8 * s, (kt >> 1) & 1, ctl));
-    if (!ok) break;
-    // every warp is done with tile kt - 1: its stage takes tile kt + 1
-    if (threadIdx.x == 0 && kt >= 1 && kt + 1 < nkt) issue_tile(issued++);
-    // S = Q^ K^^T for 16 rows x 128 keys (integer sums in FP32)
-    float x[16][4];
-#pragma unroll
-    for (int nb = 0; nb < 16; nb++) x[nb][0] = x[nb][1] = x[nb][2] = x[nb][3] = 0.0f;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ks++) {
-      uint32_t qa[4];
-      ldsm_x4(qrow + swz(arow, 32 * ks + ((j >> 1) << 4), L::kRow), qa[0], qa[1], qa[2], qa[3]);
-#pragma unroll
-      for (int nb = 0; nb < 16; nb += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kst + swz(8 * (nb + (j >> 1)) + (lane & 7), 32 * ks + ((j & 1) << 4), L::kRow), b0, b1, b2, b3);
-        mma_f16(x[nb], qa, b0, b1);
-        mma_f16(x[nb + 1], qa, b2, b3);
-      }
-    }
-    // scale to log2 units, mask, row maxima
-    const float c2 = sqk * sk_cur;
-    const bool edge = (kCausal && kt == qt) || (kt == nqt - 1 && (N % kTok) != 0);
-    float tm0 = -INFINITY, tm1 = -INFINITY;
-#pragma unroll
-    for (int nb = 0; nb < 16; nb++) {
-#pragma unroll
-      for (int e = 0; e < 4; e++) {
-        float v = x[nb][e] * c2;
-        if (edge) {
-          const int key = kt * kTok + 8 * nb + 2 * t + (e & 1);
-          const int row = row0 + ((e >> 1) << 3);
-          if (key >= N || (kCausal && key > row)) v = -INFINITY;
-        }
-        x[nb][e] = v;
-      }
-      tm0 = fmaxf(tm0, fmaxf(x[nb][0], x[nb][1]));
-      tm1 = fmaxf(tm1, fmaxf(x[nb][2], x[nb][3]));
-    }
-    tm0 = fmaxf(tm0, __shfl_xor_sync(kFull, tm0, 1));
-    tm0 = fmaxf(tm0, __shfl_xor_sync(kFull, tm0, 2));
-    tm1 = fmaxf(tm1, __shfl_xor_sync(kFull, tm1, 1));
-    tm1 = fmaxf(tm1, __shfl_xor_sync(kFull, tm1, 2));
-    const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
-    const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);  // m = -inf on the first tile: 0
-    m0 = mn0;
-    m1 = mn1;
-    // P~ = exp2(x - m); rows past N take no part in the block maximum
-    float pmax = 0.0f, rs0 = 0.0f, rs1 = 0.0f;
-#pragma unroll
-    for (int nb = 0; nb < 16; nb++) {
-      x[nb][0] = valid0 ? ex2(x[nb][0] - mn0) : 0.0f;
-      x[nb][1] = valid0 ? ex2(x[nb][1] - mn0) : 0.0f;
-      x[nb][2] = valid1 ? ex2(x[nb][2] - mn1) : 0.0f;
-      x[nb][3] = valid1 ? ex2(x[nb][3] - mn1) : 0.0f;
-      rs0 += x[nb][0] + x[nb][1];
-      rs1 += x[nb][2] + x[nb][3];
-      pmax = fmaxf(pmax, fmaxf(fmaxf(x[nb][0], x[nb][1]), fmaxf(x[nb][2], x[nb][3])));
-    }
-    l0 = l0 * al0 + rs0;
-    l1 = l1 * al1 + rs1;
-    // block maximum over the 64-query group (named barrier per group)
-    pmax = warp_max(pmax);
-    if (lane == 0) redp[s * 8 + warp] = pmax;
-    named_bar(1 + grp, 128);
-    float amax = redp[s * 8 + 4 * grp];
-#pragma unroll
-    for (int w = 1; w < 4; w++) amax = fmaxf(amax, redp[s * 8 + 4 * grp + w]);
-    const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
-    const float spv = __fdiv_rn(amax, 127.0f) * sv_cur;
-    // P^ codes: the accumulator fragments of n-blocks 2kc, 2kc+1 are the A
-    // fragment of k-step kc
-    uint32_t pa[8][4];
-#pragma unroll
-    for (int kc = 0; kc < 8; kc++) {
-      pa[kc][0] = h2(code(x[2 * kc][0], inv), code(x[2 * kc][1], inv));
-      pa[kc][1] = h2(code(x[2 * kc][2], inv), code(x[2 * kc][3], inv));
-      pa[kc][2] = h2(code(x[2 * kc + 1][0], inv), code(x[2 * kc + 1][1], inv));
-      pa[kc][3] = h2(code(x[2 * kc + 1][2], inv), code(x[2 * kc + 1][3], inv));
-    }
-    // O = O * alpha + s_P s_V (P^ V^); V^ read transposed by ldmatrix.trans.
-    // Eight output n-blocks at a time, k outermost, so that eight
-    // independent MMA chains are in flight.
-#pragma unroll
-    for (int ng = 0; ng < D / 64; ng++) {
-      float acc[8][4];
-#pragma unroll
-      for (int i = 0; i < 8; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
-#pragma unroll
-      for (int kc = 0; kc < 8; kc++) {
-#pragma unroll
-        for (int np = 0; np < 8; np += 2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vst + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 16 * (8 * ng + np + (j >> 1)), L::kRow), b0, b1,
-                    b2, b3);
-          mma_f16(acc[np], pa[kc], b0, b1);
-          mma_f16(acc[np + 1], pa[kc], b2, b3);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 8; i++) {
-        float* oo = o[8 * ng + i];
-        oo[0] = fmaf(acc[i][0], spv, oo[0] * al0);
-        oo[1] = fmaf(acc[i][1], spv, oo[1] * al0);
-        oo[2] = fmaf(acc[i][2], spv, oo[2] * al1);
-        oo[3] = fmaf(acc[i][3], spv, oo[3] * al1);
-      }
-    }
-    sk_next = kt + 1 < nkt ? ws.sk[static_cast<size_t>(bh) * nqt + kt + 1] : 0.0f;
-    sv_next = kt + 1 < nkt ? ws.sv[static_cast<size_t>(bh) * nqt + kt + 1] : 0.0f;
-  }
-  if (!ok) {
-    // abandoning: let every copy this CTA issued land before exiting (the
-    // newest phase armed on each stage's barrier)
-    if (threadIdx.x == 0) {
-      drain_wait(qbar, 0, ctl);
-      for (int last = issued - 1; last >= 0 && last >= issued - 2; last--)
-        if (!(withhold && blockIdx.x == 0 && blockIdx.y == 0 && last == 0))
-          drain_wait(full0 + 8 * (last & 1), (last >> 1) & 1, ctl);
-    }
-    return;
-  }
-  // epilogue: O / l, lse = ln(l) + m ln 2
-  l0 += __shfl_xor_sync(kFull, l0, 1);
-  l0 += __shfl_xor_sync(kFull, l0, 2);
-  l1 += __shfl_xor_sync(kFull, l1, 1);
-  l1 += __shfl_xor_sync(kFull, l1, 2);
-  const float il0 = 1.0f / l0, il1 = 1.0f / l1;
-  uint16_t* orow0 = out + (static_cast<size_t>(bh) * N + row0) * D;
-  uint16_t* orow1 = orow0 + 8 * D;
-#pragma unroll
-  for (int nd = 0; nd < D / 8; nd++) {
-    const int d = 8 * nd + 2 * t;
-    if (valid0) *reinterpret_cast<__nv_bfloat162*>(orow0 + d) = __floats2bfloat162_rn(o[nd][0] * il0, o[nd][1] * il0);
-    if (valid1) *reinterpret_cast<__nv_bfloat162*>(orow1 + d) = __floats2bfloat162_rn(o[nd][2] * il1, o[nd][3] * il1);
-  }
-  if (t == 0) {
-    if (valid0) lse[static_cast<size_t>(bh) * N + row0] = (m0 + __log2f(l0)) * kLn2;
-    if (valid1) lse[static_cast<size_t>(bh) * N + row0 + 8] = (m1 + __log2f(l1)) * kLn2;
-  }
-}
-
 // ---------------------------------------------------------------- backward
 // One CTA of 8 warps per (128 keys, head); warp w owns keys 16w..16w+15.  The
 // CTA's K^ codes and FP16 V stay in shared memory; query tiles of 64 (Q^ and
@@ -1499,12 +1275,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 //   3  correction: O in registers, rescaled by each row's factor and
 //      accumulated with each tile's PV times its block scales; the epilogue
 // P~ blocks are 64 query rows x 128 keys, as in the warp-level forward.
+template <int D>
 struct TfSmem {
-  static constexpr int kQ = 0;                    // Q^ [128][64]: 16 KB
-  static constexpr int kStageOff = 16384;
-  static constexpr int kSK = 0, kSV = 16384;      // K^ [128][64]; V^T [2][64 d][64 keys]
-  static constexpr int kStage = 32768;
-  static constexpr int kBarOff = kStageOff + kTcStages * kStage;
+  static constexpr int kHalf = 128 * 128;          // 128 rows of 128 bytes
+  static constexpr int kQ = 0;                     // Q^ [D / 64 halves][128][64]
+  static constexpr int kStageOff = D / 64 * kHalf;
+  static constexpr int kSK = 0;                    // K^ [D / 64 halves][128 keys][64]
+  static constexpr int kSV = D / 64 * kHalf;       // V^T [2 key halves][D][64 keys]
+  static constexpr int kStage = 2 * D / 64 * kHalf;
+  static constexpr int kStages = D == 64 ? 3 : 2;
+  static constexpr int kBarOff = kStageOff + kStages * kStage;
   static constexpr int kMiscOff = kBarOff + 8 * 32;
   // misc: tmem slot, abort, row max halves [2 parity][2][128], alpha [2][128],
   // block max [2 parity][8 warps], beta [2][2], final l halves [2][128], m [128]
@@ -1513,28 +1293,46 @@ struct TfSmem {
   static constexpr int kBytes = kMf + 512;
   static constexpr int kAlloc = kBytes + 1024;
 };
+static_assert(TfSmem<128>::kAlloc <= 227 * 1024, "shared memory");
+// mbarriers (3 stages at most)
 enum {
   FB_Q = 0,
   FB_FULL = 1,
-  FB_EMPTY = 1 + kTcStages,
-  FB_SDONE = 1 + 2 * kTcStages,  // + buffer
-  FB_SFREE = FB_SDONE + 2,
-  FB_PFULL = FB_SFREE + 2,
+  FB_EMPTY = 4,
+  FB_SDONE = 7,  // + buffer
+  FB_PFULL = FB_SDONE + 2,
   FB_PVDONE = FB_PFULL + 2,
   FB_PVFREE = FB_PVDONE + 2,
   FB_DRAIN = FB_PVFREE + 2,
   FB_COUNT
 };
 static_assert(FB_COUNT <= 32, "barriers");
-// tensor-memory columns: S (FP32) [2][128], P^ (FP16 pairs) [2][64], PV (FP32) [2][64]
-constexpr uint32_t kTfS = 0, kTfP = 256, kTfPv = 384;
+// tensor-memory columns: S (FP32) [2][128], then P^ (FP16 pairs) over its
+// first 64 columns; PV (FP32) [2][D]
+constexpr uint32_t kTfS = 0, kTfPv = 256;
 
-template <bool kCausal>
+// Q^ or K^ rows [rows .. rows + 127] into a [D / 64][128][64] tile (halves 16
+// KB apart): at D = 64 one bulk copy; at D = 128 two tiled copies of 128-byte
+// column halves (the rows' 16-byte chunks are XOR-permuted within each half,
+// so the copies land in the tensor core's 128-byte-swizzled layout).
+template <int D>
+__device__ __forceinline__ void load_rows(uint32_t dst, const uint16_t* src, const CUtensorMap* map, int row0,
+                                          uint32_t bar) {
+  if constexpr (D == 64) {
+    bulk_load(dst, src + static_cast<size_t>(row0) * D, 128 * 128, bar);
+  } else {
+    sagefp4::tma_load_2d(dst, map, 0, row0, bar);
+    sagefp4::tma_load_2d(dst + 128 * 128, map, 128, row0, bar);
+  }
+}
+
+template <int D, bool kCausal>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    fwd_tc_kernel(Ws ws, uint16_t* __restrict__ out, float* __restrict__ lse, int N, float scale_log2e, uint64_t wait_ns,
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, Ws ws,
+                  uint16_t* __restrict__ out, float* __restrict__ lse, int N, float scale_log2e, uint64_t wait_ns,
                   int withhold) {
-  constexpr int D = 64;
-  using L = TfSmem;
+  using L = TfSmem<D>;
+  constexpr int kSt = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(smem);
@@ -1549,7 +1347,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   auto bar = [&](int i) { return sbase + L::kBarOff + 8 * i; };
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-  float* xm = reinterpret_cast<float*>(smem + L::kXm);     // [2 halves][128 rows]
+  float* xm = reinterpret_cast<float*>(smem + L::kXm);     // [2 parity][2 halves][128 rows]
   float* al = reinterpret_cast<float*>(smem + L::kAl);     // [2 buffers][128 rows]
   float* bm = reinterpret_cast<float*>(smem + L::kBm);     // [2 parity][8 softmax warps]
   float* beta = reinterpret_cast<float*>(smem + L::kBeta); // [2 buffers][2 row blocks]
@@ -1558,13 +1356,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(FB_Q), 1);
-    for (int s = 0; s < kTcStages; s++) {
+    for (int s = 0; s < kSt; s++) {
       mbar_init(bar(FB_FULL + s), 1);
       mbar_init(bar(FB_EMPTY + s), 1);  // the MMA commit after PV
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(bar(FB_SDONE + b), 1);
-      mbar_init(bar(FB_SFREE + b), 8);
       mbar_init(bar(FB_PFULL + b), 8);
       mbar_init(bar(FB_PVDONE + b), 1);
       mbar_init(bar(FB_PVFREE + b), 4);
@@ -1586,27 +1383,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     sagefp4::regs_dec<TcRegs::kCtl>();
     if (warp == 0 && lane == 0) {
       // ---- producer
-      mbar_arrive_expect_tx(bar(FB_Q), 16384);
-      bulk_load(sbase + L::kQ, ws.qc + hb + static_cast<size_t>(qt) * kTok * D, 16384, bar(FB_Q));
+      const int hrow = bh * Np;  // the head's first row in [B*H*Np][D]
+      mbar_arrive_expect_tx(bar(FB_Q), D / 64 * L::kHalf);
+      load_rows<D>(sbase + L::kQ, ws.qc, &tm_q, hrow + qt * kTok, bar(FB_Q));
       const bool held = withhold && blockIdx.x == 0 && blockIdx.y == 0;
       int issued = 0;
       for (int kt = 0; kt < nkt; kt++) {
-        const int s = kt % kTcStages;
-        if (kt >= kTcStages && !wait1_ab(bar(FB_EMPTY + s), ((kt / kTcStages) - 1) & 1, ctl, abort)) break;
+        const int s = kt % kSt;
+        if (kt >= kSt && !wait1_ab(bar(FB_EMPTY + s), ((kt / kSt) - 1) & 1, ctl, abort)) break;
         if (held && kt == 0) continue;  // failure-detection test: this tile never arrives
         const uint32_t st = sbase + L::kStageOff + s * L::kStage;
-        const size_t ko = hb + static_cast<size_t>(kt) * kTok * D;
-        mbar_arrive_expect_tx(bar(FB_FULL + s), 32768);
-        bulk_load(st + L::kSK, ws.kc + ko, 16384, bar(FB_FULL + s));
-        bulk_load(st + L::kSV, ws.vct + ko, 16384, bar(FB_FULL + s));
+        mbar_arrive_expect_tx(bar(FB_FULL + s), L::kStage);
+        load_rows<D>(st + L::kSK, ws.kc, &tm_k, hrow + kt * kTok, bar(FB_FULL + s));
+        bulk_load(st + L::kSV, ws.vct + hb + static_cast<size_t>(kt) * kTok * D, L::kStage / 2, bar(FB_FULL + s));
         issued = kt + 1;
       }
       if (*abort) {
-        for (int last = issued - 1; last >= 0 && last >= issued - kTcStages; last--)
+        for (int last = issued - 1; last >= 0 && last >= issued - kSt; last--)
           if (!(held && last == 0)) {
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(bar(FB_FULL + last % kTcStages), (last / kTcStages) & 1) &&
-                   globaltimer_ns() - t0 < ctl.limit) {
+            while (!mbar_try_wait(bar(FB_FULL + last % kSt), (last / kSt) & 1) && globaltimer_ns() - t0 < ctl.limit) {
             }
           }
         const uint64_t t0 = globaltimer_ns();
@@ -1615,19 +1411,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     } else if (warp == 1) {
       // ---- MMA issue: the whole warp, one elected lane issues
-      const uint32_t idS = idesc_f16(128, 128), idPV = idesc_f16(128, 64);
-      // descriptors built once per operand; a K step of 16 moves 32 bytes (+2)
+      const uint32_t idS = idesc_f16(128, 128), idPV = idesc_f16(128, D);
+      // descriptors built once per operand: a K step of 16 moves 32 bytes
+      // (+2), a 64-wide half 16 KB (+1024); V^T's key halves are D * 128
+      // bytes apart
       const uint64_t dq0 = desc_k64(sbase + L::kQ, 0);
       bool ok = waitw_ab(bar(FB_Q), 0, ctl, abort);
       auto issue_s = [&](int kt) {
-        const int s = kt % kTcStages, b = kt & 1;
-        if (!waitw_ab(bar(FB_FULL + s), (kt / kTcStages) & 1, ctl, abort)) return false;
-        if (kt >= 2 && !waitw_ab(bar(FB_SFREE + b), ((kt >> 1) - 1) & 1, ctl, abort)) return false;
+        const int s = kt % kSt, b = kt & 1;
+        if (!waitw_ab(bar(FB_FULL + s), (kt / kSt) & 1, ctl, abort)) return false;
+        // buffer b: PV of tile kt - 2 has read its P^ (and so the softmax has
+        // read its S); PV's latest completion can be tile kt - 2's here
+        if (kt >= 2 && !waitw_ab(bar(FB_PVDONE + b), ((kt >> 1) - 1) & 1, ctl, abort)) return false;
         tc_fence_after();
         const uint64_t dks = desc_k64(sbase + L::kStageOff + s * L::kStage + L::kSK, 0);
         if (elect1()) {
 #pragma unroll
-          for (int k = 0; k < 4; k++) mma_f16_tc(tmem + kTfS + 128 * b, dq0 + 2 * k, dks + 2 * k, idS, k > 0);
+          for (int k = 0; k < D / 16; k++)
+            mma_f16_tc(tmem + kTfS + 128 * b, dq0 + 1024 * (k >> 2) + 2 * (k & 3), dks + 1024 * (k >> 2) + 2 * (k & 3),
+                       idS, k > 0);
           tc_commit(bar(FB_SDONE + b));
         }
         __syncwarp();
@@ -1635,17 +1437,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       };
       if (ok) ok = issue_s(0);
       for (int kt = 0; ok && kt < nkt; kt++) {
-        const int s = kt % kTcStages, b = kt & 1;
+        const int s = kt % kSt, b = kt & 1;
         if (kt + 1 < nkt && !(ok = issue_s(kt + 1))) break;
         if (!(ok = waitw_ab(bar(FB_PFULL + b), (kt >> 1) & 1, ctl, abort))) break;
         if (kt >= 2 && !(ok = waitw_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort))) break;
         tc_fence_after();
-        // P^ from tensor memory (8 columns a K step); V^T key halves 8 KB apart (+512)
+        // A: P^ over S's first 64 columns (8 columns a K step of 16 keys)
         const uint64_t dvs = desc_k64(sbase + L::kStageOff + s * L::kStage + L::kSV, 0);
         if (elect1()) {
 #pragma unroll
           for (int k = 0; k < 8; k++)
-            mma_f16_tc_ta(tmem + kTfPv + 64 * b, tmem + kTfP + 64 * b + 8 * k, dvs + 512 * (k >> 2) + 2 * (k & 3),
+            mma_f16_tc_ta(tmem + kTfPv + D * b, tmem + kTfS + 128 * b + 8 * k, dvs + 8 * D * (k >> 2) + 2 * (k & 3),
                           idPV, k > 0);
           tc_commit(bar(FB_PVDONE + b));
           tc_commit(bar(FB_EMPTY + s));
@@ -1692,9 +1494,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tmem_ld32(tmem + lanebase + kTfS + 128 * b + 64 * h, ru[0]);
       tmem_ld32(tmem + lanebase + kTfS + 128 * b + 64 * h + 32, ru[1]);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive1(bar(FB_SFREE + b));
       if ((kCausal && kt == qt) || (kt == nqt - 1 && (N % kTok) != 0)) {
         // keys past N, and (causal) past this row, do not take part
         const int k0 = kt * kTok + 64 * h;
@@ -1717,10 +1516,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // the row's maximum over both halves of the tile (xm by tile parity)
       xm[(2 * b + h) * 128 + row] = hm;
-      // alpha, beta and the P^ buffer b: the correction has read tile kt - 2's
-      // alpha and beta and, after PV of tile kt - 2 completed, its product
+      // alpha and beta of buffer b: the correction has read tile kt - 2's
       ok = ok && (kt < 2 || waitw_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort));
-      if (!group_and(ok)) break;  // also publishes xm
+      // also publishes xm, and orders both halves' loads of S before P^
+      // overwrites its first 64 columns
+      if (!group_and(ok)) break;
       const float mt = fmaxf(hm, xm[(2 * b + 1 - h) * 128 + row]);
       // c2 > 0 keeps masked keys at -inf (c2 = 0 only when every score is 0)
       const float c2 = fmaxf(sqk * sk_cur, 1e-30f);
@@ -1760,7 +1560,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       const uint64_t acc = add2(acc0, acc1);
       l = fmaf(l, alpha, lo2(acc) + hi2(acc));
-      tmem_st32(tmem + lanebase + kTfP + 64 * b + 32 * h, pw);
+      tmem_st32(tmem + lanebase + kTfS + 128 * b + 32 * h, pw);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -1777,9 +1577,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = 32 * (warp & 3) + lane;
     const int blk = (warp & 3) >> 1;
     const uint32_t lanebase = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    uint64_t o[32];
+    uint64_t o[D / 2];
 #pragma unroll
-    for (int i = 0; i < 32; i++) o[i] = 0;
+    for (int i = 0; i < D / 2; i++) o[i] = 0;
     for (int kt = 0; kt < nkt; kt++) {
       const int b = kt & 1;
       // PFULL: the softmax's alpha and beta of this tile (its release); PVDONE: the product
@@ -1787,27 +1587,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!waitw_ab(bar(FB_PVDONE + b), (kt >> 1) & 1, ctl, abort)) break;
       tc_fence_after();
       const float alpha = al[b * 128 + row], bt = beta[b * 2 + blk];
-      uint32_t ru[2][32];
-      tmem_ld32(tmem + lanebase + kTfPv + 64 * b, ru[0]);
-      tmem_ld32(tmem + lanebase + kTfPv + 64 * b + 32, ru[1]);
-      tmem_wait_ld();
+      // o = pv * beta + o * alpha; o * 1 is o, so warps whose rows' maxima
+      // all held skip the multiply
+      const uint64_t bt2 = pack2(bt, bt), al2 = pack2(alpha, alpha);
+      const bool keep = __all_sync(kFull, alpha == 1.0f);
+#pragma unroll
+      for (int c = 0; c < D / 32; c++) {
+        uint32_t ru[32];
+        tmem_ld32(tmem + lanebase + kTfPv + D * b + 32 * c, ru);
+        tmem_wait_ld();
+        if (keep) {
+#pragma unroll
+          for (int j = 0; j < 16; j++)
+            o[16 * c + j] = fma2(pack2(__uint_as_float(ru[2 * j]), __uint_as_float(ru[2 * j + 1])), bt2, o[16 * c + j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; j++)
+            o[16 * c + j] =
+                fma2(pack2(__uint_as_float(ru[2 * j]), __uint_as_float(ru[2 * j + 1])), bt2, mul2(o[16 * c + j], al2));
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive1(bar(FB_PVFREE + b));
-      // o = pv * beta + o * alpha; o * 1 is o, so rows whose maximum held skip it
-      const uint64_t bt2 = pack2(bt, bt);
-      if (__all_sync(kFull, alpha == 1.0f)) {
-#pragma unroll
-        for (int j = 0; j < 32; j++)
-          o[j] = fma2(pack2(__uint_as_float(ru[j >> 4][(j & 15) * 2]), __uint_as_float(ru[j >> 4][(j & 15) * 2 + 1])),
-                      bt2, o[j]);
-      } else {
-        const uint64_t al2 = pack2(alpha, alpha);
-#pragma unroll
-        for (int j = 0; j < 32; j++)
-          o[j] = fma2(pack2(__uint_as_float(ru[j >> 4][(j & 15) * 2]), __uint_as_float(ru[j >> 4][(j & 15) * 2 + 1])),
-                      bt2, mul2(o[j], al2));
-      }
     }
     // epilogue, once the softmax has published l and m
     tc_fence_before();
@@ -1819,7 +1621,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float il = 1.0f / lt;
         uint16_t* orow = out + (static_cast<size_t>(bh) * N + qrow) * D;
 #pragma unroll
-        for (int c = 0; c < 8; c++) {
+        for (int c = 0; c < D / 8; c++) {
           __nv_bfloat162 h0 = __floats2bfloat162_rn(lo2(o[4 * c + 0]) * il, hi2(o[4 * c + 0]) * il);
           __nv_bfloat162 h1 = __floats2bfloat162_rn(lo2(o[4 * c + 1]) * il, hi2(o[4 * c + 1]) * il);
           __nv_bfloat162 hh2 = __floats2bfloat162_rn(lo2(o[4 * c + 2]) * il, hi2(o[4 * c + 2]) * il);
@@ -2244,17 +2046,6 @@ int check_device() {
 }
 
 template <int D, bool C>
-cudaError_t launch_fwd(const Ws& w, uint16_t* o, float* lse, int BH, int N, float scale, cudaStream_t st,
-                       uint64_t wait_ns = kWaitNs, int withhold = 0) {
-  const int smem = FwdSmem<D>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  const dim3 grid((N + kTok - 1) / kTok, BH);
-  fwd_kernel<D, C><<<grid, kThreads, smem, st>>>(w, o, lse, N, scale * kLog2e, wait_ns, withhold);
-  return cudaGetLastError();
-}
-
-template <int D, bool C>
 cudaError_t launch_dkdv(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int N, float scale, cudaStream_t st,
                         uint64_t wait_ns = kWaitNs, int withhold = 0) {
   const int smem = BwdSmem<D>::kBytes;
@@ -2270,23 +2061,43 @@ cudaError_t launch_dkdv(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int N, 
 // an increase would never be granted, so it refuses to launch.
 // 2-D FP32 tensor [rows][inner] (row pitch inner * 4 bytes) with boxes of
 // [box_rows][box_inner], 128-byte swizzled (box_inner * 4 <= 128).
-bool make_map_f32(CUtensorMap* m, const float* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                  uint32_t box_rows) {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   if (!enc) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return false;
-    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   }
+  return enc;
+}
+
+bool make_map_f32(CUtensorMap* m, const float* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                  uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner * 4};
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D byte tensor [rows][inner] (row pitch inner bytes) with boxes of
+// [box_rows][box_inner], copied as they are (no swizzle).
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                 uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -2307,17 +2118,30 @@ cudaError_t launch_dkdv_tc(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int 
   return cudaGetLastError();
 }
 
-template <bool C>
+template <int D, bool C>
 cudaError_t launch_fwd_tc(const Ws& w, uint16_t* o, float* lse, int BH, int N, float scale, cudaStream_t st,
                           uint64_t wait_ns, int withhold) {
+  // D = 128: Q^ and K^ through tensor maps over the code arrays viewed as
+  // bytes [B*H*Np][256], boxes of 128 rows x 128 bytes (no swizzle: the rows
+  // carry it); D = 64 copies whole tiles and passes the maps unused
+  CUtensorMap tq, tk;
+  memset(&tq, 0, sizeof(tq));
+  memset(&tk, 0, sizeof(tk));
+  if (D == 128) {
+    const uint64_t rows = static_cast<uint64_t>(BH) * ((N + kTok - 1) / kTok * kTok);
+    if (rows > 0x7fffffffu || !make_map_u8(&tq, w.qc, 2 * D, rows, 128, 128) ||
+        !make_map_u8(&tk, w.kc, 2 * D, rows, 128, 128))
+      return cudaErrorInvalidValue;
+  }
   cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, fwd_tc_kernel<C>);
+  cudaError_t e = cudaFuncGetAttributes(&attr, fwd_tc_kernel<D, C>);
   if (e != cudaSuccess) return e;
   if (attr.numRegs != 65536 / kTcThreads) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(fwd_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, TfSmem::kAlloc);
+  e = cudaFuncSetAttribute(fwd_tc_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, TfSmem<D>::kAlloc);
   if (e != cudaSuccess) return e;
   const dim3 grid((N + kTok - 1) / kTok, BH);
-  fwd_tc_kernel<C><<<grid, kTcThreads, TfSmem::kAlloc, st>>>(w, o, lse, N, scale * kLog2e, wait_ns, withhold);
+  fwd_tc_kernel<D, C><<<grid, kTcThreads, TfSmem<D>::kAlloc, st>>>(tq, tk, w, o, lse, N, scale * kLog2e, wait_ns,
+                                                                  withhold);
   return cudaGetLastError();
 }
 
@@ -2389,11 +2213,11 @@ int sagebwd_attn_fwd(void* o, float* lse, int B, int H, int N, int D, int causal
   const int BH = B * H;
   cudaError_t e;
   if (D == 64)
-    e = causal ? launch_fwd_tc<true>(w, ob, lse, BH, N, scale, st, kWaitNs, 0)
-               : launch_fwd_tc<false>(w, ob, lse, BH, N, scale, st, kWaitNs, 0);
+    e = causal ? launch_fwd_tc<64, true>(w, ob, lse, BH, N, scale, st, kWaitNs, 0)
+               : launch_fwd_tc<64, false>(w, ob, lse, BH, N, scale, st, kWaitNs, 0);
   else
-    e = causal ? launch_fwd<128, true>(w, ob, lse, BH, N, scale, st)
-               : launch_fwd<128, false>(w, ob, lse, BH, N, scale, st);
+    e = causal ? launch_fwd_tc<128, true>(w, ob, lse, BH, N, scale, st, kWaitNs, 0)
+               : launch_fwd_tc<128, false>(w, ob, lse, BH, N, scale, st, kWaitNs, 0);
   return from_cuda(e);
 }
 
@@ -2502,8 +2326,8 @@ int sagebwd_stall_test(int kernel, void* out0, void* out1, int B, int H, int N, 
   if (kernel == 0) {
     uint16_t* o = static_cast<uint16_t*>(out0);
     float* lse = static_cast<float*>(out1);
-    e = D == 64 ? launch_fwd_tc<false>(w, o, lse, BH, N, scale, st, wait_limit_ns, 1)
-                : launch_fwd<128, false>(w, o, lse, BH, N, scale, st, wait_limit_ns, 1);
+    e = D == 64 ? launch_fwd_tc<64, false>(w, o, lse, BH, N, scale, st, wait_limit_ns, 1)
+                : launch_fwd_tc<128, false>(w, o, lse, BH, N, scale, st, wait_limit_ns, 1);
   } else {
     uint16_t *dkb = static_cast<uint16_t*>(out0), *dvb = static_cast<uint16_t*>(out1);
     e = D == 64 ? launch_dkdv_tc<false>(w, dkb, dvb, BH, N, scale, st, wait_limit_ns, 1)
