@@ -47,8 +47,8 @@ HBM_NOMINAL_GBS = 8000.0  # the "~8 TB/s" HBM3e figure the quantize target is qu
 
 
 TRAIN_METRIC = ("SageBwd 8-bit attention fwd+bwd TOPS (3.5*4*B*H*N^2*D/t, causal at half) on 1 GB300; "
-                "fraction of the measured 16-bit tensor peak of the instruction issued (D=64: tcgen05, "
-                "D=128: mma.sync)")
+                "fraction of the measured 16-bit tensor peak of the instruction each kernel issues (tcgen05; "
+                "the D=128 backward: mma.sync)")
 SAGEBWD_CALLS = ("quantize_qkv", "attn_fwd", "bwd_prep", "attn_bwd", "dq_out")
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one attn_fwd_kernel launch,
@@ -362,12 +362,13 @@ class SageBwdRun:
         return ev[0][0].elapsed_time(ev[-1][-1]), per
 
 
-def sagebwd_peak(w, fp16_mma_peak):
-    """The tensor peak the SageBwd attention kernels of workload w are judged
-    against: at D = 64 they issue tcgen05.mma kind::f16 (the measured dense
-    16-bit GEMM peak; FP16 and BF16 share the nominal rate), at D = 128 the
-    warp-level FP16 mma.sync (its measured rate)."""
-    if w.D == 64:
+def sagebwd_peak(kernel, w, fp16_mma_peak):
+    """The tensor peak a SageBwd attention kernel of workload w is judged
+    against: the ones that issue tcgen05.mma kind::f16 (the forward, and the
+    backward at D = 64) against the measured dense 16-bit GEMM peak (FP16 and
+    BF16 share the nominal rate); the backward at D = 128, warp-level FP16
+    mma.sync, against that instruction's measured rate."""
+    if kernel == "attn_fwd" or w.D == 64:
         pk = peaks()
         return pk["bf16_tflops"], f"{pk['src']} bf16 GEMM (burst), the tcgen05 kind::f16 rate"
     return fp16_mma_peak, "measured live: FP16 mma.sync m16n8k16 (FP32 accumulate) probe, the instruction issued"
@@ -380,12 +381,14 @@ def sagebwd_summary(w, per, fp16_mma_peak):
     fwd_tops = ops / (m["attn_fwd"] * 1e-3) / 1e12
     bwd_tops = 2.5 * ops / (m["attn_bwd"] * 1e-3) / 1e12
     step = sum(m.values())
-    peak, src = sagebwd_peak(w, fp16_mma_peak)
+    fpeak, fsrc = sagebwd_peak("attn_fwd", w, fp16_mma_peak)
+    bpeak, bsrc = sagebwd_peak("attn_bwd", w, fp16_mma_peak)
     return {"workload": w.name, "ms": m, "ms_per_step": step,
             "attn_fwd_tops": fwd_tops, "attn_bwd_tops": bwd_tops,
-            "peak_tflops": peak, "peak_src": src,
-            "attn_fwd_frac_of_peak": fwd_tops / peak,
-            "attn_bwd_frac_of_peak": bwd_tops / peak,
+            "attn_fwd_peak_tflops": fpeak, "attn_fwd_peak_src": fsrc,
+            "peak_tflops": bpeak, "peak_src": bsrc,
+            "attn_fwd_frac_of_peak": fwd_tops / fpeak,
+            "attn_bwd_frac_of_peak": bwd_tops / bpeak,
             "step_tops": 3.5 * ops / (step * 1e-3) / 1e12}
 
 
