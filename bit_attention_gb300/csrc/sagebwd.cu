@@ -721,21 +721,25 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int k0, uint32_t bloc
 // once dV and dK of tile t have completed.  Every wait is bounded; a wait that runs out
 // sets the status word and an abort flag that ends every role's loop.
 constexpr int kTcThreads = 512;
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 3;  // the most stages a tcgen05 kernel uses (mbarrier slots)
 struct TcRegs {
   static constexpr uint32_t kCtl = 64, kSoft = 128, kFold = 192;
 };
 static_assert(TcRegs::kCtl * 128 + TcRegs::kSoft * 256 + TcRegs::kFold * 128 <= 65536, "register split");
 
+template <int D>
 struct TcSmem {
+  static constexpr int kNH = D / 64;       // 64-wide halves of D
   static constexpr int kTile = 128 * 128;  // 128 rows of 128 bytes
-  static constexpr int kK = 0;             // K^ codes [128 keys][64]
-  static constexpr int kV = kTile;         // FP16 V [128 keys][64]
-  static constexpr int kStageOff = 2 * kTile;
-  // stage: Q^ [64 q][64], FP16 dO [64 q][64], dO^ [64 q][64], -L, D
-  static constexpr int kSQ = 0, kSDoh = 8192, kSDoc = 16384, kSL = 24576, kSD = 24832;
-  static constexpr int kStage = 25600;  // a multiple of 1024
-  static constexpr int kCodesOff = kStageOff + kTcStages * kStage;
+  static constexpr int kK = 0;             // K^ codes [kNH][128 keys][64]
+  static constexpr int kV = kNH * kTile;   // FP16 V [kNH][128 keys][64]
+  static constexpr int kStageOff = 2 * kNH * kTile;
+  // stage: Q^ [kNH][64 q][64], FP16 dO [kNH][64 q][64], dO^ of this CTA's
+  // half [64 q][64], -L, D
+  static constexpr int kSQ = 0, kSDoh = kNH * 8192, kSDoc = 2 * kNH * 8192, kSL = kSDoc + 8192, kSD = kSL + 256;
+  static constexpr int kStage = (kSD + 256 + 1023) / 1024 * 1024;
+  static constexpr int kStages = D == 64 ? 3 : 2;
+  static constexpr int kCodesOff = kStageOff + kStages * kStage;
   // codes buffer: dS^T [128 keys][64 q] (dQ's A operand, read MN-major)
   static constexpr int kCS = 0, kCodes = kTile;
   // dQ staging: per fold warp a [32 rows][32 FP32] tile, 128-byte swizzled
@@ -762,7 +766,8 @@ enum {
   TB_DRAIN = TB_KVT + 1,
   TB_COUNT
 };
-static_assert(TB_COUNT <= TcSmem::kNumBars, "barriers");
+static_assert(TB_COUNT <= 32, "barriers");
+static_assert(TcSmem<128>::kAlloc <= 227 * 1024, "shared memory");
 // tensor-memory columns
 constexpr uint32_t kTcS = 0, kTcDp = 128, kTcDv = 256, kTcDk = 320, kTcDq = 384, kTcK = 448, kTcV = 480;
 
@@ -836,12 +841,23 @@ __device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
 
-template <bool kCausal>
+// Tensor maps of the backward.  dq: the FP32 dQ accumulator [B*H*Np][D]
+// (boxes of 32 x 32, 128-byte swizzled).  At D = 128 also k, v: K^ codes and
+// FP16 V as bytes [B*H*Np][256], boxes of 128 bytes x 128 rows; q, doh, doc:
+// Q^ codes, FP16 dO and dO^ codes, boxes of 128 bytes x 64 rows (the rows'
+// 16-byte chunks are XOR-permuted within each 128-byte half, so a copied half
+// is in the 128-byte-swizzled layout).
+struct BwdMaps {
+  CUtensorMap dq, k, v, q, doh, doc;
+};
+
+template <int D, bool kCausal>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_dq, Ws ws, uint16_t* __restrict__ dk,
+    dkdv_tc_kernel(const __grid_constant__ BwdMaps maps, Ws ws, uint16_t* __restrict__ dk,
                    uint16_t* __restrict__ dv, int N, float scale, uint64_t wait_ns, int withhold) {
-  constexpr int D = 64;
-  using L = TcSmem;
+  using L = TcSmem<D>;
+  constexpr int kSt = L::kStages;
+  const int dh = D == 64 ? 0 : static_cast<int>(blockIdx.z);  // this CTA's 64 columns of dV, dK, dQ
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, by pointer arithmetic on the shared array (so
   // that the compiler keeps its accesses in the shared state space)
@@ -865,7 +881,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(TB_FIXED), 1);
-    for (int s = 0; s < kTcStages; s++) {
+    for (int s = 0; s < kSt; s++) {
       mbar_init(bar(TB_FULL + s), 1);
       mbar_init(bar(TB_EMPTY + s), 1 + 8);  // the MMA commit + the softmax warps
     }
@@ -896,34 +912,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     sagefp4::regs_dec<TcRegs::kCtl>();
     if (warp == 0 && lane == 0) {
       // ---- producer
-      const size_t off = hb + static_cast<size_t>(kb) * kTok * D;
-      mbar_arrive_expect_tx(bar(TB_FIXED), 2 * L::kTile);
-      bulk_load(sbase + L::kK, ws.kc + off, L::kTile, bar(TB_FIXED));
-      bulk_load(sbase + L::kV, ws.vh + off, L::kTile, bar(TB_FIXED));
-      const bool held = withhold && blockIdx.x == 0 && blockIdx.y == 0;
+      const int hr = static_cast<int>(hrow);  // the head's first row in [B*H*Np]
+      mbar_arrive_expect_tx(bar(TB_FIXED), 2 * L::kNH * L::kTile);
+      if constexpr (D == 64) {
+        const size_t off = hb + static_cast<size_t>(kb) * kTok * D;
+        bulk_load(sbase + L::kK, ws.kc + off, L::kTile, bar(TB_FIXED));
+        bulk_load(sbase + L::kV, ws.vh + off, L::kTile, bar(TB_FIXED));
+      } else {
+        for (int x = 0; x < 2; x++) {
+          sagefp4::tma_load_2d(sbase + L::kK + x * L::kTile, &maps.k, 128 * x, hr + kb * kTok, bar(TB_FIXED));
+          sagefp4::tma_load_2d(sbase + L::kV + x * L::kTile, &maps.v, 128 * x, hr + kb * kTok, bar(TB_FIXED));
+        }
+      }
+      const bool held = withhold && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
       int issued = 0;
       for (int it = 0; it < niter; it++) {
-        const int s = it % kTcStages;
-        if (it >= kTcStages && !wait1_ab(bar(TB_EMPTY + s), ((it / kTcStages) - 1) & 1, ctl, abort)) break;
+        const int s = it % kSt;
+        if (it >= kSt && !wait1_ab(bar(TB_EMPTY + s), ((it / kSt) - 1) & 1, ctl, abort)) break;
         if (held && it == 0) continue;  // failure-detection test: this tile never arrives
         const int qtile = q0 + it;
         const uint32_t st = sbase + L::kStageOff + s * L::kStage;
-        const size_t qo = hb + static_cast<size_t>(qtile) * kQ * D;
-        mbar_arrive_expect_tx(bar(TB_FULL + s), 3 * 8192 + 512);
-        bulk_load(st + L::kSQ, ws.qc + qo, 8192, bar(TB_FULL + s));
-        bulk_load(st + L::kSDoh, ws.doh + qo, 8192, bar(TB_FULL + s));
-        bulk_load(st + L::kSDoc, ws.doc + qo, 8192, bar(TB_FULL + s));
+        mbar_arrive_expect_tx(bar(TB_FULL + s), (2 * L::kNH + 1) * 8192 + 512);
+        if constexpr (D == 64) {
+          const size_t qo = hb + static_cast<size_t>(qtile) * kQ * D;
+          bulk_load(st + L::kSQ, ws.qc + qo, 8192, bar(TB_FULL + s));
+          bulk_load(st + L::kSDoh, ws.doh + qo, 8192, bar(TB_FULL + s));
+          bulk_load(st + L::kSDoc, ws.doc + qo, 8192, bar(TB_FULL + s));
+        } else {
+          const int r = hr + qtile * kQ;
+          for (int x = 0; x < 2; x++) {
+            sagefp4::tma_load_2d(st + L::kSQ + 8192 * x, &maps.q, 128 * x, r, bar(TB_FULL + s));
+            sagefp4::tma_load_2d(st + L::kSDoh + 8192 * x, &maps.doh, 128 * x, r, bar(TB_FULL + s));
+          }
+          sagefp4::tma_load_2d(st + L::kSDoc, &maps.doc, 128 * dh, r, bar(TB_FULL + s));
+        }
         bulk_load(st + L::kSL, ws.l2 + hrow + static_cast<size_t>(qtile) * kQ, 256, bar(TB_FULL + s));
         bulk_load(st + L::kSD, ws.dd + hrow + static_cast<size_t>(qtile) * kQ, 256, bar(TB_FULL + s));
         issued = it + 1;
       }
       if (*abort) {
         // let every copy this thread issued land before the CTA exits
-        for (int last = issued - 1; last >= 0 && last >= issued - kTcStages; last--)
+        for (int last = issued - 1; last >= 0 && last >= issued - kSt; last--)
           if (!(held && last == 0)) {
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(bar(TB_FULL + last % kTcStages), (last / kTcStages) & 1) &&
-                   globaltimer_ns() - t0 < ctl.limit) {
+            while (!mbar_try_wait(bar(TB_FULL + last % kSt), (last / kSt) & 1) && globaltimer_ns() - t0 < ctl.limit) {
             }
           }
         const uint64_t t0 = globaltimer_ns();
@@ -934,26 +966,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // ---- MMA issue: the whole warp, one elected lane issues
       // B MN-major for dV and dK (dO^ and Q^ as [64 q][64 d] rows)
       const uint32_t id = idesc_f16(128, 64), idb = idesc_f16(128, 64) | (1u << 16), idq = idesc_f16_mn(128, 64);
-      // dQ = dS^ K^, MN-major: a K step of 16 rows moves 2048 bytes (+128)
-      const uint64_t dqa = desc_mn(sbase + L::kCodesOff + L::kCS, 0, L::kCodes), dqb = desc_mn(sbase + L::kK, 0, L::kCodes);
-      bool ok = waitw_ab(bar(TB_FIXED), 0, ctl, abort) && waitw_ab(bar(TB_KVT), 0, ctl, abort);
+      // dQ = dS^ K^, MN-major: a K step of 16 rows moves 2048 bytes (+128);
+      // K^'s 64 columns of this CTA's half
+      const uint64_t dqa = desc_mn(sbase + L::kCodesOff + L::kCS, 0, L::kCodes);
+      const uint64_t dqb = desc_mn(sbase + L::kK + dh * L::kTile, 0, L::kCodes);
+      // S^T and dP^T at D = 128: K^ and V from shared memory (a 64-wide half
+      // is 16 KB, +1024)
+      const uint64_t dk0 = desc_k64(sbase + L::kK, 0), dv0 = desc_k64(sbase + L::kV, 0);
+      bool ok = waitw_ab(bar(TB_FIXED), 0, ctl, abort) && (D != 64 || waitw_ab(bar(TB_KVT), 0, ctl, abort));
       auto issue_sdp = [&](int it) {
-        const int s = it % kTcStages, b = it & 1;
-        if (!waitw_ab(bar(TB_FULL + s), (it / kTcStages) & 1, ctl, abort)) return false;
+        const int s = it % kSt, b = it & 1;
+        if (!waitw_ab(bar(TB_FULL + s), (it / kSt) & 1, ctl, abort)) return false;
         // buffer b: dV and dK of tile it - 2 have read its P^^T and dS^^T (the
         // latest completion of PDONE can be tile it - 2's: tile it - 1's dV and
         // dK are issued after this)
         if (it >= 2 && !waitw_ab(bar(TB_PDONE), (it - 2) & 1, ctl, abort)) return false;
         tc_fence_after();
         const uint32_t st = sbase + L::kStageOff + s * L::kStage;
-        // descriptors built once per operand; a K step of 16 moves 32 bytes (+2)
+        // descriptors built once per operand; a K step of 16 moves 32 bytes
+        // (+2), a 64-wide half of Q^ or dO (64 rows) 8 KB (+512)
         const uint64_t dq = desc_k64(st + L::kSQ, 0), ddo = desc_k64(st + L::kSDoh, 0);
         if (elect1()) {
+          if constexpr (D == 64) {
 #pragma unroll
-          for (int k = 0; k < 4; k++) mma_f16_tc_ta(tmem + kTcS + 64 * b, tmem + kTcK + 8 * k, dq + 2 * k, id, k > 0);
+            for (int k = 0; k < 4; k++) mma_f16_tc_ta(tmem + kTcS + 64 * b, tmem + kTcK + 8 * k, dq + 2 * k, id, k > 0);
 #pragma unroll
-          for (int k = 0; k < 4; k++)
-            mma_f16_tc_ta(tmem + kTcDp + 64 * b, tmem + kTcV + 8 * k, ddo + 2 * k, id, k > 0);
+            for (int k = 0; k < 4; k++)
+              mma_f16_tc_ta(tmem + kTcDp + 64 * b, tmem + kTcV + 8 * k, ddo + 2 * k, id, k > 0);
+          } else {
+#pragma unroll
+            for (int k = 0; k < D / 16; k++)
+              mma_f16_tc(tmem + kTcS + 64 * b, dk0 + 1024 * (k >> 2) + 2 * (k & 3), dq + 512 * (k >> 2) + 2 * (k & 3),
+                         id, k > 0);
+#pragma unroll
+            for (int k = 0; k < D / 16; k++)
+              mma_f16_tc(tmem + kTcDp + 64 * b, dv0 + 1024 * (k >> 2) + 2 * (k & 3),
+                         ddo + 512 * (k >> 2) + 2 * (k & 3), id, k > 0);
+          }
           tc_commit(bar(TB_SDONE + b));
         }
         __syncwarp();
@@ -961,7 +1010,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       };
       if (ok) ok = issue_sdp(0);
       for (int it = 0; ok && it < niter; it++) {
-        const int s = it % kTcStages, b = it & 1;
+        const int s = it % kSt, b = it & 1;
         if (it + 1 < niter && !(ok = issue_sdp(it + 1))) break;
         if (!(ok = waitw_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort))) break;
         if (b == 1) {
@@ -985,7 +1034,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (it >= 1 && !(ok = waitw_ab(bar(TB_PFREE), (it - 1) & 1, ctl, abort))) break;
         tc_fence_after();
         const uint32_t st = sbase + L::kStageOff + s * L::kStage;
-        const uint64_t ddoc = desc_mn(st + L::kSDoc, 0, 8192), dqm = desc_mn(st + L::kSQ, 0, 8192);
+        // B: this CTA's 64 columns of dO^ and Q^, MN-major
+        const uint64_t ddoc = desc_mn(st + L::kSDoc, 0, 8192), dqm = desc_mn(st + L::kSQ + 8192 * dh, 0, 8192);
         // A: P^^T and dS^^T in tensor memory (8 columns a K step of 16 queries)
         if (elect1()) {
 #pragma unroll
@@ -1020,7 +1070,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float sq_next = ws.sq[static_cast<size_t>(bh) * nkt + (q0 >> 1)];
     float sdo_next = ws.sdo[static_cast<size_t>(bh) * nkt + (q0 >> 1)];
     for (int it = 0; it < niter; it++) {
-      const int s = it % kTcStages, b = it & 1, qtile = q0 + it;
+      const int s = it % kSt, b = it & 1, qtile = q0 + it;
       const float sq = sq_next, sdo = sdo_next;
       if (it + 1 < niter) {
         sq_next = ws.sq[static_cast<size_t>(bh) * nkt + ((qtile + 1) >> 1)];
@@ -1028,7 +1078,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // a failed wait is voted on below, before anything is published
       bool ok = waitw_ab(bar(TB_SDONE + b), (it >> 1) & 1, ctl, abort) &&
-                waitw_ab(bar(TB_FULL + s), (it / kTcStages) & 1, ctl, abort);
+                waitw_ab(bar(TB_FULL + s), (it / kSt) & 1, ctl, abort);
       tc_fence_after();
       // this half of the S^T and dP^T rows: two loads in flight, one wait
       uint32_t ru[2][32];
@@ -1147,10 +1197,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
     for (int i = 0; i < 32; i++) accv[i] = acck[i] = 0;
     float fq[2] = {0.0f, 0.0f};  // dQ scales of the pair's two tiles
-    // K^ and V rows (this thread's key) into tensor memory, the A operands of
-    // S^T and dP^T for the CTA's whole life
-    bool kv_ok = waitw_ab(bar(TB_FIXED), 0, ctl, abort);
-    if (kv_ok) {
+    // D = 64: K^ and V rows (this thread's key) into tensor memory, the A
+    // operands of S^T and dP^T for the CTA's whole life
+    bool kv_ok = D != 64 || waitw_ab(bar(TB_FIXED), 0, ctl, abort);
+    if (D == 64 && kv_ok) {
 #pragma unroll
       for (int which = 0; which < 2; which++) {
         uint32_t w[32];
@@ -1221,7 +1271,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           if (lane == 0) {
-            tma_reduce_add_2d(&tm_dq, smem_addr(wt), 32 * hh, y0);
+            tma_reduce_add_2d(&maps.dq, smem_addr(wt), 64 * dh + 32 * hh, y0);
             bulk_commit();
           }
         }
@@ -1237,7 +1287,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (key < N) {
 #pragma unroll
         for (int which = 0; which < 2; which++) {
-          uint16_t* dst = (which == 0 ? dv : dk) + (static_cast<size_t>(bh) * N + key) * D;
+          uint16_t* dst = (which == 0 ? dv : dk) + (static_cast<size_t>(bh) * N + key) * D + 64 * dh;
           const float f = which == 0 ? 1.0f : scale;
           const uint64_t* acc = which == 0 ? accv : acck;
 #pragma unroll
@@ -2101,20 +2151,26 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool C>
+template <int D, bool C>
 cudaError_t launch_dkdv_tc(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int N, float scale, cudaStream_t st,
                            uint64_t wait_ns, int withhold) {
   const uint64_t rows = static_cast<uint64_t>(BH) * ((N + kTok - 1) / kTok * kTok);
-  CUtensorMap tm;
-  if (rows > 0x7fffffffu || !make_map_f32(&tm, w.dqacc, 64, rows, 32, 32)) return cudaErrorInvalidValue;
+  BwdMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  if (rows > 0x7fffffffu || !make_map_f32(&maps.dq, w.dqacc, D, rows, 32, 32)) return cudaErrorInvalidValue;
+  if (D == 128 && (!make_map_u8(&maps.k, w.kc, 2 * D, rows, 128, 128) || !make_map_u8(&maps.v, w.vh, 2 * D, rows, 128, 128) ||
+                   !make_map_u8(&maps.q, w.qc, 2 * D, rows, 128, 64) || !make_map_u8(&maps.doh, w.doh, 2 * D, rows, 128, 64) ||
+                   !make_map_u8(&maps.doc, w.doc, 2 * D, rows, 128, 64)))
+    return cudaErrorInvalidValue;
   cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, dkdv_tc_kernel<C>);
+  cudaError_t e = cudaFuncGetAttributes(&attr, dkdv_tc_kernel<D, C>);
   if (e != cudaSuccess) return e;
   if (attr.numRegs != 65536 / kTcThreads) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(dkdv_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::kAlloc);
+  e = cudaFuncSetAttribute(dkdv_tc_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  const dim3 grid((N + kTok - 1) / kTok, BH);
-  dkdv_tc_kernel<C><<<grid, kTcThreads, TcSmem::kAlloc, st>>>(tm, w, dk, dv, N, scale, wait_ns, withhold);
+  // at D = 128 two CTAs per key tile, one per 64-column half of dV, dK, dQ
+  const dim3 grid((N + kTok - 1) / kTok, BH, D / 64);
+  dkdv_tc_kernel<D, C><<<grid, kTcThreads, TcSmem<D>::kAlloc, st>>>(maps, w, dk, dv, N, scale, wait_ns, withhold);
   return cudaGetLastError();
 }
 
@@ -2247,11 +2303,11 @@ int sagebwd_attn_bwd(void* dk, void* dv, int B, int H, int N, int D, int causal,
   const int BH = B * H;
   cudaError_t e;
   if (D == 64)
-    e = causal ? launch_dkdv_tc<true>(w, dkb, dvb, BH, N, scale, st, kWaitNs, 0)
-               : launch_dkdv_tc<false>(w, dkb, dvb, BH, N, scale, st, kWaitNs, 0);
+    e = causal ? launch_dkdv_tc<64, true>(w, dkb, dvb, BH, N, scale, st, kWaitNs, 0)
+               : launch_dkdv_tc<64, false>(w, dkb, dvb, BH, N, scale, st, kWaitNs, 0);
   else
-    e = causal ? launch_dkdv<128, true>(w, dkb, dvb, BH, N, scale, st)
-               : launch_dkdv<128, false>(w, dkb, dvb, BH, N, scale, st);
+    e = causal ? launch_dkdv_tc<128, true>(w, dkb, dvb, BH, N, scale, st, kWaitNs, 0)
+               : launch_dkdv_tc<128, false>(w, dkb, dvb, BH, N, scale, st, kWaitNs, 0);
   return from_cuda(e);
 }
 
@@ -2330,8 +2386,8 @@ int sagebwd_stall_test(int kernel, void* out0, void* out1, int B, int H, int N, 
                 : launch_fwd_tc<128, false>(w, o, lse, BH, N, scale, st, wait_limit_ns, 1);
   } else {
     uint16_t *dkb = static_cast<uint16_t*>(out0), *dvb = static_cast<uint16_t*>(out1);
-    e = D == 64 ? launch_dkdv_tc<false>(w, dkb, dvb, BH, N, scale, st, wait_limit_ns, 1)
-                : launch_dkdv<128, false>(w, dkb, dvb, BH, N, scale, st, wait_limit_ns, 1);
+    e = D == 64 ? launch_dkdv_tc<64, false>(w, dkb, dvb, BH, N, scale, st, wait_limit_ns, 1)
+                : launch_dkdv_tc<128, false>(w, dkb, dvb, BH, N, scale, st, wait_limit_ns, 1);
   }
   return from_cuda(e);
 }
