@@ -47,8 +47,7 @@ HBM_NOMINAL_GBS = 8000.0  # the "~8 TB/s" HBM3e figure the quantize target is qu
 
 
 TRAIN_METRIC = ("SageBwd 8-bit attention fwd+bwd TOPS (3.5*4*B*H*N^2*D/t, causal at half) on 1 GB300; "
-                "fraction of the measured 16-bit tensor peak of the instruction each kernel issues (tcgen05; "
-                "the D=128 backward: mma.sync)")
+                "fraction of the measured dense 16-bit tensor peak (tcgen05 kind::f16)")
 SAGEBWD_CALLS = ("quantize_qkv", "attn_fwd", "bwd_prep", "attn_bwd", "dq_out")
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one attn_fwd_kernel launch,
@@ -362,33 +361,27 @@ class SageBwdRun:
         return ev[0][0].elapsed_time(ev[-1][-1]), per
 
 
-def sagebwd_peak(kernel, w, fp16_mma_peak):
-    """The tensor peak a SageBwd attention kernel of workload w is judged
-    against: the ones that issue tcgen05.mma kind::f16 (the forward, and the
-    backward at D = 64) against the measured dense 16-bit GEMM peak (FP16 and
-    BF16 share the nominal rate); the backward at D = 128, warp-level FP16
-    mma.sync, against that instruction's measured rate."""
-    if kernel == "attn_fwd" or w.D == 64:
-        pk = peaks()
-        return pk["bf16_tflops"], f"{pk['src']} bf16 GEMM (burst), the tcgen05 kind::f16 rate"
-    return fp16_mma_peak, "measured live: FP16 mma.sync m16n8k16 (FP32 accumulate) probe, the instruction issued"
+def sagebwd_peak():
+    """The tensor peak the SageBwd attention kernels are judged against: they
+    issue tcgen05.mma kind::f16, so the measured dense 16-bit GEMM peak (FP16
+    and BF16 share the nominal rate)."""
+    pk = peaks()
+    return pk["bf16_tflops"], f"{pk['src']} bf16 GEMM (burst), the tcgen05 kind::f16 rate"
 
 
-def sagebwd_summary(w, per, fp16_mma_peak):
+def sagebwd_summary(w, per):
     """Per-call means and the roofline figures of the two attention kernels."""
     m = {nm: statistics.mean(v) for nm, v in per.items()}
     ops = w.ops
     fwd_tops = ops / (m["attn_fwd"] * 1e-3) / 1e12
     bwd_tops = 2.5 * ops / (m["attn_bwd"] * 1e-3) / 1e12
     step = sum(m.values())
-    fpeak, fsrc = sagebwd_peak("attn_fwd", w, fp16_mma_peak)
-    bpeak, bsrc = sagebwd_peak("attn_bwd", w, fp16_mma_peak)
+    peak, src = sagebwd_peak()
     return {"workload": w.name, "ms": m, "ms_per_step": step,
             "attn_fwd_tops": fwd_tops, "attn_bwd_tops": bwd_tops,
-            "attn_fwd_peak_tflops": fpeak, "attn_fwd_peak_src": fsrc,
-            "peak_tflops": bpeak, "peak_src": bsrc,
-            "attn_fwd_frac_of_peak": fwd_tops / fpeak,
-            "attn_bwd_frac_of_peak": bwd_tops / bpeak,
+            "peak_tflops": peak, "peak_src": src,
+            "attn_fwd_frac_of_peak": fwd_tops / peak,
+            "attn_bwd_frac_of_peak": bwd_tops / peak,
             "step_tops": 3.5 * ops / (step * 1e-3) / 1e12}
 
 
@@ -450,8 +443,7 @@ def run_sagebwd(args, world, rank, local):
     total_ms = max_over_ranks(total_ms, world)
     ms_step = total_ms / args.steps
     value = job_throughput(3.5 * w.ops, world, ms_step)
-    fp16_peak = SB.mma_peak_tops(1)
-    summ = sagebwd_summary(w, per, fp16_peak)
+    summ = sagebwd_summary(w, per)
 
     # end to end through the public API with host buffers: every step copies
     # q, k, v, dout from pinned host memory, runs forward and backward, and
@@ -507,11 +499,11 @@ def run_sagebwd(args, world, rank, local):
                            parallelism=f"weak, {world} independent batch(es)"),
             "kernels": summ,
             "roofline": {"bound": "tensor",
-                         "kernel": "attn_bwd (" + ("dkdv_tc_kernel" if w.D == 64 else "dkdv_kernel") + ")",
+                         "kernel": "attn_bwd (dkdv_tc_kernel)",
                          "achieved": summ["attn_bwd_tops"], "peak": summ["peak_tflops"], "unit": "TFLOP/s",
                          "frac": summ["attn_bwd_frac_of_peak"], "traffic": SAGEBWD_BWD_TRAFFIC.get(w.name),
                          "traffic_unit": "DRAM bytes (read + write) per attn_bwd launch, from ncu",
-                         "peak_src": summ["peak_src"], "fp16_mma_sync_measured_tflops": fp16_peak},
+                         "peak_src": summ["peak_src"]},
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clk.summary(),
             "gpu_launches": len(SAGEBWD_CALLS) * args.steps}), flush=True)
 
@@ -690,12 +682,11 @@ def main():
         from bit_attention_gb300 import sagebwd as SB
         from bit_attention_gb300.synth import TRAIN_WORKLOADS
         torch.cuda.empty_cache()
-        fp16_peak = SB.mma_peak_tops(1)
-        sbw = {"fp16_mma_measured_tflops": fp16_peak, "metric": TRAIN_METRIC}
+        sbw = {"metric": TRAIN_METRIC}
         for name in ("train_llama1b", "train_qwen3b"):
             run = SageBwdRun(SB, TRAIN_WORKLOADS[name], dev)
             _, per = run.time(5, 3, stream)
-            sbw[name] = sagebwd_summary(run.w, per, fp16_peak)
+            sbw[name] = sagebwd_summary(run.w, per)
             del run
             torch.cuda.empty_cache()
 

@@ -14,22 +14,21 @@
 // the unquantized P~); the backward recomputes P = exp(S - L) from the saved
 // log-sum-exp.
 //
-// The INT8 products on sm_103a.  This GPU has no INT8 form of tcgen05.mma,
-// and its warp-level INT8 MMA (m16n8k32) runs at a quarter of the FP16 one
-// (m16n8k16, FP32 accumulation).  An INT8 code is an integer in [-127, 127],
-// exact in FP16; the product of two is exact in FP32, and so is every sum of
-// such products below 2^24 (127^2 * 128 < 2^21 here).  So the six INT8
-// products run on the FP16 MMA with the codes stored as FP16 values, and give
-// the integer results an INT8 MMA would (sagebwd_int_mma_probe checks this on
-// the hardware).  Each block's integer sum is then scaled by its two block
-// scales in FP32.
+// The INT8 products on sm_103a.  Its INT8 tensor rates are far below its
+// FP16 ones (the warp-level INT8 MMA runs at a quarter of the FP16 one).  An
+// INT8 code is an integer in [-127, 127], exact in FP16; the product of two is
+// exact in FP32, and so is every sum of such products below 2^24 (127^2 * 128
+// < 2^21 here).  So the six INT8 products run as tcgen05.mma kind::f16 with
+// the codes stored as FP16 values, and give the integer results an INT8 MMA
+// would (the probes check this on the hardware for every operand form used).
+// Each block's integer sum is then scaled by its two block scales in FP32.
 //
 // Layout.  Every operand lives in the workspace as FP16 rows [token][D] whose
-// 16-byte chunks are XOR-permuted by (row & 7): any 8-row-aligned run of rows
-// is a bank-conflict-free shared-memory tile for ldmatrix after one bulk copy.
-// Operands needed transposed are read with ldmatrix.trans, and an MMA's FP32
-// accumulator fragment is, pairwise converted, the A fragment of the next MMA,
-// so no operand is stored twice.
+// 16-byte chunks are XOR-permuted by (row & 7) within each 128-byte half: an
+// 8-row-aligned run of 128-byte rows is the tensor core's 128-byte-swizzled
+// tile, read K-major (D the contraction) or MN-major (tokens the
+// contraction).  The codes of Q, dO and V are also stored transposed per
+// 64-token tile (V's are the forward's PV operand).
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -76,22 +75,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // ---------------------------------------------------------------- layout
 // Byte offset of logical (row, byte) in rows W bytes wide (W = 2D: 128 or
-// 256): the 16-byte chunk index is XORed with row & 7, so the eight rows one
-// ldmatrix reads at the same logical chunk fall in eight bank groups.
+// 256): the 16-byte chunk index is XORed with row & 7 (within each 128-byte
+// half), the tensor core's 128-byte swizzle; the eight rows of a chunk column
+// also fall in eight bank groups.
 __host__ __device__ __forceinline__ int swz(int row, int byte, int W) {
   return row * W + ((((byte >> 4) ^ (row & 7))) << 4) + (byte & 15);
-}
-
-// ---------------------------------------------------------------- helpers
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
 }
 
 __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -149,10 +137,6 @@ __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-__device__ __forceinline__ void red_add_v2(float* p, float a, float b) {
-  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
-}
-
 // Tensor reduction by the copy engine: the box of `map` at (x, y) += the
 // shared-memory tile at ssrc (laid out with the map's swizzle), element-wise
 // in the map's type, in this thread's bulk group.  wait_read: this thread's
@@ -167,10 +151,6 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
 
 struct Ctl {
   int32_t* status;
@@ -190,14 +170,6 @@ __device__ __forceinline__ bool waitw(uint32_t bar, uint32_t parity, const Ctl& 
       stop = 1;
     }
     if (__shfl_sync(kFull, stop, 0)) return false;
-  }
-}
-
-// Wait used only while abandoning work, so that no copy is still writing
-// shared memory when the CTA exits: bounded, result ignored.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const Ctl& c) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity) && globaltimer_ns() - t0 < c.limit) {
   }
 }
 
@@ -321,307 +293,6 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const uint16_t* __restr
   }
 }
 
-// ---------------------------------------------------------------- backward
-// One CTA of 8 warps per (128 keys, head); warp w owns keys 16w..16w+15.  The
-// CTA's K^ codes and FP16 V stay in shared memory; query tiles of 64 (Q^ and
-// dO^ codes, FP16 dO, L and D) stream through two stages.  Per query tile:
-// S^T, P^T, dV += P^^T dO^, dP^T (FP16), dS^T, dK += dS^^T Q^, and this key
-// tile's share of dQ = dS^ K^, added to an FP32 accumulator with vector
-// reductions.
-template <int D>
-struct BwdSmem {
-  static constexpr int kRow = 2 * D;
-  static constexpr int kKc = 0;
-  static constexpr int kVh = kKc + kTok * kRow;
-  static constexpr int kFixedBytes = 2 * kTok * kRow;
-  static constexpr int kQc = 0, kDoc = kQc + kQ * kRow, kDoh = kDoc + kQ * kRow;
-  static constexpr int kL = kDoh + kQ * kRow, kDd = kL + 4 * kQ;
-  static constexpr int kStage = kDd + 4 * kQ;
-  static constexpr int kStageOff = kFixedBytes;
-  static constexpr int kDs = kStageOff + 2 * kStage;   // staged dS^ codes, [128 keys][64 queries] FP16
-  static constexpr int kBarOff = kDs + kTok * kQ * 2;  // fixed, full[2]
-  static constexpr int kRedOff = kBarOff + 64;         // [2 kinds][8] floats
-  static constexpr int kBytes = kRedOff + 2 * 8 * 4;
-};
-
-// acc[D/8][4] += f * (A B): A the warp's 16-key x 64-query code fragments
-// (k = queries), B a 64-query x D tile of FP16 rows read transposed.  Eight
-// output n-blocks at a time with k outermost: eight independent MMA chains.
-template <int D>
-__device__ __forceinline__ void mma_fold(float (&acc)[D / 8][4], const uint32_t (&a)[4][4], uint32_t tile, float f,
-                                         int lane) {
-  const int j = lane >> 3;
-#pragma unroll
-  for (int ng = 0; ng < D / 64; ng++) {
-    float t[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; i++) t[i][0] = t[i][1] = t[i][2] = t[i][3] = 0.0f;
-#pragma unroll
-    for (int kc = 0; kc < 4; kc++) {
-#pragma unroll
-      for (int np = 0; np < 8; np += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(tile + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 16 * (8 * ng + np + (j >> 1)), 2 * D), b0, b1,
-                  b2, b3);
-        mma_f16(t[np], a[kc], b0, b1);
-        mma_f16(t[np + 1], a[kc], b2, b3);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 8; i++)
-#pragma unroll
-      for (int e = 0; e < 4; e++) acc[8 * ng + i][e] = fmaf(t[i][e], f, acc[8 * ng + i][e]);
-  }
-}
-
-template <int D, bool kCausal>
-__global__ void __launch_bounds__(kThreads, 1)
-    dkdv_kernel(Ws ws, uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, int N, float scale, uint64_t wait_ns,
-                int withhold) {
-  using L = BwdSmem<D>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int nkt = (N + kTok - 1) / kTok;
-  const int Np = nkt * kTok;
-  const int nqt = Np / kQ;
-  const int kb = blockIdx.x, bh = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3, j = lane >> 3;
-  const uint32_t sbase = smem_addr(smem);
-  const uint32_t fbar = sbase + L::kBarOff, full0 = fbar + 8;
-  float* redp = reinterpret_cast<float*>(smem + L::kRedOff);
-  const Ctl ctl{ws.status, wait_ns};
-  const size_t hb = static_cast<size_t>(bh) * Np * D;
-  const size_t hrow = static_cast<size_t>(bh) * Np;
-  // withhold (failure-detection test only): CTA 0 never issues its first
-  // query tile, so its wait for that tile runs out
-  const bool held = withhold && blockIdx.x == 0 && blockIdx.y == 0;
-  const int q0 = kCausal ? 2 * kb : 0;  // first query tile that sees these keys
-  const int niter = nqt - q0;
-
-  auto issue_stage = [&](int it) {
-    const int qtile = q0 + it, s = it & 1;
-    const uint32_t st = sbase + L::kStageOff + s * L::kStage, bar = full0 + 8 * s;
-    mbar_arrive_expect_tx(bar, L::kStage);
-    const size_t off = hb + static_cast<size_t>(qtile) * kQ * D;
-    bulk_load(st + L::kQc, ws.qc + off, kQ * L::kRow, bar);
-    bulk_load(st + L::kDoc, ws.doc + off, kQ * L::kRow, bar);
-    bulk_load(st + L::kDoh, ws.doh + off, kQ * L::kRow, bar);
-    bulk_load(st + L::kL, ws.l2 + hrow + static_cast<size_t>(qtile) * kQ, 4 * kQ, bar);
-    bulk_load(st + L::kDd, ws.dd + hrow + static_cast<size_t>(qtile) * kQ, 4 * kQ, bar);
-  };
-  if (threadIdx.x == 0) {
-    mbar_init(fbar, 1);
-    mbar_init(full0, 1);
-    mbar_init(full0 + 8, 1);
-    mbar_fence_init();
-  }
-  __syncthreads();
-  int issued = 0;  // query tiles whose copies thread 0 has issued
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(fbar, L::kFixedBytes);
-    const size_t off = hb + static_cast<size_t>(kb) * kTok * D;
-    bulk_load(sbase + L::kKc, ws.kc + off, kTok * L::kRow, fbar);
-    bulk_load(sbase + L::kVh, ws.vh + off, kTok * L::kRow, fbar);
-    if (held) issued = 1;
-    for (; issued < 2 && issued < niter; issued++) issue_stage(issued);
-  }
-  // every wait's outcome is voted on by the whole CTA: here the fixed tiles
-  // and the first query tile; each later tile's vote rides on the barrier
-  // that ends the previous tile's dK
-  bool ok = __syncthreads_and(waitw(fbar, 0, ctl) && waitw(full0, 0, ctl));
-
-  const float sk = ws.sk[static_cast<size_t>(bh) * nkt + kb];
-  const int key0 = kb * kTok + 16 * warp + g;  // this thread's keys: key0, key0 + 8
-  const float c2base = sk * scale * kLog2e;
-  const int arow = 16 * warp + ((j & 1) << 3) + (lane & 7);  // A-fragment row (key) this lane addresses
-  const uint32_t dsb = sbase + L::kDs;
-  float dka[D / 8][4], dva[D / 8][4];
-#pragma unroll
-  for (int i = 0; i < D / 8; i++)
-#pragma unroll
-    for (int e = 0; e < 4; e++) dka[i][e] = dva[i][e] = 0.0f;
-
-  // the query tile's block scales, read one tile ahead
-  float sq_next = ws.sq[static_cast<size_t>(bh) * nkt + (q0 >> 1)];
-  float sdo_next = ws.sdo[static_cast<size_t>(bh) * nkt + (q0 >> 1)];
-  for (int it = 0; it < niter && ok; it++) {
-    const int qtile = q0 + it, s = it & 1;
-    const uint32_t st = sbase + L::kStageOff + s * L::kStage;
-    const float sq = sq_next, sdo = sdo_next;
-    if (it + 1 < niter) {
-      sq_next = ws.sq[static_cast<size_t>(bh) * nkt + ((qtile + 1) >> 1)];
-      sdo_next = ws.sdo[static_cast<size_t>(bh) * nkt + ((qtile + 1) >> 1)];
-    }
-    // S^T = K^ Q^^T: 16 keys x 64 queries
-    float p[8][4];
-#pragma unroll
-    for (int nb = 0; nb < 8; nb++) p[nb][0] = p[nb][1] = p[nb][2] = p[nb][3] = 0.0f;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ks++) {
-      uint32_t ka[4];
-      ldsm_x4(sbase + L::kKc + swz(arow, 32 * ks + ((j >> 1) << 4), L::kRow), ka[0], ka[1], ka[2], ka[3]);
-#pragma unroll
-      for (int nb = 0; nb < 8; nb += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(st + L::kQc + swz(8 * (nb + (j >> 1)) + (lane & 7), 32 * ks + ((j & 1) << 4), L::kRow), b0, b1, b2,
-                b3);
-        mma_f16(p[nb], ka, b0, b1);
-        mma_f16(p[nb + 1], ka, b2, b3);
-      }
-    }
-    // P^T = exp2(S^T c - L); masked and padded entries 0
-    const float c2 = c2base * sq;
-    const float* Ls = reinterpret_cast<const float*>(smem + (st - sbase) + L::kL);
-    const float* Ds = reinterpret_cast<const float*>(smem + (st - sbase) + L::kDd);
-    const bool edge = (kCausal && qtile <= 2 * kb + 1) || (qtile * kQ + kQ > N) || (kb * kTok + kTok > N);
-    float pmax = 0.0f;
-#pragma unroll
-    for (int nb = 0; nb < 8; nb++) {
-      const int qc = 8 * nb + 2 * t;  // query column within the tile
-      const float2 lq = *reinterpret_cast<const float2*>(Ls + qc);
-#pragma unroll
-      for (int e = 0; e < 4; e++) {
-        float v = ex2(fmaf(p[nb][e], c2, (e & 1) ? lq.y : lq.x));  // lq holds -L
-        if (edge) {
-          const int query = qtile * kQ + qc + (e & 1);
-          const int key = key0 + ((e >> 1) << 3);
-          if (query >= N || key >= N || (kCausal && key > query)) v = 0.0f;
-        }
-        p[nb][e] = v;
-        pmax = fmaxf(pmax, v);
-      }
-    }
-    pmax = warp_max(pmax);
-    if (lane == 0) redp[warp] = pmax;
-    __syncthreads();
-    float amax = redp[0];
-#pragma unroll
-    for (int w = 1; w < 8; w++) amax = fmaxf(amax, redp[w]);
-    float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
-    // P^^T codes as A fragments (k = queries)
-    uint32_t pa[4][4];
-#pragma unroll
-    for (int kc = 0; kc < 4; kc++) {
-      pa[kc][0] = h2(code(p[2 * kc][0], inv), code(p[2 * kc][1], inv));
-      pa[kc][1] = h2(code(p[2 * kc][2], inv), code(p[2 * kc][3], inv));
-      pa[kc][2] = h2(code(p[2 * kc + 1][0], inv), code(p[2 * kc + 1][1], inv));
-      pa[kc][3] = h2(code(p[2 * kc + 1][2], inv), code(p[2 * kc + 1][3], inv));
-    }
-    // dV += s_P s_dO (P^^T dO^); dO^ read transposed
-    mma_fold<D>(dva, pa, st + L::kDoc, __fdiv_rn(amax, 127.0f) * sdo, lane);
-    // dP^T = V dO^T in FP16, then dS^T = P^T o (dP^T - D)
-    float dp[8][4];
-#pragma unroll
-    for (int nb = 0; nb < 8; nb++) dp[nb][0] = dp[nb][1] = dp[nb][2] = dp[nb][3] = 0.0f;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ks++) {
-      uint32_t va[4];
-      ldsm_x4(sbase + L::kVh + swz(arow, 32 * ks + ((j >> 1) << 4), L::kRow), va[0], va[1], va[2], va[3]);
-#pragma unroll
-      for (int nb = 0; nb < 8; nb += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(st + L::kDoh + swz(8 * (nb + (j >> 1)) + (lane & 7), 32 * ks + ((j & 1) << 4), L::kRow), b0, b1,
-                b2, b3);
-        mma_f16(dp[nb], va, b0, b1);
-        mma_f16(dp[nb + 1], va, b2, b3);
-      }
-    }
-    float smax = 0.0f;
-#pragma unroll
-    for (int nb = 0; nb < 8; nb++) {
-      const float2 dq2 = *reinterpret_cast<const float2*>(Ds + 8 * nb + 2 * t);
-#pragma unroll
-      for (int e = 0; e < 4; e++) {
-        p[nb][e] = p[nb][e] * (dp[nb][e] - ((e & 1) ? dq2.y : dq2.x));
-        smax = fmaxf(smax, fabsf(p[nb][e]));
-      }
-    }
-    smax = warp_max(smax);
-    if (lane == 0) redp[8 + warp] = smax;
-    __syncthreads();
-    amax = redp[8];
-#pragma unroll
-    for (int w = 1; w < 8; w++) amax = fmaxf(amax, redp[8 + w]);
-    inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
-    const float sds = __fdiv_rn(amax, 127.0f);
-    // dS^^T codes: A fragments for dK, and staged ([key][query]) for dQ
-    uint32_t da[4][4];
-#pragma unroll
-    for (int kc = 0; kc < 4; kc++) {
-      da[kc][0] = h2(code(p[2 * kc][0], inv), code(p[2 * kc][1], inv));
-      da[kc][1] = h2(code(p[2 * kc][2], inv), code(p[2 * kc][3], inv));
-      da[kc][2] = h2(code(p[2 * kc + 1][0], inv), code(p[2 * kc + 1][1], inv));
-      da[kc][3] = h2(code(p[2 * kc + 1][2], inv), code(p[2 * kc + 1][3], inv));
-      // rows key 16w+g and 16w+g+8; queries 16kc+2t (+1) and 16kc+8+2t (+1)
-      sts32(dsb + swz(16 * warp + g, 2 * (16 * kc + 2 * t), 2 * kQ), da[kc][0]);
-      sts32(dsb + swz(16 * warp + g + 8, 2 * (16 * kc + 2 * t), 2 * kQ), da[kc][1]);
-      sts32(dsb + swz(16 * warp + g, 2 * (16 * kc + 8 + 2 * t), 2 * kQ), da[kc][2]);
-      sts32(dsb + swz(16 * warp + g + 8, 2 * (16 * kc + 8 + 2 * t), 2 * kQ), da[kc][3]);
-    }
-    // dK += s_dS s_Q (dS^^T Q^); Q^ read transposed
-    mma_fold<D>(dka, da, st + L::kQc, sds * sq, lane);
-    // every warp's dS^ is staged and every warp is done with stage s; the
-    // same barrier votes on the next query tile's copy (issued a tile ago)
-    const bool next_ok = it + 1 >= niter || waitw(full0 + 8 * (s ^ 1), ((it + 1) >> 1) & 1, ctl);
-    ok = __syncthreads_and(next_ok);
-    if (threadIdx.x == 0 && ok && it + 2 < niter) issue_stage(issued++);
-    // dQ[64 x D] += scale s_dS s_K (dS^ K^): warp w takes query rows
-    // 16 (w & 3) and half of the D columns; dS^ and K^ read transposed
-    {
-      const float f = sds * sk * scale;
-      const int r0 = 16 * (warp & 3);
-      const int dh = (warp >> 2) * (D / 2);
-      float acc[D / 16][4];
-#pragma unroll
-      for (int i = 0; i < D / 16; i++) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
-#pragma unroll
-      for (int kc = 0; kc < kTok / 16; kc++) {
-        uint32_t a[4];
-        ldsm_x4_t(dsb + swz(16 * kc + ((j >> 1) << 3) + (lane & 7), 2 * (r0 + ((j & 1) << 3)), 2 * kQ), a[0], a[1],
-                  a[2], a[3]);
-#pragma unroll
-        for (int nd = 0; nd < D / 16; nd += 2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(sbase + L::kKc + swz(16 * kc + ((j & 1) << 3) + (lane & 7), 2 * dh + 16 * (nd + (j >> 1)), L::kRow),
-                    b0, b1, b2, b3);
-          mma_f16(acc[nd], a, b0, b1);
-          mma_f16(acc[nd + 1], a, b2, b3);
-        }
-      }
-      float* dq0 = ws.dqacc + (hrow + static_cast<size_t>(qtile) * kQ + r0 + g) * D + dh + 2 * t;
-#pragma unroll
-      for (int nd = 0; nd < D / 16; nd++) {
-        red_add_v2(dq0 + 8 * nd, acc[nd][0] * f, acc[nd][1] * f);
-        red_add_v2(dq0 + 8 * D + 8 * nd, acc[nd][2] * f, acc[nd][3] * f);
-      }
-    }
-  }
-  if (!ok) {
-    if (threadIdx.x == 0) {
-      drain_wait(fbar, 0, ctl);
-      for (int last = issued - 1; last >= 0 && last >= issued - 2; last--)
-        if (!(held && last == 0)) drain_wait(full0 + 8 * (last & 1), (last >> 1) & 1, ctl);
-    }
-    return;
-  }
-  // dK = scale * sum, dV: bf16 rows (keys) below N
-  const int key1 = key0 + 8;
-#pragma unroll
-  for (int nd = 0; nd < D / 8; nd++) {
-    const int d = 8 * nd + 2 * t;
-    if (key0 < N) {
-      const size_t ix = (static_cast<size_t>(bh) * N + key0) * D + d;
-      *reinterpret_cast<__nv_bfloat162*>(dk + ix) = __floats2bfloat162_rn(dka[nd][0] * scale, dka[nd][1] * scale);
-      *reinterpret_cast<__nv_bfloat162*>(dv + ix) = __floats2bfloat162_rn(dva[nd][0], dva[nd][1]);
-    }
-    if (key1 < N) {
-      const size_t ix = (static_cast<size_t>(bh) * N + key1) * D + d;
-      *reinterpret_cast<__nv_bfloat162*>(dk + ix) = __floats2bfloat162_rn(dka[nd][2] * scale, dka[nd][3] * scale);
-      *reinterpret_cast<__nv_bfloat162*>(dv + ix) = __floats2bfloat162_rn(dva[nd][2], dva[nd][3]);
-    }
-  }
-}
-
 // ---------------------------------------------------------------- tcgen05
 // Instruction descriptor of tcgen05.mma kind::f16: FP16 A and B (formats 0),
 // FP32 accumulator (bits 4-5 = 1), both operands K-major, N >> 3 in bits
@@ -696,7 +367,7 @@ __device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int k0, uint32_t bloc
   return smem_desc(tile + 128 * k0, block_stride, 1024, kSwizzle128B);
 }
 
-// ---------------------------------------------------------------- backward, tcgen05 (D = 64)
+// ---------------------------------------------------------------- backward, tcgen05
 // The same backward with all five products on the 5th-generation tensor
 // cores, issued asynchronously into tensor memory by one thread while other
 // warps work: per 64-query tile the four with 128 keys as rows -- S^T = K^ Q^^T,
@@ -1313,7 +984,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// ---------------------------------------------------------------- forward, tcgen05 (D = 64)
+// ---------------------------------------------------------------- forward, tcgen05
 // The forward with S = Q^ K^^T and O_t = P~^ V^ on the 5th-generation tensor
 // cores (M = 128 query rows; S: N = 128 keys; PV: N = 64), issued by one
 // thread into double-buffered tensor memory.  The warpgroups:
@@ -2093,17 +1764,6 @@ int check_device() {
   const bool ok = (major == 10 && minor == 3);
   if (dev >= 0 && dev < 64) cache[dev] = ok ? 1 : 2;
   return ok ? SAGE_FP4_OK : SAGE_FP4_EUNSUPPORTED;
-}
-
-template <int D, bool C>
-cudaError_t launch_dkdv(const Ws& w, uint16_t* dk, uint16_t* dv, int BH, int N, float scale, cudaStream_t st,
-                        uint64_t wait_ns = kWaitNs, int withhold = 0) {
-  const int smem = BwdSmem<D>::kBytes;
-  cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  const dim3 grid((N + kTok - 1) / kTok, BH);
-  dkdv_kernel<D, C><<<grid, kThreads, smem, st>>>(w, dk, dv, N, scale, wait_ns, withhold);
-  return cudaGetLastError();
 }
 
 // The tcgen05 backward (D = 64).  Its warpgroups' setmaxnreg budgets add up
