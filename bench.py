@@ -57,12 +57,15 @@ SAGEBWD_CALLS = ("quantize_qkv", "attn_fwd", "bwd_prep", "attn_bwd", "dq_out")
 ATTN_TRAFFIC = {
     "attn_fwd B4 H32 N4096 D128 k-channel-outliers": 113.32e6 + 80.14e6,
 }
-# the same for one SageBwd attn_bwd launch (dkdv_tc_kernel at D = 64), from one
-# ncu capture of the half-head case (B1 H16 N8192 D64 causal: 118.55 MB read,
-# 27.35 MB written) scaled by the heads (the traffic is per head)
+# the same for one SageBwd attn_bwd launch (dkdv_tc_kernel), from one ncu
+# capture of the half-head cases (B1 H16 N8192 D64 causal: 118.56 MB read,
+# 28.25 MB written; B1 H8 N8192 D128 causal: 183.27 MB read, 43.57 MB written)
+# scaled by the heads (the traffic is per head)
 SAGEBWD_BWD_TRAFFIC = {
-    "attn_train B1 H32 N8192 D64 causal iid": 2 * (118.55e6 + 27.35e6),
-    "attn_train B1 H16 N8192 D64 causal iid": 118.55e6 + 27.35e6,
+    "attn_train B1 H32 N8192 D64 causal iid": 2 * (118.56e6 + 28.25e6),
+    "attn_train B1 H16 N8192 D64 causal iid": 118.56e6 + 28.25e6,
+    "attn_train B1 H16 N8192 D128 causal k-channel-outliers": 2 * (183.27e6 + 43.57e6),
+    "attn_train B1 H8 N8192 D128 causal k-channel-outliers": 183.27e6 + 43.57e6,
 }
 
 

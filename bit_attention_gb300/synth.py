@@ -64,8 +64,11 @@ TRAIN_WORKLOADS = {
     "train_llama1b": Workload("attn_train B1 H32 N8192 D64 causal iid", 1, 32, 8192, 64, True, "iid"),
     "train_qwen3b": Workload("attn_train B1 H16 N8192 D128 causal k-channel-outliers", 1, 16, 8192, 128, True,
                              "k_channel_outliers"),
-    # half the heads of the Llama-1B shape: the case the full-set profiles capture
+    # half the heads of the Llama-1B and Qwen-3B shapes: the cases the
+    # full-set profiles capture
     "train_llama1b_h16": Workload("attn_train B1 H16 N8192 D64 causal iid", 1, 16, 8192, 64, True, "iid"),
+    "train_qwen3b_h8": Workload("attn_train B1 H8 N8192 D128 causal k-channel-outliers", 1, 8, 8192, 128, True,
+                                "k_channel_outliers"),
 }
 
 
