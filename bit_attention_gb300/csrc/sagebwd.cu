@@ -988,7 +988,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // The forward with S = Q^ K^^T and O_t = P~^ V^ on the 5th-generation tensor
 // cores (M = 128 query rows; S: N = 128 keys; PV: N = 64), issued by one
 // thread into double-buffered tensor memory.  The warpgroups:
-//   0  warp 0: bulk copies; warp 1: tensor-memory allocation and MMA issue
+//   0  warp 0: bulk copies of Q^ and K^; warp 1: tensor-memory allocation and
+//      MMA issue; warp 2: bulk copies of V^T (at D = 128)
 //   1, 2  softmax: each thread owns one query row and 64 of the tile's 128
 //      keys; the row maximum and the 64-row block maxima are exchanged
 //      through shared memory; P~'s INT8 codes go to tensor memory (tcgen05.st)
@@ -1015,12 +1016,15 @@ struct TfSmem {
   static constexpr int kAlloc = kBytes + 1024;
 };
 static_assert(TfSmem<128>::kAlloc <= 227 * 1024, "shared memory");
-// mbarriers (3 stages at most)
+// mbarriers (3 stages at most); K^ and V^T of a stage fill and empty
+// separately: K^ is free once S has been computed, V^T once PV has
 enum {
   FB_Q = 0,
-  FB_FULL = 1,
-  FB_EMPTY = 4,
-  FB_SDONE = 7,  // + buffer
+  FB_KFULL = 1,
+  FB_VFULL = 4,
+  FB_KEMPTY = 7,
+  FB_VEMPTY = 10,
+  FB_SDONE = 13,  // + buffer
   FB_PFULL = FB_SDONE + 2,
   FB_PVDONE = FB_PFULL + 2,
   FB_PVFREE = FB_PVDONE + 2,
@@ -1054,6 +1058,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   int withhold) {
   using L = TfSmem<D>;
   constexpr int kSt = L::kStages;
+  // K^ and V^T rings refilled separately (at D = 64 together: measured 3%
+  // faster, the softmax sets the pace there)
+  constexpr bool kSplit = D == 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(smem);
@@ -1078,8 +1085,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(FB_Q), 1);
     for (int s = 0; s < kSt; s++) {
-      mbar_init(bar(FB_FULL + s), 1);
-      mbar_init(bar(FB_EMPTY + s), 1);  // the MMA commit after PV
+      mbar_init(bar(FB_KFULL + s), 1);
+      mbar_init(bar(FB_VFULL + s), 1);
+      mbar_init(bar(FB_KEMPTY + s), 1);  // the MMA commit after S
+      mbar_init(bar(FB_VEMPTY + s), 1);  // the MMA commit after PV
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(bar(FB_SDONE + b), 1);
@@ -1102,32 +1111,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (wg == 0) {
     sagefp4::regs_dec<TcRegs::kCtl>();
-    if (warp == 0 && lane == 0) {
-      // ---- producer
+    if ((warp == 0 || (kSplit && warp == 2)) && lane == 0) {
+      // ---- producers: warp 0 Q^ and the K^ tiles, warp 2 the V^T tiles,
+      // each ring refilled as soon as its own product has read the slot (at
+      // D = 64 warp 0 copies both, and a stage is refilled after PV)
+      const bool isk = warp == 0;
       const int hrow = bh * Np;  // the head's first row in [B*H*Np][D]
-      mbar_arrive_expect_tx(bar(FB_Q), D / 64 * L::kHalf);
-      load_rows<D>(sbase + L::kQ, ws.qc, &tm_q, hrow + qt * kTok, bar(FB_Q));
-      const bool held = withhold && blockIdx.x == 0 && blockIdx.y == 0;
+      if (isk) {
+        mbar_arrive_expect_tx(bar(FB_Q), D / 64 * L::kHalf);
+        load_rows<D>(sbase + L::kQ, ws.qc, &tm_q, hrow + qt * kTok, bar(FB_Q));
+      }
+      const int full = isk ? FB_KFULL : FB_VFULL, empty = isk && kSplit ? FB_KEMPTY : FB_VEMPTY;
+      const bool held = isk && withhold && blockIdx.x == 0 && blockIdx.y == 0;
       int issued = 0;
       for (int kt = 0; kt < nkt; kt++) {
         const int s = kt % kSt;
-        if (kt >= kSt && !wait1_ab(bar(FB_EMPTY + s), ((kt / kSt) - 1) & 1, ctl, abort)) break;
+        if (kt >= kSt && !wait1_ab(bar(empty + s), ((kt / kSt) - 1) & 1, ctl, abort)) break;
         if (held && kt == 0) continue;  // failure-detection test: this tile never arrives
         const uint32_t st = sbase + L::kStageOff + s * L::kStage;
-        mbar_arrive_expect_tx(bar(FB_FULL + s), L::kStage);
-        load_rows<D>(st + L::kSK, ws.kc, &tm_k, hrow + kt * kTok, bar(FB_FULL + s));
-        bulk_load(st + L::kSV, ws.vct + hb + static_cast<size_t>(kt) * kTok * D, L::kStage / 2, bar(FB_FULL + s));
+        mbar_arrive_expect_tx(bar(full + s), kSplit ? L::kStage / 2 : L::kStage);
+        if (isk) load_rows<D>(st + L::kSK, ws.kc, &tm_k, hrow + kt * kTok, bar(full + s));
+        if (!isk || !kSplit)
+          bulk_load(st + L::kSV, ws.vct + hb + static_cast<size_t>(kt) * kTok * D, L::kStage / 2, bar(full + s));
         issued = kt + 1;
       }
       if (*abort) {
         for (int last = issued - 1; last >= 0 && last >= issued - kSt; last--)
           if (!(held && last == 0)) {
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(bar(FB_FULL + last % kSt), (last / kSt) & 1) && globaltimer_ns() - t0 < ctl.limit) {
+            while (!mbar_try_wait(bar(full + last % kSt), (last / kSt) & 1) && globaltimer_ns() - t0 < ctl.limit) {
             }
           }
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar(FB_Q), 0) && globaltimer_ns() - t0 < ctl.limit) {
+        if (isk) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(bar(FB_Q), 0) && globaltimer_ns() - t0 < ctl.limit) {
+          }
         }
       }
     } else if (warp == 1) {
@@ -1140,7 +1158,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = waitw_ab(bar(FB_Q), 0, ctl, abort);
       auto issue_s = [&](int kt) {
         const int s = kt % kSt, b = kt & 1;
-        if (!waitw_ab(bar(FB_FULL + s), (kt / kSt) & 1, ctl, abort)) return false;
+        if (!waitw_ab(bar(FB_KFULL + s), (kt / kSt) & 1, ctl, abort)) return false;
         // buffer b: PV of tile kt - 2 has read its P^ (and so the softmax has
         // read its S); PV's latest completion can be tile kt - 2's here
         if (kt >= 2 && !waitw_ab(bar(FB_PVDONE + b), ((kt >> 1) - 1) & 1, ctl, abort)) return false;
@@ -1152,6 +1170,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mma_f16_tc(tmem + kTfS + 128 * b, dq0 + 1024 * (k >> 2) + 2 * (k & 3), dks + 1024 * (k >> 2) + 2 * (k & 3),
                        idS, k > 0);
           tc_commit(bar(FB_SDONE + b));
+          if constexpr (kSplit) tc_commit(bar(FB_KEMPTY + s));
         }
         __syncwarp();
         return true;
@@ -1162,6 +1181,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (kt + 1 < nkt && !(ok = issue_s(kt + 1))) break;
         if (!(ok = waitw_ab(bar(FB_PFULL + b), (kt >> 1) & 1, ctl, abort))) break;
         if (kt >= 2 && !(ok = waitw_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort))) break;
+        if (kSplit && !(ok = waitw_ab(bar(FB_VFULL + s), (kt / kSt) & 1, ctl, abort))) break;
         tc_fence_after();
         // A: P^ over S's first 64 columns (8 columns a K step of 16 keys)
         const uint64_t dvs = desc_k64(sbase + L::kStageOff + s * L::kStage + L::kSV, 0);
@@ -1171,7 +1191,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mma_f16_tc_ta(tmem + kTfPv + D * b, tmem + kTfS + 128 * b + 8 * k, dvs + 8 * D * (k >> 2) + 2 * (k & 3),
                           idPV, k > 0);
           tc_commit(bar(FB_PVDONE + b));
-          tc_commit(bar(FB_EMPTY + s));
+          tc_commit(bar(FB_VEMPTY + s));
         }
         __syncwarp();
       }
