@@ -405,12 +405,20 @@ struct TcSmem {
   static constexpr int kK = 0;             // K^ codes [kNH][128 keys][64]
   static constexpr int kV = kNH * kTile;   // FP16 V [kNH][128 keys][64]
   static constexpr int kStageOff = 2 * kNH * kTile;
-  // stage: Q^ [kNH][64 q][64], FP16 dO [kNH][64 q][64], dO^ of this CTA's
-  // half [64 q][64], -L, D
+  // At D = 64 one ring of query tiles, a stage holding Q^ [64 q][64], FP16
+  // dO [64 q][64], dO^ [64 q][64], -L and D.  At D = 128 two rings: ring X
+  // (S^T and dP^T's operands: Q^ [2][64 q][64], FP16 dO [2][64 q][64]),
+  // refilled once those two products are computed, and ring Y (dV and dK's
+  // operands: this CTA's halves of Q^ and dO^, [64 q][64] each; -L and D
+  // apart, at kLdOff), refilled once dV and dK are.  So the next tiles'
+  // copies are not on the path from one tile's dV and dK to the next S^T.
+  static constexpr bool kSplit = D == 128;
   static constexpr int kSQ = 0, kSDoh = kNH * 8192, kSDoc = 2 * kNH * 8192, kSL = kSDoc + 8192, kSD = kSL + 256;
-  static constexpr int kStage = (kSD + 256 + 1023) / 1024 * 1024;
-  static constexpr int kStages = D == 64 ? 3 : 2;
-  static constexpr int kCodesOff = kStageOff + kStages * kStage;
+  static constexpr int kStage = kSplit ? 2 * kNH * 8192 : (kSD + 256 + 1023) / 1024 * 1024;
+  static constexpr int kStages = kSplit ? 2 : 3;
+  static constexpr int kYOff = kStageOff + kStages * kStage;
+  static constexpr int kYQ = 0, kYDoc = 8192, kYStage = 16384, kYStages = 3;
+  static constexpr int kCodesOff = kYOff + (kSplit ? kYStages * kYStage : 0);
   // codes buffer: dS^T [128 keys][64 q] (dQ's A operand, read MN-major)
   static constexpr int kCS = 0, kCodes = kTile;
   // dQ staging: per fold warp a [32 rows][32 FP32] tile, 128-byte swizzled
@@ -418,7 +426,8 @@ struct TcSmem {
   static constexpr int kBarOff = kDqOff + 128 * 128;
   static constexpr int kNumBars = 32;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // tmem slot, abort flag, red[2][2][8], scal[4][4]
-  static constexpr int kBytes = kMiscOff + 256;
+  static constexpr int kLdOff = kMiscOff + 256;  // ring Y's -L and D: [kYStages][2][64] floats
+  static constexpr int kBytes = kLdOff + (kSplit ? kYStages * 512 : 0);
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
 };
 // mbarrier indices
@@ -435,7 +444,9 @@ enum {
   TB_QFREE = TB_QDONE + 1,
   TB_KVT = TB_QFREE + 1,     // K^ and V copied into tensor memory
   TB_DRAIN = TB_KVT + 1,
-  TB_COUNT
+  TB_YFULL = TB_DRAIN + 1,  // + ring Y slot (3, D = 128)
+  TB_YEMPTY = TB_YFULL + 3,
+  TB_COUNT = TB_YEMPTY + 3
 };
 static_assert(TB_COUNT <= 32, "barriers");
 static_assert(TcSmem<128>::kAlloc <= 227 * 1024, "shared memory");
@@ -527,7 +538,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     dkdv_tc_kernel(const __grid_constant__ BwdMaps maps, Ws ws, uint16_t* __restrict__ dk,
                    uint16_t* __restrict__ dv, int N, float scale, uint64_t wait_ns, int withhold) {
   using L = TcSmem<D>;
-  constexpr int kSt = L::kStages;
+  constexpr int kSt = L::kStages, kYSt = L::kYStages;
+  constexpr bool kSplit = L::kSplit;
   const int dh = D == 64 ? 0 : static_cast<int>(blockIdx.z);  // this CTA's 64 columns of dV, dK, dQ
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, by pointer arithmetic on the shared array (so
@@ -554,7 +566,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(bar(TB_FIXED), 1);
     for (int s = 0; s < kSt; s++) {
       mbar_init(bar(TB_FULL + s), 1);
-      mbar_init(bar(TB_EMPTY + s), 1 + 8);  // the MMA commit + the softmax warps
+      mbar_init(bar(TB_EMPTY + s), kSplit ? 1 : 1 + 8);  // the MMA commit (+ the softmax warps: -L, D)
+    }
+    for (int s = 0; s < (kSplit ? kYSt : 0); s++) {
+      mbar_init(bar(TB_YFULL + s), 1);
+      mbar_init(bar(TB_YEMPTY + s), 1 + 8);  // the MMA commit + the softmax warps
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(bar(TB_SDONE + b), 1);
@@ -581,8 +597,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (wg == 0) {
     sagefp4::regs_dec<TcRegs::kCtl>();
-    if (warp == 0 && lane == 0) {
-      // ---- producer
+    if (kSplit && warp == 2 && lane == 0) {
+      // ---- producer of ring Y (D = 128)
+      const int hr = static_cast<int>(hrow);
+      int issued = 0;
+      for (int it = 0; it < niter; it++) {
+        const int y = it % kYSt;
+        if (it >= kYSt && !wait1_ab(bar(TB_YEMPTY + y), ((it / kYSt) - 1) & 1, ctl, abort)) break;
+        const int qtile = q0 + it;
+        const uint32_t yb = sbase + L::kYOff + y * L::kYStage, ld = sbase + L::kLdOff + y * 512;
+        mbar_arrive_expect_tx(bar(TB_YFULL + y), 2 * 8192 + 512);
+        sagefp4::tma_load_2d(yb + L::kYQ, &maps.q, 128 * dh, hr + qtile * kQ, bar(TB_YFULL + y));
+        sagefp4::tma_load_2d(yb + L::kYDoc, &maps.doc, 128 * dh, hr + qtile * kQ, bar(TB_YFULL + y));
+        bulk_load(ld, ws.l2 + hrow + static_cast<size_t>(qtile) * kQ, 256, bar(TB_YFULL + y));
+        bulk_load(ld + 256, ws.dd + hrow + static_cast<size_t>(qtile) * kQ, 256, bar(TB_YFULL + y));
+        issued = it + 1;
+      }
+      if (*abort) {
+        for (int last = issued - 1; last >= 0 && last >= issued - kYSt; last--) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(bar(TB_YFULL + last % kYSt), (last / kYSt) & 1) && globaltimer_ns() - t0 < ctl.limit) {
+          }
+        }
+      }
+    } else if (warp == 0 && lane == 0) {
+      // ---- producer (of ring X at D = 128)
       const int hr = static_cast<int>(hrow);  // the head's first row in [B*H*Np]
       mbar_arrive_expect_tx(bar(TB_FIXED), 2 * L::kNH * L::kTile);
       if constexpr (D == 64) {
@@ -603,7 +642,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (held && it == 0) continue;  // failure-detection test: this tile never arrives
         const int qtile = q0 + it;
         const uint32_t st = sbase + L::kStageOff + s * L::kStage;
-        mbar_arrive_expect_tx(bar(TB_FULL + s), (2 * L::kNH + 1) * 8192 + 512);
+        mbar_arrive_expect_tx(bar(TB_FULL + s), kSplit ? L::kStage : (2 * L::kNH + 1) * 8192 + 512);
         if constexpr (D == 64) {
           const size_t qo = hb + static_cast<size_t>(qtile) * kQ * D;
           bulk_load(st + L::kSQ, ws.qc + qo, 8192, bar(TB_FULL + s));
@@ -615,10 +654,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             sagefp4::tma_load_2d(st + L::kSQ + 8192 * x, &maps.q, 128 * x, r, bar(TB_FULL + s));
             sagefp4::tma_load_2d(st + L::kSDoh + 8192 * x, &maps.doh, 128 * x, r, bar(TB_FULL + s));
           }
-          sagefp4::tma_load_2d(st + L::kSDoc, &maps.doc, 128 * dh, r, bar(TB_FULL + s));
         }
-        bulk_load(st + L::kSL, ws.l2 + hrow + static_cast<size_t>(qtile) * kQ, 256, bar(TB_FULL + s));
-        bulk_load(st + L::kSD, ws.dd + hrow + static_cast<size_t>(qtile) * kQ, 256, bar(TB_FULL + s));
+        if constexpr (!kSplit) {
+          bulk_load(st + L::kSL, ws.l2 + hrow + static_cast<size_t>(qtile) * kQ, 256, bar(TB_FULL + s));
+          bulk_load(st + L::kSD, ws.dd + hrow + static_cast<size_t>(qtile) * kQ, 256, bar(TB_FULL + s));
+        }
         issued = it + 1;
       }
       if (*abort) {
@@ -675,6 +715,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                          ddo + 512 * (k >> 2) + 2 * (k & 3), id, k > 0);
           }
           tc_commit(bar(TB_SDONE + b));
+          if constexpr (kSplit) tc_commit(bar(TB_EMPTY + s));
         }
         __syncwarp();
         return true;
@@ -703,10 +744,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         // the partials' buffer: the fold has read the previous tile's
         if (it >= 1 && !(ok = waitw_ab(bar(TB_PFREE), (it - 1) & 1, ctl, abort))) break;
+        const int y = kSplit ? it % kYSt : 0;
+        if (kSplit && !(ok = waitw_ab(bar(TB_YFULL + y), (it / kYSt) & 1, ctl, abort))) break;
         tc_fence_after();
-        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
         // B: this CTA's 64 columns of dO^ and Q^, MN-major
-        const uint64_t ddoc = desc_mn(st + L::kSDoc, 0, 8192), dqm = desc_mn(st + L::kSQ + 8192 * dh, 0, 8192);
+        const uint32_t st = sbase + L::kStageOff + s * L::kStage, yb = sbase + L::kYOff + y * L::kYStage;
+        const uint64_t ddoc = kSplit ? desc_mn(yb + L::kYDoc, 0, 8192) : desc_mn(st + L::kSDoc, 0, 8192);
+        const uint64_t dqm = kSplit ? desc_mn(yb + L::kYQ, 0, 8192) : desc_mn(st + L::kSQ + 8192 * dh, 0, 8192);
         // A: P^^T and dS^^T in tensor memory (8 columns a K step of 16 queries)
         if (elect1()) {
 #pragma unroll
@@ -716,7 +760,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int k = 0; k < 4; k++)
             mma_f16_tc_ta(tmem + kTcDk, tmem + kTcDp + 64 * b + 8 * k, dqm + 128 * k, idb, k > 0);
           tc_commit(bar(TB_PDONE));
-          tc_commit(bar(TB_EMPTY + s));
+          tc_commit(bar(kSplit ? TB_YEMPTY + y : TB_EMPTY + s));
         }
         __syncwarp();
       }
@@ -748,8 +792,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         sdo_next = ws.sdo[static_cast<size_t>(bh) * nkt + ((qtile + 1) >> 1)];
       }
       // a failed wait is voted on below, before anything is published
+      const int y = kSplit ? it % kYSt : 0;
       bool ok = waitw_ab(bar(TB_SDONE + b), (it >> 1) & 1, ctl, abort) &&
-                waitw_ab(bar(TB_FULL + s), (it / kSt) & 1, ctl, abort);
+                (kSplit ? waitw_ab(bar(TB_YFULL + y), (it / kYSt) & 1, ctl, abort)
+                        : waitw_ab(bar(TB_FULL + s), (it / kSt) & 1, ctl, abort));
       tc_fence_after();
       // this half of the S^T and dP^T rows: two loads in flight, one wait
       uint32_t ru[2][32];
@@ -763,8 +809,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         dp[i] = __uint_as_float(ru[1][i]);
       }
       // P^T = exp2(S^T c - L); masked and padded entries 0; dS^T = P^T o (dP^T - D)
-      const float* Ls = reinterpret_cast<const float*>(smem + L::kStageOff + s * L::kStage + L::kSL) + 32 * h;
-      const float* Ds = reinterpret_cast<const float*>(smem + L::kStageOff + s * L::kStage + L::kSD) + 32 * h;
+      const float* Ls = reinterpret_cast<const float*>(kSplit ? smem + L::kLdOff + y * 512
+                                                              : smem + L::kStageOff + s * L::kStage + L::kSL) + 32 * h;
+      const float* Ds = Ls + 64;
       const float c2 = c2base * sq;
       const bool edge = (kCausal && qtile <= 2 * kb + 1) || (qtile * kQ + kQ > N) || (kb * kTok + kTok > N);
       // (pairs of columns through the packed FP32 forms, each lane rounded
@@ -800,7 +847,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         smax = max3f(smax, max3f(fabsf(dp[q]), fabsf(dp[q + 1]), fabsf(dp[q + 2])), fabsf(dp[q + 3]));
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive1(bar(TB_EMPTY + s));  // L and D read
+      if (lane == 0) mbar_arrive1(bar(kSplit ? TB_YEMPTY + y : TB_EMPTY + s));  // L and D read
       // both maxima are >= 0 (or -0): the warp maximum of their bit patterns
       // with the sign bit cleared
       const uint32_t pm = redux_max_u32(__float_as_uint(pmax) & 0x7fffffffu);
