@@ -1083,10 +1083,11 @@ struct TfSmem {
   static constexpr int kStages = D == 64 ? 3 : 2;
   static constexpr int kBarOff = kStageOff + kStages * kStage;
   static constexpr int kMiscOff = kBarOff + 8 * 32;
-  // misc: tmem slot, abort, row max halves [2 parity][2][128], alpha [2][128],
-  // block max [2 parity][8 warps], beta [2][2], final l halves [2][128], m [128]
-  static constexpr int kXm = kMiscOff + 16, kAl = kXm + 2048, kBm = kAl + 1024, kBeta = kBm + 64,
-                       kLf = kBeta + 16, kMf = kLf + 1024;
+  // misc: tmem slot, abort, row max halves [2 parity][2][128], alpha [tile
+  // mod 4][128], block max [2 parity][8 warps], beta [tile mod 4][2], final l
+  // halves [2][128], m [128]
+  static constexpr int kXm = kMiscOff + 16, kAl = kXm + 2048, kBm = kAl + 2048, kBeta = kBm + 64,
+                       kLf = kBeta + 32, kMf = kLf + 1024;
   static constexpr int kBytes = kMf + 512;
   static constexpr int kAlloc = kBytes + 1024;
 };
@@ -1151,9 +1152,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
   float* xm = reinterpret_cast<float*>(smem + L::kXm);     // [2 parity][2 halves][128 rows]
-  float* al = reinterpret_cast<float*>(smem + L::kAl);     // [2 buffers][128 rows]
+  float* al = reinterpret_cast<float*>(smem + L::kAl);     // [tile mod 4][128 rows]
   float* bm = reinterpret_cast<float*>(smem + L::kBm);     // [2 parity][8 softmax warps]
-  float* beta = reinterpret_cast<float*>(smem + L::kBeta); // [2 buffers][2 row blocks]
+  float* beta = reinterpret_cast<float*>(smem + L::kBeta); // [tile mod 4][2 row blocks]
   float* lf = reinterpret_cast<float*>(smem + L::kLf);     // [2 halves][128 rows]
   float* mf = reinterpret_cast<float*>(smem + L::kMf);     // [128 rows]
 
@@ -1332,10 +1333,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // the row's maximum over both halves of the tile (xm by tile parity)
       xm[(2 * b + h) * 128 + row] = hm;
-      // alpha and beta of buffer b: the correction has read tile kt - 2's
-      ok = ok && (kt < 2 || waitw_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort));
-      // also publishes xm, and orders both halves' loads of S before P^
-      // overwrites its first 64 columns
+      // alpha and beta go to slot kt % 4, which the correction has read for
+      // tile kt - 4: S of this tile was issued after PV of tile kt - 2, and
+      // that PV after the correction had released tile kt - 4's PV buffer.
+      // The vote also publishes xm, and orders both halves' loads of S
+      // before P^ overwrites its first 64 columns
       if (!group_and(ok)) break;
       const float mt = fmaxf(hm, xm[(2 * b + 1 - h) * 128 + row]);
       // c2 > 0 keeps masked keys at -inf (c2 = 0 only when every score is 0)
@@ -1350,11 +1352,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float rp = valid ? ex2(fmaf(mt, c2, -mn)) : 0.0f;
       const uint32_t wmax = redux_max_u32(__float_as_uint(rp) & 0x7fffffffu);  // rp >= 0: bit order is value order
       if (lane == 0) bm[b * 8 + sw] = __uint_as_float(wmax);
-      if (h == 0) al[b * 128 + row] = alpha;
+      if (h == 0) al[(kt & 3) * 128 + row] = alpha;
       named_bar(3 + 2 * h + blk, 64);  // publishes bm to the block's other warp of this half
       const float amax = fmaxf(bm[b * 8 + 4 * h + 2 * blk], bm[b * 8 + 4 * h + 2 * blk + 1]);
       const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
-      if (h == 0 && wq == 2 * blk && lane == 0) beta[b * 2 + blk] = __fdiv_rn(amax, 127.0f) * sv_cur;
+      if (h == 0 && wq == 2 * blk && lane == 0) beta[(kt & 3) * 2 + blk] = __fdiv_rn(amax, 127.0f) * sv_cur;
       // one pass: P~ = exp2(s c2 - m), its row sum, and its codes
       // rint(P~ * inv): P~ * inv + 1.5 * 2^23 in one FMA rounds the exact
       // product to an integer (ties to even), and subtracting 1.5 * 2^23 is
@@ -1402,7 +1404,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!waitw_ab(bar(FB_PFULL + b), (kt >> 1) & 1, ctl, abort)) break;
       if (!waitw_ab(bar(FB_PVDONE + b), (kt >> 1) & 1, ctl, abort)) break;
       tc_fence_after();
-      const float alpha = al[b * 128 + row], bt = beta[b * 2 + blk];
+      const float alpha = al[(kt & 3) * 128 + row], bt = beta[(kt & 3) * 2 + blk];
       // o = pv * beta + o * alpha; o * 1 is o, so warps whose rows' maxima
       // all held skip the multiply
       const uint64_t bt2 = pack2(bt, bt), al2 = pack2(alpha, alpha);
