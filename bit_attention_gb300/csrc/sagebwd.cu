@@ -419,10 +419,13 @@ struct TcSmem {
   static constexpr int kYOff = kStageOff + kStages * kStage;
   static constexpr int kYQ = 0, kYDoc = 8192, kYStage = 16384, kYStages = 3;
   static constexpr int kCodesOff = kYOff + (kSplit ? kYStages * kYStage : 0);
-  // codes buffer: dS^T [128 keys][64 q] (dQ's A operand, read MN-major)
-  static constexpr int kCS = 0, kCodes = kTile;
+  // codes buffers: dS^T [128 keys][64 q] (dQ's A operand, read MN-major),
+  // one per tile: two at D = 128, four at D = 64, where the buffer a tile
+  // writes was last read by the dQ of tile t - 4's pair, which completed
+  // before dV and dK of tile t - 2 and so before this tile's S^T
+  static constexpr int kCS = 0, kCodes = kTile, kCodeBufs = kSplit ? 2 : 4;
   // dQ staging: per fold warp a [32 rows][32 FP32] tile, 128-byte swizzled
-  static constexpr int kDqOff = kCodesOff + 2 * kCodes;
+  static constexpr int kDqOff = kCodesOff + kCodeBufs * kCodes;
   static constexpr int kBarOff = kDqOff + 128 * 128;
   static constexpr int kNumBars = 32;
   static constexpr int kMiscOff = kBarOff + 8 * kNumBars;  // tmem slot, abort flag, red[2][2][8], scal[4][4]
@@ -733,12 +736,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int pr = it >> 1;
           if (pr >= 1 && !(ok = waitw_ab(bar(TB_QFREE), (pr - 1) & 1, ctl, abort))) break;
           tc_fence_after();
+          // (four codes buffers: pair pr reads buffers 2 (pr & 1) and 2 (pr & 1) + 1)
+          const uint64_t dqp = dqa + (L::kCodeBufs == 4 && (pr & 1) ? (2 * L::kCodes) >> 4 : 0);
           if (elect1()) {
 #pragma unroll
-            for (int k = 0; k < 8; k++) mma_f16_tc(tmem + kTcDq, dqa + 128 * k, dqb + 128 * k, idq, k > 0);
+            for (int k = 0; k < 8; k++) mma_f16_tc(tmem + kTcDq, dqp + 128 * k, dqb + 128 * k, idq, k > 0);
             tc_commit(bar(TB_QDONE));
-            tc_commit(bar(TB_CEMPTY + 0));
-            tc_commit(bar(TB_CEMPTY + 1));
+            if constexpr (L::kCodeBufs == 2) {
+              tc_commit(bar(TB_CEMPTY + 0));
+              tc_commit(bar(TB_CEMPTY + 1));
+            }
           }
           __syncwarp();
         }
@@ -856,9 +863,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         red[(b * 2 + 0) * 8 + sw] = __uint_as_float(pm);
         red[(b * 2 + 1) * 8 + sw] = __uint_as_float(sm);
       }
-      // the codes buffer is free once the pair's dQ (tiles it - 2, it - 1) has read it; the vote
-      // below also orders both halves' tensor-memory loads before the codes overwrite them
-      ok = ok && (it < 2 || waitw_ab(bar(TB_CEMPTY + b), ((it >> 1) - 1) & 1, ctl, abort));
+      // with two codes buffers, this tile's is free once the pair's dQ (tiles
+      // it - 2, it - 1) has read it; the vote below also orders both halves'
+      // tensor-memory loads before the codes overwrite them
+      if constexpr (L::kCodeBufs == 2)
+        ok = ok && (it < 2 || waitw_ab(bar(TB_CEMPTY + b), ((it >> 1) - 1) & 1, ctl, abort));
       if (!group_and(ok)) break;  // also publishes red[]
       const float4* r4 = reinterpret_cast<const float4*>(red + b * 16);
       const float4 p0 = r4[0], p1 = r4[1], s0 = r4[2], s1 = r4[3];
@@ -866,7 +875,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const float sa = fmaxf(max3f(max3f(s0.x, s0.y, s0.z), max3f(s0.w, s1.x, s1.y), s1.z), s1.w);
       const float pinv = pa > 0.0f ? __fdiv_rn(127.0f, pa) : 0.0f;
       const float sinv = sa > 0.0f ? __fdiv_rn(127.0f, sa) : 0.0f;
-      uint8_t* cbuf = smem + L::kCodesOff + b * L::kCodes;
+      uint8_t* cbuf = smem + L::kCodesOff + (it % L::kCodeBufs) * L::kCodes;
       const uint64_t pp = pack2(pinv, pinv), ss = pack2(sinv, sinv);
       // rint(x * inv) for a pair, as FP16x2: x * inv + 1.5 * 2^23 in one FMA
       // rounds the exact product to an integer (ties to even), and
