@@ -477,6 +477,13 @@ __device__ __forceinline__ bool waitw_ab(uint32_t bar, uint32_t parity, const Ct
 }
 
 // The same for a single thread.
+// Two bounded waits by a whole warp with one vote when both phases have
+// completed already (the usual case), else one after the other.
+__device__ __forceinline__ bool waitw2_ab(uint32_t bar0, uint32_t par0, uint32_t bar1, uint32_t par1, const Ctl& c,
+                                          volatile int* abort) {
+  if (__all_sync(kFull, mbar_try_wait(bar0, par0) && mbar_try_wait(bar1, par1))) return true;
+  return waitw_ab(bar0, par0, c, abort) && waitw_ab(bar1, par1, c, abort);
+}
 __device__ __forceinline__ bool wait1_ab(uint32_t bar, uint32_t parity, const Ctl& c, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -800,9 +807,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // a failed wait is voted on below, before anything is published
       const int y = kSplit ? it % kYSt : 0;
-      bool ok = waitw_ab(bar(TB_SDONE + b), (it >> 1) & 1, ctl, abort) &&
-                (kSplit ? waitw_ab(bar(TB_YFULL + y), (it / kYSt) & 1, ctl, abort)
-                        : waitw_ab(bar(TB_FULL + s), (it / kSt) & 1, ctl, abort));
+      bool ok = kSplit ? waitw2_ab(bar(TB_SDONE + b), (it >> 1) & 1, bar(TB_YFULL + y), (it / kYSt) & 1, ctl, abort)
+                       : waitw2_ab(bar(TB_SDONE + b), (it >> 1) & 1, bar(TB_FULL + s), (it / kSt) & 1, ctl, abort);
       tc_fence_after();
       // this half of the S^T and dP^T rows: two loads in flight, one wait
       uint32_t ru[2][32];
