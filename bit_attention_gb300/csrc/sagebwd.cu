@@ -736,14 +736,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (it + 1 < niter && !(ok = issue_sdp(it + 1))) break;
         if (!(ok = waitw_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort))) break;
         if (b == 1) {
-          // dQ of the pair (it - 1, it) first -- rows 0..63 from codes buffer
-          // 0, rows 64..127 from buffer 1, their only reader -- so that both
-          // buffers are released for the next tiles' codes; the fold has read
-          // the previous pair's dQ
+          // dQ of the pair (it - 1, it) first -- rows 0..63 from the codes
+          // buffer of tile it - 1, rows 64..127 from tile it's, their only
+          // reader -- so that the buffers are released for later tiles'
+          // codes early; the fold has read the previous pair's dQ.  With four
+          // buffers pair pr reads buffers 2 (pr & 1) and 2 (pr & 1) + 1.
           const int pr = it >> 1;
           if (pr >= 1 && !(ok = waitw_ab(bar(TB_QFREE), (pr - 1) & 1, ctl, abort))) break;
           tc_fence_after();
-          // (four codes buffers: pair pr reads buffers 2 (pr & 1) and 2 (pr & 1) + 1)
           const uint64_t dqp = dqa + (L::kCodeBufs == 4 && (pr & 1) ? (2 * L::kCodes) >> 4 : 0);
           if (elect1()) {
 #pragma unroll
