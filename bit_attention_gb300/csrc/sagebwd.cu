@@ -439,8 +439,12 @@ enum {
   TB_FULL = 1,             // + stage
   TB_EMPTY = 1 + kTcStages,  // + stage
   TB_SDONE = 1 + 2 * kTcStages,  // + buffer (2)
+  // + tile mod 4: the tile's codes and scales.  Four slots: the softmax can
+  // run up to four tiles ahead of the fold's test (tile t needs only the
+  // fold's release of tile t - 3's partials), which with two slots could
+  // complete a slot's phase twice before the fold tests it
   TB_CFULL = TB_SDONE + 2,
-  TB_CEMPTY = TB_CFULL + 2,
+  TB_CEMPTY = TB_CFULL + 4,
   TB_PDONE = TB_CEMPTY + 2,  // dV and dK partials (single buffer)
   TB_PFREE = TB_PDONE + 1,
   TB_QDONE = TB_PFREE + 1,   // dQ of a tile pair (single buffer)
@@ -584,9 +588,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(bar(TB_SDONE + b), 1);
-      mbar_init(bar(TB_CFULL + b), 8);
       mbar_init(bar(TB_CEMPTY + b), 1);  // the MMA commit after the pair's dQ
     }
+    for (int q = 0; q < 4; q++) mbar_init(bar(TB_CFULL + q), 8);
     mbar_init(bar(TB_PDONE), 1);
     mbar_init(bar(TB_PFREE), 4);
     mbar_init(bar(TB_QDONE), 1);
@@ -734,7 +738,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int it = 0; ok && it < niter; it++) {
         const int s = it % kSt, b = it & 1;
         if (it + 1 < niter && !(ok = issue_sdp(it + 1))) break;
-        if (!(ok = waitw_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort))) break;
+        if (!(ok = waitw_ab(bar(TB_CFULL + (it & 3)), (it >> 2) & 1, ctl, abort))) break;
         if (b == 1) {
           // dQ of the pair (it - 1, it) first -- rows 0..63 from the codes
           // buffer of tile it - 1, rows 64..127 from tile it's, their only
@@ -926,7 +930,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive1(bar(TB_CFULL + b));
+      if (lane == 0) mbar_arrive1(bar(TB_CFULL + (it & 3)));
     }
   } else {
     // ---- dV and dK folds, and dQ read out (warpgroup 3)
@@ -968,7 +972,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int it = 0; kv_ok && it < niter; it++) {
       const int b = it & 1;
       // CFULL: this tile's block scales (D = 128: block maxima) are written
-      if (!waitw_ab(bar(TB_CFULL + b), (it >> 1) & 1, ctl, abort)) break;
+      if (!waitw_ab(bar(TB_CFULL + (it & 3)), (it >> 2) & 1, ctl, abort)) break;
       const float* sc = scal + 4 * (it & 3);
       uint64_t fv, fk;
       if constexpr (kSplit) {
@@ -1077,21 +1081,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // ---------------------------------------------------------------- forward, tcgen05
 // The forward with S = Q^ K^^T and O_t = P~^ V^ on the 5th-generation tensor
 // cores (M = 128 query rows; S: N = 128 keys; PV: N = 64), issued by one
-// thread into double-buffered tensor memory.  The warpgroups:
-//   0  warp 0: bulk copies of Q^ and K^; warp 1: tensor-memory allocation and
-//      MMA issue; warp 2: bulk copies of V^T (at D = 128)
+// thread into double-buffered tensor memory.  A persistent CTA walks a fixed
+// list of work items, one 128-query tile of one head each (causal: the
+// longest first); the KV tiles of its items form one stream g = 0, 1, ...
+// that every role walks in the same order, so the next item's first tiles
+// overlap the current item's last ones and its epilogue.  The warpgroups:
+//   0  warp 0: bulk copies of Q^ (two slots, by item) and K^; warp 1:
+//      tensor-memory allocation and MMA issue; warp 2: bulk copies of V^T
+//      (at D = 128)
 //   1, 2  softmax: each thread owns one query row and 64 of the tile's 128
 //      keys; the row maximum and the 64-row block maxima are exchanged
 //      through shared memory; P~'s INT8 codes go to tensor memory (tcgen05.st)
 //      as the A operand of PV, each warpgroup writing its 64 keys
 //   3  correction: O in registers, rescaled by each row's factor and
-//      accumulated with each tile's PV times its block scales; the epilogue
+//      accumulated with each tile's PV times its block scales; each item's
+//      epilogue once the softmax has published the item's l and m
 // P~ blocks are 64 query rows x 128 keys, as in the warp-level forward.
 template <int D>
 struct TfSmem {
   static constexpr int kHalf = 128 * 128;          // 128 rows of 128 bytes
-  static constexpr int kQ = 0;                     // Q^ [D / 64 halves][128][64]
-  static constexpr int kStageOff = D / 64 * kHalf;
+  static constexpr int kQBytes = D / 64 * kHalf;   // Q^ [D / 64 halves][128][64]
+  static constexpr int kQ = 0;                     // two Q^ slots, by item
+  static constexpr int kStageOff = 2 * kQBytes;
   static constexpr int kSK = 0;                    // K^ [D / 64 halves][128 keys][64]
   static constexpr int kSV = D / 64 * kHalf;       // V^T [2 key halves][D][64 keys]
   static constexpr int kStage = 2 * D / 64 * kHalf;
@@ -1100,32 +1111,64 @@ struct TfSmem {
   static constexpr int kMiscOff = kBarOff + 8 * 32;
   // misc: tmem slot, abort, row max halves [2 parity][2][128], alpha [tile
   // mod 4][128], block max [2 parity][8 warps], beta [tile mod 4][2], final l
-  // halves [2][128], m [128]
+  // halves [2 item slots][2][128], m [2 item slots][128]
   static constexpr int kXm = kMiscOff + 16, kAl = kXm + 2048, kBm = kAl + 2048, kBeta = kBm + 64,
-                       kLf = kBeta + 32, kMf = kLf + 1024;
-  static constexpr int kBytes = kMf + 512;
+                       kLf = kBeta + 32, kMf = kLf + 2048;
+  static constexpr int kBytes = kMf + 1024;
   static constexpr int kAlloc = kBytes + 1024;
 };
 static_assert(TfSmem<128>::kAlloc <= 227 * 1024, "shared memory");
 // mbarriers (3 stages at most); K^ and V^T of a stage fill and empty
 // separately: K^ is free once S has been computed, V^T once PV has
 enum {
-  FB_Q = 0,
-  FB_KFULL = 1,
-  FB_VFULL = 4,
-  FB_KEMPTY = 7,
-  FB_VEMPTY = 10,
-  FB_SDONE = 13,  // + buffer
+  FB_Q = 0,        // + item slot (2): Q^ landed
+  FB_QEMPTY = 2,   // + item slot: every S of the slot's item completed
+  FB_KFULL = 4,
+  FB_VFULL = 7,
+  FB_KEMPTY = 10,
+  FB_VEMPTY = 13,
+  FB_SDONE = 16,  // + buffer
+  // + tile mod 4: P^, alpha and beta of the tile.  Four slots: the softmax
+  // can run up to four tiles ahead of the correction (tile t needs only the
+  // correction's release of PV of tile t - 4), which with two slots could
+  // complete a slot's phase twice before the correction tests it
   FB_PFULL = FB_SDONE + 2,
-  FB_PVDONE = FB_PFULL + 2,
+  FB_PVDONE = FB_PFULL + 4,
   FB_PVFREE = FB_PVDONE + 2,
-  FB_DRAIN = FB_PVFREE + 2,
+  FB_ITEM = FB_PVFREE + 2,   // + item slot: the softmax wrote the item's l and m
+  FB_LFREE = FB_ITEM + 2,    // + item slot: the correction's epilogue read them
+  FB_DRAIN = FB_LFREE + 2,
   FB_COUNT
 };
 static_assert(FB_COUNT <= 32, "barriers");
 // tensor-memory columns: S (FP32) [2][128], then P^ (FP16 pairs) over its
 // first 64 columns; PV (FP32) [2][D]
 constexpr uint32_t kTfS = 0, kTfPv = 256;
+
+// Work item it of the forward: query tile qt of head bh, with nkt KV tiles.
+// Causal items come longest first (all heads' last query tiles, then the
+// tiles before them).  CTA c of G takes in round r the item r G + c (r
+// even) or r G + G - 1 - c (r odd): dealt in this snake order, the causal
+// items' lengths even out over the CTAs (imbalance 14% -> 2% on 16 heads of
+// 64 query tiles, against dealing every round forward).
+struct FwdItem {
+  int qt, bh, nkt;
+};
+__device__ __forceinline__ int fwd_item_index(int r, int c, int G) { return r * G + ((r & 1) ? G - 1 - c : c); }
+template <bool kCausal>
+__device__ __forceinline__ FwdItem fwd_item(int it, int nqt, int BH) {
+  FwdItem r;
+  if (kCausal) {
+    r.qt = nqt - 1 - it / BH;
+    r.bh = it % BH;
+    r.nkt = r.qt + 1;
+  } else {
+    r.bh = it / nqt;
+    r.qt = it % nqt;
+    r.nkt = nqt;
+  }
+  return r;
+}
 
 // Q^ or K^ rows [rows .. rows + 127] into a [D / 64][128][64] tile (halves 16
 // KB apart): at D = 64 one bulk copy; at D = 128 two tiled copies of 128-byte
@@ -1145,8 +1188,8 @@ __device__ __forceinline__ void load_rows(uint32_t dst, const uint16_t* src, con
 template <int D, bool kCausal>
 __global__ void __launch_bounds__(kTcThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, Ws ws,
-                  uint16_t* __restrict__ out, float* __restrict__ lse, int N, float scale_log2e, uint64_t wait_ns,
-                  int withhold) {
+                  uint16_t* __restrict__ out, float* __restrict__ lse, int N, int BH, float scale_log2e,
+                  uint64_t wait_ns, int withhold) {
   using L = TfSmem<D>;
   constexpr int kSt = L::kStages;
   // K^ and V^T rings refilled separately (at D = 64 together: measured 3%
@@ -1157,11 +1200,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sbase = smem_addr(smem);
   const int nqt = (N + kTok - 1) / kTok;
   const int Np = nqt * kTok;
-  const int qt = kCausal ? (nqt - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
-  const int bh = blockIdx.y;
+  const int n_items = nqt * BH, cta = static_cast<int>(blockIdx.x), ncta = static_cast<int>(gridDim.x);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wg = warp >> 2;
-  const int nkt = kCausal ? qt + 1 : nqt;
-  const size_t hb = static_cast<size_t>(bh) * Np * D;
   const Ctl ctl{ws.status, wait_ns};
   auto bar = [&](int i) { return sbase + L::kBarOff + 8 * i; };
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -1170,11 +1210,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* al = reinterpret_cast<float*>(smem + L::kAl);     // [tile mod 4][128 rows]
   float* bm = reinterpret_cast<float*>(smem + L::kBm);     // [2 parity][8 softmax warps]
   float* beta = reinterpret_cast<float*>(smem + L::kBeta); // [tile mod 4][2 row blocks]
-  float* lf = reinterpret_cast<float*>(smem + L::kLf);     // [2 halves][128 rows]
-  float* mf = reinterpret_cast<float*>(smem + L::kMf);     // [128 rows]
+  float* lf = reinterpret_cast<float*>(smem + L::kLf);     // [2 item slots][2 halves][128 rows]
+  float* mf = reinterpret_cast<float*>(smem + L::kMf);     // [2 item slots][128 rows]
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(FB_Q), 1);
+    for (int q = 0; q < 2; q++) {
+      mbar_init(bar(FB_Q + q), 1);
+      mbar_init(bar(FB_QEMPTY + q), 1);  // the MMA commit after the item's last S
+      mbar_init(bar(FB_ITEM + q), 8);
+      mbar_init(bar(FB_LFREE + q), 4);
+    }
     for (int s = 0; s < kSt; s++) {
       mbar_init(bar(FB_KFULL + s), 1);
       mbar_init(bar(FB_VFULL + s), 1);
@@ -1183,10 +1228,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(bar(FB_SDONE + b), 1);
-      mbar_init(bar(FB_PFULL + b), 8);
       mbar_init(bar(FB_PVDONE + b), 1);
       mbar_init(bar(FB_PVFREE + b), 4);
     }
+    for (int q = 0; q < 4; q++) mbar_init(bar(FB_PFULL + q), 8);
     mbar_init(bar(FB_DRAIN), 1);
     *abort = 0;
     mbar_fence_init();
@@ -1205,56 +1250,76 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if ((warp == 0 || (kSplit && warp == 2)) && lane == 0) {
       // ---- producers: warp 0 Q^ and the K^ tiles, warp 2 the V^T tiles,
       // each ring refilled as soon as its own product has read the slot (at
-      // D = 64 warp 0 copies both, and a stage is refilled after PV)
+      // D = 64 warp 0 copies both, and a stage is refilled after PV); a Q^
+      // slot once every S of the item two before has completed
       const bool isk = warp == 0;
-      const int hrow = bh * Np;  // the head's first row in [B*H*Np][D]
-      if (isk) {
-        mbar_arrive_expect_tx(bar(FB_Q), D / 64 * L::kHalf);
-        load_rows<D>(sbase + L::kQ, ws.qc, &tm_q, hrow + qt * kTok, bar(FB_Q));
-      }
       const int full = isk ? FB_KFULL : FB_VFULL, empty = isk && kSplit ? FB_KEMPTY : FB_VEMPTY;
-      const bool held = isk && withhold && blockIdx.x == 0 && blockIdx.y == 0;
-      int issued = 0;
-      for (int kt = 0; kt < nkt; kt++) {
-        const int s = kt % kSt;
-        if (kt >= kSt && !wait1_ab(bar(empty + s), ((kt / kSt) - 1) & 1, ctl, abort)) break;
-        if (held && kt == 0) continue;  // failure-detection test: this tile never arrives
-        const uint32_t st = sbase + L::kStageOff + s * L::kStage;
-        mbar_arrive_expect_tx(bar(full + s), kSplit ? L::kStage / 2 : L::kStage);
-        if (isk) load_rows<D>(st + L::kSK, ws.kc, &tm_k, hrow + kt * kTok, bar(full + s));
-        if (!isk || !kSplit)
-          bulk_load(st + L::kSV, ws.vct + hb + static_cast<size_t>(kt) * kTok * D, L::kStage / 2, bar(full + s));
-        issued = kt + 1;
+      const bool held = isk && withhold && blockIdx.x == 0;
+      int g = 0, issued = 0, nq = 0;
+      bool run = true;
+      for (int i = 0; run; i++) {
+        const int it = fwd_item_index(i, cta, ncta);
+        if (it >= n_items) break;
+        const FwdItem I = fwd_item<kCausal>(it, nqt, BH);
+        const int hrow = I.bh * Np;  // the head's first row in [B*H*Np][D]
+        const size_t hb = static_cast<size_t>(I.bh) * Np * D;
+        if (isk) {
+          const int qs = i & 1;
+          if (i >= 2 && !wait1_ab(bar(FB_QEMPTY + qs), ((i >> 1) - 1) & 1, ctl, abort)) break;
+          mbar_arrive_expect_tx(bar(FB_Q + qs), L::kQBytes);
+          load_rows<D>(sbase + L::kQ + qs * L::kQBytes, ws.qc, &tm_q, hrow + I.qt * kTok, bar(FB_Q + qs));
+          nq = i + 1;
+        }
+        for (int kt = 0; kt < I.nkt; kt++, g++) {
+          const int s = g % kSt;
+          if (g >= kSt && !wait1_ab(bar(empty + s), ((g / kSt) - 1) & 1, ctl, abort)) {
+            run = false;
+            break;
+          }
+          if (held && g == 0) continue;  // failure-detection test: this tile never arrives
+          const uint32_t st = sbase + L::kStageOff + s * L::kStage;
+          mbar_arrive_expect_tx(bar(full + s), kSplit ? L::kStage / 2 : L::kStage);
+          if (isk) load_rows<D>(st + L::kSK, ws.kc, &tm_k, hrow + kt * kTok, bar(full + s));
+          if (!isk || !kSplit)
+            bulk_load(st + L::kSV, ws.vct + hb + static_cast<size_t>(kt) * kTok * D, L::kStage / 2, bar(full + s));
+          issued = g + 1;
+        }
       }
       if (*abort) {
+        // let every copy this thread issued land before the CTA exits
         for (int last = issued - 1; last >= 0 && last >= issued - kSt; last--)
           if (!(held && last == 0)) {
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(bar(full + last % kSt), (last / kSt) & 1) && globaltimer_ns() - t0 < ctl.limit) {
             }
           }
-        if (isk) {
+        for (int j = nq > 2 ? nq - 2 : 0; j < nq; j++) {
           const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(bar(FB_Q), 0) && globaltimer_ns() - t0 < ctl.limit) {
+          while (!mbar_try_wait(bar(FB_Q + (j & 1)), (j >> 1) & 1) && globaltimer_ns() - t0 < ctl.limit) {
           }
         }
       }
     } else if (warp == 1) {
-      // ---- MMA issue: the whole warp, one elected lane issues
+      // ---- MMA issue: the whole warp, one elected lane issues.  S runs one
+      // tile of the stream ahead of PV; its cursor (item, tile) crosses into
+      // the next item, whose Q^ slot it waits for at the item's first tile.
       const uint32_t idS = idesc_f16(128, 128), idPV = idesc_f16(128, D);
-      // descriptors built once per operand: a K step of 16 moves 32 bytes
-      // (+2), a 64-wide half 16 KB (+1024); V^T's key halves are D * 128
-      // bytes apart
-      const uint64_t dq0 = desc_k64(sbase + L::kQ, 0);
-      bool ok = waitw_ab(bar(FB_Q), 0, ctl, abort);
-      auto issue_s = [&](int kt) {
-        const int s = kt % kSt, b = kt & 1;
-        if (!waitw_ab(bar(FB_KFULL + s), (kt / kSt) & 1, ctl, abort)) return false;
-        // buffer b: PV of tile kt - 2 has read its P^ (and so the softmax has
-        // read its S); PV's latest completion can be tile kt - 2's here
-        if (kt >= 2 && !waitw_ab(bar(FB_PVDONE + b), ((kt >> 1) - 1) & 1, ctl, abort)) return false;
+      int total = 0;  // tiles of this CTA's stream
+      for (int r = 0, it; (it = fwd_item_index(r, cta, ncta)) < n_items; r++) total += fwd_item<kCausal>(it, nqt, BH).nkt;
+      int s_g = 0, s_i = 0, s_kt = 0, s_nkt = total > 0 ? fwd_item<kCausal>(cta, nqt, BH).nkt : 0;
+      // descriptors: a K step of 16 moves 32 bytes (+2), a 64-wide half 16 KB
+      // (+1024); V^T's key halves are D * 128 bytes apart
+      auto issue_s = [&]() {
+        const int g = s_g, s = g % kSt, b = g & 1, qs = s_i & 1;
+        if (s_kt == 0 && !waitw_ab(bar(FB_Q + qs), (s_i >> 1) & 1, ctl, abort)) return false;
+        if (!waitw_ab(bar(FB_KFULL + s), (g / kSt) & 1, ctl, abort)) return false;
+        // buffer b: PV of tile g - 2 has read its P^ (and so the softmax has
+        // read its S); PV's latest completion can be tile g - 2's here
+        if (g >= 2 && !waitw_ab(bar(FB_PVDONE + b), ((g >> 1) - 1) & 1, ctl, abort)) return false;
         tc_fence_after();
+        const uint64_t dq0 = desc_k64(sbase + L::kQ + qs * L::kQBytes, 0);
         const uint64_t dks = desc_k64(sbase + L::kStageOff + s * L::kStage + L::kSK, 0);
+        const bool last = s_kt == s_nkt - 1;
         if (elect1()) {
 #pragma unroll
           for (int k = 0; k < D / 16; k++)
@@ -1262,17 +1327,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                        idS, k > 0);
           tc_commit(bar(FB_SDONE + b));
           if constexpr (kSplit) tc_commit(bar(FB_KEMPTY + s));
+          if (last) tc_commit(bar(FB_QEMPTY + qs));  // the item's Q^ slot can take item i + 2
         }
         __syncwarp();
+        s_g++;
+        if (last) {
+          s_kt = 0;
+          s_i++;
+          const int nit = fwd_item_index(s_i, cta, ncta);
+          s_nkt = nit < n_items ? fwd_item<kCausal>(nit, nqt, BH).nkt : 0;
+        } else {
+          s_kt++;
+        }
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int kt = 0; ok && kt < nkt; kt++) {
-        const int s = kt % kSt, b = kt & 1;
-        if (kt + 1 < nkt && !(ok = issue_s(kt + 1))) break;
-        if (!(ok = waitw_ab(bar(FB_PFULL + b), (kt >> 1) & 1, ctl, abort))) break;
-        if (kt >= 2 && !(ok = waitw_ab(bar(FB_PVFREE + b), ((kt >> 1) - 1) & 1, ctl, abort))) break;
-        if (kSplit && !(ok = waitw_ab(bar(FB_VFULL + s), (kt / kSt) & 1, ctl, abort))) break;
+      bool ok = total == 0 || issue_s();
+      for (int g = 0; ok && g < total; g++) {
+        const int s = g % kSt, b = g & 1;
+        if (g + 1 < total && !(ok = issue_s())) break;
+        if (!(ok = waitw_ab(bar(FB_PFULL + (g & 3)), (g >> 2) & 1, ctl, abort))) break;
+        if (g >= 2 && !(ok = waitw_ab(bar(FB_PVFREE + b), ((g >> 1) - 1) & 1, ctl, abort))) break;
+        if (kSplit && !(ok = waitw_ab(bar(FB_VFULL + s), (g / kSt) & 1, ctl, abort))) break;
         tc_fence_after();
         // A: P^ over S's first 64 columns (8 columns a K step of 16 keys)
         const uint64_t dvs = desc_k64(sbase + L::kStageOff + s * L::kStage + L::kSV, 0);
@@ -1307,101 +1382,118 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int sw = 4 * h + wq;
     const int blk = wq >> 1;  // 64-row block of this row
     const uint32_t lanebase = static_cast<uint32_t>(32 * wq) << 16;
-    const int qrow = qt * kTok + row;
-    const bool valid = qrow < N;
-    const float sqk = ws.sq[static_cast<size_t>(bh) * nqt + qt] * scale_log2e;
     const uint64_t magic2 = pack2(kRintMagic, kRintMagic), nmagic2 = pack2(-kRintMagic, -kRintMagic);
-    float m = -INFINITY, l = 0.0f;
-    float sk_next = ws.sk[static_cast<size_t>(bh) * nqt], sv_next = ws.sv[static_cast<size_t>(bh) * nqt];
-    for (int kt = 0; kt < nkt; kt++) {
-      const int b = kt & 1;
-      const float sk_cur = sk_next, sv_cur = sv_next;
-      if (kt + 1 < nkt) {
-        sk_next = ws.sk[static_cast<size_t>(bh) * nqt + kt + 1];
-        sv_next = ws.sv[static_cast<size_t>(bh) * nqt + kt + 1];
-      }
-      bool ok = waitw_ab(bar(FB_SDONE + b), (kt >> 1) & 1, ctl, abort);
-      tc_fence_after();
-      uint32_t ru[2][32];
-      tmem_ld32(tmem + lanebase + kTfS + 128 * b + 64 * h, ru[0]);
-      tmem_ld32(tmem + lanebase + kTfS + 128 * b + 64 * h + 32, ru[1]);
-      tmem_wait_ld();
-      if ((kCausal && kt == qt) || (kt == nqt - 1 && (N % kTok) != 0)) {
-        // keys past N, and (causal) past this row, do not take part
-        const int k0 = kt * kTok + 64 * h;
-        const int last = kCausal ? min(N - 1, qrow) : N - 1;
-#pragma unroll
-        for (int i = 0; i < 64; i++)
-          if (k0 + i > last) ru[i >> 5][i & 31] = __float_as_uint(-INFINITY);
-      }
-      float hm;
-      {
-        float t[8];
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-          const uint32_t* r = &ru[j >> 2][(j & 3) * 8];
-          t[j] = max3f(max3f(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2])),
-                       max3f(__uint_as_float(r[3]), __uint_as_float(r[4]), __uint_as_float(r[5])),
-                       fmaxf(__uint_as_float(r[6]), __uint_as_float(r[7])));
+    bool ok = true;
+    int g = 0;
+    for (int i = 0; ok; i++) {
+      const int it = fwd_item_index(i, cta, ncta);
+      if (it >= n_items) break;
+      const FwdItem I = fwd_item<kCausal>(it, nqt, BH);
+      const int qt = I.qt, nkt = I.nkt;
+      const size_t hs = static_cast<size_t>(I.bh) * nqt;  // the head's block scales
+      const int qrow = qt * kTok + row;
+      const bool valid = qrow < N;
+      const float sqk = ws.sq[hs + qt] * scale_log2e;
+      float m = -INFINITY, l = 0.0f;
+      float sk_next = ws.sk[hs], sv_next = ws.sv[hs];
+      for (int kt = 0; kt < nkt; kt++, g++) {
+        const int b = g & 1;
+        const float sk_cur = sk_next, sv_cur = sv_next;
+        if (kt + 1 < nkt) {
+          sk_next = ws.sk[hs + kt + 1];
+          sv_next = ws.sv[hs + kt + 1];
         }
-        hm = max3f(max3f(t[0], t[1], t[2]), max3f(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
-      }
-      // the row's maximum over both halves of the tile (xm by tile parity)
-      xm[(2 * b + h) * 128 + row] = hm;
-      // alpha and beta go to slot kt % 4, which the correction has read for
-      // tile kt - 4: S of this tile was issued after PV of tile kt - 2, and
-      // that PV after the correction had released tile kt - 4's PV buffer.
-      // The vote also publishes xm, and orders both halves' loads of S
-      // before P^ overwrites its first 64 columns
-      if (!group_and(ok)) break;
-      const float mt = fmaxf(hm, xm[(2 * b + 1 - h) * 128 + row]);
-      // c2 > 0 keeps masked keys at -inf (c2 = 0 only when every score is 0)
-      const float c2 = fmaxf(sqk * sk_cur, 1e-30f);
-      const float mn = fmaxf(m, mt * c2);
-      const float alpha = ex2(m - mn);  // m = -inf on the first tile: 0
-      m = mn;
-      // The block's largest P~ is the largest of its rows' maxima, each the
-      // exponential of the same argument as the row's largest score (rows past
-      // N excluded); both halves of a row compute it alike, so each half takes
-      // the block maximum over its own two warps.
-      const float rp = valid ? ex2(fmaf(mt, c2, -mn)) : 0.0f;
-      const uint32_t wmax = redux_max_u32(__float_as_uint(rp) & 0x7fffffffu);  // rp >= 0: bit order is value order
-      if (lane == 0) bm[b * 8 + sw] = __uint_as_float(wmax);
-      if (h == 0) al[(kt & 3) * 128 + row] = alpha;
-      named_bar(3 + 2 * h + blk, 64);  // publishes bm to the block's other warp of this half
-      const float amax = fmaxf(bm[b * 8 + 4 * h + 2 * blk], bm[b * 8 + 4 * h + 2 * blk + 1]);
-      const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
-      if (h == 0 && wq == 2 * blk && lane == 0) beta[(kt & 3) * 2 + blk] = __fdiv_rn(amax, 127.0f) * sv_cur;
-      // one pass: P~ = exp2(s c2 - m), its row sum, and its codes
-      // rint(P~ * inv): P~ * inv + 1.5 * 2^23 in one FMA rounds the exact
-      // product to an integer (ties to even), and subtracting 1.5 * 2^23 is
-      // exact
-      const uint64_t c22 = pack2(c2, c2), nm2 = pack2(-mn, -mn), ii = pack2(inv, inv);
-      uint64_t acc0 = 0, acc1 = 0;
-      uint32_t pw[32];  // keys 2j, 2j + 1 of this half as FP16 codes
+        ok = waitw_ab(bar(FB_SDONE + b), (g >> 1) & 1, ctl, abort);
+        tc_fence_after();
+        uint32_t ru[2][32];
+        tmem_ld32(tmem + lanebase + kTfS + 128 * b + 64 * h, ru[0]);
+        tmem_ld32(tmem + lanebase + kTfS + 128 * b + 64 * h + 32, ru[1]);
+        tmem_wait_ld();
+        if ((kCausal && kt == qt) || (kt == nqt - 1 && (N % kTok) != 0)) {
+          // keys past N, and (causal) past this row, do not take part
+          const int k0 = kt * kTok + 64 * h;
+          const int lastk = kCausal ? min(N - 1, qrow) : N - 1;
 #pragma unroll
-      for (int j = 0; j < 32; j++) {
-        const uint32_t* r = &ru[j >> 4][(j & 15) * 2];
-        const uint64_t y = fma2(pack2(__uint_as_float(r[0]), __uint_as_float(r[1])), c22, nm2);
-        const uint64_t x = pack2(ex2(lo2(y)), ex2(hi2(y)));
-        if (j & 1)
-          acc1 = add2(acc1, x);
-        else
-          acc0 = add2(acc0, x);
-        const uint64_t n = add2(fma2(x, ii, magic2), nmagic2);
-        pw[j] = h2(lo2(n), hi2(n));
+          for (int e = 0; e < 64; e++)
+            if (k0 + e > lastk) ru[e >> 5][e & 31] = __float_as_uint(-INFINITY);
+        }
+        float hm;
+        {
+          float t[8];
+#pragma unroll
+          for (int j = 0; j < 8; j++) {
+            const uint32_t* r = &ru[j >> 2][(j & 3) * 8];
+            t[j] = max3f(max3f(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2])),
+                         max3f(__uint_as_float(r[3]), __uint_as_float(r[4]), __uint_as_float(r[5])),
+                         fmaxf(__uint_as_float(r[6]), __uint_as_float(r[7])));
+          }
+          hm = max3f(max3f(t[0], t[1], t[2]), max3f(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
+        }
+        // the row's maximum over both halves of the tile (xm by tile parity)
+        xm[(2 * b + h) * 128 + row] = hm;
+        // alpha and beta go to slot g % 4, which the correction has read for
+        // tile g - 4: S of this tile was issued after PV of tile g - 2, and
+        // that PV after the correction had released tile g - 4's PV buffer.
+        // The vote also publishes xm, and orders both halves' loads of S
+        // before P^ overwrites its first 64 columns
+        if (!(ok = group_and(ok))) break;
+        const float mt = fmaxf(hm, xm[(2 * b + 1 - h) * 128 + row]);
+        // c2 > 0 keeps masked keys at -inf (c2 = 0 only when every score is 0)
+        const float c2 = fmaxf(sqk * sk_cur, 1e-30f);
+        const float mn = fmaxf(m, mt * c2);
+        const float alpha = ex2(m - mn);  // m = -inf on the item's first tile: 0
+        m = mn;
+        // The block's largest P~ is the largest of its rows' maxima, each the
+        // exponential of the same argument as the row's largest score (rows past
+        // N excluded); both halves of a row compute it alike, so each half takes
+        // the block maximum over its own two warps.
+        const float rp = valid ? ex2(fmaf(mt, c2, -mn)) : 0.0f;
+        const uint32_t wmax = redux_max_u32(__float_as_uint(rp) & 0x7fffffffu);  // rp >= 0: bit order is value order
+        if (lane == 0) bm[b * 8 + sw] = __uint_as_float(wmax);
+        if (h == 0) al[(g & 3) * 128 + row] = alpha;
+        named_bar(3 + 2 * h + blk, 64);  // publishes bm to the block's other warp of this half
+        const float amax = fmaxf(bm[b * 8 + 4 * h + 2 * blk], bm[b * 8 + 4 * h + 2 * blk + 1]);
+        const float inv = amax > 0.0f ? __fdiv_rn(127.0f, amax) : 0.0f;
+        if (h == 0 && wq == 2 * blk && lane == 0) beta[(g & 3) * 2 + blk] = __fdiv_rn(amax, 127.0f) * sv_cur;
+        // one pass: P~ = exp2(s c2 - m), its row sum, and its codes
+        // rint(P~ * inv): P~ * inv + 1.5 * 2^23 in one FMA rounds the exact
+        // product to an integer (ties to even), and subtracting 1.5 * 2^23 is
+        // exact
+        const uint64_t c22 = pack2(c2, c2), nm2 = pack2(-mn, -mn), ii = pack2(inv, inv);
+        uint64_t acc0 = 0, acc1 = 0;
+        uint32_t pw[32];  // keys 2j, 2j + 1 of this half as FP16 codes
+#pragma unroll
+        for (int j = 0; j < 32; j++) {
+          const uint32_t* r = &ru[j >> 4][(j & 15) * 2];
+          const uint64_t y = fma2(pack2(__uint_as_float(r[0]), __uint_as_float(r[1])), c22, nm2);
+          const uint64_t x = pack2(ex2(lo2(y)), ex2(hi2(y)));
+          if (j & 1)
+            acc1 = add2(acc1, x);
+          else
+            acc0 = add2(acc0, x);
+          const uint64_t n = add2(fma2(x, ii, magic2), nmagic2);
+          pw[j] = h2(lo2(n), hi2(n));
+        }
+        const uint64_t acc = add2(acc0, acc1);
+        l = fmaf(l, alpha, lo2(acc) + hi2(acc));
+        tmem_st32(tmem + lanebase + kTfS + 128 * b + 32 * h, pw);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive1(bar(FB_PFULL + (g & 3)));
       }
-      const uint64_t acc = add2(acc0, acc1);
-      l = fmaf(l, alpha, lo2(acc) + hi2(acc));
-      tmem_st32(tmem + lanebase + kTfS + 128 * b + 32 * h, pw);
-      tmem_wait_st();
-      tc_fence_before();
+      if (!ok) break;
+      // the item's row statistics for its epilogue, in slot i % 2 once the
+      // correction has read item i - 2's (voted, so that all eight warps
+      // leave together if the wait runs out)
+      const int ls = i & 1;
+      ok = i < 2 || waitw_ab(bar(FB_LFREE + ls), ((i >> 1) - 1) & 1, ctl, abort);
+      if (!(ok = group_and(ok))) break;
+      lf[(2 * ls + h) * 128 + row] = l;
+      if (h == 0) mf[ls * 128 + row] = m;
       __syncwarp();
-      if (lane == 0) mbar_arrive1(bar(FB_PFULL + b));
+      if (lane == 0) mbar_arrive1(bar(FB_ITEM + ls));
     }
-    // the row's statistics for the epilogue
-    lf[h * 128 + row] = l;
-    if (h == 0) mf[row] = m;
     tc_fence_before();
     named_bar(2, kTcThreads);
   } else {
@@ -1410,49 +1502,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = 32 * (warp & 3) + lane;
     const int blk = (warp & 3) >> 1;
     const uint32_t lanebase = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    uint64_t o[D / 2];
+    bool ok = true;
+    int g = 0;
+    for (int i = 0; ok; i++) {
+      const int it = fwd_item_index(i, cta, ncta);
+      if (it >= n_items) break;
+      const FwdItem I = fwd_item<kCausal>(it, nqt, BH);
+      uint64_t o[D / 2];
 #pragma unroll
-    for (int i = 0; i < D / 2; i++) o[i] = 0;
-    for (int kt = 0; kt < nkt; kt++) {
-      const int b = kt & 1;
-      // PFULL: the softmax's alpha and beta of this tile (its release); PVDONE: the product
-      if (!waitw_ab(bar(FB_PFULL + b), (kt >> 1) & 1, ctl, abort)) break;
-      if (!waitw_ab(bar(FB_PVDONE + b), (kt >> 1) & 1, ctl, abort)) break;
-      tc_fence_after();
-      const float alpha = al[(kt & 3) * 128 + row], bt = beta[(kt & 3) * 2 + blk];
-      // o = pv * beta + o * alpha; o * 1 is o, so warps whose rows' maxima
-      // all held skip the multiply
-      const uint64_t bt2 = pack2(bt, bt), al2 = pack2(alpha, alpha);
-      const bool keep = __all_sync(kFull, alpha == 1.0f);
+      for (int c = 0; c < D / 2; c++) o[c] = 0;
+      for (int kt = 0; kt < I.nkt; kt++, g++) {
+        const int b = g & 1;
+        // PFULL: the softmax's alpha and beta of this tile (its release); PVDONE: the product
+        if (!(ok = waitw_ab(bar(FB_PFULL + (g & 3)), (g >> 2) & 1, ctl, abort))) break;
+        if (!(ok = waitw_ab(bar(FB_PVDONE + b), (g >> 1) & 1, ctl, abort))) break;
+        tc_fence_after();
+        const float alpha = al[(g & 3) * 128 + row], bt = beta[(g & 3) * 2 + blk];
+        // o = pv * beta + o * alpha; o * 1 is o, so warps whose rows' maxima
+        // all held skip the multiply
+        const uint64_t bt2 = pack2(bt, bt), al2 = pack2(alpha, alpha);
+        const bool keep = __all_sync(kFull, alpha == 1.0f);
 #pragma unroll
-      for (int c = 0; c < D / 32; c++) {
-        uint32_t ru[32];
-        tmem_ld32(tmem + lanebase + kTfPv + D * b + 32 * c, ru);
-        tmem_wait_ld();
-        if (keep) {
+        for (int c = 0; c < D / 32; c++) {
+          uint32_t ru[32];
+          tmem_ld32(tmem + lanebase + kTfPv + D * b + 32 * c, ru);
+          tmem_wait_ld();
+          if (keep) {
 #pragma unroll
-          for (int j = 0; j < 16; j++)
-            o[16 * c + j] = fma2(pack2(__uint_as_float(ru[2 * j]), __uint_as_float(ru[2 * j + 1])), bt2, o[16 * c + j]);
-        } else {
+            for (int j = 0; j < 16; j++)
+              o[16 * c + j] =
+                  fma2(pack2(__uint_as_float(ru[2 * j]), __uint_as_float(ru[2 * j + 1])), bt2, o[16 * c + j]);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 16; j++)
-            o[16 * c + j] =
-                fma2(pack2(__uint_as_float(ru[2 * j]), __uint_as_float(ru[2 * j + 1])), bt2, mul2(o[16 * c + j], al2));
+            for (int j = 0; j < 16; j++)
+              o[16 * c + j] = fma2(pack2(__uint_as_float(ru[2 * j]), __uint_as_float(ru[2 * j + 1])), bt2,
+                                   mul2(o[16 * c + j], al2));
+          }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive1(bar(FB_PVFREE + b));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive1(bar(FB_PVFREE + b));
-    }
-    // epilogue, once the softmax has published l and m
-    tc_fence_before();
-    named_bar(2, kTcThreads);
-    if (!*abort) {
-      const int qrow = qt * kTok + row;
-      if (qrow < N) {
-        const float lt = lf[row] + lf[128 + row];
+      if (!ok) break;
+      // the item's epilogue, once the softmax has published its l and m
+      const int ls = i & 1;
+      if (!(ok = waitw_ab(bar(FB_ITEM + ls), (i >> 1) & 1, ctl, abort))) break;
+      const int qrow = I.qt * kTok + row;
+      if (qrow < N && !*abort) {
+        const float lt = lf[2 * ls * 128 + row] + lf[(2 * ls + 1) * 128 + row];
         const float il = 1.0f / lt;
-        uint16_t* orow = out + (static_cast<size_t>(bh) * N + qrow) * D;
+        uint16_t* orow = out + (static_cast<size_t>(I.bh) * N + qrow) * D;
 #pragma unroll
         for (int c = 0; c < D / 8; c++) {
           __nv_bfloat162 h0 = __floats2bfloat162_rn(lo2(o[4 * c + 0]) * il, hi2(o[4 * c + 0]) * il);
@@ -1466,9 +1565,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           w.w = *reinterpret_cast<uint32_t*>(&h3);
           *reinterpret_cast<uint4*>(orow + 8 * c) = w;
         }
-        lse[static_cast<size_t>(bh) * N + qrow] = (mf[row] + __log2f(lt)) * kLn2;
+        lse[static_cast<size_t>(I.bh) * N + qrow] = (mf[ls * 128 + row] + __log2f(lt)) * kLn2;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(bar(FB_LFREE + ls));
     }
+    tc_fence_before();
+    named_bar(2, kTcThreads);
   }
 }
 
@@ -1967,9 +2070,15 @@ cudaError_t launch_fwd_tc(const Ws& w, uint16_t* o, float* lse, int BH, int N, f
   if (attr.numRegs != 65536 / kTcThreads) return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(fwd_tc_kernel<D, C>, cudaFuncAttributeMaxDynamicSharedMemorySize, TfSmem<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  const dim3 grid((N + kTok - 1) / kTok, BH);
-  fwd_tc_kernel<D, C><<<grid, kTcThreads, TfSmem<D>::kAlloc, st>>>(tq, tk, w, o, lse, N, scale * kLog2e, wait_ns,
-                                                                  withhold);
+  // persistent CTAs, one per SM at most, walking the work items
+  const long long items = static_cast<long long>((N + kTok - 1) / kTok) * BH;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
+  fwd_tc_kernel<D, C><<<grid, kTcThreads, TfSmem<D>::kAlloc, st>>>(tq, tk, w, o, lse, N, BH, scale * kLog2e,
+                                                                  wait_ns, withhold);
   return cudaGetLastError();
 }
 
