@@ -209,6 +209,35 @@ def test_training_workload_sampled_heads(name):
         compare(f"{name} {nm}", g, r)
 
 
+@pytest.mark.parametrize("name", ["train_llama1b", "train_qwen3b"])
+def test_training_workload_repeats_are_stable(name):
+    """Full-size shapes launched again and again: every run ends with a clean
+    status word, well inside the 1.5 s limit of a bounded wait, and gives the
+    same o, lse, dk and dv bit for bit (dq within FP32 reordering of its
+    accumulation). A barrier phase that completed twice before one of its
+    waiters tested it would show here as a run that stalls until a wait
+    runs out."""
+    import time
+    w = TRAIN_WORKLOADS[name]
+    q, k, v = (t.cuda() for t in make_qkv(w.B, w.H, w.N, w.D, w.pattern, seed=3))
+    do = make_dout(w.B, w.H, w.N, w.D, seed=3).cuda()
+    ref = None
+    for rep in range(12):
+        t0 = time.perf_counter()
+        o, lse, ws = SB.forward(q, k, v, w.causal)
+        dq, dk, dv = SB.backward(do, o, lse, ws, w.causal)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        assert ws.get_status() == 0, rep
+        assert rep == 0 or dt < 0.1, (rep, dt)
+        if ref is None:
+            ref = [t.clone() for t in (o, lse, dq, dk, dv)]
+            continue
+        for nm, a, b in zip(("o", "lse", "dk", "dv"), (o, lse, dk, dv), (ref[0], ref[1], ref[3], ref[4])):
+            assert torch.equal(a, b), (rep, nm)
+        assert torch.allclose(dq.float(), ref[2].float(), rtol=2 ** -7, atol=1e-3 * float(ref[2].float().abs().max()))
+
+
 def test_mma_peaks_are_measurable():
     i8 = SB.mma_peak_tops(0)
     f16 = SB.mma_peak_tops(1)
